@@ -1,0 +1,112 @@
+"""ctypes loader for the fp64 CPU oracle (oracle/kda_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: tests/, __graft_entry__.smoke() and the
+cpu_baseline leg of bench.py are the only users.  The CUDA library never
+imports, links or calls anything here.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+BF16, F32, F64 = 0, 1, 2
+_lib = None
+
+
+def build(src: str = _SRC, out: str = _LIB, extra_flags: Sequence[str] = ()) -> str:
+    """Compile the oracle with gcc (plain C11, -O2, POSIX threads)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC", "-pthread",
+           *extra_flags, "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _stale(lib: str, src: str) -> bool:
+    return not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src)
+
+
+def load(path: Optional[str] = None):
+    """Load (building first if needed) and return the ctypes library."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        if _stale(_LIB, _SRC):
+            build()
+        _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.kda_oracle_recurrent.argtypes = [P, P, P, I, P, P, I, P, P, P, P,
+                                         I, I, I, I, I, P, I, I]
+    lib.kda_oracle_recurrent.restype = I
+    lib.kda_oracle_chunked.argtypes = [P, P, P, I, P, P, I, P, P, P, P,
+                                       I, I, I, I, I, P, I, I, I]
+    lib.kda_oracle_chunked.restype = I
+    return lib
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"unsupported oracle input dtype {a.dtype}")
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def run(q, k, v, g, beta, cu_seqlens, initial_state=None, heads=None, chunk: int = 0,
+        nthreads: Optional[int] = None, lib=None, want_state: bool = True
+        ) -> Tuple[np.ndarray, Optional[np.ndarray]]:
+    """Run the oracle.
+
+    q, k: [T][H][dk]; v: [T][H][dv] (uint16 bf16 bits, float32 or float64);
+    g: [T][H][dk], beta: [T][H] (float32 or float64, same dtype);
+    cu_seqlens: [N+1] int; initial_state: None or [N][nsel][dv][dk] (float);
+    heads: indices of the heads to compute (default: all).
+    chunk = 0 runs the token recurrence, chunk >= 1 the chunked form.
+    Returns out [T][nsel][dv] float64 and final_state [N][nsel][dv][dk] float64.
+    """
+    lib = lib or load()
+    q, k, v = (np.ascontiguousarray(x) for x in (q, k, v))
+    g, beta = np.ascontiguousarray(g), np.ascontiguousarray(beta)
+    if g.dtype != beta.dtype:
+        beta = beta.astype(g.dtype)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu.shape[0] - 1
+    hs = np.arange(H, dtype=np.int32) if heads is None else np.ascontiguousarray(heads, dtype=np.int32)
+    nsel = hs.shape[0]
+    init = None if initial_state is None else np.ascontiguousarray(initial_state, dtype=np.float64)
+    if init is not None:
+        assert init.shape == (N, nsel, dv, dk), init.shape
+    out = np.zeros((T, nsel, dv), dtype=np.float64)
+    fin = np.zeros((N, nsel, dv, dk), dtype=np.float64) if want_state else None
+    nt = nthreads or os.cpu_count() or 1
+    args = [_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), _ptr(g), _ptr(beta), _dtype_code(g),
+            _ptr(cu), _ptr(init), _ptr(out), _ptr(fin), N, T, H, dk, dv, _ptr(hs), nsel]
+    if chunk == 0:
+        rc = lib.kda_oracle_recurrent(*args, nt)
+    else:
+        rc = lib.kda_oracle_chunked(*args, chunk, nt)
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out, fin
