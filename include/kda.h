@@ -1,0 +1,124 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) KDA chunked packed-varlen prefill.
+ *
+ * Kimi Delta Attention (KDA) is the gated delta rule with a per-channel decay
+ * that the Kimi-K3 prefill runs in its KDA layers (kern-k3-pp-prefill README,
+ * "P: the packed prefill"; the NVIDIA KDA_prefill kernels ported in SGLang
+ * PR #32890, prhub report section "实现拆解", item 3).  For every packed
+ * sequence n and head h, with S in R^{dk x dv}:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t
+ *
+ * computed per 64-row chunk in WY form: in-chunk cumulative log-decay G, the
+ * strictly lower A_kk = beta_i (k_i * exp(G_i - G_j)) . k_j, the inverse of
+ * (I + A_kk), the factors W and U, the inter-chunk state recurrence, the
+ * outputs, and the fp32 final state of every sequence.  No 1/sqrt(dk) scale
+ * is applied to q; token t's output includes token t's own write.
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ *  Pointers   all tensor pointers are DEVICE pointers; every tensor is dense
+ *             and row-major (innermost index last).  The caller owns every
+ *             buffer.  The library allocates nothing per call, keeps no
+ *             pointer after return, and is reentrant across streams.
+ *  Async      calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *             legacy default stream).  The host never reads cu_seqlens and
+ *             never synchronises.
+ *  Layouts    q, k: [T][H][dk];  v, out: [T][H][dv];  g: [T][H][dk];
+ *             beta: [T][H];  cu_seqlens: int32 [N+1];
+ *             initial_state, final_state: [N][H][dv][dk] fp32, i.e. S^T with
+ *             dk contiguous -- SGLang's recurrent-state pool layout
+ *             [slot][head][v][k] f32 (kern-k3-pp-prefill README, section
+ *             "D inside SGLang").
+ *  Packing    sequence n occupies rows [cu_seqlens[n], cu_seqlens[n+1]);
+ *             up to 16 sequences in 8192 rows is the production shape
+ *             (kern-k3-pp-prefill README, "P: the packed prefill").  Chunks
+ *             start at each sequence's first row and never cross a sequence;
+ *             the last chunk of a sequence may be partial.  A zero-length
+ *             sequence copies initial_state to final_state (zeros if NULL).
+ *  cu_seqlens contract: cu[0] = 0, nondecreasing, cu[N] = T.  It is not read
+ *             on the host; the kernels clamp every row index into [0, T], so
+ *             a bad table never makes them access memory out of bounds.
+ *  Inputs     q and k are expected L2-normalised per head by the caller.  The
+ *             tensor-core path rounds its MMA operands to fp16 (fp32
+ *             accumulation).  Values must therefore stay in fp16 range:
+ *             |v| and |S| below about 6.5e4, and the cumulative log-decay over
+ *             half a chunk (32 rows) above about -11 per channel (with
+ *             g ~ U[-0.2, 0] it is at least -6.4).
+ *  Aliasing   final_state == initial_state (the same pointer) is allowed and
+ *             updates the states in place; any other overlap between an output
+ *             and any other argument returns KDA_ERR_ALIAS.
+ *  Errors     arguments are validated synchronously before anything is
+ *             launched; a failed check returns its status and launches
+ *             nothing.  A launch failure returns KDA_ERR_CUDA (the CUDA error
+ *             stays readable through cudaGetLastError()).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,         /* a required pointer is NULL                    */
+    KDA_ERR_SHAPE = 2,        /* N < 1, T < 0, H < 1, or a size overflows      */
+    KDA_ERR_UNSUPPORTED = 3,  /* dk/dv/dtype combination or N not supported    */
+    KDA_ERR_ALIGN = 4,        /* a tensor pointer is not 16-byte aligned       */
+    KDA_ERR_ALIAS = 5,        /* an output overlaps another argument           */
+    KDA_ERR_CUDA = 6,         /* a CUDA call failed (see cudaGetLastError)     */
+    KDA_ERR_DEVICE = 7        /* no CUDA device, or not an sm_103 device       */
+} kda_status;
+
+/*
+ * kda_chunk_prefill -- bf16 q/k/v in, bf16 out (round to nearest even from
+ * the fp32 accumulator), fp32 g, beta and states.
+ *
+ *   q, k, v        bf16 bit patterns (uint16), layouts above.
+ *   g              fp32 per-token log-decay log(alpha), [T][H][dk].
+ *   beta           fp32 write strength, [T][H].
+ *   cu_seqlens     int32 [N+1], device memory.
+ *   initial_state  fp32 [N][H][dv][dk], or NULL for a zero start.
+ *   out            bf16 [T][H][dv]; every row in [0, T) is written.
+ *   final_state    fp32 [N][H][dv][dk], or NULL (not written).
+ *   N, T, H        sequences (1 <= N <= 1024), rows (T >= 0), heads (H >= 1).
+ *   dk, dv         key and value head dims; supported: dk = dv = 128.
+ *   stream         cudaStream_t to launch on.
+ * Returns a kda_status.
+ */
+int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const float *g, const float *beta, const int32_t *cu_seqlens,
+                      const float *initial_state, uint16_t *out, float *final_state,
+                      int N, int T, int H, int dk, int dv, void *stream);
+
+/*
+ * kda_chunk_prefill_f32 -- the same operation with fp32 q/k/v and fp32 out.
+ * Supported: dk = dv = 64.  All other conventions as kda_chunk_prefill.
+ */
+int kda_chunk_prefill_f32(const float *q, const float *k, const float *v,
+                          const float *g, const float *beta, const int32_t *cu_seqlens,
+                          const float *initial_state, float *out, float *final_state,
+                          int N, int T, int H, int dk, int dv, void *stream);
+
+/* Human-readable name of a kda_status value (static string, never NULL). */
+const char *kda_status_string(int status);
+
+/*
+ * kda_device_error -- read the library's sticky device error word on the
+ * current device.  Every wait inside the kernels is bounded; a wait that runs
+ * out sets a bit here and the kernel returns early (outputs are then
+ * undefined).  0 means no kernel of this library has reported an error.
+ * Synchronises the current device.  If `reset` is nonzero the word is
+ * cleared after reading.  Returns KDA_OK or KDA_ERR_CUDA.
+ */
+int kda_device_error(int *word, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

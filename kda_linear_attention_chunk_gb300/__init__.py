@@ -1,0 +1,121 @@
+"""Python binding of libkda.so, the GB300 KDA chunked packed-varlen prefill.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI of include/kda.h.  PyTorch supplies device memory
+and streams.  There is no fallback: if the library is not built, the entry
+points raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+
+KDA_OK, KDA_ERR_NULL, KDA_ERR_SHAPE, KDA_ERR_UNSUPPORTED = 0, 1, 2, 3
+KDA_ERR_ALIGN, KDA_ERR_ALIAS, KDA_ERR_CUDA, KDA_ERR_DEVICE = 4, 5, 6, 7
+
+EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error")
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}" if where else status_string(status))
+
+
+def load(path: str = LIB_PATH):
+    """Load libkda.so (built by __graft_entry__.build()); raises if missing."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkda.so is not built ({path}); run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    sig = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P]
+    for name in ("kda_chunk_prefill", "kda_chunk_prefill_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = sig
+        fn.restype = I
+    lib.kda_status_string.argtypes = [I]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), I]
+    lib.kda_device_error.restype = I
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().kda_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"kda_status {status}"
+
+
+def kda_chunk_prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                      N: int, T: int, H: int, dk: int, dv: int, stream) -> int:
+    """Raw C-ABI call: integer device pointers (0 = NULL) and sizes."""
+    return load().kda_chunk_prefill(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                                    N, T, H, dk, dv, stream)
+
+
+def kda_chunk_prefill_f32(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                          N: int, T: int, H: int, dk: int, dv: int, stream) -> int:
+    """Raw C-ABI call for fp32 q/k/v/out."""
+    return load().kda_chunk_prefill_f32(q, k, v, g, beta, cu_seqlens, initial_state, out,
+                                        final_state, N, T, H, dk, dv, stream)
+
+
+def device_error(reset: bool = False) -> int:
+    word = ctypes.c_int(0)
+    st = load().kda_device_error(ctypes.byref(word), int(reset))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_device_error")
+    return word.value
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def chunk_prefill(q, k, v, g, beta, cu_seqlens, initial_state=None, out=None, final_state=None,
+                  output_final_state: bool = True, stream=None) -> Tuple[object, Optional[object]]:
+    """KDA chunked packed-varlen prefill on torch CUDA tensors.
+
+    q, k: [T][H][dk], v: [T][H][dv] (bfloat16, or float32 with dk = dv = 64);
+    g: [T][H][dk] float32; beta: [T][H] float32; cu_seqlens: [N+1] int32 on
+    the device; initial_state: [N][H][dv][dk] float32 or None.  Returns
+    (out [T][H][dv] in q's dtype, final_state [N][H][dv][dk] float32 or None).
+    Runs asynchronously on ``stream`` (default: torch's current stream).
+    """
+    import torch
+
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("cu_seqlens", cu_seqlens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    handle = int(s.cuda_stream) if hasattr(s, "cuda_stream") else int(s)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state),
+            _ptr(out), _ptr(final_state), N, T, H, dk, dv, handle)
+    if q.dtype == torch.bfloat16:
+        st = kda_chunk_prefill(*args)
+    elif q.dtype == torch.float32:
+        st = kda_chunk_prefill_f32(*args)
+    else:
+        raise ValueError(f"unsupported q dtype {q.dtype}")
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_prefill")
+    return out, final_state

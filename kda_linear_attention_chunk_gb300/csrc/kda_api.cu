@@ -1,0 +1,182 @@
+// kda_api.cu -- the C ABI declared in include/kda.h: argument validation,
+// device checks and kernel dispatch.  Validation is synchronous and happens
+// before any CUDA call, so a rejected call touches no device state.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+__device__ int g_kda_error_word = 0;
+
+constexpr int kMaxSeqs = 1024;
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+    int checked = 0;   // 0 unknown, 1 ok, -1 unsupported
+    int num_sms = 0;
+    int *err = nullptr;
+};
+DevInfo g_dev[kMaxDevices];
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+Range range_of(const void *p, size_t bytes)
+{
+    uintptr_t lo = (uintptr_t)p;
+    return {lo, lo + (p ? bytes : 0)};
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int device_info(DevInfo **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return KDA_ERR_DEVICE;
+    }
+    DevInfo &d = g_dev[dev];
+    if (d.checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_DEVICE;
+        }
+        void *err = nullptr;
+        if (cudaGetSymbolAddress(&err, g_kda_error_word) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+        d.num_sms = sms;
+        d.err = (int *)err;
+        d.checked = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (d.checked != 1) return KDA_ERR_DEVICE;
+    *out = &d;
+    return KDA_OK;
+}
+
+// Validation shared by both entry points.  elem = bytes per q/k/v/out element.
+int validate(const void *q, const void *k, const void *v, const float *g, const float *beta,
+             const int32_t *cu, const float *s0, const void *out, const float *s1,
+             int N, int T, int H, int dk, int dv, size_t elem, bool bf16)
+{
+    if (!cu) return KDA_ERR_NULL;
+    if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+    if (N < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return KDA_ERR_SHAPE;
+    const size_t rows = (size_t)T * (size_t)H;
+    if ((size_t)N * (size_t)H > 0x7fffffffu || rows * (size_t)(dk > dv ? dk : dv) * 4 >= ((size_t)1 << 40))
+        return KDA_ERR_SHAPE;
+    if (bf16) {
+        if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+    } else {
+        if (dk != 64 || dv != 64) return KDA_ERR_UNSUPPORTED;
+    }
+    if (N > kMaxSeqs) return KDA_ERR_UNSUPPORTED;
+    const void *aligned_ptrs[] = {q, k, v, g, out, s0, s1};
+    for (const void *p : aligned_ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+    if (((uintptr_t)beta & 3u) || ((uintptr_t)cu & 3u)) return KDA_ERR_ALIGN;
+
+    const size_t state_bytes = (size_t)N * H * dv * dk * sizeof(float);
+    const Range in[] = {range_of(q, rows * dk * elem), range_of(k, rows * dk * elem),
+                        range_of(v, rows * dv * elem), range_of(g, rows * dk * sizeof(float)),
+                        range_of(beta, rows * sizeof(float)),
+                        range_of(cu, (size_t)(N + 1) * sizeof(int32_t)),
+                        range_of(s0, state_bytes)};
+    const Range ro = range_of(out, rows * dv * elem);
+    const Range rs = range_of(s1, state_bytes);
+    for (const Range &r : in)
+        if (overlap(ro, r)) return KDA_ERR_ALIAS;
+    if (overlap(ro, rs)) return KDA_ERR_ALIAS;
+    for (int i = 0; i < 6; i++)
+        if (overlap(rs, in[i])) return KDA_ERR_ALIAS;
+    if (s0 && s1 && overlap(rs, in[6]) && (s0 != s1)) return KDA_ERR_ALIAS;
+    return KDA_OK;
+}
+
+kda::KdaArgs make_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                       const int32_t *cu, const float *s0, void *out, float *s1, int N, int T, int H,
+                       int dk, int dv, void *stream, const DevInfo *d)
+{
+    kda::KdaArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu;
+    a.initial_state = s0; a.out = out; a.final_state = s1;
+    a.N = N; a.T = T; a.H = H; a.dk = dk; a.dv = dv;
+    a.stream = (cudaStream_t)stream;
+    a.err_word = d->err;
+    a.num_sms = d->num_sms;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int status)
+{
+    switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_NULL: return "KDA_ERR_NULL: a required pointer is NULL";
+    case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE: bad sizes (N >= 1, T >= 0, H >= 1) or size overflow";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: dk/dv/dtype combination or N not supported";
+    case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN: tensor pointer not 16-byte aligned";
+    case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS: an output overlaps another argument";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call failed (see cudaGetLastError)";
+    case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE: no CUDA device, or the device is not sm_103";
+    default: return "unknown kda_status";
+    }
+}
+
+int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                      const float *beta, const int32_t *cu_seqlens, const float *initial_state,
+                      uint16_t *out, float *final_state, int N, int T, int H, int dk, int dv,
+                      void *stream)
+{
+    int st = validate(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H, dk, dv,
+                      sizeof(uint16_t), true);
+    if (st != KDA_OK) return st;
+    DevInfo *d = nullptr;
+    if ((st = device_info(&d)) != KDA_OK) return st;
+    kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H,
+                               dk, dv, stream, d);
+    return kda::launch_kda_simt_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_chunk_prefill_f32(const float *q, const float *k, const float *v, const float *g,
+                          const float *beta, const int32_t *cu_seqlens, const float *initial_state,
+                          float *out, float *final_state, int N, int T, int H, int dk, int dv,
+                          void *stream)
+{
+    int st = validate(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H, dk, dv,
+                      sizeof(float), false);
+    if (st != KDA_OK) return st;
+    DevInfo *d = nullptr;
+    if ((st = device_info(&d)) != KDA_OK) return st;
+    kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H,
+                               dk, dv, stream, d);
+    return kda::launch_kda_simt_f32_d64(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_device_error(int *word, int reset)
+{
+    if (!word) return KDA_ERR_NULL;
+    if (cudaMemcpyFromSymbol(word, g_kda_error_word, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    if (reset) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_kda_error_word, &zero, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -16,3 +16,13 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(scope="session")
+def kda_lib():
+    """libkda.so, built here if missing or stale (nvcc cross-compiles without a GPU)."""
+    from kda_linear_attention_chunk_gb300 import build as kbuild
+    import kda_linear_attention_chunk_gb300 as kda
+    if kbuild.stale():
+        kbuild.build()
+    return kda.load()

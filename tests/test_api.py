@@ -1,0 +1,84 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/kda.h declares, and rejects bad arguments
+synchronously with the documented status, before touching any device.
+
+Fake, never-dereferenced addresses are only passed in calls that must fail
+validation; calls that would pass it run only on machines without a GPU."""
+import os
+import re
+
+import pytest
+
+import kda_linear_attention_chunk_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_expected_calls():
+    assert declared_entry_points() == sorted(kda.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(kda_lib):
+    for name in declared_entry_points():
+        assert hasattr(kda_lib, name), name
+
+
+def test_status_strings(kda_lib):
+    for s in range(8):
+        assert kda_lib.kda_status_string(s).decode().startswith("KDA_")
+    assert b"unknown" in kda_lib.kda_status_string(99)
+
+
+A = 1 << 20   # fake, 16-byte aligned, never dereferenced addresses
+
+
+def call(fn="kda_chunk_prefill", **over):
+    T, H, d, N = 64, 2, 128, 1
+    rows = T * H * d
+    args = dict(q=A, k=A + 2 * rows * 4, v=A + 4 * rows * 4, g=A + 6 * rows * 4, beta=A + 10 * rows * 4,
+                cu=A + 11 * rows * 4, s0=0, out=A + 12 * rows * 4, s1=0, N=N, T=T, H=H, dk=d, dv=d,
+                stream=0)
+    if fn == "kda_chunk_prefill_f32":
+        args["dk"] = args["dv"] = 64
+    args.update(over)
+    order = ["q", "k", "v", "g", "beta", "cu", "s0", "out", "s1", "N", "T", "H", "dk", "dv", "stream"]
+    return getattr(kda, fn)(*[args[n] for n in order])
+
+
+@pytest.mark.parametrize("fn", ["kda_chunk_prefill", "kda_chunk_prefill_f32"])
+def test_validation_statuses(kda_lib, fn):
+    assert call(fn, q=0) == kda.KDA_ERR_NULL
+    assert call(fn, cu=0) == kda.KDA_ERR_NULL
+    assert call(fn, N=0) == kda.KDA_ERR_SHAPE
+    assert call(fn, T=-1) == kda.KDA_ERR_SHAPE
+    assert call(fn, H=0) == kda.KDA_ERR_SHAPE
+    assert call(fn, dk=96, dv=96) == kda.KDA_ERR_UNSUPPORTED
+    assert call(fn, N=2000) == kda.KDA_ERR_UNSUPPORTED
+    assert call(fn, q=A + 8) == kda.KDA_ERR_ALIGN
+    assert call(fn, beta=A + 2) == kda.KDA_ERR_ALIGN
+    assert call(fn, out=A + 16) == kda.KDA_ERR_ALIAS                                  # out overlaps q
+    assert call(fn, s0=A + (40 << 20), s1=A + (40 << 20) + 64) == kda.KDA_ERR_ALIAS   # partial overlap
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+def test_exact_state_alias_passes_validation(kda_lib):
+    assert call(s0=A + (40 << 20), s1=A + (40 << 20)) == kda.KDA_ERR_DEVICE
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+def test_empty_rows_allow_null_tensors(kda_lib):
+    assert call(q=0, k=0, v=0, g=0, beta=0, out=0, T=0) == kda.KDA_ERR_DEVICE
