@@ -1,15 +1,11 @@
 """Seeded synthetic inputs for the KDA chunked packed-varlen prefill.
 
 This module only draws inputs.  It holds none of the method's arithmetic, so
-both the CUDA path and the CPU oracle can take their inputs from it.
-
-Generator: a counter-based splitmix64.  Element ``i`` of stream ``s`` under
-seed ``seed`` is ``mix64(mix64(seed) + s * 2**48 + i)``, where ``mix64`` is the
-splitmix64 output function (add the golden-ratio increment, then the two
-xor-shift-multiply rounds and a final xor-shift).  Because every element is a
-pure function of its flat index, any row range or head subset of a tensor can
-be drawn on its own and agrees with the full tensor.  Normal deviates use the
-Box-Muller transform on the uniforms of indices ``2i`` and ``2i + 1``.
+both the CUDA path and the CPU oracle take their inputs from it.  The element
+generator is the small C helper synthetic_gen.c (built here with gcc on first
+use): a counter-based splitmix64 with Box-Muller normals, where every value is
+a pure function of (seed, stream, flat index), so any row range or head
+subset of a tensor can be drawn on its own and agrees with the full tensor.
 
 Input recipe (the production packed prefill of the kern-k3-pp-prefill README,
 section "P: the packed prefill": up to 16 sequences in an 8192-row chunk,
@@ -20,55 +16,66 @@ contexts to 262144, per-sequence states):
 * g = log(alpha) ~ U[-0.2, 0] per token, head and channel;
 * beta = sigmoid(N(0, 1)) per token and head;
 * initial state ~ N(0, 0.02) (standard deviation) where the workload has one;
-* q, k, v rounded to bf16 (round to nearest even) unless the workload is fp32.
+* q, k, v rounded to bf16 (round to nearest even) unless the workload is fp32;
+* sequence lengths of the 16-sequence chunk: a seeded Dirichlet(1, ..., 1)
+  split of 8192 rows, each at least 1.
 
-The random values are computed in float64; numpy's elementwise log/cos/exp
-may differ in the last ulp between machines, so the bits are reproducible on
-one machine (where both arms run) and agree almost always across machines.
+Values are computed in double precision with the C library's log/cos/exp, so
+the bits are reproducible on one machine (where both arms run) and agree
+almost always across machines.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
 from typing import Dict, List, Optional, Sequence
 
 import numpy as np
 
-_M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
-_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
-_C1 = np.uint64(0xBF58476D1CE4E5B9)
-_C2 = np.uint64(0x94D049BB133111EB)
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synthetic_gen.c")
+_LIB = os.path.join(_HERE, "_build", "libsynth.so")
 
-STREAM_Q, STREAM_K, STREAM_V, STREAM_G, STREAM_BETA, STREAM_INIT, STREAM_LENS = 1, 2, 3, 4, 5, 6, 7
-
-
-def _mix64(x: np.ndarray) -> np.ndarray:
-    """splitmix64 output function on a uint64 array (wrapping arithmetic)."""
-    with np.errstate(over="ignore"):
-        z = x + _GOLDEN
-        z = (z ^ (z >> np.uint64(30))) * _C1
-        z = (z ^ (z >> np.uint64(27))) * _C2
-        return z ^ (z >> np.uint64(31))
+KIND_Q, KIND_K, KIND_V, KIND_G, KIND_BETA, KIND_STATE = range(6)
+STREAM_LENS = 7
+_gen = None
 
 
-def raw_u64(seed: int, stream: int, index: np.ndarray) -> np.ndarray:
-    key = _mix64(np.array([seed], dtype=np.uint64))[0]
-    with np.errstate(over="ignore"):
-        ctr = key + np.uint64(stream) * np.uint64(1 << 48) + index.astype(np.uint64)
-    return _mix64(ctr)
+def build_generator() -> str:
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    tmp = _LIB + f".{os.getpid()}.tmp"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread", "-o", tmp, _SRC, "-lm"],
+                   check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
 
 
-def uniform(seed: int, stream: int, index: np.ndarray) -> np.ndarray:
-    """Uniform deviates in the open interval (0, 1), float64."""
-    bits = raw_u64(seed, stream, index) >> np.uint64(11)
-    return (bits.astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
+def _lib():
+    global _gen
+    if _gen is None:
+        if not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            build_generator()
+        lib = ctypes.CDLL(_LIB)
+        lib.syn_fill.argtypes = [ctypes.c_int, ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64,
+                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+        lib.syn_fill.restype = ctypes.c_int
+        lib.syn_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p]
+        lib.syn_uniform.restype = ctypes.c_int
+        _gen = lib
+    return _gen
 
 
-def normal(seed: int, stream: int, index: np.ndarray) -> np.ndarray:
-    """Standard normal deviates (Box-Muller, cosine branch), float64."""
-    idx = index.astype(np.uint64) * np.uint64(2)
-    u1 = uniform(seed, stream, idx)
-    u2 = uniform(seed, stream, idx + np.uint64(1))
-    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def uniform(seed: int, stream: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.float64)
+    _lib().syn_uniform(seed, stream, n, out.ctypes.data)
+    return out
 
 
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -80,7 +87,7 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
-    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return (np.ascontiguousarray(b).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
 def dirichlet_lengths(total: int, parts: int, seed: int) -> List[int]:
@@ -88,7 +95,7 @@ def dirichlet_lengths(total: int, parts: int, seed: int) -> List[int]:
     Dirichlet(1, ..., 1) draw (normalised exponentials).  Each part gets
     1 + floor(p_i * (total - parts)); the rows left over go one each to the
     largest fractional remainders (ties to the lower index)."""
-    e = -np.log(uniform(seed, STREAM_LENS, np.arange(parts, dtype=np.uint64)))
+    e = -np.log(uniform(seed, STREAM_LENS, parts))
     p = e / e.sum()
     share = p * (total - parts)
     base = np.floor(share).astype(np.int64)
@@ -149,11 +156,17 @@ def workloads() -> Dict[str, Workload]:
     }
 
 
-def _flat_index(rows: np.ndarray, heads: np.ndarray, H: int, d: int) -> np.ndarray:
-    r = rows.astype(np.uint64)[:, None, None]
-    h = heads.astype(np.uint64)[None, :, None]
-    c = np.arange(d, dtype=np.uint64)[None, None, :]
-    return (r * np.uint64(H) + h) * np.uint64(d) + c
+def _heads(w: Workload, heads: Optional[Sequence[int]]) -> np.ndarray:
+    return np.arange(w.H, dtype=np.int32) if heads is None else np.asarray(list(heads), dtype=np.int32)
+
+
+def _fill(kind, w, row_lo, nrows, hs, d, shape, dtype, out_code):
+    out = np.empty(shape, dtype=dtype)
+    rc = _lib().syn_fill(kind, w.seed, row_lo, nrows, hs.ctypes.data, len(hs), w.H, d,
+                         out.ctypes.data, out_code, _threads())
+    if rc != 0:
+        raise ValueError("synthetic generator rejected its arguments")
+    return out
 
 
 def draw(w: Workload, row_lo: int = 0, row_hi: Optional[int] = None,
@@ -165,45 +178,36 @@ def draw(w: Workload, row_lo: int = 0, row_hi: Optional[int] = None,
     values are those of the full [T][H][d] tensors at those positions."""
     if row_hi is None:
         row_hi = w.T
-    hs = np.arange(w.H) if heads is None else np.asarray(list(heads), dtype=np.int64)
-    rows = np.arange(row_lo, row_hi, dtype=np.int64)
-    out: Dict[str, np.ndarray] = {}
-    for name, stream, d in (("q", STREAM_Q, w.dk), ("k", STREAM_K, w.dk), ("v", STREAM_V, w.dv)):
-        x = normal(w.seed, stream, _flat_index(rows, hs, w.H, d))
-        if name in ("q", "k"):
-            x = x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
-        out[name] = to_bf16_bits(x) if w.qkv_dtype == "bf16" else x.astype(np.float32)
-    u = uniform(w.seed, STREAM_G, _flat_index(rows, hs, w.H, w.dk))
-    out["g"] = (-0.2 * u).astype(np.float32)
-    bidx = (rows.astype(np.uint64)[:, None] * np.uint64(w.H) + hs.astype(np.uint64)[None, :])
-    out["beta"] = (1.0 / (1.0 + np.exp(-normal(w.seed, STREAM_BETA, bidx)))).astype(np.float32)
-    return out
+    hs = _heads(w, heads)
+    n = row_hi - row_lo
+    bf = w.qkv_dtype == "bf16"
+    dt, code = (np.uint16, 0) if bf else (np.float32, 1)
+    return {
+        "q": _fill(KIND_Q, w, row_lo, n, hs, w.dk, (n, len(hs), w.dk), dt, code),
+        "k": _fill(KIND_K, w, row_lo, n, hs, w.dk, (n, len(hs), w.dk), dt, code),
+        "v": _fill(KIND_V, w, row_lo, n, hs, w.dv, (n, len(hs), w.dv), dt, code),
+        "g": _fill(KIND_G, w, row_lo, n, hs, w.dk, (n, len(hs), w.dk), np.float32, 1),
+        "beta": _fill(KIND_BETA, w, row_lo, n, hs, 1, (n, len(hs)), np.float32, 1),
+    }
 
 
 def draw_initial_state(w: Workload, heads: Optional[Sequence[int]] = None) -> Optional[np.ndarray]:
     """[N][nh][dv][dk] float32 initial states, or None for a zero start."""
     if not w.init_state:
         return None
-    hs = np.arange(w.H) if heads is None else np.asarray(list(heads), dtype=np.int64)
-    n = np.arange(w.N, dtype=np.uint64)[:, None, None, None]
-    h = hs.astype(np.uint64)[None, :, None, None]
-    v = np.arange(w.dv, dtype=np.uint64)[None, None, :, None]
-    c = np.arange(w.dk, dtype=np.uint64)[None, None, None, :]
-    idx = ((n * np.uint64(w.H) + h) * np.uint64(w.dv) + v) * np.uint64(w.dk) + c
-    return (0.02 * normal(w.seed, STREAM_INIT, idx)).astype(np.float32)
+    assert w.dk == w.dv
+    hs = _heads(w, heads)
+    return _fill(KIND_STATE, w, 0, w.N, hs, w.dk, (w.N, len(hs), w.dv, w.dk), np.float32, 1)
 
 
 def random_lengths(total: int, parts: int, seed: int, allow_empty: bool = False) -> List[int]:
-    """Seeded ragged lengths for edge-case tests (may include zeros)."""
+    """Seeded ragged lengths for edge-case tests (zeros allowed if asked)."""
     if parts == 1:
         return [total]
-    u = uniform(seed, STREAM_LENS + 100, np.arange(parts - 1, dtype=np.uint64))
+    u = uniform(seed, STREAM_LENS + 100, parts - 1)
     cuts = np.sort((u * (total + 1)).astype(np.int64).clip(0, total))
-    edges = np.concatenate([[0], cuts, [total]])
-    lens = [int(x) for x in np.diff(edges)]
+    lens = [int(x) for x in np.diff(np.concatenate([[0], cuts, [total]]))]
     if not allow_empty:
         lens = [max(1, x) for x in lens]
-        diff = sum(lens) - total
-        i = int(np.argmax(lens))
-        lens[i] -= diff
+        lens[int(np.argmax(lens))] -= sum(lens) - total
     return lens
