@@ -77,11 +77,13 @@ kda_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin 
         }
         if (tid < kChunk) sm.beta[tid] = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
         __syncthreads();
-        // S <- Diag(exp(G_m)) S: the state seen from row m (with the previous
-        // chunk's pending decay to its last row folded in).
+        // S <- Diag(exp(G_m)) Diag(pend) S: first the previous chunk's pending
+        // decay to its last row, then the view from row m.  Two separate
+        // roundings, so a context split into calls (state stored after the
+        // first multiply) reproduces the single-call bits.
         for (int idx = tid; idx < D * D; idx += kThreads) {
             int c = idx / D;
-            sm.S[idx] *= sm.pend[c] * expf(sm.gm[c]);
+            sm.S[idx] = (sm.S[idx] * sm.pend[c]) * expf(sm.gm[c]);
         }
         // Decay-scaled operands (one thread per channel walks the rows).
         if (tid < D) {
