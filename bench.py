@@ -1,0 +1,322 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA chunked packed-varlen prefill on one GB300.
+
+Workload: the production packed chunk -- 16 sequences with seeded Dirichlet(1)
+lengths summing to 8192 rows, H = 32, dk = dv = 128, bf16 q/k/v/out, fp32
+g/beta, nonzero fp32 initial states, fp32 final states (kern-k3-pp-prefill
+README, "P: the packed prefill").  One step is one kda_chunk_prefill call over
+the whole chunk.  Metric: rows (tokens) per second, plus the achieved fraction
+of the HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line.  --impl reference times the fp64 CPU oracle on the host
+cores instead (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA packed-prefill tokens/s on 1 GB300 (8192-row chunk) + % of roofline"
+WORKLOAD = "packed16_8192"
+KERNEL_NAME = "kda_tc_kernel"
+BYTES_PER_TOKEN_HEAD = 1540          # q, k, v, out bf16 (4 x 256 B) + g fp32 (512 B) + beta (4 B)
+
+
+def algorithmic_bytes(w, with_initial=True, with_final=True) -> int:
+    per_state = w.dk * w.dv * 4
+    b = w.T * w.H * BYTES_PER_TOKEN_HEAD
+    b += w.N * w.H * per_state * (int(with_initial) + int(with_final))
+    return b
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    csrc = os.path.join(ROOT, "kda_linear_attention_chunk_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel sources as they are now; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    if d.get("kernel_source_sha") != kernel_source_sha() or d.get("workload") != WORKLOAD:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.p = None
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.tmp.flush()
+        rows = []
+        for line in open(self.tmp.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 9:
+                rows.append(parts)
+        os.unlink(self.tmp.name)
+        return rows
+
+
+def summarize_clocks(rows):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+    sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+    mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows)}
+
+
+def make_device_inputs(w, seed_offset, torch, np):
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+    w2 = syn.Workload(w.name, w.lengths, w.H, w.dk, w.dv, w.qkv_dtype, w.init_state, seed=w.seed + seed_offset)
+    x = syn.draw(w2)
+    s0 = syn.draw_initial_state(w2)
+    pin = {}
+    for k, v in x.items():
+        t = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16 else torch.from_numpy(v)
+        pin[k] = t.pin_memory()
+    pin["s0"] = torch.from_numpy(s0).pin_memory()
+    pin["cu"] = torch.from_numpy(w.cu_seqlens()).pin_memory()
+    dev = {k: v.cuda() for k, v in pin.items()}
+    return pin, dev
+
+
+def run_gpu_arm(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import kda_linear_attention_chunk_gb300 as kda
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    w = syn.workloads()[WORKLOAD]
+    sets = [make_device_inputs(w, i, torch, np) for i in range(2)]   # 2 rotating sets (> L2 each)
+    stream = torch.cuda.current_stream()
+    outs = [torch.empty((w.T, w.H, w.dv), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    fins = [torch.empty((w.N, w.H, w.dv, w.dk), dtype=torch.float32, device="cuda") for _ in range(2)]
+
+    def step(i):
+        d = sets[i % 2][1]
+        kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu"], initial_state=d["s0"],
+                          out=outs[i % 2], final_state=fins[i % 2], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    time.sleep(0.25)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    kernel_ms = ev0.elapsed_time(ev1) / args.steps
+
+    # end to end through the public API: pinned host inputs -> device, call, results -> pinned host
+    host_out = torch.empty((w.T, w.H, w.dv), dtype=torch.bfloat16).pin_memory()
+    host_fin = torch.empty((w.N, w.H, w.dv, w.dk), dtype=torch.float32).pin_memory()
+    dev_in = {k: torch.empty_like(v, device="cuda") for k, v in sets[0][0].items()}
+    h2d = sum(v.numel() * v.element_size() for v in sets[0][0].values())
+    d2h = host_out.numel() * 2 + host_fin.numel() * 4
+
+    def e2e_step(i):
+        pin = sets[i % 2][0]
+        for k, v in pin.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        kda.chunk_prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["cu"],
+                          initial_state=dev_in["s0"], out=outs[0], final_state=fins[0], stream=stream)
+        host_out.copy_(outs[0], non_blocking=True)
+        host_fin.copy_(fins[0], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    clocks = summarize_clocks(sampler.stop())
+    assert kda.device_error() == 0, "device error word set during the bench"
+
+    t = torch.tensor([kernel_ms, e2e_ms], device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    kernel_ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    value = world * w.T / (kernel_ms / 1e3)
+    alg = algorithmic_bytes(w)
+    peak, peak_kind = peaks()
+    achieved = alg / (kernel_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": kernel_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64; recipe in DESIGN.md)",
+        "config": {"workload": WORKLOAD, "N": w.N, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "lengths": w.lengths, "initial_state": "N(0,0.02) fp32", "final_state": True,
+                   "l2": "inputs larger than L2: 2 rotating input sets of %.0f MB" % (alg / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "e2e": {"value": world * w.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(),
+                     "kernel": KERNEL_NAME, "algorithmic_bytes_per_launch": alg,
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, heads=args.cpu_heads)
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+def cpu_baseline(w, heads: int):
+    """The oracle (fp64 token recurrence, plain C, all host cores) on a bounded
+    sample of the same workload: all 8192 rows for `heads` of the H heads."""
+    import oracle
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+
+    hs = list(range(heads))
+    x = syn.draw(w, heads=hs)
+    s0 = syn.draw_initial_state(w, heads=hs)
+    cores = os.cpu_count() or 1
+    oracle.load()
+    t0 = time.perf_counter()
+    oracle.run(x["q"], x["k"], x["v"], x["g"], x["beta"], w.cu_seqlens(), initial_state=s0,
+               nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": w.T * (heads / w.H) / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"all {w.T} rows of the {WORKLOAD} workload for {heads} of {w.H} heads; tokens/s "
+                      f"counts a row as {heads}/{w.H} of a token"}
+
+
+def run_reference_arm(args):
+    """The reference arm: the fp64 CPU oracle as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+    import oracle
+
+    w = syn.workloads()[WORKLOAD]
+    heads = args.ref_heads
+    hs = list(range(heads))
+    x = syn.draw(w, heads=hs)
+    s0 = syn.draw_initial_state(w, heads=hs)
+    cores = os.cpu_count() or 1
+    oracle.load()
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.run(x["q"], x["k"], x["v"], x["g"], x["beta"], w.cu_seqlens(), initial_state=s0,
+                   nthreads=cores)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = w.T * (heads / w.H) / (ms / 1e3)
+    sample = (f"each step: all {w.T} rows of the {WORKLOAD} workload for {heads} of {w.H} heads; "
+              f"tokens/s counts a row as {heads}/{w.H} of a token")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "N": w.N, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-heads", type=int, default=32)
+    ap.add_argument("--ref-heads", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_reference_arm(args) if args.impl == "reference" else run_gpu_arm(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
