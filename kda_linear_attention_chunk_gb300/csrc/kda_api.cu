@@ -150,7 +150,7 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
     if ((st = device_info(&d)) != KDA_OK) return st;
     kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H,
                                dk, dv, stream, d);
-    return kda::launch_kda_simt_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda::launch_kda_tc_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_chunk_prefill_f32(const float *q, const float *k, const float *v, const float *g,

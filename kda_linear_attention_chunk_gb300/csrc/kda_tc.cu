@@ -1,0 +1,863 @@
+// kda_tc.cu -- the fused tensor-core KDA chunked packed-varlen prefill for
+// GB300 (sm_103a): one persistent kernel, TMA-staged tiles, tcgen05 MMAs with
+// fp32 accumulators in TMEM, warp-specialised prep / chain / load roles.
+//
+// What one (sequence, head) "unit" computes, per 64-row chunk with L valid
+// rows (KDA recurrence S_t = (I - b k k^T) Diag(exp(g_t)) S_{t-1} + b k v^T,
+// o_t = S_t^T q_t, in the chunked WY form: cumulative log-decay G, strictly
+// lower A_kk = beta_i (k_i * exp(G_i - G_j)) . k_j, the inverse of (I + A_kk),
+// the factors W and U, the inter-chunk state recurrence, the outputs):
+//
+//   G_r  = sum_{u<=r} g_u,  m = (L-1)/2,  a_r = exp(G_r - G_m), b_r = 1/a_r
+//   Kp = K*a, Qp = Q*a, Km = K*b                 (fp16, in shared memory)
+//   [A_kk ; A_qk] = [Kp ; Qp] Km^T               MMA-a  (M=128, N=64, K=128)
+//   M  = (I + beta*strict(A_kk))^-1 diag(beta)   CUDA cores, fp32
+//   W'^T = Kp^T M^T,  U^T = V^T M^T              MMA-b  (M=128, N=64, K=64)
+//   S' = Diag(exp(G_m)) S                        (state seen from row m)
+//   Delta^T = U^T - S'^T W'^T                    MMA1a  (A = S'^T from TMEM)
+//   O^T   = S'^T Qp^T + Delta^T B^T              MMA1b + MMA3b (B = tril(A_qk))
+//   S^T  += Delta^T Km                           MMA3a  (state stays fp32 in TMEM)
+//   S   <- Diag(exp(G_{L-1} - G_m)) S            (applied at the next chunk start)
+//
+// Everything is kept "v-major" (TMEM lane = value channel v) so that every MMA
+// has M = 128 and the state S^T = [dv][dk] lives in TMEM in exactly the
+// layout of the [slot][head][v][k] state pool.  MMA operands are fp16 (fp32
+// accumulate): bf16 operands would cost ~2e-3 relative error, fp16 costs
+// ~2e-4; the midpoint reference m keeps every scaled operand within fp16 range
+// for half-chunk log-decays above about -11.
+//
+// Roles (416 threads):
+//   warps 0-3   chain: state scaling, S' and Delta conversion, the chain MMAs,
+//               output and final-state stores (one elected thread issues MMAs)
+//   warps 4-11  prep: cumulative log-decay (warp shuffles), decay-scaled
+//               operands, MMA-a, the 64x64 inverse, MMA-b, W' conversion
+//   warp 12     TMA producer and TMEM allocator
+// Two shared-memory stages let the prep of chunk c+1 overlap the chain of
+// chunk c.  Every mbarrier wait is bounded; on timeout the kernel records
+// kErrWaitTimeout in the device error word and winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+constexpr int kD = 128;
+constexpr int kThreads = 416;
+constexpr int kChainThreads = 128;
+constexpr int kPrepThreads = 256;
+constexpr int kBarChain = 1, kBarPrep = 2;
+constexpr int kMaxSortedSeqs = 256;
+
+// ---- shared memory map (bytes from a 1024-aligned base) ----------------------
+constexpr uint32_t kStageBytes = 98304;
+constexpr uint32_t kOffKQ = 0;          // [kb][K rows 0-63 | Q rows 0-63], 2 x 16 KB
+constexpr uint32_t kOffKM = 32768;      // Km, 2 x 8 KB
+constexpr uint32_t kOffV = 49152;       // V (fp16 in place of bf16), 2 x 8 KB
+constexpr uint32_t kOffGX = 65536;      // g (fp32, 4 x 8 KB); later M | B | W' (and T)
+constexpr uint32_t kOffM = kOffGX;              // M [r][j] fp16, 8 KB
+constexpr uint32_t kOffB = kOffGX + 8192;       // tril(A_qk) [r][i] fp16, 8 KB
+constexpr uint32_t kOffW = kOffGX + 16384;      // -W' [c][r] fp16, 16 KB (T fp32 before)
+constexpr uint32_t kOffL = 2 * kStageBytes;     // 196608: L fp32 64x64 (also scan exchange)
+constexpr uint32_t kOffP = kOffL + 16384;       // merge temporaries, 6 KB
+constexpr uint32_t kOffConst = kOffP + 6144;    // per stage: fm[128] pend[128] beta[64]
+constexpr uint32_t kConstBytes = 1280;
+constexpr uint32_t kOffGm = kOffConst + 2 * kConstBytes;   // G_m[128], G_last[128]
+constexpr uint32_t kOffOrder = kOffGm + 1024;              // sorted sequence order
+constexpr uint32_t kOffBar = kOffOrder + 4 * kMaxSortedSeqs;
+constexpr uint32_t kOffMisc = kOffBar + 128;
+constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;      // + alignment slack
+
+// mbarrier slots
+constexpr int kBarRawFull = 0;     // [2]
+constexpr int kBarStageFree = 2;   // [2]
+constexpr int kBarPrepDone = 4;    // [2]
+constexpr int kBarAFull = 6, kBarWFull = 7, kBarMma1 = 8, kBarMma3 = 9, kBarDrain = 10;
+
+// TMEM columns
+constexpr uint32_t kTmS = 0, kTmP = 128, kTmS0h = 384, kTmDh = 448, kTmCols = 512;
+
+constexpr uint32_t kRawBytes = 10 * 8192;       // q, k, v (2 boxes each) + g (4 boxes)
+
+struct TcParams {
+    const int32_t *cu;
+    const float *beta;
+    const float *s0;
+    __nv_bfloat16 *out;
+    float *s1;
+    int N, T, H;
+    int sorted;        // 1 if the sequence order was sorted (N <= kMaxSortedSeqs)
+    int *err;
+};
+
+struct Smem {
+    uint8_t *base;
+    __device__ uint32_t u32(uint32_t off) const { return smem_u32(base + off); }
+    template <typename T> __device__ T *ptr(uint32_t off) const { return reinterpret_cast<T *>(base + off); }
+    __device__ uint32_t bar(int i) const { return u32(kOffBar + 8 * i); }
+    __device__ volatile int *abort_flag() const { return ptr<volatile int>(kOffMisc + 4); }
+    __device__ uint32_t *tmem_base() const { return ptr<uint32_t>(kOffMisc); }
+};
+
+__device__ __forceinline__ bool role_any(bool pred, int id, int n)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// Unit u (in this CTA's schedule order) -> (sequence, head, rows).
+struct Unit {
+    int n, h, bos, eos, nchunks;
+};
+
+__device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, int u)
+{
+    Unit x;
+    const int su = u / p.H;
+    x.h = u % p.H;
+    x.n = p.sorted ? order[su] : su;
+    int b = p.cu[x.n], e = p.cu[x.n + 1];
+    b = min(max(b, 0), p.T);
+    e = min(max(e, 0), p.T);
+    if (e < b) e = b;
+    x.bos = b;
+    x.eos = e;
+    x.nchunks = (e - b + kChunk - 1) / kChunk;
+    return x;
+}
+
+// k-th unit of this CTA under a boustrophedon ("snake") deal of the
+// length-sorted unit list over the grid; -1 when exhausted.
+__device__ __forceinline__ int cta_unit(int k, int U)
+{
+    const int G = gridDim.x, b = blockIdx.x;
+    const int u = k * G + ((k & 1) ? (G - 1 - b) : b);
+    return u < U ? u : -1;
+}
+
+// swizzled index into a 64x64 fp32 matrix (conflict-free row and column access)
+__device__ __forceinline__ int swz64(int i, int j) { return i * 64 + (j ^ (i & 31)); }
+
+// byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ void record_error(const TcParams &p, const Smem &sm, int code)
+{
+    atomicOr(p.err, code);
+    *sm.abort_flag() = 1;
+}
+
+// =============================================================================
+// prep role: warps 4-11
+// =============================================================================
+__device__ void prep_elementwise(const TcParams &p, const Smem &sm, int s, const Unit &un, int row0, int L,
+                                 int pt)
+{
+    const int pw = pt >> 5, lane = pt & 31;
+    const int rr = lane & 7, cg = lane >> 3;
+    const int r = pw * 8 + rr;
+    const uint32_t st = s * kStageBytes;
+    float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
+    float *xchg = sm.ptr<float>(kOffL);            // [8 warps][128 channels]
+    float *gmx = sm.ptr<float>(kOffGm);
+    float *glx = gmx + 128;
+
+    float beta_r = 0.f;
+    if (cg == 0 && r < L) beta_r = __ldg(p.beta + (size_t)(row0 + r) * p.H + un.h);
+
+    // g -> inclusive prefix over rows, per channel
+    float G[32];
+    {
+        const uint8_t *gb = sm.base + st + kOffGX + cg * 8192;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            float4 x = *reinterpret_cast<const float4 *>(gb + sw128_chunk(r, j));
+            G[4 * j + 0] = x.x; G[4 * j + 1] = x.y; G[4 * j + 2] = x.z; G[4 * j + 3] = x.w;
+        }
+        if (r >= L) {
+#pragma unroll
+            for (int j = 0; j < 32; j++) G[j] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            float y = __shfl_up_sync(0xffffffffu, G[j], d, 8);
+            if (rr >= d) G[j] += y;
+        }
+    }
+    if (rr == 7) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(xchg + pw * 128 + 32 * cg + j) = make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
+    }
+    named_bar(kBarPrep, kPrepThreads);
+    for (int w = 0; w < pw; w++) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 x = *reinterpret_cast<const float4 *>(xchg + w * 128 + 32 * cg + j);
+            G[j] += x.x; G[j + 1] += x.y; G[j + 2] += x.z; G[j + 3] += x.w;
+        }
+    }
+    const int m = (L - 1) >> 1;
+    if (r == m) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(gmx + 32 * cg + j) = make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
+    }
+    if (r == L - 1) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(glx + 32 * cg + j) = make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
+    }
+    if (cg == 0) cst[256 + r] = beta_r;
+    named_bar(kBarPrep, kPrepThreads);
+
+    float gm[32];
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        float4 x = *reinterpret_cast<const float4 *>(gmx + 32 * cg + j);
+        gm[j] = x.x; gm[j + 1] = x.y; gm[j + 2] = x.z; gm[j + 3] = x.w;
+    }
+    if (r == 0) {
+        // chain constants: fm = exp(G_m) (view from row m), pend = exp(G_last - G_m)
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            cst[32 * cg + j] = __expf(gm[j]);
+            cst[128 + 32 * cg + j] = __expf(glx[32 * cg + j] - gm[j]);
+        }
+    }
+
+    // decay-scaled fp16 operands, in place over the bf16 tiles
+    const int kb = cg >> 1;
+    uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
+    uint8_t *qt = kt + 8192;
+    uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
+    uint8_t *vt = sm.base + st + kOffV + kb * 8192;
+    const bool valid = r < L;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
+        uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
+        uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
+        uint4 vq = *reinterpret_cast<const uint4 *>(vt + off);
+        const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+        const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
+        const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
+        uint32_t okp[4], okm[4], oqp[4], ov[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int g0 = 8 * j + 2 * e;
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+            if (valid) {
+                a0 = __expf(G[g0] - gm[g0]);
+                a1 = __expf(G[g0 + 1] - gm[g0 + 1]);
+                b0 = __expf(gm[g0] - G[g0]);
+                b1 = __expf(gm[g0 + 1] - G[g0 + 1]);
+            }
+            const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
+            const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
+            okp[e] = pack_f16x2(k0 * a0, k1 * a1);
+            okm[e] = pack_f16x2(k0 * b0, k1 * b1);
+            oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
+            ov[e] = valid ? pack_f16x2(bf16lo(vw[e]), bf16hi(vw[e])) : 0u;
+        }
+        *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
+        *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
+        *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
+        *reinterpret_cast<uint4 *>(vt + off) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+    }
+    fence_proxy_async_smem();
+    named_bar(kBarPrep, kPrepThreads);
+}
+
+// A readout: strictly lower, beta-scaled A_kk -> L (fp32 smem);
+// lower A_qk (diagonal included) -> B (fp16, K-major [r][i]).
+__device__ void prep_read_a(const Smem &sm, int s, uint32_t tmem, int pt)
+{
+    const int pw = pt >> 5, lane = pt & 31;
+    const int sp = pw & 3, ch = pw >> 2;
+    const int R = 32 * sp + lane;
+    uint32_t a[32];
+    tmem_ld32(tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * sp) << 16) + 32 * ch, a);
+    tmem_wait_ld();
+    const float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
+    if (R < 64) {
+        float *Lm = sm.ptr<float>(kOffL);
+        const float bi = cst[256 + R];
+#pragma unroll
+        for (int jj = 0; jj < 32; jj++) {
+            const int j = 32 * ch + jj;
+            Lm[swz64(R, j)] = (j < R) ? bi * __uint_as_float(a[jj]) : 0.f;
+        }
+    } else {
+        const int rr = R - 64;
+        uint8_t *Bt = sm.base + s * kStageBytes + kOffB;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int i0 = 32 * ch + 8 * q + 2 * e;
+                const float x0 = (i0 <= rr) ? __uint_as_float(a[8 * q + 2 * e]) : 0.f;
+                const float x1 = (i0 + 1 <= rr) ? __uint_as_float(a[8 * q + 2 * e + 1]) : 0.f;
+                w[e] = pack_f16x2(x0, x1);
+            }
+            *reinterpret_cast<uint4 *>(Bt + sw128_chunk(rr, 4 * ch + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    named_bar(kBarPrep, kPrepThreads);
+}
+
+// (I + L)^-1 by 16x16 diagonal-block forward substitution (warp shuffles)
+// and two levels of block merges; then M = T diag(beta) -> fp16.
+__device__ void prep_inverse(const Smem &sm, int s, int pt)
+{
+    const float *Lm = sm.ptr<float>(kOffL);
+    float *Tm = sm.ptr<float>(s * kStageBytes + kOffW);   // fp32 64x64, swizzled
+    float *P1 = sm.ptr<float>(kOffP);                     // [2][16][16]
+    float *P2 = P1 + 512;                                 // [32][32]
+    const float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
+
+    if (pt < 64) {
+        const int i = pt, blk = i >> 4, a = i & 15, lane = pt & 31;
+        float Lr[16], x[16];
+#pragma unroll
+        for (int t = 0; t < 16; t++) {
+            Lr[t] = Lm[swz64(i, 16 * blk + t)];
+            x[t] = (t == a) ? 1.f : 0.f;
+        }
+#pragma unroll
+        for (int a2 = 0; a2 < 15; a2++) {
+            const int src = (lane & 16) | a2;
+#pragma unroll
+            for (int col = 0; col <= a2; col++) {
+                const float xs = __shfl_sync(0xffffffffu, x[col], src);
+                if (a > a2) x[col] -= Lr[a2] * xs;
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 16; t++)
+            if (t <= a) Tm[swz64(i, 16 * blk + t)] = x[t];
+    }
+    named_bar(kBarPrep, kPrepThreads);
+    // level 1: T10 = -X1 (L10 X0), T32 = -X3 (L32 X2)
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int idx = pt + 256 * e;
+        const int bl = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+        const int r0 = 32 * bl + 16, c0 = 32 * bl;
+        float acc = 0.f;
+        for (int kk = cc; kk < 16; kk++) acc += Lm[swz64(r0 + rr, c0 + kk)] * Tm[swz64(c0 + kk, c0 + cc)];
+        P1[idx] = acc;
+    }
+    named_bar(kBarPrep, kPrepThreads);
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        const int idx = pt + 256 * e;
+        const int bl = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+        const int r0 = 32 * bl + 16, c0 = 32 * bl;
+        float acc = 0.f;
+        for (int kk = 0; kk <= rr; kk++) acc += Tm[swz64(r0 + rr, r0 + kk)] * P1[bl * 256 + kk * 16 + cc];
+        Tm[swz64(r0 + rr, c0 + cc)] = -acc;
+    }
+    named_bar(kBarPrep, kPrepThreads);
+    // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (L[32:64, 0:32] T[0:32, 0:32])
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const int idx = pt + 256 * e;
+        const int r2 = idx >> 5, cc = idx & 31;
+        float acc = 0.f;
+        for (int kk = cc; kk < 32; kk++) acc += Lm[swz64(32 + r2, kk)] * Tm[swz64(kk, cc)];
+        P2[idx] = acc;
+    }
+    named_bar(kBarPrep, kPrepThreads);
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const int idx = pt + 256 * e;
+        const int r2 = idx >> 5, cc = idx & 31;
+        float acc = 0.f;
+        for (int kk = 0; kk <= r2; kk++) acc += Tm[swz64(32 + r2, 32 + kk)] * P2[kk * 32 + cc];
+        Tm[swz64(32 + r2, cc)] = -acc;
+    }
+    named_bar(kBarPrep, kPrepThreads);
+    // M = T diag(beta), unit lower triangular T
+    {
+        const int r = pt >> 2, qq = pt & 3;
+        uint8_t *Mt = sm.base + s * kStageBytes + kOffM;
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int j0 = 16 * qq + 8 * u + 2 * e;
+                float x0 = (j0 < r) ? Tm[swz64(r, j0)] : (j0 == r ? 1.f : 0.f);
+                float x1 = (j0 + 1 < r) ? Tm[swz64(r, j0 + 1)] : (j0 + 1 == r ? 1.f : 0.f);
+                w[e] = pack_f16x2(x0 * cst[256 + j0], x1 * cst[256 + j0 + 1]);
+            }
+            *reinterpret_cast<uint4 *>(Mt + sw128_chunk(r, 2 * qq + u)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    fence_proxy_async_smem();
+    named_bar(kBarPrep, kPrepThreads);
+}
+
+// -W'^T (TMEM, lane = key channel c, column = row r) -> fp16 MN-major [c][r]
+__device__ void prep_read_w(const Smem &sm, int s, uint32_t tmem, int pt)
+{
+    const int pw = pt >> 5, lane = pt & 31;
+    const int sp = pw & 3, ch = pw >> 2;
+    const int c = 32 * sp + lane;
+    uint32_t a[32];
+    tmem_ld32(tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * sp) << 16) + 32 * ch, a);
+    tmem_wait_ld();
+    uint8_t *Wt = sm.base + s * kStageBytes + kOffW;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++)
+            w[e] = pack_f16x2(-__uint_as_float(a[8 * q + 2 * e]), -__uint_as_float(a[8 * q + 2 * e + 1]));
+        *reinterpret_cast<uint4 *>(Wt + sw128_chunk(c, 4 * ch + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    named_bar(kBarPrep, kPrepThreads);
+}
+
+__device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
+{
+    const uint32_t st = sm.u32(s * kStageBytes);
+    const uint32_t id = idesc_f16(128, 64, 0, 0);
+#pragma unroll
+    for (int ks = 0; ks < 8; ks++) {
+        const int kb = ks >> 2, kin = ks & 3;
+        const uint64_t ad = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(st + kOffKM + kb * 8192 + kin * 32, 16, 1024);
+        mma_ss(tmem + kTmP + 128 * s + 64, ad, bd, id, ks > 0);
+    }
+}
+
+__device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
+{
+    const uint32_t st = sm.u32(s * kStageBytes);
+    const uint32_t id = idesc_f16(128, 64, 1, 0);
+#pragma unroll
+    for (int ks = 0; ks < 4; ks++) {
+        const uint64_t bd = smem_desc_sw128(st + kOffM + ks * 32, 16, 1024);
+        const uint64_t aw = smem_desc_sw128(st + kOffKQ + ks * 2048, 16384, 1024);   // Kp^T, MN-major
+        const uint64_t au = smem_desc_sw128(st + kOffV + ks * 2048, 8192, 1024);     // V^T, MN-major
+        mma_ss(tmem + kTmP + 128 * s + 64, aw, bd, id, ks > 0);
+        mma_ss(tmem + kTmP + 128 * s, au, bd, id, ks > 0);
+    }
+}
+
+__device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, int U)
+{
+    const int pt = threadIdx.x - kChainThreads;
+    const uint32_t tmem = *sm.tmem_base();
+    int item = 0;
+    for (int k = 0;; k++) {
+        const int u = cta_unit(k, U);
+        if (u < 0) break;
+        const Unit un = get_unit(p, order, u);
+        for (int c = 0; c < un.nchunks; c++, item++) {
+            const int s = item & 1;
+            const int row0 = un.bos + c * kChunk;
+            const int L = min(kChunk, un.eos - row0);
+            bool ok = mbar_wait(sm.bar(kBarRawFull + s), (item >> 1) & 1, sm.abort_flag());
+            if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            prep_elementwise(p, sm, s, un, row0, L, pt);
+            if (pt == 0) {
+                tc_fence_after();
+                issue_mma_a(sm, s, tmem);
+                mma_commit(sm.bar(kBarAFull));
+            }
+            ok = mbar_wait(sm.bar(kBarAFull), item & 1, sm.abort_flag());
+            if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            tc_fence_after();
+            prep_read_a(sm, s, tmem, pt);
+            prep_inverse(sm, s, pt);
+            if (pt == 0) {
+                tc_fence_after();
+                issue_mma_b(sm, s, tmem);
+                mma_commit(sm.bar(kBarWFull));
+            }
+            ok = mbar_wait(sm.bar(kBarWFull), item & 1, sm.abort_flag());
+            if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            tc_fence_after();
+            prep_read_w(sm, s, tmem, pt);
+            if (pt == 0) mbar_arrive(sm.bar(kBarPrepDone + s));
+        }
+    }
+}
+
+// =============================================================================
+// chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
+// =============================================================================
+struct PendingOut {
+    int valid, s, row0, L, h;
+};
+
+__device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, const PendingOut &po, int v)
+{
+    const int w = v >> 5;
+    __nv_bfloat16 *dst = p.out + ((size_t)po.row0 * p.H + po.h) * kD + v;
+    const size_t row_stride = (size_t)p.H * kD;
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+        uint32_t o[32];
+        tmem_ld32(tmem + kTmP + 128 * po.s + 64 + ((uint32_t)(32 * w) << 16) + 32 * half, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            const int r = 32 * half + j;
+            if (r < po.L) dst[(size_t)r * row_stride] = __float2bfloat16_rn(__uint_as_float(o[j]));
+        }
+    }
+    tc_fence_before();
+    named_bar(kBarChain, kChainThreads);
+    if (v == 0) mbar_arrive(sm.bar(kBarStageFree + po.s));
+}
+
+__device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, int U)
+{
+    const int v = threadIdx.x;
+    const int w = v >> 5;
+    const uint32_t tmem = *sm.tmem_base();
+    const uint32_t lane_off = (uint32_t)(32 * w) << 16;
+    int item = 0;
+    PendingOut po = {0, 0, 0, 0, 0};
+    for (int k = 0;; k++) {
+        const int u = cta_unit(k, U);
+        if (u < 0) break;
+        const Unit un = get_unit(p, order, u);
+        const size_t soff = (((size_t)un.n * p.H + un.h) * kD + v) * kD;
+        if (un.nchunks == 0) {
+            if (p.s1) {
+                for (int c = 0; c < kD; c += 4) {
+                    float4 x = p.s0 ? *reinterpret_cast<const float4 *>(p.s0 + soff + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    *reinterpret_cast<float4 *>(p.s1 + soff + c) = x;
+                }
+            }
+            continue;
+        }
+        // initial state -> S (TMEM, lane v, columns = key channels)
+#pragma unroll
+        for (int cb = 0; cb < 4; cb++) {
+            uint32_t x[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                float4 f = p.s0 ? *reinterpret_cast<const float4 *>(p.s0 + soff + 32 * cb + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x[j] = __float_as_uint(f.x); x[j + 1] = __float_as_uint(f.y);
+                x[j + 2] = __float_as_uint(f.z); x[j + 3] = __float_as_uint(f.w);
+            }
+            tmem_st32(tmem + kTmS + lane_off + 32 * cb, x);
+        }
+        tmem_wait_st();
+        int prev_s = -1;
+        for (int c = 0; c < un.nchunks; c++, item++) {
+            const int s = item & 1;
+            const int row0 = un.bos + c * kChunk;
+            const int L = min(kChunk, un.eos - row0);
+            bool ok = mbar_wait(sm.bar(kBarPrepDone + s), (item >> 1) & 1, sm.abort_flag());
+            if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            tc_fence_after();
+            // S <- (S * pend_prev) * fm ; S'h = fp16(S)
+            const float *fm = sm.ptr<float>(kOffConst + s * kConstBytes);
+            const float *pend = prev_s >= 0 ? sm.ptr<float>(kOffConst + prev_s * kConstBytes + 512) : nullptr;
+#pragma unroll
+            for (int cb = 0; cb < 4; cb++) {
+                uint32_t x[32];
+                tmem_ld32(tmem + kTmS + lane_off + 32 * cb, x);
+                tmem_wait_ld();
+                uint32_t hpk[16];
+#pragma unroll
+                for (int j = 0; j < 32; j++) {
+                    float f = __uint_as_float(x[j]);
+                    if (pend) f = __fmul_rn(f, pend[32 * cb + j]);
+                    f = __fmul_rn(f, fm[32 * cb + j]);
+                    x[j] = __float_as_uint(f);
+                }
+#pragma unroll
+                for (int j = 0; j < 16; j++) hpk[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                tmem_st32(tmem + kTmS + lane_off + 32 * cb, x);
+                tmem_st16(tmem + kTmS0h + lane_off + 16 * cb, hpk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar(kBarChain, kChainThreads);
+            if (v == 0) {
+                tc_fence_after();
+                const uint32_t st = sm.u32(s * kStageBytes);
+                const uint32_t id_w = idesc_f16(128, 64, 0, 1), id_q = idesc_f16(128, 64, 0, 0);
+#pragma unroll
+                for (int ks = 0; ks < 8; ks++) {
+                    const uint64_t bw = smem_desc_sw128(st + kOffW + ks * 2048, 16, 1024);
+                    const int kb = ks >> 2, kin = ks & 3;
+                    const uint64_t bq = smem_desc_sw128(st + kOffKQ + kb * 16384 + 8192 + kin * 32, 16, 1024);
+                    mma_ts(tmem + kTmP + 128 * s, tmem + kTmS0h + 8 * ks, bw, id_w, 1);
+                    mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmS0h + 8 * ks, bq, id_q, ks > 0);
+                }
+                mma_commit(sm.bar(kBarMma1));
+            }
+            // the previous chunk's output while MMA1 runs
+            if (po.valid) chain_store_out(p, sm, tmem, po, v);
+            ok = mbar_wait(sm.bar(kBarMma1), item & 1, sm.abort_flag());
+            if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            tc_fence_after();
+            // Delta^T (fp32, TMEM) -> fp16 A operand
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                uint32_t x[32];
+                tmem_ld32(tmem + kTmP + 128 * s + lane_off + 32 * half, x);
+                tmem_wait_ld();
+                uint32_t hpk[16];
+#pragma unroll
+                for (int j = 0; j < 16; j++) hpk[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                tmem_st16(tmem + kTmDh + lane_off + 16 * half, hpk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar(kBarChain, kChainThreads);
+            if (v == 0) {
+                tc_fence_after();
+                const uint32_t st = sm.u32(s * kStageBytes);
+                const uint32_t id_s = idesc_f16(128, 128, 0, 1), id_o = idesc_f16(128, 64, 0, 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ks++) {
+                    const uint64_t bk = smem_desc_sw128(st + kOffKM + ks * 2048, 8192, 1024);   // Km, MN-major
+                    const uint64_t bb = smem_desc_sw128(st + kOffB + ks * 32, 16, 1024);
+                    mma_ts(tmem + kTmS, tmem + kTmDh + 8 * ks, bk, id_s, 1);
+                    mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmDh + 8 * ks, bb, id_o, 1);
+                }
+                mma_commit(sm.bar(kBarMma3));
+                mma_commit(sm.bar(kBarStageFree + s));
+            }
+            ok = mbar_wait(sm.bar(kBarMma3), item & 1, sm.abort_flag());
+            if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            tc_fence_after();
+            po = {1, s, row0, L, un.h};
+            prev_s = s;
+        }
+        // unit end: final state = S * pend_last, then the last chunk's output
+        if (p.s1) {
+            const float *pend = sm.ptr<float>(kOffConst + prev_s * kConstBytes + 512);
+#pragma unroll
+            for (int cb = 0; cb < 4; cb++) {
+                uint32_t x[32];
+                tmem_ld32(tmem + kTmS + lane_off + 32 * cb, x);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float4 f = make_float4(__fmul_rn(__uint_as_float(x[j]), pend[32 * cb + j]),
+                                           __fmul_rn(__uint_as_float(x[j + 1]), pend[32 * cb + j + 1]),
+                                           __fmul_rn(__uint_as_float(x[j + 2]), pend[32 * cb + j + 2]),
+                                           __fmul_rn(__uint_as_float(x[j + 3]), pend[32 * cb + j + 3]));
+                    *reinterpret_cast<float4 *>(p.s1 + soff + 32 * cb + j) = f;
+                }
+            }
+        }
+        chain_store_out(p, sm, tmem, po, v);
+        po.valid = 0;
+    }
+}
+
+// =============================================================================
+// load role: warp 12, one elected lane
+// =============================================================================
+__device__ void load_role(const TcParams &p, const Smem &sm, const int *order, int U, const CUtensorMap *tq,
+                          const CUtensorMap *tk, const CUtensorMap *tv, const CUtensorMap *tg)
+{
+    int item = 0;
+    bool failed = false;
+    for (int k = 0; !failed; k++) {
+        const int u = cta_unit(k, U);
+        if (u < 0) break;
+        const Unit un = get_unit(p, order, u);
+        for (int c = 0; c < un.nchunks; c++, item++) {
+            const int s = item & 1;
+            if (item >= 2 && !mbar_wait(sm.bar(kBarStageFree + s), ((item >> 1) - 1) & 1, sm.abort_flag())) {
+                record_error(p, sm, kErrWaitTimeout);
+                failed = true;
+                break;
+            }
+            const int row0 = un.bos + c * kChunk;
+            const uint32_t st = sm.u32(s * kStageBytes);
+            const uint32_t bar = sm.bar(kBarRawFull + s);
+            mbar_arrive_expect_tx(bar, kRawBytes);
+            for (int kb = 0; kb < 2; kb++) {
+                tma_load_3d(st + kOffKQ + kb * 16384, tk, 64 * kb, un.h, row0, bar);
+                tma_load_3d(st + kOffKQ + kb * 16384 + 8192, tq, 64 * kb, un.h, row0, bar);
+                tma_load_3d(st + kOffV + kb * 8192, tv, 64 * kb, un.h, row0, bar);
+            }
+            for (int cb = 0; cb < 4; cb++) tma_load_3d(st + kOffGX + cb * 8192, tg, 32 * cb, un.h, row0, bar);
+        }
+    }
+    // let the copies still in flight land before the CTA can exit
+    for (int back = 1; back <= 2; back++) {
+        const int it = item - back;
+        if (it < 0) break;
+        mbar_wait(sm.bar(kBarRawFull + (it & 1)), (it >> 1) & 1, sm.abort_flag(), 1u << 14);
+    }
+}
+
+// =============================================================================
+__global__ void __launch_bounds__(kThreads, 1)
+kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem sm;
+    sm.base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int U = p.N * p.H;
+    int *order = sm.ptr<int>(kOffOrder);
+
+    // schedule: sequences sorted by length, longest first (ties: lower index)
+    if (p.sorted) {
+        int *lens = sm.ptr<int>(kOffL);
+        for (int n = tid; n < p.N; n += kThreads) {
+            int b = min(max(p.cu[n], 0), p.T), e = min(max(p.cu[n + 1], 0), p.T);
+            if (p.cu[n] < 0 || p.cu[n] > p.T || p.cu[n + 1] < 0 || p.cu[n + 1] > p.T) atomicOr(p.err, kErrBadSeqlens);
+            lens[n] = max(e - b, 0);
+        }
+        __syncthreads();
+        for (int n = tid; n < p.N; n += kThreads) {
+            int rank = 0;
+            const int ln = lens[n];
+            for (int m2 = 0; m2 < p.N; m2++) {
+                const int lm = lens[m2];
+                rank += (lm > ln) || (lm == ln && m2 < n);
+            }
+            order[rank] = n;
+        }
+    }
+    if (tid == 0) {
+        *sm.abort_flag() = 0;
+        for (int i = 0; i < 2; i++) {
+            mbar_init(sm.bar(kBarRawFull + i), 1);
+            mbar_init(sm.bar(kBarStageFree + i), 2);
+            mbar_init(sm.bar(kBarPrepDone + i), 1);
+        }
+        mbar_init(sm.bar(kBarAFull), 1);
+        mbar_init(sm.bar(kBarWFull), 1);
+        mbar_init(sm.bar(kBarMma1), 1);
+        mbar_init(sm.bar(kBarMma3), 1);
+        mbar_init(sm.bar(kBarDrain), 2);
+        mbar_fence_init();
+    }
+    if (warp == 12) {
+        tmem_alloc(sm.u32(kOffMisc), kTmCols);
+        tmem_relinquish();
+        if ((tid & 31) == 0) {
+            tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tg);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (warp < 4) {
+        chain_role(p, sm, order, U);
+        if (tid == 0) {
+            mma_commit(sm.bar(kBarDrain));
+            mbar_wait(sm.bar(kBarDrain), 0, sm.abort_flag(), 1u << 14);
+        }
+    } else if (warp < 12) {
+        prep_role(p, sm, order, U);
+        if (tid == kChainThreads) {
+            mma_commit(sm.bar(kBarDrain));
+            mbar_wait(sm.bar(kBarDrain), 0, sm.abort_flag(), 1u << 14);
+        }
+    } else if ((tid & 31) == 0) {
+        load_role(p, sm, order, U, &tq, &tk, &tv, &tg);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 12) tmem_dealloc(*sm.tmem_base(), kTmCols);
+}
+
+// ---- host side ------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem, int T, int H, int box_inner)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * elem, (cuuint64_t)H * kD * elem};
+    cuuint32_t box[3] = {(cuuint32_t)box_inner, 1, (cuuint32_t)kChunk};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
+{
+    CUtensorMap tq, tk, tv, tg;
+    memset(&tq, 0, sizeof tq); memset(&tk, 0, sizeof tk); memset(&tv, 0, sizeof tv); memset(&tg, 0, sizeof tg);
+    if (a.T > 0) {
+        if (!make_map(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
+            !make_map(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
+            !make_map(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
+            !make_map(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32))
+            return cudaErrorInvalidValue;
+    }
+    static int attr_set[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kda_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = 1;
+    }
+    TcParams p;
+    p.cu = a.cu_seqlens;
+    p.beta = a.beta;
+    p.s0 = a.initial_state;
+    p.out = (__nv_bfloat16 *)a.out;
+    p.s1 = a.final_state;
+    p.N = a.N;
+    p.T = a.T;
+    p.H = a.H;
+    p.sorted = a.N <= kMaxSortedSeqs ? 1 : 0;
+    p.err = a.err_word;
+    const int units = a.N * a.H;
+    const int grid = units < a.num_sms ? units : a.num_sms;
+    kda_tc_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tg, p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
