@@ -3,10 +3,14 @@
 Tolerances (relative L2 over the whole tensor): 2e-3 on outputs, 1e-3 on
 final states.  bf16 outputs alone carry about 1.66e-3 of round-to-nearest
 error against the fp64 result; the kernel's own error (fp16 MMA operands,
-fp32 accumulation) must fit in the rest.  The small cases are also checked
-element by element: |gpu - ref| <= 2^-8 |ref| + 1e-2 rms(ref) for bf16 outputs
-(half an ulp of bf16 plus a bound on the kernel's own error) and
-<= 5e-3 rms(ref) for fp32 outputs and states.
+fp32 accumulation) must fit in the rest.
+
+The small cases are also checked element by element, to catch localised
+corruption (a wrong row, head or index is off by about 100% of the tensor's
+RMS) rather than to restate the L2 contract: |gpu - ref| <= 2^-8 |ref| +
+0.05 rms(ref) for bf16 outputs (half an ulp of bf16, plus 5% of the RMS for
+the kernel's worst-case operand roundings, where a sum of fp16-rounded terms
+partly cancels) and <= 0.05 rms(ref) for fp32 outputs and states.
 """
 import numpy as np
 import pytest
@@ -20,7 +24,7 @@ pytestmark = pytest.mark.gpu
 
 def check_elementwise(gpu, ref, bf16):
     rms = float(np.sqrt(np.mean(ref * ref)))
-    bound = (2.0 ** -8) * np.abs(ref) + 1e-2 * rms if bf16 else 5e-3 * rms
+    bound = (2.0 ** -8) * np.abs(ref) + 0.05 * rms if bf16 else 0.05 * rms
     bad = np.abs(gpu - ref) > bound
     assert not bad.any(), f"{int(bad.sum())} elements out of bound; worst {np.max(np.abs(gpu - ref)):.3e}"
 
