@@ -52,7 +52,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Bounded wait: gives up after `limit` polls (each poll may suspend the
-// thread for up to ~20 us) or as soon as *abort is set by another thread.
+// thread for up to ~20 us) or once *abort, set by another thread, is seen
+// (checked every 64 polls, so idle waiters cost few issue slots).
 // Returns false when it gave up; the caller then records an error and winds
 // the kernel down.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
@@ -60,7 +61,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 {
     for (uint32_t it = 0; it < limit; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
+        if ((it & 63) == 63 && *abort) return false;
     }
     return false;
 }

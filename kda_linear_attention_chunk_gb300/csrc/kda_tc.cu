@@ -47,6 +47,19 @@ namespace {
 
 using namespace sm100;
 
+// Optional phase timestamps of CTA 0 (compiled in only with -DKDA_TRACE).
+#ifdef KDA_TRACE
+__device__ unsigned long long g_kda_trace[3][128][8];
+#define KDA_PHASE(role, item, point)                                                  \
+    do {                                                                              \
+        if (blockIdx.x == 0 && (item) < 128) g_kda_trace[role][item][point] = clock64(); \
+    } while (0)
+#else
+#define KDA_PHASE(role, item, point) \
+    do {                             \
+    } while (0)
+#endif
+
 constexpr int kD = 128;
 constexpr int kThreads = 416;
 constexpr int kChainThreads = 128;
@@ -352,19 +365,28 @@ __device__ void prep_inverse(const Smem &sm, int s, int pt)
                 if (a > a2) x[col] -= Lr[a2] * xs;
             }
         }
+        // the row within its 32-wide block: the diagonal 16x16 inverse, and
+        // zeros in the 16 columns beside it (the strictly upper block is
+        // zero; the lower one is overwritten by the merge below)
+        const int other = 16 * (blk ^ 1);
 #pragma unroll
-        for (int t = 0; t < 16; t++)
-            if (t <= a) Tm[swz64(i, 16 * blk + t)] = x[t];
+        for (int t = 0; t < 16; t++) {
+            Tm[swz64(i, 16 * blk + t)] = x[t];
+            Tm[swz64(i, other + t)] = 0.f;
+        }
     }
     named_bar(kBarPrep, kPrepThreads);
-    // level 1: T10 = -X1 (L10 X0), T32 = -X3 (L32 X2)
+    // level 1: T10 = -X1 (L10 X0), T32 = -X3 (L32 X2).  Loops run over the
+    // full block with zeros above the diagonal, so all lanes read one row of
+    // T per step (no bank conflicts) and the loads can be hoisted.
 #pragma unroll
     for (int e = 0; e < 2; e++) {
         const int idx = pt + 256 * e;
         const int bl = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
         const int r0 = 32 * bl + 16, c0 = 32 * bl;
         float acc = 0.f;
-        for (int kk = cc; kk < 16; kk++) acc += Lm[swz64(r0 + rr, c0 + kk)] * Tm[swz64(c0 + kk, c0 + cc)];
+#pragma unroll
+        for (int kk = 0; kk < 16; kk++) acc += Lm[swz64(r0 + rr, c0 + kk)] * Tm[swz64(c0 + kk, c0 + cc)];
         P1[idx] = acc;
     }
     named_bar(kBarPrep, kPrepThreads);
@@ -374,7 +396,8 @@ __device__ void prep_inverse(const Smem &sm, int s, int pt)
         const int bl = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
         const int r0 = 32 * bl + 16, c0 = 32 * bl;
         float acc = 0.f;
-        for (int kk = 0; kk <= rr; kk++) acc += Tm[swz64(r0 + rr, r0 + kk)] * P1[bl * 256 + kk * 16 + cc];
+#pragma unroll
+        for (int kk = 0; kk < 16; kk++) acc += Tm[swz64(r0 + rr, r0 + kk)] * P1[bl * 256 + kk * 16 + cc];
         Tm[swz64(r0 + rr, c0 + cc)] = -acc;
     }
     named_bar(kBarPrep, kPrepThreads);
@@ -384,7 +407,8 @@ __device__ void prep_inverse(const Smem &sm, int s, int pt)
         const int idx = pt + 256 * e;
         const int r2 = idx >> 5, cc = idx & 31;
         float acc = 0.f;
-        for (int kk = cc; kk < 32; kk++) acc += Lm[swz64(32 + r2, kk)] * Tm[swz64(kk, cc)];
+#pragma unroll
+        for (int kk = 0; kk < 32; kk++) acc += Lm[swz64(32 + r2, kk)] * Tm[swz64(kk, cc)];
         P2[idx] = acc;
     }
     named_bar(kBarPrep, kPrepThreads);
@@ -393,7 +417,8 @@ __device__ void prep_inverse(const Smem &sm, int s, int pt)
         const int idx = pt + 256 * e;
         const int r2 = idx >> 5, cc = idx & 31;
         float acc = 0.f;
-        for (int kk = 0; kk <= r2; kk++) acc += Tm[swz64(32 + r2, 32 + kk)] * P2[kk * 32 + cc];
+#pragma unroll
+        for (int kk = 0; kk < 32; kk++) acc += Tm[swz64(32 + r2, 32 + kk)] * P2[kk * 32 + cc];
         Tm[swz64(32 + r2, cc)] = -acc;
     }
     named_bar(kBarPrep, kPrepThreads);
@@ -483,7 +508,9 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
             const int L = min(kChunk, un.eos - row0);
             bool ok = mbar_wait(sm.bar(kBarRawFull + s), (item >> 1) & 1, sm.abort_flag());
             if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (pt == 0) KDA_PHASE(0, item, 0);
             prep_elementwise(p, sm, s, un, row0, L, pt);
+            if (pt == 0) KDA_PHASE(0, item, 1);
             if (pt == 0) {
                 tc_fence_after();
                 issue_mma_a(sm, s, tmem);
@@ -491,9 +518,12 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
             }
             ok = mbar_wait(sm.bar(kBarAFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (pt == 0) KDA_PHASE(0, item, 2);
             tc_fence_after();
             prep_read_a(sm, s, tmem, pt);
+            if (pt == 0) KDA_PHASE(0, item, 3);
             prep_inverse(sm, s, pt);
+            if (pt == 0) KDA_PHASE(0, item, 4);
             if (pt == 0) {
                 tc_fence_after();
                 issue_mma_b(sm, s, tmem);
@@ -501,8 +531,10 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
             }
             ok = mbar_wait(sm.bar(kBarWFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (pt == 0) KDA_PHASE(0, item, 5);
             tc_fence_after();
             prep_read_w(sm, s, tmem, pt);
+            if (pt == 0) KDA_PHASE(0, item, 6);
             if (pt == 0) mbar_arrive(sm.bar(kBarPrepDone + s));
         }
     }
@@ -578,6 +610,7 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
             const int L = min(kChunk, un.eos - row0);
             bool ok = mbar_wait(sm.bar(kBarPrepDone + s), (item >> 1) & 1, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (v == 0) KDA_PHASE(1, item, 0);
             tc_fence_after();
             // S <- (S * pend_prev) * fm ; S'h = fp16(S)
             const float *fm = sm.ptr<float>(kOffConst + s * kConstBytes);
@@ -589,11 +622,17 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
                 tmem_wait_ld();
                 uint32_t hpk[16];
 #pragma unroll
-                for (int j = 0; j < 32; j++) {
-                    float f = __uint_as_float(x[j]);
-                    if (pend) f = __fmul_rn(f, pend[32 * cb + j]);
-                    f = __fmul_rn(f, fm[32 * cb + j]);
-                    x[j] = __float_as_uint(f);
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 f4 = *reinterpret_cast<const float4 *>(fm + 32 * cb + j);
+                    const float4 p4 = pend ? *reinterpret_cast<const float4 *>(pend + 32 * cb + j)
+                                           : make_float4(1.f, 1.f, 1.f, 1.f);
+                    const float fv[4] = {f4.x, f4.y, f4.z, f4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        float f = __uint_as_float(x[j + e]);
+                        if (pend) f = __fmul_rn(f, pv[e]);
+                        x[j + e] = __float_as_uint(__fmul_rn(f, fv[e]));
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < 16; j++) hpk[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
@@ -616,11 +655,14 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
                     mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmS0h + 8 * ks, bq, id_q, ks > 0);
                 }
                 mma_commit(sm.bar(kBarMma1));
+                KDA_PHASE(1, item, 1);
             }
             // the previous chunk's output while MMA1 runs
             if (po.valid) chain_store_out(p, sm, tmem, po, v);
+            if (v == 0) KDA_PHASE(1, item, 2);
             ok = mbar_wait(sm.bar(kBarMma1), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (v == 0) KDA_PHASE(1, item, 3);
             tc_fence_after();
             // Delta^T (fp32, TMEM) -> fp16 A operand
 #pragma unroll
@@ -649,9 +691,11 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
                 }
                 mma_commit(sm.bar(kBarMma3));
                 mma_commit(sm.bar(kBarStageFree + s));
+                KDA_PHASE(1, item, 4);
             }
             ok = mbar_wait(sm.bar(kBarMma3), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (v == 0) KDA_PHASE(1, item, 5);
             tc_fence_after();
             po = {1, s, row0, L, un.h};
             prev_s = s;
@@ -698,6 +742,7 @@ __device__ void load_role(const TcParams &p, const Smem &sm, const int *order, i
                 failed = true;
                 break;
             }
+            KDA_PHASE(2, item, 0);
             const int row0 = un.bos + c * kChunk;
             const uint32_t st = sm.u32(s * kStageBytes);
             const uint32_t bar = sm.bar(kBarRawFull + s);
