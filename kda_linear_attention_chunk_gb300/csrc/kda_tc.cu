@@ -161,8 +161,11 @@ __device__ __forceinline__ int cta_unit(int k, int U)
     return u < U ? u : -1;
 }
 
-// swizzled index into a 64x64 fp32 matrix (conflict-free row and column access)
-__device__ __forceinline__ int swz64(int i, int j) { return i * 64 + (j ^ (i & 31)); }
+// rotated index into a 64x64 fp32 matrix: row i starts 4*i words further
+// round the row, so an 8-row x 4-column block (a tf32 mma A fragment) or a
+// quarter-warp reading 8 rows x 16 bytes touches distinct banks; groups of
+// 4 consecutive columns stay contiguous and 16-byte aligned.
+__device__ __forceinline__ int rot64(int i, int j) { return i * 64 + ((j + 4 * i) & 63); }
 
 // byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
@@ -173,132 +176,146 @@ __device__ __forceinline__ void record_error(const TcParams &p, const Smem &sm, 
     *sm.abort_flag() = 1;
 }
 
+// ---- small fp32-accurate products on the warp MMA (3 x tf32 split) ---------------
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// d += A[16x8] * B[8x8] with A = hi + lo and B = hi + lo split into tf32 parts
+// (the lo*lo term is dropped): about fp32 accuracy.
+__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], const float (&b)[2])
+{
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        ah[i] = to_tf32(a[i]);
+        al[i] = to_tf32(a[i] - __uint_as_float(ah[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        bh[i] = to_tf32(b[i]);
+        bl[i] = to_tf32(b[i] - __uint_as_float(bh[i]));
+    }
+    mma_tf32(d, al, bh);
+    mma_tf32(d, ah, bl);
+    mma_tf32(d, ah, bh);
+}
+
 // =============================================================================
 // prep role: warps 4-11
 // =============================================================================
 __device__ void prep_elementwise(const TcParams &p, const Smem &sm, int s, const Unit &un, int row0, int L,
                                  int pt)
 {
+    const uint32_t st = s * kStageBytes;
+    float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
+    float *gmx = sm.ptr<float>(kOffGm);
+    const int m = (L - 1) >> 1;
+
+    if (pt < 128) {
+        // one thread per key channel walks the rows: G = inclusive prefix of g,
+        // written back in place (fp32, same swizzled layout)
+        const int c = pt, cb = c >> 5, cc = c & 31;
+        uint8_t *gb = sm.base + st + kOffGX + cb * 8192 + 4 * (cc & 3);
+        float acc = 0.f, gm = 0.f;
+#pragma unroll
+        for (int r0 = 0; r0 < kChunk; r0 += 16) {
+            float x[16];
+#pragma unroll
+            for (int t = 0; t < 16; t++) x[t] = *reinterpret_cast<const float *>(gb + sw128_chunk(r0 + t, cc >> 2));
+#pragma unroll
+            for (int t = 0; t < 16; t++) {
+                const int r = r0 + t;
+                if (r < L) acc += x[t];
+                if (r == m) gm = acc;
+                *reinterpret_cast<float *>(gb + sw128_chunk(r, cc >> 2)) = acc;
+            }
+        }
+        gmx[c] = gm;
+        cst[c] = __expf(gm);                 // fm: the state seen from row m
+        cst[128 + c] = __expf(acc - gm);     // pend: decay from row m to the last row
+    } else {
+        // value tile bf16 -> fp16 in place (rows past the chunk zeroed), betas
+        const int q = pt - 128;
+        uint8_t *vt = sm.base + st + kOffV;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int idx = q + 128 * i;           // 16-byte chunk index in the 16 KB tile
+            const int r = (idx >> 3) & 63;
+            uint4 *ptr = reinterpret_cast<uint4 *>(vt + idx * 16);
+            uint4 w = *ptr;
+            const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) o[e] = r < L ? pack_f16x2(bf16lo(in[e]), bf16hi(in[e])) : 0u;
+            *ptr = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (q < kChunk) cst[256 + q] = q < L ? __ldg(p.beta + (size_t)(row0 + q) * p.H + un.h) : 0.f;
+    }
+    named_bar(kBarPrep, kPrepThreads);
+
+    // decay-scaled fp16 operands, in place over the bf16 tiles: row r, channels
+    // 32*cg .. 32*cg+31
     const int pw = pt >> 5, lane = pt & 31;
     const int rr = lane & 7, cg = lane >> 3;
     const int r = pw * 8 + rr;
-    const uint32_t st = s * kStageBytes;
-    float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
-    float *xchg = sm.ptr<float>(kOffL);            // [8 warps][128 channels]
-    float *gmx = sm.ptr<float>(kOffGm);
-    float *glx = gmx + 128;
-
-    float beta_r = 0.f;
-    if (cg == 0 && r < L) beta_r = __ldg(p.beta + (size_t)(row0 + r) * p.H + un.h);
-
-    // g -> inclusive prefix over rows, per channel
-    float G[32];
-    {
-        const uint8_t *gb = sm.base + st + kOffGX + cg * 8192;
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            float4 x = *reinterpret_cast<const float4 *>(gb + sw128_chunk(r, j));
-            G[4 * j + 0] = x.x; G[4 * j + 1] = x.y; G[4 * j + 2] = x.z; G[4 * j + 3] = x.w;
-        }
-        if (r >= L) {
-#pragma unroll
-            for (int j = 0; j < 32; j++) G[j] = 0.f;
-        }
-    }
-#pragma unroll
-    for (int d = 1; d < 8; d <<= 1) {
-#pragma unroll
-        for (int j = 0; j < 32; j++) {
-            float y = __shfl_up_sync(0xffffffffu, G[j], d, 8);
-            if (rr >= d) G[j] += y;
-        }
-    }
-    if (rr == 7) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4 *>(xchg + pw * 128 + 32 * cg + j) = make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
-    }
-    named_bar(kBarPrep, kPrepThreads);
-    for (int w = 0; w < pw; w++) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            float4 x = *reinterpret_cast<const float4 *>(xchg + w * 128 + 32 * cg + j);
-            G[j] += x.x; G[j + 1] += x.y; G[j + 2] += x.z; G[j + 3] += x.w;
-        }
-    }
-    const int m = (L - 1) >> 1;
-    if (r == m) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4 *>(gmx + 32 * cg + j) = make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
-    }
-    if (r == L - 1) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4 *>(glx + 32 * cg + j) = make_float4(G[j], G[j + 1], G[j + 2], G[j + 3]);
-    }
-    if (cg == 0) cst[256 + r] = beta_r;
-    named_bar(kBarPrep, kPrepThreads);
-
-    float gm[32];
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-        float4 x = *reinterpret_cast<const float4 *>(gmx + 32 * cg + j);
-        gm[j] = x.x; gm[j + 1] = x.y; gm[j + 2] = x.z; gm[j + 3] = x.w;
-    }
-    if (r == 0) {
-        // chain constants: fm = exp(G_m) (view from row m), pend = exp(G_last - G_m)
-#pragma unroll
-        for (int j = 0; j < 32; j++) {
-            cst[32 * cg + j] = __expf(gm[j]);
-            cst[128 + 32 * cg + j] = __expf(glx[32 * cg + j] - gm[j]);
-        }
-    }
-
-    // decay-scaled fp16 operands, in place over the bf16 tiles
+    const bool valid = r < L;
     const int kb = cg >> 1;
     uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
     uint8_t *qt = kt + 8192;
     uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
-    uint8_t *vt = sm.base + st + kOffV + kb * 8192;
-    const bool valid = r < L;
+    const uint8_t *gt = sm.base + st + kOffGX + cg * 8192;
 #pragma unroll
     for (int j = 0; j < 4; j++) {
+        // 8 channels: 32*cg + 8*j + e
+        const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
+        const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
+        const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
+        const float4 m1 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j + 4);
+        const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
         const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
-        uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
-        uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
-        uint4 vq = *reinterpret_cast<const uint4 *>(vt + off);
+        const uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
+        const uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
         const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
         const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
-        const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
-        uint32_t okp[4], okm[4], oqp[4], ov[4];
+        uint32_t okp[4], okm[4], oqp[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-            const int g0 = 8 * j + 2 * e;
             float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
             if (valid) {
-                a0 = __expf(G[g0] - gm[g0]);
-                a1 = __expf(G[g0 + 1] - gm[g0 + 1]);
-                b0 = __expf(gm[g0] - G[g0]);
-                b1 = __expf(gm[g0 + 1] - G[g0 + 1]);
+                a0 = __expf(G[2 * e] - M[2 * e]);
+                a1 = __expf(G[2 * e + 1] - M[2 * e + 1]);
+                b0 = __expf(M[2 * e] - G[2 * e]);
+                b1 = __expf(M[2 * e + 1] - G[2 * e + 1]);
             }
             const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
             const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
             okp[e] = pack_f16x2(k0 * a0, k1 * a1);
             okm[e] = pack_f16x2(k0 * b0, k1 * b1);
             oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
-            ov[e] = valid ? pack_f16x2(bf16lo(vw[e]), bf16hi(vw[e])) : 0u;
         }
         *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
         *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
         *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
-        *reinterpret_cast<uint4 *>(vt + off) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
     }
     fence_proxy_async_smem();
     named_bar(kBarPrep, kPrepThreads);
 }
 
-// A readout: strictly lower, beta-scaled A_kk -> L (fp32 smem);
+// A readout: strictly lower, beta-scaled A_kk -> L (fp32, rotated layout);
 // lower A_qk (diagonal included) -> B (fp16, K-major [r][i]).
 __device__ void prep_read_a(const Smem &sm, int s, uint32_t tmem, int pt)
 {
@@ -313,9 +330,12 @@ __device__ void prep_read_a(const Smem &sm, int s, uint32_t tmem, int pt)
         float *Lm = sm.ptr<float>(kOffL);
         const float bi = cst[256 + R];
 #pragma unroll
-        for (int jj = 0; jj < 32; jj++) {
-            const int j = 32 * ch + jj;
-            Lm[swz64(R, j)] = (j < R) ? bi * __uint_as_float(a[jj]) : 0.f;
+        for (int q4 = 0; q4 < 8; q4++) {
+            const int j0 = 32 * ch + 4 * q4;
+            float v4[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) v4[e] = (j0 + e < R) ? bi * __uint_as_float(a[4 * q4 + e]) : 0.f;
+            *reinterpret_cast<float4 *>(Lm + rot64(R, j0)) = make_float4(v4[0], v4[1], v4[2], v4[3]);
         }
     } else {
         const int rr = R - 64;
@@ -338,24 +358,41 @@ __device__ void prep_read_a(const Smem &sm, int s, uint32_t tmem, int pt)
     named_bar(kBarPrep, kPrepThreads);
 }
 
+// One m16n8 tile of D = sum_k A[r0 + .][ka + k] * B[kb + k][c0 + .] over k-steps
+// [ks0, ks1) of 8, A and B read from fp32 smem through `la` / `lb` (row, col)
+// index functions; 3 x tf32 on the warp MMA.
+template <typename FA, typename FB>
+__device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, int ks1, int lane)
+{
+    const int g = lane >> 2, t = lane & 3;
+    for (int ks = ks0; ks < ks1; ks++) {
+        const float a[4] = {la(g, 8 * ks + t), la(g + 8, 8 * ks + t), la(g, 8 * ks + t + 4), la(g + 8, 8 * ks + t + 4)};
+        const float b[2] = {lb(8 * ks + t, g), lb(8 * ks + t + 4, g)};
+        mma_3xtf32(d, a, b);
+    }
+}
+
 // (I + L)^-1 by 16x16 diagonal-block forward substitution (warp shuffles)
-// and two levels of block merges; then M = T diag(beta) -> fp16.
+// and two levels of block merges on the warp MMA; then M = T diag(beta) -> fp16.
 __device__ void prep_inverse(const Smem &sm, int s, int pt)
 {
     const float *Lm = sm.ptr<float>(kOffL);
-    float *Tm = sm.ptr<float>(s * kStageBytes + kOffW);   // fp32 64x64, swizzled
-    float *P1 = sm.ptr<float>(kOffP);                     // [2][16][16]
-    float *P2 = P1 + 512;                                 // [32][32]
+    float *Tm = sm.ptr<float>(s * kStageBytes + kOffW);   // fp32 64x64, rotated
+    float *P1 = sm.ptr<float>(kOffP);                     // [2][16][24]
+    float *P2 = P1;                                       // [32][40] (after P1 is dead)
     const float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
+    const int pw = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
 
     if (pt < 64) {
-        const int i = pt, blk = i >> 4, a = i & 15, lane = pt & 31;
+        const int i = pt, blk = i >> 4, a = i & 15;
         float Lr[16], x[16];
 #pragma unroll
-        for (int t = 0; t < 16; t++) {
-            Lr[t] = Lm[swz64(i, 16 * blk + t)];
-            x[t] = (t == a) ? 1.f : 0.f;
+        for (int q = 0; q < 4; q++) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(Lm + rot64(i, 16 * blk + 4 * q));
+            Lr[4 * q] = l4.x; Lr[4 * q + 1] = l4.y; Lr[4 * q + 2] = l4.z; Lr[4 * q + 3] = l4.w;
         }
+#pragma unroll
+        for (int q = 0; q < 16; q++) x[q] = (q == a) ? 1.f : 0.f;
 #pragma unroll
         for (int a2 = 0; a2 < 15; a2++) {
             const int src = (lane & 16) | a2;
@@ -365,75 +402,79 @@ __device__ void prep_inverse(const Smem &sm, int s, int pt)
                 if (a > a2) x[col] -= Lr[a2] * xs;
             }
         }
-        // the row within its 32-wide block: the diagonal 16x16 inverse, and
-        // zeros in the 16 columns beside it (the strictly upper block is
-        // zero; the lower one is overwritten by the merge below)
+        // the diagonal 16x16 inverse, and zeros in the 16 columns beside it
+        // within the 32-wide block (upper: stays zero; lower: merged below)
         const int other = 16 * (blk ^ 1);
 #pragma unroll
-        for (int t = 0; t < 16; t++) {
-            Tm[swz64(i, 16 * blk + t)] = x[t];
-            Tm[swz64(i, other + t)] = 0.f;
+        for (int q = 0; q < 4; q++) {
+            *reinterpret_cast<float4 *>(Tm + rot64(i, 16 * blk + 4 * q)) =
+                make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            *reinterpret_cast<float4 *>(Tm + rot64(i, other + 4 * q)) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
     named_bar(kBarPrep, kPrepThreads);
-    // level 1: T10 = -X1 (L10 X0), T32 = -X3 (L32 X2).  Loops run over the
-    // full block with zeros above the diagonal, so all lanes read one row of
-    // T per step (no bank conflicts) and the loads can be hoisted.
-#pragma unroll
-    for (int e = 0; e < 2; e++) {
-        const int idx = pt + 256 * e;
-        const int bl = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+    // level 1 (warps 0-3 of the role): P = L10 X0, then T10 = -X1 P, for the
+    // two 32-wide diagonal blocks
+    if (pw < 4) {
+        const int bl = pw >> 1, nt = pw & 1;
         const int r0 = 32 * bl + 16, c0 = 32 * bl;
-        float acc = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 16; kk++) acc += Lm[swz64(r0 + rr, c0 + kk)] * Tm[swz64(c0 + kk, c0 + cc)];
-        P1[idx] = acc;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(d, [&](int rr, int kk) { return Lm[rot64(r0 + rr, c0 + kk)]; },
+                 [&](int kk, int cc) { return Tm[rot64(c0 + kk, c0 + 8 * nt + cc)]; }, nt, 2, lane);
+        float *P = P1 + bl * 384;
+        *reinterpret_cast<float2 *>(P + g * 24 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(P + (g + 8) * 24 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
     }
     named_bar(kBarPrep, kPrepThreads);
-#pragma unroll
-    for (int e = 0; e < 2; e++) {
-        const int idx = pt + 256 * e;
-        const int bl = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+    if (pw < 4) {
+        const int bl = pw >> 1, nt = pw & 1;
         const int r0 = 32 * bl + 16, c0 = 32 * bl;
-        float acc = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 16; kk++) acc += Tm[swz64(r0 + rr, r0 + kk)] * P1[bl * 256 + kk * 16 + cc];
-        Tm[swz64(r0 + rr, c0 + cc)] = -acc;
+        const float *P = P1 + bl * 384;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(d, [&](int rr, int kk) { return Tm[rot64(r0 + rr, r0 + kk)]; },
+                 [&](int kk, int cc) { return P[kk * 24 + 8 * nt + cc]; }, 0, 2, lane);
+        *reinterpret_cast<float2 *>(Tm + rot64(r0 + g, c0 + 8 * nt + 2 * t)) = make_float2(-d[0], -d[1]);
+        *reinterpret_cast<float2 *>(Tm + rot64(r0 + g + 8, c0 + 8 * nt + 2 * t)) = make_float2(-d[2], -d[3]);
     }
     named_bar(kBarPrep, kPrepThreads);
-    // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (L[32:64, 0:32] T[0:32, 0:32])
-#pragma unroll
-    for (int e = 0; e < 4; e++) {
-        const int idx = pt + 256 * e;
-        const int r2 = idx >> 5, cc = idx & 31;
-        float acc = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 32; kk++) acc += Lm[swz64(32 + r2, kk)] * Tm[swz64(kk, cc)];
-        P2[idx] = acc;
+    // level 2 (all 8 warps, one m16n8 tile each):
+    // P2 = L[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] P2
+    {
+        const int mt = pw >> 2, nt = pw & 3;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(d, [&](int rr, int kk) { return Lm[rot64(32 + 16 * mt + rr, kk)]; },
+                 [&](int kk, int cc) { return Tm[rot64(kk, 8 * nt + cc)]; }, nt, 4, lane);
+        *reinterpret_cast<float2 *>(P2 + (16 * mt + g) * 40 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(P2 + (16 * mt + g + 8) * 40 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
     }
     named_bar(kBarPrep, kPrepThreads);
-#pragma unroll
-    for (int e = 0; e < 4; e++) {
-        const int idx = pt + 256 * e;
-        const int r2 = idx >> 5, cc = idx & 31;
-        float acc = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 32; kk++) acc += Tm[swz64(32 + r2, 32 + kk)] * P2[kk * 32 + cc];
-        Tm[swz64(32 + r2, cc)] = -acc;
+    {
+        const int mt = pw >> 2, nt = pw & 3;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(d, [&](int rr, int kk) { return Tm[rot64(32 + 16 * mt + rr, 32 + kk)]; },
+                 [&](int kk, int cc) { return P2[kk * 40 + 8 * nt + cc]; }, 0, 2 * mt + 2, lane);
+        *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g, 8 * nt + 2 * t)) = make_float2(-d[0], -d[1]);
+        *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g + 8, 8 * nt + 2 * t)) = make_float2(-d[2], -d[3]);
     }
     named_bar(kBarPrep, kPrepThreads);
-    // M = T diag(beta), unit lower triangular T
+    // M = T diag(beta), T unit lower triangular
     {
         const int r = pt >> 2, qq = pt & 3;
         uint8_t *Mt = sm.base + s * kStageBytes + kOffM;
+        float tv[16];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(Tm + rot64(r, 16 * qq + 4 * q));
+            tv[4 * q] = t4.x; tv[4 * q + 1] = t4.y; tv[4 * q + 2] = t4.z; tv[4 * q + 3] = t4.w;
+        }
 #pragma unroll
         for (int u = 0; u < 2; u++) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                const int j0 = 16 * qq + 8 * u + 2 * e;
-                float x0 = (j0 < r) ? Tm[swz64(r, j0)] : (j0 == r ? 1.f : 0.f);
-                float x1 = (j0 + 1 < r) ? Tm[swz64(r, j0 + 1)] : (j0 + 1 == r ? 1.f : 0.f);
+                const int jl = 8 * u + 2 * e, j0 = 16 * qq + jl;
+                const float x0 = (j0 < r) ? tv[jl] : (j0 == r ? 1.f : 0.f);
+                const float x1 = (j0 + 1 < r) ? tv[jl + 1] : (j0 + 1 == r ? 1.f : 0.f);
                 w[e] = pack_f16x2(x0 * cst[256 + j0], x1 * cst[256 + j0 + 1]);
             }
             *reinterpret_cast<uint4 *>(Mt + sw128_chunk(r, 2 * qq + u)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -543,29 +584,61 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
 // =============================================================================
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
-struct PendingOut {
-    int valid, s, row0, L, h;
-};
-
-__device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, const PendingOut &po, int v)
+// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L; then
+// release the stage (the second arrival on stage_free, after MMA3's commit).
+__device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, int s, int row0, int L, int h,
+                                int v)
 {
     const int w = v >> 5;
-    __nv_bfloat16 *dst = p.out + ((size_t)po.row0 * p.H + po.h) * kD + v;
+    __nv_bfloat16 *dst = p.out + ((size_t)row0 * p.H + h) * kD + v;
     const size_t row_stride = (size_t)p.H * kD;
+    uint32_t o[64];
+    tmem_ld32(tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * w) << 16), *reinterpret_cast<uint32_t(*)[32]>(o));
+    tmem_ld32(tmem + kTmP + 128 * s + 96 + ((uint32_t)(32 * w) << 16), *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+    tmem_wait_ld();
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
-        uint32_t o[32];
-        tmem_ld32(tmem + kTmP + 128 * po.s + 64 + ((uint32_t)(32 * w) << 16) + 32 * half, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; j++) {
-            const int r = 32 * half + j;
-            if (r < po.L) dst[(size_t)r * row_stride] = __float2bfloat16_rn(__uint_as_float(o[j]));
-        }
-    }
+    for (int r = 0; r < 64; r++)
+        if (r < L) dst[(size_t)r * row_stride] = __float2bfloat16_rn(__uint_as_float(o[r]));
     tc_fence_before();
     named_bar(kBarChain, kChainThreads);
-    if (v == 0) mbar_arrive(sm.bar(kBarStageFree + po.s));
+    if (v == 0) mbar_arrive(sm.bar(kBarStageFree + s));
+}
+
+// S <- (S * pend) * fm column by column (pend may be null), written back, and
+// its fp16 copy S'h (two per 32-bit column) for the chain MMAs.
+__device__ __forceinline__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float *fm, const float *pend)
+{
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+        uint32_t x[64];
+        tmem_ld32(tmem + kTmS + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(x));
+        tmem_ld32(tmem + kTmS + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+            const float4 f4 = *reinterpret_cast<const float4 *>(fm + 64 * half + j);
+            const float4 p4 = pend ? *reinterpret_cast<const float4 *>(pend + 64 * half + j)
+                                   : make_float4(1.f, 1.f, 1.f, 1.f);
+            const float fv[4] = {f4.x, f4.y, f4.z, f4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                float f = __uint_as_float(x[j + e]);
+                if (pend) f = __fmul_rn(f, pv[e]);
+                x[j + e] = __float_as_uint(__fmul_rn(f, fv[e]));
+            }
+        }
+        uint32_t h0[16], h1[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            h0[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+            h1[j] = pack_f16x2(__uint_as_float(x[32 + 2 * j]), __uint_as_float(x[32 + 2 * j + 1]));
+        }
+        tmem_st32(tmem + kTmS + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(x));
+        tmem_st32(tmem + kTmS + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+        tmem_st16(tmem + kTmS0h + lane_off + 32 * half, h0);
+        tmem_st16(tmem + kTmS0h + lane_off + 32 * half + 16, h1);
+    }
+    tmem_wait_st();
 }
 
 __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, int U)
@@ -575,7 +648,6 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
     const uint32_t tmem = *sm.tmem_base();
     const uint32_t lane_off = (uint32_t)(32 * w) << 16;
     int item = 0;
-    PendingOut po = {0, 0, 0, 0, 0};
     for (int k = 0;; k++) {
         const int u = cta_unit(k, U);
         if (u < 0) break;
@@ -612,34 +684,8 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (v == 0) KDA_PHASE(1, item, 0);
             tc_fence_after();
-            // S <- (S * pend_prev) * fm ; S'h = fp16(S)
-            const float *fm = sm.ptr<float>(kOffConst + s * kConstBytes);
-            const float *pend = prev_s >= 0 ? sm.ptr<float>(kOffConst + prev_s * kConstBytes + 512) : nullptr;
-#pragma unroll
-            for (int cb = 0; cb < 4; cb++) {
-                uint32_t x[32];
-                tmem_ld32(tmem + kTmS + lane_off + 32 * cb, x);
-                tmem_wait_ld();
-                uint32_t hpk[16];
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 f4 = *reinterpret_cast<const float4 *>(fm + 32 * cb + j);
-                    const float4 p4 = pend ? *reinterpret_cast<const float4 *>(pend + 32 * cb + j)
-                                           : make_float4(1.f, 1.f, 1.f, 1.f);
-                    const float fv[4] = {f4.x, f4.y, f4.z, f4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        float f = __uint_as_float(x[j + e]);
-                        if (pend) f = __fmul_rn(f, pv[e]);
-                        x[j + e] = __float_as_uint(__fmul_rn(f, fv[e]));
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 16; j++) hpk[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-                tmem_st32(tmem + kTmS + lane_off + 32 * cb, x);
-                tmem_st16(tmem + kTmS0h + lane_off + 16 * cb, hpk);
-            }
-            tmem_wait_st();
+            chain_scale_state(tmem, lane_off, sm.ptr<float>(kOffConst + s * kConstBytes),
+                              prev_s >= 0 ? sm.ptr<float>(kOffConst + prev_s * kConstBytes + 512) : nullptr);
             tc_fence_before();
             named_bar(kBarChain, kChainThreads);
             if (v == 0) {
@@ -657,23 +703,24 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
                 mma_commit(sm.bar(kBarMma1));
                 KDA_PHASE(1, item, 1);
             }
-            // the previous chunk's output while MMA1 runs
-            if (po.valid) chain_store_out(p, sm, tmem, po, v);
-            if (v == 0) KDA_PHASE(1, item, 2);
             ok = mbar_wait(sm.bar(kBarMma1), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (v == 0) KDA_PHASE(1, item, 3);
+            if (v == 0) KDA_PHASE(1, item, 2);
             tc_fence_after();
             // Delta^T (fp32, TMEM) -> fp16 A operand
-#pragma unroll
-            for (int half = 0; half < 2; half++) {
-                uint32_t x[32];
-                tmem_ld32(tmem + kTmP + 128 * s + lane_off + 32 * half, x);
+            {
+                uint32_t x[64];
+                tmem_ld32(tmem + kTmP + 128 * s + lane_off, *reinterpret_cast<uint32_t(*)[32]>(x));
+                tmem_ld32(tmem + kTmP + 128 * s + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
                 tmem_wait_ld();
-                uint32_t hpk[16];
+                uint32_t h0[16], h1[16];
 #pragma unroll
-                for (int j = 0; j < 16; j++) hpk[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-                tmem_st16(tmem + kTmDh + lane_off + 16 * half, hpk);
+                for (int j = 0; j < 16; j++) {
+                    h0[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                    h1[j] = pack_f16x2(__uint_as_float(x[32 + 2 * j]), __uint_as_float(x[32 + 2 * j + 1]));
+                }
+                tmem_st16(tmem + kTmDh + lane_off, h0);
+                tmem_st16(tmem + kTmDh + lane_off + 16, h1);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -691,16 +738,17 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
                 }
                 mma_commit(sm.bar(kBarMma3));
                 mma_commit(sm.bar(kBarStageFree + s));
-                KDA_PHASE(1, item, 4);
+                KDA_PHASE(1, item, 3);
             }
             ok = mbar_wait(sm.bar(kBarMma3), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (v == 0) KDA_PHASE(1, item, 5);
+            if (v == 0) KDA_PHASE(1, item, 4);
             tc_fence_after();
-            po = {1, s, row0, L, un.h};
+            chain_store_out(p, sm, tmem, s, row0, L, un.h, v);
+            if (v == 0) KDA_PHASE(1, item, 5);
             prev_s = s;
         }
-        // unit end: final state = S * pend_last, then the last chunk's output
+        // unit end: final state = S * pend_last
         if (p.s1) {
             const float *pend = sm.ptr<float>(kOffConst + prev_s * kConstBytes + 512);
 #pragma unroll
@@ -718,8 +766,6 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
                 }
             }
         }
-        chain_store_out(p, sm, tmem, po, v);
-        po.valid = 0;
     }
 }
 
