@@ -49,7 +49,7 @@ using namespace sm100;
 
 // Optional phase timestamps of CTA 0 (compiled in only with -DKDA_TRACE).
 #ifdef KDA_TRACE
-__device__ unsigned long long g_kda_trace[3][128][8];
+__device__ unsigned long long g_kda_trace[3][128][16];
 #define KDA_PHASE(role, item, point)                                                  \
     do {                                                                              \
         if (blockIdx.x == 0 && (item) < 128) g_kda_trace[role][item][point] = clock64(); \
@@ -84,7 +84,11 @@ constexpr uint32_t kOffGm = kOffConst + 2 * kConstBytes;   // G_m[128], G_last[1
 constexpr uint32_t kOffOrder = kOffGm + 1024;              // sorted sequence order
 constexpr uint32_t kOffBar = kOffOrder + 4 * kMaxSortedSeqs;
 constexpr uint32_t kOffMisc = kOffBar + 128;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;      // + alignment slack
+// pend = exp(G_last - G_m) of chunk i lives in slot i % 3: the chain reads it at
+// the start of chunk i+1 (or at the end of the unit), after chunk i's stage has
+// already been handed back, and only chunk i+3's prep can overwrite it.
+constexpr uint32_t kOffPend = kOffMisc + 64;
+constexpr uint32_t kSmemBytes = kOffPend + 3 * 512 + 1024;  // + alignment slack
 
 // mbarrier slots
 constexpr int kBarRawFull = 0;     // [2]
@@ -216,8 +220,8 @@ __device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], c
 // =============================================================================
 // prep role: warps 4-11
 // =============================================================================
-__device__ void prep_elementwise(const TcParams &p, const Smem &sm, int s, const Unit &un, int row0, int L,
-                                 int pt)
+__device__ void prep_elementwise(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0,
+                                 int L, int pt)
 {
     const uint32_t st = s * kStageBytes;
     float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
@@ -245,7 +249,8 @@ __device__ void prep_elementwise(const TcParams &p, const Smem &sm, int s, const
         }
         gmx[c] = gm;
         cst[c] = __expf(gm);                 // fm: the state seen from row m
-        cst[128 + c] = __expf(acc - gm);     // pend: decay from row m to the last row
+        sm.ptr<float>(kOffPend)[(item % 3) * 128 + c] = __expf(acc - gm);   // decay from row m to the last row
+        if (pt == 0) KDA_PHASE(0, item, 1);
     } else {
         // value tile bf16 -> fp16 in place (rows past the chunk zeroed), betas
         const int q = pt - 128;
@@ -265,6 +270,7 @@ __device__ void prep_elementwise(const TcParams &p, const Smem &sm, int s, const
         if (q < kChunk) cst[256 + q] = q < L ? __ldg(p.beta + (size_t)(row0 + q) * p.H + un.h) : 0.f;
     }
     named_bar(kBarPrep, kPrepThreads);
+    if (pt == 0) KDA_PHASE(0, item, 2);
 
     // decay-scaled fp16 operands, in place over the bf16 tiles: row r, channels
     // 32*cg .. 32*cg+31
@@ -374,7 +380,7 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
 
 // (I + L)^-1 by 16x16 diagonal-block forward substitution (warp shuffles)
 // and two levels of block merges on the warp MMA; then M = T diag(beta) -> fp16.
-__device__ void prep_inverse(const Smem &sm, int s, int pt)
+__device__ void prep_inverse(const Smem &sm, int s, int item, int pt)
 {
     const float *Lm = sm.ptr<float>(kOffL);
     float *Tm = sm.ptr<float>(s * kStageBytes + kOffW);   // fp32 64x64, rotated
@@ -413,6 +419,7 @@ __device__ void prep_inverse(const Smem &sm, int s, int pt)
         }
     }
     named_bar(kBarPrep, kPrepThreads);
+    if (pt == 0) KDA_PHASE(0, item, 6);
     // level 1 (warps 0-3 of the role): P = L10 X0, then T10 = -X1 P, for the
     // two 32-wide diagonal blocks
     if (pw < 4) {
@@ -437,6 +444,7 @@ __device__ void prep_inverse(const Smem &sm, int s, int pt)
         *reinterpret_cast<float2 *>(Tm + rot64(r0 + g + 8, c0 + 8 * nt + 2 * t)) = make_float2(-d[2], -d[3]);
     }
     named_bar(kBarPrep, kPrepThreads);
+    if (pt == 0) KDA_PHASE(0, item, 7);
     // level 2 (all 8 warps, one m16n8 tile each):
     // P2 = L[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] P2
     {
@@ -457,6 +465,7 @@ __device__ void prep_inverse(const Smem &sm, int s, int pt)
         *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g + 8, 8 * nt + 2 * t)) = make_float2(-d[2], -d[3]);
     }
     named_bar(kBarPrep, kPrepThreads);
+    if (pt == 0) KDA_PHASE(0, item, 8);
     // M = T diag(beta), T unit lower triangular
     {
         const int r = pt >> 2, qq = pt & 3;
@@ -550,8 +559,8 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
             bool ok = mbar_wait(sm.bar(kBarRawFull + s), (item >> 1) & 1, sm.abort_flag());
             if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (pt == 0) KDA_PHASE(0, item, 0);
-            prep_elementwise(p, sm, s, un, row0, L, pt);
-            if (pt == 0) KDA_PHASE(0, item, 1);
+            prep_elementwise(p, sm, s, item, un, row0, L, pt);
+            if (pt == 0) KDA_PHASE(0, item, 3);
             if (pt == 0) {
                 tc_fence_after();
                 issue_mma_a(sm, s, tmem);
@@ -559,12 +568,12 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
             }
             ok = mbar_wait(sm.bar(kBarAFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (pt == 0) KDA_PHASE(0, item, 2);
+            if (pt == 0) KDA_PHASE(0, item, 4);
             tc_fence_after();
             prep_read_a(sm, s, tmem, pt);
-            if (pt == 0) KDA_PHASE(0, item, 3);
-            prep_inverse(sm, s, pt);
-            if (pt == 0) KDA_PHASE(0, item, 4);
+            if (pt == 0) KDA_PHASE(0, item, 5);
+            prep_inverse(sm, s, item, pt);
+            if (pt == 0) KDA_PHASE(0, item, 9);
             if (pt == 0) {
                 tc_fence_after();
                 issue_mma_b(sm, s, tmem);
@@ -572,10 +581,10 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
             }
             ok = mbar_wait(sm.bar(kBarWFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (pt == 0) KDA_PHASE(0, item, 5);
+            if (pt == 0) KDA_PHASE(0, item, 10);
             tc_fence_after();
             prep_read_w(sm, s, tmem, pt);
-            if (pt == 0) KDA_PHASE(0, item, 6);
+            if (pt == 0) KDA_PHASE(0, item, 11);
             if (pt == 0) mbar_arrive(sm.bar(kBarPrepDone + s));
         }
     }
@@ -675,7 +684,6 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
             tmem_st32(tmem + kTmS + lane_off + 32 * cb, x);
         }
         tmem_wait_st();
-        int prev_s = -1;
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const int row0 = un.bos + c * kChunk;
@@ -685,7 +693,8 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
             if (v == 0) KDA_PHASE(1, item, 0);
             tc_fence_after();
             chain_scale_state(tmem, lane_off, sm.ptr<float>(kOffConst + s * kConstBytes),
-                              prev_s >= 0 ? sm.ptr<float>(kOffConst + prev_s * kConstBytes + 512) : nullptr);
+                              c > 0 ? sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128 : nullptr);
+            if (v == 0) KDA_PHASE(1, item, 6);
             tc_fence_before();
             named_bar(kBarChain, kChainThreads);
             if (v == 0) {
@@ -723,6 +732,7 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
                 tmem_st16(tmem + kTmDh + lane_off + 16, h1);
             }
             tmem_wait_st();
+            if (v == 0) KDA_PHASE(1, item, 7);
             tc_fence_before();
             named_bar(kBarChain, kChainThreads);
             if (v == 0) {
@@ -746,11 +756,10 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
             tc_fence_after();
             chain_store_out(p, sm, tmem, s, row0, L, un.h, v);
             if (v == 0) KDA_PHASE(1, item, 5);
-            prev_s = s;
         }
-        // unit end: final state = S * pend_last
+        // unit end: final state = S * pend of the unit's last chunk
         if (p.s1) {
-            const float *pend = sm.ptr<float>(kOffConst + prev_s * kConstBytes + 512);
+            const float *pend = sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128;
 #pragma unroll
             for (int cb = 0; cb < 4; cb++) {
                 uint32_t x[32];
