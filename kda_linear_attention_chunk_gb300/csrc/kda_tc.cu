@@ -63,8 +63,8 @@ __device__ unsigned long long g_kda_trace[3][128][16];
 constexpr int kD = 128;
 constexpr int kThreads = 416;
 constexpr int kChainThreads = 128;
-constexpr int kPrepThreads = 256;
-constexpr int kBarChain = 1, kBarPrep = 2;
+constexpr int kGroupThreads = 128;                  // prep groups E and I
+constexpr int kBarChain = 1, kBarE = 2, kBarI = 3;   // named barriers
 constexpr int kMaxSortedSeqs = 256;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----------------------
@@ -73,11 +73,11 @@ constexpr uint32_t kOffKQ = 0;          // [kb][K rows 0-63 | Q rows 0-63], 2 x 
 constexpr uint32_t kOffKM = 32768;      // Km, 2 x 8 KB
 constexpr uint32_t kOffV = 49152;       // V (fp16 in place of bf16), 2 x 8 KB
 constexpr uint32_t kOffGX = 65536;      // g (fp32, 4 x 8 KB); later M | B | W' (and T)
-constexpr uint32_t kOffM = kOffGX;              // M [r][j] fp16, 8 KB
+constexpr uint32_t kOffM = kOffGX;              // M [r][j] fp16, 8 KB (off-diagonal L blocks before)
 constexpr uint32_t kOffB = kOffGX + 8192;       // tril(A_qk) [r][i] fp16, 8 KB
 constexpr uint32_t kOffW = kOffGX + 16384;      // -W' [c][r] fp16, 16 KB (T fp32 before)
-constexpr uint32_t kOffL = 2 * kStageBytes;     // 196608: L fp32 64x64 (also scan exchange)
-constexpr uint32_t kOffP = kOffL + 16384;       // merge temporaries, 6 KB
+constexpr uint32_t kOffEScr = 2 * kStageBytes;  // 196608: group E scan exchange, 2 KB
+constexpr uint32_t kOffP = kOffEScr + 2048;     // group I merge temporaries, 6 KB
 constexpr uint32_t kOffConst = kOffP + 6144;    // per stage: fm[128] pend[128] beta[64]
 constexpr uint32_t kConstBytes = 1280;
 constexpr uint32_t kOffGm = kOffConst + 2 * kConstBytes;   // G_m[128], G_last[128]
@@ -95,6 +95,7 @@ constexpr int kBarRawFull = 0;     // [2]
 constexpr int kBarStageFree = 2;   // [2]
 constexpr int kBarPrepDone = 4;    // [2]
 constexpr int kBarAFull = 6, kBarWFull = 7, kBarMma1 = 8, kBarMma3 = 9, kBarDrain = 10;
+constexpr int kBarEDone = 11;      // [2]: group E finished a chunk (A readout, diagonal inverses)
 
 // TMEM columns
 constexpr uint32_t kTmS = 0, kTmP = 128, kTmS0h = 384, kTmDh = 448, kTmCols = 512;
@@ -217,153 +218,6 @@ __device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], c
     mma_tf32(d, ah, bh);
 }
 
-// =============================================================================
-// prep role: warps 4-11
-// =============================================================================
-__device__ void prep_elementwise(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0,
-                                 int L, int pt)
-{
-    const uint32_t st = s * kStageBytes;
-    float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
-    float *gmx = sm.ptr<float>(kOffGm);
-    const int m = (L - 1) >> 1;
-
-    if (pt < 128) {
-        // one thread per key channel walks the rows: G = inclusive prefix of g,
-        // written back in place (fp32, same swizzled layout)
-        const int c = pt, cb = c >> 5, cc = c & 31;
-        uint8_t *gb = sm.base + st + kOffGX + cb * 8192 + 4 * (cc & 3);
-        float acc = 0.f, gm = 0.f;
-#pragma unroll
-        for (int r0 = 0; r0 < kChunk; r0 += 16) {
-            float x[16];
-#pragma unroll
-            for (int t = 0; t < 16; t++) x[t] = *reinterpret_cast<const float *>(gb + sw128_chunk(r0 + t, cc >> 2));
-#pragma unroll
-            for (int t = 0; t < 16; t++) {
-                const int r = r0 + t;
-                if (r < L) acc += x[t];
-                if (r == m) gm = acc;
-                *reinterpret_cast<float *>(gb + sw128_chunk(r, cc >> 2)) = acc;
-            }
-        }
-        gmx[c] = gm;
-        cst[c] = __expf(gm);                 // fm: the state seen from row m
-        sm.ptr<float>(kOffPend)[(item % 3) * 128 + c] = __expf(acc - gm);   // decay from row m to the last row
-        if (pt == 0) KDA_PHASE(0, item, 1);
-    } else {
-        // value tile bf16 -> fp16 in place (rows past the chunk zeroed), betas
-        const int q = pt - 128;
-        uint8_t *vt = sm.base + st + kOffV;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const int idx = q + 128 * i;           // 16-byte chunk index in the 16 KB tile
-            const int r = (idx >> 3) & 63;
-            uint4 *ptr = reinterpret_cast<uint4 *>(vt + idx * 16);
-            uint4 w = *ptr;
-            const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) o[e] = r < L ? pack_f16x2(bf16lo(in[e]), bf16hi(in[e])) : 0u;
-            *ptr = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (q < kChunk) cst[256 + q] = q < L ? __ldg(p.beta + (size_t)(row0 + q) * p.H + un.h) : 0.f;
-    }
-    named_bar(kBarPrep, kPrepThreads);
-    if (pt == 0) KDA_PHASE(0, item, 2);
-
-    // decay-scaled fp16 operands, in place over the bf16 tiles: row r, channels
-    // 32*cg .. 32*cg+31
-    const int pw = pt >> 5, lane = pt & 31;
-    const int rr = lane & 7, cg = lane >> 3;
-    const int r = pw * 8 + rr;
-    const bool valid = r < L;
-    const int kb = cg >> 1;
-    uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
-    uint8_t *qt = kt + 8192;
-    uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
-    const uint8_t *gt = sm.base + st + kOffGX + cg * 8192;
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        // 8 channels: 32*cg + 8*j + e
-        const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
-        const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
-        const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
-        const float4 m1 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j + 4);
-        const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
-        const uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
-        const uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
-        const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
-        const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
-        uint32_t okp[4], okm[4], oqp[4];
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-            if (valid) {
-                a0 = __expf(G[2 * e] - M[2 * e]);
-                a1 = __expf(G[2 * e + 1] - M[2 * e + 1]);
-                b0 = __expf(M[2 * e] - G[2 * e]);
-                b1 = __expf(M[2 * e + 1] - G[2 * e + 1]);
-            }
-            const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
-            const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
-            okp[e] = pack_f16x2(k0 * a0, k1 * a1);
-            okm[e] = pack_f16x2(k0 * b0, k1 * b1);
-            oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
-        }
-        *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
-        *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
-        *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
-    }
-    fence_proxy_async_smem();
-    named_bar(kBarPrep, kPrepThreads);
-}
-
-// A readout: strictly lower, beta-scaled A_kk -> L (fp32, rotated layout);
-// lower A_qk (diagonal included) -> B (fp16, K-major [r][i]).
-__device__ void prep_read_a(const Smem &sm, int s, uint32_t tmem, int pt)
-{
-    const int pw = pt >> 5, lane = pt & 31;
-    const int sp = pw & 3, ch = pw >> 2;
-    const int R = 32 * sp + lane;
-    uint32_t a[32];
-    tmem_ld32(tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * sp) << 16) + 32 * ch, a);
-    tmem_wait_ld();
-    const float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
-    if (R < 64) {
-        float *Lm = sm.ptr<float>(kOffL);
-        const float bi = cst[256 + R];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; q4++) {
-            const int j0 = 32 * ch + 4 * q4;
-            float v4[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) v4[e] = (j0 + e < R) ? bi * __uint_as_float(a[4 * q4 + e]) : 0.f;
-            *reinterpret_cast<float4 *>(Lm + rot64(R, j0)) = make_float4(v4[0], v4[1], v4[2], v4[3]);
-        }
-    } else {
-        const int rr = R - 64;
-        uint8_t *Bt = sm.base + s * kStageBytes + kOffB;
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int i0 = 32 * ch + 8 * q + 2 * e;
-                const float x0 = (i0 <= rr) ? __uint_as_float(a[8 * q + 2 * e]) : 0.f;
-                const float x1 = (i0 + 1 <= rr) ? __uint_as_float(a[8 * q + 2 * e + 1]) : 0.f;
-                w[e] = pack_f16x2(x0, x1);
-            }
-            *reinterpret_cast<uint4 *>(Bt + sw128_chunk(rr, 4 * ch + q)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    named_bar(kBarPrep, kPrepThreads);
-}
-
 // One m16n8 tile of D = sum_k A[r0 + .][ka + k] * B[kb + k][c0 + .] over k-steps
 // [ks0, ks1) of 8, A and B read from fp32 smem through `la` / `lb` (row, col)
 // index functions; 3 x tf32 on the warp MMA.
@@ -378,142 +232,225 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
     }
 }
 
-// (I + L)^-1 by 16x16 diagonal-block forward substitution (warp shuffles)
-// and two levels of block merges on the warp MMA; then M = T diag(beta) -> fp16.
-__device__ void prep_inverse(const Smem &sm, int s, int item, int pt)
-{
-    const float *Lm = sm.ptr<float>(kOffL);
-    float *Tm = sm.ptr<float>(s * kStageBytes + kOffW);   // fp32 64x64, rotated
-    float *P1 = sm.ptr<float>(kOffP);                     // [2][16][24]
-    float *P2 = P1;                                       // [32][40] (after P1 is dead)
-    const float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
-    const int pw = pt >> 5, lane = pt & 31, g = lane >> 2, t = lane & 3;
+// =============================================================================
+// prep, group E (warps 4-7): cumulative log-decay, decay-scaled operands,
+// MMA-a, the A readout and the 16x16 diagonal inverses
+// =============================================================================
+// L_off: the off-diagonal blocks of L the merges need, kept in the stage's M
+// region until M is written: L10 [16][20], L32 [16][20], L[32:64, 0:32] [32][36]
+// (row strides chosen so warp-MMA A fragments hit distinct banks).
+constexpr int kL10 = 0, kL32 = 320, kL2 = 640;
 
-    if (pt < 64) {
-        const int i = pt, blk = i >> 4, a = i & 15;
-        float Lr[16], x[16];
+__device__ void e_scan(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0, int L, int et)
+{
+    const int ew = et >> 5, lane = et & 31;
+    const uint32_t st = s * kStageBytes;
+    float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
+    float4 *xchg = sm.ptr<float4>(kOffEScr);            // [4 row groups][32 chunk columns]
+    float *gmx = sm.ptr<float>(kOffGm), *glx = gmx + 128;
+    const int m = (L - 1) >> 1;
+    // thread = (row group ew: rows 16*ew .. +15) x (4 channels 4*lane .. +3)
+    uint8_t *gb = sm.base + st + kOffGX + (lane >> 3) * 8192;
+    const int jc = lane & 7;
+    float4 x[16];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(Lm + rot64(i, 16 * blk + 4 * q));
-            Lr[4 * q] = l4.x; Lr[4 * q + 1] = l4.y; Lr[4 * q + 2] = l4.z; Lr[4 * q + 3] = l4.w;
-        }
+    for (int t = 0; t < 16; t++) {
+        const int r = 16 * ew + t;
+        x[t] = r < L ? *reinterpret_cast<const float4 *>(gb + sw128_chunk(r, jc)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-        for (int q = 0; q < 16; q++) x[q] = (q == a) ? 1.f : 0.f;
+    for (int t = 1; t < 16; t++) {
+        x[t].x += x[t - 1].x; x[t].y += x[t - 1].y; x[t].z += x[t - 1].z; x[t].w += x[t - 1].w;
+    }
+    xchg[ew * 32 + lane] = x[15];
+    named_bar(kBarE, kGroupThreads);
+    float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < ew; w++) {
+        const float4 y = xchg[w * 32 + lane];
+        pre.x += y.x; pre.y += y.y; pre.z += y.z; pre.w += y.w;
+    }
 #pragma unroll
-        for (int a2 = 0; a2 < 15; a2++) {
-            const int src = (lane & 16) | a2;
+    for (int t = 0; t < 16; t++) {
+        const int r = 16 * ew + t;
+        float4 G = make_float4(x[t].x + pre.x, x[t].y + pre.y, x[t].z + pre.z, x[t].w + pre.w);
+        *reinterpret_cast<float4 *>(gb + sw128_chunk(r, jc)) = G;
+        if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = G;
+        if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = G;
+    }
+    named_bar(kBarE, kGroupThreads);
+    // chain constants, one thread per key channel
+    cst[et] = __expf(gmx[et]);                                                  // view from row m
+    sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = __expf(glx[et] - gmx[et]);  // row m -> last row
+    if (et < kChunk) cst[256 + et] = et < L ? __ldg(p.beta + (size_t)(row0 + et) * p.H + un.h) : 0.f;
+}
+
+// Kp = K*exp(G - G_m), Qp = Q*exp(G - G_m), Km = K*exp(G_m - G) as fp16, in
+// place over the bf16 tiles; rows past the chunk become zero.
+__device__ void e_operands(const Smem &sm, int s, int L, int et)
+{
+    const int ew = et >> 5, lane = et & 31;
+    const int rr = lane & 7, cg = lane >> 3;
+    const uint32_t st = s * kStageBytes;
+    const float *gmx = sm.ptr<float>(kOffGm);
+    const int kb = cg >> 1;
+    uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
+    uint8_t *qt = kt + 8192;
+    uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
+    const uint8_t *gt = sm.base + st + kOffGX + cg * 8192;
+#pragma unroll 1
+    for (int hf = 0; hf < 2; hf++) {
+        const int r = 16 * ew + 8 * hf + rr;
+        const bool valid = r < L;
 #pragma unroll
-            for (int col = 0; col <= a2; col++) {
-                const float xs = __shfl_sync(0xffffffffu, x[col], src);
-                if (a > a2) x[col] -= Lr[a2] * xs;
+        for (int j = 0; j < 4; j++) {
+            const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
+            const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
+            const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
+            const float4 m1 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j + 4);
+            const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
+            const uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
+            const uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
+            const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+            const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
+            uint32_t okp[4], okm[4], oqp[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+                if (valid) {
+                    a0 = __expf(G[2 * e] - M[2 * e]);
+                    a1 = __expf(G[2 * e + 1] - M[2 * e + 1]);
+                    b0 = __expf(M[2 * e] - G[2 * e]);
+                    b1 = __expf(M[2 * e + 1] - G[2 * e + 1]);
+                }
+                const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
+                const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
+                okp[e] = pack_f16x2(k0 * a0, k1 * a1);
+                okm[e] = pack_f16x2(k0 * b0, k1 * b1);
+                oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
             }
-        }
-        // the diagonal 16x16 inverse, and zeros in the 16 columns beside it
-        // within the 32-wide block (upper: stays zero; lower: merged below)
-        const int other = 16 * (blk ^ 1);
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            *reinterpret_cast<float4 *>(Tm + rot64(i, 16 * blk + 4 * q)) =
-                make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-            *reinterpret_cast<float4 *>(Tm + rot64(i, other + 4 * q)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
+            *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
+            *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
         }
     }
-    named_bar(kBarPrep, kPrepThreads);
-    if (pt == 0) KDA_PHASE(0, item, 6);
-    // level 1 (warps 0-3 of the role): P = L10 X0, then T10 = -X1 P, for the
-    // two 32-wide diagonal blocks
-    if (pw < 4) {
-        const int bl = pw >> 1, nt = pw & 1;
-        const int r0 = 32 * bl + 16, c0 = 32 * bl;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(d, [&](int rr, int kk) { return Lm[rot64(r0 + rr, c0 + kk)]; },
-                 [&](int kk, int cc) { return Tm[rot64(c0 + kk, c0 + 8 * nt + cc)]; }, nt, 2, lane);
-        float *P = P1 + bl * 384;
-        *reinterpret_cast<float2 *>(P + g * 24 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
-        *reinterpret_cast<float2 *>(P + (g + 8) * 24 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
-    }
-    named_bar(kBarPrep, kPrepThreads);
-    if (pw < 4) {
-        const int bl = pw >> 1, nt = pw & 1;
-        const int r0 = 32 * bl + 16, c0 = 32 * bl;
-        const float *P = P1 + bl * 384;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(d, [&](int rr, int kk) { return Tm[rot64(r0 + rr, r0 + kk)]; },
-                 [&](int kk, int cc) { return P[kk * 24 + 8 * nt + cc]; }, 0, 2, lane);
-        *reinterpret_cast<float2 *>(Tm + rot64(r0 + g, c0 + 8 * nt + 2 * t)) = make_float2(-d[0], -d[1]);
-        *reinterpret_cast<float2 *>(Tm + rot64(r0 + g + 8, c0 + 8 * nt + 2 * t)) = make_float2(-d[2], -d[3]);
-    }
-    named_bar(kBarPrep, kPrepThreads);
-    if (pt == 0) KDA_PHASE(0, item, 7);
-    // level 2 (all 8 warps, one m16n8 tile each):
-    // P2 = L[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] P2
-    {
-        const int mt = pw >> 2, nt = pw & 3;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(d, [&](int rr, int kk) { return Lm[rot64(32 + 16 * mt + rr, kk)]; },
-                 [&](int kk, int cc) { return Tm[rot64(kk, 8 * nt + cc)]; }, nt, 4, lane);
-        *reinterpret_cast<float2 *>(P2 + (16 * mt + g) * 40 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
-        *reinterpret_cast<float2 *>(P2 + (16 * mt + g + 8) * 40 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
-    }
-    named_bar(kBarPrep, kPrepThreads);
-    {
-        const int mt = pw >> 2, nt = pw & 3;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(d, [&](int rr, int kk) { return Tm[rot64(32 + 16 * mt + rr, 32 + kk)]; },
-                 [&](int kk, int cc) { return P2[kk * 40 + 8 * nt + cc]; }, 0, 2 * mt + 2, lane);
-        *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g, 8 * nt + 2 * t)) = make_float2(-d[0], -d[1]);
-        *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g + 8, 8 * nt + 2 * t)) = make_float2(-d[2], -d[3]);
-    }
-    named_bar(kBarPrep, kPrepThreads);
-    if (pt == 0) KDA_PHASE(0, item, 8);
-    // M = T diag(beta), T unit lower triangular
-    {
-        const int r = pt >> 2, qq = pt & 3;
-        uint8_t *Mt = sm.base + s * kStageBytes + kOffM;
-        float tv[16];
+}
+
+// value tile bf16 -> fp16 in place; rows past the chunk become zero
+__device__ void e_convert_v(const Smem &sm, int s, int L, int et)
+{
+    uint8_t *vt = sm.base + s * kStageBytes + kOffV;
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const float4 t4 = *reinterpret_cast<const float4 *>(Tm + rot64(r, 16 * qq + 4 * q));
-            tv[4 * q] = t4.x; tv[4 * q + 1] = t4.y; tv[4 * q + 2] = t4.z; tv[4 * q + 3] = t4.w;
+    for (int i = 0; i < 8; i++) {
+        const int idx = et + 128 * i;              // 16-byte chunk index in the 16 KB tile
+        const int r = (idx >> 3) & 63;
+        uint4 *ptr = reinterpret_cast<uint4 *>(vt + idx * 16);
+        const uint4 w = *ptr;
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) o[e] = r < L ? pack_f16x2(bf16lo(in[e]), bf16hi(in[e])) : 0u;
+        *ptr = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// forward substitution of one 16x16 unit lower triangular block held one row
+// per lane in 16-lane groups: x = row `a` of (I + Lb)^-1
+__device__ __forceinline__ void diag_inverse16(const float (&Lr)[16], float (&x)[16], int a, int lane)
+{
+#pragma unroll
+    for (int q = 0; q < 16; q++) x[q] = (q == a) ? 1.f : 0.f;
+#pragma unroll
+    for (int a2 = 0; a2 < 15; a2++) {
+        const int src = (lane & 16) | a2;
+#pragma unroll
+        for (int col = 0; col <= a2; col++) {
+            const float xs = __shfl_sync(0xffffffffu, x[col], src);
+            if (a > a2) x[col] -= Lr[a2] * xs;
         }
+    }
+}
+
+// A readout.  Lanes 64-127 (A_qk rows): lower part, diagonal included -> B
+// (fp16 [r][i]).  Lanes 0-63 (A_kk rows i): L_i = beta_i * strict(A_kk row i)
+// stays in registers; the 16x16 diagonal block inverse X of the row's block
+// goes to T (fp32), the off-diagonal blocks the merges need go to L_off.
+__device__ void e_read_a(const Smem &sm, int s, uint32_t tmem, int et)
+{
+    const int ew = et >> 5, lane = et & 31;
+    const uint32_t st = s * kStageBytes;
+    uint32_t a[64];
+    const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * ew) << 16);
+    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(a));
+    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+    tmem_wait_ld();
+    if (ew >= 2) {
+        const int r = 32 * (ew - 2) + lane;
+        uint8_t *Bt = sm.base + st + kOffB;
 #pragma unroll
-        for (int u = 0; u < 2; u++) {
+        for (int q = 0; q < 8; q++) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                const int jl = 8 * u + 2 * e, j0 = 16 * qq + jl;
-                const float x0 = (j0 < r) ? tv[jl] : (j0 == r ? 1.f : 0.f);
-                const float x1 = (j0 + 1 < r) ? tv[jl + 1] : (j0 + 1 == r ? 1.f : 0.f);
-                w[e] = pack_f16x2(x0 * cst[256 + j0], x1 * cst[256 + j0 + 1]);
+                const int i0 = 8 * q + 2 * e;
+                const float x0 = (i0 <= r) ? __uint_as_float(a[i0]) : 0.f;
+                const float x1 = (i0 + 1 <= r) ? __uint_as_float(a[i0 + 1]) : 0.f;
+                w[e] = pack_f16x2(x0, x1);
             }
-            *reinterpret_cast<uint4 *>(Mt + sw128_chunk(r, 2 * qq + u)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(Bt + sw128_chunk(r, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        return;
+    }
+    const int i = 32 * ew + lane, blk = i >> 4, a16 = i & 15;
+    const float bi = sm.ptr<float>(kOffConst + s * kConstBytes)[256 + i];
+    float Lr[16], x[16];
+    // the row's own 16-column diagonal block (static register indices per branch)
+    if (ew == 0) {
+#pragma unroll
+        for (int t = 0; t < 16; t++) {
+            const float lo = (t < i) ? bi * __uint_as_float(a[t]) : 0.f;
+            const float hi = (16 + t < i) ? bi * __uint_as_float(a[16 + t]) : 0.f;
+            Lr[t] = (lane & 16) ? hi : lo;
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < 16; t++) {
+            const float lo = (32 + t < i) ? bi * __uint_as_float(a[32 + t]) : 0.f;
+            const float hi = (48 + t < i) ? bi * __uint_as_float(a[48 + t]) : 0.f;
+            Lr[t] = (lane & 16) ? hi : lo;
         }
     }
-    fence_proxy_async_smem();
-    named_bar(kBarPrep, kPrepThreads);
-}
-
-// -W'^T (TMEM, lane = key channel c, column = row r) -> fp16 MN-major [c][r]
-__device__ void prep_read_w(const Smem &sm, int s, uint32_t tmem, int pt)
-{
-    const int pw = pt >> 5, lane = pt & 31;
-    const int sp = pw & 3, ch = pw >> 2;
-    const int c = 32 * sp + lane;
-    uint32_t a[32];
-    tmem_ld32(tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * sp) << 16) + 32 * ch, a);
-    tmem_wait_ld();
-    uint8_t *Wt = sm.base + s * kStageBytes + kOffW;
+    diag_inverse16(Lr, x, a16, lane);
+    float *Tm = sm.ptr<float>(st + kOffW);
+    const int other = 16 * (blk ^ 1);
 #pragma unroll
     for (int q = 0; q < 4; q++) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; e++)
-            w[e] = pack_f16x2(-__uint_as_float(a[8 * q + 2 * e]), -__uint_as_float(a[8 * q + 2 * e + 1]));
-        *reinterpret_cast<uint4 *>(Wt + sw128_chunk(c, 4 * ch + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<float4 *>(Tm + rot64(i, 16 * blk + 4 * q)) =
+            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        *reinterpret_cast<float4 *>(Tm + rot64(i, other + 4 * q)) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    named_bar(kBarPrep, kPrepThreads);
+    float *Lo = sm.ptr<float>(st + kOffM);
+    auto lval = [&](int j) { return (j < i) ? bi * __uint_as_float(a[j]) : 0.f; };
+    if (ew == 0) {
+        if (lane >= 16) {                          // rows 16-31: L10 = L[16:32, 0:16]
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                *reinterpret_cast<float4 *>(Lo + kL10 + (i - 16) * 20 + 4 * q) =
+                    make_float4(lval(4 * q), lval(4 * q + 1), lval(4 * q + 2), lval(4 * q + 3));
+        }
+    } else {                                       // rows 32-63: L[32:64, 0:32]; rows 48-63 also L32
+#pragma unroll
+        for (int q = 0; q < 8; q++)
+            *reinterpret_cast<float4 *>(Lo + kL2 + (i - 32) * 36 + 4 * q) =
+                make_float4(lval(4 * q), lval(4 * q + 1), lval(4 * q + 2), lval(4 * q + 3));
+        if (lane >= 16) {
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                *reinterpret_cast<float4 *>(Lo + kL32 + (i - 48) * 20 + 4 * q) =
+                    make_float4(lval(32 + 4 * q), lval(33 + 4 * q), lval(34 + 4 * q), lval(35 + 4 * q));
+        }
+    }
 }
 
 __device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
@@ -526,6 +463,134 @@ __device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
         const uint64_t ad = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
         const uint64_t bd = smem_desc_sw128(st + kOffKM + kb * 8192 + kin * 32, 16, 1024);
         mma_ss(tmem + kTmP + 128 * s + 64, ad, bd, id, ks > 0);
+    }
+}
+
+__device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int U)
+{
+    const int et = threadIdx.x - kChainThreads;
+    const uint32_t tmem = *sm.tmem_base();
+    int item = 0;
+    for (int k = 0;; k++) {
+        const int u = cta_unit(k, U);
+        if (u < 0) break;
+        const Unit un = get_unit(p, order, u);
+        for (int c = 0; c < un.nchunks; c++, item++) {
+            const int s = item & 1;
+            const int row0 = un.bos + c * kChunk;
+            const int L = min(kChunk, un.eos - row0);
+            bool ok = mbar_wait(sm.bar(kBarRawFull + s), (item >> 1) & 1, sm.abort_flag());
+            if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (et == 0) KDA_PHASE(0, item, 0);
+            e_scan(p, sm, s, item, un, row0, L, et);
+            if (et == 0) KDA_PHASE(0, item, 1);
+            e_operands(sm, s, L, et);
+            fence_proxy_async_smem();
+            named_bar(kBarE, kGroupThreads);
+            if (et == 0) {
+                KDA_PHASE(0, item, 2);
+                tc_fence_after();
+                issue_mma_a(sm, s, tmem);
+                mma_commit(sm.bar(kBarAFull));
+            }
+            e_convert_v(sm, s, L, et);
+            fence_proxy_async_smem();
+            ok = mbar_wait(sm.bar(kBarAFull), item & 1, sm.abort_flag());
+            if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (et == 0) KDA_PHASE(0, item, 3);
+            tc_fence_after();
+            e_read_a(sm, s, tmem, et);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(kBarE, kGroupThreads);
+            if (et == 0) {
+                KDA_PHASE(0, item, 4);
+                mbar_arrive(sm.bar(kBarEDone + s));
+            }
+        }
+    }
+}
+
+// =============================================================================
+// prep, group I (warps 8-11): block merges of the inverse on the warp MMA,
+// M = T diag(beta), MMA-b, and the -W' conversion
+// =============================================================================
+__device__ void i_merge(const Smem &sm, int s, int it)
+{
+    const int iw = it >> 5, lane = it & 31, g = lane >> 2, t = lane & 3;
+    const uint32_t st = s * kStageBytes;
+    float *Tm = sm.ptr<float>(st + kOffW);
+    const float *Lo = sm.ptr<float>(st + kOffM);
+    float *P1 = sm.ptr<float>(kOffP);            // [2][16][24]
+    float *P2 = P1;                              // [32][40] once P1 is dead
+    // level 1: P = L10 X0 (or L32 X2), then T10 = -X1 P (or T32 = -X3 P)
+    {
+        const int bl = iw >> 1, nt = iw & 1;
+        const int r0 = 32 * bl + 16, c0 = 32 * bl;
+        const float *Lb = Lo + (bl ? kL32 : kL10);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(d, [&](int rr, int kk) { return Lb[rr * 20 + kk]; },
+                 [&](int kk, int cc) { return Tm[rot64(c0 + kk, c0 + 8 * nt + cc)]; }, nt, 2, lane);
+        float *P = P1 + bl * 384;
+        *reinterpret_cast<float2 *>(P + g * 24 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(P + (g + 8) * 24 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
+        named_bar(kBarI, kGroupThreads);
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(e, [&](int rr, int kk) { return Tm[rot64(r0 + rr, r0 + kk)]; },
+                 [&](int kk, int cc) { return P[kk * 24 + 8 * nt + cc]; }, 0, 2, lane);
+        *reinterpret_cast<float2 *>(Tm + rot64(r0 + g, c0 + 8 * nt + 2 * t)) = make_float2(-e[0], -e[1]);
+        *reinterpret_cast<float2 *>(Tm + rot64(r0 + g + 8, c0 + 8 * nt + 2 * t)) = make_float2(-e[2], -e[3]);
+    }
+    named_bar(kBarI, kGroupThreads);
+    // level 2: P2 = L[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] P2
+#pragma unroll
+    for (int tt = 0; tt < 2; tt++) {
+        const int tile = 2 * iw + tt, mt = tile >> 2, nt = tile & 3;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(d, [&](int rr, int kk) { return Lo[kL2 + (16 * mt + rr) * 36 + kk]; },
+                 [&](int kk, int cc) { return Tm[rot64(kk, 8 * nt + cc)]; }, nt, 4, lane);
+        *reinterpret_cast<float2 *>(P2 + (16 * mt + g) * 40 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(P2 + (16 * mt + g + 8) * 40 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
+    }
+    named_bar(kBarI, kGroupThreads);
+#pragma unroll
+    for (int tt = 0; tt < 2; tt++) {
+        const int tile = 2 * iw + tt, mt = tile >> 2, nt = tile & 3;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(d, [&](int rr, int kk) { return Tm[rot64(32 + 16 * mt + rr, 32 + kk)]; },
+                 [&](int kk, int cc) { return P2[kk * 40 + 8 * nt + cc]; }, 0, 2 * mt + 2, lane);
+        *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g, 8 * nt + 2 * t)) = make_float2(-d[0], -d[1]);
+        *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g + 8, 8 * nt + 2 * t)) = make_float2(-d[2], -d[3]);
+    }
+    named_bar(kBarI, kGroupThreads);
+}
+
+// M = T diag(beta) (T unit lower triangular) -> fp16 K-major [r][j]
+__device__ void i_make_m(const Smem &sm, int s, int it)
+{
+    const uint32_t st = s * kStageBytes;
+    const float *Tm = sm.ptr<float>(st + kOffW);
+    const float *bt = sm.ptr<float>(kOffConst + s * kConstBytes) + 256;
+    uint8_t *Mt = sm.base + st + kOffM;
+    const int r = it >> 1, hh = it & 1;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const int j0 = 32 * hh + 8 * q;
+        const float4 t0 = *reinterpret_cast<const float4 *>(Tm + rot64(r, j0));
+        const float4 t1 = *reinterpret_cast<const float4 *>(Tm + rot64(r, j0 + 4));
+        const float4 b0 = *reinterpret_cast<const float4 *>(bt + j0);
+        const float4 b1 = *reinterpret_cast<const float4 *>(bt + j0 + 4);
+        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        float mv[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const int j = j0 + e;
+            mv[e] = ((j < r) ? tv[e] : (j == r ? 1.f : 0.f)) * bv[e];
+        }
+        *reinterpret_cast<uint4 *>(Mt + sw128_chunk(r, 4 * hh + q)) =
+            make_uint4(pack_f16x2(mv[0], mv[1]), pack_f16x2(mv[2], mv[3]), pack_f16x2(mv[4], mv[5]),
+                       pack_f16x2(mv[6], mv[7]));
     }
 }
 
@@ -543,9 +608,30 @@ __device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
     }
 }
 
-__device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, int U)
+// -W'^T (TMEM, lane = key channel c, column = row r) -> fp16 MN-major [c][r]
+__device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
 {
-    const int pt = threadIdx.x - kChainThreads;
+    const int iw = it >> 5, lane = it & 31;
+    const int c = 32 * iw + lane;
+    uint32_t a[64];
+    const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * iw) << 16);
+    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(a));
+    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+    tmem_wait_ld();
+    uint8_t *Wt = sm.base + s * kStageBytes + kOffW;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++)
+            w[e] = pack_f16x2(-__uint_as_float(a[8 * q + 2 * e]), -__uint_as_float(a[8 * q + 2 * e + 1]));
+        *reinterpret_cast<uint4 *>(Wt + sw128_chunk(c, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+__device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int U)
+{
+    const int it = threadIdx.x - kChainThreads - kGroupThreads;
     const uint32_t tmem = *sm.tmem_base();
     int item = 0;
     for (int k = 0;; k++) {
@@ -554,38 +640,32 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
         const Unit un = get_unit(p, order, u);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
-            const int row0 = un.bos + c * kChunk;
-            const int L = min(kChunk, un.eos - row0);
-            bool ok = mbar_wait(sm.bar(kBarRawFull + s), (item >> 1) & 1, sm.abort_flag());
-            if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (pt == 0) KDA_PHASE(0, item, 0);
-            prep_elementwise(p, sm, s, item, un, row0, L, pt);
-            if (pt == 0) KDA_PHASE(0, item, 3);
-            if (pt == 0) {
-                tc_fence_after();
-                issue_mma_a(sm, s, tmem);
-                mma_commit(sm.bar(kBarAFull));
-            }
-            ok = mbar_wait(sm.bar(kBarAFull), item & 1, sm.abort_flag());
-            if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (pt == 0) KDA_PHASE(0, item, 4);
-            tc_fence_after();
-            prep_read_a(sm, s, tmem, pt);
-            if (pt == 0) KDA_PHASE(0, item, 5);
-            prep_inverse(sm, s, item, pt);
-            if (pt == 0) KDA_PHASE(0, item, 9);
-            if (pt == 0) {
+            bool ok = mbar_wait(sm.bar(kBarEDone + s), (item >> 1) & 1, sm.abort_flag());
+            if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (it == 0) KDA_PHASE(0, item, 5);
+            i_merge(sm, s, it);
+            if (it == 0) KDA_PHASE(0, item, 6);
+            i_make_m(sm, s, it);
+            fence_proxy_async_smem();
+            named_bar(kBarI, kGroupThreads);
+            if (it == 0) {
+                KDA_PHASE(0, item, 7);
                 tc_fence_after();
                 issue_mma_b(sm, s, tmem);
                 mma_commit(sm.bar(kBarWFull));
             }
             ok = mbar_wait(sm.bar(kBarWFull), item & 1, sm.abort_flag());
-            if (role_any(!ok, kBarPrep, kPrepThreads)) { if (pt == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (pt == 0) KDA_PHASE(0, item, 10);
+            if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (it == 0) KDA_PHASE(0, item, 8);
             tc_fence_after();
-            prep_read_w(sm, s, tmem, pt);
-            if (pt == 0) KDA_PHASE(0, item, 11);
-            if (pt == 0) mbar_arrive(sm.bar(kBarPrepDone + s));
+            i_read_w(sm, s, tmem, it);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(kBarI, kGroupThreads);
+            if (it == 0) {
+                KDA_PHASE(0, item, 9);
+                mbar_arrive(sm.bar(kBarPrepDone + s));
+            }
         }
     }
 }
@@ -593,22 +673,34 @@ __device__ void prep_role(const TcParams &p, const Smem &sm, const int *order, i
 // =============================================================================
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
-// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L; then
-// release the stage (the second arrival on stage_free, after MMA3's commit).
+// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L,
+// transposed through the stage's value tile (free once MMA-b has run) so the
+// global stores are 16-byte row pieces; then release the stage (the second
+// arrival on stage_free, after MMA3's commit).
 __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, int s, int row0, int L, int h,
                                 int v)
 {
     const int w = v >> 5;
-    __nv_bfloat16 *dst = p.out + ((size_t)row0 * p.H + h) * kD + v;
-    const size_t row_stride = (size_t)p.H * kD;
     uint32_t o[64];
-    tmem_ld32(tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * w) << 16), *reinterpret_cast<uint32_t(*)[32]>(o));
-    tmem_ld32(tmem + kTmP + 128 * s + 96 + ((uint32_t)(32 * w) << 16), *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+    const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * w) << 16);
+    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(o));
+    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
     tmem_wait_ld();
+    __nv_bfloat16 *ot = sm.ptr<__nv_bfloat16>(s * kStageBytes + kOffV);     // [64][128]
 #pragma unroll
-    for (int r = 0; r < 64; r++)
-        if (r < L) dst[(size_t)r * row_stride] = __float2bfloat16_rn(__uint_as_float(o[r]));
+    for (int r = 0; r < 64; r++) ot[r * kD + v] = __float2bfloat16_rn(__uint_as_float(o[r]));
     tc_fence_before();
+    named_bar(kBarChain, kChainThreads);
+    const size_t row_stride = (size_t)p.H * kD;
+    __nv_bfloat16 *dst = p.out + ((size_t)row0 * p.H + h) * kD;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const int idx = v + 128 * k, r = idx >> 4, q = idx & 15;
+        if (r < L)
+            *reinterpret_cast<uint4 *>(dst + (size_t)r * row_stride + 8 * q) =
+                *reinterpret_cast<const uint4 *>(ot + r * kD + 8 * q);
+    }
+    fence_proxy_async_smem();
     named_bar(kBarChain, kChainThreads);
     if (v == 0) mbar_arrive(sm.bar(kBarStageFree + s));
 }
@@ -832,7 +924,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
     // schedule: sequences sorted by length, longest first (ties: lower index)
     if (p.sorted) {
-        int *lens = sm.ptr<int>(kOffL);
+        int *lens = sm.ptr<int>(kOffP);
         for (int n = tid; n < p.N; n += kThreads) {
             int b = min(max(p.cu[n], 0), p.T), e = min(max(p.cu[n + 1], 0), p.T);
             if (p.cu[n] < 0 || p.cu[n] > p.T || p.cu[n + 1] < 0 || p.cu[n + 1] > p.T) atomicOr(p.err, kErrBadSeqlens);
@@ -860,7 +952,9 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         mbar_init(sm.bar(kBarWFull), 1);
         mbar_init(sm.bar(kBarMma1), 1);
         mbar_init(sm.bar(kBarMma3), 1);
-        mbar_init(sm.bar(kBarDrain), 2);
+        mbar_init(sm.bar(kBarDrain), 3);
+        mbar_init(sm.bar(kBarEDone), 1);
+        mbar_init(sm.bar(kBarEDone + 1), 1);
         mbar_fence_init();
     }
     if (warp == 12) {
@@ -876,18 +970,17 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
     if (warp < 4) {
         chain_role(p, sm, order, U);
-        if (tid == 0) {
-            mma_commit(sm.bar(kBarDrain));
-            mbar_wait(sm.bar(kBarDrain), 0, sm.abort_flag(), 1u << 14);
-        }
+    } else if (warp < 8) {
+        e_role(p, sm, order, U);
     } else if (warp < 12) {
-        prep_role(p, sm, order, U);
-        if (tid == kChainThreads) {
-            mma_commit(sm.bar(kBarDrain));
-            mbar_wait(sm.bar(kBarDrain), 0, sm.abort_flag(), 1u << 14);
-        }
+        i_role(p, sm, order, U);
     } else if ((tid & 31) == 0) {
         load_role(p, sm, order, U, &tq, &tk, &tv, &tg);
+    }
+    // every MMA this CTA issued has completed before TMEM is released
+    if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kGroupThreads) {
+        mma_commit(sm.bar(kBarDrain));
+        mbar_wait(sm.bar(kBarDrain), 0, sm.abort_flag(), 1u << 14);
     }
     tc_fence_before();
     __syncthreads();
