@@ -61,7 +61,7 @@ __device__ unsigned long long g_kda_trace[3][128][16];
 #endif
 
 constexpr int kD = 128;
-constexpr int kThreads = 416;
+constexpr int kThreads = 384;
 constexpr int kChainThreads = 128;
 constexpr int kGroupThreads = 128;                  // prep groups E and I
 constexpr int kBarChain = 1, kBarE = 2, kBarI = 3;   // named barriers
@@ -92,7 +92,6 @@ constexpr uint32_t kSmemBytes = kOffPend + 3 * 512 + 1024;  // + alignment slack
 
 // mbarrier slots
 constexpr int kBarRawFull = 0;     // [2]
-constexpr int kBarStageFree = 2;   // [2]
 constexpr int kBarPrepDone = 4;    // [2]
 constexpr int kBarAFull = 6, kBarWFull = 7, kBarMma1 = 8, kBarMma3 = 9, kBarDrain = 10;
 constexpr int kBarEDone = 11;      // [2]: group E finished a chunk (A readout, diagonal inverses)
@@ -671,6 +670,61 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
 }
 
 // =============================================================================
+// TMA loads, issued by the chain's elected thread: the first two chunks at the
+// start, then chunk i+2 as soon as chunk i has released its stage (after MMA3
+// and the output store, the last readers of the stage).
+// =============================================================================
+struct Maps {
+    const CUtensorMap *q, *k, *v, *g;
+};
+
+struct LoadCursor {
+    int k = -1, c = 0, item = 0;
+    bool done = false;
+    Unit un = {0, 0, 0, 0, 0};
+};
+
+__device__ bool cursor_issue(LoadCursor &L, const TcParams &p, const Smem &sm, const int *order, int U, const Maps &m)
+{
+    while (!L.done && L.c >= L.un.nchunks) {
+        const int u = cta_unit(++L.k, U);
+        if (u < 0) {
+            L.done = true;
+            break;
+        }
+        L.un = get_unit(p, order, u);
+        L.c = 0;
+    }
+    if (L.done) return false;
+    const int s = L.item & 1;
+    KDA_PHASE(2, L.item, 0);
+    const int row0 = L.un.bos + L.c * kChunk;
+    const uint32_t st = sm.u32(s * kStageBytes);
+    const uint32_t bar = sm.bar(kBarRawFull + s);
+    mbar_arrive_expect_tx(bar, kRawBytes);
+    for (int kb = 0; kb < 2; kb++) {
+        tma_load_3d(st + kOffKQ + kb * 16384, m.k, 64 * kb, L.un.h, row0, bar);
+        tma_load_3d(st + kOffKQ + kb * 16384 + 8192, m.q, 64 * kb, L.un.h, row0, bar);
+        tma_load_3d(st + kOffV + kb * 8192, m.v, 64 * kb, L.un.h, row0, bar);
+    }
+    for (int cb = 0; cb < 4; cb++) tma_load_3d(st + kOffGX + cb * 8192, m.g, 32 * cb, L.un.h, row0, bar);
+    L.c++;
+    L.item++;
+    return true;
+}
+
+// copies still in flight land before the CTA exits (normally a no-op: every
+// issued chunk has been consumed)
+__device__ void cursor_drain(const LoadCursor &L, const Smem &sm)
+{
+    for (int back = 1; back <= 2; back++) {
+        const int it = L.item - back;
+        if (it < 0) break;
+        mbar_wait(sm.bar(kBarRawFull + (it & 1)), (it >> 1) & 1, sm.abort_flag(), 1u << 14);
+    }
+}
+
+// =============================================================================
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
 // O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L,
@@ -702,7 +756,6 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem
     }
     fence_proxy_async_smem();
     named_bar(kBarChain, kChainThreads);
-    if (v == 0) mbar_arrive(sm.bar(kBarStageFree + s));
 }
 
 // S <- (S * pend) * fm column by column (pend may be null), written back, and
@@ -742,12 +795,9 @@ __device__ __forceinline__ void chain_scale_state(uint32_t tmem, uint32_t lane_o
     tmem_wait_st();
 }
 
-__device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, int U)
+__device__ void chain_units(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps,
+                            LoadCursor &cur, uint32_t tmem, uint32_t lane_off, int v)
 {
-    const int v = threadIdx.x;
-    const int w = v >> 5;
-    const uint32_t tmem = *sm.tmem_base();
-    const uint32_t lane_off = (uint32_t)(32 * w) << 16;
     int item = 0;
     for (int k = 0;; k++) {
         const int u = cta_unit(k, U);
@@ -839,7 +889,6 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
                     mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmDh + 8 * ks, bb, id_o, 1);
                 }
                 mma_commit(sm.bar(kBarMma3));
-                mma_commit(sm.bar(kBarStageFree + s));
                 KDA_PHASE(1, item, 3);
             }
             ok = mbar_wait(sm.bar(kBarMma3), item & 1, sm.abort_flag());
@@ -847,7 +896,10 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
             if (v == 0) KDA_PHASE(1, item, 4);
             tc_fence_after();
             chain_store_out(p, sm, tmem, s, row0, L, un.h, v);
-            if (v == 0) KDA_PHASE(1, item, 5);
+            if (v == 0) {
+                KDA_PHASE(1, item, 5);
+                cursor_issue(cur, p, sm, order, U, maps);    // chunk item+2 into the freed stage
+            }
         }
         // unit end: final state = S * pend of the unit's last chunk
         if (p.s1) {
@@ -870,44 +922,19 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
     }
 }
 
-// =============================================================================
-// load role: warp 12, one elected lane
-// =============================================================================
-__device__ void load_role(const TcParams &p, const Smem &sm, const int *order, int U, const CUtensorMap *tq,
-                          const CUtensorMap *tk, const CUtensorMap *tv, const CUtensorMap *tg)
+__device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps)
 {
-    int item = 0;
-    bool failed = false;
-    for (int k = 0; !failed; k++) {
-        const int u = cta_unit(k, U);
-        if (u < 0) break;
-        const Unit un = get_unit(p, order, u);
-        for (int c = 0; c < un.nchunks; c++, item++) {
-            const int s = item & 1;
-            if (item >= 2 && !mbar_wait(sm.bar(kBarStageFree + s), ((item >> 1) - 1) & 1, sm.abort_flag())) {
-                record_error(p, sm, kErrWaitTimeout);
-                failed = true;
-                break;
-            }
-            KDA_PHASE(2, item, 0);
-            const int row0 = un.bos + c * kChunk;
-            const uint32_t st = sm.u32(s * kStageBytes);
-            const uint32_t bar = sm.bar(kBarRawFull + s);
-            mbar_arrive_expect_tx(bar, kRawBytes);
-            for (int kb = 0; kb < 2; kb++) {
-                tma_load_3d(st + kOffKQ + kb * 16384, tk, 64 * kb, un.h, row0, bar);
-                tma_load_3d(st + kOffKQ + kb * 16384 + 8192, tq, 64 * kb, un.h, row0, bar);
-                tma_load_3d(st + kOffV + kb * 8192, tv, 64 * kb, un.h, row0, bar);
-            }
-            for (int cb = 0; cb < 4; cb++) tma_load_3d(st + kOffGX + cb * 8192, tg, 32 * cb, un.h, row0, bar);
-        }
+    const int v = threadIdx.x;
+    const int w = v >> 5;
+    const uint32_t tmem = *sm.tmem_base();
+    const uint32_t lane_off = (uint32_t)(32 * w) << 16;
+    LoadCursor cur;
+    if (v == 0) {
+        cursor_issue(cur, p, sm, order, U, maps);
+        cursor_issue(cur, p, sm, order, U, maps);
     }
-    // let the copies still in flight land before the CTA can exit
-    for (int back = 1; back <= 2; back++) {
-        const int it = item - back;
-        if (it < 0) break;
-        mbar_wait(sm.bar(kBarRawFull + (it & 1)), (it >> 1) & 1, sm.abort_flag(), 1u << 14);
-    }
+    chain_units(p, sm, order, U, maps, cur, tmem, lane_off, v);
+    if (v == 0) cursor_drain(cur, sm);
 }
 
 // =============================================================================
@@ -945,7 +972,6 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         *sm.abort_flag() = 0;
         for (int i = 0; i < 2; i++) {
             mbar_init(sm.bar(kBarRawFull + i), 1);
-            mbar_init(sm.bar(kBarStageFree + i), 2);
             mbar_init(sm.bar(kBarPrepDone + i), 1);
         }
         mbar_init(sm.bar(kBarAFull), 1);
@@ -957,7 +983,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         mbar_init(sm.bar(kBarEDone + 1), 1);
         mbar_fence_init();
     }
-    if (warp == 12) {
+    if (warp == 0) {
         tmem_alloc(sm.u32(kOffMisc), kTmCols);
         tmem_relinquish();
         if ((tid & 31) == 0) {
@@ -968,14 +994,13 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
 
+    const Maps maps = {&tq, &tk, &tv, &tg};
     if (warp < 4) {
-        chain_role(p, sm, order, U);
+        chain_role(p, sm, order, U, maps);
     } else if (warp < 8) {
         e_role(p, sm, order, U);
-    } else if (warp < 12) {
+    } else {
         i_role(p, sm, order, U);
-    } else if ((tid & 31) == 0) {
-        load_role(p, sm, order, U, &tq, &tk, &tv, &tg);
     }
     // every MMA this CTA issued has completed before TMEM is released
     if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kGroupThreads) {
@@ -985,7 +1010,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 12) tmem_dealloc(*sm.tmem_base(), kTmCols);
+    if (warp == 0) tmem_dealloc(*sm.tmem_base(), kTmCols);
 }
 
 // ---- host side ------------------------------------------------------------------
