@@ -95,6 +95,8 @@ constexpr int kBarRawFull = 0;     // [2]
 constexpr int kBarPrepDone = 4;    // [2]
 constexpr int kBarAFull = 6, kBarWFull = 7, kBarMma1 = 8, kBarMma3 = 9, kBarDrain = 10;
 constexpr int kBarEDone = 11;      // [2]: group E finished a chunk (A readout, diagonal inverses)
+constexpr int kBarODone = 13;      // [2]: the chain has stored a chunk's outputs (TMEM P_s free)
+constexpr int kBarMmaO = 15;       // all of a chunk's output MMAs are done
 
 // TMEM columns
 constexpr uint32_t kTmS = 0, kTmP = 128, kTmS0h = 384, kTmDh = 448, kTmCols = 512;
@@ -240,16 +242,23 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
 // (row strides chosen so warp-MMA A fragments hit distinct banks).
 constexpr int kL10 = 0, kL32 = 320, kL2 = 640;
 
-__device__ void e_scan(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0, int L, int et)
+// Cumulative log-decay and the decay-scaled operands in one pass.  Thread =
+// (row group ew: rows 16*ew .. +15) x (4 key channels 4*lane .. +3): the
+// prefix over rows runs in registers, groups exchange their totals once, and
+// G never goes back to shared memory.  Kp = K*exp(G - G_m), Qp = Q*exp(G - G_m),
+// Km = K*exp(G_m - G) become fp16 in place over the bf16 tiles (rows past the
+// chunk zero).  Also writes the chain constants and the betas.
+__device__ void e_scan_operands(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0, int L,
+                                int et)
 {
     const int ew = et >> 5, lane = et & 31;
     const uint32_t st = s * kStageBytes;
     float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
-    float4 *xchg = sm.ptr<float4>(kOffEScr);            // [4 row groups][32 chunk columns]
+    float4 *xchg = sm.ptr<float4>(kOffEScr);            // [4 row groups][32 channel quads]
     float *gmx = sm.ptr<float>(kOffGm), *glx = gmx + 128;
     const int m = (L - 1) >> 1;
-    // thread = (row group ew: rows 16*ew .. +15) x (4 channels 4*lane .. +3)
-    uint8_t *gb = sm.base + st + kOffGX + (lane >> 3) * 8192;
+    const float beta_r = (et < L) ? __ldg(p.beta + (size_t)(row0 + et) * p.H + un.h) : 0.f;
+    const uint8_t *gb = sm.base + st + kOffGX + (lane >> 3) * 8192;
     const int jc = lane & 7;
     float4 x[16];
 #pragma unroll
@@ -270,69 +279,44 @@ __device__ void e_scan(const TcParams &p, const Smem &sm, int s, int item, const
     }
 #pragma unroll
     for (int t = 0; t < 16; t++) {
+        x[t].x += pre.x; x[t].y += pre.y; x[t].z += pre.z; x[t].w += pre.w;
         const int r = 16 * ew + t;
-        float4 G = make_float4(x[t].x + pre.x, x[t].y + pre.y, x[t].z + pre.z, x[t].w + pre.w);
-        *reinterpret_cast<float4 *>(gb + sw128_chunk(r, jc)) = G;
-        if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = G;
-        if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = G;
+        if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = x[t];
+        if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = x[t];
     }
     named_bar(kBarE, kGroupThreads);
-    // chain constants, one thread per key channel
     cst[et] = __expf(gmx[et]);                                                  // view from row m
     sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = __expf(glx[et] - gmx[et]);  // row m -> last row
-    if (et < kChunk) cst[256 + et] = et < L ? __ldg(p.beta + (size_t)(row0 + et) * p.H + un.h) : 0.f;
-}
-
-// Kp = K*exp(G - G_m), Qp = Q*exp(G - G_m), Km = K*exp(G_m - G) as fp16, in
-// place over the bf16 tiles; rows past the chunk become zero.
-__device__ void e_operands(const Smem &sm, int s, int L, int et)
-{
-    const int ew = et >> 5, lane = et & 31;
-    const int rr = lane & 7, cg = lane >> 3;
-    const uint32_t st = s * kStageBytes;
-    const float *gmx = sm.ptr<float>(kOffGm);
-    const int kb = cg >> 1;
+    if (et < kChunk) cst[256 + et] = beta_r;
+    const float4 gm = *reinterpret_cast<const float4 *>(gmx + 4 * lane);
+    // bf16/fp16 tiles: channels 4*lane .. +3 = 8 bytes of K block (lane >> 4)
+    const int kb = lane >> 4, ch = (lane & 15) >> 1, half = lane & 1;
     uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
     uint8_t *qt = kt + 8192;
     uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
-    const uint8_t *gt = sm.base + st + kOffGX + cg * 8192;
-#pragma unroll 1
-    for (int hf = 0; hf < 2; hf++) {
-        const int r = 16 * ew + 8 * hf + rr;
-        const bool valid = r < L;
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
-            const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
-            const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
-            const float4 m1 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j + 4);
-            const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-            const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
-            const uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
-            const uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
-            const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
-            const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
-            uint32_t okp[4], okm[4], oqp[4];
+    for (int t = 0; t < 16; t++) {
+        const int r = 16 * ew + t;
+        const uint32_t off = sw128_chunk(r, ch) + 8 * half;
+        float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r < L) {
+            const float G[4] = {x[t].x, x[t].y, x[t].z, x[t].w}, M[4] = {gm.x, gm.y, gm.z, gm.w};
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-                if (valid) {
-                    a0 = __expf(G[2 * e] - M[2 * e]);
-                    a1 = __expf(G[2 * e + 1] - M[2 * e + 1]);
-                    b0 = __expf(M[2 * e] - G[2 * e]);
-                    b1 = __expf(M[2 * e + 1] - G[2 * e + 1]);
-                }
-                const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
-                const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
-                okp[e] = pack_f16x2(k0 * a0, k1 * a1);
-                okm[e] = pack_f16x2(k0 * b0, k1 * b1);
-                oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
+                a[e] = __expf(G[e] - M[e]);
+                b[e] = __expf(M[e] - G[e]);
             }
-            *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
-            *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
-            *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
         }
+        const uint2 kw = *reinterpret_cast<const uint2 *>(kt + off);
+        const uint2 qw = *reinterpret_cast<const uint2 *>(qt + off);
+        const float k0 = bf16lo(kw.x), k1 = bf16hi(kw.x), k2 = bf16lo(kw.y), k3 = bf16hi(kw.y);
+        const float q0 = bf16lo(qw.x), q1 = bf16hi(qw.x), q2 = bf16lo(qw.y), q3 = bf16hi(qw.y);
+        *reinterpret_cast<uint2 *>(kt + off) =
+            make_uint2(pack_f16x2(k0 * a[0], k1 * a[1]), pack_f16x2(k2 * a[2], k3 * a[3]));
+        *reinterpret_cast<uint2 *>(qt + off) =
+            make_uint2(pack_f16x2(q0 * a[0], q1 * a[1]), pack_f16x2(q2 * a[2], q3 * a[3]));
+        *reinterpret_cast<uint2 *>(kmt + off) =
+            make_uint2(pack_f16x2(k0 * b[0], k1 * b[1]), pack_f16x2(k2 * b[2], k3 * b[3]));
     }
 }
 
@@ -481,12 +465,14 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             bool ok = mbar_wait(sm.bar(kBarRawFull + s), (item >> 1) & 1, sm.abort_flag());
             if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (et == 0) KDA_PHASE(0, item, 0);
-            e_scan(p, sm, s, item, un, row0, L, et);
-            if (et == 0) KDA_PHASE(0, item, 1);
-            e_operands(sm, s, L, et);
+            e_scan_operands(p, sm, s, item, un, row0, L, et);
             fence_proxy_async_smem();
             named_bar(kBarE, kGroupThreads);
             if (et == 0) {
+                KDA_PHASE(0, item, 1);
+                // TMEM P_s is free once the chain has stored chunk item-2's outputs
+                if (item >= 2 && !mbar_wait(sm.bar(kBarODone + s), ((item >> 1) - 1) & 1, sm.abort_flag()))
+                    record_error(p, sm, kErrWaitTimeout);
                 KDA_PHASE(0, item, 2);
                 tc_fence_after();
                 issue_mma_a(sm, s, tmem);
@@ -727,35 +713,34 @@ __device__ void cursor_drain(const LoadCursor &L, const Smem &sm)
 // =============================================================================
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
-// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L,
-// transposed through the stage's value tile (free once MMA-b has run) so the
-// global stores are 16-byte row pieces; then release the stage (the second
-// arrival on stage_free, after MMA3's commit).
+// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L.
+// Lane pairs (v, v^1) swap halves so that each lane stores (v, v+1) pairs as
+// 4-byte words: the even lane rows 0-31, the odd lane rows 32-63.
 __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, int s, int row0, int L, int h,
-                                int v)
+                                int v, int item)
 {
-    const int w = v >> 5;
+    const int w = v >> 5, odd = v & 1;
     uint32_t o[64];
     const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * w) << 16);
     tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(o));
     tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
     tmem_wait_ld();
-    __nv_bfloat16 *ot = sm.ptr<__nv_bfloat16>(s * kStageBytes + kOffV);     // [64][128]
+    if (v == 0) KDA_PHASE(1, item, 8);
+    const size_t row_stride = (size_t)p.H * kD;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + ((size_t)row0 * p.H + h) * kD + (v & ~1));
 #pragma unroll
-    for (int r = 0; r < 64; r++) ot[r * kD + v] = __float2bfloat16_rn(__uint_as_float(o[r]));
+    for (int j = 0; j < 32; j++) {
+        const uint32_t mine = odd ? o[32 + j] : o[j];
+        const uint32_t give = odd ? o[j] : o[32 + j];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, give, 1);
+        const int r = odd ? 32 + j : j;
+        const uint32_t lo = odd ? got : mine, hi = odd ? mine : got;
+        if (r < L) dst[(size_t)r * (row_stride / 2)] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
+    }
+    if (v == 0) KDA_PHASE(1, item, 9);
     tc_fence_before();
     named_bar(kBarChain, kChainThreads);
-    const size_t row_stride = (size_t)p.H * kD;
-    __nv_bfloat16 *dst = p.out + ((size_t)row0 * p.H + h) * kD;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        const int idx = v + 128 * k, r = idx >> 4, q = idx & 15;
-        if (r < L)
-            *reinterpret_cast<uint4 *>(dst + (size_t)r * row_stride + 8 * q) =
-                *reinterpret_cast<const uint4 *>(ot + r * kD + 8 * q);
-    }
-    fence_proxy_async_smem();
-    named_bar(kBarChain, kChainThreads);
+    if (v == 0) mbar_arrive(sm.bar(kBarODone + s));
 }
 
 // S <- (S * pend) * fm column by column (pend may be null), written back, and
@@ -843,15 +828,19 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 tc_fence_after();
                 const uint32_t st = sm.u32(s * kStageBytes);
                 const uint32_t id_w = idesc_f16(128, 64, 0, 1), id_q = idesc_f16(128, 64, 0, 0);
+                // Delta half first (it gates the chain), then the output half
 #pragma unroll
                 for (int ks = 0; ks < 8; ks++) {
                     const uint64_t bw = smem_desc_sw128(st + kOffW + ks * 2048, 16, 1024);
-                    const int kb = ks >> 2, kin = ks & 3;
-                    const uint64_t bq = smem_desc_sw128(st + kOffKQ + kb * 16384 + 8192 + kin * 32, 16, 1024);
                     mma_ts(tmem + kTmP + 128 * s, tmem + kTmS0h + 8 * ks, bw, id_w, 1);
-                    mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmS0h + 8 * ks, bq, id_q, ks > 0);
                 }
                 mma_commit(sm.bar(kBarMma1));
+#pragma unroll
+                for (int ks = 0; ks < 8; ks++) {
+                    const int kb = ks >> 2, kin = ks & 3;
+                    const uint64_t bq = smem_desc_sw128(st + kOffKQ + kb * 16384 + 8192 + kin * 32, 16, 1024);
+                    mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmS0h + 8 * ks, bq, id_q, ks > 0);
+                }
                 KDA_PHASE(1, item, 1);
             }
             ok = mbar_wait(sm.bar(kBarMma1), item & 1, sm.abort_flag());
@@ -881,25 +870,32 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 tc_fence_after();
                 const uint32_t st = sm.u32(s * kStageBytes);
                 const uint32_t id_s = idesc_f16(128, 128, 0, 1), id_o = idesc_f16(128, 64, 0, 0);
+                // state update first, then the rest of the output
 #pragma unroll
                 for (int ks = 0; ks < 4; ks++) {
                     const uint64_t bk = smem_desc_sw128(st + kOffKM + ks * 2048, 8192, 1024);   // Km, MN-major
-                    const uint64_t bb = smem_desc_sw128(st + kOffB + ks * 32, 16, 1024);
                     mma_ts(tmem + kTmS, tmem + kTmDh + 8 * ks, bk, id_s, 1);
-                    mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmDh + 8 * ks, bb, id_o, 1);
                 }
                 mma_commit(sm.bar(kBarMma3));
+#pragma unroll
+                for (int ks = 0; ks < 4; ks++) {
+                    const uint64_t bb = smem_desc_sw128(st + kOffB + ks * 32, 16, 1024);
+                    mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmDh + 8 * ks, bb, id_o, 1);
+                }
+                mma_commit(sm.bar(kBarMmaO));
                 KDA_PHASE(1, item, 3);
             }
-            ok = mbar_wait(sm.bar(kBarMma3), item & 1, sm.abort_flag());
+            // every MMA of this chunk is done: its shared-memory stage is free
+            ok = mbar_wait(sm.bar(kBarMma3), item & 1, sm.abort_flag()) &&
+                 mbar_wait(sm.bar(kBarMmaO), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (v == 0) KDA_PHASE(1, item, 4);
-            tc_fence_after();
-            chain_store_out(p, sm, tmem, s, row0, L, un.h, v);
             if (v == 0) {
-                KDA_PHASE(1, item, 5);
+                KDA_PHASE(1, item, 4);
                 cursor_issue(cur, p, sm, order, U, maps);    // chunk item+2 into the freed stage
             }
+            tc_fence_after();
+            chain_store_out(p, sm, tmem, s, row0, L, un.h, v, item);
+            if (v == 0) KDA_PHASE(1, item, 5);
         }
         // unit end: final state = S * pend of the unit's last chunk
         if (p.s1) {
@@ -981,6 +977,9 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         mbar_init(sm.bar(kBarDrain), 3);
         mbar_init(sm.bar(kBarEDone), 1);
         mbar_init(sm.bar(kBarEDone + 1), 1);
+        mbar_init(sm.bar(kBarODone), 1);
+        mbar_init(sm.bar(kBarODone + 1), 1);
+        mbar_init(sm.bar(kBarMmaO), 1);
         mbar_fence_init();
     }
     if (warp == 0) {
