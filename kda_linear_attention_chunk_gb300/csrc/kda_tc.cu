@@ -81,14 +81,15 @@ constexpr uint32_t kOffP = kOffEScr + 2048;     // group I merge temporaries, 6 
 constexpr uint32_t kOffConst = kOffP + 6144;    // per stage: fm[128] pend[128] beta[64]
 constexpr uint32_t kConstBytes = 1280;
 constexpr uint32_t kOffGm = kOffConst + 2 * kConstBytes;   // G_m[128], G_last[128]
-constexpr uint32_t kOffOrder = kOffGm + 1024;              // sorted sequence order
-constexpr uint32_t kOffBar = kOffOrder + 4 * kMaxSortedSeqs;
+constexpr uint32_t kOffOrder = kOffGm + 1024;              // sorted order, then {bos, eos} per sequence
+constexpr uint32_t kOffBar = kOffOrder + 12 * kMaxSortedSeqs;
 constexpr uint32_t kOffMisc = kOffBar + 128;
 // pend = exp(G_last - G_m) of chunk i lives in slot i % 3: the chain reads it at
 // the start of chunk i+1 (or at the end of the unit), after chunk i's stage has
 // already been handed back, and only chunk i+3's prep can overwrite it.
 constexpr uint32_t kOffPend = kOffMisc + 64;
-constexpr uint32_t kSmemBytes = kOffPend + 3 * 512 + 1024;  // + alignment slack
+constexpr uint32_t kOffOT = kOffPend + 3 * 512;            // output transpose, bf16 [64][128]
+constexpr uint32_t kSmemBytes = kOffOT + 16384 + 1024;     // + alignment slack
 
 // mbarrier slots
 constexpr int kBarRawFull = 0;     // [2]
@@ -147,10 +148,18 @@ __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, in
     Unit x;
     const int su = u / p.H;
     x.h = u % p.H;
-    x.n = p.sorted ? order[su] : su;
-    int b = p.cu[x.n], e = p.cu[x.n + 1];
-    b = min(max(b, 0), p.T);
-    e = min(max(e, 0), p.T);
+    int b, e;
+    if (p.sorted) {
+        // order[] is followed in shared memory by the clamped {bos, eos} rows
+        x.n = order[su];
+        const int2 be = reinterpret_cast<const int2 *>(order + kMaxSortedSeqs)[x.n];
+        b = be.x;
+        e = be.y;
+    } else {
+        x.n = su;
+        b = min(max(p.cu[x.n], 0), p.T);
+        e = min(max(p.cu[x.n + 1], 0), p.T);
+    }
     if (e < b) e = b;
     x.bos = b;
     x.eos = e;
@@ -242,23 +251,17 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
 // (row strides chosen so warp-MMA A fragments hit distinct banks).
 constexpr int kL10 = 0, kL32 = 320, kL2 = 640;
 
-// Cumulative log-decay and the decay-scaled operands in one pass.  Thread =
-// (row group ew: rows 16*ew .. +15) x (4 key channels 4*lane .. +3): the
-// prefix over rows runs in registers, groups exchange their totals once, and
-// G never goes back to shared memory.  Kp = K*exp(G - G_m), Qp = Q*exp(G - G_m),
-// Km = K*exp(G_m - G) become fp16 in place over the bf16 tiles (rows past the
-// chunk zero).  Also writes the chain constants and the betas.
-__device__ void e_scan_operands(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0, int L,
-                                int et)
+__device__ void e_scan(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0, int L, int et)
 {
     const int ew = et >> 5, lane = et & 31;
     const uint32_t st = s * kStageBytes;
     float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
-    float4 *xchg = sm.ptr<float4>(kOffEScr);            // [4 row groups][32 channel quads]
+    float4 *xchg = sm.ptr<float4>(kOffEScr);            // [4 row groups][32 chunk columns]
     float *gmx = sm.ptr<float>(kOffGm), *glx = gmx + 128;
     const int m = (L - 1) >> 1;
-    const float beta_r = (et < L) ? __ldg(p.beta + (size_t)(row0 + et) * p.H + un.h) : 0.f;
-    const uint8_t *gb = sm.base + st + kOffGX + (lane >> 3) * 8192;
+    const float beta_r = (et < L) ? __ldg(p.beta + (size_t)(row0 + et) * p.H + un.h) : 0.f;   // issued early
+    // thread = (row group ew: rows 16*ew .. +15) x (4 channels 4*lane .. +3)
+    uint8_t *gb = sm.base + st + kOffGX + (lane >> 3) * 8192;
     const int jc = lane & 7;
     float4 x[16];
 #pragma unroll
@@ -279,44 +282,69 @@ __device__ void e_scan_operands(const TcParams &p, const Smem &sm, int s, int it
     }
 #pragma unroll
     for (int t = 0; t < 16; t++) {
-        x[t].x += pre.x; x[t].y += pre.y; x[t].z += pre.z; x[t].w += pre.w;
         const int r = 16 * ew + t;
-        if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = x[t];
-        if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = x[t];
+        float4 G = make_float4(x[t].x + pre.x, x[t].y + pre.y, x[t].z + pre.z, x[t].w + pre.w);
+        *reinterpret_cast<float4 *>(gb + sw128_chunk(r, jc)) = G;
+        if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = G;
+        if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = G;
     }
     named_bar(kBarE, kGroupThreads);
+    // chain constants, one thread per key channel
     cst[et] = __expf(gmx[et]);                                                  // view from row m
     sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = __expf(glx[et] - gmx[et]);  // row m -> last row
     if (et < kChunk) cst[256 + et] = beta_r;
-    const float4 gm = *reinterpret_cast<const float4 *>(gmx + 4 * lane);
-    // bf16/fp16 tiles: channels 4*lane .. +3 = 8 bytes of K block (lane >> 4)
-    const int kb = lane >> 4, ch = (lane & 15) >> 1, half = lane & 1;
+}
+
+// Kp = K*exp(G - G_m), Qp = Q*exp(G - G_m), Km = K*exp(G_m - G) as fp16, in
+// place over the bf16 tiles; rows past the chunk become zero.
+__device__ void e_operands(const Smem &sm, int s, int L, int et)
+{
+    const int ew = et >> 5, lane = et & 31;
+    const int rr = lane & 7, cg = lane >> 3;
+    const uint32_t st = s * kStageBytes;
+    const float *gmx = sm.ptr<float>(kOffGm);
+    const int kb = cg >> 1;
     uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
     uint8_t *qt = kt + 8192;
     uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
+    const uint8_t *gt = sm.base + st + kOffGX + cg * 8192;
+#pragma unroll 1
+    for (int hf = 0; hf < 2; hf++) {
+        const int r = 16 * ew + 8 * hf + rr;
+        const bool valid = r < L;
 #pragma unroll
-    for (int t = 0; t < 16; t++) {
-        const int r = 16 * ew + t;
-        const uint32_t off = sw128_chunk(r, ch) + 8 * half;
-        float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
-        if (r < L) {
-            const float G[4] = {x[t].x, x[t].y, x[t].z, x[t].w}, M[4] = {gm.x, gm.y, gm.z, gm.w};
+        for (int j = 0; j < 4; j++) {
+            const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
+            const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
+            const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
+            const float4 m1 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j + 4);
+            const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
+            const uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
+            const uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
+            const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+            const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
+            uint32_t okp[4], okm[4], oqp[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                a[e] = __expf(G[e] - M[e]);
-                b[e] = __expf(M[e] - G[e]);
+                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+                if (valid) {
+                    a0 = __expf(G[2 * e] - M[2 * e]);
+                    a1 = __expf(G[2 * e + 1] - M[2 * e + 1]);
+                    b0 = __expf(M[2 * e] - G[2 * e]);
+                    b1 = __expf(M[2 * e + 1] - G[2 * e + 1]);
+                }
+                const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
+                const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
+                okp[e] = pack_f16x2(k0 * a0, k1 * a1);
+                okm[e] = pack_f16x2(k0 * b0, k1 * b1);
+                oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
             }
+            *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
+            *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
+            *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
         }
-        const uint2 kw = *reinterpret_cast<const uint2 *>(kt + off);
-        const uint2 qw = *reinterpret_cast<const uint2 *>(qt + off);
-        const float k0 = bf16lo(kw.x), k1 = bf16hi(kw.x), k2 = bf16lo(kw.y), k3 = bf16hi(kw.y);
-        const float q0 = bf16lo(qw.x), q1 = bf16hi(qw.x), q2 = bf16lo(qw.y), q3 = bf16hi(qw.y);
-        *reinterpret_cast<uint2 *>(kt + off) =
-            make_uint2(pack_f16x2(k0 * a[0], k1 * a[1]), pack_f16x2(k2 * a[2], k3 * a[3]));
-        *reinterpret_cast<uint2 *>(qt + off) =
-            make_uint2(pack_f16x2(q0 * a[0], q1 * a[1]), pack_f16x2(q2 * a[2], q3 * a[3]));
-        *reinterpret_cast<uint2 *>(kmt + off) =
-            make_uint2(pack_f16x2(k0 * b[0], k1 * b[1]), pack_f16x2(k2 * b[2], k3 * b[3]));
     }
 }
 
@@ -465,7 +493,8 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             bool ok = mbar_wait(sm.bar(kBarRawFull + s), (item >> 1) & 1, sm.abort_flag());
             if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (et == 0) KDA_PHASE(0, item, 0);
-            e_scan_operands(p, sm, s, item, un, row0, L, et);
+            e_scan(p, sm, s, item, un, row0, L, et);
+            e_operands(sm, s, L, et);
             fence_proxy_async_smem();
             named_bar(kBarE, kGroupThreads);
             if (et == 0) {
@@ -713,34 +742,36 @@ __device__ void cursor_drain(const LoadCursor &L, const Smem &sm)
 // =============================================================================
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
-// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L.
-// Lane pairs (v, v^1) swap halves so that each lane stores (v, v+1) pairs as
-// 4-byte words: the even lane rows 0-31, the odd lane rows 32-63.
+// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L,
+// transposed through a dedicated shared buffer so the global stores are
+// 16-byte row pieces.  Then TMEM P_s may be reused (o_done).
 __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, int s, int row0, int L, int h,
                                 int v, int item)
 {
-    const int w = v >> 5, odd = v & 1;
+    const int w = v >> 5;
     uint32_t o[64];
     const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * w) << 16);
     tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(o));
     tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
     tmem_wait_ld();
     if (v == 0) KDA_PHASE(1, item, 8);
-    const size_t row_stride = (size_t)p.H * kD;
-    uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + ((size_t)row0 * p.H + h) * kD + (v & ~1));
+    __nv_bfloat16 *ot = sm.ptr<__nv_bfloat16>(kOffOT);   // [64][128]
 #pragma unroll
-    for (int j = 0; j < 32; j++) {
-        const uint32_t mine = odd ? o[32 + j] : o[j];
-        const uint32_t give = odd ? o[j] : o[32 + j];
-        const uint32_t got = __shfl_xor_sync(0xffffffffu, give, 1);
-        const int r = odd ? 32 + j : j;
-        const uint32_t lo = odd ? got : mine, hi = odd ? mine : got;
-        if (r < L) dst[(size_t)r * (row_stride / 2)] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
-    }
-    if (v == 0) KDA_PHASE(1, item, 9);
+    for (int r = 0; r < 64; r++) ot[r * kD + v] = __float2bfloat16_rn(__uint_as_float(o[r]));
     tc_fence_before();
     named_bar(kBarChain, kChainThreads);
-    if (v == 0) mbar_arrive(sm.bar(kBarODone + s));
+    if (v == 0) mbar_arrive(sm.bar(kBarODone + s));      // TMEM P_s has been read by all lanes
+    const size_t row_stride = (size_t)p.H * kD;
+    __nv_bfloat16 *dst = p.out + ((size_t)row0 * p.H + h) * kD;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const int idx = v + 128 * k, r = idx >> 4, q = idx & 15;
+        if (r < L)
+            *reinterpret_cast<uint4 *>(dst + (size_t)r * row_stride + 8 * q) =
+                *reinterpret_cast<const uint4 *>(ot + r * kD + 8 * q);
+    }
+    if (v == 0) KDA_PHASE(1, item, 9);
+    named_bar(kBarChain, kChainThreads);                 // the transpose buffer is free again
 }
 
 // S <- (S * pend) * fm column by column (pend may be null), written back, and
@@ -948,10 +979,14 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     // schedule: sequences sorted by length, longest first (ties: lower index)
     if (p.sorted) {
         int *lens = sm.ptr<int>(kOffP);
+        int2 *rows = reinterpret_cast<int2 *>(order + kMaxSortedSeqs);
         for (int n = tid; n < p.N; n += kThreads) {
-            int b = min(max(p.cu[n], 0), p.T), e = min(max(p.cu[n + 1], 0), p.T);
-            if (p.cu[n] < 0 || p.cu[n] > p.T || p.cu[n + 1] < 0 || p.cu[n + 1] > p.T) atomicOr(p.err, kErrBadSeqlens);
-            lens[n] = max(e - b, 0);
+            const int cb = p.cu[n], ce = p.cu[n + 1];
+            int b = min(max(cb, 0), p.T), e = min(max(ce, 0), p.T);
+            if (cb < 0 || cb > p.T || ce < 0 || ce > p.T) atomicOr(p.err, kErrBadSeqlens);
+            if (e < b) e = b;
+            rows[n] = make_int2(b, e);
+            lens[n] = e - b;
         }
         __syncthreads();
         for (int n = tid; n < p.N; n += kThreads) {
