@@ -387,7 +387,7 @@ __device__ __forceinline__ void diag_inverse16(const float (&Lr)[16], float (&x)
 // (fp16 [r][i]).  Lanes 0-63 (A_kk rows i): L_i = beta_i * strict(A_kk row i)
 // stays in registers; the 16x16 diagonal block inverse X of the row's block
 // goes to T (fp32), the off-diagonal blocks the merges need go to L_off.
-__device__ void e_read_a(const Smem &sm, int s, uint32_t tmem, int et)
+__device__ void e_read_a(const Smem &sm, int s, uint32_t tmem, int et, int item)
 {
     const int ew = et >> 5, lane = et & 31;
     const uint32_t st = s * kStageBytes;
@@ -432,7 +432,9 @@ __device__ void e_read_a(const Smem &sm, int s, uint32_t tmem, int et)
             Lr[t] = (lane & 16) ? hi : lo;
         }
     }
+    if (et == 0) KDA_PHASE(0, item, 12);
     diag_inverse16(Lr, x, a16, lane);
+    if (et == 0) KDA_PHASE(0, item, 13);
     float *Tm = sm.ptr<float>(st + kOffW);
     const int other = 16 * (blk ^ 1);
 #pragma unroll
@@ -513,7 +515,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (et == 0) KDA_PHASE(0, item, 3);
             tc_fence_after();
-            e_read_a(sm, s, tmem, et);
+            e_read_a(sm, s, tmem, et, item);
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(kBarE, kGroupThreads);
@@ -660,7 +662,9 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
             i_merge(sm, s, it);
             if (it == 0) KDA_PHASE(0, item, 6);
             i_make_m(sm, s, it);
+            if (it == 0) KDA_PHASE(0, item, 10);
             fence_proxy_async_smem();
+            if (it == 0) KDA_PHASE(0, item, 11);
             named_bar(kBarI, kGroupThreads);
             if (it == 0) {
                 KDA_PHASE(0, item, 7);
@@ -923,6 +927,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             if (v == 0) {
                 KDA_PHASE(1, item, 4);
                 cursor_issue(cur, p, sm, order, U, maps);    // chunk item+2 into the freed stage
+                KDA_PHASE(1, item, 10);
             }
             tc_fence_after();
             chain_store_out(p, sm, tmem, s, row0, L, un.h, v, item);
