@@ -249,7 +249,11 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
 // L_off: the off-diagonal blocks of L the merges need, kept in the stage's M
 // region until M is written: L10 [16][20], L32 [16][20], L[32:64, 0:32] [32][36]
 // (row strides chosen so warp-MMA A fragments hit distinct banks).
-constexpr int kL10 = 0, kL32 = 320, kL2 = 640;
+// fp32 block store in the stage's W region (until W' is written): X0..X3 (the
+// 16x16 diagonal inverses) and T10, T32, each [16][20]; then the off-diagonal
+// L blocks L10 [16][20], L32 [16][20] and L[32:64, 0:32] [32][36].  Row strides
+// keep warp-MMA fragment loads (nearly) conflict-free.
+constexpr int kTcX = 0, kTcT = 1280, kL10 = 1920, kL32 = 2240, kL2 = 2560;
 
 __device__ void e_scan(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0, int L, int et)
 {
@@ -303,6 +307,7 @@ __device__ void e_operands(const Smem &sm, int s, int L, int et)
     const int rr = lane & 7, cg = lane >> 3;
     const uint32_t st = s * kStageBytes;
     const float *gmx = sm.ptr<float>(kOffGm);
+    const float *bt = sm.ptr<float>(kOffConst + s * kConstBytes) + 256;
     const int kb = cg >> 1;
     uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
     uint8_t *qt = kt + 8192;
@@ -312,6 +317,7 @@ __device__ void e_operands(const Smem &sm, int s, int L, int et)
     for (int hf = 0; hf < 2; hf++) {
         const int r = 16 * ew + 8 * hf + rr;
         const bool valid = r < L;
+        const float br = bt[r];                    // beta_r (0 past the chunk)
 #pragma unroll
         for (int j = 0; j < 4; j++) {
             const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
@@ -337,7 +343,7 @@ __device__ void e_operands(const Smem &sm, int s, int L, int et)
                 }
                 const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
                 const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
-                okp[e] = pack_f16x2(k0 * a0, k1 * a1);
+                okp[e] = pack_f16x2(k0 * (a0 * br), k1 * (a1 * br));
                 okm[e] = pack_f16x2(k0 * b0, k1 * b1);
                 oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
             }
@@ -348,10 +354,11 @@ __device__ void e_operands(const Smem &sm, int s, int L, int et)
     }
 }
 
-// value tile bf16 -> fp16 in place; rows past the chunk become zero
+// value tile bf16 -> beta_r * v as fp16, in place; rows past the chunk become zero
 __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
 {
     uint8_t *vt = sm.base + s * kStageBytes + kOffV;
+    const float *bt = sm.ptr<float>(kOffConst + s * kConstBytes) + 256;
 #pragma unroll
     for (int i = 0; i < 8; i++) {
         const int idx = et + 128 * i;              // 16-byte chunk index in the 16 KB tile
@@ -361,7 +368,8 @@ __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
         const uint32_t in[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < 4; e++) o[e] = r < L ? pack_f16x2(bf16lo(in[e]), bf16hi(in[e])) : 0u;
+        const float br = bt[r];
+        for (int e = 0; e < 4; e++) o[e] = r < L ? pack_f16x2(bf16lo(in[e]) * br, bf16hi(in[e]) * br) : 0u;
         *ptr = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
@@ -383,10 +391,12 @@ __device__ __forceinline__ void diag_inverse16(const float (&Lr)[16], float (&x)
     }
 }
 
-// A readout.  Lanes 64-127 (A_qk rows): lower part, diagonal included -> B
-// (fp16 [r][i]).  Lanes 0-63 (A_kk rows i): L_i = beta_i * strict(A_kk row i)
-// stays in registers; the 16x16 diagonal block inverse X of the row's block
-// goes to T (fp32), the off-diagonal blocks the merges need go to L_off.
+// A readout.  Lanes 64-127 (A_qk rows r): lower part, diagonal included -> B
+// (fp16 [r][i]).  Lanes 0-63 (A_kk rows i; beta_i is folded into Kp, so this
+// already is the beta-scaled A_kk): the strict lower part L_i stays in
+// registers; the inverse X of its 16x16 diagonal block goes to the fp32 block
+// store and, followed by zeros, to the fp16 operand T16; the off-diagonal L
+// blocks the merges need go next to the fp32 blocks.
 __device__ void e_read_a(const Smem &sm, int s, uint32_t tmem, int et, int item)
 {
     const int ew = et >> 5, lane = et & 31;
@@ -414,53 +424,44 @@ __device__ void e_read_a(const Smem &sm, int s, uint32_t tmem, int et, int item)
         return;
     }
     const int i = 32 * ew + lane, blk = i >> 4, a16 = i & 15;
-    const float bi = sm.ptr<float>(kOffConst + s * kConstBytes)[256 + i];
+    auto lval = [&](int j) { return (j < i) ? __uint_as_float(a[j]) : 0.f; };
     float Lr[16], x[16];
-    // the row's own 16-column diagonal block (static register indices per branch)
     if (ew == 0) {
 #pragma unroll
-        for (int t = 0; t < 16; t++) {
-            const float lo = (t < i) ? bi * __uint_as_float(a[t]) : 0.f;
-            const float hi = (16 + t < i) ? bi * __uint_as_float(a[16 + t]) : 0.f;
-            Lr[t] = (lane & 16) ? hi : lo;
-        }
+        for (int t = 0; t < 16; t++) Lr[t] = (lane & 16) ? lval(16 + t) : lval(t);
     } else {
 #pragma unroll
-        for (int t = 0; t < 16; t++) {
-            const float lo = (32 + t < i) ? bi * __uint_as_float(a[32 + t]) : 0.f;
-            const float hi = (48 + t < i) ? bi * __uint_as_float(a[48 + t]) : 0.f;
-            Lr[t] = (lane & 16) ? hi : lo;
-        }
+        for (int t = 0; t < 16; t++) Lr[t] = (lane & 16) ? lval(48 + t) : lval(32 + t);
     }
     if (et == 0) KDA_PHASE(0, item, 12);
     diag_inverse16(Lr, x, a16, lane);
     if (et == 0) KDA_PHASE(0, item, 13);
-    float *Tm = sm.ptr<float>(st + kOffW);
-    const int other = 16 * (blk ^ 1);
+    float *W = sm.ptr<float>(st + kOffW);
+    float *xb = W + kTcX + blk * 320 + a16 * 20;
 #pragma unroll
-    for (int q = 0; q < 4; q++) {
-        *reinterpret_cast<float4 *>(Tm + rot64(i, 16 * blk + 4 * q)) =
-            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-        *reinterpret_cast<float4 *>(Tm + rot64(i, other + 4 * q)) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float *Lo = sm.ptr<float>(st + kOffM);
-    auto lval = [&](int j) { return (j < i) ? bi * __uint_as_float(a[j]) : 0.f; };
+    for (int q = 0; q < 4; q++) *reinterpret_cast<float4 *>(xb + 4 * q) = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    uint8_t *T16 = sm.base + st + kOffM;
+    *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, 2 * blk)) =
+        make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]), pack_f16x2(x[6], x[7]));
+    *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, 2 * blk + 1)) =
+        make_uint4(pack_f16x2(x[8], x[9]), pack_f16x2(x[10], x[11]), pack_f16x2(x[12], x[13]), pack_f16x2(x[14], x[15]));
+    for (int q = 2 * blk + 2; q < 8; q++) *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, q)) = make_uint4(0u, 0u, 0u, 0u);
     if (ew == 0) {
         if (lane >= 16) {                          // rows 16-31: L10 = L[16:32, 0:16]
 #pragma unroll
             for (int q = 0; q < 4; q++)
-                *reinterpret_cast<float4 *>(Lo + kL10 + (i - 16) * 20 + 4 * q) =
+                *reinterpret_cast<float4 *>(W + kL10 + (i - 16) * 20 + 4 * q) =
                     make_float4(lval(4 * q), lval(4 * q + 1), lval(4 * q + 2), lval(4 * q + 3));
         }
     } else {                                       // rows 32-63: L[32:64, 0:32]; rows 48-63 also L32
 #pragma unroll
         for (int q = 0; q < 8; q++)
-            *reinterpret_cast<float4 *>(Lo + kL2 + (i - 32) * 36 + 4 * q) =
+            *reinterpret_cast<float4 *>(W + kL2 + (i - 32) * 36 + 4 * q) =
                 make_float4(lval(4 * q), lval(4 * q + 1), lval(4 * q + 2), lval(4 * q + 3));
         if (lane >= 16) {
 #pragma unroll
             for (int q = 0; q < 4; q++)
-                *reinterpret_cast<float4 *>(Lo + kL32 + (i - 48) * 20 + 4 * q) =
+                *reinterpret_cast<float4 *>(W + kL32 + (i - 48) * 20 + 4 * q) =
                     make_float4(lval(32 + 4 * q), lval(33 + 4 * q), lval(34 + 4 * q), lval(35 + 4 * q));
         }
     }
@@ -531,82 +532,93 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
 // prep, group I (warps 8-11): block merges of the inverse on the warp MMA,
 // M = T diag(beta), MMA-b, and the -W' conversion
 // =============================================================================
+// Block merges of (I + L)^-1 on the warp MMA (3 x tf32), from the fp32 blocks
+// X0..X3 and the L blocks; the merged blocks go to the fp16 operand T16 (and,
+// for T10/T32, which level 2 reads again, to the fp32 block store).
+//   level 1: T10 = -X1 (L10 X0),  T32 = -X3 (L32 X2)
+//   level 2: T[32:64, 0:32] = -T[32:64, 32:64] (L[32:64, 0:32] T[0:32, 0:32])
 __device__ void i_merge(const Smem &sm, int s, int it)
 {
     const int iw = it >> 5, lane = it & 31, g = lane >> 2, t = lane & 3;
     const uint32_t st = s * kStageBytes;
-    float *Tm = sm.ptr<float>(st + kOffW);
-    const float *Lo = sm.ptr<float>(st + kOffM);
+    float *W = sm.ptr<float>(st + kOffW);
+    uint8_t *T16 = sm.base + st + kOffM;
     float *P1 = sm.ptr<float>(kOffP);            // [2][16][24]
     float *P2 = P1;                              // [32][40] once P1 is dead
-    // level 1: P = L10 X0 (or L32 X2), then T10 = -X1 P (or T32 = -X3 P)
+    auto put16 = [&](int r, int c, float v0, float v1) {   // c even
+        *reinterpret_cast<uint32_t *>(T16 + sw128_chunk(r, c >> 3) + 2 * (c & 7)) = pack_f16x2(v0, v1);
+    };
     {
         const int bl = iw >> 1, nt = iw & 1;
-        const int r0 = 32 * bl + 16, c0 = 32 * bl;
-        const float *Lb = Lo + (bl ? kL32 : kL10);
+        const float *Lb = W + (bl ? kL32 : kL10);
+        const float *Xc = W + kTcX + (2 * bl) * 320;
+        const float *Xr = W + kTcX + (2 * bl + 1) * 320;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         tile_mma(d, [&](int rr, int kk) { return Lb[rr * 20 + kk]; },
-                 [&](int kk, int cc) { return Tm[rot64(c0 + kk, c0 + 8 * nt + cc)]; }, nt, 2, lane);
+                 [&](int kk, int cc) { return Xc[kk * 20 + 8 * nt + cc]; }, nt, 2, lane);
         float *P = P1 + bl * 384;
         *reinterpret_cast<float2 *>(P + g * 24 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
         *reinterpret_cast<float2 *>(P + (g + 8) * 24 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
         named_bar(kBarI, kGroupThreads);
         float e[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(e, [&](int rr, int kk) { return Tm[rot64(r0 + rr, r0 + kk)]; },
+        tile_mma(e, [&](int rr, int kk) { return Xr[rr * 20 + kk]; },
                  [&](int kk, int cc) { return P[kk * 24 + 8 * nt + cc]; }, 0, 2, lane);
-        *reinterpret_cast<float2 *>(Tm + rot64(r0 + g, c0 + 8 * nt + 2 * t)) = make_float2(-e[0], -e[1]);
-        *reinterpret_cast<float2 *>(Tm + rot64(r0 + g + 8, c0 + 8 * nt + 2 * t)) = make_float2(-e[2], -e[3]);
+        float *To = W + kTcT + bl * 320;
+        *reinterpret_cast<float2 *>(To + g * 20 + 8 * nt + 2 * t) = make_float2(-e[0], -e[1]);
+        *reinterpret_cast<float2 *>(To + (g + 8) * 20 + 8 * nt + 2 * t) = make_float2(-e[2], -e[3]);
+        const int r0 = 32 * bl + 16, c0 = 32 * bl;
+        put16(r0 + g, c0 + 8 * nt + 2 * t, -e[0], -e[1]);
+        put16(r0 + g + 8, c0 + 8 * nt + 2 * t, -e[2], -e[3]);
     }
     named_bar(kBarI, kGroupThreads);
-    // level 2: P2 = L[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] P2
+    // level 2: each warp one 16-row slab mt and two 8-column tiles n0, n0+1
+    // sharing the A fragment (two independent accumulation chains)
+    const int mt = iw >> 1, n0 = 2 * (iw & 1);
+    {
+        auto T01 = [&](int kk, int cc) -> float {           // T[0:32, 0:32]
+            if (kk < 16) return cc < 16 ? W[kTcX + kk * 20 + cc] : 0.f;
+            return cc < 16 ? W[kTcT + (kk - 16) * 20 + cc] : W[kTcX + 320 + (kk - 16) * 20 + (cc - 16)];
+        };
+        const float *L2 = W + kL2;
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int tt = 0; tt < 2; tt++) {
-        const int tile = 2 * iw + tt, mt = tile >> 2, nt = tile & 3;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(d, [&](int rr, int kk) { return Lo[kL2 + (16 * mt + rr) * 36 + kk]; },
-                 [&](int kk, int cc) { return Tm[rot64(kk, 8 * nt + cc)]; }, nt, 4, lane);
-        *reinterpret_cast<float2 *>(P2 + (16 * mt + g) * 40 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
-        *reinterpret_cast<float2 *>(P2 + (16 * mt + g + 8) * 40 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
-    }
-    named_bar(kBarI, kGroupThreads);
-#pragma unroll
-    for (int tt = 0; tt < 2; tt++) {
-        const int tile = 2 * iw + tt, mt = tile >> 2, nt = tile & 3;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(d, [&](int rr, int kk) { return Tm[rot64(32 + 16 * mt + rr, 32 + kk)]; },
-                 [&](int kk, int cc) { return P2[kk * 40 + 8 * nt + cc]; }, 0, 2 * mt + 2, lane);
-        *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g, 8 * nt + 2 * t)) = make_float2(-d[0], -d[1]);
-        *reinterpret_cast<float2 *>(Tm + rot64(32 + 16 * mt + g + 8, 8 * nt + 2 * t)) = make_float2(-d[2], -d[3]);
-    }
-    named_bar(kBarI, kGroupThreads);
-}
-
-// M = T diag(beta) (T unit lower triangular) -> fp16 K-major [r][j]
-__device__ void i_make_m(const Smem &sm, int s, int it)
-{
-    const uint32_t st = s * kStageBytes;
-    const float *Tm = sm.ptr<float>(st + kOffW);
-    const float *bt = sm.ptr<float>(kOffConst + s * kConstBytes) + 256;
-    uint8_t *Mt = sm.base + st + kOffM;
-    const int r = it >> 1, hh = it & 1;
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-        const int j0 = 32 * hh + 8 * q;
-        const float4 t0 = *reinterpret_cast<const float4 *>(Tm + rot64(r, j0));
-        const float4 t1 = *reinterpret_cast<const float4 *>(Tm + rot64(r, j0 + 4));
-        const float4 b0 = *reinterpret_cast<const float4 *>(bt + j0);
-        const float4 b1 = *reinterpret_cast<const float4 *>(bt + j0 + 4);
-        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-        float mv[8];
-#pragma unroll
-        for (int e = 0; e < 8; e++) {
-            const int j = j0 + e;
-            mv[e] = ((j < r) ? tv[e] : (j == r ? 1.f : 0.f)) * bv[e];
+        for (int ks = 0; ks < 4; ks++) {
+            if (ks < n0) continue;
+            const int r = 16 * mt + g, k0 = 8 * ks + t;
+            const float a[4] = {L2[r * 36 + k0], L2[(r + 8) * 36 + k0], L2[r * 36 + k0 + 4], L2[(r + 8) * 36 + k0 + 4]};
+            const float b0[2] = {T01(k0, 8 * n0 + g), T01(k0 + 4, 8 * n0 + g)};
+            const float b1[2] = {T01(k0, 8 * n0 + 8 + g), T01(k0 + 4, 8 * n0 + 8 + g)};
+            mma_3xtf32(d0, a, b0);
+            mma_3xtf32(d1, a, b1);
         }
-        *reinterpret_cast<uint4 *>(Mt + sw128_chunk(r, 4 * hh + q)) =
-            make_uint4(pack_f16x2(mv[0], mv[1]), pack_f16x2(mv[2], mv[3]), pack_f16x2(mv[4], mv[5]),
-                       pack_f16x2(mv[6], mv[7]));
+        const int r = 16 * mt + g;
+        *reinterpret_cast<float2 *>(P2 + r * 40 + 8 * n0 + 2 * t) = make_float2(d0[0], d0[1]);
+        *reinterpret_cast<float2 *>(P2 + (r + 8) * 40 + 8 * n0 + 2 * t) = make_float2(d0[2], d0[3]);
+        *reinterpret_cast<float2 *>(P2 + r * 40 + 8 * n0 + 8 + 2 * t) = make_float2(d1[0], d1[1]);
+        *reinterpret_cast<float2 *>(P2 + (r + 8) * 40 + 8 * n0 + 8 + 2 * t) = make_float2(d1[2], d1[3]);
+    }
+    named_bar(kBarI, kGroupThreads);
+    {
+        auto T23 = [&](int rr, int kk) -> float {           // T[32:64, 32:64]
+            if (rr < 16) return kk < 16 ? W[kTcX + 640 + rr * 20 + kk] : 0.f;
+            return kk < 16 ? W[kTcT + 320 + (rr - 16) * 20 + kk] : W[kTcX + 960 + (rr - 16) * 20 + (kk - 16)];
+        };
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 4; ks++) {
+            if (ks > 2 * mt + 1) continue;
+            const int rr = 16 * mt + g, k0 = 8 * ks + t;
+            const float a[4] = {T23(rr, k0), T23(rr + 8, k0), T23(rr, k0 + 4), T23(rr + 8, k0 + 4)};
+            const float b0[2] = {P2[k0 * 40 + 8 * n0 + g], P2[(k0 + 4) * 40 + 8 * n0 + g]};
+            const float b1[2] = {P2[k0 * 40 + 8 * n0 + 8 + g], P2[(k0 + 4) * 40 + 8 * n0 + 8 + g]};
+            mma_3xtf32(d0, a, b0);
+            mma_3xtf32(d1, a, b1);
+        }
+        const int r = 32 + 16 * mt + g;
+        put16(r, 8 * n0 + 2 * t, -d0[0], -d0[1]);
+        put16(r + 8, 8 * n0 + 2 * t, -d0[2], -d0[3]);
+        put16(r, 8 * n0 + 8 + 2 * t, -d1[0], -d1[1]);
+        put16(r + 8, 8 * n0 + 8 + 2 * t, -d1[2], -d1[3]);
     }
 }
 
@@ -661,10 +673,7 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
             if (it == 0) KDA_PHASE(0, item, 5);
             i_merge(sm, s, it);
             if (it == 0) KDA_PHASE(0, item, 6);
-            i_make_m(sm, s, it);
-            if (it == 0) KDA_PHASE(0, item, 10);
             fence_proxy_async_smem();
-            if (it == 0) KDA_PHASE(0, item, 11);
             named_bar(kBarI, kGroupThreads);
             if (it == 0) {
                 KDA_PHASE(0, item, 7);
@@ -721,12 +730,14 @@ __device__ bool cursor_issue(LoadCursor &L, const TcParams &p, const Smem &sm, c
     const uint32_t st = sm.u32(s * kStageBytes);
     const uint32_t bar = sm.bar(kBarRawFull + s);
     mbar_arrive_expect_tx(bar, kRawBytes);
+    // k and q: one box per 64-channel half (the halves interleave with each
+    // other in shared memory); v and g: one 4-D box each, channel blocks outermost
     for (int kb = 0; kb < 2; kb++) {
         tma_load_3d(st + kOffKQ + kb * 16384, m.k, 64 * kb, L.un.h, row0, bar);
         tma_load_3d(st + kOffKQ + kb * 16384 + 8192, m.q, 64 * kb, L.un.h, row0, bar);
-        tma_load_3d(st + kOffV + kb * 8192, m.v, 64 * kb, L.un.h, row0, bar);
     }
-    for (int cb = 0; cb < 4; cb++) tma_load_3d(st + kOffGX + cb * 8192, m.g, 32 * cb, L.un.h, row0, bar);
+    tma_load_4d(st + kOffV, m.v, 0, row0, 0, L.un.h, bar);
+    tma_load_4d(st + kOffGX, m.g, 0, row0, 0, L.un.h, bar);
     L.c++;
     L.item++;
     return true;
@@ -1066,6 +1077,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+// [T][H][128] viewed as 4-D {c (box_inner wide), row, channel block, head}:
+// one box {box_inner, 64 rows, 128/box_inner blocks, 1} lands as
+// [block][row][c] in shared memory -- the 128B-swizzled tiles, blocks apart.
+bool make_map4(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem, int T, int H, int box_inner)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int nblk = kD / box_inner;
+    cuuint64_t dims[4] = {(cuuint64_t)box_inner, (cuuint64_t)T, (cuuint64_t)nblk, (cuuint64_t)H};
+    cuuint64_t strides[3] = {(cuuint64_t)H * kD * elem, (cuuint64_t)box_inner * elem, (cuuint64_t)kD * elem};
+    cuuint32_t box[4] = {(cuuint32_t)box_inner, (cuuint32_t)kChunk, (cuuint32_t)nblk, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem, int T, int H, int box_inner)
 {
     auto fn = encode_fn();
@@ -1088,8 +1116,8 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     if (a.T > 0) {
         if (!make_map(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
             !make_map(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
-            !make_map(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
-            !make_map(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32))
+            !make_map4(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
+            !make_map4(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32))
             return cudaErrorInvalidValue;
     }
     static int attr_set[64] = {0};
