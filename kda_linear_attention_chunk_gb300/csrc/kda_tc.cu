@@ -292,11 +292,11 @@ __device__ void e_scan(const TcParams &p, const Smem &sm, int s, int item, const
         if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = G;
         if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = G;
     }
+    if (et < kChunk) cst[256 + et] = beta_r;    // read by the operand pass right after the barrier
     named_bar(kBarE, kGroupThreads);
     // chain constants, one thread per key channel
     cst[et] = __expf(gmx[et]);                                                  // view from row m
     sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = __expf(glx[et] - gmx[et]);  // row m -> last row
-    if (et < kChunk) cst[256 + et] = beta_r;
 }
 
 // Kp = K*exp(G - G_m), Qp = Q*exp(G - G_m), Km = K*exp(G_m - G) as fp16, in
