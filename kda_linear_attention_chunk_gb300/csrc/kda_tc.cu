@@ -68,41 +68,50 @@ constexpr int kBarChain = 1, kBarE = 2, kBarI = 3;   // named barriers
 constexpr int kMaxSortedSeqs = 256;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----------------------
-constexpr uint32_t kStageBytes = 98304;
-constexpr uint32_t kOffKQ = 0;          // [kb][K rows 0-63 | Q rows 0-63], 2 x 16 KB
+// Two 72 KB stages hold what lives from a chunk's k/q/v loads until the chain's
+// MMAs on it are done; g, T16 and group I's fp32 blocks are single shared
+// buffers because only one chunk at a time uses them.
+constexpr uint32_t kStageBytes = 73728;
+constexpr uint32_t kOffKQ = 0;          // [kb][K rows 0-63 | Q rows 0-63], 2 x 16 KB; K later -W' [c][r]
 constexpr uint32_t kOffKM = 32768;      // Km, 2 x 8 KB
-constexpr uint32_t kOffV = 49152;       // V (fp16 in place of bf16), 2 x 8 KB
-constexpr uint32_t kOffGX = 65536;      // g (fp32, 4 x 8 KB); later M | B | W' (and T)
-constexpr uint32_t kOffM = kOffGX;              // M [r][j] fp16, 8 KB (off-diagonal L blocks before)
-constexpr uint32_t kOffB = kOffGX + 8192;       // tril(A_qk) [r][i] fp16, 8 KB
-constexpr uint32_t kOffW = kOffGX + 16384;      // -W' [c][r] fp16, 16 KB (T fp32 before)
-constexpr uint32_t kOffEScr = 2 * kStageBytes;  // 196608: group E scan exchange, 2 KB
+constexpr uint32_t kOffV = 49152;       // V (fp16 in place of bf16), 2 x 8 KB; later the output transpose
+constexpr uint32_t kOffB = 65536;       // tril(A_qk) [r][i] fp16, 8 KB
+constexpr uint32_t kOffG = 2 * kStageBytes;     // g slot (fp32, 4 x 8 KB), read once by the decay scan
+constexpr uint32_t kOffT16 = kOffG + 32768;     // T = (I + A_kk)^-1 [r][j] fp16, 8 KB (MMA-b operand)
+constexpr uint32_t kOffTmp = kOffT16 + 8192;    // group I fp32 blocks of the inverse, 16 KB
+constexpr uint32_t kOffEScr = kOffTmp + 16384;  // group E scan exchange, 2 KB
 constexpr uint32_t kOffP = kOffEScr + 2048;     // group I merge temporaries, 6 KB
-constexpr uint32_t kOffConst = kOffP + 6144;    // per stage: fm[128] pend[128] beta[64]
+constexpr uint32_t kOffConst = kOffP + 6144;    // per stage: fm[128] | unused | beta[64]
 constexpr uint32_t kConstBytes = 1280;
 constexpr uint32_t kOffGm = kOffConst + 2 * kConstBytes;   // G_m[128], G_last[128]
 constexpr uint32_t kOffOrder = kOffGm + 1024;              // sorted order, then {bos, eos} per sequence
 constexpr uint32_t kOffBar = kOffOrder + 12 * kMaxSortedSeqs;
-constexpr uint32_t kOffMisc = kOffBar + 128;
+constexpr uint32_t kOffMisc = kOffBar + 256;     // TMEM base, abort flag, schedule length, schedule
 // pend = exp(G_last - G_m) of chunk i lives in slot i % 3: the chain reads it at
-// the start of chunk i+1 (or at the end of the unit), after chunk i's stage has
-// already been handed back, and only chunk i+3's prep can overwrite it.
-constexpr uint32_t kOffPend = kOffMisc + 64;
-constexpr uint32_t kOffOT = kOffPend + 3 * 512;            // output transpose, bf16 [64][128]
-constexpr uint32_t kSmemBytes = kOffOT + 16384 + 1024;     // + alignment slack
+// the start of chunk i+1 (or at the end of the unit), and only chunk i+3's
+// decay scan, which waits for chunk i+1's stage, can overwrite it.
+constexpr uint32_t kOffPend = kOffMisc + 128;
+constexpr uint32_t kSmemBytes = kOffPend + 3 * 512 + 1024;   // + alignment slack
 
-// mbarrier slots
-constexpr int kBarRawFull = 0;     // [2]
-constexpr int kBarPrepDone = 4;    // [2]
-constexpr int kBarAFull = 6, kBarWFull = 7, kBarMma1 = 8, kBarMma3 = 9, kBarDrain = 10;
-constexpr int kBarEDone = 11;      // [2]: group E finished a chunk (A readout, diagonal inverses)
-constexpr int kBarODone = 13;      // [2]: the chain has stored a chunk's outputs (TMEM P_s free)
-constexpr int kBarMmaO = 15;       // all of a chunk's output MMAs are done
+// mbarrier slots ([2] = one per stage)
+constexpr int kBarKQFull = 0;      // [2]: k, q tiles landed
+constexpr int kBarVFull = 2;       // [2]: v tile landed
+constexpr int kBarPrepDone = 4;    // [2]: prep finished a chunk (-W' written)
+constexpr int kBarAFull = 6;       // [2]: MMA-a done
+constexpr int kBarEDone = 8;       // [2]: group E finished a chunk's operands (128 arrivals)
+constexpr int kBarODone = 10;      // [2]: the chain has read a chunk's outputs (TMEM P_s free)
+constexpr int kBarFmReady = 12;    // [2]: the chunk's decay constants are written (128 arrivals)
+constexpr int kBarKmFree = 14;     // [2]: the chain's MMAs on the stage are done (Km, B free)
+constexpr int kBarGFull = 16;      // g slot landed
+constexpr int kBarWFull = 17, kBarMma1 = 18, kBarMma1O = 19, kBarMma3 = 20, kBarDrain = 21;
+constexpr int kMaxRounds = 24;     // longest per-CTA unit list of the balanced deal
 
 // TMEM columns
 constexpr uint32_t kTmS = 0, kTmP = 128, kTmS0h = 384, kTmDh = 448, kTmCols = 512;
 
-constexpr uint32_t kRawBytes = 10 * 8192;       // q, k, v (2 boxes each) + g (4 boxes)
+constexpr uint32_t kKQBytes = 4 * 8192;        // k and q tiles (bf16)
+constexpr uint32_t kVBytes = 2 * 8192;         // v tile (bf16)
+constexpr uint32_t kGBytes = 4 * 8192;         // g tile (fp32)
 
 struct TcParams {
     const int32_t *cu;
@@ -122,6 +131,8 @@ struct Smem {
     __device__ uint32_t bar(int i) const { return u32(kOffBar + 8 * i); }
     __device__ volatile int *abort_flag() const { return ptr<volatile int>(kOffMisc + 4); }
     __device__ uint32_t *tmem_base() const { return ptr<uint32_t>(kOffMisc); }
+    __device__ int *sched_len() const { return ptr<int>(kOffMisc + 8); }   // -1: snake deal
+    __device__ int *sched() const { return ptr<int>(kOffMisc + 16); }      // [kMaxRounds]
 };
 
 __device__ __forceinline__ bool role_any(bool pred, int id, int n)
@@ -167,20 +178,18 @@ __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, in
     return x;
 }
 
-// k-th unit of this CTA under a boustrophedon ("snake") deal of the
-// length-sorted unit list over the grid; -1 when exhausted.
-__device__ __forceinline__ int cta_unit(int k, int U)
+// k-th unit of this CTA, -1 when exhausted: the balanced deal made in the
+// prologue when there is one, else a boustrophedon ("snake") deal of the
+// length-sorted unit list over the grid.
+__device__ __forceinline__ int cta_unit(const Smem &sm, int k, int U)
 {
+    const int n = *sm.sched_len();
+    if (n >= 0) return k < n ? sm.sched()[k] : -1;
     const int G = gridDim.x, b = blockIdx.x;
     const int u = k * G + ((k & 1) ? (G - 1 - b) : b);
     return u < U ? u : -1;
 }
 
-// rotated index into a 64x64 fp32 matrix: row i starts 4*i words further
-// round the row, so an 8-row x 4-column block (a tf32 mma A fragment) or a
-// quarter-warp reading 8 rows x 16 bytes touches distinct banks; groups of
-// 4 consecutive columns stay contiguous and 16-byte aligned.
-__device__ __forceinline__ int rot64(int i, int j) { return i * 64 + ((j + 4 * i) & 63); }
 
 // byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
@@ -243,115 +252,184 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
 }
 
 // =============================================================================
-// prep, group E (warps 4-7): cumulative log-decay, decay-scaled operands,
-// MMA-a, the A readout and the 16x16 diagonal inverses
+// TMA loads.  The chain's elected thread loads k, q and v into the stages (the
+// first two chunks at the start, then chunk i+2 as soon as chunk i has released
+// the regions: k and q after MMA1, v after the output store); group E's first
+// thread loads g into the single g slot as soon as the decay scan has read the
+// previous chunk's g.
 // =============================================================================
-// L_off: the off-diagonal blocks of L the merges need, kept in the stage's M
-// region until M is written: L10 [16][20], L32 [16][20], L[32:64, 0:32] [32][36]
-// (row strides chosen so warp-MMA A fragments hit distinct banks).
-// fp32 block store in the stage's W region (until W' is written): X0..X3 (the
-// 16x16 diagonal inverses) and T10, T32, each [16][20]; then the off-diagonal
-// L blocks L10 [16][20], L32 [16][20] and L[32:64, 0:32] [32][36].  Row strides
-// keep warp-MMA fragment loads (nearly) conflict-free.
-constexpr int kTcX = 0, kTcT = 1280, kL10 = 1920, kL32 = 2240, kL2 = 2560;
+struct Maps {
+    const CUtensorMap *q, *k, *v, *g;
+};
 
-__device__ void e_scan(const TcParams &p, const Smem &sm, int s, int item, const Unit &un, int row0, int L, int et)
+// Walks this CTA's chunks in schedule order.
+struct LoadCursor {
+    int k = -1, c = 0, item = 0;
+    bool done = false;
+    Unit un = {0, 0, 0, 0, 0};
+    int row0 = 0;
+};
+
+// Advances to the next chunk (its coordinates: row0, un.h; its index: item - 1);
+// false when the schedule is exhausted.
+__device__ bool cursor_next(LoadCursor &L, const TcParams &p, const Smem &sm, const int *order, int U)
+{
+    while (!L.done && L.c >= L.un.nchunks) {
+        const int u = cta_unit(sm, ++L.k, U);
+        if (u < 0) {
+            L.done = true;
+            break;
+        }
+        L.un = get_unit(p, order, u);
+        L.c = 0;
+    }
+    if (L.done) return false;
+    L.row0 = L.un.bos + L.c * kChunk;
+    L.c++;
+    L.item++;
+    return true;
+}
+
+// k and q of chunk `item`: one 3-D box per 64-channel half (the halves of k and
+// q interleave in shared memory)
+__device__ void issue_kq(const Smem &sm, const Maps &m, int item, int row0, int h)
+{
+    const uint32_t st = sm.u32((item & 1) * kStageBytes);
+    const uint32_t bar = sm.bar(kBarKQFull + (item & 1));
+    KDA_PHASE(2, item, 0);
+    mbar_arrive_expect_tx(bar, kKQBytes);
+    for (int kb = 0; kb < 2; kb++) {
+        tma_load_3d(st + kOffKQ + kb * 16384, m.k, 64 * kb, h, row0, bar);
+        tma_load_3d(st + kOffKQ + kb * 16384 + 8192, m.q, 64 * kb, h, row0, bar);
+    }
+}
+
+// v of chunk `item`: one 4-D box, channel blocks outermost
+__device__ void issue_v(const Smem &sm, const Maps &m, int item, int row0, int h)
+{
+    const uint32_t bar = sm.bar(kBarVFull + (item & 1));
+    mbar_arrive_expect_tx(bar, kVBytes);
+    tma_load_4d(sm.u32((item & 1) * kStageBytes + kOffV), m.v, 0, row0, 0, h, bar);
+}
+
+// g of the next chunk into the g slot: one 4-D box of four 32-channel blocks
+__device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
+{
+    const uint32_t bar = sm.bar(kBarGFull);
+    mbar_arrive_expect_tx(bar, kGBytes);
+    tma_load_4d(sm.u32(kOffG), m.g, 0, row0, 0, h, bar);
+}
+
+// =============================================================================
+// prep, group E (warps 4-7): cumulative log-decay, the decay-scaled operands,
+// MMA-a and beta*V.  Loops are kept rolled: each warp runs its loop bodies
+// once per chunk next to two other roles, so compact code matters more than
+// unrolling.
+// =============================================================================
+
+// Group E's decay pass over one chunk; `beta_r` is the beta of row et (zero
+// past the chunk), loaded a chunk ahead.
+// Scan: thread = (row group ew: rows 16*ew .. +15) x (key channels 4*lane ..
+// +3); the row prefix runs in registers, the four row groups exchange their
+// totals once, and G is written back over g in the g slot.
+// Operands: thread = (row 16*ew + 8*hf + (lane & 7)) x (channels 32*cg + 8*j ..
+// +7, cg = lane >> 3), 16-byte accesses; Kp = beta*K*exp(G - G_m),
+// Qp = Q*exp(G - G_m) and Km = K*exp(G_m - G) become fp16 in place over the
+// bf16 tiles (rows past the chunk zero).  Returns false if a wait ran out.
+__device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r)
 {
     const int ew = et >> 5, lane = et & 31;
     const uint32_t st = s * kStageBytes;
     float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
-    float4 *xchg = sm.ptr<float4>(kOffEScr);            // [4 row groups][32 chunk columns]
     float *gmx = sm.ptr<float>(kOffGm), *glx = gmx + 128;
     const int m = (L - 1) >> 1;
-    const float beta_r = (et < L) ? __ldg(p.beta + (size_t)(row0 + et) * p.H + un.h) : 0.f;   // issued early
-    // thread = (row group ew: rows 16*ew .. +15) x (4 channels 4*lane .. +3)
-    uint8_t *gb = sm.base + st + kOffGX + (lane >> 3) * 8192;
-    const int jc = lane & 7;
-    float4 x[16];
+    {
+        float4 *xchg = sm.ptr<float4>(kOffEScr);            // [4 row groups][32 channel quads]
+        uint8_t *gb = sm.base + kOffG + (lane >> 3) * 8192;
+        const int jc = lane & 7;
+        float4 x[16];
 #pragma unroll
-    for (int t = 0; t < 16; t++) {
-        const int r = 16 * ew + t;
-        x[t] = r < L ? *reinterpret_cast<const float4 *>(gb + sw128_chunk(r, jc)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+        for (int t = 0; t < 16; t++) {
+            const int r = 16 * ew + t;
+            x[t] = r < L ? *reinterpret_cast<const float4 *>(gb + sw128_chunk(r, jc)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-    for (int t = 1; t < 16; t++) {
-        x[t].x += x[t - 1].x; x[t].y += x[t - 1].y; x[t].z += x[t - 1].z; x[t].w += x[t - 1].w;
+        for (int t = 1; t < 16; t++) {
+            x[t].x += x[t - 1].x; x[t].y += x[t - 1].y; x[t].z += x[t - 1].z; x[t].w += x[t - 1].w;
+        }
+        xchg[ew * 32 + lane] = x[15];
+        named_bar(kBarE, kGroupThreads);
+        float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < ew; w++) {
+            const float4 y = xchg[w * 32 + lane];
+            pre.x += y.x; pre.y += y.y; pre.z += y.z; pre.w += y.w;
+        }
+#pragma unroll
+        for (int t = 0; t < 16; t++) {
+            x[t].x += pre.x; x[t].y += pre.y; x[t].z += pre.z; x[t].w += pre.w;
+            const int r = 16 * ew + t;
+            *reinterpret_cast<float4 *>(gb + sw128_chunk(r, jc)) = x[t];
+            if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = x[t];
+            if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = x[t];
+        }
     }
-    xchg[ew * 32 + lane] = x[15];
+    if (et < kChunk) cst[256 + et] = beta_r;
     named_bar(kBarE, kGroupThreads);
-    float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < ew; w++) {
-        const float4 y = xchg[w * 32 + lane];
-        pre.x += y.x; pre.y += y.y; pre.z += y.z; pre.w += y.w;
-    }
-#pragma unroll
-    for (int t = 0; t < 16; t++) {
-        const int r = 16 * ew + t;
-        float4 G = make_float4(x[t].x + pre.x, x[t].y + pre.y, x[t].z + pre.z, x[t].w + pre.w);
-        *reinterpret_cast<float4 *>(gb + sw128_chunk(r, jc)) = G;
-        if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = G;
-        if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = G;
-    }
-    if (et < kChunk) cst[256 + et] = beta_r;    // read by the operand pass right after the barrier
-    named_bar(kBarE, kGroupThreads);
+    // k and q of this chunk have landed -- so the chain is past its MMA1 of chunk
+    // item-2 and no longer reads that chunk's fm or pend slot -- and Km of chunk
+    // item-2 is no longer read
+    if (et == 0) KDA_PHASE(0, item, 15);
+    bool ok = mbar_wait(sm.bar(kBarKQFull + s), (item >> 1) & 1, sm.abort_flag());
+    if (ok && item >= 2) ok = mbar_wait(sm.bar(kBarKmFree + s), ((item >> 1) - 1) & 1, sm.abort_flag());
+    if (role_any(!ok, kBarE, kGroupThreads)) return false;
+    if (et == 0) KDA_PHASE(0, item, 14);
     // chain constants, one thread per key channel
     cst[et] = __expf(gmx[et]);                                                  // view from row m
     sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = __expf(glx[et] - gmx[et]);  // row m -> last row
-}
-
-// Kp = K*exp(G - G_m), Qp = Q*exp(G - G_m), Km = K*exp(G_m - G) as fp16, in
-// place over the bf16 tiles; rows past the chunk become zero.
-__device__ void e_operands(const Smem &sm, int s, int L, int et)
-{
-    const int ew = et >> 5, lane = et & 31;
-    const int rr = lane & 7, cg = lane >> 3;
-    const uint32_t st = s * kStageBytes;
-    const float *gmx = sm.ptr<float>(kOffGm);
-    const float *bt = sm.ptr<float>(kOffConst + s * kConstBytes) + 256;
-    const int kb = cg >> 1;
+    mbar_arrive(sm.bar(kBarFmReady + s));
+    const int rr = lane & 7, cg = lane >> 3, kb = cg >> 1;
     uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
     uint8_t *qt = kt + 8192;
     uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
-    const uint8_t *gt = sm.base + st + kOffGX + cg * 8192;
+    const uint8_t *gt = sm.base + kOffG + cg * 8192;
 #pragma unroll 1
-    for (int hf = 0; hf < 2; hf++) {
-        const int r = 16 * ew + 8 * hf + rr;
+    for (int step = 0; step < 8; step++) {
+        const int j = step & 3;
+        const int r = 16 * ew + 8 * (step >> 2) + rr;
         const bool valid = r < L;
-        const float br = bt[r];                    // beta_r (0 past the chunk)
+        const float br = cst[256 + r];                 // zero past the chunk
+        const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
+        const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
+        const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
+        const float4 m1 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j + 4);
+        const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
+        const uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
+        const uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
+        const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
+        const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
+        uint32_t okp[4], okm[4], oqp[4];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
-            const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
-            const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
-            const float4 m1 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j + 4);
-            const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-            const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
-            const uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
-            const uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
-            const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
-            const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
-            uint32_t okp[4], okm[4], oqp[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-                if (valid) {
-                    a0 = __expf(G[2 * e] - M[2 * e]);
-                    a1 = __expf(G[2 * e + 1] - M[2 * e + 1]);
-                    b0 = __expf(M[2 * e] - G[2 * e]);
-                    b1 = __expf(M[2 * e + 1] - G[2 * e + 1]);
-                }
-                const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
-                const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
-                okp[e] = pack_f16x2(k0 * (a0 * br), k1 * (a1 * br));
-                okm[e] = pack_f16x2(k0 * b0, k1 * b1);
-                oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
+        for (int e = 0; e < 4; e++) {
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+            if (valid) {
+                a0 = __expf(G[2 * e] - M[2 * e]);
+                a1 = __expf(G[2 * e + 1] - M[2 * e + 1]);
+                b0 = __expf(M[2 * e] - G[2 * e]);
+                b1 = __expf(M[2 * e + 1] - G[2 * e + 1]);
             }
-            *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
-            *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
-            *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
+            const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
+            const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
+            okp[e] = pack_f16x2(k0 * (a0 * br), k1 * (a1 * br));
+            okm[e] = pack_f16x2(k0 * b0, k1 * b1);
+            oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
         }
+        *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
+        *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
+        *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
     }
+    return true;
 }
 
 // value tile bf16 -> beta_r * v as fp16, in place; rows past the chunk become zero
@@ -359,7 +437,7 @@ __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
 {
     uint8_t *vt = sm.base + s * kStageBytes + kOffV;
     const float *bt = sm.ptr<float>(kOffConst + s * kConstBytes) + 256;
-#pragma unroll
+#pragma unroll 2
     for (int i = 0; i < 8; i++) {
         const int idx = et + 128 * i;              // 16-byte chunk index in the 16 KB tile
         const int r = (idx >> 3) & 63;
@@ -367,103 +445,10 @@ __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
         const uint4 w = *ptr;
         const uint32_t in[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[4];
-#pragma unroll
         const float br = bt[r];
+#pragma unroll
         for (int e = 0; e < 4; e++) o[e] = r < L ? pack_f16x2(bf16lo(in[e]) * br, bf16hi(in[e]) * br) : 0u;
         *ptr = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-}
-
-// forward substitution of one 16x16 unit lower triangular block held one row
-// per lane in 16-lane groups: x = row `a` of (I + Lb)^-1
-__device__ __forceinline__ void diag_inverse16(const float (&Lr)[16], float (&x)[16], int a, int lane)
-{
-#pragma unroll
-    for (int q = 0; q < 16; q++) x[q] = (q == a) ? 1.f : 0.f;
-#pragma unroll
-    for (int a2 = 0; a2 < 15; a2++) {
-        const int src = (lane & 16) | a2;
-#pragma unroll
-        for (int col = 0; col <= a2; col++) {
-            const float xs = __shfl_sync(0xffffffffu, x[col], src);
-            if (a > a2) x[col] -= Lr[a2] * xs;
-        }
-    }
-}
-
-// A readout.  Lanes 64-127 (A_qk rows r): lower part, diagonal included -> B
-// (fp16 [r][i]).  Lanes 0-63 (A_kk rows i; beta_i is folded into Kp, so this
-// already is the beta-scaled A_kk): the strict lower part L_i stays in
-// registers; the inverse X of its 16x16 diagonal block goes to the fp32 block
-// store and, followed by zeros, to the fp16 operand T16; the off-diagonal L
-// blocks the merges need go next to the fp32 blocks.
-__device__ void e_read_a(const Smem &sm, int s, uint32_t tmem, int et, int item)
-{
-    const int ew = et >> 5, lane = et & 31;
-    const uint32_t st = s * kStageBytes;
-    uint32_t a[64];
-    const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * ew) << 16);
-    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(a));
-    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-    tmem_wait_ld();
-    if (ew >= 2) {
-        const int r = 32 * (ew - 2) + lane;
-        uint8_t *Bt = sm.base + st + kOffB;
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int i0 = 8 * q + 2 * e;
-                const float x0 = (i0 <= r) ? __uint_as_float(a[i0]) : 0.f;
-                const float x1 = (i0 + 1 <= r) ? __uint_as_float(a[i0 + 1]) : 0.f;
-                w[e] = pack_f16x2(x0, x1);
-            }
-            *reinterpret_cast<uint4 *>(Bt + sw128_chunk(r, q)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        return;
-    }
-    const int i = 32 * ew + lane, blk = i >> 4, a16 = i & 15;
-    auto lval = [&](int j) { return (j < i) ? __uint_as_float(a[j]) : 0.f; };
-    float Lr[16], x[16];
-    if (ew == 0) {
-#pragma unroll
-        for (int t = 0; t < 16; t++) Lr[t] = (lane & 16) ? lval(16 + t) : lval(t);
-    } else {
-#pragma unroll
-        for (int t = 0; t < 16; t++) Lr[t] = (lane & 16) ? lval(48 + t) : lval(32 + t);
-    }
-    if (et == 0) KDA_PHASE(0, item, 12);
-    diag_inverse16(Lr, x, a16, lane);
-    if (et == 0) KDA_PHASE(0, item, 13);
-    float *W = sm.ptr<float>(st + kOffW);
-    float *xb = W + kTcX + blk * 320 + a16 * 20;
-#pragma unroll
-    for (int q = 0; q < 4; q++) *reinterpret_cast<float4 *>(xb + 4 * q) = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-    uint8_t *T16 = sm.base + st + kOffM;
-    *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, 2 * blk)) =
-        make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]), pack_f16x2(x[6], x[7]));
-    *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, 2 * blk + 1)) =
-        make_uint4(pack_f16x2(x[8], x[9]), pack_f16x2(x[10], x[11]), pack_f16x2(x[12], x[13]), pack_f16x2(x[14], x[15]));
-    for (int q = 2 * blk + 2; q < 8; q++) *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, q)) = make_uint4(0u, 0u, 0u, 0u);
-    if (ew == 0) {
-        if (lane >= 16) {                          // rows 16-31: L10 = L[16:32, 0:16]
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                *reinterpret_cast<float4 *>(W + kL10 + (i - 16) * 20 + 4 * q) =
-                    make_float4(lval(4 * q), lval(4 * q + 1), lval(4 * q + 2), lval(4 * q + 3));
-        }
-    } else {                                       // rows 32-63: L[32:64, 0:32]; rows 48-63 also L32
-#pragma unroll
-        for (int q = 0; q < 8; q++)
-            *reinterpret_cast<float4 *>(W + kL2 + (i - 32) * 36 + 4 * q) =
-                make_float4(lval(4 * q), lval(4 * q + 1), lval(4 * q + 2), lval(4 * q + 3));
-        if (lane >= 16) {
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                *reinterpret_cast<float4 *>(W + kL32 + (i - 48) * 20 + 4 * q) =
-                    make_float4(lval(32 + 4 * q), lval(33 + 4 * q), lval(34 + 4 * q), lval(35 + 4 * q));
-        }
     }
 }
 
@@ -480,69 +465,207 @@ __device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
     }
 }
 
-__device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int U)
+__device__ __forceinline__ float load_beta(const TcParams &p, const LoadCursor &c, int et)
+{
+    const int L = min(kChunk, c.un.eos - c.row0);
+    return et < L ? __ldg(p.beta + (size_t)(c.row0 + et) * p.H + c.un.h) : 0.f;
+}
+
+__device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps)
 {
     const int et = threadIdx.x - kChainThreads;
     const uint32_t tmem = *sm.tmem_base();
+    // g and the betas run one chunk ahead: `ahead` is the chunk whose g is in
+    // flight (every thread walks it; thread 0 issues the load)
+    LoadCursor ahead;
+    float beta_next = 0.f;
+    if (cursor_next(ahead, p, sm, order, U)) {
+        if (et == 0) {
+            KDA_PHASE(2, 0, 1);
+            issue_g(sm, maps, ahead.row0, ahead.un.h);
+        }
+        beta_next = load_beta(p, ahead, et);
+    }
     int item = 0;
     for (int k = 0;; k++) {
-        const int u = cta_unit(k, U);
+        const int u = cta_unit(sm, k, U);
         if (u < 0) break;
         const Unit un = get_unit(p, order, u);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
-            const int row0 = un.bos + c * kChunk;
-            const int L = min(kChunk, un.eos - row0);
-            bool ok = mbar_wait(sm.bar(kBarRawFull + s), (item >> 1) & 1, sm.abort_flag());
+            const uint32_t ph = (item >> 1) & 1;
+            const int L = min(kChunk, un.eos - (un.bos + c * kChunk));
+            const float beta_r = beta_next;
+            bool ok = mbar_wait(sm.bar(kBarGFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (et == 0) KDA_PHASE(0, item, 0);
-            e_scan(p, sm, s, item, un, row0, L, et);
-            e_operands(sm, s, L, et);
+            if (!e_pass(sm, s, item, L, et, beta_r)) {
+                if (et == 0) record_error(p, sm, kErrWaitTimeout);
+                return;
+            }
             fence_proxy_async_smem();
-            named_bar(kBarE, kGroupThreads);
+            named_bar(kBarE, kGroupThreads);               // operands written, the g slot read
             if (et == 0) {
                 KDA_PHASE(0, item, 1);
-                // TMEM P_s is free once the chain has stored chunk item-2's outputs
+                // TMEM P_s is free once the chain has read chunk item-2's outputs
                 if (item >= 2 && !mbar_wait(sm.bar(kBarODone + s), ((item >> 1) - 1) & 1, sm.abort_flag()))
                     record_error(p, sm, kErrWaitTimeout);
                 KDA_PHASE(0, item, 2);
                 tc_fence_after();
                 issue_mma_a(sm, s, tmem);
-                mma_commit(sm.bar(kBarAFull));
+                mma_commit(sm.bar(kBarAFull + s));
             }
+            if (cursor_next(ahead, p, sm, order, U)) {
+                if (et == 0) {
+                    KDA_PHASE(2, ahead.item - 1, 1);
+                    issue_g(sm, maps, ahead.row0, ahead.un.h);
+                }
+                beta_next = load_beta(p, ahead, et);
+            }
+            ok = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
+            if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             e_convert_v(sm, s, L, et);
             fence_proxy_async_smem();
-            ok = mbar_wait(sm.bar(kBarAFull), item & 1, sm.abort_flag());
-            if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (et == 0) KDA_PHASE(0, item, 3);
-            tc_fence_after();
-            e_read_a(sm, s, tmem, et, item);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar(kBarE, kGroupThreads);
-            if (et == 0) {
-                KDA_PHASE(0, item, 4);
-                mbar_arrive(sm.bar(kBarEDone + s));
-            }
+            mbar_arrive(sm.bar(kBarEDone + s));            // every operand of this chunk is written
+            if (et == 0) KDA_PHASE(0, item, 4);
         }
     }
 }
 
 // =============================================================================
-// prep, group I (warps 8-11): block merges of the inverse on the warp MMA,
-// M = T diag(beta), MMA-b, and the -W' conversion
+// prep, group I (warps 8-11): the A readout, the inverse T = (I + A_kk)^-1,
+// MMA-b and the -W' conversion
 // =============================================================================
-// Block merges of (I + L)^-1 on the warp MMA (3 x tf32), from the fp32 blocks
-// X0..X3 and the L blocks; the merged blocks go to the fp16 operand T16 (and,
-// for T10/T32, which level 2 reads again, to the fp32 block store).
-//   level 1: T10 = -X1 (L10 X0),  T32 = -X3 (L32 X2)
-//   level 2: T[32:64, 0:32] = -T[32:64, 32:64] (L[32:64, 0:32] T[0:32, 0:32])
-__device__ void i_merge(const Smem &sm, int s, int it)
+// fp32 blocks of the inverse in the shared kOffTmp region (float offsets):
+//   D0 = T[0:32, 0:32], D1 = T[32:64, 32:64]  dense [32][36] (upper-right 16x16 zero)
+//   L2 = L[32:64, 0:32] [32][36],  L10 = L[16:32, 0:16], L32 = L[48:64, 32:48] [16][20]
+// and, in the kOffP region while the diagonal blocks are solved, the four
+// 16x16 diagonal blocks of L, [4][16][20].  Row strides keep warp-MMA
+// fragment loads conflict-free.
+constexpr int kD0 = 0, kD1 = 1152, kL2 = 2304, kL10 = 3456, kL32 = 3776;
+
+// Inverse of the unit lower-triangular 16x16 block (I + Lb) by forward
+// substitution, one column per lane: x[r] = e_c[r] - sum_{j<r} Lb[r][j] x[j].
+// Lb is read from shared memory (rows zero right of the diagonal).
+__device__ __forceinline__ void solve_column16(const float *Lb, int c, float (&x)[16])
+{
+#pragma unroll
+    for (int r = 0; r < 16; r++) x[r] = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; r++) {
+        float s0 = (r == c) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < r; j += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(Lb + r * 20 + j);
+            s0 -= l4.x * x[j];
+            s1 -= l4.y * x[j + 1];
+            s2 -= l4.z * x[j + 2];
+            s3 -= l4.w * x[j + 3];
+        }
+        x[r] = (s0 + s1) + (s2 + s3);
+    }
+}
+
+// A readout.  Warps 10-11 (A_qk rows r): lower part, diagonal included -> B
+// (fp16 [r][i]).  Warps 8-9 (A_kk rows i; beta_i is folded into Kp, so this
+// already is the beta-scaled A_kk): the strictly lower part goes to the L
+// blocks; the 16x16 diagonal blocks are inverted column by column into D0/D1
+// and, as fp16, into T16.
+__device__ void i_read_a(const Smem &sm, int s, uint32_t tmem, int it, int item)
+{
+    const int ew = it >> 5, lane = it & 31;
+    uint32_t a[64];
+    const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * ew) << 16);
+    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(a));
+    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+    tmem_wait_ld();
+    if (ew >= 2) {
+        const int r = 32 * (ew - 2) + lane;
+        uint8_t *Bt = sm.base + s * kStageBytes + kOffB;
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int i0 = 8 * q + 2 * e;
+                const float x0 = (i0 <= r) ? __uint_as_float(a[i0]) : 0.f;
+                const float x1 = (i0 + 1 <= r) ? __uint_as_float(a[i0 + 1]) : 0.f;
+                w[e] = pack_f16x2(x0, x1);
+            }
+            *reinterpret_cast<uint4 *>(Bt + sw128_chunk(r, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        return;
+    }
+    const int i = 32 * ew + lane, blk = i >> 4, a16 = i & 15;
+    auto lval = [&](int j) { return (j < i) ? __uint_as_float(a[j]) : 0.f; };
+    float *W = sm.ptr<float>(kOffTmp);
+    float *Ld = sm.ptr<float>(kOffP) + blk * 320 + a16 * 20;
+    if (ew == 0) {
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            *reinterpret_cast<float4 *>(Ld + 4 * q) =
+                (lane & 16) ? make_float4(lval(16 + 4 * q), lval(17 + 4 * q), lval(18 + 4 * q), lval(19 + 4 * q))
+                            : make_float4(lval(4 * q), lval(1 + 4 * q), lval(2 + 4 * q), lval(3 + 4 * q));
+        if (lane >= 16) {                          // rows 16-31: L10 = L[16:32, 0:16]
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                *reinterpret_cast<float4 *>(W + kL10 + (i - 16) * 20 + 4 * q) =
+                    make_float4(lval(4 * q), lval(4 * q + 1), lval(4 * q + 2), lval(4 * q + 3));
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            *reinterpret_cast<float4 *>(Ld + 4 * q) =
+                (lane & 16) ? make_float4(lval(48 + 4 * q), lval(49 + 4 * q), lval(50 + 4 * q), lval(51 + 4 * q))
+                            : make_float4(lval(32 + 4 * q), lval(33 + 4 * q), lval(34 + 4 * q), lval(35 + 4 * q));
+        // rows 32-63: L[32:64, 0:32]; rows 48-63 also L32
+#pragma unroll
+        for (int q = 0; q < 8; q++)
+            *reinterpret_cast<float4 *>(W + kL2 + (i - 32) * 36 + 4 * q) =
+                make_float4(lval(4 * q), lval(4 * q + 1), lval(4 * q + 2), lval(4 * q + 3));
+        if (lane >= 16) {
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                *reinterpret_cast<float4 *>(W + kL32 + (i - 48) * 20 + 4 * q) =
+                    make_float4(lval(32 + 4 * q), lval(33 + 4 * q), lval(34 + 4 * q), lval(35 + 4 * q));
+        }
+    }
+    __syncwarp();
+    if (it == 0) KDA_PHASE(0, item, 12);
+    {   // lane = column c of diagonal block bb (this warp's two blocks)
+        const int c = lane & 15, bb = 2 * ew + (lane >> 4);
+        float x[16];
+        solve_column16(sm.ptr<float>(kOffP) + bb * 320, c, x);
+        float *D = W + (ew ? kD1 : kD0) + (lane >> 4) * (16 * 36 + 16);
+#pragma unroll
+        for (int r = 0; r < 16; r++) D[r * 36 + c] = x[r];
+    }
+    __syncwarp();
+    if (it == 0) KDA_PHASE(0, item, 13);
+    {   // row i of its diagonal block -> fp16 T16 (two 16-byte chunks)
+        const float *Dr = W + (ew ? kD1 : kD0) + lane * 36 + (lane >> 4) * 16;
+        uint32_t h[8];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(Dr + 4 * q);
+            h[2 * q] = pack_f16x2(v4.x, v4.y);
+            h[2 * q + 1] = pack_f16x2(v4.z, v4.w);
+        }
+        uint8_t *T16 = sm.base + kOffT16;
+        *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, 2 * blk)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, 2 * blk + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+}
+
+// Block merges of (I + L)^-1 on the warp MMA (3 x tf32), on the dense fp32
+// blocks; the merged blocks also go to the fp16 operand T16.
+//   level 1: T10 = -X1 (L10 X0),  T32 = -X3 (L32 X2)       (into D0 / D1)
+//   level 2: T[32:64, 0:32] = -D1 (L[32:64, 0:32] D0)
+__device__ void i_merge(const Smem &sm, int it)
 {
     const int iw = it >> 5, lane = it & 31, g = lane >> 2, t = lane & 3;
-    const uint32_t st = s * kStageBytes;
-    float *W = sm.ptr<float>(st + kOffW);
-    uint8_t *T16 = sm.base + st + kOffM;
+    float *W = sm.ptr<float>(kOffTmp);
+    uint8_t *T16 = sm.base + kOffT16;
     float *P1 = sm.ptr<float>(kOffP);            // [2][16][24]
     float *P2 = P1;                              // [32][40] once P1 is dead
     auto put16 = [&](int r, int c, float v0, float v1) {   // c even
@@ -550,22 +673,20 @@ __device__ void i_merge(const Smem &sm, int s, int it)
     };
     {
         const int bl = iw >> 1, nt = iw & 1;
+        float *D = W + (bl ? kD1 : kD0);
         const float *Lb = W + (bl ? kL32 : kL10);
-        const float *Xc = W + kTcX + (2 * bl) * 320;
-        const float *Xr = W + kTcX + (2 * bl + 1) * 320;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         tile_mma(d, [&](int rr, int kk) { return Lb[rr * 20 + kk]; },
-                 [&](int kk, int cc) { return Xc[kk * 20 + 8 * nt + cc]; }, nt, 2, lane);
+                 [&](int kk, int cc) { return D[kk * 36 + 8 * nt + cc]; }, nt, 2, lane);
         float *P = P1 + bl * 384;
         *reinterpret_cast<float2 *>(P + g * 24 + 8 * nt + 2 * t) = make_float2(d[0], d[1]);
         *reinterpret_cast<float2 *>(P + (g + 8) * 24 + 8 * nt + 2 * t) = make_float2(d[2], d[3]);
         named_bar(kBarI, kGroupThreads);
         float e[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(e, [&](int rr, int kk) { return Xr[rr * 20 + kk]; },
+        tile_mma(e, [&](int rr, int kk) { return D[(16 + rr) * 36 + 16 + kk]; },
                  [&](int kk, int cc) { return P[kk * 24 + 8 * nt + cc]; }, 0, 2, lane);
-        float *To = W + kTcT + bl * 320;
-        *reinterpret_cast<float2 *>(To + g * 20 + 8 * nt + 2 * t) = make_float2(-e[0], -e[1]);
-        *reinterpret_cast<float2 *>(To + (g + 8) * 20 + 8 * nt + 2 * t) = make_float2(-e[2], -e[3]);
+        *reinterpret_cast<float2 *>(D + (16 + g) * 36 + 8 * nt + 2 * t) = make_float2(-e[0], -e[1]);
+        *reinterpret_cast<float2 *>(D + (24 + g) * 36 + 8 * nt + 2 * t) = make_float2(-e[2], -e[3]);
         const int r0 = 32 * bl + 16, c0 = 32 * bl;
         put16(r0 + g, c0 + 8 * nt + 2 * t, -e[0], -e[1]);
         put16(r0 + g + 8, c0 + 8 * nt + 2 * t, -e[2], -e[3]);
@@ -575,19 +696,14 @@ __device__ void i_merge(const Smem &sm, int s, int it)
     // sharing the A fragment (two independent accumulation chains)
     const int mt = iw >> 1, n0 = 2 * (iw & 1);
     {
-        auto T01 = [&](int kk, int cc) -> float {           // T[0:32, 0:32]
-            if (kk < 16) return cc < 16 ? W[kTcX + kk * 20 + cc] : 0.f;
-            return cc < 16 ? W[kTcT + (kk - 16) * 20 + cc] : W[kTcX + 320 + (kk - 16) * 20 + (cc - 16)];
-        };
-        const float *L2 = W + kL2;
+        const float *L2 = W + kL2, *D0 = W + kD0;
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 4; ks++) {
-            if (ks < n0) continue;
+#pragma unroll 1
+        for (int ks = n0; ks < 4; ks++) {           // D0 is zero above its diagonal
             const int r = 16 * mt + g, k0 = 8 * ks + t;
             const float a[4] = {L2[r * 36 + k0], L2[(r + 8) * 36 + k0], L2[r * 36 + k0 + 4], L2[(r + 8) * 36 + k0 + 4]};
-            const float b0[2] = {T01(k0, 8 * n0 + g), T01(k0 + 4, 8 * n0 + g)};
-            const float b1[2] = {T01(k0, 8 * n0 + 8 + g), T01(k0 + 4, 8 * n0 + 8 + g)};
+            const float b0[2] = {D0[k0 * 36 + 8 * n0 + g], D0[(k0 + 4) * 36 + 8 * n0 + g]};
+            const float b1[2] = {D0[k0 * 36 + 8 * n0 + 8 + g], D0[(k0 + 4) * 36 + 8 * n0 + 8 + g]};
             mma_3xtf32(d0, a, b0);
             mma_3xtf32(d1, a, b1);
         }
@@ -599,16 +715,12 @@ __device__ void i_merge(const Smem &sm, int s, int it)
     }
     named_bar(kBarI, kGroupThreads);
     {
-        auto T23 = [&](int rr, int kk) -> float {           // T[32:64, 32:64]
-            if (rr < 16) return kk < 16 ? W[kTcX + 640 + rr * 20 + kk] : 0.f;
-            return kk < 16 ? W[kTcT + 320 + (rr - 16) * 20 + kk] : W[kTcX + 960 + (rr - 16) * 20 + (kk - 16)];
-        };
+        const float *D1 = W + kD1;
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < 4; ks++) {
-            if (ks > 2 * mt + 1) continue;
+#pragma unroll 1
+        for (int ks = 0; ks <= 2 * mt + 1; ks++) {   // D1 is zero above its diagonal
             const int rr = 16 * mt + g, k0 = 8 * ks + t;
-            const float a[4] = {T23(rr, k0), T23(rr + 8, k0), T23(rr, k0 + 4), T23(rr + 8, k0 + 4)};
+            const float a[4] = {D1[rr * 36 + k0], D1[(rr + 8) * 36 + k0], D1[rr * 36 + k0 + 4], D1[(rr + 8) * 36 + k0 + 4]};
             const float b0[2] = {P2[k0 * 40 + 8 * n0 + g], P2[(k0 + 4) * 40 + 8 * n0 + g]};
             const float b1[2] = {P2[k0 * 40 + 8 * n0 + 8 + g], P2[(k0 + 4) * 40 + 8 * n0 + 8 + g]};
             mma_3xtf32(d0, a, b0);
@@ -628,7 +740,7 @@ __device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
     const uint32_t id = idesc_f16(128, 64, 1, 0);
 #pragma unroll
     for (int ks = 0; ks < 4; ks++) {
-        const uint64_t bd = smem_desc_sw128(st + kOffM + ks * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(sm.u32(kOffT16) + ks * 32, 16, 1024);
         const uint64_t aw = smem_desc_sw128(st + kOffKQ + ks * 2048, 16384, 1024);   // Kp^T, MN-major
         const uint64_t au = smem_desc_sw128(st + kOffV + ks * 2048, 8192, 1024);     // V^T, MN-major
         mma_ss(tmem + kTmP + 128 * s + 64, aw, bd, id, ks > 0);
@@ -637,6 +749,8 @@ __device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
 }
 
 // -W'^T (TMEM, lane = key channel c, column = row r) -> fp16 MN-major [c][r]
+// in the stage's K region (Kp is dead once MMA-b is done): channels 0-63 where
+// the first K half was, 64-127 where the second was
 __device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
 {
     const int iw = it >> 5, lane = it & 31;
@@ -646,14 +760,14 @@ __device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
     tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(a));
     tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
     tmem_wait_ld();
-    uint8_t *Wt = sm.base + s * kStageBytes + kOffW;
+    uint8_t *Wt = sm.base + s * kStageBytes + kOffKQ + (c >> 6) * 16384;
 #pragma unroll
     for (int q = 0; q < 8; q++) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; e++)
             w[e] = pack_f16x2(-__uint_as_float(a[8 * q + 2 * e]), -__uint_as_float(a[8 * q + 2 * e + 1]));
-        *reinterpret_cast<uint4 *>(Wt + sw128_chunk(c, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(Wt + sw128_chunk(c & 63, q)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -661,25 +775,51 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
 {
     const int it = threadIdx.x - kChainThreads - kGroupThreads;
     const uint32_t tmem = *sm.tmem_base();
+    {   // zeros that stay for the whole kernel: T16's 16-byte chunks right of each
+        // row's diagonal block, and the upper-right 16x16 blocks of D0 and D1
+        uint8_t *T16 = sm.base + kOffT16;
+        for (int idx = it; idx < 64 * 8; idx += kGroupThreads) {
+            const int r = idx >> 3, q = idx & 7;
+            if (q > 2 * (r >> 4) + 1) *reinterpret_cast<uint4 *>(T16 + sw128_chunk(r, q)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        float *W = sm.ptr<float>(kOffTmp);
+        for (int idx = it; idx < 2 * 16 * 16; idx += kGroupThreads) {
+            const int b = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
+            W[(b ? kD1 : kD0) + r * 36 + 16 + c] = 0.f;
+        }
+        fence_proxy_async_smem();
+    }
     int item = 0;
     for (int k = 0;; k++) {
-        const int u = cta_unit(k, U);
+        const int u = cta_unit(sm, k, U);
         if (u < 0) break;
         const Unit un = get_unit(p, order, u);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
-            bool ok = mbar_wait(sm.bar(kBarEDone + s), (item >> 1) & 1, sm.abort_flag());
+            const uint32_t ph = (item >> 1) & 1;
+            // MMA-a done implies group E's operand pass is over
+            bool ok = mbar_wait(sm.bar(kBarAFull + s), ph, sm.abort_flag());
             if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (it == 0) KDA_PHASE(0, item, 5);
-            i_merge(sm, s, it);
+            tc_fence_after();
+            i_read_a(sm, s, tmem, it, item);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(kBarI, kGroupThreads);
+            if (it == 0) KDA_PHASE(0, item, 3);
+            i_merge(sm, it);
             if (it == 0) KDA_PHASE(0, item, 6);
             fence_proxy_async_smem();
             named_bar(kBarI, kGroupThreads);
             if (it == 0) {
-                KDA_PHASE(0, item, 7);
-                tc_fence_after();
-                issue_mma_b(sm, s, tmem);
-                mma_commit(sm.bar(kBarWFull));
+                if (!mbar_wait(sm.bar(kBarEDone + s), ph, sm.abort_flag())) {
+                    record_error(p, sm, kErrWaitTimeout);
+                } else {
+                    KDA_PHASE(0, item, 7);
+                    tc_fence_after();
+                    issue_mma_b(sm, s, tmem);
+                    mma_commit(sm.bar(kBarWFull));
+                }
             }
             ok = mbar_wait(sm.bar(kBarWFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
@@ -698,68 +838,12 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
 }
 
 // =============================================================================
-// TMA loads, issued by the chain's elected thread: the first two chunks at the
-// start, then chunk i+2 as soon as chunk i has released its stage (after MMA3
-// and the output store, the last readers of the stage).
-// =============================================================================
-struct Maps {
-    const CUtensorMap *q, *k, *v, *g;
-};
-
-struct LoadCursor {
-    int k = -1, c = 0, item = 0;
-    bool done = false;
-    Unit un = {0, 0, 0, 0, 0};
-};
-
-__device__ bool cursor_issue(LoadCursor &L, const TcParams &p, const Smem &sm, const int *order, int U, const Maps &m)
-{
-    while (!L.done && L.c >= L.un.nchunks) {
-        const int u = cta_unit(++L.k, U);
-        if (u < 0) {
-            L.done = true;
-            break;
-        }
-        L.un = get_unit(p, order, u);
-        L.c = 0;
-    }
-    if (L.done) return false;
-    const int s = L.item & 1;
-    KDA_PHASE(2, L.item, 0);
-    const int row0 = L.un.bos + L.c * kChunk;
-    const uint32_t st = sm.u32(s * kStageBytes);
-    const uint32_t bar = sm.bar(kBarRawFull + s);
-    mbar_arrive_expect_tx(bar, kRawBytes);
-    // k and q: one box per 64-channel half (the halves interleave with each
-    // other in shared memory); v and g: one 4-D box each, channel blocks outermost
-    for (int kb = 0; kb < 2; kb++) {
-        tma_load_3d(st + kOffKQ + kb * 16384, m.k, 64 * kb, L.un.h, row0, bar);
-        tma_load_3d(st + kOffKQ + kb * 16384 + 8192, m.q, 64 * kb, L.un.h, row0, bar);
-    }
-    tma_load_4d(st + kOffV, m.v, 0, row0, 0, L.un.h, bar);
-    tma_load_4d(st + kOffGX, m.g, 0, row0, 0, L.un.h, bar);
-    L.c++;
-    L.item++;
-    return true;
-}
-
-// copies still in flight land before the CTA exits (normally a no-op: every
-// issued chunk has been consumed)
-__device__ void cursor_drain(const LoadCursor &L, const Smem &sm)
-{
-    for (int back = 1; back <= 2; back++) {
-        const int it = L.item - back;
-        if (it < 0) break;
-        mbar_wait(sm.bar(kBarRawFull + (it & 1)), (it >> 1) & 1, sm.abort_flag(), 1u << 14);
-    }
-}
-
-// =============================================================================
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
 // O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L,
-// transposed through a dedicated shared buffer so the global stores are
-// 16-byte row pieces.  Then TMEM P_s may be reused (o_done).
+// transposed through the stage's V region (dead since MMA-b) so the global
+// stores are 16-byte row pieces.  TMEM P_s may be reused (o_done) as soon as
+// every lane has read it.
 __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, int s, int row0, int L, int h,
                                 int v, int item)
 {
@@ -770,7 +854,7 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem
     tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
     tmem_wait_ld();
     if (v == 0) KDA_PHASE(1, item, 8);
-    __nv_bfloat16 *ot = sm.ptr<__nv_bfloat16>(kOffOT);   // [64][128]
+    __nv_bfloat16 *ot = sm.ptr<__nv_bfloat16>(s * kStageBytes + kOffV);   // [64][128]
 #pragma unroll
     for (int r = 0; r < 64; r++) ot[r * kD + v] = __float2bfloat16_rn(__uint_as_float(o[r]));
     tc_fence_before();
@@ -786,14 +870,15 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem
                 *reinterpret_cast<const uint4 *>(ot + r * kD + 8 * q);
     }
     if (v == 0) KDA_PHASE(1, item, 9);
+    fence_proxy_async_smem();                            // the next v tile lands here by TMA
     named_bar(kBarChain, kChainThreads);                 // the transpose buffer is free again
 }
 
 // S <- (S * pend) * fm column by column (pend may be null), written back, and
 // its fp16 copy S'h (two per 32-bit column) for the chain MMAs.
-__device__ __forceinline__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float *fm, const float *pend)
+__device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float *fm, const float *pend)
 {
-#pragma unroll
+#pragma unroll 1
     for (int half = 0; half < 2; half++) {
         uint32_t x[64];
         tmem_ld32(tmem + kTmS + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(x));
@@ -830,8 +915,9 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                             LoadCursor &cur, uint32_t tmem, uint32_t lane_off, int v)
 {
     int item = 0;
+    bool v_pending = false;   // thread 0: chunk cur.item-1's k and q are requested, its v not yet
     for (int k = 0;; k++) {
-        const int u = cta_unit(k, U);
+        const int u = cta_unit(sm, k, U);
         if (u < 0) break;
         const Unit un = get_unit(p, order, u);
         const size_t soff = (((size_t)un.n * p.H + un.h) * kD + v) * kD;
@@ -859,9 +945,12 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
         tmem_wait_st();
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
+            const uint32_t ph = (item >> 1) & 1;
             const int row0 = un.bos + c * kChunk;
             const int L = min(kChunk, un.eos - row0);
-            bool ok = mbar_wait(sm.bar(kBarPrepDone + s), (item >> 1) & 1, sm.abort_flag());
+            // the state is rescaled as soon as the chunk's decay constants exist,
+            // while the prep still works on the chunk's inverse and W'
+            bool ok = mbar_wait(sm.bar(kBarFmReady + s), ph, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (v == 0) KDA_PHASE(1, item, 0);
             tc_fence_after();
@@ -869,15 +958,18 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                               c > 0 ? sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128 : nullptr);
             if (v == 0) KDA_PHASE(1, item, 6);
             tc_fence_before();
-            named_bar(kBarChain, kChainThreads);
+            ok = mbar_wait(sm.bar(kBarPrepDone + s), ph, sm.abort_flag());
+            if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (v == 0) {
+                KDA_PHASE(1, item, 11);
                 tc_fence_after();
                 const uint32_t st = sm.u32(s * kStageBytes);
                 const uint32_t id_w = idesc_f16(128, 64, 0, 1), id_q = idesc_f16(128, 64, 0, 0);
-                // Delta half first (it gates the chain), then the output half
+                // Delta half first (it gates the chain), then the output half; -W' sits
+                // in the K region, channels 0-63 and 64-127 16 KB apart
 #pragma unroll
                 for (int ks = 0; ks < 8; ks++) {
-                    const uint64_t bw = smem_desc_sw128(st + kOffW + ks * 2048, 16, 1024);
+                    const uint64_t bw = smem_desc_sw128(st + kOffKQ + (ks >> 2) * 16384 + (ks & 3) * 2048, 16, 1024);
                     mma_ts(tmem + kTmP + 128 * s, tmem + kTmS0h + 8 * ks, bw, id_w, 1);
                 }
                 mma_commit(sm.bar(kBarMma1));
@@ -887,6 +979,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                     const uint64_t bq = smem_desc_sw128(st + kOffKQ + kb * 16384 + 8192 + kin * 32, 16, 1024);
                     mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmS0h + 8 * ks, bq, id_q, ks > 0);
                 }
+                mma_commit(sm.bar(kBarMma1O));
                 KDA_PHASE(1, item, 1);
             }
             ok = mbar_wait(sm.bar(kBarMma1), item & 1, sm.abort_flag());
@@ -922,26 +1015,34 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                     const uint64_t bk = smem_desc_sw128(st + kOffKM + ks * 2048, 8192, 1024);   // Km, MN-major
                     mma_ts(tmem + kTmS, tmem + kTmDh + 8 * ks, bk, id_s, 1);
                 }
-                mma_commit(sm.bar(kBarMma3));
 #pragma unroll
                 for (int ks = 0; ks < 4; ks++) {
                     const uint64_t bb = smem_desc_sw128(st + kOffB + ks * 32, 16, 1024);
                     mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmDh + 8 * ks, bb, id_o, 1);
                 }
-                mma_commit(sm.bar(kBarMmaO));
+                mma_commit(sm.bar(kBarMma3));
+                // -W' and Qp have been read: chunk item+2's k and q may land
+                if (!mbar_wait(sm.bar(kBarMma1O), item & 1, sm.abort_flag())) {
+                    record_error(p, sm, kErrWaitTimeout);
+                } else if (cursor_next(cur, p, sm, order, U)) {
+                    issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+                    v_pending = true;
+                }
                 KDA_PHASE(1, item, 3);
             }
-            // every MMA of this chunk is done: its shared-memory stage is free
-            ok = mbar_wait(sm.bar(kBarMma3), item & 1, sm.abort_flag()) &&
-                 mbar_wait(sm.bar(kBarMmaO), item & 1, sm.abort_flag());
+            // every MMA of this chunk is done: Km and B are free, O^T is final
+            ok = mbar_wait(sm.bar(kBarMma3), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (v == 0) {
                 KDA_PHASE(1, item, 4);
-                cursor_issue(cur, p, sm, order, U, maps);    // chunk item+2 into the freed stage
-                KDA_PHASE(1, item, 10);
+                mbar_arrive(sm.bar(kBarKmFree + s));
             }
             tc_fence_after();
             chain_store_out(p, sm, tmem, s, row0, L, un.h, v, item);
+            if (v == 0 && v_pending) {                      // the V region is free again
+                issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+                v_pending = false;
+            }
             if (v == 0) KDA_PHASE(1, item, 5);
         }
         // unit end: final state = S * pend of the unit's last chunk
@@ -973,11 +1074,21 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
     const uint32_t lane_off = (uint32_t)(32 * w) << 16;
     LoadCursor cur;
     if (v == 0) {
-        cursor_issue(cur, p, sm, order, U, maps);
-        cursor_issue(cur, p, sm, order, U, maps);
+        for (int i = 0; i < 2 && cursor_next(cur, p, sm, order, U); i++) {
+            issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+            issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+        }
     }
     chain_units(p, sm, order, U, maps, cur, tmem, lane_off, v);
-    if (v == 0) cursor_drain(cur, sm);
+    if (v == 0) {
+        // copies still in flight land before the CTA exits (normally none: every
+        // requested chunk has been consumed)
+        for (int back = 1; back <= 2 && cur.item - back >= 0; back++) {
+            const int it = cur.item - back;
+            mbar_wait(sm.bar(kBarKQFull + (it & 1)), (it >> 1) & 1, sm.abort_flag(), 1u << 14);
+            mbar_wait(sm.bar(kBarVFull + (it & 1)), (it >> 1) & 1, sm.abort_flag(), 1u << 14);
+        }
+    }
 }
 
 // =============================================================================
@@ -1014,23 +1125,60 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             }
             order[rank] = n;
         }
+        __syncthreads();
+        // Balanced deal of the sorted units (longest first), in rounds of one
+        // unit per CTA: in each round the CTA with the r-th smallest load so
+        // far (in chunks; ties by index) takes the r-th longest unit left.
+        // Every CTA computes the same deal and keeps its own list.
+        const int G = gridDim.x;
+        const int R = (U + G - 1) / G;
+        if (R <= kMaxRounds && G <= kThreads) {
+            int *load = sm.ptr<int>(kOffP + 1024);
+            int *mine = sm.sched();
+            int lj = 0;
+            for (int r = 0; r < R; r++) {
+                if (tid < G) load[tid] = lj;
+                __syncthreads();
+                if (tid < G) {
+                    int rank = 0;
+                    for (int i = 0; i < G; i++) {
+                        const int li = load[i];
+                        rank += (li < lj) || (li == lj && i < tid);
+                    }
+                    const int u = r * G + rank;
+                    if (u < U) {
+                        const int2 be = rows[order[u / p.H]];
+                        lj += (be.y - be.x + kChunk - 1) / kChunk;
+                    }
+                    if (tid == (int)blockIdx.x) mine[r] = u < U ? u : -1;
+                }
+                __syncthreads();
+            }
+            if (tid == 0) *sm.sched_len() = R;
+        } else if (tid == 0) {
+            *sm.sched_len() = -1;
+        }
+    } else if (tid == 0) {
+        *sm.sched_len() = -1;
     }
     if (tid == 0) {
         *sm.abort_flag() = 0;
         for (int i = 0; i < 2; i++) {
-            mbar_init(sm.bar(kBarRawFull + i), 1);
+            mbar_init(sm.bar(kBarKQFull + i), 1);
+            mbar_init(sm.bar(kBarVFull + i), 1);
             mbar_init(sm.bar(kBarPrepDone + i), 1);
+            mbar_init(sm.bar(kBarAFull + i), 1);
+            mbar_init(sm.bar(kBarEDone + i), kGroupThreads);
+            mbar_init(sm.bar(kBarODone + i), 1);
+            mbar_init(sm.bar(kBarFmReady + i), kGroupThreads);
+            mbar_init(sm.bar(kBarKmFree + i), 1);
         }
-        mbar_init(sm.bar(kBarAFull), 1);
+        mbar_init(sm.bar(kBarGFull), 1);
         mbar_init(sm.bar(kBarWFull), 1);
         mbar_init(sm.bar(kBarMma1), 1);
+        mbar_init(sm.bar(kBarMma1O), 1);
         mbar_init(sm.bar(kBarMma3), 1);
         mbar_init(sm.bar(kBarDrain), 3);
-        mbar_init(sm.bar(kBarEDone), 1);
-        mbar_init(sm.bar(kBarEDone + 1), 1);
-        mbar_init(sm.bar(kBarODone), 1);
-        mbar_init(sm.bar(kBarODone + 1), 1);
-        mbar_init(sm.bar(kBarMmaO), 1);
         mbar_fence_init();
     }
     if (warp == 0) {
@@ -1048,7 +1196,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     if (warp < 4) {
         chain_role(p, sm, order, U, maps);
     } else if (warp < 8) {
-        e_role(p, sm, order, U);
+        e_role(p, sm, order, U, maps);
     } else {
         i_role(p, sm, order, U);
     }
