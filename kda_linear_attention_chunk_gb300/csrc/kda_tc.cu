@@ -74,7 +74,7 @@ constexpr int kMaxSortedSeqs = 256;
 constexpr uint32_t kStageBytes = 73728;
 constexpr uint32_t kOffKQ = 0;          // [kb][K rows 0-63 | Q rows 0-63], 2 x 16 KB; K later -W' [c][r]
 constexpr uint32_t kOffKM = 32768;      // Km, 2 x 8 KB
-constexpr uint32_t kOffV = 49152;       // V (fp16 in place of bf16), 2 x 8 KB; later the output transpose
+constexpr uint32_t kOffV = 49152;       // V (fp16 in place of bf16), 2 x 8 KB
 constexpr uint32_t kOffB = 65536;       // tril(A_qk) [r][i] fp16, 8 KB
 constexpr uint32_t kOffG = 2 * kStageBytes;     // g slot (fp32, 4 x 8 KB), read once by the decay scan
 constexpr uint32_t kOffT16 = kOffG + 32768;     // T = (I + A_kk)^-1 [r][j] fp16, 8 KB (MMA-b operand)
@@ -91,7 +91,8 @@ constexpr uint32_t kOffMisc = kOffBar + 256;     // TMEM base, abort flag, sched
 // the start of chunk i+1 (or at the end of the unit), and only chunk i+3's
 // decay scan, which waits for chunk i+1's stage, can overwrite it.
 constexpr uint32_t kOffPend = kOffMisc + 128;
-constexpr uint32_t kSmemBytes = kOffPend + 3 * 512 + 1024;   // + alignment slack
+constexpr uint32_t kOffOT = kOffPend + 3 * 512;             // output transpose, bf16 [32][128]
+constexpr uint32_t kSmemBytes = kOffOT + 8192 + 1024;       // + alignment slack
 
 // mbarrier slots ([2] = one per stage)
 constexpr int kBarKQFull = 0;      // [2]: k, q tiles landed
@@ -194,6 +195,16 @@ __device__ __forceinline__ int cta_unit(const Smem &sm, int k, int U)
 // byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
 
+// 2^x on the special-function unit (approximate, subnormal results flushed to
+// zero).  The decay pass keeps its log-decays in base 2: exp(G) = 2^(G log2 e).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;   // 1 / ln 2
+
 __device__ __forceinline__ void record_error(const TcParams &p, const Smem &sm, int code)
 {
     atomicOr(p.err, code);
@@ -254,9 +265,9 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
 // =============================================================================
 // TMA loads.  The chain's elected thread loads k, q and v into the stages (the
 // first two chunks at the start, then chunk i+2 as soon as chunk i has released
-// the regions: k and q after MMA1, v after the output store); group E's first
-// thread loads g into the single g slot as soon as the decay scan has read the
-// previous chunk's g.
+// the regions: v once MMA-b is done, k and q once MMA1 is done); group E's
+// first thread loads g into the single g slot as soon as the operand pass has
+// read the previous chunk's G.
 // =============================================================================
 struct Maps {
     const CUtensorMap *q, *k, *v, *g;
@@ -330,8 +341,9 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // Group E's decay pass over one chunk; `beta_r` is the beta of row et (zero
 // past the chunk), loaded a chunk ahead.
 // Scan: thread = (row group ew: rows 16*ew .. +15) x (key channels 4*lane ..
-// +3); the row prefix runs in registers, the four row groups exchange their
-// totals once, and G is written back over g in the g slot.
+// +3); the row prefix of g * log2(e) runs in registers, the four row groups
+// exchange their totals once, and G (in base 2) is written back over g in the
+// g slot.
 // Operands: thread = (row 16*ew + 8*hf + (lane & 7)) x (channels 32*cg + 8*j ..
 // +7, cg = lane >> 3), 16-byte accesses; Kp = beta*K*exp(G - G_m),
 // Qp = Q*exp(G - G_m) and Km = K*exp(G_m - G) become fp16 in place over the
@@ -351,7 +363,8 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
 #pragma unroll
         for (int t = 0; t < 16; t++) {
             const int r = 16 * ew + t;
-            x[t] = r < L ? *reinterpret_cast<const float4 *>(gb + sw128_chunk(r, jc)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 g4 = r < L ? *reinterpret_cast<const float4 *>(gb + sw128_chunk(r, jc)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[t] = make_float4(g4.x * kLog2e, g4.y * kLog2e, g4.z * kLog2e, g4.w * kLog2e);   // base-2 log-decay
         }
 #pragma unroll
         for (int t = 1; t < 16; t++) {
@@ -384,15 +397,16 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
     if (role_any(!ok, kBarE, kGroupThreads)) return false;
     if (et == 0) KDA_PHASE(0, item, 14);
     // chain constants, one thread per key channel
-    cst[et] = __expf(gmx[et]);                                                  // view from row m
-    sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = __expf(glx[et] - gmx[et]);  // row m -> last row
+    cst[et] = ex2(gmx[et]);                                                  // view from row m
+    sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = ex2(glx[et] - gmx[et]);  // row m -> last row
     mbar_arrive(sm.bar(kBarFmReady + s));
+    if (et == 0) KDA_PHASE(0, item, 10);
     const int rr = lane & 7, cg = lane >> 3, kb = cg >> 1;
     uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
     uint8_t *qt = kt + 8192;
     uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
     const uint8_t *gt = sm.base + kOffG + cg * 8192;
-#pragma unroll 1
+#pragma unroll 2
     for (int step = 0; step < 8; step++) {
         const int j = step & 3;
         const int r = 16 * ew + 8 * (step >> 2) + rr;
@@ -414,10 +428,10 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
         for (int e = 0; e < 4; e++) {
             float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
             if (valid) {
-                a0 = __expf(G[2 * e] - M[2 * e]);
-                a1 = __expf(G[2 * e + 1] - M[2 * e + 1]);
-                b0 = __expf(M[2 * e] - G[2 * e]);
-                b1 = __expf(M[2 * e + 1] - G[2 * e + 1]);
+                a0 = ex2(G[2 * e] - M[2 * e]);
+                a1 = ex2(G[2 * e + 1] - M[2 * e + 1]);
+                b0 = ex2(M[2 * e] - G[2 * e]);
+                b1 = ex2(M[2 * e + 1] - G[2 * e + 1]);
             }
             const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
             const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
@@ -429,6 +443,7 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
         *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
         *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
     }
+    if (et == 0) KDA_PHASE(0, item, 11);
     return true;
 }
 
@@ -514,6 +529,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                 tc_fence_after();
                 issue_mma_a(sm, s, tmem);
                 mma_commit(sm.bar(kBarAFull + s));
+                KDA_PHASE(2, item, 2);
             }
             if (cursor_next(ahead, p, sm, order, U)) {
                 if (et == 0) {
@@ -522,8 +538,11 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                 }
                 beta_next = load_beta(p, ahead, et);
             }
+            if (et == 0) KDA_PHASE(2, item, 6);
             ok = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
+            if (et == 0) KDA_PHASE(2, item, 4);
             if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (et == 0) KDA_PHASE(2, item, 5);
             e_convert_v(sm, s, L, et);
             fence_proxy_async_smem();
             mbar_arrive(sm.bar(kBarEDone + s));            // every operand of this chunk is written
@@ -819,6 +838,7 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
                     tc_fence_after();
                     issue_mma_b(sm, s, tmem);
                     mma_commit(sm.bar(kBarWFull));
+                    KDA_PHASE(2, item, 3);
                 }
             }
             ok = mbar_wait(sm.bar(kBarWFull), item & 1, sm.abort_flag());
@@ -841,7 +861,7 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
 // O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L,
-// transposed through the stage's V region (dead since MMA-b) so the global
+// transposed 32 rows at a time through the 8 KB output buffer so the global
 // stores are 16-byte row pieces.  TMEM P_s may be reused (o_done) as soon as
 // every lane has read it.
 __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, int s, int row0, int L, int h,
@@ -853,25 +873,27 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem
     tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(o));
     tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
     tmem_wait_ld();
-    if (v == 0) KDA_PHASE(1, item, 8);
-    __nv_bfloat16 *ot = sm.ptr<__nv_bfloat16>(s * kStageBytes + kOffV);   // [64][128]
-#pragma unroll
-    for (int r = 0; r < 64; r++) ot[r * kD + v] = __float2bfloat16_rn(__uint_as_float(o[r]));
     tc_fence_before();
-    named_bar(kBarChain, kChainThreads);
-    if (v == 0) mbar_arrive(sm.bar(kBarODone + s));      // TMEM P_s has been read by all lanes
+    if (v == 0) KDA_PHASE(1, item, 8);
+    __nv_bfloat16 *ot = sm.ptr<__nv_bfloat16>(kOffOT);   // [32][128]
     const size_t row_stride = (size_t)p.H * kD;
     __nv_bfloat16 *dst = p.out + ((size_t)row0 * p.H + h) * kD;
 #pragma unroll
-    for (int k = 0; k < 8; k++) {
-        const int idx = v + 128 * k, r = idx >> 4, q = idx & 15;
-        if (r < L)
-            *reinterpret_cast<uint4 *>(dst + (size_t)r * row_stride + 8 * q) =
-                *reinterpret_cast<const uint4 *>(ot + r * kD + 8 * q);
+    for (int half = 0; half < 2; half++) {
+#pragma unroll
+        for (int r = 0; r < 32; r++) ot[r * kD + v] = __float2bfloat16_rn(__uint_as_float(o[32 * half + r]));
+        named_bar(kBarChain, kChainThreads);
+        if (half == 0 && v == 0) mbar_arrive(sm.bar(kBarODone + s));   // every lane has read TMEM P_s
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const int idx = v + 128 * k, r = idx >> 4, q = idx & 15;
+            if (32 * half + r < L)
+                *reinterpret_cast<uint4 *>(dst + (size_t)(32 * half + r) * row_stride + 8 * q) =
+                    *reinterpret_cast<const uint4 *>(ot + r * kD + 8 * q);
+        }
+        named_bar(kBarChain, kChainThreads);             // the buffer is free again
     }
     if (v == 0) KDA_PHASE(1, item, 9);
-    fence_proxy_async_smem();                            // the next v tile lands here by TMA
-    named_bar(kBarChain, kChainThreads);                 // the transpose buffer is free again
 }
 
 // S <- (S * pend) * fm column by column (pend may be null), written back, and
@@ -915,7 +937,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                             LoadCursor &cur, uint32_t tmem, uint32_t lane_off, int v)
 {
     int item = 0;
-    bool v_pending = false;   // thread 0: chunk cur.item-1's k and q are requested, its v not yet
+    bool kq_pending = false;  // thread 0: chunk cur.item-1's v is requested, its k and q not yet
     for (int k = 0;; k++) {
         const int u = cta_unit(sm, k, U);
         if (u < 0) break;
@@ -962,6 +984,12 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (v == 0) {
                 KDA_PHASE(1, item, 11);
+                // MMA-b is done with V: chunk item+2's v may land
+                if (cursor_next(cur, p, sm, order, U)) {
+                    issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+                    kq_pending = true;
+                }
+                KDA_PHASE(1, item, 12);
                 tc_fence_after();
                 const uint32_t st = sm.u32(s * kStageBytes);
                 const uint32_t id_w = idesc_f16(128, 64, 0, 1), id_q = idesc_f16(128, 64, 0, 0);
@@ -1021,12 +1049,13 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                     mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmDh + 8 * ks, bb, id_o, 1);
                 }
                 mma_commit(sm.bar(kBarMma3));
+                KDA_PHASE(1, item, 13);
                 // -W' and Qp have been read: chunk item+2's k and q may land
                 if (!mbar_wait(sm.bar(kBarMma1O), item & 1, sm.abort_flag())) {
                     record_error(p, sm, kErrWaitTimeout);
-                } else if (cursor_next(cur, p, sm, order, U)) {
+                } else if (kq_pending) {
                     issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
-                    v_pending = true;
+                    kq_pending = false;
                 }
                 KDA_PHASE(1, item, 3);
             }
@@ -1039,10 +1068,6 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             }
             tc_fence_after();
             chain_store_out(p, sm, tmem, s, row0, L, un.h, v, item);
-            if (v == 0 && v_pending) {                      // the V region is free again
-                issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
-                v_pending = false;
-            }
             if (v == 0) KDA_PHASE(1, item, 5);
         }
         // unit end: final state = S * pend of the unit's last chunk
