@@ -49,10 +49,20 @@ using namespace sm100;
 
 // Optional phase timestamps of CTA 0 (compiled in only with -DKDA_TRACE).
 #ifdef KDA_TRACE
+#ifndef KDA_TRACE_CTA
+#define KDA_TRACE_CTA 0
+#endif
 __device__ unsigned long long g_kda_trace[3][128][16];
+__device__ unsigned long long g_kda_cta[1024][4];   // per CTA: start, end (global timer), items, units
+__device__ __forceinline__ unsigned long long kda_gtimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
 #define KDA_PHASE(role, item, point)                                                  \
     do {                                                                              \
-        if (blockIdx.x == 0 && (item) < 128) g_kda_trace[role][item][point] = clock64(); \
+        if (blockIdx.x == KDA_TRACE_CTA && (item) < 128) g_kda_trace[role][item][point] = clock64(); \
     } while (0)
 #else
 #define KDA_PHASE(role, item, point) \
@@ -211,7 +221,7 @@ __device__ __forceinline__ void record_error(const TcParams &p, const Smem &sm, 
     *sm.abort_flag() = 1;
 }
 
-// ---- small fp32-accurate products on the warp MMA (3 x tf32 split) ---------------
+// ---- small products on the warp MMA (tf32) ------------------------------------------
 __device__ __forceinline__ uint32_t to_tf32(float x)
 {
     uint32_t r;
@@ -228,29 +238,18 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// d += A[16x8] * B[8x8] with A = hi + lo and B = hi + lo split into tf32 parts
-// (the lo*lo term is dropped): about fp32 accuracy.
-__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], const float (&b)[2])
+// d += A[16x8] * B[8x8] with both operands rounded to tf32 (10-bit mantissa,
+// the precision of the fp16 operand T16 the merged blocks end up in)
+__device__ __forceinline__ void mma_1xtf32(float (&d)[4], const float (&a)[4], const float (&b)[2])
 {
-    uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        ah[i] = to_tf32(a[i]);
-        al[i] = to_tf32(a[i] - __uint_as_float(ah[i]));
-    }
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-        bh[i] = to_tf32(b[i]);
-        bl[i] = to_tf32(b[i] - __uint_as_float(bh[i]));
-    }
-    mma_tf32(d, al, bh);
-    mma_tf32(d, ah, bl);
+    const uint32_t ah[4] = {to_tf32(a[0]), to_tf32(a[1]), to_tf32(a[2]), to_tf32(a[3])};
+    const uint32_t bh[2] = {to_tf32(b[0]), to_tf32(b[1])};
     mma_tf32(d, ah, bh);
 }
 
 // One m16n8 tile of D = sum_k A[r0 + .][ka + k] * B[kb + k][c0 + .] over k-steps
 // [ks0, ks1) of 8, A and B read from fp32 smem through `la` / `lb` (row, col)
-// index functions; 3 x tf32 on the warp MMA.
+// index functions; tf32 on the warp MMA.
 template <typename FA, typename FB>
 __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, int ks1, int lane)
 {
@@ -258,7 +257,7 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
     for (int ks = ks0; ks < ks1; ks++) {
         const float a[4] = {la(g, 8 * ks + t), la(g + 8, 8 * ks + t), la(g, 8 * ks + t + 4), la(g + 8, 8 * ks + t + 4)};
         const float b[2] = {lb(8 * ks + t, g), lb(8 * ks + t + 4, g)};
-        mma_3xtf32(d, a, b);
+        mma_1xtf32(d, a, b);
     }
 }
 
@@ -676,8 +675,10 @@ __device__ void i_read_a(const Smem &sm, int s, uint32_t tmem, int it, int item)
     }
 }
 
-// Block merges of (I + L)^-1 on the warp MMA (3 x tf32), on the dense fp32
-// blocks; the merged blocks also go to the fp16 operand T16.
+// Block merges of (I + L)^-1 on the warp MMA (tf32 operands, fp32 accumulate),
+// on the dense fp32 blocks; the merged blocks go to the fp16 operand T16, whose
+// own rounding is of the same size as the tf32 operand rounding (the fp32
+// diagonal inverses are exact to fp32).
 //   level 1: T10 = -X1 (L10 X0),  T32 = -X3 (L32 X2)       (into D0 / D1)
 //   level 2: T[32:64, 0:32] = -D1 (L[32:64, 0:32] D0)
 __device__ void i_merge(const Smem &sm, int it)
@@ -723,8 +724,8 @@ __device__ void i_merge(const Smem &sm, int it)
             const float a[4] = {L2[r * 36 + k0], L2[(r + 8) * 36 + k0], L2[r * 36 + k0 + 4], L2[(r + 8) * 36 + k0 + 4]};
             const float b0[2] = {D0[k0 * 36 + 8 * n0 + g], D0[(k0 + 4) * 36 + 8 * n0 + g]};
             const float b1[2] = {D0[k0 * 36 + 8 * n0 + 8 + g], D0[(k0 + 4) * 36 + 8 * n0 + 8 + g]};
-            mma_3xtf32(d0, a, b0);
-            mma_3xtf32(d1, a, b1);
+            mma_1xtf32(d0, a, b0);
+            mma_1xtf32(d1, a, b1);
         }
         const int r = 16 * mt + g;
         *reinterpret_cast<float2 *>(P2 + r * 40 + 8 * n0 + 2 * t) = make_float2(d0[0], d0[1]);
@@ -742,8 +743,8 @@ __device__ void i_merge(const Smem &sm, int it)
             const float a[4] = {D1[rr * 36 + k0], D1[(rr + 8) * 36 + k0], D1[rr * 36 + k0 + 4], D1[(rr + 8) * 36 + k0 + 4]};
             const float b0[2] = {P2[k0 * 40 + 8 * n0 + g], P2[(k0 + 4) * 40 + 8 * n0 + g]};
             const float b1[2] = {P2[k0 * 40 + 8 * n0 + 8 + g], P2[(k0 + 4) * 40 + 8 * n0 + 8 + g]};
-            mma_3xtf32(d0, a, b0);
-            mma_3xtf32(d1, a, b1);
+            mma_1xtf32(d0, a, b0);
+            mma_1xtf32(d1, a, b1);
         }
         const int r = 32 + 16 * mt + g;
         put16(r, 8 * n0 + 2 * t, -d0[0], -d0[1]);
@@ -952,17 +953,27 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             }
             continue;
         }
-        // initial state -> S (TMEM, lane v, columns = key channels)
+        // the next unit's initial state heads for L2 while this unit runs
+        if (v == 0 && p.s0) {
+            const int un2 = cta_unit(sm, k + 1, U);
+            if (un2 >= 0) {
+                const Unit nx = get_unit(p, order, un2);
+                const float *src = p.s0 + ((size_t)nx.n * p.H + nx.h) * kD * kD;
+                for (int part = 0; part < 4; part++) prefetch_l2(src + part * 4096, 16384);
+            }
+        }
+        // initial state -> S (TMEM, lane v, columns = key channels), 64 columns a round
+#pragma unroll 1
+        for (int hb = 0; hb < 2; hb++) {
+            uint32_t x[64];
 #pragma unroll
-        for (int cb = 0; cb < 4; cb++) {
-            uint32_t x[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 f = p.s0 ? *reinterpret_cast<const float4 *>(p.s0 + soff + 32 * cb + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 64; j += 4) {
+                float4 f = p.s0 ? *reinterpret_cast<const float4 *>(p.s0 + soff + 64 * hb + j) : make_float4(0.f, 0.f, 0.f, 0.f);
                 x[j] = __float_as_uint(f.x); x[j + 1] = __float_as_uint(f.y);
                 x[j + 2] = __float_as_uint(f.z); x[j + 3] = __float_as_uint(f.w);
             }
-            tmem_st32(tmem + kTmS + lane_off + 32 * cb, x);
+            tmem_st32(tmem + kTmS + lane_off + 64 * hb, *reinterpret_cast<uint32_t(*)[32]>(x));
+            tmem_st32(tmem + kTmS + lane_off + 64 * hb + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
         }
         tmem_wait_st();
         for (int c = 0; c < un.nchunks; c++, item++) {
@@ -1217,6 +1228,9 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
 
+#ifdef KDA_TRACE
+    if (tid == 0 && blockIdx.x < 1024) g_kda_cta[blockIdx.x][0] = kda_gtimer();
+#endif
     const Maps maps = {&tq, &tk, &tv, &tg};
     if (warp < 4) {
         chain_role(p, sm, order, U, maps);
@@ -1234,6 +1248,20 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(*sm.tmem_base(), kTmCols);
+#ifdef KDA_TRACE
+    if (tid == 0 && blockIdx.x < 1024) {
+        g_kda_cta[blockIdx.x][1] = kda_gtimer();
+        int items = 0, units = 0;
+        for (int k = 0;; k++) {
+            const int u = cta_unit(sm, k, U);
+            if (u < 0) break;
+            units++;
+            items += get_unit(p, order, u).nchunks;
+        }
+        g_kda_cta[blockIdx.x][2] = items;
+        g_kda_cta[blockIdx.x][3] = units;
+    }
+#endif
 }
 
 // ---- host side ------------------------------------------------------------------
