@@ -5,12 +5,22 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "kda.h"
 #include "kda_internal.h"
 
 namespace {
 
 __device__ int g_kda_error_word = 0;
+
+// Scratch of the dynamic unit deal: per slot a claim counter and a count of
+// finished CTAs; the last CTA of a launch returns its slot to zero.  Calls take
+// slots round-robin, so launches in flight at the same time (on different
+// streams) use different slots unless more than kSchedSlots are in flight.
+constexpr int kSchedSlots = 256;
+static __device__ __align__(256) unsigned int g_kda_sched[kSchedSlots][2];
+std::atomic<unsigned> g_sched_next{0};
 
 constexpr int kMaxSeqs = 1024;
 constexpr int kMaxDevices = 64;
@@ -19,6 +29,7 @@ struct DevInfo {
     int checked = 0;   // 0 unknown, 1 ok, -1 unsupported
     int num_sms = 0;
     int *err = nullptr;
+    unsigned int *sched = nullptr;
 };
 DevInfo g_dev[kMaxDevices];
 
@@ -52,13 +63,15 @@ int device_info(DevInfo **out)
             cudaGetLastError();
             return KDA_ERR_DEVICE;
         }
-        void *err = nullptr;
-        if (cudaGetSymbolAddress(&err, g_kda_error_word) != cudaSuccess) {
+        void *err = nullptr, *sched = nullptr;
+        if (cudaGetSymbolAddress(&err, g_kda_error_word) != cudaSuccess ||
+            cudaGetSymbolAddress(&sched, g_kda_sched) != cudaSuccess) {
             cudaGetLastError();
             return KDA_ERR_CUDA;
         }
         d.num_sms = sms;
         d.err = (int *)err;
+        d.sched = (unsigned int *)sched;
         d.checked = (major == 10 && minor == 3) ? 1 : -1;
     }
     if (d.checked != 1) return KDA_ERR_DEVICE;
@@ -115,6 +128,7 @@ kda::KdaArgs make_args(const void *q, const void *k, const void *v, const float 
     a.N = N; a.T = T; a.H = H; a.dk = dk; a.dv = dv;
     a.stream = (cudaStream_t)stream;
     a.err_word = d->err;
+    a.sched = d->sched + 2 * (g_sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
     a.num_sms = d->num_sms;
     return a;
 }

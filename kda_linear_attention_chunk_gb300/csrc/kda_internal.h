@@ -17,6 +17,7 @@ struct KdaArgs {
     int N, T, H, dk, dv;
     cudaStream_t stream;
     int *err_word;                  // device address of the sticky error word
+    unsigned int *sched;            // 2 words of device scratch for the dynamic unit deal (reset by the kernel), or nullptr
     int num_sms;                    // SM count of the current device
 };
 

@@ -133,6 +133,7 @@ struct TcParams {
     int N, T, H;
     int sorted;        // 1 if the sequence order was sorted (N <= kMaxSortedSeqs)
     int *err;
+    unsigned int *sched;   // dynamic deal: [claim counter, finished CTAs], or nullptr
 };
 
 struct Smem {
@@ -142,8 +143,12 @@ struct Smem {
     __device__ uint32_t bar(int i) const { return u32(kOffBar + 8 * i); }
     __device__ volatile int *abort_flag() const { return ptr<volatile int>(kOffMisc + 4); }
     __device__ uint32_t *tmem_base() const { return ptr<uint32_t>(kOffMisc); }
-    __device__ int *sched_len() const { return ptr<int>(kOffMisc + 8); }   // -1: snake deal
-    __device__ int *sched() const { return ptr<int>(kOffMisc + 16); }      // [kMaxRounds]
+    // unit deal: mode >= 0 static list of that length, -1 snake, -2 dynamic
+    __device__ int *sched_len() const { return ptr<int>(kOffMisc + 8); }
+    __device__ volatile int *published() const { return ptr<volatile int>(kOffMisc + 12); }   // dynamic: units in the ring
+    __device__ volatile int *claim_done() const { return ptr<volatile int>(kOffMisc + 16); }  // dynamic: no more claims
+    __device__ int *units_nonempty() const { return ptr<int>(kOffMisc + 20); }
+    __device__ int *sched() const { return ptr<int>(kOffMisc + 24); }      // static list [kMaxRounds] / ring [8]
 };
 
 __device__ __forceinline__ bool role_any(bool pred, int id, int n)
@@ -189,13 +194,34 @@ __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, in
     return x;
 }
 
-// k-th unit of this CTA, -1 when exhausted: the balanced deal made in the
-// prologue when there is one, else a boustrophedon ("snake") deal of the
-// length-sorted unit list over the grid.
+// Dynamic deal: unit k of this CTA once group E's first thread has published
+// it (units are claimed one ahead of the furthest loader); after the last
+// claim, the CTA's share of the empty units (dealt round-robin) follows.
+__device__ __noinline__ int dyn_unit(const Smem &sm, int k, int U)
+{
+    for (uint32_t it = 0; it < (1u << 22); it++) {
+        const int pub = *sm.published();
+        __threadfence_block();
+        if (k < pub) return reinterpret_cast<volatile int *>(sm.sched())[k & 7];
+        if (*sm.claim_done()) {
+            const int u = *sm.units_nonempty() + (int)blockIdx.x + (k - pub) * (int)gridDim.x;
+            return u < U ? u : -1;
+        }
+        if (*sm.abort_flag()) return -1;
+        __nanosleep(64);
+    }
+    *sm.abort_flag() = 1;
+    return -1;
+}
+
+// k-th unit of this CTA, -1 when exhausted: the dynamic deal, the balanced
+// static deal made in the prologue, or else a boustrophedon ("snake") deal of
+// the length-sorted unit list over the grid.
 __device__ __forceinline__ int cta_unit(const Smem &sm, int k, int U)
 {
     const int n = *sm.sched_len();
     if (n >= 0) return k < n ? sm.sched()[k] : -1;
+    if (n == -2) return dyn_unit(sm, k, U);
     const int G = gridDim.x, b = blockIdx.x;
     const int u = k * G + ((k & 1) ? (G - 1 - b) : b);
     return u < U ? u : -1;
@@ -203,6 +229,19 @@ __device__ __forceinline__ int cta_unit(const Smem &sm, int k, int U)
 
 
 // byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
+// k-th unit of this CTA if it is already known (-1: exhausted, -2: not yet
+// claimed); never waits.
+__device__ __forceinline__ int cta_unit_peek(const Smem &sm, int k, int U)
+{
+    if (*sm.sched_len() != -2) return cta_unit(sm, k, U);
+    const int pub = *sm.published();
+    __threadfence_block();
+    if (k < pub) return reinterpret_cast<volatile int *>(sm.sched())[k & 7];
+    if (!*sm.claim_done()) return -2;
+    const int u = *sm.units_nonempty() + (int)blockIdx.x + (k - pub) * (int)gridDim.x;
+    return u < U ? u : -1;
+}
+
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
 
 // 2^x on the special-function unit (approximate, subnormal results flushed to
@@ -493,7 +532,35 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
     // flight (every thread walks it; thread 0 issues the load)
     LoadCursor ahead;
     float beta_next = 0.f;
+    // dynamic deal: when the g loads reach the last chunk of a unit, thread 0
+    // claims the next unit, and publishes the claim (to the ring in shared
+    // memory) one step later -- late enough that a CTA only takes more work
+    // when it is about to run out, early enough to hide the atomic's latency
+    const bool dyn = *sm.sched_len() == -2;
+    unsigned claim = 0;
+    int claim_slot = -1;
+    auto publish = [&]() {
+        if (claim_slot >= 0) {
+            const int u = (int)gridDim.x + (int)claim;
+            if (u < *sm.units_nonempty()) {
+                reinterpret_cast<volatile int *>(sm.sched())[claim_slot & 7] = u;
+                __threadfence_block();
+                *sm.published() = claim_slot + 1;
+            } else {
+                __threadfence_block();
+                *sm.claim_done() = 1;
+            }
+            claim_slot = -1;
+        }
+    };
+    auto maybe_claim = [&](int k) {   // the g loads have just reached the last chunk of unit k
+        if (dyn && et == 0 && claim_slot < 0 && !*sm.claim_done() && *sm.published() == k + 1) {
+            claim = atomicAdd(p.sched, 1u);
+            claim_slot = k + 1;
+        }
+    };
     if (cursor_next(ahead, p, sm, order, U)) {
+        if (ahead.c == ahead.un.nchunks) maybe_claim(ahead.k);
         if (et == 0) {
             KDA_PHASE(2, 0, 1);
             issue_g(sm, maps, ahead.row0, ahead.un.h);
@@ -510,6 +577,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             const uint32_t ph = (item >> 1) & 1;
             const int L = min(kChunk, un.eos - (un.bos + c * kChunk));
             const float beta_r = beta_next;
+            if (et == 0) publish();
             bool ok = mbar_wait(sm.bar(kBarGFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (et == 0) KDA_PHASE(0, item, 0);
@@ -530,7 +598,9 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                 mma_commit(sm.bar(kBarAFull + s));
                 KDA_PHASE(2, item, 2);
             }
+            if (et == 0) publish();
             if (cursor_next(ahead, p, sm, order, U)) {
+                if (ahead.c == ahead.un.nchunks) maybe_claim(ahead.k);
                 if (et == 0) {
                     KDA_PHASE(2, ahead.item - 1, 1);
                     issue_g(sm, maps, ahead.row0, ahead.un.h);
@@ -953,15 +1023,6 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             }
             continue;
         }
-        // the next unit's initial state heads for L2 while this unit runs
-        if (v == 0 && p.s0) {
-            const int un2 = cta_unit(sm, k + 1, U);
-            if (un2 >= 0) {
-                const Unit nx = get_unit(p, order, un2);
-                const float *src = p.s0 + ((size_t)nx.n * p.H + nx.h) * kD * kD;
-                for (int part = 0; part < 4; part++) prefetch_l2(src + part * 4096, 16384);
-            }
-        }
         // initial state -> S (TMEM, lane v, columns = key channels), 64 columns a round
 #pragma unroll 1
         for (int hb = 0; hb < 2; hb++) {
@@ -986,6 +1047,15 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             bool ok = mbar_wait(sm.bar(kBarFmReady + s), ph, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (v == 0) KDA_PHASE(1, item, 0);
+            if (v == 0 && p.s0 && c == un.nchunks - 1) {
+                // the next unit's initial state heads for L2 during this last chunk
+                const int un2 = cta_unit_peek(sm, k + 1, U);
+                if (un2 >= 0) {
+                    const Unit nx = get_unit(p, order, un2);
+                    const float *src = p.s0 + ((size_t)nx.n * p.H + nx.h) * kD * kD;
+                    for (int part = 0; part < 4; part++) prefetch_l2(src + part * 4096, 16384);
+                }
+            }
             tc_fence_after();
             chain_scale_state(tmem, lane_off, sm.ptr<float>(kOffConst + s * kConstBytes),
                               c > 0 ? sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128 : nullptr);
@@ -1081,6 +1151,9 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             chain_store_out(p, sm, tmem, s, row0, L, un.h, v, item);
             if (v == 0) KDA_PHASE(1, item, 5);
         }
+#ifdef KDA_TRACE
+        if (v == 0 && blockIdx.x < 1024) { g_kda_cta[blockIdx.x][2] = item; g_kda_cta[blockIdx.x][3] = k + 1; }
+#endif
         // unit end: final state = S * pend of the unit's last chunk
         if (p.s1) {
             const float *pend = sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128;
@@ -1162,13 +1235,28 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             order[rank] = n;
         }
         __syncthreads();
-        // Balanced deal of the sorted units (longest first), in rounds of one
-        // unit per CTA: in each round the CTA with the r-th smallest load so
-        // far (in chunks; ties by index) takes the r-th longest unit left.
-        // Every CTA computes the same deal and keeps its own list.
         const int G = gridDim.x;
         const int R = (U + G - 1) / G;
-        if (R <= kMaxRounds && G <= kThreads) {
+        if (p.sched) {
+            // Dynamic deal: CTA b starts with the b-th longest unit; the rest of
+            // the nonempty units (longest first) go to whichever CTA claims them
+            // next, so faster SMs take more work.
+            if (tid == 0) {
+                int ne = 0;
+                for (int n = 0; n < p.N; n++) ne += lens[n] > 0;
+                const int une = ne * p.H;
+                *sm.units_nonempty() = une;
+                const bool first = (int)blockIdx.x < une;
+                sm.sched()[0] = first ? (int)blockIdx.x : -1;
+                *sm.published() = first ? 1 : 0;
+                *sm.claim_done() = first ? 0 : 1;
+                *sm.sched_len() = -2;
+            }
+        } else if (R <= kMaxRounds && G <= kThreads) {
+            // Balanced deal of the sorted units (longest first), in rounds of one
+            // unit per CTA: in each round the CTA with the r-th smallest load so
+            // far (in chunks; ties by index) takes the r-th longest unit left.
+            // Every CTA computes the same deal and keeps its own list.
             int *load = sm.ptr<int>(kOffP + 1024);
             int *mine = sm.sched();
             int lj = 0;
@@ -1248,18 +1336,17 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(*sm.tmem_base(), kTmCols);
+    // the last CTA to finish returns the dynamic deal's scratch slot to zero
+    if (tid == 0 && p.sched) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
+    }
 #ifdef KDA_TRACE
     if (tid == 0 && blockIdx.x < 1024) {
         g_kda_cta[blockIdx.x][1] = kda_gtimer();
-        int items = 0, units = 0;
-        for (int k = 0;; k++) {
-            const int u = cta_unit(sm, k, U);
-            if (u < 0) break;
-            units++;
-            items += get_unit(p, order, u).nchunks;
-        }
-        g_kda_cta[blockIdx.x][2] = items;
-        g_kda_cta[blockIdx.x][3] = units;
     }
 #endif
 }
@@ -1340,6 +1427,7 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     p.H = a.H;
     p.sorted = a.N <= kMaxSortedSeqs ? 1 : 0;
     p.err = a.err_word;
+    p.sched = a.sched;
     const int units = a.N * a.H;
     const int grid = units < a.num_sms ? units : a.num_sms;
     kda_tc_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tg, p);

@@ -26,3 +26,23 @@ def kda_lib():
     if kbuild.stale():
         kbuild.build()
     return kda.load()
+
+
+@pytest.fixture(autouse=True)
+def _no_device_timeouts(request):
+    """Every GPU test must leave no bounded-wait timeout (bit 1 of the device
+    error word) behind: a kernel that gave up on a wait wound down early, and
+    its outputs must not be mistaken for results."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import torch
+    import kda_linear_attention_chunk_gb300 as kda
+    if not torch.cuda.is_available():
+        yield
+        return
+    kda.device_error(reset=True)
+    yield
+    torch.cuda.synchronize()
+    word = kda.device_error(reset=True)
+    assert not (word & 1), f"a kernel wait timed out during the test (device error word {word:#x})"
