@@ -71,7 +71,8 @@ typedef enum {
     KDA_ERR_ALIGN = 4,        /* a tensor pointer is not 16-byte aligned       */
     KDA_ERR_ALIAS = 5,        /* an output overlaps another argument           */
     KDA_ERR_CUDA = 6,         /* a CUDA call failed (see cudaGetLastError)     */
-    KDA_ERR_DEVICE = 7        /* no CUDA device, or not an sm_103 device       */
+    KDA_ERR_DEVICE = 7,       /* no CUDA device, or not an sm_103 device       */
+    KDA_ERR_NOALLOC_LIMIT = 8 /* N above KDA_NOALLOC_MAX_SEQS (noalloc entry)  */
 } kda_status;
 
 /*
@@ -103,6 +104,38 @@ int kda_chunk_prefill_f32(const float *q, const float *k, const float *v,
                           const float *g, const float *beta, const int32_t *cu_seqlens,
                           const float *initial_state, float *out, float *final_state,
                           int N, int T, int H, int dk, int dv, void *stream);
+
+/*
+ * kda_chunk_prefill_noalloc -- kda_chunk_prefill for packed batches of up to
+ * KDA_NOALLOC_MAX_SEQS sequences, for callers that cannot allocate device
+ * memory per call: code inside a serving runtime whose device memory is laid
+ * out in full when a model is loaded (all buffers come from a fixed pool), or
+ * a layer library that is handed only its tensors.  The pages have no
+ * counterpart of this entry point; it exists for those callers.
+ *
+ * With many sequences the work is dealt to the SMs by length from a shared
+ * counter, which needs a sequence table in device memory.  That table lives in
+ * a static array inside the library (about 196 KB, held by every GPU that
+ * loads the library until the process exits), so the call itself allocates
+ * nothing -- no cudaMalloc, cudaFree or library allocator.
+ *
+ * Arguments, layouts, results and errors are those of kda_chunk_prefill,
+ * except 1 <= N <= KDA_NOALLOC_MAX_SEQS; a larger N returns
+ * KDA_ERR_NOALLOC_LIMIT and launches nothing.  Results are the same as
+ * kda_chunk_prefill's (the per-sequence arithmetic does not depend on the
+ * schedule).
+ *
+ * The first call on a device looks up the array's device address (and checks
+ * the device) with that device current; make that first call before any
+ * stream capture.  Every call shares the one array: the call clears the parts
+ * that must start at zero, but calls whose kernels overlap on the GPU (on
+ * different streams without ordering between them) race on it -- order them.
+ */
+#define KDA_NOALLOC_MAX_SEQS 16384
+int kda_chunk_prefill_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              const float *g, const float *beta, const int32_t *cu_seqlens,
+                              const float *initial_state, uint16_t *out, float *final_state,
+                              int N, int T, int H, int dk, int dv, void *stream);
 
 /* Human-readable name of a kda_status value (static string, never NULL). */
 const char *kda_status_string(int status);

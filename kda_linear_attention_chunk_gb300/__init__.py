@@ -16,8 +16,11 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 
 KDA_OK, KDA_ERR_NULL, KDA_ERR_SHAPE, KDA_ERR_UNSUPPORTED = 0, 1, 2, 3
 KDA_ERR_ALIGN, KDA_ERR_ALIAS, KDA_ERR_CUDA, KDA_ERR_DEVICE = 4, 5, 6, 7
+KDA_ERR_NOALLOC_LIMIT = 8
+KDA_NOALLOC_MAX_SEQS = 16384
 
-EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error")
+EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error",
+            "kda_chunk_prefill_noalloc")
 
 _lib = None
 
@@ -38,7 +41,7 @@ def load(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     P, I = ctypes.c_void_p, ctypes.c_int
     sig = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P]
-    for name in ("kda_chunk_prefill", "kda_chunk_prefill_f32"):
+    for name in ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_chunk_prefill_noalloc"):
         fn = getattr(lib, name)
         fn.argtypes = sig
         fn.restype = I
@@ -70,6 +73,15 @@ def kda_chunk_prefill_f32(q, k, v, g, beta, cu_seqlens, initial_state, out, fina
     """Raw C-ABI call for fp32 q/k/v/out."""
     return load().kda_chunk_prefill_f32(q, k, v, g, beta, cu_seqlens, initial_state, out,
                                         final_state, N, T, H, dk, dv, stream)
+
+
+def kda_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                              N: int, T: int, H: int, dk: int, dv: int, stream) -> int:
+    """Raw C-ABI call of the entry point that allocates nothing (up to
+    KDA_NOALLOC_MAX_SEQS sequences; its scheduling table lives inside the
+    library, for callers that cannot allocate device memory per call)."""
+    return load().kda_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, initial_state, out,
+                                            final_state, N, T, H, dk, dv, stream)
 
 
 def device_error(reset: bool = False) -> int:

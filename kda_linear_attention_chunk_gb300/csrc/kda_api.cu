@@ -82,7 +82,7 @@ int device_info(DevInfo **out)
 // Validation shared by both entry points.  elem = bytes per q/k/v/out element.
 int validate(const void *q, const void *k, const void *v, const float *g, const float *beta,
              const int32_t *cu, const float *s0, const void *out, const float *s1,
-             int N, int T, int H, int dk, int dv, size_t elem, bool bf16)
+             int N, int T, int H, int dk, int dv, size_t elem, bool bf16, int max_seqs = kMaxSeqs)
 {
     if (!cu) return KDA_ERR_NULL;
     if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
@@ -95,7 +95,7 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
     } else {
         if (dk != 64 || dv != 64) return KDA_ERR_UNSUPPORTED;
     }
-    if (N > kMaxSeqs) return KDA_ERR_UNSUPPORTED;
+    if (N > max_seqs) return KDA_ERR_UNSUPPORTED;
     const void *aligned_ptrs[] = {q, k, v, g, out, s0, s1};
     for (const void *p : aligned_ptrs)
         if (p && !aligned16(p)) return KDA_ERR_ALIGN;
@@ -135,6 +135,25 @@ kda::KdaArgs make_args(const void *q, const void *k, const void *v, const float 
 
 }  // namespace
 
+namespace kda {
+
+int validate_bf16_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                       const int32_t *cu, const float *s0, const void *out, const float *s1, int N, int T, int H,
+                       int dk, int dv, int max_seqs)
+{
+    return validate(q, k, v, g, beta, cu, s0, out, s1, N, T, H, dk, dv, sizeof(uint16_t), true, max_seqs);
+}
+
+int error_word_address(int **out)
+{
+    DevInfo *d = nullptr;
+    const int st = device_info(&d);
+    if (st == KDA_OK) *out = d->err;
+    return st;
+}
+
+}  // namespace kda
+
 extern "C" {
 
 const char *kda_status_string(int status)
@@ -148,6 +167,8 @@ const char *kda_status_string(int status)
     case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS: an output overlaps another argument";
     case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call failed (see cudaGetLastError)";
     case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE: no CUDA device, or the device is not sm_103";
+    case KDA_ERR_NOALLOC_LIMIT:
+        return "KDA_ERR_NOALLOC_LIMIT: N is above KDA_NOALLOC_MAX_SEQS, the size of the library-held scratch";
     default: return "unknown kda_status";
     }
 }

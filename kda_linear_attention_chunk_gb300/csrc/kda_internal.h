@@ -19,10 +19,23 @@ struct KdaArgs {
     int *err_word;                  // device address of the sticky error word
     unsigned int *sched;            // 2 words of device scratch for the dynamic unit deal (reset by the kernel), or nullptr
     int num_sms;                    // SM count of the current device
+    // optional: a length-sorted unit order prepared in device memory (any N);
+    // when set, the tensor-core kernel reads its sequence table from here
+    const int *g_order = nullptr;   // [N] sequence indices, longest first
+    const int2 *g_rows = nullptr;   // [N] clamped {bos, eos}
+    const int *g_units_nonempty = nullptr;   // nonempty sequences x H
 };
 
 cudaError_t launch_kda_simt_f32_d64(const KdaArgs &a);
 cudaError_t launch_kda_simt_bf16_d128(const KdaArgs &a);
 cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a);
+int tc_max_sorted_seqs();   // largest N the tensor-core kernel sorts by itself
+
+// kda_api.cu: the checks of kda_chunk_prefill with another limit on N, and the
+// current device's error-word address (also checks the device)
+int validate_bf16_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                       const int32_t *cu, const float *s0, const void *out, const float *s1, int N, int T, int H,
+                       int dk, int dv, int max_seqs);
+int error_word_address(int **out);
 
 }  // namespace kda

@@ -131,7 +131,10 @@ struct TcParams {
     __nv_bfloat16 *out;
     float *s1;
     int N, T, H;
-    int sorted;        // 1 if the sequence order was sorted (N <= kMaxSortedSeqs)
+    int sorted;        // 1: sorted here (N <= kMaxSortedSeqs); 2: sorted order given in g_order/g_rows; 0: unsorted
+    const int *g_order;
+    const int2 *g_rows;
+    const int *g_une;
     int *err;
     unsigned int *sched;   // dynamic deal: [claim counter, finished CTAs], or nullptr
 };
@@ -176,10 +179,15 @@ __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, in
     const int su = u / p.H;
     x.h = u % p.H;
     int b, e;
-    if (p.sorted) {
+    if (p.sorted == 1) {
         // order[] is followed in shared memory by the clamped {bos, eos} rows
         x.n = order[su];
         const int2 be = reinterpret_cast<const int2 *>(order + kMaxSortedSeqs)[x.n];
+        b = be.x;
+        e = be.y;
+    } else if (p.sorted == 2) {
+        x.n = p.g_order[su];
+        const int2 be = p.g_rows[x.n];
         b = be.x;
         e = be.y;
     } else {
@@ -1213,7 +1221,19 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     int *order = sm.ptr<int>(kOffOrder);
 
     // schedule: sequences sorted by length, longest first (ties: lower index)
-    if (p.sorted) {
+    if (p.sorted == 2) {
+        // the sorted order and the row table were prepared in device memory
+        if (tid == 0 && !p.sched) *sm.sched_len() = -1;
+        if (tid == 0 && p.sched) {
+            const int une = *p.g_une;
+            const bool first = (int)blockIdx.x < une;
+            *sm.units_nonempty() = une;
+            sm.sched()[0] = first ? (int)blockIdx.x : -1;
+            *sm.published() = first ? 1 : 0;
+            *sm.claim_done() = first ? 0 : 1;
+            *sm.sched_len() = -2;
+        }
+    } else if (p.sorted) {
         int *lens = sm.ptr<int>(kOffP);
         int2 *rows = reinterpret_cast<int2 *>(order + kMaxSortedSeqs);
         for (int n = tid; n < p.N; n += kThreads) {
@@ -1397,6 +1417,8 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem
 
 }  // namespace
 
+int tc_max_sorted_seqs() { return kMaxSortedSeqs; }
+
 cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
 {
     CUtensorMap tq, tk, tv, tg;
@@ -1425,7 +1447,10 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     p.N = a.N;
     p.T = a.T;
     p.H = a.H;
-    p.sorted = a.N <= kMaxSortedSeqs ? 1 : 0;
+    p.sorted = a.g_order ? 2 : (a.N <= kMaxSortedSeqs ? 1 : 0);
+    p.g_order = a.g_order;
+    p.g_rows = a.g_rows;
+    p.g_une = a.g_units_nonempty;
     p.err = a.err_word;
     p.sched = a.sched;
     const int units = a.N * a.H;
