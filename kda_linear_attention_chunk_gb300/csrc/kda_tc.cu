@@ -101,8 +101,9 @@ constexpr uint32_t kOffMisc = kOffBar + 256;     // TMEM base, abort flag, sched
 // the start of chunk i+1 (or at the end of the unit), and only chunk i+3's
 // decay scan, which waits for chunk i+1's stage, can overwrite it.
 constexpr uint32_t kOffPend = kOffMisc + 128;
-constexpr uint32_t kOffOT = kOffPend + 3 * 512;             // output transpose, bf16 [32][128]
-constexpr uint32_t kSmemBytes = kOffOT + 8192 + 1024;       // + alignment slack
+constexpr uint32_t kOffOT = kOffPend + 3 * 512;             // output transpose, bf16 [32][128], rows 272 B apart
+constexpr uint32_t kOTRow = 272;
+constexpr uint32_t kSmemBytes = kOffOT + 32 * kOTRow + 1024;   // + alignment slack
 
 // mbarrier slots ([2] = one per stage)
 constexpr int kBarKQFull = 0;      // [2]: k, q tiles landed
@@ -939,36 +940,55 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
 // =============================================================================
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
-// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L,
-// transposed 32 rows at a time through the 8 KB output buffer so the global
-// stores are 16-byte row pieces.  TMEM P_s may be reused (o_done) as soon as
-// every lane has read it.
+// O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L.
+// TMEM is read in the warp-MMA fragment layout (16x256b), and stmatrix.trans
+// writes each 8 x 8 block transposed into the output buffer (32 rows at a time,
+// rows padded to 272 bytes so the 8 rows of a block fall in distinct banks);
+// the global stores are then 16-byte row pieces.  TMEM P_s may be reused
+// (o_done) as soon as every lane has read it.
 __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, int s, int row0, int L, int h,
                                 int v, int item)
 {
-    const int w = v >> 5;
-    uint32_t o[64];
+    const int w = v >> 5, lane = v & 31;
+    uint32_t o[2][4][8];                                  // [16-lane half][16-column block][fragment]
     const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * w) << 16);
-    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(o));
-    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+#pragma unroll
+    for (int hl = 0; hl < 2; hl++)
+#pragma unroll
+        for (int cb = 0; cb < 4; cb++) tmem_ld16x256_x2(src + ((uint32_t)(16 * hl) << 16) + 16 * cb, o[hl][cb]);
     tmem_wait_ld();
     tc_fence_before();
     if (v == 0) KDA_PHASE(1, item, 8);
-    __nv_bfloat16 *ot = sm.ptr<__nv_bfloat16>(kOffOT);   // [32][128]
+    const uint32_t ot = sm.u32(kOffOT);
+    const int mi = lane >> 3, k8 = lane & 7;              // this thread's stored matrix and row
     const size_t row_stride = (size_t)p.H * kD;
     __nv_bfloat16 *dst = p.out + ((size_t)row0 * p.H + h) * kD;
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
+    for (int half = 0; half < 2; half++) {                // output rows 32*half .. +31
 #pragma unroll
-        for (int r = 0; r < 32; r++) ot[r * kD + v] = __float2bfloat16_rn(__uint_as_float(o[32 * half + r]));
+        for (int c2 = 0; c2 < 2; c2++) {
+            const int cb = 2 * half + c2;
+#pragma unroll
+            for (int hl = 0; hl < 2; hl++) {
+                const uint32_t *f = o[hl][cb];
+                const int rl = 16 * c2 + ((mi & 2) ? 8 : 0) + k8;          // row within the buffer
+                const int vc = 32 * w + 16 * hl + ((mi & 1) ? 8 : 0);      // first value channel
+                stmatrix_x4_trans(ot + rl * kOTRow + 2 * vc,
+                                  pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1])),
+                                  pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3])),
+                                  pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5])),
+                                  pack_bf16x2(__uint_as_float(f[6]), __uint_as_float(f[7])));
+            }
+        }
         named_bar(kBarChain, kChainThreads);
         if (half == 0 && v == 0) mbar_arrive(sm.bar(kBarODone + s));   // every lane has read TMEM P_s
+        const uint8_t *ob = sm.base + kOffOT;
 #pragma unroll
         for (int k = 0; k < 4; k++) {
             const int idx = v + 128 * k, r = idx >> 4, q = idx & 15;
             if (32 * half + r < L)
                 *reinterpret_cast<uint4 *>(dst + (size_t)(32 * half + r) * row_stride + 8 * q) =
-                    *reinterpret_cast<const uint4 *>(ot + r * kD + 8 * q);
+                    *reinterpret_cast<const uint4 *>(ob + r * kOTRow + 16 * q);
         }
         named_bar(kBarChain, kChainThreads);             // the buffer is free again
     }
