@@ -115,7 +115,7 @@ constexpr int kBarODone = 10;      // [2]: the chain has read a chunk's outputs 
 constexpr int kBarFmReady = 12;    // [2]: the chunk's decay constants are written (128 arrivals)
 constexpr int kBarKmFree = 14;     // [2]: the chain's MMAs on the stage are done (Km, B free)
 constexpr int kBarGFull = 16;      // g slot landed
-constexpr int kBarWFull = 17, kBarMma1 = 18, kBarMma1O = 19, kBarMma3 = 20, kBarDrain = 21;
+constexpr int kBarWFull = 17, kBarMma1 = 18, kBarMma3 = 20, kBarDrain = 21;
 constexpr int kMaxRounds = 24;     // longest per-CTA unit list of the balanced deal
 
 // TMEM columns
@@ -847,27 +847,41 @@ __device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
     }
 }
 
-// -W'^T (TMEM, lane = key channel c, column = row r) -> fp16 MN-major [c][r]
-// in the stage's K region (Kp is dead once MMA-b is done): channels 0-63 where
-// the first K half was, 64-127 where the second was
+// -W'^T (TMEM, lane = key channel c, column = row r) -> -W' as fp16 K-major
+// [r][c] in the stage's K rows (Kp is dead once MMA-b is done), so that
+// [-W' ; Qp] is one 128-row operand for MMA1.  TMEM is read in the warp-MMA
+// fragment layout and each 8 x 8 block is stored transposed (stmatrix.trans).
+// Then the TMEM columns MMA1 accumulates the output into are zeroed.
 __device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
 {
     const int iw = it >> 5, lane = it & 31;
-    const int c = 32 * iw + lane;
-    uint32_t a[64];
+    const int mi = lane >> 3, k8 = lane & 7;              // this thread's stored matrix and row
     const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * iw) << 16);
-    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(a));
-    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-    tmem_wait_ld();
-    uint8_t *Wt = sm.base + s * kStageBytes + kOffKQ + (c >> 6) * 16384;
+    const uint32_t kq = sm.u32(s * kStageBytes + kOffKQ);
 #pragma unroll
-    for (int q = 0; q < 8; q++) {
-        uint32_t w[4];
+    for (int hl = 0; hl < 2; hl++) {
+        uint32_t f[4][8];                                 // [16-column block][fragment]
 #pragma unroll
-        for (int e = 0; e < 4; e++)
-            w[e] = pack_f16x2(-__uint_as_float(a[8 * q + 2 * e]), -__uint_as_float(a[8 * q + 2 * e + 1]));
-        *reinterpret_cast<uint4 *>(Wt + sw128_chunk(c & 63, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int cb = 0; cb < 4; cb++) tmem_ld16x256_x2(src + ((uint32_t)(16 * hl) << 16) + 16 * cb, f[cb]);
+        tmem_wait_ld();
+        const int c = 32 * iw + 16 * hl + ((mi & 1) ? 8 : 0);          // first key channel of the block
+        const uint32_t base = kq + (c >> 6) * 16384;
+#pragma unroll
+        for (int cb = 0; cb < 4; cb++) {
+            const int r = 16 * cb + ((mi & 2) ? 8 : 0) + k8;
+            stmatrix_x4_trans(base + sw128_chunk(r, (c & 63) >> 3),
+                              pack_f16x2(-__uint_as_float(f[cb][0]), -__uint_as_float(f[cb][1])),
+                              pack_f16x2(-__uint_as_float(f[cb][2]), -__uint_as_float(f[cb][3])),
+                              pack_f16x2(-__uint_as_float(f[cb][4]), -__uint_as_float(f[cb][5])),
+                              pack_f16x2(-__uint_as_float(f[cb][6]), -__uint_as_float(f[cb][7])));
+        }
     }
+    uint32_t z[32];
+#pragma unroll
+    for (int j = 0; j < 32; j++) z[j] = 0u;
+    tmem_st32(src, z);
+    tmem_st32(src + 32, z);
+    tmem_wait_st();
 }
 
 __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int U)
@@ -1101,27 +1115,27 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 KDA_PHASE(1, item, 12);
                 tc_fence_after();
                 const uint32_t st = sm.u32(s * kStageBytes);
-                const uint32_t id_w = idesc_f16(128, 64, 0, 1), id_q = idesc_f16(128, 64, 0, 0);
-                // Delta half first (it gates the chain), then the output half; -W' sits
-                // in the K region, channels 0-63 and 64-127 16 KB apart
-#pragma unroll
-                for (int ks = 0; ks < 8; ks++) {
-                    const uint64_t bw = smem_desc_sw128(st + kOffKQ + (ks >> 2) * 16384 + (ks & 3) * 2048, 16, 1024);
-                    mma_ts(tmem + kTmP + 128 * s, tmem + kTmS0h + 8 * ks, bw, id_w, 1);
-                }
-                mma_commit(sm.bar(kBarMma1));
+                // [U^T | 0] += S'^T [-W' ; Qp]^T: the Delta half and the output half in
+                // one N = 128 MMA (the K rows of each stage block hold -W', the Q rows Qp)
+                const uint32_t id1 = idesc_f16(128, 128, 0, 0);
 #pragma unroll
                 for (int ks = 0; ks < 8; ks++) {
                     const int kb = ks >> 2, kin = ks & 3;
-                    const uint64_t bq = smem_desc_sw128(st + kOffKQ + kb * 16384 + 8192 + kin * 32, 16, 1024);
-                    mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmS0h + 8 * ks, bq, id_q, ks > 0);
+                    const uint64_t bwq = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
+                    mma_ts(tmem + kTmP + 128 * s, tmem + kTmS0h + 8 * ks, bwq, id1, 1);
                 }
-                mma_commit(sm.bar(kBarMma1O));
+                mma_commit(sm.bar(kBarMma1));
                 KDA_PHASE(1, item, 1);
             }
             ok = mbar_wait(sm.bar(kBarMma1), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (v == 0) KDA_PHASE(1, item, 2);
+            if (v == 0) {
+                KDA_PHASE(1, item, 2);
+                if (kq_pending) {                             // -W' and Qp have been read
+                    issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+                    kq_pending = false;
+                }
+            }
             tc_fence_after();
             // Delta^T (fp32, TMEM) -> fp16 A operand
             {
@@ -1159,13 +1173,6 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 }
                 mma_commit(sm.bar(kBarMma3));
                 KDA_PHASE(1, item, 13);
-                // -W' and Qp have been read: chunk item+2's k and q may land
-                if (!mbar_wait(sm.bar(kBarMma1O), item & 1, sm.abort_flag())) {
-                    record_error(p, sm, kErrWaitTimeout);
-                } else if (kq_pending) {
-                    issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
-                    kq_pending = false;
-                }
                 KDA_PHASE(1, item, 3);
             }
             // every MMA of this chunk is done: Km and B are free, O^T is final
@@ -1340,7 +1347,6 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         mbar_init(sm.bar(kBarGFull), 1);
         mbar_init(sm.bar(kBarWFull), 1);
         mbar_init(sm.bar(kBarMma1), 1);
-        mbar_init(sm.bar(kBarMma1O), 1);
         mbar_init(sm.bar(kBarMma3), 1);
         mbar_init(sm.bar(kBarDrain), 3);
         mbar_fence_init();
