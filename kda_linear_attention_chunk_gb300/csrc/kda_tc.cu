@@ -71,9 +71,10 @@ __device__ __forceinline__ unsigned long long kda_gtimer()
 #endif
 
 constexpr int kD = 128;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kChainThreads = 128;
-constexpr int kGroupThreads = 128;                  // prep groups E and I
+constexpr int kEThreads = 256;                      // prep group E (warps 4-11)
+constexpr int kGroupThreads = 128;                  // prep group I (warps 12-15)
 constexpr int kBarChain = 1, kBarE = 2, kBarI = 3;   // named barriers
 constexpr int kMaxSortedSeqs = 256;
 
@@ -385,80 +386,82 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // unrolling.
 // =============================================================================
 
-// Group E's decay pass over one chunk; `beta_r` is the beta of row et (zero
-// past the chunk), loaded a chunk ahead.
-// Scan: thread = (row group ew: rows 16*ew .. +15) x (key channels 4*lane ..
-// +3); the row prefix of g * log2(e) runs in registers, the four row groups
-// exchange their totals once, and G (in base 2) is written back over g in the
-// g slot.
-// Operands: thread = (row 16*ew + 8*hf + (lane & 7)) x (channels 32*cg + 8*j ..
-// +7, cg = lane >> 3), 16-byte accesses; Kp = beta*K*exp(G - G_m),
+// Group E's decay pass over one chunk (256 threads); `beta_r` is the beta of
+// row et (zero past the chunk), loaded a chunk ahead.
+// Scan: thread = (row group ew: rows 16*ew .. +15) x (channel half chh) x (key
+// channels 64*chh + 2*lane, +1); the row prefix of g * log2(e) runs in
+// registers, the four row groups exchange their totals once, and G (in base 2)
+// is written back over g in the g slot.
+// Operands: thread = (row 8*w + (lane & 7), w = et / 32) x (channels 32*cg +
+// 8*j .. +7, cg = lane >> 3), 16-byte accesses; Kp = beta*K*exp(G - G_m),
 // Qp = Q*exp(G - G_m) and Km = K*exp(G_m - G) become fp16 in place over the
 // bf16 tiles (rows past the chunk zero).  Returns false if a wait ran out.
 __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r)
 {
-    const int ew = et >> 5, lane = et & 31;
+    const int lane = et & 31;
     const uint32_t st = s * kStageBytes;
     float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
     float *gmx = sm.ptr<float>(kOffGm), *glx = gmx + 128;
     const int m = (L - 1) >> 1;
     {
-        float4 *xchg = sm.ptr<float4>(kOffEScr);            // [4 row groups][32 channel quads]
-        uint8_t *gb = sm.base + kOffG + (lane >> 3) * 8192;
-        const int jc = lane & 7;
-        float4 x[16];
+        const int ew = (et >> 5) & 3, chh = et >> 7;
+        const int c0 = 64 * chh + 2 * lane;                  // this thread's two channels
+        float *xchg = sm.ptr<float>(kOffEScr);               // [4 row groups][128 channels]
+        uint8_t *gb = sm.base + kOffG + (c0 >> 5) * 8192;
+        const int jc = (c0 & 31) >> 2, sub = 8 * (lane & 1);
+        float2 x[16];
 #pragma unroll
         for (int t = 0; t < 16; t++) {
             const int r = 16 * ew + t;
-            float4 g4 = r < L ? *reinterpret_cast<const float4 *>(gb + sw128_chunk(r, jc)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            x[t] = make_float4(g4.x * kLog2e, g4.y * kLog2e, g4.z * kLog2e, g4.w * kLog2e);   // base-2 log-decay
+            const float2 g2 = r < L ? *reinterpret_cast<const float2 *>(gb + sw128_chunk(r, jc) + sub) : make_float2(0.f, 0.f);
+            x[t] = make_float2(g2.x * kLog2e, g2.y * kLog2e);   // base-2 log-decay
         }
 #pragma unroll
         for (int t = 1; t < 16; t++) {
-            x[t].x += x[t - 1].x; x[t].y += x[t - 1].y; x[t].z += x[t - 1].z; x[t].w += x[t - 1].w;
+            x[t].x += x[t - 1].x; x[t].y += x[t - 1].y;
         }
-        xchg[ew * 32 + lane] = x[15];
-        named_bar(kBarE, kGroupThreads);
-        float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float2 *>(xchg + ew * 128 + c0) = x[15];
+        named_bar(kBarE, kEThreads);
+        float2 pre = make_float2(0.f, 0.f);
         for (int w = 0; w < ew; w++) {
-            const float4 y = xchg[w * 32 + lane];
-            pre.x += y.x; pre.y += y.y; pre.z += y.z; pre.w += y.w;
+            const float2 y = *reinterpret_cast<const float2 *>(xchg + w * 128 + c0);
+            pre.x += y.x; pre.y += y.y;
         }
 #pragma unroll
         for (int t = 0; t < 16; t++) {
-            x[t].x += pre.x; x[t].y += pre.y; x[t].z += pre.z; x[t].w += pre.w;
+            x[t].x += pre.x; x[t].y += pre.y;
             const int r = 16 * ew + t;
-            *reinterpret_cast<float4 *>(gb + sw128_chunk(r, jc)) = x[t];
-            if (r == m) *reinterpret_cast<float4 *>(gmx + 4 * lane) = x[t];
-            if (r == L - 1) *reinterpret_cast<float4 *>(glx + 4 * lane) = x[t];
+            *reinterpret_cast<float2 *>(gb + sw128_chunk(r, jc) + sub) = x[t];
+            if (r == m) *reinterpret_cast<float2 *>(gmx + c0) = x[t];
+            if (r == L - 1) *reinterpret_cast<float2 *>(glx + c0) = x[t];
         }
     }
     if (et < kChunk) cst[256 + et] = beta_r;
-    named_bar(kBarE, kGroupThreads);
+    named_bar(kBarE, kEThreads);
     // k and q of this chunk have landed -- so the chain is past its MMA1 of chunk
     // item-2 and no longer reads that chunk's fm or pend slot -- and Km of chunk
     // item-2 is no longer read
     if (et == 0) KDA_PHASE(0, item, 15);
     bool ok = mbar_wait(sm.bar(kBarKQFull + s), (item >> 1) & 1, sm.abort_flag());
     if (ok && item >= 2) ok = mbar_wait(sm.bar(kBarKmFree + s), ((item >> 1) - 1) & 1, sm.abort_flag());
-    if (role_any(!ok, kBarE, kGroupThreads)) return false;
+    if (role_any(!ok, kBarE, kEThreads)) return false;
     if (et == 0) KDA_PHASE(0, item, 14);
-    // chain constants, one thread per key channel
-    cst[et] = ex2(gmx[et]);                                                  // view from row m
-    sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = ex2(glx[et] - gmx[et]);  // row m -> last row
-    mbar_arrive(sm.bar(kBarFmReady + s));
+    if (et < 128) {   // chain constants, one thread per key channel
+        cst[et] = ex2(gmx[et]);                                                  // view from row m
+        sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = ex2(glx[et] - gmx[et]);  // row m -> last row
+        mbar_arrive(sm.bar(kBarFmReady + s));
+    }
     if (et == 0) KDA_PHASE(0, item, 10);
     const int rr = lane & 7, cg = lane >> 3, kb = cg >> 1;
+    const int r = 8 * (et >> 5) + rr;
+    const bool valid = r < L;
+    const float br = cst[256 + r];                     // zero past the chunk
     uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
     uint8_t *qt = kt + 8192;
     uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
     const uint8_t *gt = sm.base + kOffG + cg * 8192;
 #pragma unroll 2
-    for (int step = 0; step < 8; step++) {
-        const int j = step & 3;
-        const int r = 16 * ew + 8 * (step >> 2) + rr;
-        const bool valid = r < L;
-        const float br = cst[256 + r];                 // zero past the chunk
+    for (int j = 0; j < 4; j++) {
         const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
         const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
         const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
@@ -500,8 +503,8 @@ __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
     uint8_t *vt = sm.base + s * kStageBytes + kOffV;
     const float *bt = sm.ptr<float>(kOffConst + s * kConstBytes) + 256;
 #pragma unroll 2
-    for (int i = 0; i < 8; i++) {
-        const int idx = et + 128 * i;              // 16-byte chunk index in the 16 KB tile
+    for (int i = 0; i < 4; i++) {
+        const int idx = et + kEThreads * i;        // 16-byte chunk index in the 16 KB tile
         const int r = (idx >> 3) & 63;
         uint4 *ptr = reinterpret_cast<uint4 *>(vt + idx * 16);
         const uint4 w = *ptr;
@@ -588,14 +591,14 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             const float beta_r = beta_next;
             if (et == 0) publish();
             bool ok = mbar_wait(sm.bar(kBarGFull), item & 1, sm.abort_flag());
-            if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (role_any(!ok, kBarE, kEThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (et == 0) KDA_PHASE(0, item, 0);
             if (!e_pass(sm, s, item, L, et, beta_r)) {
                 if (et == 0) record_error(p, sm, kErrWaitTimeout);
                 return;
             }
             fence_proxy_async_smem();
-            named_bar(kBarE, kGroupThreads);               // operands written, the g slot read
+            named_bar(kBarE, kEThreads);                   // operands written, the g slot read
             if (et == 0) {
                 KDA_PHASE(0, item, 1);
                 // TMEM P_s is free once the chain has read chunk item-2's outputs
@@ -619,7 +622,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             if (et == 0) KDA_PHASE(2, item, 6);
             ok = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
             if (et == 0) KDA_PHASE(2, item, 4);
-            if (role_any(!ok, kBarE, kGroupThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (role_any(!ok, kBarE, kEThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (et == 0) KDA_PHASE(2, item, 5);
             e_convert_v(sm, s, L, et);
             fence_proxy_async_smem();
@@ -886,7 +889,7 @@ __device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
 
 __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int U)
 {
-    const int it = threadIdx.x - kChainThreads - kGroupThreads;
+    const int it = threadIdx.x - kChainThreads - kEThreads;
     const uint32_t tmem = *sm.tmem_base();
     {   // zeros that stay for the whole kernel: T16's 16-byte chunks right of each
         // row's diagonal block, and the upper-right 16x16 blocks of D0 and D1
@@ -1014,15 +1017,14 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem
 __device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float *fm, const float *pend)
 {
 #pragma unroll 1
-    for (int half = 0; half < 2; half++) {
-        uint32_t x[64];
-        tmem_ld32(tmem + kTmS + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(x));
-        tmem_ld32(tmem + kTmS + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+    for (int q = 0; q < 4; q++) {                       // 32 key channels at a time
+        uint32_t x[32];
+        tmem_ld32(tmem + kTmS + lane_off + 32 * q, x);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-            const float4 f4 = *reinterpret_cast<const float4 *>(fm + 64 * half + j);
-            const float4 p4 = pend ? *reinterpret_cast<const float4 *>(pend + 64 * half + j)
+        for (int j = 0; j < 32; j += 4) {
+            const float4 f4 = *reinterpret_cast<const float4 *>(fm + 32 * q + j);
+            const float4 p4 = pend ? *reinterpret_cast<const float4 *>(pend + 32 * q + j)
                                    : make_float4(1.f, 1.f, 1.f, 1.f);
             const float fv[4] = {f4.x, f4.y, f4.z, f4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
@@ -1032,16 +1034,11 @@ __device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float 
                 x[j + e] = __float_as_uint(__fmul_rn(f, fv[e]));
             }
         }
-        uint32_t h0[16], h1[16];
+        uint32_t h[16];
 #pragma unroll
-        for (int j = 0; j < 16; j++) {
-            h0[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-            h1[j] = pack_f16x2(__uint_as_float(x[32 + 2 * j]), __uint_as_float(x[32 + 2 * j + 1]));
-        }
-        tmem_st32(tmem + kTmS + lane_off + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(x));
-        tmem_st32(tmem + kTmS + lane_off + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
-        tmem_st16(tmem + kTmS0h + lane_off + 32 * half, h0);
-        tmem_st16(tmem + kTmS0h + lane_off + 32 * half + 16, h1);
+        for (int j = 0; j < 16; j++) h[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+        tmem_st32(tmem + kTmS + lane_off + 32 * q, x);
+        tmem_st16(tmem + kTmS0h + lane_off + 16 * q, h);
     }
     tmem_wait_st();
 }
@@ -1339,7 +1336,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             mbar_init(sm.bar(kBarVFull + i), 1);
             mbar_init(sm.bar(kBarPrepDone + i), 1);
             mbar_init(sm.bar(kBarAFull + i), 1);
-            mbar_init(sm.bar(kBarEDone + i), kGroupThreads);
+            mbar_init(sm.bar(kBarEDone + i), kEThreads);
             mbar_init(sm.bar(kBarODone + i), 1);
             mbar_init(sm.bar(kBarFmReady + i), kGroupThreads);
             mbar_init(sm.bar(kBarKmFree + i), 1);
@@ -1368,13 +1365,13 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     const Maps maps = {&tq, &tk, &tv, &tg};
     if (warp < 4) {
         chain_role(p, sm, order, U, maps);
-    } else if (warp < 8) {
+    } else if (warp < 12) {
         e_role(p, sm, order, U, maps);
     } else {
         i_role(p, sm, order, U);
     }
     // every MMA this CTA issued has completed before TMEM is released
-    if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kGroupThreads) {
+    if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads) {
         mma_commit(sm.bar(kBarDrain));
         mbar_wait(sm.bar(kBarDrain), 0, sm.abort_flag(), 1u << 14);
     }
