@@ -109,14 +109,14 @@ constexpr uint32_t kSmemBytes = kOffOT + 32 * kOTRow + 1024;   // + alignment sl
 // mbarrier slots ([2] = one per stage)
 constexpr int kBarKQFull = 0;      // [2]: k, q tiles landed
 constexpr int kBarVFull = 2;       // [2]: v tile landed
-constexpr int kBarPrepDone = 4;    // [2]: prep finished a chunk (-W' written)
+constexpr int kBarPrepDone = 4;    // [2]: MMA-b of a chunk is done (W'^T and U^T in TMEM)
 constexpr int kBarAFull = 6;       // [2]: MMA-a done
 constexpr int kBarEDone = 8;       // [2]: group E finished a chunk's operands (128 arrivals)
 constexpr int kBarODone = 10;      // [2]: the chain has read a chunk's outputs (TMEM P_s free)
 constexpr int kBarFmReady = 12;    // [2]: the chunk's decay constants are written (128 arrivals)
 constexpr int kBarKmFree = 14;     // [2]: the chain's MMAs on the stage are done (Km, B free)
 constexpr int kBarGFull = 16;      // g slot landed
-constexpr int kBarWFull = 17, kBarMma1 = 18, kBarMma3 = 20, kBarDrain = 21;
+constexpr int kBarMma1 = 18, kBarMma3 = 20, kBarDrain = 21;
 constexpr int kMaxRounds = 24;     // longest per-CTA unit list of the balanced deal
 
 // TMEM columns
@@ -913,8 +913,11 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const uint32_t ph = (item >> 1) & 1;
-            // MMA-a done implies group E's operand pass is over
+            // MMA-a done implies group E's operand pass is over; MMA-b of the previous
+            // chunk must be done before T16 is rewritten
             bool ok = mbar_wait(sm.bar(kBarAFull + s), ph, sm.abort_flag());
+            if (ok && item >= 1)
+                ok = mbar_wait(sm.bar(kBarPrepDone + ((item - 1) & 1)), ((item - 1) >> 1) & 1, sm.abort_flag());
             if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (it == 0) KDA_PHASE(0, item, 5);
             tc_fence_after();
@@ -934,21 +937,10 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
                     KDA_PHASE(0, item, 7);
                     tc_fence_after();
                     issue_mma_b(sm, s, tmem);
-                    mma_commit(sm.bar(kBarWFull));
-                    KDA_PHASE(2, item, 3);
+                    mma_commit(sm.bar(kBarPrepDone + s));     // the chain takes W' from here
+                    KDA_PHASE(0, item, 8);
+                    KDA_PHASE(0, item, 9);
                 }
-            }
-            ok = mbar_wait(sm.bar(kBarWFull), item & 1, sm.abort_flag());
-            if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (it == 0) KDA_PHASE(0, item, 8);
-            tc_fence_after();
-            i_read_w(sm, s, tmem, it);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar(kBarI, kGroupThreads);
-            if (it == 0) {
-                KDA_PHASE(0, item, 9);
-                mbar_arrive(sm.bar(kBarPrepDone + s));
             }
         }
     }
@@ -1102,6 +1094,12 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             tc_fence_before();
             ok = mbar_wait(sm.bar(kBarPrepDone + s), ph, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            // -W' out of TMEM into the K rows of the stage (and the output columns zeroed)
+            tc_fence_after();
+            i_read_w(sm, s, tmem, v);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(kBarChain, kChainThreads);
             if (v == 0) {
                 KDA_PHASE(1, item, 11);
                 // MMA-b is done with V: chunk item+2's v may land
@@ -1342,7 +1340,6 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             mbar_init(sm.bar(kBarKmFree + i), 1);
         }
         mbar_init(sm.bar(kBarGFull), 1);
-        mbar_init(sm.bar(kBarWFull), 1);
         mbar_init(sm.bar(kBarMma1), 1);
         mbar_init(sm.bar(kBarMma3), 1);
         mbar_init(sm.bar(kBarDrain), 3);
