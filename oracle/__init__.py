@@ -110,3 +110,51 @@ def run(q, k, v, g, beta, cu_seqlens, initial_state=None, heads=None, chunk: int
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
     return out, fin
+
+
+def run_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_pool, out=None, heads=None,
+              chunk: int = 0, nthreads: Optional[int] = None, lib=None):
+    """Slot-indexed states (kern-k3-pp-prefill README, section "D inside
+    SGLang": a KDA layer's recurrent state sits in a pool laid out
+    [slot][head][v][k] f32, reached through a table of slot ids, and padded
+    entries carry slot -1, which the kernel skips).
+
+    Sequence n starts from state_pool[state_slots[n]] and its final state
+    replaces that entry.  A sequence whose slot id is -1 is padding: nothing
+    of it is computed, its rows of `out` keep what they held and the pool is
+    not touched.  An id outside [-1, num_slots) is handled like -1 and
+    reported.  Valid ids must be distinct (two sequences cannot own one
+    state).
+
+    Inputs as run(); state_slots: [N] int; state_pool: [num_slots][nsel][dv][dk];
+    out: [T][nsel][dv] values kept in the skipped rows (default NaN).
+    Returns (out [T][nsel][dv], pool [num_slots][nsel][dv][dk], both float64,
+    and the list of sequence indices whose id was out of range).
+    """
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    slots = np.asarray(state_slots, dtype=np.int64)
+    pool = np.array(state_pool, dtype=np.float64)          # a copy: updated below
+    num_slots = pool.shape[0]
+    N = cu.shape[0] - 1
+    assert slots.shape == (N,), slots.shape
+    T = q.shape[0]
+    nsel = pool.shape[1]
+    dv = v.shape[2]
+    res = (np.full((T, nsel, dv), np.nan) if out is None else np.array(out, dtype=np.float64))
+    bad = [n for n in range(N) if slots[n] < -1 or slots[n] >= num_slots]
+    live = [n for n in range(N) if 0 <= slots[n] < num_slots]
+    if len(set(int(slots[n]) for n in live)) != len(live):
+        raise ValueError("two sequences name the same state slot")
+    if not live:
+        return res, pool, bad
+    # The live sequences, packed back to back, form one ordinary call whose
+    # initial states are gathered from the pool.
+    rows = np.concatenate([np.arange(cu[n], cu[n + 1]) for n in live]).astype(np.int64)
+    lens = [int(cu[n + 1] - cu[n]) for n in live]
+    sub_cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    sub_out, fin = run(q[rows], k[rows], v[rows], g[rows], beta[rows], sub_cu,
+                       initial_state=pool[slots[live]], heads=heads, chunk=chunk,
+                       nthreads=nthreads, lib=lib)
+    res[rows] = sub_out
+    pool[slots[live]] = fin
+    return res, pool, bad
