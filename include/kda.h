@@ -137,14 +137,50 @@ int kda_chunk_prefill_noalloc(const uint16_t *q, const uint16_t *k, const uint16
                               const float *initial_state, uint16_t *out, float *final_state,
                               int N, int T, int H, int dk, int dv, void *stream);
 
+/*
+ * kda_chunk_prefill_slots -- kda_chunk_prefill with the recurrent states kept
+ * in a pool that a serving engine owns and addresses by slot id (kern-k3-pp-
+ * prefill README, section "D inside SGLang": a KDA layer's state lives in the
+ * engine's pool laid out [slot][head][v][k] f32 and is reached through a
+ * table of slot ids, where a padded entry carries slot -1 and is skipped).
+ *
+ *   state_slots  int32 [N], device memory: the pool entry of sequence n.
+ *                -1 marks a padded sequence: nothing of it is computed, its
+ *                rows of `out` are not written and the pool is not touched.
+ *   state_pool   fp32 [num_slots][H][dv][dk], device memory.  Sequence n
+ *                starts from state_pool[state_slots[n]] and its final state
+ *                replaces that entry (in place).  Entries that no sequence
+ *                names are not touched.  A sequence of zero rows leaves its
+ *                entry as it was.
+ *   num_slots    entries in the pool (>= 1).
+ * All other arguments, layouts and limits are those of kda_chunk_prefill
+ * (which takes dense [N][H][dv][dk] states instead).
+ *
+ * The ids are not read on the host.  Valid ids must be distinct: two
+ * sequences that name one entry race on it.  An id outside [-1, num_slots)
+ * is treated like -1 and sets bit 8 of the device error word
+ * (kda_device_error).  Results for a sequence equal, bit for bit, those of
+ * kda_chunk_prefill given the same rows and that sequence's entry as its
+ * initial state.  Returns a kda_status; KDA_ERR_NULL if state_slots or
+ * state_pool is NULL, KDA_ERR_SHAPE if num_slots < 1, KDA_ERR_ALIAS if the
+ * pool overlaps any other argument.
+ */
+int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const float *g, const float *beta, const int32_t *cu_seqlens,
+                            const int32_t *state_slots, float *state_pool, int num_slots,
+                            uint16_t *out, int N, int T, int H, int dk, int dv, void *stream);
+
 /* Human-readable name of a kda_status value (static string, never NULL). */
 const char *kda_status_string(int status);
 
 /*
  * kda_device_error -- read the library's sticky device error word on the
  * current device.  Every wait inside the kernels is bounded; a wait that runs
- * out sets a bit here and the kernel returns early (outputs are then
- * undefined).  0 means no kernel of this library has reported an error.
+ * out sets bit 1 here and the kernel returns early (outputs are then
+ * undefined).  Bit 2: a cu_seqlens entry broke its contract (indices were
+ * clamped).  Bit 8: a state slot id was outside [-1, num_slots) (that
+ * sequence was skipped).  0 means no kernel of this library has reported an
+ * error.
  * Synchronises the current device.  If `reset` is nonzero the word is
  * cleared after reading.  Returns KDA_OK or KDA_ERR_CUDA.
  */

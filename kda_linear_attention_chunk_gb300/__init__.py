@@ -20,7 +20,8 @@ KDA_ERR_NOALLOC_LIMIT = 8
 KDA_NOALLOC_MAX_SEQS = 16384
 
 EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error",
-            "kda_chunk_prefill_noalloc")
+            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots")
+ERR_BAD_SLOT = 8   # device error word bit: a state slot id outside [-1, num_slots)
 
 _lib = None
 
@@ -45,6 +46,8 @@ def load(path: str = LIB_PATH):
         fn = getattr(lib, name)
         fn.argtypes = sig
         fn.restype = I
+    lib.kda_chunk_prefill_slots.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, P]
+    lib.kda_chunk_prefill_slots.restype = I
     lib.kda_status_string.argtypes = [I]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), I]
@@ -82,6 +85,13 @@ def kda_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, initial_state, out, 
     library, for callers that cannot allocate device memory per call)."""
     return load().kda_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, initial_state, out,
                                             final_state, N, T, H, dk, dv, stream)
+
+
+def kda_chunk_prefill_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_pool, num_slots: int, out,
+                            N: int, T: int, H: int, dk: int, dv: int, stream) -> int:
+    """Raw C-ABI call with the states in a slot-addressed pool."""
+    return load().kda_chunk_prefill_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_pool,
+                                          num_slots, out, N, T, H, dk, dv, stream)
 
 
 def device_error(reset: bool = False) -> int:
@@ -131,3 +141,40 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens, initial_state=None, out=None, fi
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_prefill")
     return out, final_state
+
+
+def chunk_prefill_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_pool, out=None, stream=None):
+    """KDA prefill with slot-addressed states, on torch CUDA tensors.
+
+    q, k, v: [T][H][128] bfloat16; g: [T][H][128] float32; beta: [T][H]
+    float32; cu_seqlens: [N+1] int32 and state_slots: [N] int32 on the device
+    (-1 = padded sequence, skipped); state_pool: [num_slots][H][128][128]
+    float32, read and updated in place.  Returns out [T][H][128] bfloat16
+    (rows of padded sequences keep what ``out`` held; a fresh ``out`` is
+    uninitialised there).  Runs asynchronously on ``stream``.
+    """
+    import torch
+
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    N = cu_seqlens.shape[0] - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("cu_seqlens", cu_seqlens),
+                    ("state_slots", state_slots), ("state_pool", state_pool)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("chunk_prefill_slots takes bfloat16 q/k/v")
+    if state_slots.dtype != torch.int32 or tuple(state_slots.shape) != (N,):
+        raise ValueError("state_slots must be int32 [N]")
+    if state_pool.dtype != torch.float32 or tuple(state_pool.shape[1:]) != (H, dv, dk):
+        raise ValueError("state_pool must be float32 [num_slots][H][dv][dk]")
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    handle = int(s.cuda_stream) if hasattr(s, "cuda_stream") else int(s)
+    st = kda_chunk_prefill_slots(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+                                 _ptr(state_slots), _ptr(state_pool), int(state_pool.shape[0]), _ptr(out),
+                                 N, T, H, dk, dv, handle)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_prefill_slots")
+    return out

@@ -79,16 +79,21 @@ int device_info(DevInfo **out)
     return KDA_OK;
 }
 
-// Validation shared by both entry points.  elem = bytes per q/k/v/out element.
+// Validation shared by the entry points.  elem = bytes per q/k/v/out element;
+// the state tensors hold state_n entries of [H][dv][dk] (N unless the states
+// are addressed through the slot table `slots`, an [N] int32 input).
 int validate(const void *q, const void *k, const void *v, const float *g, const float *beta,
              const int32_t *cu, const float *s0, const void *out, const float *s1,
-             int N, int T, int H, int dk, int dv, size_t elem, bool bf16, int max_seqs = kMaxSeqs)
+             int N, int T, int H, int dk, int dv, size_t elem, bool bf16, int max_seqs = kMaxSeqs,
+             const int32_t *slots = nullptr, int state_n = -1)
 {
+    if (state_n < 0) state_n = N;
     if (!cu) return KDA_ERR_NULL;
     if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
     if (N < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return KDA_ERR_SHAPE;
     const size_t rows = (size_t)T * (size_t)H;
-    if ((size_t)N * (size_t)H > 0x7fffffffu || rows * (size_t)(dk > dv ? dk : dv) * 4 >= ((size_t)1 << 40))
+    if ((size_t)N * (size_t)H > 0x7fffffffu || rows * (size_t)(dk > dv ? dk : dv) * 4 >= ((size_t)1 << 40) ||
+        (size_t)state_n * (size_t)H > 0x7fffffffu)
         return KDA_ERR_SHAPE;
     if (bf16) {
         if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
@@ -99,22 +104,24 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
     const void *aligned_ptrs[] = {q, k, v, g, out, s0, s1};
     for (const void *p : aligned_ptrs)
         if (p && !aligned16(p)) return KDA_ERR_ALIGN;
-    if (((uintptr_t)beta & 3u) || ((uintptr_t)cu & 3u)) return KDA_ERR_ALIGN;
+    if (((uintptr_t)beta & 3u) || ((uintptr_t)cu & 3u) || ((uintptr_t)slots & 3u)) return KDA_ERR_ALIGN;
 
-    const size_t state_bytes = (size_t)N * H * dv * dk * sizeof(float);
+    const size_t state_bytes = (size_t)state_n * H * dv * dk * sizeof(float);
     const Range in[] = {range_of(q, rows * dk * elem), range_of(k, rows * dk * elem),
                         range_of(v, rows * dv * elem), range_of(g, rows * dk * sizeof(float)),
                         range_of(beta, rows * sizeof(float)),
                         range_of(cu, (size_t)(N + 1) * sizeof(int32_t)),
+                        range_of(slots, (size_t)N * sizeof(int32_t)),
                         range_of(s0, state_bytes)};
+    constexpr int kStateIn = 7;   // in[kStateIn] is the initial state
     const Range ro = range_of(out, rows * dv * elem);
     const Range rs = range_of(s1, state_bytes);
     for (const Range &r : in)
         if (overlap(ro, r)) return KDA_ERR_ALIAS;
     if (overlap(ro, rs)) return KDA_ERR_ALIAS;
-    for (int i = 0; i < 6; i++)
+    for (int i = 0; i < kStateIn; i++)
         if (overlap(rs, in[i])) return KDA_ERR_ALIAS;
-    if (s0 && s1 && overlap(rs, in[6]) && (s0 != s1)) return KDA_ERR_ALIAS;
+    if (s0 && s1 && overlap(rs, in[kStateIn]) && (s0 != s1)) return KDA_ERR_ALIAS;
     return KDA_OK;
 }
 
@@ -201,6 +208,25 @@ int kda_chunk_prefill_f32(const float *q, const float *k, const float *v, const 
     kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H,
                                dk, dv, stream, d);
     return kda::launch_kda_simt_f32_d64(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                            const float *beta, const int32_t *cu_seqlens, const int32_t *state_slots,
+                            float *state_pool, int num_slots, uint16_t *out, int N, int T, int H, int dk,
+                            int dv, void *stream)
+{
+    if (!state_slots || !state_pool) return KDA_ERR_NULL;
+    if (num_slots < 1) return KDA_ERR_SHAPE;
+    int st = validate(q, k, v, g, beta, cu_seqlens, state_pool, out, state_pool, N, T, H, dk, dv,
+                      sizeof(uint16_t), true, kMaxSeqs, state_slots, num_slots);
+    if (st != KDA_OK) return st;
+    DevInfo *d = nullptr;
+    if ((st = device_info(&d)) != KDA_OK) return st;
+    kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, state_pool, out, state_pool, N, T, H,
+                               dk, dv, stream, d);
+    a.state_slots = state_slots;
+    a.num_slots = num_slots;
+    return kda::launch_kda_tc_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_device_error(int *word, int reset)

@@ -14,6 +14,7 @@ enum : int {
     kErrWaitTimeout = 1,   // a bounded mbarrier wait ran out
     kErrBadSeqlens = 2,    // cu_seqlens violated its contract (indices clamped)
     kErrLayout = 4,        // shared-memory carve-up did not fit (never expected)
+    kErrBadSlot = 8,       // a state slot id outside [-1, num_slots) (that sequence skipped)
 };
 
 __device__ __forceinline__ float load_in(const float *p) { return __ldg(p); }

@@ -24,6 +24,10 @@ struct KdaArgs {
     const int *g_order = nullptr;   // [N] sequence indices, longest first
     const int2 *g_rows = nullptr;   // [N] clamped {bos, eos}
     const int *g_units_nonempty = nullptr;   // nonempty sequences x H
+    // optional: states addressed through a slot table (tensor-core kernel);
+    // initial_state == final_state is then the pool [num_slots][H][dv][dk]
+    const int32_t *state_slots = nullptr;    // [N], -1 = padded sequence
+    int num_slots = 0;
 };
 
 cudaError_t launch_kda_simt_f32_d64(const KdaArgs &a);

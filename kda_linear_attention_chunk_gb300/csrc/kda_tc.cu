@@ -139,6 +139,8 @@ struct TcParams {
     const int *g_une;
     int *err;
     unsigned int *sched;   // dynamic deal: [claim counter, finished CTAs], or nullptr
+    const int *slots;      // [N] state-pool entry of each sequence (-1: padding), or nullptr (entry n)
+    int num_slots;         // entries in the state pool when slots is set
 };
 
 struct Smem {
@@ -170,9 +172,21 @@ __device__ __forceinline__ bool role_any(bool pred, int id, int n)
     return r != 0;
 }
 
-// Unit u (in this CTA's schedule order) -> (sequence, head, rows).
+// State-pool entry of sequence n: n itself, or its id in the slot table.  A
+// padded sequence (id -1) has none, and neither has an id outside
+// [-1, num_slots), which is also reported; such a sequence is skipped.
+__device__ __forceinline__ int state_index(const TcParams &p, int n)
+{
+    if (!p.slots) return n;
+    const int s = __ldg(p.slots + n);
+    if (s >= 0 && s < p.num_slots) return s;
+    if (s != -1) atomicOr(p.err, kErrBadSlot);
+    return -1;
+}
+
+// Unit u (in this CTA's schedule order) -> (sequence, head, rows, state entry).
 struct Unit {
-    int n, h, bos, eos, nchunks;
+    int n, h, bos, eos, nchunks, st;
 };
 
 __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, int u)
@@ -197,7 +211,8 @@ __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, in
         b = min(max(p.cu[x.n], 0), p.T);
         e = min(max(p.cu[x.n + 1], 0), p.T);
     }
-    if (e < b) e = b;
+    x.st = state_index(p, x.n);
+    if (e < b || x.st < 0) e = b;
     x.bos = b;
     x.eos = e;
     x.nchunks = (e - b + kChunk - 1) / kChunk;
@@ -1044,9 +1059,9 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
         const int u = cta_unit(sm, k, U);
         if (u < 0) break;
         const Unit un = get_unit(p, order, u);
-        const size_t soff = (((size_t)un.n * p.H + un.h) * kD + v) * kD;
+        const size_t soff = (((size_t)max(un.st, 0) * p.H + un.h) * kD + v) * kD;
         if (un.nchunks == 0) {
-            if (p.s1) {
+            if (p.s1 && un.st >= 0) {
                 for (int c = 0; c < kD; c += 4) {
                     float4 x = p.s0 ? *reinterpret_cast<const float4 *>(p.s0 + soff + c) : make_float4(0.f, 0.f, 0.f, 0.f);
                     *reinterpret_cast<float4 *>(p.s1 + soff + c) = x;
@@ -1083,8 +1098,10 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 const int un2 = cta_unit_peek(sm, k + 1, U);
                 if (un2 >= 0) {
                     const Unit nx = get_unit(p, order, un2);
-                    const float *src = p.s0 + ((size_t)nx.n * p.H + nx.h) * kD * kD;
-                    for (int part = 0; part < 4; part++) prefetch_l2(src + part * 4096, 16384);
+                    if (nx.st >= 0) {
+                        const float *src = p.s0 + ((size_t)nx.st * p.H + nx.h) * kD * kD;
+                        for (int part = 0; part < 4; part++) prefetch_l2(src + part * 4096, 16384);
+                    }
                 }
             }
             tc_fence_after();
@@ -1262,7 +1279,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const int cb = p.cu[n], ce = p.cu[n + 1];
             int b = min(max(cb, 0), p.T), e = min(max(ce, 0), p.T);
             if (cb < 0 || cb > p.T || ce < 0 || ce > p.T) atomicOr(p.err, kErrBadSeqlens);
-            if (e < b) e = b;
+            if (e < b || state_index(p, n) < 0) e = b;
             rows[n] = make_int2(b, e);
             lens[n] = e - b;
         }
@@ -1473,6 +1490,8 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     p.g_une = a.g_units_nonempty;
     p.err = a.err_word;
     p.sched = a.sched;
+    p.slots = a.state_slots;
+    p.num_slots = a.num_slots;
     const int units = a.N * a.H;
     const int grid = units < a.num_sms ? units : a.num_sms;
     kda_tc_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tg, p);

@@ -82,3 +82,36 @@ def test_exact_state_alias_passes_validation(kda_lib):
 @pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
 def test_empty_rows_allow_null_tensors(kda_lib):
     assert call(q=0, k=0, v=0, g=0, beta=0, out=0, T=0) == kda.KDA_ERR_DEVICE
+
+
+def call_slots(**over):
+    T, H, d, N = 64, 2, 128, 3
+    rows = T * H * d
+    args = dict(q=A, k=A + 2 * rows * 4, v=A + 4 * rows * 4, g=A + 6 * rows * 4, beta=A + 10 * rows * 4,
+                cu=A + 11 * rows * 4, slots=A + 11 * rows * 4 + 64, pool=A + (40 << 20), num_slots=5,
+                out=A + 12 * rows * 4, N=N, T=T, H=H, dk=d, dv=d, stream=0)
+    args.update(over)
+    order = ["q", "k", "v", "g", "beta", "cu", "slots", "pool", "num_slots", "out", "N", "T", "H", "dk", "dv",
+             "stream"]
+    return kda.kda_chunk_prefill_slots(*[args[n] for n in order])
+
+
+def test_slots_validation_statuses(kda_lib):
+    pool_bytes = 5 * 2 * 128 * 128 * 4
+    assert call_slots(slots=0) == kda.KDA_ERR_NULL
+    assert call_slots(pool=0) == kda.KDA_ERR_NULL
+    assert call_slots(num_slots=0) == kda.KDA_ERR_SHAPE
+    assert call_slots(N=0) == kda.KDA_ERR_SHAPE
+    assert call_slots(dk=64, dv=64) == kda.KDA_ERR_UNSUPPORTED
+    assert call_slots(N=2000) == kda.KDA_ERR_UNSUPPORTED
+    assert call_slots(slots=A + (1 << 19) + 2) == kda.KDA_ERR_ALIGN
+    assert call_slots(pool=A + (40 << 20) + 8) == kda.KDA_ERR_ALIGN
+    assert call_slots(pool=A) == kda.KDA_ERR_ALIAS                                     # pool over q
+    assert call_slots(slots=A + (40 << 20) + pool_bytes - 4) == kda.KDA_ERR_ALIAS      # slots inside the pool
+    assert call_slots(out=A + (60 << 20), slots=A + (60 << 20) + 16) == kda.KDA_ERR_ALIAS   # slots inside out
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+def test_slots_valid_call_passes_validation(kda_lib):
+    assert call_slots() == kda.KDA_ERR_DEVICE
+    assert call_slots(pool=A + (40 << 20) + 5 * 2 * 128 * 128 * 4) == kda.KDA_ERR_DEVICE   # pool just past
