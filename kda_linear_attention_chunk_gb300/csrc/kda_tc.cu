@@ -174,10 +174,13 @@ __device__ __forceinline__ bool role_any(bool pred, int id, int n)
 
 // State-pool entry of sequence n: n itself, or its id in the slot table.  A
 // padded sequence (id -1) has none, and neither has an id outside
-// [-1, num_slots), which is also reported; such a sequence is skipped.
+// [-1, num_slots), which is also reported; such a sequence is skipped.  The
+// kernel is built twice, with and without the slot table, so that the dense
+// form carries none of this code.
+template <bool kSlots>
 __device__ __forceinline__ int state_index(const TcParams &p, int n)
 {
-    if (!p.slots) return n;
+    if (!kSlots) return n;
     const int s = __ldg(p.slots + n);
     if (s >= 0 && s < p.num_slots) return s;
     if (s != -1) atomicOr(p.err, kErrBadSlot);
@@ -189,6 +192,7 @@ struct Unit {
     int n, h, bos, eos, nchunks, st;
 };
 
+template <bool kSlots>
 __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, int u)
 {
     Unit x;
@@ -211,8 +215,8 @@ __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, in
         b = min(max(p.cu[x.n], 0), p.T);
         e = min(max(p.cu[x.n + 1], 0), p.T);
     }
-    x.st = state_index(p, x.n);
-    if (e < b || x.st < 0) e = b;
+    x.st = state_index<kSlots>(p, x.n);
+    if (e < b || (kSlots && x.st < 0)) e = b;
     x.bos = b;
     x.eos = e;
     x.nchunks = (e - b + kChunk - 1) / kChunk;
@@ -346,6 +350,7 @@ struct LoadCursor {
 
 // Advances to the next chunk (its coordinates: row0, un.h; its index: item - 1);
 // false when the schedule is exhausted.
+template <bool kSlots>
 __device__ bool cursor_next(LoadCursor &L, const TcParams &p, const Smem &sm, const int *order, int U)
 {
     while (!L.done && L.c >= L.un.nchunks) {
@@ -354,7 +359,7 @@ __device__ bool cursor_next(LoadCursor &L, const TcParams &p, const Smem &sm, co
             L.done = true;
             break;
         }
-        L.un = get_unit(p, order, u);
+        L.un = get_unit<kSlots>(p, order, u);
         L.c = 0;
     }
     if (L.done) return false;
@@ -551,6 +556,7 @@ __device__ __forceinline__ float load_beta(const TcParams &p, const LoadCursor &
     return et < L ? __ldg(p.beta + (size_t)(c.row0 + et) * p.H + c.un.h) : 0.f;
 }
 
+template <bool kSlots>
 __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps)
 {
     const int et = threadIdx.x - kChainThreads;
@@ -586,7 +592,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             claim_slot = k + 1;
         }
     };
-    if (cursor_next(ahead, p, sm, order, U)) {
+    if (cursor_next<kSlots>(ahead, p, sm, order, U)) {
         if (ahead.c == ahead.un.nchunks) maybe_claim(ahead.k);
         if (et == 0) {
             KDA_PHASE(2, 0, 1);
@@ -598,7 +604,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
     for (int k = 0;; k++) {
         const int u = cta_unit(sm, k, U);
         if (u < 0) break;
-        const Unit un = get_unit(p, order, u);
+        const Unit un = get_unit<kSlots>(p, order, u);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const uint32_t ph = (item >> 1) & 1;
@@ -626,7 +632,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                 KDA_PHASE(2, item, 2);
             }
             if (et == 0) publish();
-            if (cursor_next(ahead, p, sm, order, U)) {
+            if (cursor_next<kSlots>(ahead, p, sm, order, U)) {
                 if (ahead.c == ahead.un.nchunks) maybe_claim(ahead.k);
                 if (et == 0) {
                     KDA_PHASE(2, ahead.item - 1, 1);
@@ -902,6 +908,7 @@ __device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
     tmem_wait_st();
 }
 
+template <bool kSlots>
 __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int U)
 {
     const int it = threadIdx.x - kChainThreads - kEThreads;
@@ -924,7 +931,7 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
     for (int k = 0;; k++) {
         const int u = cta_unit(sm, k, U);
         if (u < 0) break;
-        const Unit un = get_unit(p, order, u);
+        const Unit un = get_unit<kSlots>(p, order, u);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const uint32_t ph = (item >> 1) & 1;
@@ -1050,6 +1057,7 @@ __device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float 
     tmem_wait_st();
 }
 
+template <bool kSlots>
 __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps,
                             LoadCursor &cur, uint32_t tmem, uint32_t lane_off, int v)
 {
@@ -1058,10 +1066,10 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
     for (int k = 0;; k++) {
         const int u = cta_unit(sm, k, U);
         if (u < 0) break;
-        const Unit un = get_unit(p, order, u);
-        const size_t soff = (((size_t)max(un.st, 0) * p.H + un.h) * kD + v) * kD;
+        const Unit un = get_unit<kSlots>(p, order, u);
+        const size_t soff = (((size_t)un.st * p.H + un.h) * kD + v) * kD;   // used only when st >= 0
         if (un.nchunks == 0) {
-            if (p.s1 && un.st >= 0) {
+            if (p.s1 && (!kSlots || un.st >= 0)) {
                 for (int c = 0; c < kD; c += 4) {
                     float4 x = p.s0 ? *reinterpret_cast<const float4 *>(p.s0 + soff + c) : make_float4(0.f, 0.f, 0.f, 0.f);
                     *reinterpret_cast<float4 *>(p.s1 + soff + c) = x;
@@ -1097,8 +1105,8 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 // the next unit's initial state heads for L2 during this last chunk
                 const int un2 = cta_unit_peek(sm, k + 1, U);
                 if (un2 >= 0) {
-                    const Unit nx = get_unit(p, order, un2);
-                    if (nx.st >= 0) {
+                    const Unit nx = get_unit<kSlots>(p, order, un2);
+                    if (!kSlots || nx.st >= 0) {
                         const float *src = p.s0 + ((size_t)nx.st * p.H + nx.h) * kD * kD;
                         for (int part = 0; part < 4; part++) prefetch_l2(src + part * 4096, 16384);
                     }
@@ -1120,7 +1128,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             if (v == 0) {
                 KDA_PHASE(1, item, 11);
                 // MMA-b is done with V: chunk item+2's v may land
-                if (cursor_next(cur, p, sm, order, U)) {
+                if (cursor_next<kSlots>(cur, p, sm, order, U)) {
                     issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
                     kq_pending = true;
                 }
@@ -1222,6 +1230,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
     }
 }
 
+template <bool kSlots>
 __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps)
 {
     const int v = threadIdx.x;
@@ -1230,12 +1239,12 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
     const uint32_t lane_off = (uint32_t)(32 * w) << 16;
     LoadCursor cur;
     if (v == 0) {
-        for (int i = 0; i < 2 && cursor_next(cur, p, sm, order, U); i++) {
+        for (int i = 0; i < 2 && cursor_next<kSlots>(cur, p, sm, order, U); i++) {
             issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
             issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
         }
     }
-    chain_units(p, sm, order, U, maps, cur, tmem, lane_off, v);
+    chain_units<kSlots>(p, sm, order, U, maps, cur, tmem, lane_off, v);
     if (v == 0) {
         // copies still in flight land before the CTA exits (normally none: every
         // requested chunk has been consumed)
@@ -1248,6 +1257,7 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
 }
 
 // =============================================================================
+template <bool kSlots>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, TcParams p)
@@ -1279,7 +1289,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const int cb = p.cu[n], ce = p.cu[n + 1];
             int b = min(max(cb, 0), p.T), e = min(max(ce, 0), p.T);
             if (cb < 0 || cb > p.T || ce < 0 || ce > p.T) atomicOr(p.err, kErrBadSeqlens);
-            if (e < b || state_index(p, n) < 0) e = b;
+            if (e < b || (kSlots && state_index<kSlots>(p, n) < 0)) e = b;
             rows[n] = make_int2(b, e);
             lens[n] = e - b;
         }
@@ -1378,11 +1388,11 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 #endif
     const Maps maps = {&tq, &tk, &tv, &tg};
     if (warp < 4) {
-        chain_role(p, sm, order, U, maps);
+        chain_role<kSlots>(p, sm, order, U, maps);
     } else if (warp < 12) {
-        e_role(p, sm, order, U, maps);
+        e_role<kSlots>(p, sm, order, U, maps);
     } else {
-        i_role(p, sm, order, U);
+        i_role<kSlots>(p, sm, order, U);
     }
     // every MMA this CTA issued has completed before TMEM is released
     if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads) {
@@ -1467,13 +1477,15 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
             !make_map4(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32))
             return cudaErrorInvalidValue;
     }
-    static int attr_set[64] = {0};
+    const bool slots = a.state_slots != nullptr;
+    auto *kernel = slots ? kda_tc_kernel<true> : kda_tc_kernel<false>;
+    static int attr_set[2][64] = {{0}};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kda_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (dev >= 0 && dev < 64 && !attr_set[slots][dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = 1;
+        attr_set[slots][dev] = 1;
     }
     TcParams p;
     p.cu = a.cu_seqlens;
@@ -1494,7 +1506,7 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     p.num_slots = a.num_slots;
     const int units = a.N * a.H;
     const int grid = units < a.num_sms ? units : a.num_sms;
-    kda_tc_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tg, p);
+    kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tg, p);
     return cudaGetLastError();
 }
 

@@ -41,6 +41,7 @@ def _no_device_timeouts(request):
     if not torch.cuda.is_available():
         yield
         return
+    request.getfixturevalue("kda_lib")   # builds libkda.so when missing or stale
     kda.device_error(reset=True)
     yield
     torch.cuda.synchronize()
