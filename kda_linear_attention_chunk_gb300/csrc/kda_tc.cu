@@ -407,54 +407,56 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // =============================================================================
 
 // Group E's decay pass over one chunk (256 threads); `beta_r` is the beta of
-// row et (zero past the chunk), loaded a chunk ahead.
-// Scan: thread = (row group ew: rows 16*ew .. +15) x (channel half chh) x (key
-// channels 64*chh + 2*lane, +1); the row prefix of g * log2(e) runs in
-// registers, the four row groups exchange their totals once, and G (in base 2)
-// is written back over g in the g slot.
-// Operands: thread = (row 8*w + (lane & 7), w = et / 32) x (channels 32*cg +
-// 8*j .. +7, cg = lane >> 3), 16-byte accesses; Kp = beta*K*exp(G - G_m),
-// Qp = Q*exp(G - G_m) and Km = K*exp(G_m - G) become fp16 in place over the
-// bf16 tiles (rows past the chunk zero).  Returns false if a wait ran out.
-__device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r)
+// row et (zero past the chunk), loaded a chunk ahead.  Thread = (row group
+// ew: rows 16*ew .. +15) x (channel half chh) x (key channels c0 = 64*chh +
+// 2*lane, +1).  The row prefix of g * log2(e) runs in registers and the four
+// row groups exchange their totals once; from then on the g slot is no longer
+// read (`released` runs: the next chunk's g may be requested) and G, in base
+// 2, stays in registers.  With G_m the G of the middle row m, Kp = beta*K*
+// 2^(G - G_m), Qp = Q*2^(G - G_m) and Km = K*2^(G_m - G) become fp16 in place
+// over the bf16 tiles (rows past the chunk zero).  Returns false if a wait ran
+// out.
+template <class F>
+__device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r, F &&released)
 {
     const int lane = et & 31;
     const uint32_t st = s * kStageBytes;
     float *cst = sm.ptr<float>(kOffConst + s * kConstBytes);
     float *gmx = sm.ptr<float>(kOffGm), *glx = gmx + 128;
     const int m = (L - 1) >> 1;
+    const int ew = (et >> 5) & 3, chh = et >> 7;
+    const int c0 = 64 * chh + 2 * lane;                      // this thread's two channels
+    float *xchg = sm.ptr<float>(kOffEScr);                   // [4 row groups][128 channels]
+    float2 x[16];
     {
-        const int ew = (et >> 5) & 3, chh = et >> 7;
-        const int c0 = 64 * chh + 2 * lane;                  // this thread's two channels
-        float *xchg = sm.ptr<float>(kOffEScr);               // [4 row groups][128 channels]
-        uint8_t *gb = sm.base + kOffG + (c0 >> 5) * 8192;
+        const uint8_t *gb = sm.base + kOffG + (c0 >> 5) * 8192;
         const int jc = (c0 & 31) >> 2, sub = 8 * (lane & 1);
-        float2 x[16];
 #pragma unroll
         for (int t = 0; t < 16; t++) {
             const int r = 16 * ew + t;
             const float2 g2 = r < L ? *reinterpret_cast<const float2 *>(gb + sw128_chunk(r, jc) + sub) : make_float2(0.f, 0.f);
             x[t] = make_float2(g2.x * kLog2e, g2.y * kLog2e);   // base-2 log-decay
         }
+    }
 #pragma unroll
-        for (int t = 1; t < 16; t++) {
-            x[t].x += x[t - 1].x; x[t].y += x[t - 1].y;
-        }
-        *reinterpret_cast<float2 *>(xchg + ew * 128 + c0) = x[15];
-        named_bar(kBarE, kEThreads);
-        float2 pre = make_float2(0.f, 0.f);
-        for (int w = 0; w < ew; w++) {
-            const float2 y = *reinterpret_cast<const float2 *>(xchg + w * 128 + c0);
-            pre.x += y.x; pre.y += y.y;
-        }
+    for (int t = 1; t < 16; t++) {
+        x[t].x += x[t - 1].x; x[t].y += x[t - 1].y;
+    }
+    *reinterpret_cast<float2 *>(xchg + ew * 128 + c0) = x[15];
+    fence_proxy_async_smem();   // the reads of the g slot come before a load that overwrites it
+    named_bar(kBarE, kEThreads);
+    released();
+    float2 pre = make_float2(0.f, 0.f);
+    for (int w = 0; w < ew; w++) {
+        const float2 y = *reinterpret_cast<const float2 *>(xchg + w * 128 + c0);
+        pre.x += y.x; pre.y += y.y;
+    }
 #pragma unroll
-        for (int t = 0; t < 16; t++) {
-            x[t].x += pre.x; x[t].y += pre.y;
-            const int r = 16 * ew + t;
-            *reinterpret_cast<float2 *>(gb + sw128_chunk(r, jc) + sub) = x[t];
-            if (r == m) *reinterpret_cast<float2 *>(gmx + c0) = x[t];
-            if (r == L - 1) *reinterpret_cast<float2 *>(glx + c0) = x[t];
-        }
+    for (int t = 0; t < 16; t++) {
+        x[t].x += pre.x; x[t].y += pre.y;
+        const int r = 16 * ew + t;
+        if (r == m) *reinterpret_cast<float2 *>(gmx + c0) = x[t];
+        if (r == L - 1) *reinterpret_cast<float2 *>(glx + c0) = x[t];
     }
     if (et < kChunk) cst[256 + et] = beta_r;
     named_bar(kBarE, kEThreads);
@@ -472,46 +474,36 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
         mbar_arrive(sm.bar(kBarFmReady + s));
     }
     if (et == 0) KDA_PHASE(0, item, 10);
-    const int rr = lane & 7, cg = lane >> 3, kb = cg >> 1;
-    const int r = 8 * (et >> 5) + rr;
-    const bool valid = r < L;
-    const float br = cst[256 + r];                     // zero past the chunk
-    uint8_t *kt = sm.base + st + kOffKQ + kb * 16384;
+    const float2 gm = *reinterpret_cast<const float2 *>(gmx + c0);
+    uint8_t *kt = sm.base + st + kOffKQ + chh * 16384;   // this channel half's 64-channel block
     uint8_t *qt = kt + 8192;
-    uint8_t *kmt = sm.base + st + kOffKM + kb * 8192;
-    const uint8_t *gt = sm.base + kOffG + cg * 8192;
-#pragma unroll 2
-    for (int j = 0; j < 4; j++) {
-        const float4 g0 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j));
-        const float4 g1 = *reinterpret_cast<const float4 *>(gt + sw128_chunk(r, 2 * j + 1));
-        const float4 m0 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j);
-        const float4 m1 = *reinterpret_cast<const float4 *>(gmx + 32 * cg + 8 * j + 4);
-        const uint32_t off = sw128_chunk(r, 4 * (cg & 1) + j);
-        const uint4 kq = *reinterpret_cast<const uint4 *>(kt + off);
-        const uint4 qq = *reinterpret_cast<const uint4 *>(qt + off);
-        const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        const float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
-        const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w};
-        uint32_t okp[4], okm[4], oqp[4];
+    uint8_t *kmt = sm.base + st + kOffKM + chh * 8192;
+    const int jk = lane >> 2;                            // 16-byte chunk of channel c0 in the row
+    const uint32_t cb = 4 * (lane & 3);                  // byte of channel c0 in that chunk
+#pragma unroll 1
+    for (int half = 0; half < 2; half++) {
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
+        for (int t = 0; t < 8; t++) {
+            const int r = 16 * ew + 8 * half + t;
+            const uint32_t off = sw128_chunk(r, jk) + cb;
+            const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
+            const uint32_t qw = *reinterpret_cast<const uint32_t *>(qt + off);
+            const float br = cst[256 + r];               // zero past the chunk
             float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-            if (valid) {
-                a0 = ex2(G[2 * e] - M[2 * e]);
-                a1 = ex2(G[2 * e + 1] - M[2 * e + 1]);
-                b0 = ex2(M[2 * e] - G[2 * e]);
-                b1 = ex2(M[2 * e + 1] - G[2 * e + 1]);
+            if (r < L) {
+                a0 = ex2(x[t].x - gm.x);
+                a1 = ex2(x[t].y - gm.y);
+                b0 = ex2(gm.x - x[t].x);
+                b1 = ex2(gm.y - x[t].y);
             }
-            const float k0 = bf16lo(kw[e]), k1 = bf16hi(kw[e]);
-            const float q0 = bf16lo(qw[e]), q1 = bf16hi(qw[e]);
-            okp[e] = pack_f16x2(k0 * (a0 * br), k1 * (a1 * br));
-            okm[e] = pack_f16x2(k0 * b0, k1 * b1);
-            oqp[e] = pack_f16x2(q0 * a0, q1 * a1);
+            const float k0 = bf16lo(kw), k1 = bf16hi(kw);
+            const float q0 = bf16lo(qw), q1 = bf16hi(qw);
+            *reinterpret_cast<uint32_t *>(kt + off) = pack_f16x2(k0 * (a0 * br), k1 * (a1 * br));
+            *reinterpret_cast<uint32_t *>(qt + off) = pack_f16x2(q0 * a0, q1 * a1);
+            *reinterpret_cast<uint32_t *>(kmt + off) = pack_f16x2(k0 * b0, k1 * b1);
         }
-        *reinterpret_cast<uint4 *>(kt + off) = make_uint4(okp[0], okp[1], okp[2], okp[3]);
-        *reinterpret_cast<uint4 *>(qt + off) = make_uint4(oqp[0], oqp[1], oqp[2], oqp[3]);
-        *reinterpret_cast<uint4 *>(kmt + off) = make_uint4(okm[0], okm[1], okm[2], okm[3]);
+#pragma unroll
+        for (int t = 0; t < 8; t++) x[t] = x[t + 8];
     }
     if (et == 0) KDA_PHASE(0, item, 11);
     return true;
@@ -614,12 +606,23 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             bool ok = mbar_wait(sm.bar(kBarGFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarE, kEThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (et == 0) KDA_PHASE(0, item, 0);
-            if (!e_pass(sm, s, item, L, et, beta_r)) {
+            // the next chunk's g is requested as soon as this chunk's g is read
+            auto next_g = [&]() {
+                if (cursor_next<kSlots>(ahead, p, sm, order, U)) {
+                    if (ahead.c == ahead.un.nchunks) maybe_claim(ahead.k);
+                    if (et == 0) {
+                        KDA_PHASE(2, ahead.item - 1, 1);
+                        issue_g(sm, maps, ahead.row0, ahead.un.h);
+                    }
+                    beta_next = load_beta(p, ahead, et);
+                }
+            };
+            if (!e_pass(sm, s, item, L, et, beta_r, next_g)) {
                 if (et == 0) record_error(p, sm, kErrWaitTimeout);
                 return;
             }
             fence_proxy_async_smem();
-            named_bar(kBarE, kEThreads);                   // operands written, the g slot read
+            named_bar(kBarE, kEThreads);                   // operands written
             if (et == 0) {
                 KDA_PHASE(0, item, 1);
                 // TMEM P_s is free once the chain has read chunk item-2's outputs
@@ -632,14 +635,6 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                 KDA_PHASE(2, item, 2);
             }
             if (et == 0) publish();
-            if (cursor_next<kSlots>(ahead, p, sm, order, U)) {
-                if (ahead.c == ahead.un.nchunks) maybe_claim(ahead.k);
-                if (et == 0) {
-                    KDA_PHASE(2, ahead.item - 1, 1);
-                    issue_g(sm, maps, ahead.row0, ahead.un.h);
-                }
-                beta_next = load_beta(p, ahead, et);
-            }
             if (et == 0) KDA_PHASE(2, item, 6);
             ok = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
             if (et == 0) KDA_PHASE(2, item, 4);
