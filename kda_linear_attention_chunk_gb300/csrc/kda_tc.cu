@@ -533,7 +533,7 @@ __device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
 {
     const uint32_t st = sm.u32(s * kStageBytes);
     const uint32_t id = idesc_f16(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
     for (int ks = 0; ks < 8; ks++) {
         const int kb = ks >> 2, kin = ks & 3;
         const uint64_t ad = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
@@ -856,7 +856,7 @@ __device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
 {
     const uint32_t st = sm.u32(s * kStageBytes);
     const uint32_t id = idesc_f16(128, 64, 1, 0);
-#pragma unroll
+#pragma unroll 1
     for (int ks = 0; ks < 4; ks++) {
         const uint64_t bd = smem_desc_sw128(sm.u32(kOffT16) + ks * 32, 16, 1024);
         const uint64_t aw = smem_desc_sw128(st + kOffKQ + ks * 2048, 16384, 1024);   // Kp^T, MN-major
@@ -1023,13 +1023,17 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem
 
 // S <- (S * pend) * fm column by column (pend may be null), written back, and
 // its fp16 copy S'h (two per 32-bit column) for the chain MMAs.
-__device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float *fm, const float *pend)
+__device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float *fm, const float *pend, int item)
 {
 #pragma unroll 1
     for (int q = 0; q < 4; q++) {                       // 32 key channels at a time
         uint32_t x[32];
         tmem_ld32(tmem + kTmS + lane_off + 32 * q, x);
         tmem_wait_ld();
+        if (lane_off == 0 && threadIdx.x == 0) {
+            if (q == 0) KDA_PHASE(1, item, 15);
+            if (q == 3) KDA_PHASE(1, item, 10);
+        }
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             const float4 f4 = *reinterpret_cast<const float4 *>(fm + 32 * q + j);
@@ -1049,6 +1053,7 @@ __device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float 
         tmem_st32(tmem + kTmS + lane_off + 32 * q, x);
         tmem_st16(tmem + kTmS0h + lane_off + 16 * q, h);
     }
+    if (lane_off == 0 && threadIdx.x == 0) KDA_PHASE(1, item, 14);
     tmem_wait_st();
 }
 
@@ -1109,7 +1114,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             }
             tc_fence_after();
             chain_scale_state(tmem, lane_off, sm.ptr<float>(kOffConst + s * kConstBytes),
-                              c > 0 ? sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128 : nullptr);
+                              c > 0 ? sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128 : nullptr, item);
             if (v == 0) KDA_PHASE(1, item, 6);
             tc_fence_before();
             ok = mbar_wait(sm.bar(kBarPrepDone + s), ph, sm.abort_flag());
@@ -1133,7 +1138,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 // [U^T | 0] += S'^T [-W' ; Qp]^T: the Delta half and the output half in
                 // one N = 128 MMA (the K rows of each stage block hold -W', the Q rows Qp)
                 const uint32_t id1 = idesc_f16(128, 128, 0, 0);
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ks++) {
                     const int kb = ks >> 2, kin = ks & 3;
                     const uint64_t bwq = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
@@ -1176,12 +1181,12 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 const uint32_t st = sm.u32(s * kStageBytes);
                 const uint32_t id_s = idesc_f16(128, 128, 0, 1), id_o = idesc_f16(128, 64, 0, 0);
                 // state update first, then the rest of the output
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 4; ks++) {
                     const uint64_t bk = smem_desc_sw128(st + kOffKM + ks * 2048, 8192, 1024);   // Km, MN-major
                     mma_ts(tmem + kTmS, tmem + kTmDh + 8 * ks, bk, id_s, 1);
                 }
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < 4; ks++) {
                     const uint64_t bb = smem_desc_sw128(st + kOffB + ks * 32, 16, 1024);
                     mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmDh + 8 * ks, bb, id_o, 1);
