@@ -514,7 +514,7 @@ __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
 {
     uint8_t *vt = sm.base + s * kStageBytes + kOffV;
     const float *bt = sm.ptr<float>(kOffConst + s * kConstBytes) + 256;
-#pragma unroll 2
+#pragma unroll 1
     for (int i = 0; i < 4; i++) {
         const int idx = et + kEThreads * i;        // 16-byte chunk index in the 16 KB tile
         const int r = (idx >> 3) & 63;
@@ -877,7 +877,7 @@ __device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
     const int mi = lane >> 3, k8 = lane & 7;              // this thread's stored matrix and row
     const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * iw) << 16);
     const uint32_t kq = sm.u32(s * kStageBytes + kOffKQ);
-#pragma unroll
+#pragma unroll 1
     for (int hl = 0; hl < 2; hl++) {
         uint32_t f[4][8];                                 // [16-column block][fragment]
 #pragma unroll
@@ -1212,7 +1212,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
         // unit end: final state = S * pend of the unit's last chunk
         if (p.s1) {
             const float *pend = sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128;
-#pragma unroll
+#pragma unroll 1
             for (int cb = 0; cb < 4; cb++) {
                 uint32_t x[32];
                 tmem_ld32(tmem + kTmS + lane_off + 32 * cb, x);
