@@ -117,7 +117,6 @@ constexpr int kBarFmReady = 12;    // [2]: the chunk's decay constants are writt
 constexpr int kBarKmFree = 14;     // [2]: the chain's MMAs on the stage are done (Km, B free)
 constexpr int kBarGFull = 16;      // g slot landed
 constexpr int kBarMma1 = 18, kBarMma3 = 20, kBarDrain = 21;
-constexpr int kMaxRounds = 24;     // longest per-CTA unit list of the balanced deal
 
 // TMEM columns
 constexpr uint32_t kTmS = 0, kTmP = 128, kTmS0h = 384, kTmDh = 448, kTmCols = 512;
@@ -133,7 +132,6 @@ struct TcParams {
     __nv_bfloat16 *out;
     float *s1;
     int N, T, H;
-    int sorted;        // 1: sorted here (N <= kMaxSortedSeqs); 2: sorted order given in g_order/g_rows; 0: unsorted
     const int *g_order;
     const int2 *g_rows;
     const int *g_une;
@@ -150,12 +148,11 @@ struct Smem {
     __device__ uint32_t bar(int i) const { return u32(kOffBar + 8 * i); }
     __device__ volatile int *abort_flag() const { return ptr<volatile int>(kOffMisc + 4); }
     __device__ uint32_t *tmem_base() const { return ptr<uint32_t>(kOffMisc); }
-    // unit deal: mode >= 0 static list of that length, -1 snake, -2 dynamic
-    __device__ int *sched_len() const { return ptr<int>(kOffMisc + 8); }
+    // dynamic unit deal
     __device__ volatile int *published() const { return ptr<volatile int>(kOffMisc + 12); }   // dynamic: units in the ring
     __device__ volatile int *claim_done() const { return ptr<volatile int>(kOffMisc + 16); }  // dynamic: no more claims
     __device__ int *units_nonempty() const { return ptr<int>(kOffMisc + 20); }
-    __device__ int *sched() const { return ptr<int>(kOffMisc + 24); }      // static list [kMaxRounds] / ring [8]
+    __device__ int *sched() const { return ptr<int>(kOffMisc + 24); }      // ring [8] of claimed units
 };
 
 __device__ __forceinline__ bool role_any(bool pred, int id, int n)
@@ -192,20 +189,20 @@ struct Unit {
     int n, h, bos, eos, nchunks, st;
 };
 
-template <bool kSlots>
+template <bool kSlots, int kSort>
 __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, int u)
 {
     Unit x;
     const int su = u / p.H;
     x.h = u % p.H;
     int b, e;
-    if (p.sorted == 1) {
+    if constexpr (kSort == 1) {
         // order[] is followed in shared memory by the clamped {bos, eos} rows
         x.n = order[su];
         const int2 be = reinterpret_cast<const int2 *>(order + kMaxSortedSeqs)[x.n];
         b = be.x;
         e = be.y;
-    } else if (p.sorted == 2) {
+    } else if constexpr (kSort == 2) {
         x.n = p.g_order[su];
         const int2 be = p.g_rows[x.n];
         b = be.x;
@@ -243,26 +240,28 @@ __device__ __noinline__ int dyn_unit(const Smem &sm, int k, int U)
     return -1;
 }
 
-// k-th unit of this CTA, -1 when exhausted: the dynamic deal, the balanced
-// static deal made in the prologue, or else a boustrophedon ("snake") deal of
-// the length-sorted unit list over the grid.
+// k-th unit of this CTA, -1 when exhausted: the dynamic deal of the
+// length-sorted units, or (unsorted) a boustrophedon ("snake") deal over the grid.
+template <int kSort>
 __device__ __forceinline__ int cta_unit(const Smem &sm, int k, int U)
 {
-    const int n = *sm.sched_len();
-    if (n >= 0) return k < n ? sm.sched()[k] : -1;
-    if (n == -2) return dyn_unit(sm, k, U);
-    const int G = gridDim.x, b = blockIdx.x;
-    const int u = k * G + ((k & 1) ? (G - 1 - b) : b);
-    return u < U ? u : -1;
+    if constexpr (kSort != 0) {
+        return dyn_unit(sm, k, U);
+    } else {
+        const int G = gridDim.x, b = blockIdx.x;
+        const int u = k * G + ((k & 1) ? (G - 1 - b) : b);
+        return u < U ? u : -1;
+    }
 }
 
 
 // byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
 // k-th unit of this CTA if it is already known (-1: exhausted, -2: not yet
 // claimed); never waits.
+template <int kSort>
 __device__ __forceinline__ int cta_unit_peek(const Smem &sm, int k, int U)
 {
-    if (*sm.sched_len() != -2) return cta_unit(sm, k, U);
+    if constexpr (kSort == 0) return cta_unit<kSort>(sm, k, U);
     const int pub = *sm.published();
     __threadfence_block();
     if (k < pub) return reinterpret_cast<volatile int *>(sm.sched())[k & 7];
@@ -350,16 +349,16 @@ struct LoadCursor {
 
 // Advances to the next chunk (its coordinates: row0, un.h; its index: item - 1);
 // false when the schedule is exhausted.
-template <bool kSlots>
+template <bool kSlots, int kSort>
 __device__ bool cursor_next(LoadCursor &L, const TcParams &p, const Smem &sm, const int *order, int U)
 {
     while (!L.done && L.c >= L.un.nchunks) {
-        const int u = cta_unit(sm, ++L.k, U);
+        const int u = cta_unit<kSort>(sm, ++L.k, U);
         if (u < 0) {
             L.done = true;
             break;
         }
-        L.un = get_unit<kSlots>(p, order, u);
+        L.un = get_unit<kSlots, kSort>(p, order, u);
         L.c = 0;
     }
     if (L.done) return false;
@@ -548,7 +547,7 @@ __device__ __forceinline__ float load_beta(const TcParams &p, const LoadCursor &
     return et < L ? __ldg(p.beta + (size_t)(c.row0 + et) * p.H + c.un.h) : 0.f;
 }
 
-template <bool kSlots>
+template <bool kSlots, int kSort>
 __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps)
 {
     const int et = threadIdx.x - kChainThreads;
@@ -561,7 +560,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
     // claims the next unit, and publishes the claim (to the ring in shared
     // memory) one step later -- late enough that a CTA only takes more work
     // when it is about to run out, early enough to hide the atomic's latency
-    const bool dyn = *sm.sched_len() == -2;
+    constexpr bool dyn = kSort != 0;
     unsigned claim = 0;
     int claim_slot = -1;
     auto publish = [&]() {
@@ -584,7 +583,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             claim_slot = k + 1;
         }
     };
-    if (cursor_next<kSlots>(ahead, p, sm, order, U)) {
+    if (cursor_next<kSlots, kSort>(ahead, p, sm, order, U)) {
         if (ahead.c == ahead.un.nchunks) maybe_claim(ahead.k);
         if (et == 0) {
             KDA_PHASE(2, 0, 1);
@@ -594,9 +593,9 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
     }
     int item = 0;
     for (int k = 0;; k++) {
-        const int u = cta_unit(sm, k, U);
+        const int u = cta_unit<kSort>(sm, k, U);
         if (u < 0) break;
-        const Unit un = get_unit<kSlots>(p, order, u);
+        const Unit un = get_unit<kSlots, kSort>(p, order, u);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const uint32_t ph = (item >> 1) & 1;
@@ -608,7 +607,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             if (et == 0) KDA_PHASE(0, item, 0);
             // the next chunk's g is requested as soon as this chunk's g is read
             auto next_g = [&]() {
-                if (cursor_next<kSlots>(ahead, p, sm, order, U)) {
+                if (cursor_next<kSlots, kSort>(ahead, p, sm, order, U)) {
                     if (ahead.c == ahead.un.nchunks) maybe_claim(ahead.k);
                     if (et == 0) {
                         KDA_PHASE(2, ahead.item - 1, 1);
@@ -903,7 +902,7 @@ __device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
     tmem_wait_st();
 }
 
-template <bool kSlots>
+template <bool kSlots, int kSort>
 __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int U)
 {
     const int it = threadIdx.x - kChainThreads - kEThreads;
@@ -924,9 +923,9 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
     }
     int item = 0;
     for (int k = 0;; k++) {
-        const int u = cta_unit(sm, k, U);
+        const int u = cta_unit<kSort>(sm, k, U);
         if (u < 0) break;
-        const Unit un = get_unit<kSlots>(p, order, u);
+        const Unit un = get_unit<kSlots, kSort>(p, order, u);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const uint32_t ph = (item >> 1) & 1;
@@ -1057,16 +1056,16 @@ __device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float 
     tmem_wait_st();
 }
 
-template <bool kSlots>
+template <bool kSlots, int kSort>
 __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps,
                             LoadCursor &cur, uint32_t tmem, uint32_t lane_off, int v)
 {
     int item = 0;
     bool kq_pending = false;  // thread 0: chunk cur.item-1's v is requested, its k and q not yet
     for (int k = 0;; k++) {
-        const int u = cta_unit(sm, k, U);
+        const int u = cta_unit<kSort>(sm, k, U);
         if (u < 0) break;
-        const Unit un = get_unit<kSlots>(p, order, u);
+        const Unit un = get_unit<kSlots, kSort>(p, order, u);
         const size_t soff = (((size_t)un.st * p.H + un.h) * kD + v) * kD;   // used only when st >= 0
         if (un.nchunks == 0) {
             if (p.s1 && (!kSlots || un.st >= 0)) {
@@ -1103,9 +1102,9 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             if (v == 0) KDA_PHASE(1, item, 0);
             if (v == 0 && p.s0 && c == un.nchunks - 1) {
                 // the next unit's initial state heads for L2 during this last chunk
-                const int un2 = cta_unit_peek(sm, k + 1, U);
+                const int un2 = cta_unit_peek<kSort>(sm, k + 1, U);
                 if (un2 >= 0) {
-                    const Unit nx = get_unit<kSlots>(p, order, un2);
+                    const Unit nx = get_unit<kSlots, kSort>(p, order, un2);
                     if (!kSlots || nx.st >= 0) {
                         const float *src = p.s0 + ((size_t)nx.st * p.H + nx.h) * kD * kD;
                         for (int part = 0; part < 4; part++) prefetch_l2(src + part * 4096, 16384);
@@ -1128,7 +1127,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             if (v == 0) {
                 KDA_PHASE(1, item, 11);
                 // MMA-b is done with V: chunk item+2's v may land
-                if (cursor_next<kSlots>(cur, p, sm, order, U)) {
+                if (cursor_next<kSlots, kSort>(cur, p, sm, order, U)) {
                     issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
                     kq_pending = true;
                 }
@@ -1230,7 +1229,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
     }
 }
 
-template <bool kSlots>
+template <bool kSlots, int kSort>
 __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps)
 {
     const int v = threadIdx.x;
@@ -1239,12 +1238,12 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
     const uint32_t lane_off = (uint32_t)(32 * w) << 16;
     LoadCursor cur;
     if (v == 0) {
-        for (int i = 0; i < 2 && cursor_next<kSlots>(cur, p, sm, order, U); i++) {
+        for (int i = 0; i < 2 && cursor_next<kSlots, kSort>(cur, p, sm, order, U); i++) {
             issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
             issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
         }
     }
-    chain_units<kSlots>(p, sm, order, U, maps, cur, tmem, lane_off, v);
+    chain_units<kSlots, kSort>(p, sm, order, U, maps, cur, tmem, lane_off, v);
     if (v == 0) {
         // copies still in flight land before the CTA exits (normally none: every
         // requested chunk has been consumed)
@@ -1257,7 +1256,7 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
 }
 
 // =============================================================================
-template <bool kSlots>
+template <bool kSlots, int kSort>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, TcParams p)
@@ -1269,90 +1268,50 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     const int U = p.N * p.H;
     int *order = sm.ptr<int>(kOffOrder);
 
-    // schedule: sequences sorted by length, longest first (ties: lower index)
-    if (p.sorted == 2) {
-        // the sorted order and the row table were prepared in device memory
-        if (tid == 0 && !p.sched) *sm.sched_len() = -1;
-        if (tid == 0 && p.sched) {
-            const int une = *p.g_une;
+    // schedule: sequences sorted by length, longest first (ties: lower index), dealt
+    // dynamically: CTA b starts with the b-th longest unit; the rest of the
+    // nonempty units (longest first) go to whichever CTA claims them next, so
+    // faster SMs take more work.  Unsorted (more sequences than are sorted here
+    // and no order given): the snake deal, which needs no set-up.
+    if constexpr (kSort != 0) {
+        int une = 0;   // nonempty sequences x H
+        if constexpr (kSort == 2) {
+            // the sorted order and the row table were prepared in device memory
+            if (tid == 0) une = *p.g_une;
+        } else {
+            int *lens = sm.ptr<int>(kOffP);
+            int2 *rows = reinterpret_cast<int2 *>(order + kMaxSortedSeqs);
+            for (int n = tid; n < p.N; n += kThreads) {
+                const int cb = p.cu[n], ce = p.cu[n + 1];
+                int b = min(max(cb, 0), p.T), e = min(max(ce, 0), p.T);
+                if (cb < 0 || cb > p.T || ce < 0 || ce > p.T) atomicOr(p.err, kErrBadSeqlens);
+                if (e < b || (kSlots && state_index<kSlots>(p, n) < 0)) e = b;
+                rows[n] = make_int2(b, e);
+                lens[n] = e - b;
+            }
+            __syncthreads();
+            for (int n = tid; n < p.N; n += kThreads) {
+                int rank = 0;
+                const int ln = lens[n];
+                for (int m2 = 0; m2 < p.N; m2++) {
+                    const int lm = lens[m2];
+                    rank += (lm > ln) || (lm == ln && m2 < n);
+                }
+                order[rank] = n;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                for (int n = 0; n < p.N; n++) une += lens[n] > 0;
+                une *= p.H;
+            }
+        }
+        if (tid == 0) {
             const bool first = (int)blockIdx.x < une;
             *sm.units_nonempty() = une;
             sm.sched()[0] = first ? (int)blockIdx.x : -1;
             *sm.published() = first ? 1 : 0;
             *sm.claim_done() = first ? 0 : 1;
-            *sm.sched_len() = -2;
         }
-    } else if (p.sorted) {
-        int *lens = sm.ptr<int>(kOffP);
-        int2 *rows = reinterpret_cast<int2 *>(order + kMaxSortedSeqs);
-        for (int n = tid; n < p.N; n += kThreads) {
-            const int cb = p.cu[n], ce = p.cu[n + 1];
-            int b = min(max(cb, 0), p.T), e = min(max(ce, 0), p.T);
-            if (cb < 0 || cb > p.T || ce < 0 || ce > p.T) atomicOr(p.err, kErrBadSeqlens);
-            if (e < b || (kSlots && state_index<kSlots>(p, n) < 0)) e = b;
-            rows[n] = make_int2(b, e);
-            lens[n] = e - b;
-        }
-        __syncthreads();
-        for (int n = tid; n < p.N; n += kThreads) {
-            int rank = 0;
-            const int ln = lens[n];
-            for (int m2 = 0; m2 < p.N; m2++) {
-                const int lm = lens[m2];
-                rank += (lm > ln) || (lm == ln && m2 < n);
-            }
-            order[rank] = n;
-        }
-        __syncthreads();
-        const int G = gridDim.x;
-        const int R = (U + G - 1) / G;
-        if (p.sched) {
-            // Dynamic deal: CTA b starts with the b-th longest unit; the rest of
-            // the nonempty units (longest first) go to whichever CTA claims them
-            // next, so faster SMs take more work.
-            if (tid == 0) {
-                int ne = 0;
-                for (int n = 0; n < p.N; n++) ne += lens[n] > 0;
-                const int une = ne * p.H;
-                *sm.units_nonempty() = une;
-                const bool first = (int)blockIdx.x < une;
-                sm.sched()[0] = first ? (int)blockIdx.x : -1;
-                *sm.published() = first ? 1 : 0;
-                *sm.claim_done() = first ? 0 : 1;
-                *sm.sched_len() = -2;
-            }
-        } else if (R <= kMaxRounds && G <= kThreads) {
-            // Balanced deal of the sorted units (longest first), in rounds of one
-            // unit per CTA: in each round the CTA with the r-th smallest load so
-            // far (in chunks; ties by index) takes the r-th longest unit left.
-            // Every CTA computes the same deal and keeps its own list.
-            int *load = sm.ptr<int>(kOffP + 1024);
-            int *mine = sm.sched();
-            int lj = 0;
-            for (int r = 0; r < R; r++) {
-                if (tid < G) load[tid] = lj;
-                __syncthreads();
-                if (tid < G) {
-                    int rank = 0;
-                    for (int i = 0; i < G; i++) {
-                        const int li = load[i];
-                        rank += (li < lj) || (li == lj && i < tid);
-                    }
-                    const int u = r * G + rank;
-                    if (u < U) {
-                        const int2 be = rows[order[u / p.H]];
-                        lj += (be.y - be.x + kChunk - 1) / kChunk;
-                    }
-                    if (tid == (int)blockIdx.x) mine[r] = u < U ? u : -1;
-                }
-                __syncthreads();
-            }
-            if (tid == 0) *sm.sched_len() = R;
-        } else if (tid == 0) {
-            *sm.sched_len() = -1;
-        }
-    } else if (tid == 0) {
-        *sm.sched_len() = -1;
     }
     if (tid == 0) {
         *sm.abort_flag() = 0;
@@ -1388,11 +1347,11 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 #endif
     const Maps maps = {&tq, &tk, &tv, &tg};
     if (warp < 4) {
-        chain_role<kSlots>(p, sm, order, U, maps);
+        chain_role<kSlots, kSort>(p, sm, order, U, maps);
     } else if (warp < 12) {
-        e_role<kSlots>(p, sm, order, U, maps);
+        e_role<kSlots, kSort>(p, sm, order, U, maps);
     } else {
-        i_role<kSlots>(p, sm, order, U);
+        i_role<kSlots, kSort>(p, sm, order, U);
     }
     // every MMA this CTA issued has completed before TMEM is released
     if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads) {
@@ -1477,15 +1436,23 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
             !make_map4(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32))
             return cudaErrorInvalidValue;
     }
-    const bool slots = a.state_slots != nullptr;
-    auto *kernel = slots ? kda_tc_kernel<true> : kda_tc_kernel<false>;
-    static int attr_set[2][64] = {{0}};
+    // one kernel per (slot table, sort mode): 1 sorted here (N <= kMaxSortedSeqs),
+    // 2 sorted order given in g_order/g_rows, 0 unsorted; modes 1 and 2 deal
+    // dynamically and need the deal's scratch words
+    const int sort = a.g_order ? 2 : (a.N <= kMaxSortedSeqs ? 1 : 0);
+    if (sort != 0 && !a.sched) return cudaErrorInvalidValue;
+    const int variant = 3 * (a.state_slots != nullptr) + sort;
+    using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, TcParams);
+    static const Kernel kernels[6] = {kda_tc_kernel<false, 0>, kda_tc_kernel<false, 1>, kda_tc_kernel<false, 2>,
+                                      kda_tc_kernel<true, 0>,  kda_tc_kernel<true, 1>,  kda_tc_kernel<true, 2>};
+    const Kernel kernel = kernels[variant];
+    static int attr_set[6][64] = {{0}};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[slots][dev]) {
+    if (dev >= 0 && dev < 64 && !attr_set[variant][dev]) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set[slots][dev] = 1;
+        attr_set[variant][dev] = 1;
     }
     TcParams p;
     p.cu = a.cu_seqlens;
@@ -1496,7 +1463,6 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     p.N = a.N;
     p.T = a.T;
     p.H = a.H;
-    p.sorted = a.g_order ? 2 : (a.N <= kMaxSortedSeqs ? 1 : 0);
     p.g_order = a.g_order;
     p.g_rows = a.g_rows;
     p.g_une = a.g_units_nonempty;
