@@ -49,10 +49,14 @@ def peaks():
     return 6800.0, "fallback"
 
 
+# the sources kda_tc_kernel is compiled from (its launcher included)
+KERNEL_SOURCES = ("kda_common.cuh", "kda_internal.h", "kda_sm100.cuh", "kda_tc.cu")
+
+
 def kernel_source_sha() -> str:
     csrc = os.path.join(ROOT, "kda_linear_attention_chunk_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
