@@ -49,22 +49,26 @@ def peaks():
     return 6800.0, "fallback"
 
 
-# the sources kda_tc_kernel is compiled from (its launcher included)
+# the sources a kernel is compiled from (its launcher included)
 KERNEL_SOURCES = ("kda_common.cuh", "kda_internal.h", "kda_sm100.cuh", "kda_tc.cu")
+DECODE_SOURCES = ("kda_common.cuh", "kda_decode.h", "kda_decode.cu")
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(sources=None) -> str:
     csrc = os.path.join(ROOT, "kda_linear_attention_chunk_gb300", "csrc")
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources or KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.txt),
-    if it was taken on the kernel sources as they are now; else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
+def recorded_traffic(workload: str = None, sources=None):
+    """DRAM bytes per launch from a committed ncu summary (profiles/traffic.txt for
+    the prefill, profiles/traffic_<workload>.txt otherwise), if it was taken on
+    the kernel sources as they are now; else None."""
+    workload = workload or WORKLOAD
+    name = "traffic.txt" if workload == WORKLOAD else f"traffic_{workload}.txt"
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     d = {}
@@ -72,7 +76,7 @@ def recorded_traffic():
         if ":" in line and not line.lstrip().startswith("#"):
             key, val = line.split(":", 1)
             d[key.strip()] = val.strip()
-    if d.get("kernel_source_sha") != kernel_source_sha() or d.get("workload") != WORKLOAD:
+    if d.get("kernel_source_sha") != kernel_source_sha(sources) or d.get("workload") != workload:
         return None
     return int(d["dram_bytes_per_launch"]) if "dram_bytes_per_launch" in d else None
 
@@ -139,6 +143,57 @@ def make_device_inputs(w, seed_offset, torch, np):
     pin["cu"] = torch.from_numpy(w.cu_seqlens()).pin_memory()
     dev = {k: v.cuda() for k, v in pin.items()}
     return pin, dev
+
+
+DECODE_N, DECODE_H = 64, 32   # decode: 64 running requests, one token each, 32 heads
+
+
+def decode_bytes(n_live: int, n: int, h: int) -> int:
+    """Algorithmic bytes of one decode step: each live (sequence, head) reads and
+    writes its 64 KiB state; per row-head q, k, v, out (256 B each), g (512 B),
+    beta (4 B); the slot table."""
+    return n_live * h * 2 * 128 * 128 * 4 + n * h * (4 * 256 + 512 + 4) + 4 * n
+
+
+def measure_decode(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
+    """kda_decode on DECODE_N sequences x DECODE_H heads: a pool of 2 x DECODE_N
+    entries, the steps alternating between two slot tables that name disjoint
+    halves of it (each half 134 MB, above L2), CUDA events on the stream."""
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+    n, h = DECODE_N, DECODE_H
+    w = syn.Workload("decode64_h32", [1] * n, H=h, dk=128, dv=128, seed=77)
+    x = syn.draw(w)
+    d = {k: (torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16
+             else torch.from_numpy(v)).cuda() for k, v in x.items()}
+    rng = np.random.default_rng(77)
+    pool = torch.from_numpy((0.02 * rng.standard_normal((2 * n, h, 128, 128))).astype(np.float32)).cuda()
+    perm = rng.permutation(2 * n).astype(np.int32)
+    tables = [torch.from_numpy(np.sort(perm[:n])).cuda(), torch.from_numpy(np.sort(perm[n:])).cuda()]
+    out = torch.empty((n, h, 128), dtype=torch.bfloat16, device="cuda")
+
+    def step(i):
+        kda.decode(d["q"], d["k"], d["v"], d["g"], d["beta"], pool, state_slots=tables[i % 2], out=out,
+                   stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    alg = decode_bytes(n, n, h)
+    peak, peak_kind = peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    return {"workload": "decode64_h32", "kernel": "kda_decode_kernel", "N": n, "H": h, "steps": steps,
+            "us_per_step": ms * 1e3, "tokens_per_s": n / (ms / 1e3),
+            "l2": "2 slot tables over disjoint halves of a 2 x 64-entry pool (134 MB each)",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": alg,
+                         "traffic": recorded_traffic("decode64_h32", DECODE_SOURCES)}}
 
 
 def run_gpu_arm(args):
@@ -210,6 +265,7 @@ def run_gpu_arm(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     clocks = summarize_clocks(sampler.stop())
+    decode = measure_decode(torch, np, kda, stream) if not args.no_decode else None
     assert kda.device_error() == 0, "device error word set during the bench"
 
     t = torch.tensor([kernel_ms, e2e_ms], device="cuda")
@@ -244,6 +300,8 @@ def run_gpu_arm(args):
                      else "fallback 6.8 TB/s"},
         "clocks": clocks,
     }
+    if decode is not None:
+        line["decode"] = decode
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, heads=args.cpu_heads)
     if world > 1:
@@ -321,6 +379,7 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=32)
     ap.add_argument("--ref-heads", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

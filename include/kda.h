@@ -170,6 +170,36 @@ int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t
                             const int32_t *state_slots, float *state_pool, int num_slots,
                             uint16_t *out, int N, int T, int H, int dk, int dv, void *stream);
 
+/*
+ * kda_decode -- one step of the recurrence for each of N sequences (one new
+ * token each), the decode that runs between prefills (kern-k3-pp-prefill
+ * README: the KDA step over a rank's heads on the engine's state pool, padded
+ * rows skipped, section "D inside SGLang").  For sequence n and head h, with S
+ * the entry state_pool[state_slots[n]][h]:
+ *
+ *     S <- (I - beta k k^T) Diag(exp(g)) S + beta k v^T,   out = S^T q
+ *
+ * which is kda_chunk_prefill_slots on cu_seqlens = {0, 1, ..., N}.
+ *
+ *   q, k, v      bf16 bits [N][H][dk|dv], row n = sequence n's token.
+ *   g, beta      fp32 [N][H][dk], [N][H].
+ *   state_slots  int32 [N], device memory, or NULL for entry n.  -1 marks a
+ *                padded row: nothing of it is computed or written.  An id
+ *                outside [-1, num_slots) is treated like -1 and sets bit 8 of
+ *                the device error word.  Valid ids must be distinct.
+ *   state_pool   fp32 [num_slots][H][dv][dk], updated in place; entries no
+ *                row names are not touched.  With state_slots NULL,
+ *                num_slots >= N.
+ *   out          bf16 bits [N][H][dv].
+ *   N, H         rows (sequences) >= 1, heads >= 1; dk = dv = 128.
+ * Tensor pointers must be 16-byte aligned (beta and state_slots 4-byte); the
+ * pool must not overlap any other argument and out must not overlap an
+ * input.  Returns a kda_status.
+ */
+int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+               const float *beta, const int32_t *state_slots, float *state_pool, int num_slots,
+               uint16_t *out, int N, int H, int dk, int dv, void *stream);
+
 /* Human-readable name of a kda_status value (static string, never NULL). */
 const char *kda_status_string(int status);
 

@@ -20,7 +20,7 @@ KDA_ERR_NOALLOC_LIMIT = 8
 KDA_NOALLOC_MAX_SEQS = 16384
 
 EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error",
-            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots")
+            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode")
 ERR_BAD_SLOT = 8   # device error word bit: a state slot id outside [-1, num_slots)
 
 _lib = None
@@ -48,6 +48,8 @@ def load(path: str = LIB_PATH):
         fn.restype = I
     lib.kda_chunk_prefill_slots.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, P]
     lib.kda_chunk_prefill_slots.restype = I
+    lib.kda_decode.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, P]
+    lib.kda_decode.restype = I
     lib.kda_status_string.argtypes = [I]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), I]
@@ -92,6 +94,12 @@ def kda_chunk_prefill_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_poo
     """Raw C-ABI call with the states in a slot-addressed pool."""
     return load().kda_chunk_prefill_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_pool,
                                           num_slots, out, N, T, H, dk, dv, stream)
+
+
+def kda_decode(q, k, v, g, beta, state_slots, state_pool, num_slots: int, out, N: int, H: int, dk: int, dv: int,
+               stream) -> int:
+    """Raw C-ABI call: one recurrence step per sequence on a slot-addressed pool."""
+    return load().kda_decode(q, k, v, g, beta, state_slots, state_pool, num_slots, out, N, H, dk, dv, stream)
 
 
 def device_error(reset: bool = False) -> int:
@@ -177,4 +185,40 @@ def chunk_prefill_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_pool, o
                                  N, T, H, dk, dv, handle)
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_prefill_slots")
+    return out
+
+
+def decode(q, k, v, g, beta, state_pool, state_slots=None, out=None, stream=None):
+    """One KDA recurrence step per sequence (decode) on torch CUDA tensors.
+
+    q, k, v: [N][H][128] bfloat16 (row n = sequence n's new token); g:
+    [N][H][128] float32; beta: [N][H] float32; state_pool:
+    [num_slots][H][128][128] float32, updated in place; state_slots: [N] int32
+    on the device (-1 = padded row, skipped) or None for entry n.  Returns out
+    [N][H][128] bfloat16 (rows of padded sequences keep what ``out`` held).
+    """
+    import torch
+
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    tensors = [("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state_pool", state_pool)]
+    if state_slots is not None:
+        tensors.append(("state_slots", state_slots))
+    for name, t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("decode takes bfloat16 q/k/v")
+    if state_slots is not None and (state_slots.dtype != torch.int32 or tuple(state_slots.shape) != (N,)):
+        raise ValueError("state_slots must be int32 [N]")
+    if state_pool.dtype != torch.float32 or tuple(state_pool.shape[1:]) != (H, dv, dk):
+        raise ValueError("state_pool must be float32 [num_slots][H][dv][dk]")
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    handle = int(s.cuda_stream) if hasattr(s, "cuda_stream") else int(s)
+    st = kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_slots), _ptr(state_pool),
+                    int(state_pool.shape[0]), _ptr(out), N, H, dk, dv, handle)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode")
     return out

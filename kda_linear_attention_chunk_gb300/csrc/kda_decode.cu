@@ -1,0 +1,122 @@
+// kda_decode.cu -- one KDA recurrence step per sequence (decode), states in a
+// slot-addressed pool, updated in place.
+//
+// For sequence n and head h, with S = pool[slot[n]][h] (stored as S^T, [v][k]):
+//     S <- (I - beta k k^T) Diag(exp(g)) S + beta k v^T,   o = S^T q
+// i.e. S'[v][c] = S[v][c] exp(g_c),  e_v = sum_c S'[v][c] k_c,
+//      S[v][c]  = S'[v][c] + beta k_c (v_v - e_v),  o_v = sum_c S[v][c] q_c.
+// (The Kimi-K3 decode runs this step over a rank's heads on states held in the
+// engine's [slot][head][v][k] f32 pool, skipping padded rows, slot -1:
+// kern-k3-pp-prefill README, "D inside SGLang".)
+//
+// The step moves 128 KB of state per (sequence, head) against 1.5 KB of
+// inputs, so it is bound by HBM bandwidth: two CTAs (64 value rows each) stream
+// one state through registers once.  Thread (v, quarter) owns value row v and
+// the 16-byte pieces
+// 4j + quarter (j = 0..7) of it, so the four threads of a row read 64
+// contiguous bytes per load and a warp reads 16 full sectors.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kda_common.cuh"
+#include "kda_decode.h"
+
+namespace kda {
+namespace {
+
+constexpr int kDecThreads = 256;   // 64 value rows x 4 threads
+constexpr float kDecLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float dec_ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+struct DecodeParams {
+    const uint16_t *q, *k, *v;   // [N][H][128] bf16
+    const float *g, *beta;       // [N][H][128], [N][H]
+    const int32_t *slots;        // [N] or nullptr (entry n)
+    float *pool;                 // [num_slots][H][128][128]
+    uint16_t *out;               // [N][H][128] bf16
+    int N, H, num_slots;
+    int *err;
+};
+
+__global__ void __launch_bounds__(kDecThreads, 3) kda_decode_kernel(DecodeParams p)
+{
+    __shared__ float4 sa[32], sk[32], sq[32];   // exp(g), k, q of this (sequence, head), 128 each
+    const int rh = blockIdx.x >> 1, vhalf = blockIdx.x & 1;   // (sequence, head), half of the value rows
+    const int n = rh / p.H, h = rh % p.H;
+    int slot = n;
+    if (p.slots) {
+        slot = p.slots[n];
+        if (slot < -1 || slot >= p.num_slots) {
+            if (threadIdx.x == 0) atomicOr(p.err, kErrBadSlot);
+            return;
+        }
+        if (slot < 0) return;   // padded row: nothing is computed or written
+    }
+    const size_t row = (size_t)n * p.H + h;
+    const int tid = threadIdx.x;
+    if (tid < 128) {
+        reinterpret_cast<float *>(sa)[tid] = dec_ex2(p.g[row * 128 + tid] * kDecLog2e);
+        reinterpret_cast<float *>(sk)[tid] = bf16_bits_to_float(p.k[row * 128 + tid]);
+        reinterpret_cast<float *>(sq)[tid] = bf16_bits_to_float(p.q[row * 128 + tid]);
+    }
+    const int vr = 64 * vhalf + (tid >> 2), qt = tid & 3;
+    const float vv = bf16_bits_to_float(p.v[row * 128 + vr]);
+    const float beta = p.beta[row];
+    float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
+    float4 s[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) s[j] = st[4 * j + qt];
+    __syncthreads();
+    float e = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const float4 a = sa[4 * j + qt], kk = sk[4 * j + qt];
+        s[j].x *= a.x; s[j].y *= a.y; s[j].z *= a.z; s[j].w *= a.w;
+        e = fmaf(s[j].x, kk.x, e); e = fmaf(s[j].y, kk.y, e);
+        e = fmaf(s[j].z, kk.z, e); e = fmaf(s[j].w, kk.w, e);
+    }
+    e += __shfl_xor_sync(0xffffffffu, e, 1);
+    e += __shfl_xor_sync(0xffffffffu, e, 2);
+    const float u = beta * (vv - e);
+    float o = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const float4 kk = sk[4 * j + qt], qq = sq[4 * j + qt];
+        s[j].x = fmaf(kk.x, u, s[j].x); s[j].y = fmaf(kk.y, u, s[j].y);
+        s[j].z = fmaf(kk.z, u, s[j].z); s[j].w = fmaf(kk.w, u, s[j].w);
+        o = fmaf(s[j].x, qq.x, o); o = fmaf(s[j].y, qq.y, o);
+        o = fmaf(s[j].z, qq.z, o); o = fmaf(s[j].w, qq.w, o);
+        st[4 * j + qt] = s[j];
+    }
+    o += __shfl_xor_sync(0xffffffffu, o, 1);
+    o += __shfl_xor_sync(0xffffffffu, o, 2);
+    if (qt == 0) {
+        const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+        p.out[row * 128 + vr] = *reinterpret_cast<const uint16_t *>(&ob);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kda_decode_bf16_d128(const DecodeArgs &a)
+{
+    if (a.N == 0) return cudaSuccess;
+    DecodeParams p;
+    p.q = (const uint16_t *)a.q; p.k = (const uint16_t *)a.k; p.v = (const uint16_t *)a.v;
+    p.g = a.g; p.beta = a.beta; p.slots = a.state_slots; p.pool = a.state_pool;
+    p.out = (uint16_t *)a.out;
+    p.N = a.N; p.H = a.H; p.num_slots = a.num_slots;
+    p.err = a.err_word;
+    kda_decode_kernel<<<2 * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

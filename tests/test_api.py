@@ -115,3 +115,32 @@ def test_slots_validation_statuses(kda_lib):
 def test_slots_valid_call_passes_validation(kda_lib):
     assert call_slots() == kda.KDA_ERR_DEVICE
     assert call_slots(pool=A + (40 << 20) + 5 * 2 * 128 * 128 * 4) == kda.KDA_ERR_DEVICE   # pool just past
+
+
+def call_decode(**over):
+    N, H, d = 4, 2, 128
+    rows = N * H * d
+    args = dict(q=A, k=A + 2 * rows, v=A + 4 * rows, g=A + 6 * rows, beta=A + 10 * rows, slots=A + 11 * rows,
+                pool=A + (40 << 20), num_slots=6, out=A + 12 * rows, N=N, H=H, dk=d, dv=d, stream=0)
+    args.update(over)
+    order = ["q", "k", "v", "g", "beta", "slots", "pool", "num_slots", "out", "N", "H", "dk", "dv", "stream"]
+    return kda.kda_decode(*[args[n] for n in order])
+
+
+def test_decode_validation_statuses(kda_lib):
+    assert call_decode(q=0) == kda.KDA_ERR_NULL
+    assert call_decode(pool=0) == kda.KDA_ERR_NULL
+    assert call_decode(N=0) == kda.KDA_ERR_SHAPE
+    assert call_decode(num_slots=0) == kda.KDA_ERR_SHAPE
+    assert call_decode(slots=0, num_slots=3) == kda.KDA_ERR_SHAPE          # entry n needs num_slots >= N
+    assert call_decode(dk=64, dv=64) == kda.KDA_ERR_UNSUPPORTED
+    assert call_decode(q=A + 8) == kda.KDA_ERR_ALIGN
+    assert call_decode(slots=A + 11 * 1024 + 2) == kda.KDA_ERR_ALIGN
+    assert call_decode(pool=A) == kda.KDA_ERR_ALIAS                        # pool over q
+    assert call_decode(out=A + 6 * 1024) == kda.KDA_ERR_ALIAS              # out over v
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+def test_decode_valid_call_passes_validation(kda_lib):
+    assert call_decode() == kda.KDA_ERR_DEVICE
+    assert call_decode(slots=0, num_slots=4) == kda.KDA_ERR_DEVICE
