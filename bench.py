@@ -196,6 +196,63 @@ def measure_decode(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
                          "traffic": recorded_traffic("decode64_h32", DECODE_SOURCES)}}
 
 
+FOLD_W = 8   # speculative window: 8 draft tokens a sequence
+
+
+def fold_bytes(accepted, h: int, w: int) -> int:
+    """Algorithmic bytes of one fold: each (sequence, head) with accepted > 0 reads
+    and writes its 64 KiB state and reads k, v (256 B each), g (512 B) and beta
+    (4 B) of its accepted tokens; the accepted counts and slot table."""
+    n = len(accepted)
+    live = int((accepted > 0).sum())
+    toks = int(accepted.sum())
+    return live * h * 2 * 128 * 128 * 4 + toks * h * (2 * 256 + 512 + 4) + 8 * n
+
+
+def measure_fold(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
+    """kda_fold_commit on DECODE_N sequences x DECODE_H heads with windows of
+    FOLD_W tokens and seeded accepted counts in [0, FOLD_W]; the steps alternate
+    between two slot tables over disjoint halves of the pool (above L2)."""
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+    n, h, w = DECODE_N, DECODE_H, FOLD_W
+    wl = syn.Workload("fold64_w8_h32", [w] * n, H=h, dk=128, dv=128, seed=78)
+    x = syn.draw(wl)
+    d = {}
+    for k in ("k", "v", "g", "beta"):
+        v = x[k]
+        t = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16 else torch.from_numpy(v)
+        d[k] = t.reshape((n, w) + tuple(t.shape[1:])).contiguous().cuda()
+    rng = np.random.default_rng(78)
+    accepted = rng.integers(0, w + 1, n).astype(np.int32)
+    acc_t = torch.from_numpy(accepted).cuda()
+    pool = torch.from_numpy((0.02 * rng.standard_normal((2 * n, h, 128, 128))).astype(np.float32)).cuda()
+    perm = rng.permutation(2 * n).astype(np.int32)
+    tables = [torch.from_numpy(np.sort(perm[:n])).cuda(), torch.from_numpy(np.sort(perm[n:])).cuda()]
+
+    def step(i):
+        kda.fold_commit(d["k"], d["v"], d["g"], d["beta"], acc_t, pool, state_slots=tables[i % 2], stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    alg = fold_bytes(accepted, h, w)
+    peak, _ = peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    return {"workload": "fold64_w8_h32", "kernel": "kda_fold_kernel", "N": n, "H": h, "window": w,
+            "accepted_tokens": int(accepted.sum()), "steps": steps, "us_per_step": ms * 1e3,
+            "l2": "2 slot tables over disjoint halves of a 2 x 64-entry pool (134 MB each)",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": alg,
+                         "traffic": recorded_traffic("fold64_w8_h32", DECODE_SOURCES)}}
+
+
 def run_gpu_arm(args):
     import numpy as np
     import torch
@@ -266,6 +323,7 @@ def run_gpu_arm(args):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     clocks = summarize_clocks(sampler.stop())
     decode = measure_decode(torch, np, kda, stream) if not args.no_decode else None
+    fold = measure_fold(torch, np, kda, stream) if not args.no_decode else None
     assert kda.device_error() == 0, "device error word set during the bench"
 
     t = torch.tensor([kernel_ms, e2e_ms], device="cuda")
@@ -302,6 +360,8 @@ def run_gpu_arm(args):
     }
     if decode is not None:
         line["decode"] = decode
+    if fold is not None:
+        line["fold"] = fold
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, heads=args.cpu_heads)
     if world > 1:
@@ -379,7 +439,7 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=32)
     ap.add_argument("--ref-heads", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step and fold measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -200,6 +200,36 @@ int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
                const float *beta, const int32_t *state_slots, float *state_pool, int num_slots,
                uint16_t *out, int N, int H, int dk, int dv, void *stream);
 
+/*
+ * kda_fold_commit -- the state commit of a speculative decoding round (the
+ * ReplaySSM exact fold: SGLang PR #32890, prhub report section "实现拆解",
+ * item 3 and the speculative-decoding file list).  A verify pass scores W
+ * draft tokens per sequence without committing states; once accepted[n] of
+ * them are kept, this call folds exactly those tokens into the state:
+ *
+ *     for t in 0 .. accepted[n]-1:
+ *         S <- (I - beta_t k_t k_t^T) Diag(exp(g_t)) S + beta_t k_t v_t^T
+ *
+ * with S the entry state_pool[state_slots[n]][h] for every head h.  The
+ * result equals accepted[n] calls of kda_decode bit for bit (the same per-step
+ * arithmetic), while reading and writing each state once.  No outputs are
+ * produced (the verify pass already scored the tokens).
+ *
+ *   k, v         bf16 bits [N][W][H][dk|dv]: sequence n's window of W tokens.
+ *   g, beta      fp32 [N][W][H][dk], [N][W][H].
+ *   accepted     int32 [N], device memory, each in [0, W]; 0 leaves the state
+ *                untouched.  A count outside [0, W] is clamped into it and
+ *                sets bit 16 of the device error word.
+ *   state_slots  int32 [N] or NULL (entry n); -1 skips the sequence; an id
+ *                outside [-1, num_slots) is skipped and sets bit 8.
+ *   state_pool   fp32 [num_slots][H][dv][dk], updated in place.
+ *   N, W, H      sequences >= 1, window length >= 1, heads >= 1; dk = dv = 128.
+ * Alignment and aliasing rules as kda_decode.  Returns a kda_status.
+ */
+int kda_fold_commit(const uint16_t *k, const uint16_t *v, const float *g, const float *beta,
+                    const int32_t *accepted, const int32_t *state_slots, float *state_pool,
+                    int num_slots, int N, int W, int H, int dk, int dv, void *stream);
+
 /* Human-readable name of a kda_status value (static string, never NULL). */
 const char *kda_status_string(int status);
 
@@ -209,7 +239,8 @@ const char *kda_status_string(int status);
  * out sets bit 1 here and the kernel returns early (outputs are then
  * undefined).  Bit 2: a cu_seqlens entry broke its contract (indices were
  * clamped).  Bit 8: a state slot id was outside [-1, num_slots) (that
- * sequence was skipped).  0 means no kernel of this library has reported an
+ * sequence was skipped).  Bit 16: an accepted count of kda_fold_commit was
+ * outside [0, W] (clamped).  0 means no kernel of this library has reported an
  * error.
  * Synchronises the current device.  If `reset` is nonzero the word is
  * cleared after reading.  Returns KDA_OK or KDA_ERR_CUDA.

@@ -20,8 +20,9 @@ KDA_ERR_NOALLOC_LIMIT = 8
 KDA_NOALLOC_MAX_SEQS = 16384
 
 EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error",
-            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode")
+            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode", "kda_fold_commit")
 ERR_BAD_SLOT = 8   # device error word bit: a state slot id outside [-1, num_slots)
+ERR_BAD_ACCEPTED = 16   # device error word bit: an accepted count outside [0, window]
 
 _lib = None
 
@@ -50,6 +51,8 @@ def load(path: str = LIB_PATH):
     lib.kda_chunk_prefill_slots.restype = I
     lib.kda_decode.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, P]
     lib.kda_decode.restype = I
+    lib.kda_fold_commit.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
+    lib.kda_fold_commit.restype = I
     lib.kda_status_string.argtypes = [I]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), I]
@@ -100,6 +103,13 @@ def kda_decode(q, k, v, g, beta, state_slots, state_pool, num_slots: int, out, N
                stream) -> int:
     """Raw C-ABI call: one recurrence step per sequence on a slot-addressed pool."""
     return load().kda_decode(q, k, v, g, beta, state_slots, state_pool, num_slots, out, N, H, dk, dv, stream)
+
+
+def kda_fold_commit(k, v, g, beta, accepted, state_slots, state_pool, num_slots: int, N: int, W: int, H: int,
+                    dk: int, dv: int, stream) -> int:
+    """Raw C-ABI call: fold the accepted tokens of each window into the pool."""
+    return load().kda_fold_commit(k, v, g, beta, accepted, state_slots, state_pool, num_slots, N, W, H, dk, dv,
+                                  stream)
 
 
 def device_error(reset: bool = False) -> int:
@@ -222,3 +232,36 @@ def decode(q, k, v, g, beta, state_pool, state_slots=None, out=None, stream=None
     if st != KDA_OK:
         raise KdaError(st, "kda_decode")
     return out
+
+
+def fold_commit(k, v, g, beta, accepted, state_pool, state_slots=None, stream=None):
+    """Commit of a speculative round on torch CUDA tensors: the first accepted[n]
+    tokens of sequence n's window are folded into its state.
+
+    k, v: [N][W][H][128] bfloat16; g: [N][W][H][128] float32; beta: [N][W][H]
+    float32; accepted: [N] int32 on the device; state_pool:
+    [num_slots][H][128][128] float32, updated in place; state_slots: [N] int32
+    (-1 = skip) or None for entry n.
+    """
+    import torch
+
+    N, W, H, dk = k.shape
+    dv = v.shape[3]
+    tensors = [("k", k), ("v", v), ("g", g), ("beta", beta), ("accepted", accepted), ("state_pool", state_pool)]
+    if state_slots is not None:
+        tensors.append(("state_slots", state_slots))
+    for name, t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k.dtype != torch.bfloat16:
+        raise ValueError("fold_commit takes bfloat16 k/v")
+    if accepted.dtype != torch.int32 or tuple(accepted.shape) != (N,):
+        raise ValueError("accepted must be int32 [N]")
+    if state_pool.dtype != torch.float32 or tuple(state_pool.shape[1:]) != (H, dv, dk):
+        raise ValueError("state_pool must be float32 [num_slots][H][dv][dk]")
+    s = stream if stream is not None else torch.cuda.current_stream(k.device)
+    handle = int(s.cuda_stream) if hasattr(s, "cuda_stream") else int(s)
+    st = kda_fold_commit(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(accepted), _ptr(state_slots),
+                         _ptr(state_pool), int(state_pool.shape[0]), N, W, H, dk, dv, handle)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fold_commit")

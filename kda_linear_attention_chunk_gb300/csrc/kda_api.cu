@@ -264,6 +264,41 @@ int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
     return kda::launch_kda_decode_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+int kda_fold_commit(const uint16_t *k, const uint16_t *v, const float *g, const float *beta, const int32_t *accepted,
+                    const int32_t *state_slots, float *state_pool, int num_slots, int N, int W, int H, int dk, int dv,
+                    void *stream)
+{
+    if (!k || !v || !g || !beta || !accepted || !state_pool) return KDA_ERR_NULL;
+    if (N < 1 || W < 1 || H < 1 || dk < 1 || dv < 1 || num_slots < 1) return KDA_ERR_SHAPE;
+    if (!state_slots && num_slots < N) return KDA_ERR_SHAPE;
+    const size_t rows = (size_t)N * W * H;
+    if ((size_t)N * (size_t)H > 0x3fffffffu || (size_t)num_slots * (size_t)H > 0x7fffffffu ||
+        rows * 128 * 4 >= ((size_t)1 << 40))
+        return KDA_ERR_SHAPE;
+    if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+    const void *aligned_ptrs[] = {k, v, g, state_pool};
+    for (const void *p : aligned_ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGN;
+    if (((uintptr_t)beta & 3u) || ((uintptr_t)accepted & 3u) || ((uintptr_t)state_slots & 3u)) return KDA_ERR_ALIGN;
+    const Range in[] = {range_of(k, rows * dk * 2), range_of(v, rows * dv * 2),
+                        range_of(g, rows * dk * sizeof(float)), range_of(beta, rows * sizeof(float)),
+                        range_of(accepted, (size_t)N * sizeof(int32_t)),
+                        range_of(state_slots, (size_t)N * sizeof(int32_t))};
+    const Range rp = range_of(state_pool, (size_t)num_slots * H * dv * dk * sizeof(float));
+    for (const Range &r : in)
+        if (overlap(rp, r)) return KDA_ERR_ALIAS;
+    DevInfo *d = nullptr;
+    int st;
+    if ((st = device_info(&d)) != KDA_OK) return st;
+    kda::FoldArgs a;
+    a.k = k; a.v = v; a.g = g; a.beta = beta; a.accepted = accepted;
+    a.state_slots = state_slots; a.state_pool = state_pool;
+    a.N = N; a.W = W; a.H = H; a.num_slots = num_slots;
+    a.stream = (cudaStream_t)stream;
+    a.err_word = d->err;
+    return kda::launch_kda_fold_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 int kda_device_error(int *word, int reset)
 {
     if (!word) return KDA_ERR_NULL;

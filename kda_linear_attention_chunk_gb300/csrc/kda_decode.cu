@@ -46,20 +46,65 @@ struct DecodeParams {
     int *err;
 };
 
+// One token's update of this thread's 32 state entries (row vr, pieces 4j + qt),
+// with exp(g), k and q of the token staged in shared memory:
+//   S' = S exp(g),  e = S' . k (over the row's four threads),
+//   S = S' + k beta (v - e),  returns S . q (over the row's four threads).
+// The decode step and the fold both run exactly this sequence of operations,
+// so folding a tokens equals a decode steps bit for bit.
+__device__ __forceinline__ float token_step(float4 (&s)[8], const float4 *sa, const float4 *sk, const float4 *sq,
+                                            int qt, float vv, float beta)
+{
+    float e = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const float4 a = sa[4 * j + qt], kk = sk[4 * j + qt];
+        s[j].x *= a.x; s[j].y *= a.y; s[j].z *= a.z; s[j].w *= a.w;
+        e = fmaf(s[j].x, kk.x, e); e = fmaf(s[j].y, kk.y, e);
+        e = fmaf(s[j].z, kk.z, e); e = fmaf(s[j].w, kk.w, e);
+    }
+    e += __shfl_xor_sync(0xffffffffu, e, 1);
+    e += __shfl_xor_sync(0xffffffffu, e, 2);
+    const float u = beta * (vv - e);
+    float o = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const float4 kk = sk[4 * j + qt];
+        s[j].x = fmaf(kk.x, u, s[j].x); s[j].y = fmaf(kk.y, u, s[j].y);
+        s[j].z = fmaf(kk.z, u, s[j].z); s[j].w = fmaf(kk.w, u, s[j].w);
+        if (sq) {
+            const float4 qq = sq[4 * j + qt];
+            o = fmaf(s[j].x, qq.x, o); o = fmaf(s[j].y, qq.y, o);
+            o = fmaf(s[j].z, qq.z, o); o = fmaf(s[j].w, qq.w, o);
+        }
+    }
+    if (sq) {
+        o += __shfl_xor_sync(0xffffffffu, o, 1);
+        o += __shfl_xor_sync(0xffffffffu, o, 2);
+    }
+    return o;
+}
+
+// The pool entry of sequence n, -1 to skip it (padding, or an id outside the
+// pool, which is reported).
+__device__ __forceinline__ int decode_slot(const int32_t *slots, int n, int num_slots, int *err)
+{
+    if (!slots) return n;
+    const int slot = slots[n];
+    if (slot < -1 || slot >= num_slots) {
+        if (threadIdx.x == 0) atomicOr(err, kErrBadSlot);
+        return -1;
+    }
+    return slot;
+}
+
 __global__ void __launch_bounds__(kDecThreads, 3) kda_decode_kernel(DecodeParams p)
 {
     __shared__ float4 sa[32], sk[32], sq[32];   // exp(g), k, q of this (sequence, head), 128 each
     const int rh = blockIdx.x >> 1, vhalf = blockIdx.x & 1;   // (sequence, head), half of the value rows
     const int n = rh / p.H, h = rh % p.H;
-    int slot = n;
-    if (p.slots) {
-        slot = p.slots[n];
-        if (slot < -1 || slot >= p.num_slots) {
-            if (threadIdx.x == 0) atomicOr(p.err, kErrBadSlot);
-            return;
-        }
-        if (slot < 0) return;   // padded row: nothing is computed or written
-    }
+    const int slot = decode_slot(p.slots, n, p.num_slots, p.err);
+    if (slot < 0) return;   // padded row: nothing is computed or written
     const size_t row = (size_t)n * p.H + h;
     const int tid = threadIdx.x;
     if (tid < 128) {
@@ -75,33 +120,68 @@ __global__ void __launch_bounds__(kDecThreads, 3) kda_decode_kernel(DecodeParams
 #pragma unroll
     for (int j = 0; j < 8; j++) s[j] = st[4 * j + qt];
     __syncthreads();
-    float e = 0.f;
+    const float o = token_step(s, sa, sk, sq, qt, vv, beta);
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const float4 a = sa[4 * j + qt], kk = sk[4 * j + qt];
-        s[j].x *= a.x; s[j].y *= a.y; s[j].z *= a.z; s[j].w *= a.w;
-        e = fmaf(s[j].x, kk.x, e); e = fmaf(s[j].y, kk.y, e);
-        e = fmaf(s[j].z, kk.z, e); e = fmaf(s[j].w, kk.w, e);
-    }
-    e += __shfl_xor_sync(0xffffffffu, e, 1);
-    e += __shfl_xor_sync(0xffffffffu, e, 2);
-    const float u = beta * (vv - e);
-    float o = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const float4 kk = sk[4 * j + qt], qq = sq[4 * j + qt];
-        s[j].x = fmaf(kk.x, u, s[j].x); s[j].y = fmaf(kk.y, u, s[j].y);
-        s[j].z = fmaf(kk.z, u, s[j].z); s[j].w = fmaf(kk.w, u, s[j].w);
-        o = fmaf(s[j].x, qq.x, o); o = fmaf(s[j].y, qq.y, o);
-        o = fmaf(s[j].z, qq.z, o); o = fmaf(s[j].w, qq.w, o);
-        st[4 * j + qt] = s[j];
-    }
-    o += __shfl_xor_sync(0xffffffffu, o, 1);
-    o += __shfl_xor_sync(0xffffffffu, o, 2);
+    for (int j = 0; j < 8; j++) st[4 * j + qt] = s[j];
     if (qt == 0) {
         const __nv_bfloat16 ob = __float2bfloat16_rn(o);
         p.out[row * 128 + vr] = *reinterpret_cast<const uint16_t *>(&ob);
     }
+}
+
+struct FoldParams {
+    const uint16_t *k, *v;       // [N][W][H][128] bf16: each sequence's window of W tokens
+    const float *g, *beta;       // [N][W][H][128], [N][W][H]
+    const int32_t *accepted;     // [N]: fold the first accepted[n] tokens of the window
+    const int32_t *slots;        // [N] or nullptr (entry n)
+    float *pool;                 // [num_slots][H][128][128]
+    int N, W, H, num_slots;
+    int *err;
+};
+
+// Commit of a speculative round: the state takes the first accepted[n] tokens
+// of sequence n's window, one token_step each.  The state stays in registers;
+// the tokens' exp(g), k, v and beta are staged in shared memory up to
+// kFoldBatch tokens at a time, all loads of a batch in flight together, so the
+// steps themselves wait on no memory.
+constexpr int kFoldBatch = 16;
+
+__global__ void __launch_bounds__(kDecThreads, 3) kda_fold_kernel(FoldParams p)
+{
+    __shared__ float4 sa[kFoldBatch][32], sk[kFoldBatch][32];
+    __shared__ float sv[kFoldBatch][128], sb[kFoldBatch];
+    const int rh = blockIdx.x >> 1, vhalf = blockIdx.x & 1;
+    const int n = rh / p.H, h = rh % p.H;
+    const int slot = decode_slot(p.slots, n, p.num_slots, p.err);
+    if (slot < 0) return;
+    int acc = p.accepted[n];
+    if (acc < 0 || acc > p.W) {
+        if (threadIdx.x == 0) atomicOr(p.err, kErrBadAccepted);
+        acc = acc < 0 ? 0 : p.W;
+    }
+    if (acc == 0) return;   // nothing accepted: the state stays as it is
+    const int tid = threadIdx.x;
+    const int vr = 64 * vhalf + (tid >> 2), qt = tid & 3;
+    float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
+    float4 s[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) s[j] = st[4 * j + qt];
+    for (int t0 = 0; t0 < acc; t0 += kFoldBatch) {
+        const int nt = min(kFoldBatch, acc - t0);
+        if (t0 > 0) __syncthreads();           // the previous batch is no longer read
+        for (int i = tid; i < nt * 128; i += kDecThreads) {
+            const int t = i >> 7, c = i & 127;
+            const size_t row = ((size_t)n * p.W + t0 + t) * p.H + h;
+            reinterpret_cast<float *>(sa[t])[c] = dec_ex2(p.g[row * 128 + c] * kDecLog2e);
+            reinterpret_cast<float *>(sk[t])[c] = bf16_bits_to_float(p.k[row * 128 + c]);
+            sv[t][c] = bf16_bits_to_float(p.v[row * 128 + c]);
+            if (c == 0) sb[t] = p.beta[row];
+        }
+        __syncthreads();
+        for (int t = 0; t < nt; t++) token_step(s, sa[t], sk[t], nullptr, qt, sv[t][vr], sb[t]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j++) st[4 * j + qt] = s[j];
 }
 
 }  // namespace
@@ -116,6 +196,17 @@ cudaError_t launch_kda_decode_bf16_d128(const DecodeArgs &a)
     p.N = a.N; p.H = a.H; p.num_slots = a.num_slots;
     p.err = a.err_word;
     kda_decode_kernel<<<2 * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kda_fold_bf16_d128(const FoldArgs &a)
+{
+    FoldParams p;
+    p.k = (const uint16_t *)a.k; p.v = (const uint16_t *)a.v;
+    p.g = a.g; p.beta = a.beta; p.accepted = a.accepted; p.slots = a.state_slots; p.pool = a.state_pool;
+    p.N = a.N; p.W = a.W; p.H = a.H; p.num_slots = a.num_slots;
+    p.err = a.err_word;
+    kda_fold_kernel<<<2 * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
     return cudaGetLastError();
 }
 

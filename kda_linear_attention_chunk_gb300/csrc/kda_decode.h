@@ -21,4 +21,22 @@ struct DecodeArgs {
 
 cudaError_t launch_kda_decode_bf16_d128(const DecodeArgs &a);
 
+// device error word bit of the fold (bits 1-8 are listed in kda_common.cuh):
+// an accepted count outside [0, window] (clamped)
+enum : int { kErrBadAccepted = 16 };
+
+// commit of a speculative round: the first accepted[n] tokens of each window
+struct FoldArgs {
+    const void *k, *v;              // [N][W][H][128] bf16
+    const float *g, *beta;          // [N][W][H][128], [N][W][H]
+    const int32_t *accepted;        // [N]
+    const int32_t *state_slots;     // [N] or nullptr (entry n)
+    float *state_pool;              // [num_slots][H][128][128]
+    int N, W, H, num_slots;
+    cudaStream_t stream;
+    int *err_word;
+};
+
+cudaError_t launch_kda_fold_bf16_d128(const FoldArgs &a);
+
 }  // namespace kda

@@ -144,3 +144,29 @@ def test_decode_validation_statuses(kda_lib):
 def test_decode_valid_call_passes_validation(kda_lib):
     assert call_decode() == kda.KDA_ERR_DEVICE
     assert call_decode(slots=0, num_slots=4) == kda.KDA_ERR_DEVICE
+
+
+def call_fold(**over):
+    N, W, H, d = 4, 3, 2, 128
+    rows = N * W * H * d
+    args = dict(k=A, v=A + 2 * rows, g=A + 4 * rows, beta=A + 8 * rows, acc=A + 8 * rows + 4096,
+                slots=A + 8 * rows + 8192, pool=A + (40 << 20), num_slots=6, N=N, W=W, H=H, dk=d, dv=d, stream=0)
+    args.update(over)
+    order = ["k", "v", "g", "beta", "acc", "slots", "pool", "num_slots", "N", "W", "H", "dk", "dv", "stream"]
+    return kda.kda_fold_commit(*[args[n] for n in order])
+
+
+def test_fold_validation_statuses(kda_lib):
+    assert call_fold(k=0) == kda.KDA_ERR_NULL
+    assert call_fold(acc=0) == kda.KDA_ERR_NULL
+    assert call_fold(W=0) == kda.KDA_ERR_SHAPE
+    assert call_fold(slots=0, num_slots=3) == kda.KDA_ERR_SHAPE
+    assert call_fold(dk=64, dv=64) == kda.KDA_ERR_UNSUPPORTED
+    assert call_fold(k=A + 8) == kda.KDA_ERR_ALIGN
+    assert call_fold(acc=A + 8 * 3072 * 4 + 4098) == kda.KDA_ERR_ALIGN
+    assert call_fold(pool=A) == kda.KDA_ERR_ALIAS
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+def test_fold_valid_call_passes_validation(kda_lib):
+    assert call_fold() == kda.KDA_ERR_DEVICE
