@@ -253,6 +253,21 @@ def measure_fold(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
                          "traffic": recorded_traffic("fold64_w8_h32", DECODE_SOURCES)}}
 
 
+def max_over_ranks(values, world: int, dist=None, device="cpu"):
+    """Every rank's timings -> their maximum over the ranks (each rank gets it):
+    the job takes as long as its slowest replica."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def replica_throughput(rows_per_replica: int, world: int, ms_per_step: float) -> float:
+    """Whole-job rows/s: every replica processes its own copy of the workload."""
+    return world * rows_per_replica / (ms_per_step / 1e3)
+
+
 def run_gpu_arm(args):
     import numpy as np
     import torch
@@ -326,17 +341,15 @@ def run_gpu_arm(args):
     fold = measure_fold(torch, np, kda, stream) if not args.no_decode else None
     assert kda.device_error() == 0, "device error word set during the bench"
 
-    t = torch.tensor([kernel_ms, e2e_ms], device="cuda")
+    kernel_ms, e2e_ms = max_over_ranks([kernel_ms, e2e_ms], world, dist, device="cuda")
     if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
         dist.barrier()
-    kernel_ms, e2e_ms = float(t[0]), float(t[1])
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return None
 
-    value = world * w.T / (kernel_ms / 1e3)
+    value = replica_throughput(w.T, world, kernel_ms)
     alg = algorithmic_bytes(w)
     peak, peak_kind = peaks()
     achieved = alg / (kernel_ms / 1e3) / 1e9
@@ -348,7 +361,7 @@ def run_gpu_arm(args):
                    "lengths": w.lengths, "initial_state": "N(0,0.02) fp32", "final_state": True,
                    "l2": "inputs larger than L2: 2 rotating input sets of %.0f MB" % (alg / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "e2e": {"value": world * w.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": replica_throughput(w.T, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
