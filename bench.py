@@ -309,30 +309,55 @@ def run_gpu_arm(args):
     torch.cuda.synchronize()
     kernel_ms = ev0.elapsed_time(ev1) / args.steps
 
-    # end to end through the public API: pinned host inputs -> device, call, results -> pinned host
-    host_out = torch.empty((w.T, w.H, w.dv), dtype=torch.bfloat16).pin_memory()
-    host_fin = torch.empty((w.N, w.H, w.dv, w.dk), dtype=torch.float32).pin_memory()
-    dev_in = {k: torch.empty_like(v, device="cuda") for k, v in sets[0][0].items()}
+    # end to end through the public API: every step copies its inputs from pinned
+    # host memory, runs the call and reads its results back to pinned host memory.
+    # Steps are pipelined over three streams (inputs in, compute, results out)
+    # with two device buffer sets, so one step's inputs travel in while the
+    # previous step's results travel out (the host link carries both directions).
+    host_out = [torch.empty((w.T, w.H, w.dv), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    host_fin = [torch.empty((w.N, w.H, w.dv, w.dk), dtype=torch.float32).pin_memory() for _ in range(2)]
+    dev_in = [{k: torch.empty_like(v, device="cuda") for k, v in sets[0][0].items()} for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in sets[0][0].values())
-    d2h = host_out.numel() * 2 + host_fin.numel() * 4
+    d2h = host_out[0].numel() * 2 + host_fin[0].numel() * 4
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]       # inputs of buffer b landed
+    ev_k = [torch.cuda.Event() for _ in range(2)]        # call on buffer b done
+    ev_out = [torch.cuda.Event() for _ in range(2)]      # results of buffer b read back
 
     def e2e_step(i):
+        b = i % 2
         pin = sets[i % 2][0]
-        for k, v in pin.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        kda.chunk_prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["cu"],
-                          initial_state=dev_in["s0"], out=outs[0], final_state=fins[0], stream=stream)
-        host_out.copy_(outs[0], non_blocking=True)
-        host_fin.copy_(fins[0], non_blocking=True)
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_k[b])                 # buffer b's previous call has read its inputs
+            for k, v in pin.items():
+                dev_in[b][k].copy_(v, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])                 # buffer b's previous results are read back
+        kda.chunk_prefill(dev_in[b]["q"], dev_in[b]["k"], dev_in[b]["v"], dev_in[b]["g"], dev_in[b]["beta"],
+                          dev_in[b]["cu"], initial_state=dev_in[b]["s0"], out=outs[b], final_state=fins[b],
+                          stream=stream)
+        ev_k[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_k[b])
+            host_out[b].copy_(outs[b], non_blocking=True)
+            host_fin[b].copy_(fins[b], non_blocking=True)
+            ev_out[b].record(s_out)
 
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 50))
+    # device timing: the input stream starts after e0; e1 follows the last read-back
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    s_in.wait_event(e0)
     for i in range(e2e_steps):
         e2e_step(i)
+    stream.wait_event(ev_out[(e2e_steps - 1) % 2])
+    stream.wait_event(ev_out[e2e_steps % 2])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
