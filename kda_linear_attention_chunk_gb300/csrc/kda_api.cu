@@ -237,7 +237,7 @@ int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
     if (!q || !k || !v || !g || !beta || !state_pool || !out) return KDA_ERR_NULL;
     if (N < 1 || H < 1 || dk < 1 || dv < 1 || num_slots < 1) return KDA_ERR_SHAPE;
     if (!state_slots && num_slots < N) return KDA_ERR_SHAPE;
-    if ((size_t)N * (size_t)H > 0x3fffffffu || (size_t)num_slots * (size_t)H > 0x7fffffffu) return KDA_ERR_SHAPE;
+    if ((size_t)N * (size_t)H > 0x1fffffffu || (size_t)num_slots * (size_t)H > 0x7fffffffu) return KDA_ERR_SHAPE;
     if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
     const void *aligned_ptrs[] = {q, k, v, g, out, state_pool};
     for (const void *p : aligned_ptrs)
@@ -272,7 +272,7 @@ int kda_fold_commit(const uint16_t *k, const uint16_t *v, const float *g, const 
     if (N < 1 || W < 1 || H < 1 || dk < 1 || dv < 1 || num_slots < 1) return KDA_ERR_SHAPE;
     if (!state_slots && num_slots < N) return KDA_ERR_SHAPE;
     const size_t rows = (size_t)N * W * H;
-    if ((size_t)N * (size_t)H > 0x3fffffffu || (size_t)num_slots * (size_t)H > 0x7fffffffu ||
+    if ((size_t)N * (size_t)H > 0x1fffffffu || (size_t)num_slots * (size_t)H > 0x7fffffffu ||
         rows * 128 * 4 >= ((size_t)1 << 40))
         return KDA_ERR_SHAPE;
     if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;

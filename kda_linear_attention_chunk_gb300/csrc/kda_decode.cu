@@ -10,11 +10,10 @@
 // kern-k3-pp-prefill README, "D inside SGLang".)
 //
 // The step moves 128 KB of state per (sequence, head) against 1.5 KB of
-// inputs, so it is bound by HBM bandwidth: two CTAs (64 value rows each) stream
-// one state through registers once.  Thread (v, quarter) owns value row v and
-// the 16-byte pieces
-// 4j + quarter (j = 0..7) of it, so the four threads of a row read 64
-// contiguous bytes per load and a warp reads 16 full sectors.
+// inputs, so it is bound by HBM bandwidth: four CTAs (32 value rows each) stream
+// one state through registers once.  Thread (v, e) owns value row v and the
+// 16-byte pieces 8j + e (j = 0..3) of it, so the eight threads of a row read
+// 128 contiguous bytes per load and a warp reads four full lines.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -24,7 +23,8 @@
 namespace kda {
 namespace {
 
-constexpr int kDecThreads = 256;   // 64 value rows x 4 threads
+constexpr int kDecThreads = 256;   // 32 value rows x 8 threads
+constexpr int kDecRows = 32;       // value rows per CTA
 constexpr float kDecLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float dec_ex2(float x)
@@ -46,34 +46,35 @@ struct DecodeParams {
     int *err;
 };
 
-// One token's update of this thread's 32 state entries (row vr, pieces 4j + qt),
+// One token's update of this thread's 16 state entries (row vr, pieces 8j + e),
 // with exp(g), k and q of the token staged in shared memory:
-//   S' = S exp(g),  e = S' . k (over the row's four threads),
-//   S = S' + k beta (v - e),  returns S . q (over the row's four threads).
+//   S' = S exp(g),  e = S' . k (over the row's eight threads),
+//   S = S' + k beta (v - e),  returns S . q (over the row's eight threads).
 // The decode step and the fold both run exactly this sequence of operations,
 // so folding a tokens equals a decode steps bit for bit.
-__device__ __forceinline__ float token_step(float4 (&s)[8], const float4 *sa, const float4 *sk, const float4 *sq,
-                                            int qt, float vv, float beta)
+__device__ __forceinline__ float token_step(float4 (&s)[4], const float4 *sa, const float4 *sk, const float4 *sq,
+                                            int qe, float vv, float beta)
 {
     float e = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const float4 a = sa[4 * j + qt], kk = sk[4 * j + qt];
+    for (int j = 0; j < 4; j++) {
+        const float4 a = sa[8 * j + qe], kk = sk[8 * j + qe];
         s[j].x *= a.x; s[j].y *= a.y; s[j].z *= a.z; s[j].w *= a.w;
         e = fmaf(s[j].x, kk.x, e); e = fmaf(s[j].y, kk.y, e);
         e = fmaf(s[j].z, kk.z, e); e = fmaf(s[j].w, kk.w, e);
     }
     e += __shfl_xor_sync(0xffffffffu, e, 1);
     e += __shfl_xor_sync(0xffffffffu, e, 2);
+    e += __shfl_xor_sync(0xffffffffu, e, 4);
     const float u = beta * (vv - e);
     float o = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const float4 kk = sk[4 * j + qt];
+    for (int j = 0; j < 4; j++) {
+        const float4 kk = sk[8 * j + qe];
         s[j].x = fmaf(kk.x, u, s[j].x); s[j].y = fmaf(kk.y, u, s[j].y);
         s[j].z = fmaf(kk.z, u, s[j].z); s[j].w = fmaf(kk.w, u, s[j].w);
         if (sq) {
-            const float4 qq = sq[4 * j + qt];
+            const float4 qq = sq[8 * j + qe];
             o = fmaf(s[j].x, qq.x, o); o = fmaf(s[j].y, qq.y, o);
             o = fmaf(s[j].z, qq.z, o); o = fmaf(s[j].w, qq.w, o);
         }
@@ -81,6 +82,7 @@ __device__ __forceinline__ float token_step(float4 (&s)[8], const float4 *sa, co
     if (sq) {
         o += __shfl_xor_sync(0xffffffffu, o, 1);
         o += __shfl_xor_sync(0xffffffffu, o, 2);
+        o += __shfl_xor_sync(0xffffffffu, o, 4);
     }
     return o;
 }
@@ -98,10 +100,10 @@ __device__ __forceinline__ int decode_slot(const int32_t *slots, int n, int num_
     return slot;
 }
 
-__global__ void __launch_bounds__(kDecThreads, 3) kda_decode_kernel(DecodeParams p)
+__global__ void __launch_bounds__(kDecThreads, 4) kda_decode_kernel(DecodeParams p)
 {
     __shared__ float4 sa[32], sk[32], sq[32];   // exp(g), k, q of this (sequence, head), 128 each
-    const int rh = blockIdx.x >> 1, vhalf = blockIdx.x & 1;   // (sequence, head), half of the value rows
+    const int rh = blockIdx.x >> 2, vq = blockIdx.x & 3;   // (sequence, head), quarter of the value rows
     const int n = rh / p.H, h = rh % p.H;
     const int slot = decode_slot(p.slots, n, p.num_slots, p.err);
     if (slot < 0) return;   // padded row: nothing is computed or written
@@ -112,18 +114,18 @@ __global__ void __launch_bounds__(kDecThreads, 3) kda_decode_kernel(DecodeParams
         reinterpret_cast<float *>(sk)[tid] = bf16_bits_to_float(p.k[row * 128 + tid]);
         reinterpret_cast<float *>(sq)[tid] = bf16_bits_to_float(p.q[row * 128 + tid]);
     }
-    const int vr = 64 * vhalf + (tid >> 2), qt = tid & 3;
+    const int vr = kDecRows * vq + (tid >> 3), qe = tid & 7;
     const float vv = bf16_bits_to_float(p.v[row * 128 + vr]);
     const float beta = p.beta[row];
     float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
-    float4 s[8];
+    float4 s[4];
 #pragma unroll
-    for (int j = 0; j < 8; j++) s[j] = st[4 * j + qt];
+    for (int j = 0; j < 4; j++) s[j] = st[8 * j + qe];
     __syncthreads();
-    const float o = token_step(s, sa, sk, sq, qt, vv, beta);
+    const float o = token_step(s, sa, sk, sq, qe, vv, beta);
 #pragma unroll
-    for (int j = 0; j < 8; j++) st[4 * j + qt] = s[j];
-    if (qt == 0) {
+    for (int j = 0; j < 4; j++) st[8 * j + qe] = s[j];
+    if (qe == 0) {
         const __nv_bfloat16 ob = __float2bfloat16_rn(o);
         p.out[row * 128 + vr] = *reinterpret_cast<const uint16_t *>(&ob);
     }
@@ -146,11 +148,11 @@ struct FoldParams {
 // steps themselves wait on no memory.
 constexpr int kFoldBatch = 16;
 
-__global__ void __launch_bounds__(kDecThreads, 3) kda_fold_kernel(FoldParams p)
+__global__ void __launch_bounds__(kDecThreads, 4) kda_fold_kernel(FoldParams p)
 {
     __shared__ float4 sa[kFoldBatch][32], sk[kFoldBatch][32];
     __shared__ float sv[kFoldBatch][128], sb[kFoldBatch];
-    const int rh = blockIdx.x >> 1, vhalf = blockIdx.x & 1;
+    const int rh = blockIdx.x >> 2, vq = blockIdx.x & 3;
     const int n = rh / p.H, h = rh % p.H;
     const int slot = decode_slot(p.slots, n, p.num_slots, p.err);
     if (slot < 0) return;
@@ -161,11 +163,11 @@ __global__ void __launch_bounds__(kDecThreads, 3) kda_fold_kernel(FoldParams p)
     }
     if (acc == 0) return;   // nothing accepted: the state stays as it is
     const int tid = threadIdx.x;
-    const int vr = 64 * vhalf + (tid >> 2), qt = tid & 3;
+    const int vr = kDecRows * vq + (tid >> 3), qe = tid & 7;
     float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
-    float4 s[8];
+    float4 s[4];
 #pragma unroll
-    for (int j = 0; j < 8; j++) s[j] = st[4 * j + qt];
+    for (int j = 0; j < 4; j++) s[j] = st[8 * j + qe];
     for (int t0 = 0; t0 < acc; t0 += kFoldBatch) {
         const int nt = min(kFoldBatch, acc - t0);
         if (t0 > 0) __syncthreads();           // the previous batch is no longer read
@@ -178,10 +180,10 @@ __global__ void __launch_bounds__(kDecThreads, 3) kda_fold_kernel(FoldParams p)
             if (c == 0) sb[t] = p.beta[row];
         }
         __syncthreads();
-        for (int t = 0; t < nt; t++) token_step(s, sa[t], sk[t], nullptr, qt, sv[t][vr], sb[t]);
+        for (int t = 0; t < nt; t++) token_step(s, sa[t], sk[t], nullptr, qe, sv[t][vr], sb[t]);
     }
 #pragma unroll
-    for (int j = 0; j < 8; j++) st[4 * j + qt] = s[j];
+    for (int j = 0; j < 4; j++) st[8 * j + qe] = s[j];
 }
 
 }  // namespace
@@ -195,7 +197,7 @@ cudaError_t launch_kda_decode_bf16_d128(const DecodeArgs &a)
     p.out = (uint16_t *)a.out;
     p.N = a.N; p.H = a.H; p.num_slots = a.num_slots;
     p.err = a.err_word;
-    kda_decode_kernel<<<2 * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
+    kda_decode_kernel<<<(128 / kDecRows) * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -206,7 +208,7 @@ cudaError_t launch_kda_fold_bf16_d128(const FoldArgs &a)
     p.g = a.g; p.beta = a.beta; p.accepted = a.accepted; p.slots = a.state_slots; p.pool = a.state_pool;
     p.N = a.N; p.W = a.W; p.H = a.H; p.num_slots = a.num_slots;
     p.err = a.err_word;
-    kda_fold_kernel<<<2 * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
+    kda_fold_kernel<<<(128 / kDecRows) * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
     return cudaGetLastError();
 }
 
