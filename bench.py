@@ -268,6 +268,65 @@ def replica_throughput(rows_per_replica: int, world: int, ms_per_step: float) ->
     return world * rows_per_replica / (ms_per_step / 1e3)
 
 
+def config_bytes(w, rows: int, with_initial: bool) -> int:
+    """Algorithmic bytes of one call over `rows` rows of workload w: per row-head
+    q, k, v, out, g, beta (1540 B at bf16 d = 128; 1284 B at fp32 d = 64), plus
+    the states read (if any) and written."""
+    per_row_head = (w.dk + w.dk + w.dv + w.dv) * (2 if w.qkv_dtype == "bf16" else 4) + 4 * w.dk + 4
+    n = 1 if w.calls > 1 else w.N
+    return rows * w.H * per_row_head + n * w.H * w.dk * w.dv * 4 * (int(with_initial) + 1)
+
+
+def measure_configs(torch, np, kda, stream, reps: int = 3):
+    """The other four workloads, one line each: time per call (CUDA events, after
+    one warm-up), tokens/s and the fraction of the HBM roofline.  The context of
+    262,144 rows runs as its 32 chained calls of 8192 rows with the state carried;
+    for timing, every call reads the same 8192-row input set (each call's inputs
+    exceed L2, so nothing is served from a previous call)."""
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+    peak, _ = peaks()
+    res = {}
+    for name, w in syn.workloads().items():
+        if name == WORKLOAD:
+            continue
+        rows = w.T // w.calls
+        x = syn.draw(w, 0, rows)
+        dt = torch.bfloat16 if w.qkv_dtype == "bf16" else torch.float32
+        d = {k: (torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16
+                 else torch.from_numpy(v)).cuda() for k, v in x.items()}
+        cu = torch.tensor(w.cu_seqlens() if w.calls == 1 else [0, rows], dtype=torch.int32, device="cuda")
+        n = 1 if w.calls > 1 else w.N
+        s0 = syn.draw_initial_state(w)
+        s0 = torch.from_numpy(s0).cuda() if s0 is not None else None
+        out = torch.empty((rows, w.H, w.dv), dtype=dt, device="cuda")
+        fin = [torch.empty((n, w.H, w.dv, w.dk), dtype=torch.float32, device="cuda") for _ in range(2)]
+
+        def run():
+            state = s0
+            for c in range(w.calls):
+                kda.chunk_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, initial_state=state, out=out,
+                                  final_state=fin[c % 2], stream=stream)
+                state = fin[c % 2]
+
+        run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_call = e0.elapsed_time(e1) / (reps * w.calls)
+        alg = sum(config_bytes(w, rows, with_initial=(s0 is not None) or c > 0) for c in range(w.calls)) / w.calls
+        res[name] = {"calls": w.calls, "rows_per_call": rows, "us_per_call": ms_call * 1e3,
+                     "tokens_per_s": rows / (ms_call / 1e3),
+                     "roofline_frac": alg / (ms_call / 1e3) / 1e9 / peak,
+                     "units": n * w.H}
+        del d, out, fin, s0
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu_arm(args):
     import numpy as np
     import torch
@@ -364,6 +423,7 @@ def run_gpu_arm(args):
     clocks = summarize_clocks(sampler.stop())
     decode = measure_decode(torch, np, kda, stream) if not args.no_decode else None
     fold = measure_fold(torch, np, kda, stream) if not args.no_decode else None
+    configs = measure_configs(torch, np, kda, stream) if not args.no_configs else None
     assert kda.device_error() == 0, "device error word set during the bench"
 
     kernel_ms, e2e_ms = max_over_ranks([kernel_ms, e2e_ms], world, dist, device="cuda")
@@ -400,6 +460,8 @@ def run_gpu_arm(args):
         line["decode"] = decode
     if fold is not None:
         line["fold"] = fold
+    if configs is not None:
+        line["configs"] = configs
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, heads=args.cpu_heads)
     if world > 1:
@@ -478,6 +540,7 @@ def main():
     ap.add_argument("--ref-heads", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-step and fold measurements")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other four workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

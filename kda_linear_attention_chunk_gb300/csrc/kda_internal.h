@@ -31,7 +31,6 @@ struct KdaArgs {
 };
 
 cudaError_t launch_kda_simt_f32_d64(const KdaArgs &a);
-cudaError_t launch_kda_simt_bf16_d128(const KdaArgs &a);
 cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a);
 int tc_max_sorted_seqs();   // largest N the tensor-core kernel sorts by itself
 

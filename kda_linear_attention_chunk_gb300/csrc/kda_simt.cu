@@ -35,6 +35,9 @@ struct SimtSmem {
     float V[kChunk * D];            // [r][v]; later R = V - Kp S'
     float A[kChunk * kAStride];     // L -> T -> M, in place
     float B[kChunk * kAStride];
+    float G[kChunk * D];            // [r][c]: g of the chunk, then its cumulative sum G
+    float Kin[kChunk * D];          // [r][c]: k and q of the chunk as loaded
+    float Qin[kChunk * D];
     float gm[D], gl[D], pend[D];
     float beta[kChunk];
 };
@@ -65,17 +68,29 @@ kda_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin 
     for (int c0 = bos; c0 < eos; c0 += kChunk) {
         const int L = min(kChunk, eos - c0);
         const int m = (L - 1) / 2;
-        // G_m and G_{L-1} per channel.
-        if (tid < D) {
-            float acc = 0.f, gmv = 0.f;
-            for (int r = 0; r < L; r++) {
-                acc += g[((size_t)(c0 + r) * H + h) * D + tid];
-                if (r == m) gmv = acc;
-            }
-            sm.gm[tid] = gmv;
-            sm.gl[tid] = acc;
+        // The chunk's g, k, q and v tiles into shared memory, all threads, one row
+        // of D channels per warp pass (rows past the chunk zero).
+        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
+            const int r = idx / D, c = idx % D;
+            const size_t off = ((size_t)(c0 + r) * H + h) * D + c;
+            const bool in = r < L;
+            sm.G[idx] = in ? g[off] : 0.f;
+            sm.Kin[idx] = in ? load_in(k + off) : 0.f;
+            sm.Qin[idx] = in ? load_in(q + off) : 0.f;
+            sm.V[idx] = in ? load_in(v + off) : 0.f;
         }
         if (tid < kChunk) sm.beta[tid] = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        __syncthreads();
+        // G = running sum of g over the rows, per channel; G_m and G_{L-1}.
+        if (tid < D) {
+            float acc = 0.f;
+            for (int r = 0; r < L; r++) {
+                acc += sm.G[r * D + tid];
+                sm.G[r * D + tid] = acc;
+            }
+            sm.gm[tid] = sm.G[m * D + tid];
+            sm.gl[tid] = acc;
+        }
         __syncthreads();
         // S <- Diag(exp(G_m)) Diag(pend) S: first the previous chunk's pending
         // decay to its last row, then the view from row m.  Two separate
@@ -85,31 +100,22 @@ kda_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin 
             int c = idx / D;
             sm.S[idx] = (sm.S[idx] * sm.pend[c]) * expf(sm.gm[c]);
         }
-        // Decay-scaled operands (one thread per channel walks the rows).
-        if (tid < D) {
-            const int c = tid;
-            float acc = 0.f;
-            for (int r = 0; r < kChunk; r++) {
-                float kp = 0.f, km = 0.f, qp = 0.f;
-                if (r < L) {
-                    const size_t off = ((size_t)(c0 + r) * H + h) * D + c;
-                    acc += g[off];
-                    float a = expf(acc - sm.gm[c]);
-                    float b = expf(sm.gm[c] - acc);
-                    float kv = load_in(k + off), qv = load_in(q + off);
-                    kp = kv * a;
-                    km = kv * b;
-                    qp = qv * a;
-                }
-                sm.Kp[r * D + c] = kp;
-                sm.Km[r * D + c] = km;
-                sm.Qp[r * D + c] = qp;
+        // Decay-scaled operands, all threads over the tile.
+        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
+            const int r = idx / D, c = idx % D;
+            float kp = 0.f, km = 0.f, qp = 0.f;
+            if (r < L) {
+                const float G = sm.G[idx];
+                const float a = expf(G - sm.gm[c]);
+                const float b = expf(sm.gm[c] - G);
+                const float kv = sm.Kin[idx], qv = sm.Qin[idx];
+                kp = kv * a;
+                km = kv * b;
+                qp = qv * a;
             }
-        } else {
-            for (int idx = tid - D; idx < kChunk * D; idx += kThreads - D) {
-                int r = idx / D, vv = idx % D;
-                sm.V[idx] = r < L ? load_in(v + ((size_t)(c0 + r) * H + h) * D + vv) : 0.f;
-            }
+            sm.Kp[idx] = kp;
+            sm.Km[idx] = km;
+            sm.Qp[idx] = qp;
         }
         __syncthreads();
         // A (strictly lower, beta-scaled) and B (lower incl. diagonal).  The
@@ -210,9 +216,5 @@ static cudaError_t launch_simt(const KdaArgs &a)
 }
 
 cudaError_t launch_kda_simt_f32_d64(const KdaArgs &a) { return launch_simt<float, float, 64>(a); }
-cudaError_t launch_kda_simt_bf16_d128(const KdaArgs &a)
-{
-    return launch_simt<__nv_bfloat16, __nv_bfloat16, 128>(a);
-}
 
 }  // namespace kda
