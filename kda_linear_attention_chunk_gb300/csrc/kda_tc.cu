@@ -1015,7 +1015,9 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem
                 *reinterpret_cast<uint4 *>(dst + (size_t)(32 * half + r) * row_stride + 8 * q) =
                     *reinterpret_cast<const uint4 *>(ob + r * kOTRow + 16 * q);
         }
-        named_bar(kBarChain, kChainThreads);             // the buffer is free again
+        // the buffer is free again before the next half; the next chunk's rows are
+        // stored only after several more chain barriers
+        if (half == 0) named_bar(kBarChain, kChainThreads);
     }
     if (v == 0) KDA_PHASE(1, item, 9);
 }
