@@ -54,11 +54,20 @@ KERNEL_SOURCES = ("kda_common.cuh", "kda_internal.h", "kda_sm100.cuh", "kda_tc.c
 DECODE_SOURCES = ("kda_common.cuh", "kda_decode.h", "kda_decode.cu")
 
 
+def code_only(text: str) -> str:
+    """C/C++ source without comments, trailing blanks and empty lines: what the
+    compiler sees (comment edits do not invalidate a recorded measurement)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_sha(sources=None) -> str:
     csrc = os.path.join(ROOT, "kda_linear_attention_chunk_gb300", "csrc")
     h = hashlib.sha256()
     for f in sources or KERNEL_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,14 +9,14 @@
 // the factors W and U, the inter-chunk state recurrence, the outputs):
 //
 //   G_r  = sum_{u<=r} g_u,  m = (L-1)/2,  a_r = exp(G_r - G_m), b_r = 1/a_r
-//   Kp = K*a, Qp = Q*a, Km = K*b                 (fp16, in shared memory)
+//   Kp = beta*K*a, Qp = Q*a, Km = K*b            (fp16, in shared memory)
 //   [A_kk ; A_qk] = [Kp ; Qp] Km^T               MMA-a  (M=128, N=64, K=128)
-//   M  = (I + beta*strict(A_kk))^-1 diag(beta)   CUDA cores, fp32
-//   W'^T = Kp^T M^T,  U^T = V^T M^T              MMA-b  (M=128, N=64, K=64)
+//   T  = (I + strict(A_kk))^-1                   CUDA cores + warp MMA
+//   W'^T = Kp^T T^T,  U^T = (beta*V)^T T^T       MMA-b  (M=128, N=64, K=64)
 //   S' = Diag(exp(G_m)) S                        (state seen from row m)
-//   Delta^T = U^T - S'^T W'^T                    MMA1a  (A = S'^T from TMEM)
-//   O^T   = S'^T Qp^T + Delta^T B^T              MMA1b + MMA3b (B = tril(A_qk))
-//   S^T  += Delta^T Km                           MMA3a  (state stays fp32 in TMEM)
+//   [Delta^T | O^T] = [U^T | 0] + S'^T [-W' ; Qp]^T   MMA1 (one N=128 MMA, A = S'^T from TMEM)
+//   O^T  += Delta^T tril(A_qk)^T                 MMA3O
+//   S^T  += Delta^T Km                           MMA3S  (state stays fp32 in TMEM)
 //   S   <- Diag(exp(G_{L-1} - G_m)) S            (applied at the next chunk start)
 //
 // Everything is kept "v-major" (TMEM lane = value channel v) so that every MMA
@@ -26,12 +26,15 @@
 // ~2e-4; the midpoint reference m keeps every scaled operand within fp16 range
 // for half-chunk log-decays above about -11.
 //
-// Roles (416 threads):
-//   warps 0-3   chain: state scaling, S' and Delta conversion, the chain MMAs,
-//               output and final-state stores (one elected thread issues MMAs)
-//   warps 4-11  prep: cumulative log-decay (warp shuffles), decay-scaled
-//               operands, MMA-a, the 64x64 inverse, MMA-b, W' conversion
-//   warp 12     TMA producer and TMEM allocator
+// Roles (512 threads, 16 warps):
+//   warps 0-3    chain: state rescaling and its fp16 copy, -W' out of TMEM,
+//                MMA1, the Delta conversion, MMA3, output and final-state
+//                stores; its first thread requests the k/q/v tiles and issues
+//                the chain MMAs; warp 0 allocates TMEM
+//   warps 4-11   group E: cumulative log-decay, decay-scaled operands, MMA-a,
+//                beta*V; requests the next chunk's g and claims units
+//   warps 12-15  group I: A readout, the 64x64 inverse (16x16 diagonal blocks
+//                by forward substitution, block merges on the warp MMA), MMA-b
 // Two shared-memory stages let the prep of chunk c+1 overlap the chain of
 // chunk c.  Every mbarrier wait is bounded; on timeout the kernel records
 // kErrWaitTimeout in the device error word and winds down.
