@@ -15,8 +15,8 @@
 //   W'^T = Kp^T T^T,  U^T = (beta*V)^T T^T       MMA-b  (M=128, N=64, K=64)
 //   S' = Diag(exp(G_m)) S                        (state seen from row m)
 //   [Delta^T | O^T] = [U^T | 0] + S'^T [-W' ; Qp]^T   MMA1 (one N=128 MMA, A = S'^T from TMEM)
-//   O^T  += Delta^T tril(A_qk)^T                 MMA3O
-//   S^T  += Delta^T Km                           MMA3S  (state stays fp32 in TMEM)
+//   O^T += Delta^T tril(A_qk)^T, S^T += Delta^T Km  MMA3 (one N=192 MMA over
+//                                                [tril(A_qk)^T | Km]; the state stays fp32 in TMEM)
 //   S   <- Diag(exp(G_{L-1} - G_m)) S            (applied at the next chunk start)
 //
 // Everything is kept "v-major" (TMEM lane = value channel v) so that every MMA
@@ -27,14 +27,15 @@
 // for half-chunk log-decays above about -11.
 //
 // Roles (512 threads, 16 warps):
-//   warps 0-3    chain: state rescaling and its fp16 copy, -W' out of TMEM,
-//                MMA1, the Delta conversion, MMA3, output and final-state
-//                stores; its first thread requests the k/q/v tiles and issues
-//                the chain MMAs; warp 0 allocates TMEM
+//   warps 0-3    chain: state rescaling and its fp16 copy, MMA1, the Delta
+//                conversion, MMA3, output and final-state stores; its first
+//                thread requests the k/q/v tiles and issues the chain MMAs;
+//                warp 0 allocates TMEM
 //   warps 4-11   group E: cumulative log-decay, decay-scaled operands, MMA-a,
 //                beta*V; requests the next chunk's g and claims units
 //   warps 12-15  group I: A readout, the 64x64 inverse (16x16 diagonal blocks
-//                by forward substitution, block merges on the warp MMA), MMA-b
+//                by forward substitution, block merges on the warp MMA), MMA-b,
+//                -W' out of TMEM into the stage as MMA1's operand
 // Two shared-memory stages let the prep of chunk c+1 overlap the chain of
 // chunk c.  Every mbarrier wait is bounded; on timeout the kernel records
 // kErrWaitTimeout in the device error word and winds down.
@@ -86,10 +87,20 @@ constexpr int kMaxSortedSeqs = 256;
 // MMAs on it are done; g, T16 and group I's fp32 blocks are single shared
 // buffers because only one chunk at a time uses them.
 constexpr uint32_t kStageBytes = 73728;
-constexpr uint32_t kOffKQ = 0;          // [kb][K rows 0-63 | Q rows 0-63], 2 x 16 KB; K later -W' [c][r]
-constexpr uint32_t kOffKM = 32768;      // Km, 2 x 8 KB
-constexpr uint32_t kOffV = 49152;       // V (fp16 in place of bf16), 2 x 8 KB
-constexpr uint32_t kOffB = 65536;       // tril(A_qk) [r][i] fp16, 8 KB
+// k and q: [kb][128 rows][64 channels], 2 x 16 KB, K rows first in stage 0 and
+// Q rows first in stage 1 (so that MMA1's [Delta | O] output follows the TMEM
+// order below); the K rows later hold -W' [r][c]
+constexpr uint32_t kOffKQ = 0;
+constexpr uint32_t kOffV = 32768;       // V (fp16 in place of bf16), 2 x 8 KB
+// Km [kb][r][c] (2 x 8 KB) and tril(A_qk)^T [i][r] (8 KB): three 64-column
+// blocks, adjacent in the order of the TMEM columns MMA3 accumulates into --
+// stage 0 [tril(A_qk)^T | Km], stage 1 [Km | tril(A_qk)^T] -- so that MMA3 reads
+// one N = 192 operand (MN-major) from here
+constexpr uint32_t kOffMma3 = 49152;
+__device__ __forceinline__ uint32_t off_k(int s) { return s ? 8192u : 0u; }        // K rows in a kb block
+__device__ __forceinline__ uint32_t off_q(int s) { return s ? 0u : 8192u; }        // Q rows in a kb block
+__device__ __forceinline__ uint32_t off_km(int s) { return s ? 49152u : 57344u; }   // Km
+__device__ __forceinline__ uint32_t off_bq(int s) { return s ? 65536u : 49152u; }   // tril(A_qk)^T
 constexpr uint32_t kOffG = 2 * kStageBytes;     // g slot (fp32, 4 x 8 KB), read once by the decay scan
 constexpr uint32_t kOffT16 = kOffG + 32768;     // T = (I + A_kk)^-1 [r][j] fp16, 8 KB (MMA-b operand)
 constexpr uint32_t kOffTmp = kOffT16 + 8192;    // group I fp32 blocks of the inverse, 16 KB
@@ -105,24 +116,31 @@ constexpr uint32_t kOffMisc = kOffBar + 256;     // TMEM base, abort flag, sched
 // the start of chunk i+1 (or at the end of the unit), and only chunk i+3's
 // decay scan, which waits for chunk i+1's stage, can overwrite it.
 constexpr uint32_t kOffPend = kOffMisc + 128;
-constexpr uint32_t kOffOT = kOffPend + 3 * 512;             // output transpose, bf16 [32][128], rows 272 B apart
-constexpr uint32_t kOTRow = 272;
-constexpr uint32_t kSmemBytes = kOffOT + 32 * kOTRow + 1024;   // + alignment slack
+// output rows 32-63 of a chunk, bf16 [2 channel blocks][32 rows][64], 128B-swizzled
+// (rows 0-31 go to the stage's tril(A_qk) buffer, free once MMA3 is done)
+constexpr uint32_t kOffOT = (kOffPend + 3 * 512 + 1023) & ~1023u;
+constexpr uint32_t kSmemBytes = kOffOT + 8192 + 1024;   // + alignment slack
 
 // mbarrier slots ([2] = one per stage)
 constexpr int kBarKQFull = 0;      // [2]: k, q tiles landed
 constexpr int kBarVFull = 2;       // [2]: v tile landed
 constexpr int kBarPrepDone = 4;    // [2]: MMA-b of a chunk is done (W'^T and U^T in TMEM)
 constexpr int kBarAFull = 6;       // [2]: MMA-a done
-constexpr int kBarEDone = 8;       // [2]: group E finished a chunk's operands (128 arrivals)
+constexpr int kBarEDone = 8;       // [2]: group E has written a chunk's beta*V (256 arrivals)
 constexpr int kBarODone = 10;      // [2]: the chain has read a chunk's outputs (TMEM P_s free)
 constexpr int kBarFmReady = 12;    // [2]: the chunk's decay constants are written (128 arrivals)
 constexpr int kBarKmFree = 14;     // [2]: the chain's MMAs on the stage are done (Km, B free)
 constexpr int kBarGFull = 16;      // g slot landed
 constexpr int kBarMma1 = 18, kBarMma3 = 20, kBarDrain = 21;
+constexpr int kBarWReady = 22;     // [2]: -W' is in the stage's K rows, TMEM output columns zeroed (128 arrivals)
 
-// TMEM columns
-constexpr uint32_t kTmS = 0, kTmP = 128, kTmS0h = 384, kTmDh = 448, kTmCols = 512;
+// TMEM columns: [Delta_0 | O_0 | S | O_1 | Delta_1 | S'h | Delta h].  The O_s
+// columns take A (MMA-a), then W'^T (MMA-b), then the outputs; Delta_s takes
+// U^T (MMA-b), then Delta^T.  MMA1 writes [Delta_0 | O_0] or [O_1 | Delta_1]
+// (N = 128), MMA3 [O_0 | S] or [S | O_1] (N = 192).
+constexpr uint32_t kTmS = 128, kTmS0h = 384, kTmDh = 448, kTmCols = 512;
+__device__ __forceinline__ uint32_t tm_o(int s) { return s ? 256u : 64u; }
+__device__ __forceinline__ uint32_t tm_d(int s) { return s ? 320u : 0u; }
 
 constexpr uint32_t kKQBytes = 4 * 8192;        // k and q tiles (bf16)
 constexpr uint32_t kVBytes = 2 * 8192;         // v tile (bf16)
@@ -339,7 +357,7 @@ __device__ __forceinline__ void tile_mma(float (&d)[4], FA la, FB lb, int ks0, i
 // read the previous chunk's G.
 // =============================================================================
 struct Maps {
-    const CUtensorMap *q, *k, *v, *g;
+    const CUtensorMap *q, *k, *v, *g, *o;
 };
 
 // Walks this CTA's chunks in schedule order.
@@ -380,8 +398,8 @@ __device__ void issue_kq(const Smem &sm, const Maps &m, int item, int row0, int 
     KDA_PHASE(2, item, 0);
     mbar_arrive_expect_tx(bar, kKQBytes);
     for (int kb = 0; kb < 2; kb++) {
-        tma_load_3d(st + kOffKQ + kb * 16384, m.k, 64 * kb, h, row0, bar);
-        tma_load_3d(st + kOffKQ + kb * 16384 + 8192, m.q, 64 * kb, h, row0, bar);
+        tma_load_3d(st + kOffKQ + kb * 16384 + off_k(item & 1), m.k, 64 * kb, h, row0, bar);
+        tma_load_3d(st + kOffKQ + kb * 16384 + off_q(item & 1), m.q, 64 * kb, h, row0, bar);
     }
 }
 
@@ -418,8 +436,8 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // 2^(G - G_m), Qp = Q*2^(G - G_m) and Km = K*2^(G_m - G) become fp16 in place
 // over the bf16 tiles (rows past the chunk zero).  Returns false if a wait ran
 // out.
-template <class F>
-__device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r, F &&released)
+template <class F, class V>
+__device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r, F &&released, V &&before_kq)
 {
     const int lane = et & 31;
     const uint32_t st = s * kStageBytes;
@@ -462,6 +480,7 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
     }
     if (et < kChunk) cst[256 + et] = beta_r;
     named_bar(kBarE, kEThreads);
+    if (!before_kq()) return false;
     // k and q of this chunk have landed -- so the chain is past its MMA1 of chunk
     // item-2 and no longer reads that chunk's fm or pend slot -- and Km of chunk
     // item-2 is no longer read
@@ -477,9 +496,9 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
     }
     if (et == 0) KDA_PHASE(0, item, 10);
     const float2 gm = *reinterpret_cast<const float2 *>(gmx + c0);
-    uint8_t *kt = sm.base + st + kOffKQ + chh * 16384;   // this channel half's 64-channel block
-    uint8_t *qt = kt + 8192;
-    uint8_t *kmt = sm.base + st + kOffKM + chh * 8192;
+    uint8_t *kt = sm.base + st + kOffKQ + chh * 16384 + off_k(s);   // this channel half's 64-channel block
+    uint8_t *qt = sm.base + st + kOffKQ + chh * 16384 + off_q(s);
+    uint8_t *kmt = sm.base + st + off_km(s) + chh * 8192;
     const int jk = lane >> 2;                            // 16-byte chunk of channel c0 in the row
     const uint32_t cb = 4 * (lane & 3);                  // byte of channel c0 in that chunk
 #pragma unroll 1
@@ -539,8 +558,8 @@ __device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
     for (int ks = 0; ks < 8; ks++) {
         const int kb = ks >> 2, kin = ks & 3;
         const uint64_t ad = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(st + kOffKM + kb * 8192 + kin * 32, 16, 1024);
-        mma_ss(tmem + kTmP + 128 * s + 64, ad, bd, id, ks > 0);
+        const uint64_t bd = smem_desc_sw128(st + off_km(s) + kb * 8192 + kin * 32, 16, 1024);
+        mma_ss(tmem + tm_o(s), ad, bd, id, ks > 0);
     }
 }
 
@@ -619,7 +638,17 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                     beta_next = load_beta(p, ahead, et);
                 }
             };
-            if (!e_pass(sm, s, item, L, et, beta_r, next_g)) {
+            // beta*V as soon as v has landed (the betas are in place after the scan):
+            // before the wait for k and q, so that MMA-b never waits for it
+            auto convert_v = [&]() -> bool {
+                const bool okv = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
+                if (role_any(!okv, kBarE, kEThreads)) return false;
+                e_convert_v(sm, s, L, et);
+                fence_proxy_async_smem();
+                mbar_arrive(sm.bar(kBarEDone + s));
+                return true;
+            };
+            if (!e_pass(sm, s, item, L, et, beta_r, next_g, convert_v)) {
                 if (et == 0) record_error(p, sm, kErrWaitTimeout);
                 return;
             }
@@ -637,14 +666,6 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                 KDA_PHASE(2, item, 2);
             }
             if (et == 0) publish();
-            if (et == 0) KDA_PHASE(2, item, 6);
-            ok = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
-            if (et == 0) KDA_PHASE(2, item, 4);
-            if (role_any(!ok, kBarE, kEThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            if (et == 0) KDA_PHASE(2, item, 5);
-            e_convert_v(sm, s, L, et);
-            fence_proxy_async_smem();
-            mbar_arrive(sm.bar(kBarEDone + s));            // every operand of this chunk is written
             if (et == 0) KDA_PHASE(0, item, 4);
         }
     }
@@ -684,41 +705,53 @@ __device__ __forceinline__ void solve_column16(const float *Lb, int c, float (&x
     }
 }
 
-// A readout.  Warps 10-11 (A_qk rows r): lower part, diagonal included -> B
-// (fp16 [r][i]).  Warps 8-9 (A_kk rows i; beta_i is folded into Kp, so this
-// already is the beta-scaled A_kk): the strictly lower part goes to the L
-// blocks; the 16x16 diagonal blocks are inverted column by column into D0/D1
-// and, as fp16, into T16.
+// A readout (A in TMEM: lane = row of [Kp ; Qp], stage 1 [Qp ; Kp]).  The two
+// A_qk warps (query rows r): the lower part, diagonal included, goes to the
+// MMA3 operand tril(A_qk)^T [i][r] (fp16, each 8 x 8 block stored transposed).
+// The two A_kk warps (rows i; beta_i is folded into Kp, so this already is the
+// beta-scaled A_kk): the strictly lower part goes to the L blocks; the 16x16
+// diagonal blocks are inverted column by column into D0/D1 and, as fp16, into
+// T16.
 __device__ void i_read_a(const Smem &sm, int s, uint32_t tmem, int it, int item)
 {
     const int ew = it >> 5, lane = it & 31;
-    uint32_t a[64];
-    const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * ew) << 16);
-    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(a));
-    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-    tmem_wait_ld();
-    if (ew >= 2) {
-        const int r = 32 * (ew - 2) + lane;
-        uint8_t *Bt = sm.base + s * kStageBytes + kOffB;
+    const int hw = ew & 1;                        // which 32 rows of A_kk or A_qk
+    const uint32_t src = tmem + tm_o(s) + ((uint32_t)(32 * ew) << 16);
+    if ((ew >= 2) != (s == 1)) {                  // A_qk: lanes 64-127 in stage 0, 0-63 in stage 1
+        const uint32_t bt = sm.u32(s * kStageBytes + off_bq(s));
+        const int mi = lane >> 3, k8 = lane & 7;  // this thread's stored matrix and row
+#pragma unroll 1
+        for (int hl = 0; hl < 2; hl++) {
+            uint32_t f[4][8];                     // [16-column block][fragment]
 #pragma unroll
-        for (int q = 0; q < 8; q++) {
-            uint32_t w[4];
+            for (int cb = 0; cb < 4; cb++) tmem_ld16x256_x2(src + ((uint32_t)(16 * hl) << 16) + 16 * cb, f[cb]);
+            tmem_wait_ld();
+            const int r0 = 32 * hw + 16 * hl + (lane >> 2);              // query rows of the fragments: r0, r0 + 8
+            const int rs = 32 * hw + 16 * hl + ((mi & 1) ? 8 : 0);       // first query row of the stored block
 #pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int i0 = 8 * q + 2 * e;
-                const float x0 = (i0 <= r) ? __uint_as_float(a[i0]) : 0.f;
-                const float x1 = (i0 + 1 <= r) ? __uint_as_float(a[i0 + 1]) : 0.f;
-                w[e] = pack_f16x2(x0, x1);
+            for (int cb = 0; cb < 4; cb++) {
+                float x[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const int r = r0 + ((j & 2) ? 8 : 0), i = 16 * cb + 8 * (j >> 2) + 2 * (lane & 3) + (j & 1);
+                    x[j] = i <= r ? __uint_as_float(f[cb][j]) : 0.f;
+                }
+                const int row = 16 * cb + ((mi & 2) ? 8 : 0) + k8;           // key row i of the stored block
+                stmatrix_x4_trans(bt + sw128_chunk(row, rs >> 3), pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]),
+                                  pack_f16x2(x[4], x[5]), pack_f16x2(x[6], x[7]));
             }
-            *reinterpret_cast<uint4 *>(Bt + sw128_chunk(r, q)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         return;
     }
-    const int i = 32 * ew + lane, blk = i >> 4, a16 = i & 15;
+    uint32_t a[64];
+    tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(a));
+    tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+    tmem_wait_ld();
+    const int i = 32 * hw + lane, blk = i >> 4, a16 = i & 15;
     auto lval = [&](int j) { return (j < i) ? __uint_as_float(a[j]) : 0.f; };
     float *W = sm.ptr<float>(kOffTmp);
     float *Ld = sm.ptr<float>(kOffP) + blk * 320 + a16 * 20;
-    if (ew == 0) {
+    if (hw == 0) {
 #pragma unroll
         for (int q = 0; q < 4; q++)
             *reinterpret_cast<float4 *>(Ld + 4 * q) =
@@ -751,17 +784,17 @@ __device__ void i_read_a(const Smem &sm, int s, uint32_t tmem, int it, int item)
     __syncwarp();
     if (it == 0) KDA_PHASE(0, item, 12);
     {   // lane = column c of diagonal block bb (this warp's two blocks)
-        const int c = lane & 15, bb = 2 * ew + (lane >> 4);
+        const int c = lane & 15, bb = 2 * hw + (lane >> 4);
         float x[16];
         solve_column16(sm.ptr<float>(kOffP) + bb * 320, c, x);
-        float *D = W + (ew ? kD1 : kD0) + (lane >> 4) * (16 * 36 + 16);
+        float *D = W + (hw ? kD1 : kD0) + (lane >> 4) * (16 * 36 + 16);
 #pragma unroll
         for (int r = 0; r < 16; r++) D[r * 36 + c] = x[r];
     }
     __syncwarp();
     if (it == 0) KDA_PHASE(0, item, 13);
     {   // row i of its diagonal block -> fp16 T16 (two 16-byte chunks)
-        const float *Dr = W + (ew ? kD1 : kD0) + lane * 36 + (lane >> 4) * 16;
+        const float *Dr = W + (hw ? kD1 : kD0) + lane * 36 + (lane >> 4) * 16;
         uint32_t h[8];
 #pragma unroll
         for (int q = 0; q < 4; q++) {
@@ -861,10 +894,10 @@ __device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
 #pragma unroll 1
     for (int ks = 0; ks < 4; ks++) {
         const uint64_t bd = smem_desc_sw128(sm.u32(kOffT16) + ks * 32, 16, 1024);
-        const uint64_t aw = smem_desc_sw128(st + kOffKQ + ks * 2048, 16384, 1024);   // Kp^T, MN-major
-        const uint64_t au = smem_desc_sw128(st + kOffV + ks * 2048, 8192, 1024);     // V^T, MN-major
-        mma_ss(tmem + kTmP + 128 * s + 64, aw, bd, id, ks > 0);
-        mma_ss(tmem + kTmP + 128 * s, au, bd, id, ks > 0);
+        const uint64_t aw = smem_desc_sw128(st + kOffKQ + off_k(s) + ks * 2048, 16384, 1024);   // Kp^T, MN-major
+        const uint64_t au = smem_desc_sw128(st + kOffV + ks * 2048, 8192, 1024);                // V^T, MN-major
+        mma_ss(tmem + tm_o(s), aw, bd, id, ks > 0);
+        mma_ss(tmem + tm_d(s), au, bd, id, ks > 0);
     }
 }
 
@@ -877,8 +910,8 @@ __device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
 {
     const int iw = it >> 5, lane = it & 31;
     const int mi = lane >> 3, k8 = lane & 7;              // this thread's stored matrix and row
-    const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * iw) << 16);
-    const uint32_t kq = sm.u32(s * kStageBytes + kOffKQ);
+    const uint32_t src = tmem + tm_o(s) + ((uint32_t)(32 * iw) << 16);
+    const uint32_t kq = sm.u32(s * kStageBytes + kOffKQ + off_k(s));
 #pragma unroll 1
     for (int hl = 0; hl < 2; hl++) {
         uint32_t f[4][8];                                 // [16-column block][fragment]
@@ -932,11 +965,9 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const uint32_t ph = (item >> 1) & 1;
-            // MMA-a done implies group E's operand pass is over; MMA-b of the previous
-            // chunk must be done before T16 is rewritten
+            // MMA-a done implies group E's operand pass is over (MMA-b of the previous
+            // chunk, the last reader of T16, was waited for below)
             bool ok = mbar_wait(sm.bar(kBarAFull + s), ph, sm.abort_flag());
-            if (ok && item >= 1)
-                ok = mbar_wait(sm.bar(kBarPrepDone + ((item - 1) & 1)), ((item - 1) >> 1) & 1, sm.abort_flag());
             if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (it == 0) KDA_PHASE(0, item, 5);
             tc_fence_after();
@@ -956,11 +987,20 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
                     KDA_PHASE(0, item, 7);
                     tc_fence_after();
                     issue_mma_b(sm, s, tmem);
-                    mma_commit(sm.bar(kBarPrepDone + s));     // the chain takes W' from here
+                    mma_commit(sm.bar(kBarPrepDone + s));
                     KDA_PHASE(0, item, 8);
-                    KDA_PHASE(0, item, 9);
                 }
             }
+            // -W' out of TMEM into the K rows of the stage (and the output columns
+            // zeroed) for the chain's MMA1
+            ok = mbar_wait(sm.bar(kBarPrepDone + s), ph, sm.abort_flag());
+            if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            tc_fence_after();
+            i_read_w(sm, s, tmem, it);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(sm.bar(kBarWReady + s));
+            if (it == 0) KDA_PHASE(0, item, 9);
         }
     }
 }
@@ -969,17 +1009,20 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
 // chain role: warps 0-3 (thread v owns TMEM lane v = value channel v)
 // =============================================================================
 // O^T (TMEM, lane v, column r) -> out[row0 + r][h][v] (bf16), rows r < L.
-// TMEM is read in the warp-MMA fragment layout (16x256b), and stmatrix.trans
-// writes each 8 x 8 block transposed into the output buffer (32 rows at a time,
-// rows padded to 272 bytes so the 8 rows of a block fall in distinct banks);
-// the global stores are then 16-byte row pieces.  TMEM P_s may be reused
-// (o_done) as soon as every lane has read it.
-__device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem, int s, int row0, int L, int h,
-                                int v, int item)
+// TMEM is read in the warp-MMA fragment layout (16x256b) and stmatrix.trans
+// writes each 8 x 8 block transposed into two 128B-swizzled tiles of 32 rows:
+// rows 0-31 into the stage's tril(A_qk) buffer (MMA3 is done with it), rows
+// 32-63 into the output buffer.  The first thread stores each full tile with
+// one bulk tensor copy; the rows r < L of a partial tile are stored by every
+// thread, 16 bytes at a time.  The first thread later waits until the copies
+// have read the tiles and only then hands TMEM P_s and the tril(A_qk) buffer
+// back to the prep (o_done).
+__device__ void chain_store_out(const TcParams &p, const Smem &sm, const Maps &maps, uint32_t tmem, int s, int row0,
+                                int L, int h, int v, int item)
 {
     const int w = v >> 5, lane = v & 31;
     uint32_t o[2][4][8];                                  // [16-lane half][16-column block][fragment]
-    const uint32_t src = tmem + kTmP + 128 * s + 64 + ((uint32_t)(32 * w) << 16);
+    const uint32_t src = tmem + tm_o(s) + ((uint32_t)(32 * w) << 16);
 #pragma unroll
     for (int hl = 0; hl < 2; hl++)
 #pragma unroll
@@ -987,40 +1030,39 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, uint32_t tmem
     tmem_wait_ld();
     tc_fence_before();
     if (v == 0) KDA_PHASE(1, item, 8);
-    const uint32_t ot = sm.u32(kOffOT);
+    const uint32_t tile0 = sm.u32(s * kStageBytes + off_bq(s)), tile1 = sm.u32(kOffOT);
     const int mi = lane >> 3, k8 = lane & 7;              // this thread's stored matrix and row
-    const size_t row_stride = (size_t)p.H * kD;
-    __nv_bfloat16 *dst = p.out + ((size_t)row0 * p.H + h) * kD;
 #pragma unroll
-    for (int half = 0; half < 2; half++) {                // output rows 32*half .. +31
+    for (int cb = 0; cb < 4; cb++) {                      // output rows 16*cb .. +15
 #pragma unroll
-        for (int c2 = 0; c2 < 2; c2++) {
-            const int cb = 2 * half + c2;
-#pragma unroll
-            for (int hl = 0; hl < 2; hl++) {
-                const uint32_t *f = o[hl][cb];
-                const int rl = 16 * c2 + ((mi & 2) ? 8 : 0) + k8;          // row within the buffer
-                const int vc = 32 * w + 16 * hl + ((mi & 1) ? 8 : 0);      // first value channel
-                stmatrix_x4_trans(ot + rl * kOTRow + 2 * vc,
-                                  pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1])),
-                                  pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3])),
-                                  pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5])),
-                                  pack_bf16x2(__uint_as_float(f[6]), __uint_as_float(f[7])));
-            }
+        for (int hl = 0; hl < 2; hl++) {
+            const uint32_t *f = o[hl][cb];
+            const int rl = 16 * (cb & 1) + ((mi & 2) ? 8 : 0) + k8;      // row within the tile
+            const int vc = 32 * w + 16 * hl + ((mi & 1) ? 8 : 0);      // first value channel
+            stmatrix_x4_trans((cb < 2 ? tile0 : tile1) + (vc >> 6) * 4096 + sw128_chunk(rl, (vc & 63) >> 3),
+                              pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1])),
+                              pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3])),
+                              pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5])),
+                              pack_bf16x2(__uint_as_float(f[6]), __uint_as_float(f[7])));
         }
-        named_bar(kBarChain, kChainThreads);
-        if (half == 0 && v == 0) mbar_arrive(sm.bar(kBarODone + s));   // every lane has read TMEM P_s
-        const uint8_t *ob = sm.base + kOffOT;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int idx = v + 128 * k, r = idx >> 4, q = idx & 15;
-            if (32 * half + r < L)
-                *reinterpret_cast<uint4 *>(dst + (size_t)(32 * half + r) * row_stride + 8 * q) =
-                    *reinterpret_cast<const uint4 *>(ob + r * kOTRow + 16 * q);
+    }
+    fence_proxy_async_smem();
+    named_bar(kBarChain, kChainThreads);
+    if (v == 0) {
+        if (L >= 32) tma_store_4d(maps.o, 0, row0, 0, h, tile0);
+        if (L == kChunk) tma_store_4d(maps.o, 0, row0 + 32, 0, h, tile1);
+        bulk_commit();
+    }
+    if (L < kChunk) {                                     // the partial tile, row by row
+        const int half = L < 32 ? 0 : 1, nr = L - 32 * half;
+        const uint8_t *tb = sm.base + (half ? kOffOT : s * kStageBytes + off_bq(s));
+        const size_t row_stride = (size_t)p.H * kD;
+        __nv_bfloat16 *dst = p.out + ((size_t)(row0 + 32 * half) * p.H + h) * kD;
+        for (int idx = v; idx < nr * 16; idx += kChainThreads) {
+            const int r = idx >> 4, q = idx & 15;
+            *reinterpret_cast<uint4 *>(dst + (size_t)r * row_stride + 8 * q) =
+                *reinterpret_cast<const uint4 *>(tb + (q >> 3) * 4096 + sw128_chunk(r, q & 7));
         }
-        // the buffer is free again before the next half; the next chunk's rows are
-        // stored only after several more chain barriers
-        if (half == 0) named_bar(kBarChain, kChainThreads);
     }
     if (v == 0) KDA_PHASE(1, item, 9);
 }
@@ -1067,6 +1109,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
 {
     int item = 0;
     bool kq_pending = false;  // thread 0: chunk cur.item-1's v is requested, its k and q not yet
+    int o_pending = -1;       // thread 0: stage whose output copies may still read their tiles
     for (int k = 0;; k++) {
         const int u = cta_unit<kSort>(sm, k, U);
         if (u < 0) break;
@@ -1120,15 +1163,17 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             chain_scale_state(tmem, lane_off, sm.ptr<float>(kOffConst + s * kConstBytes),
                               c > 0 ? sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128 : nullptr, item);
             if (v == 0) KDA_PHASE(1, item, 6);
+            if (v == 0 && o_pending >= 0) {
+                // the previous chunk's output copies have read their tiles (long since)
+                bulk_wait_read0();
+                mbar_arrive(sm.bar(kBarODone + o_pending));
+                o_pending = -1;
+            }
             tc_fence_before();
-            ok = mbar_wait(sm.bar(kBarPrepDone + s), ph, sm.abort_flag());
+            // group I has put -W' into the stage (so MMA-b is done) -- and the
+            // barrier orders every lane's S'h stores before MMA1
+            ok = mbar_wait(sm.bar(kBarWReady + s), ph, sm.abort_flag());
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
-            // -W' out of TMEM into the K rows of the stage (and the output columns zeroed)
-            tc_fence_after();
-            i_read_w(sm, s, tmem, v);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar(kBarChain, kChainThreads);
             if (v == 0) {
                 KDA_PHASE(1, item, 11);
                 // MMA-b is done with V: chunk item+2's v may land
@@ -1140,13 +1185,14 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 tc_fence_after();
                 const uint32_t st = sm.u32(s * kStageBytes);
                 // [U^T | 0] += S'^T [-W' ; Qp]^T: the Delta half and the output half in
-                // one N = 128 MMA (the K rows of each stage block hold -W', the Q rows Qp)
+                // one N = 128 MMA (the K rows of each stage block hold -W', the Q rows
+                // Qp; in stage 1 Q rows first, output half first)
                 const uint32_t id1 = idesc_f16(128, 128, 0, 0);
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ks++) {
                     const int kb = ks >> 2, kin = ks & 3;
                     const uint64_t bwq = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
-                    mma_ts(tmem + kTmP + 128 * s, tmem + kTmS0h + 8 * ks, bwq, id1, 1);
+                    mma_ts(tmem + (s ? tm_o(1) : tm_d(0)), tmem + kTmS0h + 8 * ks, bwq, id1, 1);
                 }
                 mma_commit(sm.bar(kBarMma1));
                 KDA_PHASE(1, item, 1);
@@ -1164,8 +1210,8 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             // Delta^T (fp32, TMEM) -> fp16 A operand
             {
                 uint32_t x[64];
-                tmem_ld32(tmem + kTmP + 128 * s + lane_off, *reinterpret_cast<uint32_t(*)[32]>(x));
-                tmem_ld32(tmem + kTmP + 128 * s + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+                tmem_ld32(tmem + tm_d(s) + lane_off, *reinterpret_cast<uint32_t(*)[32]>(x));
+                tmem_ld32(tmem + tm_d(s) + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
                 tmem_wait_ld();
                 uint32_t h0[16], h1[16];
 #pragma unroll
@@ -1183,17 +1229,14 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             if (v == 0) {
                 tc_fence_after();
                 const uint32_t st = sm.u32(s * kStageBytes);
-                const uint32_t id_s = idesc_f16(128, 128, 0, 1), id_o = idesc_f16(128, 64, 0, 0);
-                // state update first, then the rest of the output
+                // the state update and the rest of the output in one N = 192 MMA:
+                // [O^T | S^T] += Delta^T [tril(A_qk)^T | Km] in stage 0,
+                // [S^T | O^T] += Delta^T [Km | tril(A_qk)^T] in stage 1 (B MN-major)
+                const uint32_t id3 = idesc_f16(128, 192, 0, 1);
 #pragma unroll 1
                 for (int ks = 0; ks < 4; ks++) {
-                    const uint64_t bk = smem_desc_sw128(st + kOffKM + ks * 2048, 8192, 1024);   // Km, MN-major
-                    mma_ts(tmem + kTmS, tmem + kTmDh + 8 * ks, bk, id_s, 1);
-                }
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ks++) {
-                    const uint64_t bb = smem_desc_sw128(st + kOffB + ks * 32, 16, 1024);
-                    mma_ts(tmem + kTmP + 128 * s + 64, tmem + kTmDh + 8 * ks, bb, id_o, 1);
+                    const uint64_t b3 = smem_desc_sw128(st + kOffMma3 + ks * 2048, 8192, 1024);
+                    mma_ts(tmem + (s ? kTmS : tm_o(0)), tmem + kTmDh + 8 * ks, b3, id3, 1);
                 }
                 mma_commit(sm.bar(kBarMma3));
                 KDA_PHASE(1, item, 13);
@@ -1207,7 +1250,8 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 mbar_arrive(sm.bar(kBarKmFree + s));
             }
             tc_fence_after();
-            chain_store_out(p, sm, tmem, s, row0, L, un.h, v, item);
+            chain_store_out(p, sm, maps, tmem, s, row0, L, un.h, v, item);
+            if (v == 0) o_pending = s;
             if (v == 0) KDA_PHASE(1, item, 5);
         }
 #ifdef KDA_TRACE
@@ -1250,6 +1294,7 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
     }
     chain_units<kSlots, kSort>(p, sm, order, U, maps, cur, tmem, lane_off, v);
     if (v == 0) {
+        bulk_wait0();   // the output copies are complete
         // copies still in flight land before the CTA exits (normally none: every
         // requested chunk has been consumed)
         for (int back = 1; back <= 2 && cur.item - back >= 0; back++) {
@@ -1264,7 +1309,8 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
 template <bool kSlots, int kSort>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, TcParams p)
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
+              const __grid_constant__ CUtensorMap to, TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem sm;
@@ -1329,6 +1375,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             mbar_init(sm.bar(kBarODone + i), 1);
             mbar_init(sm.bar(kBarFmReady + i), kGroupThreads);
             mbar_init(sm.bar(kBarKmFree + i), 1);
+            mbar_init(sm.bar(kBarWReady + i), kGroupThreads);
         }
         mbar_init(sm.bar(kBarGFull), 1);
         mbar_init(sm.bar(kBarMma1), 1);
@@ -1341,6 +1388,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         tmem_relinquish();
         if ((tid & 31) == 0) {
             tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tg);
+            tma_prefetch_desc(&to);
         }
     }
     tc_fence_before();
@@ -1350,7 +1398,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 #ifdef KDA_TRACE
     if (tid == 0 && blockIdx.x < 1024) g_kda_cta[blockIdx.x][0] = kda_gtimer();
 #endif
-    const Maps maps = {&tq, &tk, &tv, &tg};
+    const Maps maps = {&tq, &tk, &tv, &tg, &to};
     if (warp < 4) {
         chain_role<kSlots, kSort>(p, sm, order, U, maps);
     } else if (warp < 12) {
@@ -1397,16 +1445,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // [T][H][128] viewed as 4-D {c (box_inner wide), row, channel block, head}:
-// one box {box_inner, 64 rows, 128/box_inner blocks, 1} lands as
-// [block][row][c] in shared memory -- the 128B-swizzled tiles, blocks apart.
-bool make_map4(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem, int T, int H, int box_inner)
+// one box {box_inner, box_rows, 128/box_inner blocks, 1} is [block][row][c] in
+// shared memory -- the 128B-swizzled tiles, blocks apart.
+bool make_map4(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem, int T, int H, int box_inner,
+               int box_rows = kChunk)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     const int nblk = kD / box_inner;
     cuuint64_t dims[4] = {(cuuint64_t)box_inner, (cuuint64_t)T, (cuuint64_t)nblk, (cuuint64_t)H};
     cuuint64_t strides[3] = {(cuuint64_t)H * kD * elem, (cuuint64_t)box_inner * elem, (cuuint64_t)kD * elem};
-    cuuint32_t box[4] = {(cuuint32_t)box_inner, (cuuint32_t)kChunk, (cuuint32_t)nblk, 1};
+    cuuint32_t box[4] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, (cuuint32_t)nblk, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1432,13 +1481,15 @@ int tc_max_sorted_seqs() { return kMaxSortedSeqs; }
 
 cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
 {
-    CUtensorMap tq, tk, tv, tg;
+    CUtensorMap tq, tk, tv, tg, to;
     memset(&tq, 0, sizeof tq); memset(&tk, 0, sizeof tk); memset(&tv, 0, sizeof tv); memset(&tg, 0, sizeof tg);
+    memset(&to, 0, sizeof to);
     if (a.T > 0) {
         if (!make_map(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
             !make_map(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
             !make_map4(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64) ||
-            !make_map4(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32))
+            !make_map4(&tg, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.T, a.H, 32) ||
+            !make_map4(&to, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64, 32))
             return cudaErrorInvalidValue;
     }
     // one kernel per (slot table, sort mode): 1 sorted here (N <= kMaxSortedSeqs),
@@ -1447,7 +1498,8 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     const int sort = a.g_order ? 2 : (a.N <= kMaxSortedSeqs ? 1 : 0);
     if (sort != 0 && !a.sched) return cudaErrorInvalidValue;
     const int variant = 3 * (a.state_slots != nullptr) + sort;
-    using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, TcParams);
+    using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                            const CUtensorMap, TcParams);
     static const Kernel kernels[6] = {kda_tc_kernel<false, 0>, kda_tc_kernel<false, 1>, kda_tc_kernel<false, 2>,
                                       kda_tc_kernel<true, 0>,  kda_tc_kernel<true, 1>,  kda_tc_kernel<true, 2>};
     const Kernel kernel = kernels[variant];
@@ -1477,7 +1529,7 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     p.num_slots = a.num_slots;
     const int units = a.N * a.H;
     const int grid = units < a.num_sms ? units : a.num_sms;
-    kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tg, p);
+    kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tg, to, p);
     return cudaGetLastError();
 }
 
