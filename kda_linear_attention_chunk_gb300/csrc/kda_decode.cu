@@ -55,19 +55,20 @@ struct DecodeParams {
 __device__ __forceinline__ float token_step(float4 (&s)[4], const float4 *sa, const float4 *sk, const float4 *sq,
                                             int qe, float vv, float beta)
 {
-    float e = 0.f;
+    float ep[4];                      // four partial sums: short dependent chains
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         const float4 a = sa[8 * j + qe], kk = sk[8 * j + qe];
         s[j].x *= a.x; s[j].y *= a.y; s[j].z *= a.z; s[j].w *= a.w;
-        e = fmaf(s[j].x, kk.x, e); e = fmaf(s[j].y, kk.y, e);
-        e = fmaf(s[j].z, kk.z, e); e = fmaf(s[j].w, kk.w, e);
+        ep[j] = s[j].x * kk.x; ep[j] = fmaf(s[j].y, kk.y, ep[j]);
+        ep[j] = fmaf(s[j].z, kk.z, ep[j]); ep[j] = fmaf(s[j].w, kk.w, ep[j]);
     }
+    float e = (ep[0] + ep[1]) + (ep[2] + ep[3]);
     e += __shfl_xor_sync(0xffffffffu, e, 1);
     e += __shfl_xor_sync(0xffffffffu, e, 2);
     e += __shfl_xor_sync(0xffffffffu, e, 4);
     const float u = beta * (vv - e);
-    float o = 0.f;
+    float op[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         const float4 kk = sk[8 * j + qe];
@@ -75,11 +76,13 @@ __device__ __forceinline__ float token_step(float4 (&s)[4], const float4 *sa, co
         s[j].z = fmaf(kk.z, u, s[j].z); s[j].w = fmaf(kk.w, u, s[j].w);
         if (sq) {
             const float4 qq = sq[8 * j + qe];
-            o = fmaf(s[j].x, qq.x, o); o = fmaf(s[j].y, qq.y, o);
-            o = fmaf(s[j].z, qq.z, o); o = fmaf(s[j].w, qq.w, o);
+            op[j] = s[j].x * qq.x; op[j] = fmaf(s[j].y, qq.y, op[j]);
+            op[j] = fmaf(s[j].z, qq.z, op[j]); op[j] = fmaf(s[j].w, qq.w, op[j]);
         }
     }
+    float o = 0.f;
     if (sq) {
+        o = (op[0] + op[1]) + (op[2] + op[3]);
         o += __shfl_xor_sync(0xffffffffu, o, 1);
         o += __shfl_xor_sync(0xffffffffu, o, 2);
         o += __shfl_xor_sync(0xffffffffu, o, 4);
@@ -100,7 +103,7 @@ __device__ __forceinline__ int decode_slot(const int32_t *slots, int n, int num_
     return slot;
 }
 
-__global__ void __launch_bounds__(kDecThreads, 4) kda_decode_kernel(DecodeParams p)
+__global__ void __launch_bounds__(kDecThreads, 5) kda_decode_kernel(DecodeParams p)
 {
     __shared__ float4 sa[32], sk[32], sq[32];   // exp(g), k, q of this (sequence, head), 128 each
     const int rh = blockIdx.x >> 2, vq = blockIdx.x & 3;   // (sequence, head), quarter of the value rows
@@ -148,7 +151,7 @@ struct FoldParams {
 // steps themselves wait on no memory.
 constexpr int kFoldBatch = 16;
 
-__global__ void __launch_bounds__(kDecThreads, 4) kda_fold_kernel(FoldParams p)
+__global__ void __launch_bounds__(kDecThreads, 5) kda_fold_kernel(FoldParams p)
 {
     __shared__ float4 sa[kFoldBatch][32], sk[kFoldBatch][32];
     __shared__ float sv[kFoldBatch][128], sb[kFoldBatch];
