@@ -52,6 +52,7 @@ def peaks():
 # the sources a kernel is compiled from (its launcher included)
 KERNEL_SOURCES = ("kda_common.cuh", "kda_internal.h", "kda_sm100.cuh", "kda_tc.cu")
 DECODE_SOURCES = ("kda_common.cuh", "kda_decode.h", "kda_decode.cu")
+CONV_SOURCES = ("kda_common.cuh", "kda_conv.h", "kda_conv.cu")
 
 
 def code_only(text: str) -> str:
@@ -203,6 +204,64 @@ def measure_decode(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "algorithmic_bytes_per_launch": alg,
                          "traffic": recorded_traffic("decode64_h32", DECODE_SOURCES)}}
+
+
+def conv_bytes(lengths, h: int) -> int:
+    """Algorithmic bytes of one short-conv prologue call: per row-head the q, k,
+    v projections in and q, k, v out (256 B each); the filters (3 x H x 128 x 4
+    fp32); per sequence with rows its window entry read and written (3 taps x
+    3 streams x H x 128 bf16 each way); cu_seqlens and the slot table."""
+    t = int(sum(lengths))
+    live = sum(1 for n in lengths if n > 0)
+    n = len(lengths)
+    return t * h * 6 * 256 + 3 * h * 128 * 4 * 4 + live * 2 * 9 * h * 128 * 2 + 4 * (2 * n + 1)
+
+
+def measure_conv(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
+    """kda_short_conv (SiLU) on the packed 8192-row workload's lengths at H = 32:
+    two rotating input sets (each call moves 403 MB, above L2), windows in a
+    pool of 2 x 16 entries, the calls alternating between its halves."""
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+    n_heads = 32
+    lengths = list(syn.workloads()[WORKLOAD].lengths)
+    rng = np.random.default_rng(79)
+    t_rows = int(sum(lengths))
+    sets = []
+    for _ in range(2):
+        xs = [torch.from_numpy((rng.standard_normal((t_rows, n_heads, 128))).astype(np.float32)).to(torch.bfloat16).cuda()
+              for _ in range(3)]
+        outs = tuple(torch.empty_like(xs[0]) for _ in range(3))
+        sets.append((xs, outs))
+    w = torch.from_numpy((0.5 * rng.standard_normal((3, n_heads * 128, 4))).astype(np.float32)).cuda()
+    n = len(lengths)
+    pool = torch.zeros((2 * n, 3, 3, n_heads * 128), dtype=torch.bfloat16, device="cuda")
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)).cuda()
+    tables = [torch.arange(0, n, dtype=torch.int32, device="cuda"), torch.arange(n, 2 * n, dtype=torch.int32, device="cuda")]
+
+    def step(i):
+        xs, outs = sets[i % 2]
+        kda.short_conv(xs[0], xs[1], xs[2], w, cu, pool, conv_slots=tables[(i // 2) % 2], activation="silu",
+                       out=outs, stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    alg = conv_bytes(lengths, n_heads)
+    peak, _ = peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    return {"workload": "conv_packed16_8192_h32", "kernel": "kda_conv_kernel + kda_conv_window_kernel",
+            "T": t_rows, "N": n, "H": n_heads, "activation": "silu", "steps": steps, "us_per_call": ms * 1e3,
+            "tokens_per_s": t_rows / (ms / 1e3), "l2": "2 rotating input sets of 201 MB (projections) each",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": alg,
+                         "traffic": recorded_traffic("conv_packed16_8192_h32", CONV_SOURCES)}}
 
 
 FOLD_W = 8   # speculative window: 8 draft tokens a sequence
@@ -432,6 +491,7 @@ def run_gpu_arm(args):
     clocks = summarize_clocks(sampler.stop())
     decode = measure_decode(torch, np, kda, stream) if not args.no_decode else None
     fold = measure_fold(torch, np, kda, stream) if not args.no_decode else None
+    conv = measure_conv(torch, np, kda, stream) if not args.no_decode else None
     configs = measure_configs(torch, np, kda, stream) if not args.no_configs else None
     assert kda.device_error() == 0, "device error word set during the bench"
 
@@ -469,6 +529,8 @@ def run_gpu_arm(args):
         line["decode"] = decode
     if fold is not None:
         line["fold"] = fold
+    if conv is not None:
+        line["conv"] = conv
     if configs is not None:
         line["configs"] = configs
     if not args.no_cpu_baseline:
@@ -548,7 +610,8 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=32)
     ap.add_argument("--ref-heads", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step and fold measurements")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-step, fold and short-conv measurements")
     ap.add_argument("--no-configs", action="store_true", help="skip the other four workloads")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -230,6 +230,54 @@ int kda_fold_commit(const uint16_t *k, const uint16_t *v, const float *g, const 
                     const int32_t *accepted, const int32_t *state_slots, float *state_pool,
                     int num_slots, int N, int W, int H, int dk, int dv, void *stream);
 
+/*
+ * kda_short_conv -- the short-conv + L2-norm prologue that turns a KDA layer's
+ * q, k, v projections into the kernel's q, k, v, with each sequence's conv
+ * window carried across calls (kern-k3-pp-prefill README: section "P: the
+ * packed prefill" runs the KDA layers with per-sequence conv windows and
+ * states; section "D inside SGLang" keeps the window in the engine's pool laid
+ * out [slot][tap][q | k | v] bf16, indexed by the same slot ids as the state).
+ * For sequence n (rows t = 0 .. L-1 from cu_seqlens[n]), stream s in {q, k, v}
+ * and channel c (flat over the H heads of d channels):
+ *
+ *     x_{-3}, x_{-2}, x_{-1}   the window's taps 0, 1, 2 (oldest first)
+ *     y_t[c] = sum_{j=0..3} conv_weight[s][c][j] * x_{t-3+j}[c]
+ *     y_t    = y_t, or SiLU(y_t) = y_t / (1 + exp(-y_t)) with activation 1
+ *     q_t = y_t / sqrt(|y_t|^2 + eps) over each head's d channels; k_t likewise;
+ *     v_t = y_t
+ *
+ * after which the window holds the last three rows of [old taps ; the L rows].
+ * The pages fix the window layout; the kernel size (four taps: the three
+ * carried rows and the row itself) is read off the window, and the weights,
+ * the activation and eps are the caller's.
+ *
+ *   xq, xk, xv   bf16 bits [T][H][d], the projections of the packed rows.
+ *   conv_weight  fp32 [3][H*d][4]: stream (q, k, v), channel, tap; tap 3
+ *                weighs the row itself.
+ *   cu_seqlens   int32 [N+1], as for kda_chunk_prefill.
+ *   conv_slots   int32 [N], device memory, or NULL for entry n: the pool entry
+ *                of sequence n.  -1 marks a padded sequence: its rows of the
+ *                outputs are not written and its entry is not touched.  An id
+ *                outside [-1, num_slots) is treated like -1 and sets bit 8 of
+ *                the device error word.  Valid ids must be distinct.
+ *   conv_pool    bf16 bits [num_slots][3 taps][3 streams][H*d], updated in
+ *                place; a sequence of zero rows leaves its entry as it was.
+ *   q_out, k_out, v_out  bf16 bits [T][H][d] (rows of no sequence and of
+ *                padded sequences are not written).
+ *   activation   0 (none) or 1 (SiLU); eps >= 0 (an all-zero row with eps 0
+ *                gives NaN, as the formula does).
+ *   N >= 1, T >= 0, H >= 1; d = 128.
+ * Tensor pointers must be 16-byte aligned (cu_seqlens and conv_slots 4-byte).
+ * The outputs must not overlap an input, the pool or each other; the pool must
+ * not overlap an input.  Two kernels run on `stream`: the conv (which reads
+ * the old windows), then the window update.  Returns a kda_status.
+ */
+int kda_short_conv(const uint16_t *xq, const uint16_t *xk, const uint16_t *xv,
+                   const float *conv_weight, const int32_t *cu_seqlens,
+                   const int32_t *conv_slots, uint16_t *conv_pool, int num_slots,
+                   uint16_t *q_out, uint16_t *k_out, uint16_t *v_out, int N, int T, int H, int d,
+                   int activation, float eps, void *stream);
+
 /* Human-readable name of a kda_status value (static string, never NULL). */
 const char *kda_status_string(int status);
 

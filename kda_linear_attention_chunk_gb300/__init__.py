@@ -20,7 +20,8 @@ KDA_ERR_NOALLOC_LIMIT = 8
 KDA_NOALLOC_MAX_SEQS = 16384
 
 EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error",
-            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode", "kda_fold_commit")
+            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode", "kda_fold_commit",
+            "kda_short_conv")
 ERR_BAD_SLOT = 8   # device error word bit: a state slot id outside [-1, num_slots)
 ERR_BAD_ACCEPTED = 16   # device error word bit: an accepted count outside [0, window]
 
@@ -53,6 +54,8 @@ def load(path: str = LIB_PATH):
     lib.kda_decode.restype = I
     lib.kda_fold_commit.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
     lib.kda_fold_commit.restype = I
+    lib.kda_short_conv.argtypes = [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, ctypes.c_float, P]
+    lib.kda_short_conv.restype = I
     lib.kda_status_string.argtypes = [I]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), I]
@@ -110,6 +113,13 @@ def kda_fold_commit(k, v, g, beta, accepted, state_slots, state_pool, num_slots:
     """Raw C-ABI call: fold the accepted tokens of each window into the pool."""
     return load().kda_fold_commit(k, v, g, beta, accepted, state_slots, state_pool, num_slots, N, W, H, dk, dv,
                                   stream)
+
+
+def kda_short_conv(xq, xk, xv, conv_weight, cu_seqlens, conv_slots, conv_pool, num_slots: int, q_out, k_out,
+                   v_out, N: int, T: int, H: int, d: int, activation: int, eps: float, stream) -> int:
+    """Raw C-ABI call: short conv + L2 norm prologue, conv windows in a slot-addressed pool."""
+    return load().kda_short_conv(xq, xk, xv, conv_weight, cu_seqlens, conv_slots, conv_pool, num_slots, q_out,
+                                 k_out, v_out, N, T, H, d, activation, eps, stream)
 
 
 def device_error(reset: bool = False) -> int:
@@ -265,3 +275,51 @@ def fold_commit(k, v, g, beta, accepted, state_pool, state_slots=None, stream=No
                          _ptr(state_pool), int(state_pool.shape[0]), N, W, H, dk, dv, handle)
     if st != KDA_OK:
         raise KdaError(st, "kda_fold_commit")
+
+
+ACTIVATIONS = {"none": 0, "silu": 1}
+
+
+def short_conv(xq, xk, xv, conv_weight, cu_seqlens, conv_pool, conv_slots=None, activation: str = "silu",
+               eps: float = 1e-6, out=None, stream=None):
+    """Short conv + L2 norm prologue on torch CUDA tensors.
+
+    xq, xk, xv: [T][H][128] bfloat16; conv_weight: [3][H*128][4] float32 (tap
+    3 weighs the row itself); cu_seqlens: [N+1] int32; conv_pool:
+    [num_slots][3][3][H*128] bfloat16, updated in place; conv_slots: [N] int32
+    (-1 = padded, skipped) or None for entry n.  activation "none" or "silu".
+    Returns (q, k, v), each [T][H][128] bfloat16 (q and k with unit L2 norm
+    per head).
+    """
+    import torch
+
+    T, H, d = xq.shape
+    N = int(cu_seqlens.shape[0]) - 1
+    tensors = [("xq", xq), ("xk", xk), ("xv", xv), ("conv_weight", conv_weight), ("cu_seqlens", cu_seqlens),
+               ("conv_pool", conv_pool)]
+    if conv_slots is not None:
+        tensors.append(("conv_slots", conv_slots))
+    for name, t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if xq.dtype != torch.bfloat16 or xk.dtype != torch.bfloat16 or xv.dtype != torch.bfloat16:
+        raise ValueError("short_conv takes bfloat16 projections")
+    if conv_weight.dtype != torch.float32 or tuple(conv_weight.shape) != (3, H * d, 4):
+        raise ValueError("conv_weight must be float32 [3][H*d][4]")
+    if conv_pool.dtype != torch.bfloat16 or tuple(conv_pool.shape[1:]) != (3, 3, H * d):
+        raise ValueError("conv_pool must be bfloat16 [num_slots][3][3][H*d]")
+    if conv_slots is not None and (conv_slots.dtype != torch.int32 or tuple(conv_slots.shape) != (N,)):
+        raise ValueError("conv_slots must be int32 [N]")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    if out is None:
+        out = tuple(torch.empty_like(xq) for _ in range(3))
+    q, k, v = out
+    s = stream if stream is not None else torch.cuda.current_stream(xq.device)
+    handle = int(s.cuda_stream) if hasattr(s, "cuda_stream") else int(s)
+    st = kda_short_conv(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(conv_weight), _ptr(cu_seqlens), _ptr(conv_slots),
+                        _ptr(conv_pool), int(conv_pool.shape[0]), _ptr(q), _ptr(k), _ptr(v), N, T, H, d,
+                        ACTIVATIONS[activation], float(eps), handle)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_short_conv")
+    return q, k, v

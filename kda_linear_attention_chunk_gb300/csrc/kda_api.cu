@@ -8,6 +8,7 @@
 #include <atomic>
 
 #include "kda.h"
+#include "kda_conv.h"
 #include "kda_decode.h"
 #include "kda_internal.h"
 
@@ -297,6 +298,61 @@ int kda_fold_commit(const uint16_t *k, const uint16_t *v, const float *g, const 
     a.stream = (cudaStream_t)stream;
     a.err_word = d->err;
     return kda::launch_kda_fold_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_short_conv(const uint16_t *xq, const uint16_t *xk, const uint16_t *xv, const float *conv_weight,
+                   const int32_t *cu_seqlens, const int32_t *conv_slots, uint16_t *conv_pool, int num_slots,
+                   uint16_t *q_out, uint16_t *k_out, uint16_t *v_out, int N, int T, int H, int d,
+                   int activation, float eps, void *stream)
+{
+    if (!cu_seqlens || !conv_weight || !conv_pool) return KDA_ERR_NULL;
+    if (T > 0 && (!xq || !xk || !xv || !q_out || !k_out || !v_out)) return KDA_ERR_NULL;
+    if (N < 1 || T < 0 || H < 1 || d < 1 || num_slots < 1) return KDA_ERR_SHAPE;
+    if (!conv_slots && num_slots < N) return KDA_ERR_SHAPE;
+    if (activation != 0 && activation != 1) return KDA_ERR_SHAPE;
+    if (!(eps >= 0.f && eps <= 3.0e38f)) return KDA_ERR_SHAPE;   // also rejects NaN
+    const size_t rows = (size_t)T * (size_t)H;
+    if (rows * 128 * 2 >= ((size_t)1 << 40) || (size_t)N * (size_t)H > ((size_t)1 << 26) ||
+        (size_t)num_slots * (size_t)H * 128 * 9 * 2 >= ((size_t)1 << 40))
+        return KDA_ERR_SHAPE;
+    if (d != 128) return KDA_ERR_UNSUPPORTED;
+    const void *aligned_ptrs[] = {xq, xk, xv, q_out, k_out, v_out, conv_pool, conv_weight};
+    for (const void *p : aligned_ptrs)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+    if (((uintptr_t)cu_seqlens & 3u) || ((uintptr_t)conv_slots & 3u)) return KDA_ERR_ALIGN;
+    const size_t xbytes = rows * 128 * 2;
+    const Range in[] = {range_of(xq, xbytes), range_of(xk, xbytes), range_of(xv, xbytes),
+                        range_of(conv_weight, (size_t)3 * H * 128 * 4 * sizeof(float)),
+                        range_of(cu_seqlens, (size_t)(N + 1) * sizeof(int32_t)),
+                        range_of(conv_slots, (size_t)N * sizeof(int32_t))};
+    const Range rp = range_of(conv_pool, (size_t)num_slots * 9 * H * 128 * 2);
+    const Range ro[] = {range_of(q_out, xbytes), range_of(k_out, xbytes), range_of(v_out, xbytes)};
+    for (const Range &r : in) {
+        if (overlap(rp, r)) return KDA_ERR_ALIAS;
+        for (const Range &o : ro)
+            if (overlap(o, r)) return KDA_ERR_ALIAS;
+    }
+    for (int i = 0; i < 3; i++) {
+        if (overlap(ro[i], rp)) return KDA_ERR_ALIAS;
+        for (int j = i + 1; j < 3; j++)
+            if (overlap(ro[i], ro[j])) return KDA_ERR_ALIAS;
+    }
+    DevInfo *dv = nullptr;
+    int st;
+    if ((st = device_info(&dv)) != KDA_OK) return st;
+    kda::ConvArgs a;
+    a.x[0] = xq; a.x[1] = xk; a.x[2] = xv;
+    a.y[0] = q_out; a.y[1] = k_out; a.y[2] = v_out;
+    a.weight = conv_weight;
+    a.cu_seqlens = cu_seqlens;
+    a.conv_slots = conv_slots;
+    a.conv_pool = conv_pool;
+    a.N = N; a.T = T; a.H = H; a.num_slots = num_slots;
+    a.activation = activation;
+    a.eps = eps;
+    a.stream = (cudaStream_t)stream;
+    a.err_word = dv->err;
+    return kda::launch_kda_conv_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_device_error(int *word, int reset)

@@ -1,0 +1,233 @@
+// kda_conv.cu -- the short-conv + L2-norm prologue of a KDA layer over packed
+// sequences, with each sequence's conv window carried across calls in a
+// slot-addressed pool (kern-k3-pp-prefill README: section "P: the packed
+// prefill" runs the KDA layers with per-sequence conv windows and states;
+// section "D inside SGLang" keeps the window in the engine's pool, laid out
+// [slot][tap][q | k | v] bf16 and indexed by the same slot ids as the state).
+//
+// For sequence n (rows bos .. eos-1, t counted from bos), stream s in
+// {q, k, v} and channel c (flat over the H heads of 128 channels):
+//     x_{-3}, x_{-2}, x_{-1}  = the window's taps 0, 1, 2 (oldest first)
+//     y_t[c] = sum_{j=0..3} w[s][c][j] x_{t-3+j}[c]   (tap 3 weighs the row itself)
+//     y_t    = act(y_t)                                (identity or SiLU)
+//     q_t, k_t = y_t / sqrt(|y_t|^2 + eps)             (per head, 128 channels)
+//     v_t    = y_t
+// after which the window holds x_{L-3}, x_{L-2}, x_{L-1}: the last three rows
+// of [old taps ; the sequence's L rows].
+//
+// kda_conv_kernel: one warp per (block of 32 rows, head, stream).  Lane l owns
+// channels 4l .. 4l+3 of the head, holds their 16 weights and the three
+// previous rows in registers and keeps the next rows' loads in flight; each
+// row is one 256-byte load and one 256-byte store per warp.  The L2 norm is a
+// warp reduction.  kda_conv_window_kernel then writes the new windows in
+// place; it runs after the first kernel on the same stream, so every read of
+// an old window precedes its rewrite.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kda_common.cuh"
+#include "kda_conv.h"
+
+namespace kda {
+namespace {
+
+constexpr int kConvRows = 32;    // rows per warp
+constexpr int kConvWarps = 4;    // warps per CTA
+constexpr int kConvAhead = 4;    // rows whose loads are in flight ahead of use
+
+struct ConvParams {
+    const uint16_t *x[3];
+    uint16_t *y[3];
+    const float *w;
+    const int32_t *cu, *slots;
+    uint16_t *pool;
+    int N, T, H, num_slots, act;
+    float eps;
+    int *err;
+};
+
+// stream s of a 3-array kept in the kernel parameters (a runtime index would
+// copy the parameter block to local memory)
+template <typename T>
+__device__ __forceinline__ T pick(const T (&a)[3], int s) { return s == 0 ? a[0] : s == 1 ? a[1] : a[2]; }
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi)
+{
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// cu_seqlens[i] clamped into [0, T]
+__device__ __forceinline__ int cu_at(const int32_t *cu, int i, int T) { return min(max(cu[i], 0), T); }
+
+// The last sequence n in [0, N) with cu[n] <= t (cu non-decreasing): a 32-way
+// search, one load per lane and step.
+__device__ int seq_of(const int32_t *cu, int N, int T, int t, int lane)
+{
+    int lo = 0, hi = N;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int idx = lo + lane * step;
+        const unsigned m = __ballot_sync(0xffffffffu, idx < hi && cu_at(cu, idx, T) <= t);
+        lo += (m ? 31 - __clz(m) : 0) * step;
+        hi = min(lo + step, hi);
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kConvWarps * 32, 7) kda_conv_kernel(ConvParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * kConvWarps + (threadIdx.x >> 5);   // ((block * 3 + s) * H + h)
+    const int h = item % p.H, s = (item / p.H) % 3, t0 = (item / p.H / 3) * kConvRows;
+    if (t0 >= p.T) return;
+    const int t1 = min(t0 + kConvRows, p.T);
+    const size_t HC = (size_t)p.H * 128;         // elements per row of a stream
+    const int gc = h * 128 + 4 * lane;            // this lane's first channel
+    float wt[4][4];                               // [channel][tap]
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float4 f = __ldg(reinterpret_cast<const float4 *>(p.w + (s * HC + gc + i) * 4));
+        wt[i][0] = f.x; wt[i][1] = f.y; wt[i][2] = f.z; wt[i][3] = f.w;
+    }
+    const uint16_t *xs = pick(p.x, s);
+    uint16_t *ys = pick(p.y, s);
+    const int tend = cu_at(p.cu, p.N, p.T);       // rows from here on belong to no sequence
+    int n = seq_of(p.cu, p.N, p.T, t0, lane);
+    int bos = cu_at(p.cu, n, p.T), eos = cu_at(p.cu, n + 1, p.T);
+    int t = t0;
+    while (t < t1 && t < tend) {
+        while (t >= eos && n < p.N - 1) {         // the sequence holding row t
+            n++;
+            bos = cu_at(p.cu, n, p.T);
+            eos = cu_at(p.cu, n + 1, p.T);
+        }
+        if (t < bos || t >= eos) {                // malformed cu_seqlens: a row of no sequence
+            t++;
+            continue;
+        }
+        const int seg_end = min(eos, t1);
+        const int slot = p.slots ? p.slots[n] : n;
+        if (slot < 0 || slot >= p.num_slots) {    // padded (or invalid: reported) -- skipped
+            if (slot != -1 && lane == 0) atomicOr(p.err, kErrBadSlot);
+            t = seg_end;
+            continue;
+        }
+        // the three rows before t: earlier rows of the sequence or the window's taps
+        float hist[3][4];
+#pragma unroll
+        for (int j = 0; j < 3; j++) {
+            const int r = t - 3 + j;
+            const uint2 raw = r >= bos ? __ldg(reinterpret_cast<const uint2 *>(xs + (size_t)r * HC + gc))
+                                       : *reinterpret_cast<const uint2 *>(
+                                             p.pool + ((size_t)(slot * 3 + (r - bos + 3)) * 3 + s) * HC + gc);
+            hist[j][0] = bf_lo(raw.x); hist[j][1] = bf_hi(raw.x); hist[j][2] = bf_lo(raw.y); hist[j][3] = bf_hi(raw.y);
+        }
+        const uint16_t *xrow = xs + (size_t)t * HC + gc;     // row r of this lane's channels
+        uint16_t *yrow = ys + (size_t)t * HC + gc;
+        uint2 nxt[kConvAhead];                                 // rows r .. r + kConvAhead - 1
+#pragma unroll
+        for (int i = 0; i < kConvAhead; i++)
+            nxt[i] = t + i < seg_end ? __ldg(reinterpret_cast<const uint2 *>(xrow + i * HC)) : make_uint2(0u, 0u);
+#pragma unroll 1
+        for (int r = t; r < seg_end; r++, xrow += HC, yrow += HC) {
+            const uint2 cur = nxt[0];
+#pragma unroll
+            for (int i = 0; i + 1 < kConvAhead; i++) nxt[i] = nxt[i + 1];
+            nxt[kConvAhead - 1] = r + kConvAhead < seg_end
+                                      ? __ldg(reinterpret_cast<const uint2 *>(xrow + kConvAhead * HC))
+                                      : make_uint2(0u, 0u);
+            const float xv[4] = {bf_lo(cur.x), bf_hi(cur.x), bf_lo(cur.y), bf_hi(cur.y)};
+            float y[4];
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                float a = wt[c][0] * hist[0][c];
+                a = fmaf(wt[c][1], hist[1][c], a);
+                a = fmaf(wt[c][2], hist[2][c], a);
+                a = fmaf(wt[c][3], xv[c], a);
+                y[c] = p.act ? a * __frcp_rn(1.f + __expf(-a)) : a;   // SiLU: a * sigmoid(a)
+            }
+            float scale = 1.f;
+            if (s < 2) {                          // q and k: unit L2 norm per head
+                float ss = y[0] * y[0];
+                ss = fmaf(y[1], y[1], ss);
+                ss = fmaf(y[2], y[2], ss);
+                ss = fmaf(y[3], y[3], ss);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                scale = rsqrtf(ss + p.eps);
+            }
+            *reinterpret_cast<uint2 *>(yrow) =
+                make_uint2(pack_bf2(y[0] * scale, y[1] * scale), pack_bf2(y[2] * scale, y[3] * scale));
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                hist[0][c] = hist[1][c];
+                hist[1][c] = hist[2][c];
+                hist[2][c] = xv[c];
+            }
+        }
+        t = seg_end;
+    }
+}
+
+// New windows: thread = (sequence, stream, 8 channels); the taps are the last
+// three rows of [old taps ; the sequence's rows], all read before any write.
+__global__ void __launch_bounds__(256) kda_conv_window_kernel(ConvParams p)
+{
+    const int pieces = p.H * 16;                  // 8-channel pieces per stream row
+    const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;
+    if (idx >= (long long)p.N * 3 * pieces) return;
+    const int piece = (int)(idx % pieces), s = (int)((idx / pieces) % 3), n = (int)(idx / pieces / 3);
+    const int slot = p.slots ? p.slots[n] : n;
+    if (piece == 0 && s == 0) {
+        if (p.cu[n] < 0 || p.cu[n] > p.T || p.cu[n + 1] < 0 || p.cu[n + 1] > p.T) atomicOr(p.err, kErrBadSeqlens);
+        if (slot < -1 || slot >= p.num_slots) atomicOr(p.err, kErrBadSlot);
+    }
+    if (slot < 0 || slot >= p.num_slots) return;
+    const int bos = cu_at(p.cu, n, p.T), L = cu_at(p.cu, n + 1, p.T) - bos;
+    if (L <= 0) return;                           // no rows: the window stays
+    const size_t HC = (size_t)p.H * 128;
+    const int gc = piece * 8;
+    uint4 tap[3];
+#pragma unroll
+    for (int j = 0; j < 3; j++) {
+        const int r = L - 3 + j;                  // row of the new tap j (negative: an old tap)
+        tap[j] = r >= 0 ? *reinterpret_cast<const uint4 *>(pick(p.x, s) + (size_t)(bos + r) * HC + gc)
+                        : *reinterpret_cast<const uint4 *>(p.pool + ((size_t)(slot * 3 + (r + 3)) * 3 + s) * HC + gc);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; j++) *reinterpret_cast<uint4 *>(p.pool + ((size_t)(slot * 3 + j) * 3 + s) * HC + gc) = tap[j];
+}
+
+}  // namespace
+
+cudaError_t launch_kda_conv_bf16_d128(const ConvArgs &a)
+{
+    ConvParams p;
+    for (int s = 0; s < 3; s++) {
+        p.x[s] = (const uint16_t *)a.x[s];
+        p.y[s] = (uint16_t *)a.y[s];
+    }
+    p.w = a.weight;
+    p.cu = a.cu_seqlens;
+    p.slots = a.conv_slots;
+    p.pool = (uint16_t *)a.conv_pool;
+    p.N = a.N; p.T = a.T; p.H = a.H; p.num_slots = a.num_slots;
+    p.act = a.activation;
+    p.eps = a.eps;
+    p.err = a.err_word;
+    if (a.T > 0) {
+        const long long items = (long long)((a.T + kConvRows - 1) / kConvRows) * 3 * a.H;
+        kda_conv_kernel<<<(unsigned)((items + kConvWarps - 1) / kConvWarps), kConvWarps * 32, 0, a.stream>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const long long threads = (long long)a.N * 3 * a.H * 16;
+    kda_conv_window_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

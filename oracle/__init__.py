@@ -158,3 +158,74 @@ def run_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_pool, out=None, h
     res[rows] = sub_out
     pool[slots[live]] = fin
     return res, pool, bad
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> the exact float64 values they encode."""
+    return (np.asarray(a, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def short_conv(xq, xk, xv, conv_weight, cu_seqlens, conv_pool, conv_slots=None, activation: str = "silu",
+               eps: float = 1e-6):
+    """The short-conv + L2-norm prologue of a KDA layer (kern-k3-pp-prefill
+    README: section "P: the packed prefill" runs the KDA layers with
+    per-sequence conv windows and states; section "D inside SGLang" keeps the
+    window in the engine's pool laid out [slot][tap][q | k | v] bf16, indexed
+    by the same slot ids as the state).
+
+    The pages fix the window layout only.  Readings: the window carries the
+    three rows before a sequence's first row, so the causal conv has four
+    taps; the weights [3][H*D][4] (tap 3 weighs the row itself) and the
+    activation (none or SiLU) are the caller's; q and k are scaled to unit L2
+    norm per head, y / sqrt(|y|^2 + eps); v is not.
+
+    For sequence n with window entry s = conv_slots[n] (n if None), rows
+    t = 0 .. L-1 and each stream (q, k, v), in this order:
+      1. the input sequence is [taps 0, 1, 2 of the entry ; its L rows];
+      2. y_t = sum_j w[j] * input[t + j] over j = 0 .. 3, channel by channel;
+      3. the activation;
+      4. for q and k, the per-head L2 normalisation;
+      5. the entry's taps become the last three rows of that input sequence.
+    A sequence whose id is -1 is padding: nothing of it is computed or written.
+    An id outside [-1, num_slots) is handled like -1 and reported.
+
+    xq, xk, xv: uint16 bf16 bits [T][H][D]; conv_weight: float [3][H*D][4];
+    conv_pool: uint16 bf16 bits [num_slots][3][3][H*D].
+    Returns (q, k, v) float64 [T][H][D] (NaN in rows not computed), the new
+    pool (uint16 bits) and the list of sequence indices whose id was out of
+    range.
+    """
+    xs = [np.asarray(a, dtype=np.uint16) for a in (xq, xk, xv)]
+    T, H, D = xs[0].shape
+    C = H * D
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    N = cu.shape[0] - 1
+    w = np.asarray(conv_weight, dtype=np.float64).reshape(3, C, 4)
+    pool = np.array(conv_pool, dtype=np.uint16)             # a copy: updated below
+    num_slots = pool.shape[0]
+    assert pool.shape == (num_slots, 3, 3, C), pool.shape
+    slots = np.arange(N) if conv_slots is None else np.asarray(conv_slots, dtype=np.int64)
+    outs = [np.full((T, C), np.nan) for _ in range(3)]
+    bad = [n for n in range(N) if slots[n] < -1 or slots[n] >= num_slots]
+    for n in range(N):
+        slot = int(slots[n])
+        if not 0 <= slot < num_slots:
+            continue
+        b, e = int(cu[n]), int(cu[n + 1])
+        L = e - b
+        if L <= 0:
+            continue
+        for s in range(3):
+            seq_bits = np.concatenate([pool[slot, :, s, :], xs[s].reshape(T, C)[b:e]], axis=0)   # [3 + L][C]
+            seq = bf16_bits_to_f64(seq_bits)
+            y = sum(w[s, :, j] * seq[j:j + L] for j in range(4))                              # [L][C]
+            if activation == "silu":
+                y = y / (1.0 + np.exp(-y))
+            elif activation != "none":
+                raise ValueError(activation)
+            if s < 2:
+                yh = y.reshape(L, H, D)
+                y = (yh / np.sqrt((yh * yh).sum(axis=2, keepdims=True) + eps)).reshape(L, C)
+            outs[s][b:e] = y
+            pool[slot, :, s, :] = seq_bits[L:L + 3]
+    return tuple(o.reshape(T, H, D) for o in outs), pool, bad

@@ -170,3 +170,45 @@ def test_fold_validation_statuses(kda_lib):
 @pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
 def test_fold_valid_call_passes_validation(kda_lib):
     assert call_fold() == kda.KDA_ERR_DEVICE
+
+
+def call_conv(**over):
+    N, T, H, d = 3, 40, 2, 128
+    xb = T * H * d * 2
+    args = dict(xq=A, xk=A + xb, xv=A + 2 * xb, w=A + 3 * xb, cu=A + 3 * xb + 16384, slots=A + 3 * xb + 20480,
+                pool=A + (8 << 20), num_slots=5, q=A + (16 << 20), k=A + (16 << 20) + xb, v=A + (16 << 20) + 2 * xb,
+                N=N, T=T, H=H, d=d, act=1, eps=1e-6, stream=0)
+    args.update(over)
+    order = ["xq", "xk", "xv", "w", "cu", "slots", "pool", "num_slots", "q", "k", "v", "N", "T", "H", "d", "act",
+             "eps", "stream"]
+    return kda.kda_short_conv(*[args[n] for n in order])
+
+
+def test_conv_validation_statuses(kda_lib):
+    assert call_conv(xq=0) == kda.KDA_ERR_NULL
+    assert call_conv(w=0) == kda.KDA_ERR_NULL
+    assert call_conv(pool=0) == kda.KDA_ERR_NULL
+    assert call_conv(N=0) == kda.KDA_ERR_SHAPE
+    assert call_conv(num_slots=0) == kda.KDA_ERR_SHAPE
+    assert call_conv(slots=0, num_slots=2) == kda.KDA_ERR_SHAPE            # entry n needs num_slots >= N
+    assert call_conv(act=2) == kda.KDA_ERR_SHAPE
+    assert call_conv(eps=-1.0) == kda.KDA_ERR_SHAPE
+    assert call_conv(eps=float("nan")) == kda.KDA_ERR_SHAPE
+    assert call_conv(d=64) == kda.KDA_ERR_UNSUPPORTED
+    assert call_conv(xk=A + 40 * 2 * 128 * 2 + 8) == kda.KDA_ERR_ALIGN
+    assert call_conv(cu=A + 3 * 40 * 2 * 128 * 2 + 16386) == kda.KDA_ERR_ALIGN
+    assert call_conv(pool=A) == kda.KDA_ERR_ALIAS                          # pool over xq
+    assert call_conv(v=A + 40 * 2 * 128 * 2) == kda.KDA_ERR_ALIAS          # v_out over xk
+    assert call_conv(k=A + (16 << 20)) == kda.KDA_ERR_ALIAS                # k_out over q_out
+    assert call_conv(q=A + (8 << 20)) == kda.KDA_ERR_ALIAS                 # q_out over the pool
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+def test_conv_empty_rows_allow_null_tensors(kda_lib):
+    assert call_conv(xq=0, xk=0, xv=0, q=0, k=0, v=0, T=0) == kda.KDA_ERR_DEVICE
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+def test_conv_valid_call_passes_validation(kda_lib):
+    assert call_conv() == kda.KDA_ERR_DEVICE
+    assert call_conv(slots=0, num_slots=3, act=0, eps=0.0) == kda.KDA_ERR_DEVICE
