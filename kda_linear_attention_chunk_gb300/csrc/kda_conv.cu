@@ -33,7 +33,6 @@ namespace {
 
 constexpr int kConvRows = 32;    // rows per warp
 constexpr int kConvWarps = 4;    // warps per CTA
-constexpr int kConvAhead = 4;    // rows whose loads are in flight ahead of use
 
 struct ConvParams {
     const uint16_t *x[3];
@@ -60,6 +59,15 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&b);
 }
 
+// SiLU(a) = a * sigmoid(a) = (a/2) (1 + tanh(a/2)): one hardware tanh
+__device__ __forceinline__ float silu(float a)
+{
+    const float h = 0.5f * a;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
+
 // cu_seqlens[i] clamped into [0, T]
 __device__ __forceinline__ int cu_at(const int32_t *cu, int i, int T) { return min(max(cu[i], 0), T); }
 
@@ -78,7 +86,7 @@ __device__ int seq_of(const int32_t *cu, int N, int T, int t, int lane)
     return lo;
 }
 
-__global__ void __launch_bounds__(kConvWarps * 32, 7) kda_conv_kernel(ConvParams p)
+__global__ void __launch_bounds__(kConvWarps * 32, 6) kda_conv_kernel(ConvParams p)
 {
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * kConvWarps + (threadIdx.x >> 5);   // ((block * 3 + s) * H + h)
@@ -116,58 +124,62 @@ __global__ void __launch_bounds__(kConvWarps * 32, 7) kda_conv_kernel(ConvParams
             t = seg_end;
             continue;
         }
-        // the three rows before t: earlier rows of the sequence or the window's taps
-        float hist[3][4];
+        // xa holds rows g-3 .. g+3 of a group of four rows g .. g+3 (floats, this
+        // lane's four channels); the three rows before t are earlier rows of the
+        // sequence or the window's taps
+        float xa[7][4];
 #pragma unroll
         for (int j = 0; j < 3; j++) {
             const int r = t - 3 + j;
             const uint2 raw = r >= bos ? __ldg(reinterpret_cast<const uint2 *>(xs + (size_t)r * HC + gc))
                                        : *reinterpret_cast<const uint2 *>(
                                              p.pool + ((size_t)(slot * 3 + (r - bos + 3)) * 3 + s) * HC + gc);
-            hist[j][0] = bf_lo(raw.x); hist[j][1] = bf_hi(raw.x); hist[j][2] = bf_lo(raw.y); hist[j][3] = bf_hi(raw.y);
+            xa[j][0] = bf_lo(raw.x); xa[j][1] = bf_hi(raw.x); xa[j][2] = bf_lo(raw.y); xa[j][3] = bf_hi(raw.y);
         }
-        const uint16_t *xrow = xs + (size_t)t * HC + gc;     // row r of this lane's channels
+        const uint16_t *xrow = xs + (size_t)t * HC + gc;     // row g of this lane's channels
         uint16_t *yrow = ys + (size_t)t * HC + gc;
-        uint2 nxt[kConvAhead];                                 // rows r .. r + kConvAhead - 1
+        uint2 ld[4];                                           // rows g .. g+3, then the next group's
 #pragma unroll
-        for (int i = 0; i < kConvAhead; i++)
-            nxt[i] = t + i < seg_end ? __ldg(reinterpret_cast<const uint2 *>(xrow + i * HC)) : make_uint2(0u, 0u);
+        for (int i = 0; i < 4; i++)
+            ld[i] = t + i < seg_end ? __ldg(reinterpret_cast<const uint2 *>(xrow + i * HC)) : make_uint2(0u, 0u);
 #pragma unroll 1
-        for (int r = t; r < seg_end; r++, xrow += HC, yrow += HC) {
-            const uint2 cur = nxt[0];
+        for (int g = t; g < seg_end; g += 4, xrow += 4 * HC, yrow += 4 * HC) {
 #pragma unroll
-            for (int i = 0; i + 1 < kConvAhead; i++) nxt[i] = nxt[i + 1];
-            nxt[kConvAhead - 1] = r + kConvAhead < seg_end
-                                      ? __ldg(reinterpret_cast<const uint2 *>(xrow + kConvAhead * HC))
-                                      : make_uint2(0u, 0u);
-            const float xv[4] = {bf_lo(cur.x), bf_hi(cur.x), bf_lo(cur.y), bf_hi(cur.y)};
-            float y[4];
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                float a = wt[c][0] * hist[0][c];
-                a = fmaf(wt[c][1], hist[1][c], a);
-                a = fmaf(wt[c][2], hist[2][c], a);
-                a = fmaf(wt[c][3], xv[c], a);
-                y[c] = p.act ? a * __frcp_rn(1.f + __expf(-a)) : a;   // SiLU: a * sigmoid(a)
+            for (int i = 0; i < 4; i++) {
+                xa[3 + i][0] = bf_lo(ld[i].x); xa[3 + i][1] = bf_hi(ld[i].x);
+                xa[3 + i][2] = bf_lo(ld[i].y); xa[3 + i][3] = bf_hi(ld[i].y);
+                ld[i] = g + 4 + i < seg_end ? __ldg(reinterpret_cast<const uint2 *>(xrow + (4 + i) * HC))
+                                            : make_uint2(0u, 0u);
             }
-            float scale = 1.f;
-            if (s < 2) {                          // q and k: unit L2 norm per head
-                float ss = y[0] * y[0];
-                ss = fmaf(y[1], y[1], ss);
-                ss = fmaf(y[2], y[2], ss);
-                ss = fmaf(y[3], y[3], ss);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                scale = rsqrtf(ss + p.eps);
-            }
-            *reinterpret_cast<uint2 *>(yrow) =
-                make_uint2(pack_bf2(y[0] * scale, y[1] * scale), pack_bf2(y[2] * scale, y[3] * scale));
+            for (int i = 0; i < 4; i++) {
+                if (g + i >= seg_end) break;
+                float y[4];
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                hist[0][c] = hist[1][c];
-                hist[1][c] = hist[2][c];
-                hist[2][c] = xv[c];
+                for (int c = 0; c < 4; c++) {
+                    float a = wt[c][0] * xa[i][c];
+                    a = fmaf(wt[c][1], xa[i + 1][c], a);
+                    a = fmaf(wt[c][2], xa[i + 2][c], a);
+                    a = fmaf(wt[c][3], xa[i + 3][c], a);
+                    y[c] = p.act ? silu(a) : a;
+                }
+                float scale = 1.f;
+                if (s < 2) {                      // q and k: unit L2 norm per head
+                    float ss = y[0] * y[0];
+                    ss = fmaf(y[1], y[1], ss);
+                    ss = fmaf(y[2], y[2], ss);
+                    ss = fmaf(y[3], y[3], ss);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                    scale = rsqrtf(ss + p.eps);
+                }
+                *reinterpret_cast<uint2 *>(yrow + i * HC) =
+                    make_uint2(pack_bf2(y[0] * scale, y[1] * scale), pack_bf2(y[2] * scale, y[3] * scale));
             }
+#pragma unroll
+            for (int j = 0; j < 3; j++)
+#pragma unroll
+                for (int c = 0; c < 4; c++) xa[j][c] = xa[4 + j][c];
         }
         t = seg_end;
     }
