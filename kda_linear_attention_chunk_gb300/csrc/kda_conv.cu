@@ -16,12 +16,15 @@
 // of [old taps ; the sequence's L rows].
 //
 // kda_conv_kernel: one warp per (block of 32 rows, head, stream).  Lane l owns
-// channels 4l .. 4l+3 of the head, holds their 16 weights and the three
-// previous rows in registers and keeps the next rows' loads in flight; each
-// row is one 256-byte load and one 256-byte store per warp.  The L2 norm is a
-// warp reduction.  kda_conv_window_kernel then writes the new windows in
-// place; it runs after the first kernel on the same stream, so every read of
-// an old window precedes its rewrite.
+// channels 4l .. 4l+3 of the head and holds their 16 weights.  Rows go in
+// groups of four over a window of seven rows in registers (the three before
+// the group and the group), with the next group's loads in flight; each row is
+// one 256-byte load and one 256-byte store per warp.  The L2 norm is a warp
+// reduction.  The kernel is bound by instruction issue rather than by memory,
+// so the per-row code is kept short (no per-row register shifts; SiLU through
+// one tanh).  kda_conv_window_kernel then writes the new windows in place; it
+// runs after the first kernel on the same stream, so every read of an old
+// window precedes its rewrite.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
