@@ -22,9 +22,10 @@
 // one 256-byte load and one 256-byte store per warp.  The L2 norm is a warp
 // reduction.  The kernel is bound by instruction issue rather than by memory,
 // so the per-row code is kept short (no per-row register shifts; SiLU through
-// one tanh).  kda_conv_window_kernel then writes the new windows in place; it
-// runs after the first kernel on the same stream, so every read of an old
-// window precedes its rewrite.
+// one tanh).  Only the warp that holds a sequence's first row reads the
+// sequence's window (for that row's three predecessors), so that warp also
+// writes the new window, right after reading the old one; the new taps are
+// input rows (or, for sequences shorter than three rows, old taps it holds).
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -89,13 +90,35 @@ __device__ int seq_of(const int32_t *cu, int N, int T, int t, int lane)
     return lo;
 }
 
+// Edge x of the row blocks, moved so that no block starts among a sequence's
+// first three rows (whose predecessors are window taps): then only the warp
+// that holds a sequence's first row reads its window.  Both warps that share
+// an edge compute it the same way.
+__device__ int block_edge(const ConvParams &p, int x, int lane)
+{
+    if (x >= p.T) return p.T;
+    const int n = seq_of(p.cu, p.N, p.T, x, lane);
+    const int b = cu_at(p.cu, n, p.T), e = cu_at(p.cu, n + 1, p.T);
+    const int first3 = min(b + 3, e);
+    return (b < x && x < first3) ? first3 : x;
+}
+
 __global__ void __launch_bounds__(kConvWarps * 32, 6) kda_conv_kernel(ConvParams p)
 {
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * kConvWarps + (threadIdx.x >> 5);   // ((block * 3 + s) * H + h)
-    const int h = item % p.H, s = (item / p.H) % 3, t0 = (item / p.H / 3) * kConvRows;
-    if (t0 >= p.T) return;
-    const int t1 = min(t0 + kConvRows, p.T);
+    if (item == 0) {                              // every sequence's bounds and id, checked once
+        for (int m = lane; m <= p.N; m += 32) {
+            if (p.cu[m] < 0 || p.cu[m] > p.T) atomicOr(p.err, kErrBadSeqlens);
+            if (m < p.N) {
+                const int sl = p.slots ? p.slots[m] : m;
+                if (sl < -1 || sl >= p.num_slots) atomicOr(p.err, kErrBadSlot);
+            }
+        }
+    }
+    const int h = item % p.H, s = (item / p.H) % 3, b32 = (item / p.H / 3) * kConvRows;
+    if (b32 >= p.T) return;
+    const int t0 = block_edge(p, b32, lane), t1 = block_edge(p, b32 + kConvRows, lane);
     const size_t HC = (size_t)p.H * 128;         // elements per row of a stream
     const int gc = h * 128 + 4 * lane;            // this lane's first channel
     float wt[4][4];                               // [channel][tap]
@@ -122,8 +145,7 @@ __global__ void __launch_bounds__(kConvWarps * 32, 6) kda_conv_kernel(ConvParams
         }
         const int seg_end = min(eos, t1);
         const int slot = p.slots ? p.slots[n] : n;
-        if (slot < 0 || slot >= p.num_slots) {    // padded (or invalid: reported) -- skipped
-            if (slot != -1 && lane == 0) atomicOr(p.err, kErrBadSlot);
+        if (slot < 0 || slot >= p.num_slots) {    // padded (or an id outside the pool) -- skipped
             t = seg_end;
             continue;
         }
@@ -131,13 +153,29 @@ __global__ void __launch_bounds__(kConvWarps * 32, 6) kda_conv_kernel(ConvParams
         // lane's four channels); the three rows before t are earlier rows of the
         // sequence or the window's taps
         float xa[7][4];
+        uint16_t *win = p.pool + (size_t)slot * 9 * HC + (size_t)s * HC + gc;   // tap j at win + 3 * j * HC
+        uint2 raw[3];
 #pragma unroll
         for (int j = 0; j < 3; j++) {
             const int r = t - 3 + j;
-            const uint2 raw = r >= bos ? __ldg(reinterpret_cast<const uint2 *>(xs + (size_t)r * HC + gc))
-                                       : *reinterpret_cast<const uint2 *>(
-                                             p.pool + ((size_t)(slot * 3 + (r - bos + 3)) * 3 + s) * HC + gc);
-            xa[j][0] = bf_lo(raw.x); xa[j][1] = bf_hi(raw.x); xa[j][2] = bf_lo(raw.y); xa[j][3] = bf_hi(raw.y);
+            raw[j] = r >= bos ? __ldg(reinterpret_cast<const uint2 *>(xs + (size_t)r * HC + gc))
+                              : *reinterpret_cast<const uint2 *>(win + (size_t)(3 * (r - bos + 3)) * HC);
+            xa[j][0] = bf_lo(raw[j].x); xa[j][1] = bf_hi(raw[j].x); xa[j][2] = bf_lo(raw[j].y); xa[j][3] = bf_hi(raw[j].y);
+        }
+        if (t == bos) {
+            // This warp holds the sequence's first row, so it alone reads the old
+            // window (just done) and it writes the new one: the last three rows of
+            // [old taps ; the L rows].
+            const int L = eos - bos;
+            uint2 nw[3];
+#pragma unroll
+            for (int j = 0; j < 3; j++) {
+                const int r = L - 3 + j;          // row of new tap j; r < 0: old tap r + 3
+                nw[j] = r >= 0 ? __ldg(reinterpret_cast<const uint2 *>(xs + (size_t)(bos + r) * HC + gc))
+                               : r == -2 ? raw[1] : raw[2];
+            }
+#pragma unroll
+            for (int j = 0; j < 3; j++) *reinterpret_cast<uint2 *>(win + (size_t)(3 * j) * HC) = nw[j];
         }
         const uint16_t *xrow = xs + (size_t)t * HC + gc;     // row g of this lane's channels
         uint16_t *yrow = ys + (size_t)t * HC + gc;
@@ -188,35 +226,6 @@ __global__ void __launch_bounds__(kConvWarps * 32, 6) kda_conv_kernel(ConvParams
     }
 }
 
-// New windows: thread = (sequence, stream, 8 channels); the taps are the last
-// three rows of [old taps ; the sequence's rows], all read before any write.
-__global__ void __launch_bounds__(256) kda_conv_window_kernel(ConvParams p)
-{
-    const int pieces = p.H * 16;                  // 8-channel pieces per stream row
-    const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;
-    if (idx >= (long long)p.N * 3 * pieces) return;
-    const int piece = (int)(idx % pieces), s = (int)((idx / pieces) % 3), n = (int)(idx / pieces / 3);
-    const int slot = p.slots ? p.slots[n] : n;
-    if (piece == 0 && s == 0) {
-        if (p.cu[n] < 0 || p.cu[n] > p.T || p.cu[n + 1] < 0 || p.cu[n + 1] > p.T) atomicOr(p.err, kErrBadSeqlens);
-        if (slot < -1 || slot >= p.num_slots) atomicOr(p.err, kErrBadSlot);
-    }
-    if (slot < 0 || slot >= p.num_slots) return;
-    const int bos = cu_at(p.cu, n, p.T), L = cu_at(p.cu, n + 1, p.T) - bos;
-    if (L <= 0) return;                           // no rows: the window stays
-    const size_t HC = (size_t)p.H * 128;
-    const int gc = piece * 8;
-    uint4 tap[3];
-#pragma unroll
-    for (int j = 0; j < 3; j++) {
-        const int r = L - 3 + j;                  // row of the new tap j (negative: an old tap)
-        tap[j] = r >= 0 ? *reinterpret_cast<const uint4 *>(pick(p.x, s) + (size_t)(bos + r) * HC + gc)
-                        : *reinterpret_cast<const uint4 *>(p.pool + ((size_t)(slot * 3 + (r + 3)) * 3 + s) * HC + gc);
-    }
-#pragma unroll
-    for (int j = 0; j < 3; j++) *reinterpret_cast<uint4 *>(p.pool + ((size_t)(slot * 3 + j) * 3 + s) * HC + gc) = tap[j];
-}
-
 }  // namespace
 
 cudaError_t launch_kda_conv_bf16_d128(const ConvArgs &a)
@@ -234,14 +243,9 @@ cudaError_t launch_kda_conv_bf16_d128(const ConvArgs &a)
     p.act = a.activation;
     p.eps = a.eps;
     p.err = a.err_word;
-    if (a.T > 0) {
-        const long long items = (long long)((a.T + kConvRows - 1) / kConvRows) * 3 * a.H;
-        kda_conv_kernel<<<(unsigned)((items + kConvWarps - 1) / kConvWarps), kConvWarps * 32, 0, a.stream>>>(p);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    const long long threads = (long long)a.N * 3 * a.H * 16;
-    kda_conv_window_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, a.stream>>>(p);
+    const long long items = (long long)((a.T + kConvRows - 1) / kConvRows) * 3 * a.H;
+    const long long blocks = items > 0 ? (items + kConvWarps - 1) / kConvWarps : 1;   // block 0 checks the ids
+    kda_conv_kernel<<<(unsigned)blocks, kConvWarps * 32, 0, a.stream>>>(p);
     return cudaGetLastError();
 }
 

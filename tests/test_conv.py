@@ -141,3 +141,24 @@ def test_conv_packed16_8192_h32():
     for g, r in zip(got, ref):
         assert rel_l2(g, r) <= CONV_TOL
     np.testing.assert_array_equal(host_bits(pool_t), new_pool)
+
+
+@pytest.mark.parametrize("seed", [16, 17, 18])
+def test_conv_short_sequences_at_every_block_offset(seed):
+    """Many sequences of 1 to 6 rows among longer ones, so that sequences start
+    at every offset within the kernel's 32-row blocks, the first three rows of
+    a sequence (which read its window) included."""
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in rng.integers(1, 7, 90)]
+    for pos in (10, 40, 70):
+        lens[pos] = int(rng.integers(30, 70))
+    H = 2
+    num_slots = len(lens) + 5
+    xs, w, pool, cu = draw(lens, H, num_slots, seed=seed)
+    slots = rng.permutation(num_slots)[:len(lens)].astype(np.int32)
+    pool_t = dev_bf16(pool)
+    got = gpu_conv(xs, w, pool_t, cu, slots)
+    ref, new_pool, _ = oracle.short_conv(*xs, w, cu, pool, slots)
+    for g, r in zip(got, ref):
+        assert rel_l2(g, r) <= CONV_TOL
+    np.testing.assert_array_equal(host_bits(pool_t), new_pool)
