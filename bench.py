@@ -256,7 +256,7 @@ def measure_conv(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
     alg = conv_bytes(lengths, n_heads)
     peak, _ = peaks()
     achieved = alg / (ms / 1e3) / 1e9
-    return {"workload": "conv_packed16_8192_h32", "kernel": "kda_conv_kernel + kda_conv_window_kernel",
+    return {"workload": "conv_packed16_8192_h32", "kernel": "kda_conv_kernel",
             "T": t_rows, "N": n, "H": n_heads, "activation": "silu", "steps": steps, "us_per_call": ms * 1e3,
             "tokens_per_s": t_rows / (ms / 1e3), "l2": "2 rotating input sets of 201 MB (projections) each",
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

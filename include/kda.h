@@ -269,8 +269,9 @@ int kda_fold_commit(const uint16_t *k, const uint16_t *v, const float *g, const 
  *   N >= 1, T >= 0, H >= 1; d = 128.
  * Tensor pointers must be 16-byte aligned (cu_seqlens and conv_slots 4-byte).
  * The outputs must not overlap an input, the pool or each other; the pool must
- * not overlap an input.  Two kernels run on `stream`: the conv (which reads
- * the old windows), then the window update.  Returns a kda_status.
+ * not overlap an input.  One kernel runs on `stream`; the warp that holds a
+ * sequence's first row alone reads its window and then rewrites it.  Returns
+ * a kda_status.
  */
 int kda_short_conv(const uint16_t *xq, const uint16_t *xk, const uint16_t *xv,
                    const float *conv_weight, const int32_t *cu_seqlens,
