@@ -550,11 +550,13 @@ __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
     }
 }
 
+// (unrolled, unlike the other issue loops: group E, which issues it, sets the
+// cadence, and the unrolled issue is faster; measured)
 __device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
 {
     const uint32_t st = sm.u32(s * kStageBytes);
     const uint32_t id = idesc_f16(128, 64, 0, 0);
-#pragma unroll 1
+#pragma unroll
     for (int ks = 0; ks < 8; ks++) {
         const int kb = ks >> 2, kin = ks & 3;
         const uint64_t ad = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
