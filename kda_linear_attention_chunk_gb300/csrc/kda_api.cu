@@ -295,6 +295,7 @@ int kda_fold_commit(const uint16_t *k, const uint16_t *v, const float *g, const 
     a.k = k; a.v = v; a.g = g; a.beta = beta; a.accepted = accepted;
     a.state_slots = state_slots; a.state_pool = state_pool;
     a.N = N; a.W = W; a.H = H; a.num_slots = num_slots;
+    a.num_sms = d->num_sms;
     a.stream = (cudaStream_t)stream;
     a.err_word = d->err;
     return kda::launch_kda_fold_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

@@ -141,52 +141,164 @@ struct FoldParams {
     const int32_t *slots;        // [N] or nullptr (entry n)
     float *pool;                 // [num_slots][H][128][128]
     int N, W, H, num_slots;
+    int items;                   // 4 N H: (sequence, head, quarter of the value rows)
     int *err;
 };
 
 // Commit of a speculative round: the state takes the first accepted[n] tokens
-// of sequence n's window, one token_step each.  The state stays in registers;
-// the tokens' exp(g), k, v and beta are staged in shared memory up to
-// kFoldBatch tokens at a time, all loads of a batch in flight together, so the
-// steps themselves wait on no memory.
+// of sequence n's window, one token_step each.  A persistent CTA walks items
+// (sequence, head, quarter of the value rows); while it steps one item's state
+// (in registers) through its tokens, the next item's state rows are loading
+// into registers and its tokens' g, k, v and beta are copying (cp.async) into
+// the other of two raw buffers.  Before an item's steps its raw tokens become
+// exp(g), k, v and beta in fp32 (the decode step's operands), so the steps
+// wait on no memory.  Up to kFoldBatch tokens go ahead like this; further ones
+// (windows longer than kFoldBatch) are staged batch by batch.
 constexpr int kFoldBatch = 16;
 
-__global__ void __launch_bounds__(kDecThreads, 5) kda_fold_kernel(FoldParams p)
+struct FoldItem {
+    int n, h, vq, slot, acc;     // acc 0: nothing to do (padded, bad id, or none accepted)
+};
+
+__device__ __forceinline__ FoldItem fold_item(const FoldParams &p, int q)
 {
-    __shared__ float4 sa[kFoldBatch][32], sk[kFoldBatch][32];
-    __shared__ float sv[kFoldBatch][128], sb[kFoldBatch];
-    const int rh = blockIdx.x >> 2, vq = blockIdx.x & 3;
-    const int n = rh / p.H, h = rh % p.H;
-    const int slot = decode_slot(p.slots, n, p.num_slots, p.err);
-    if (slot < 0) return;
-    int acc = p.accepted[n];
-    if (acc < 0 || acc > p.W) {
-        if (threadIdx.x == 0) atomicOr(p.err, kErrBadAccepted);
-        acc = acc < 0 ? 0 : p.W;
-    }
-    if (acc == 0) return;   // nothing accepted: the state stays as it is
-    const int tid = threadIdx.x;
-    const int vr = kDecRows * vq + (tid >> 3), qe = tid & 7;
-    float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
-    float4 s[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) s[j] = st[8 * j + qe];
-    for (int t0 = 0; t0 < acc; t0 += kFoldBatch) {
-        const int nt = min(kFoldBatch, acc - t0);
-        if (t0 > 0) __syncthreads();           // the previous batch is no longer read
-        for (int i = tid; i < nt * 128; i += kDecThreads) {
-            const int t = i >> 7, c = i & 127;
-            const size_t row = ((size_t)n * p.W + t0 + t) * p.H + h;
-            reinterpret_cast<float *>(sa[t])[c] = dec_ex2(p.g[row * 128 + c] * kDecLog2e);
-            reinterpret_cast<float *>(sk[t])[c] = bf16_bits_to_float(p.k[row * 128 + c]);
-            sv[t][c] = bf16_bits_to_float(p.v[row * 128 + c]);
-            if (c == 0) sb[t] = p.beta[row];
+    FoldItem it;
+    it.n = (q >> 2) / p.H;
+    it.h = (q >> 2) % p.H;
+    it.vq = q & 3;
+    it.slot = decode_slot(p.slots, it.n, p.num_slots, p.err);
+    it.acc = 0;
+    if (it.slot >= 0) {
+        int acc = p.accepted[it.n];
+        if (acc < 0 || acc > p.W) {
+            if (threadIdx.x == 0) atomicOr(p.err, kErrBadAccepted);
+            acc = acc < 0 ? 0 : p.W;
         }
-        __syncthreads();
-        for (int t = 0; t < nt; t++) token_step(s, sa[t], sk[t], nullptr, qe, sv[t][vr], sb[t]);
+        it.acc = acc;
     }
+    return it;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *ptr) { return (uint32_t)__cvta_generic_to_shared(ptr); }
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+struct FoldRaw {                 // one item's first kFoldBatch tokens as stored in global memory
+    float g[kFoldBatch][128];
+    uint16_t k[kFoldBatch][128];
+    uint16_t v[kFoldBatch][kDecRows];   // this quarter's value rows only
+    float beta[kFoldBatch];
+};
+
+__device__ __forceinline__ size_t fold_row(const FoldParams &p, const FoldItem &it, int t)
+{
+    return ((size_t)it.n * p.W + t) * p.H + it.h;
+}
+
+__device__ void fold_issue_tokens(const FoldParams &p, const FoldItem &it, FoldRaw &raw, int tid)
+{
+    const int nt = min(it.acc, kFoldBatch);
+    for (int i = tid; i < nt * 32; i += kDecThreads) {     // g: 32 pieces of 16 B a token
+        const int t = i >> 5, c = 4 * (i & 31);
+        cp_async16(&raw.g[t][c], p.g + fold_row(p, it, t) * 128 + c);
+    }
+    for (int i = tid; i < nt * 16; i += kDecThreads) {     // k: 16 pieces
+        const int t = i >> 4, c = 8 * (i & 15);
+        cp_async16(&raw.k[t][c], p.k + fold_row(p, it, t) * 128 + c);
+    }
+    for (int i = tid; i < nt * 4; i += kDecThreads) {      // v of this quarter: 4 pieces
+        const int t = i >> 2, c = 8 * (i & 3);
+        cp_async16(&raw.v[t][c], p.v + fold_row(p, it, t) * 128 + kDecRows * it.vq + c);
+    }
+    if (tid < nt) cp_async4(&raw.beta[tid], p.beta + fold_row(p, it, tid));
+}
+
+__global__ void __launch_bounds__(kDecThreads, 4) kda_fold_kernel(FoldParams p)
+{
+    __shared__ FoldRaw raw[2];
+    __shared__ float4 sa[kFoldBatch][32], sk[kFoldBatch][32];
+    __shared__ float sv[kFoldBatch][kDecRows], sb[kFoldBatch];
+    const int tid = threadIdx.x, qe = tid & 7, vl = tid >> 3;   // value row vl of the quarter
+    auto state_rows = [&](const FoldItem &it) {
+        return reinterpret_cast<float4 *>(p.pool + (((size_t)it.slot * p.H + it.h) * 128 + kDecRows * it.vq + vl) * 128);
+    };
+    int q = blockIdx.x, b = 0;
+    FoldItem it = fold_item(p, q);
+    float4 s[4];
+    if (it.acc > 0) {
+        const float4 *st = state_rows(it);
 #pragma unroll
-    for (int j = 0; j < 4; j++) st[8 * j + qe] = s[j];
+        for (int j = 0; j < 4; j++) s[j] = st[8 * j + qe];
+        fold_issue_tokens(p, it, raw[0], tid);
+    }
+    cp_async_commit();
+    while (q < p.items) {
+        const int qn = q + gridDim.x;
+        FoldItem nx;
+        nx.acc = 0;
+        if (qn < p.items) nx = fold_item(p, qn);
+        if (it.acc > 0) {
+            // this item's raw tokens have landed and the previous item's steps are
+            // over: convert them into the step operands
+            cp_async_wait_all();
+            __syncthreads();
+            const int nt = min(it.acc, kFoldBatch);
+            for (int i = tid; i < nt * 128; i += kDecThreads) {
+                const int t = i >> 7, c = i & 127;
+                reinterpret_cast<float *>(sa[t])[c] = dec_ex2(raw[b].g[t][c] * kDecLog2e);
+                reinterpret_cast<float *>(sk[t])[c] = bf16_bits_to_float(raw[b].k[t][c]);
+            }
+            for (int i = tid; i < nt * kDecRows; i += kDecThreads)
+                sv[i / kDecRows][i % kDecRows] = bf16_bits_to_float(raw[b].v[i / kDecRows][i % kDecRows]);
+            if (tid < nt) sb[tid] = raw[b].beta[tid];
+            __syncthreads();
+        }
+        // the next item's state and tokens go out before this item's steps
+        float4 sn[4];
+        if (nx.acc > 0) {
+            const float4 *st = state_rows(nx);
+#pragma unroll
+            for (int j = 0; j < 4; j++) sn[j] = st[8 * j + qe];
+            fold_issue_tokens(p, nx, raw[b ^ 1], tid);
+        }
+        cp_async_commit();
+        if (it.acc > 0) {
+            const int nt = min(it.acc, kFoldBatch);
+            for (int t = 0; t < nt; t++) token_step(s, sa[t], sk[t], nullptr, qe, sv[t][vl], sb[t]);
+            for (int t0 = kFoldBatch; t0 < it.acc; t0 += kFoldBatch) {   // windows longer than kFoldBatch
+                const int mt = min(kFoldBatch, it.acc - t0);
+                __syncthreads();                 // the previous batch is no longer read
+                for (int i = tid; i < mt * 128; i += kDecThreads) {
+                    const int t = i >> 7, c = i & 127;
+                    const size_t row = fold_row(p, it, t0 + t);
+                    reinterpret_cast<float *>(sa[t])[c] = dec_ex2(p.g[row * 128 + c] * kDecLog2e);
+                    reinterpret_cast<float *>(sk[t])[c] = bf16_bits_to_float(p.k[row * 128 + c]);
+                    if (c < kDecRows) sv[t][c] = bf16_bits_to_float(p.v[row * 128 + kDecRows * it.vq + c]);
+                    if (c == 0) sb[t] = p.beta[row];
+                }
+                __syncthreads();
+                for (int t = 0; t < mt; t++) token_step(s, sa[t], sk[t], nullptr, qe, sv[t][vl], sb[t]);
+            }
+            float4 *st = state_rows(it);
+#pragma unroll
+            for (int j = 0; j < 4; j++) st[8 * j + qe] = s[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j++) s[j] = sn[j];
+        it = nx;
+        q = qn;
+        b ^= 1;
+    }
+    cp_async_wait_all();
 }
 
 }  // namespace
@@ -210,8 +322,11 @@ cudaError_t launch_kda_fold_bf16_d128(const FoldArgs &a)
     p.k = (const uint16_t *)a.k; p.v = (const uint16_t *)a.v;
     p.g = a.g; p.beta = a.beta; p.accepted = a.accepted; p.slots = a.state_slots; p.pool = a.state_pool;
     p.N = a.N; p.W = a.W; p.H = a.H; p.num_slots = a.num_slots;
+    p.items = (128 / kDecRows) * a.N * a.H;
     p.err = a.err_word;
-    kda_fold_kernel<<<(128 / kDecRows) * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
+    const int per_sm = 4;
+    const int grid = a.num_sms > 0 && p.items > a.num_sms * per_sm ? a.num_sms * per_sm : p.items;
+    kda_fold_kernel<<<grid, kDecThreads, 0, a.stream>>>(p);
     return cudaGetLastError();
 }
 

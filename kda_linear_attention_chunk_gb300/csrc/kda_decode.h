@@ -33,6 +33,7 @@ struct FoldArgs {
     const int32_t *state_slots;     // [N] or nullptr (entry n)
     float *state_pool;              // [num_slots][H][128][128]
     int N, W, H, num_slots;
+    int num_sms;                    // persistent grid: 4 CTAs per SM
     cudaStream_t stream;
     int *err_word;
 };
