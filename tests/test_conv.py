@@ -162,3 +162,29 @@ def test_conv_short_sequences_at_every_block_offset(seed):
     for g, r in zip(got, ref):
         assert rel_l2(g, r) <= CONV_TOL
     np.testing.assert_array_equal(host_bits(pool_t), new_pool)
+
+
+def test_conv_then_prefill_matches_the_oracle_chain():
+    """The prologue's q, k, v fed to the prefill (as a layer runs them) against
+    the oracle's prologue, rounded to bf16, fed to the oracle's recurrence."""
+    from gpu_util import OUT_TOL, STATE_TOL, to_dev
+    t = torch()
+    lens = [70, 1, 130, 5, 64]
+    H = 2
+    xs, w, pool, cu = draw(lens, H, len(lens), seed=19)
+    rng = np.random.default_rng(19)
+    T = int(cu[-1])
+    g = (-0.2 * rng.random((T, H, 128))).astype(np.float32)
+    beta = rng.random((T, H)).astype(np.float32)
+    s0 = (0.02 * rng.standard_normal((len(lens), H, 128, 128))).astype(np.float32)
+    pool_t = dev_bf16(pool)
+    x_t = [dev_bf16(x) for x in xs]
+    q, k, v = kda.short_conv(*x_t, t.from_numpy(w).cuda(), t.from_numpy(cu).cuda(), pool_t, activation="silu")
+    out, fin = kda.chunk_prefill(q, k, v, to_dev(g), to_dev(beta), t.from_numpy(cu).cuda(),
+                                 initial_state=to_dev(s0))
+    t.cuda.synchronize()
+    (qr, kr, vr), _, _ = oracle.short_conv(*xs, w, cu, pool, None, activation="silu")
+    qb, kb, vb = (bf16_bits(a.astype(np.float32)) for a in (qr, kr, vr))
+    o_ref, f_ref = oracle.run(qb, kb, vb, g, beta, cu, initial_state=s0)
+    assert rel_l2(out.float().cpu().numpy(), o_ref) <= OUT_TOL
+    assert rel_l2(fin.cpu().numpy(), f_ref) <= STATE_TOL
