@@ -15,7 +15,7 @@
 // after which the window holds x_{L-3}, x_{L-2}, x_{L-1}: the last three rows
 // of [old taps ; the sequence's L rows].
 //
-// kda_conv_kernel: one warp per (block of 32 rows, head, stream).  Lane l owns
+// kda_conv_kernel: one warp per (block of 64 rows, head, stream).  Lane l owns
 // channels 4l .. 4l+3 of the head and holds their 16 weights.  Rows go in
 // groups of four over a window of seven rows in registers (the three before
 // the group and the group), with the next group's loads in flight; each row is
@@ -35,7 +35,7 @@
 namespace kda {
 namespace {
 
-constexpr int kConvRows = 32;    // rows per warp
+constexpr int kConvRows = 64;    // rows per warp
 constexpr int kConvWarps = 4;    // warps per CTA
 
 struct ConvParams {

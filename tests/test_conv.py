@@ -146,12 +146,13 @@ def test_conv_packed16_8192_h32():
 @pytest.mark.parametrize("seed", [16, 17, 18])
 def test_conv_short_sequences_at_every_block_offset(seed):
     """Many sequences of 1 to 6 rows among longer ones, so that sequences start
-    at every offset within the kernel's 32-row blocks, the first three rows of
-    a sequence (which read its window) included."""
+    at (nearly) every offset within the kernel's 64-row blocks, the last three
+    rows before a block edge included (a sequence starting there has its
+    window read by the warp of the earlier block only)."""
     rng = np.random.default_rng(seed)
-    lens = [int(x) for x in rng.integers(1, 7, 90)]
-    for pos in (10, 40, 70):
-        lens[pos] = int(rng.integers(30, 70))
+    lens = [int(x) for x in rng.integers(1, 7, 200)]
+    for pos in (10, 60, 120, 170):
+        lens[pos] = int(rng.integers(30, 140))
     H = 2
     num_slots = len(lens) + 5
     xs, w, pool, cu = draw(lens, H, num_slots, seed=seed)
