@@ -510,7 +510,7 @@ def run_gpu_arm(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": kernel_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64; recipe in DESIGN.md)",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64 inputs, workload shapes of the packed prefill)",
         "config": {"workload": WORKLOAD, "N": w.N, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "lengths": w.lengths, "initial_state": "N(0,0.02) fp32", "final_state": True,
                    "l2": "inputs larger than L2: 2 rotating input sets of %.0f MB" % (alg / 1e6),
