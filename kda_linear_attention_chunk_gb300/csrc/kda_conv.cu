@@ -19,8 +19,8 @@
 // channels 4l .. 4l+3 of the head and holds their 16 weights.  Rows go in
 // groups of four over a window of seven rows in registers (the three before
 // the group and the group), with the next group's loads in flight; each row is
-// one 256-byte load and one 256-byte store per warp.  The L2 norm is a warp
-// reduction.  The kernel is bound by instruction issue rather than by memory,
+// one 256-byte load and one 256-byte store per warp.  The L2 norms of a
+// group's four rows are one butterfly across the warp (ten shuffles).  The kernel is bound by instruction issue rather than by memory,
 // so the per-row code is kept short (no per-row register shifts; SiLU through
 // one tanh).  Only the warp that holds a sequence's first row reads the
 // sequence's window (for that row's three predecessors), so that warp also
@@ -192,30 +192,44 @@ __global__ void __launch_bounds__(kConvWarps * 32, 6) kda_conv_kernel(ConvParams
                 ld[i] = g + 4 + i < seg_end ? __ldg(reinterpret_cast<const uint2 *>(xrow + (4 + i) * HC))
                                             : make_uint2(0u, 0u);
             }
+            float y[4][4];                        // rows g .. g+3 (past the segment: zeros, not stored)
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-                if (g + i >= seg_end) break;
-                float y[4];
+            for (int i = 0; i < 4; i++)
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
                     float a = wt[c][0] * xa[i][c];
                     a = fmaf(wt[c][1], xa[i + 1][c], a);
                     a = fmaf(wt[c][2], xa[i + 2][c], a);
                     a = fmaf(wt[c][3], xa[i + 3][c], a);
-                    y[c] = p.act ? silu(a) : a;
+                    y[i][c] = p.act ? silu(a) : a;
                 }
-                float scale = 1.f;
-                if (s < 2) {                      // q and k: unit L2 norm per head
-                    float ss = y[0] * y[0];
-                    ss = fmaf(y[1], y[1], ss);
-                    ss = fmaf(y[2], y[2], ss);
-                    ss = fmaf(y[3], y[3], ss);
+            float sc[4] = {1.f, 1.f, 1.f, 1.f};
+            if (s < 2) {
+                // the four rows' squared norms in one butterfly: lanes 0-15 gather rows
+                // 0 and 1, lanes 16-31 rows 2 and 3, then bit 3 of the lane picks one
+                // row; lane 16 r1 + 8 r0 ends up with row 2 r1 + r0
+                float ss[4];
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                    scale = rsqrtf(ss + p.eps);
+                for (int i = 0; i < 4; i++) {
+                    ss[i] = y[i][0] * y[i][0];
+                    ss[i] = fmaf(y[i][1], y[i][1], ss[i]);
+                    ss[i] = fmaf(y[i][2], y[i][2], ss[i]);
+                    ss[i] = fmaf(y[i][3], y[i][3], ss[i]);
                 }
-                *reinterpret_cast<uint2 *>(yrow + i * HC) =
-                    make_uint2(pack_bf2(y[0] * scale, y[1] * scale), pack_bf2(y[2] * scale, y[3] * scale));
+                const bool h16 = lane & 16, h8 = lane & 8;
+                const float a0 = (h16 ? ss[2] : ss[0]) + __shfl_xor_sync(0xffffffffu, h16 ? ss[0] : ss[2], 16);
+                const float a1 = (h16 ? ss[3] : ss[1]) + __shfl_xor_sync(0xffffffffu, h16 ? ss[1] : ss[3], 16);
+                float b = (h8 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, h8 ? a0 : a1, 8);
+#pragma unroll
+                for (int o = 4; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+#pragma unroll
+                for (int i = 0; i < 4; i++) sc[i] = rsqrtf(__shfl_sync(0xffffffffu, b, 16 * (i >> 1) + 8 * (i & 1)) + p.eps);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                if (g + i >= seg_end) break;
+                *reinterpret_cast<uint2 *>(yrow + i * HC) = make_uint2(pack_bf2(y[i][0] * sc[i], y[i][1] * sc[i]),
+                                                                       pack_bf2(y[i][2] * sc[i], y[i][3] * sc[i]));
             }
 #pragma unroll
             for (int j = 0; j < 3; j++)
