@@ -201,6 +201,47 @@ int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
                uint16_t *out, int N, int H, int dk, int dv, void *stream);
 
 /*
+ * kda_decode_conv -- kda_decode with the short conv + L2-norm prologue of
+ * kda_short_conv fused in front of it (kern-k3-pp-prefill README, section
+ * "D inside SGLang": the packed decode step runs the conv on the step's rows
+ * with the windows in the engine's pool, then the recurrence).  For each row n
+ * (one token of sequence n) and head h, with the window of conv_slots[n]:
+ *
+ *     q, k, v  = the conv of kda_short_conv over [window taps 0..2 ; x_n]
+ *                (optional SiLU; q and k scaled to unit L2 norm over the
+ *                head's channels with eps as there), kept in fp32;
+ *     then the kda_decode step on state_pool[state_slots[n]][h] with those
+ *     q, k, v and g, beta, writing out[n][h];
+ *     the window becomes [taps 1, 2 ; x_n].
+ *
+ * One kernel: the four CTAs that share a (sequence, head) form a cluster and
+ * rewrite the window only after all four have read it.  Results differ from
+ * kda_short_conv followed by kda_decode only in that q, k and v are not
+ * rounded to bf16 between the two.
+ *
+ *   xq, xk, xv   bf16 bits [N][H][dk|dv]: the step's projections.
+ *   conv_weight  fp32 [3][H*128][4], as for kda_short_conv.
+ *   conv_slots   int32 [N] or NULL (entry n): the window entry of row n.
+ *   conv_pool    bf16 bits [conv_num_slots][3 taps][3 streams][H*128], the
+ *                layout kda_short_conv reads and writes; updated in place.
+ *   g, beta, state_slots, state_pool, num_slots, out: as for kda_decode.
+ *   activation, eps: as for kda_short_conv.
+ *   N, H         rows (sequences) >= 1, heads >= 1; dk = dv = 128.
+ * A row whose state id or window id is -1 is padding: nothing of it is
+ * computed or written (neither its state, its window nor its out row).  An id
+ * outside [-1, num_slots) (or [-1, conv_num_slots)) is treated like -1 and
+ * sets bit 8 of the device error word.  Valid ids must be distinct within
+ * each table.  Tensor pointers must be 16-byte aligned (beta and the slot
+ * tables 4-byte); the pools and out must not overlap an input or each other.
+ * Returns a kda_status.
+ */
+int kda_decode_conv(const uint16_t *xq, const uint16_t *xk, const uint16_t *xv,
+                    const float *conv_weight, const int32_t *conv_slots, uint16_t *conv_pool,
+                    int conv_num_slots, const float *g, const float *beta,
+                    const int32_t *state_slots, float *state_pool, int num_slots, uint16_t *out,
+                    int N, int H, int dk, int dv, int activation, float eps, void *stream);
+
+/*
  * kda_fold_commit -- the state commit of a speculative decoding round (the
  * ReplaySSM exact fold: SGLang PR #32890, prhub report section "实现拆解",
  * item 3 and the speculative-decoding file list).  A verify pass scores W

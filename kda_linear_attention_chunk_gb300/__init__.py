@@ -21,7 +21,7 @@ KDA_NOALLOC_MAX_SEQS = 16384
 
 EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error",
             "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode", "kda_fold_commit",
-            "kda_short_conv")
+            "kda_short_conv", "kda_decode_conv")
 ERR_BAD_SLOT = 8   # device error word bit: a state slot id outside [-1, num_slots)
 ERR_BAD_ACCEPTED = 16   # device error word bit: an accepted count outside [0, window]
 
@@ -56,6 +56,8 @@ def load(path: str = LIB_PATH):
     lib.kda_fold_commit.restype = I
     lib.kda_short_conv.argtypes = [P, P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, ctypes.c_float, P]
     lib.kda_short_conv.restype = I
+    lib.kda_decode_conv.argtypes = [P, P, P, P, P, P, I, P, P, P, P, I, P, I, I, I, I, I, ctypes.c_float, P]
+    lib.kda_decode_conv.restype = I
     lib.kda_status_string.argtypes = [I]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), I]
@@ -120,6 +122,14 @@ def kda_short_conv(xq, xk, xv, conv_weight, cu_seqlens, conv_slots, conv_pool, n
     """Raw C-ABI call: short conv + L2 norm prologue, conv windows in a slot-addressed pool."""
     return load().kda_short_conv(xq, xk, xv, conv_weight, cu_seqlens, conv_slots, conv_pool, num_slots, q_out,
                                  k_out, v_out, N, T, H, d, activation, eps, stream)
+
+
+def kda_decode_conv(xq, xk, xv, conv_weight, conv_slots, conv_pool, conv_num_slots: int, g, beta, state_slots,
+                    state_pool, num_slots: int, out, N: int, H: int, dk: int, dv: int, activation: int, eps: float,
+                    stream) -> int:
+    """Raw C-ABI call: the decode step with the short conv fused in front of it."""
+    return load().kda_decode_conv(xq, xk, xv, conv_weight, conv_slots, conv_pool, conv_num_slots, g, beta,
+                                  state_slots, state_pool, num_slots, out, N, H, dk, dv, activation, eps, stream)
 
 
 def device_error(reset: bool = False) -> int:
@@ -323,3 +333,52 @@ def short_conv(xq, xk, xv, conv_weight, cu_seqlens, conv_pool, conv_slots=None, 
     if st != KDA_OK:
         raise KdaError(st, "kda_short_conv")
     return q, k, v
+
+
+def decode_conv(xq, xk, xv, conv_weight, conv_pool, g, beta, state_pool, conv_slots=None, state_slots=None,
+                activation: str = "silu", eps: float = 1e-6, out=None, stream=None):
+    """The decode step with the short conv + L2 norm prologue fused in front of
+    it, on torch CUDA tensors.
+
+    xq, xk, xv: [N][H][128] bfloat16 (row n = sequence n's new token, before
+    the conv); conv_weight: [3][H*128][4] float32; conv_pool:
+    [conv_num_slots][3][3][H*128] bfloat16 and state_pool:
+    [num_slots][H][128][128] float32, both updated in place; conv_slots,
+    state_slots: [N] int32 (-1 = padded row, skipped) or None for entry n;
+    g: [N][H][128] float32; beta: [N][H] float32.  Returns out [N][H][128]
+    bfloat16 (rows of padded sequences keep what ``out`` held).
+    """
+    import torch
+
+    N, H, d = xq.shape
+    tensors = [("xq", xq), ("xk", xk), ("xv", xv), ("conv_weight", conv_weight), ("conv_pool", conv_pool),
+               ("g", g), ("beta", beta), ("state_pool", state_pool)]
+    for name, t in (("conv_slots", conv_slots), ("state_slots", state_slots)):
+        if t is not None:
+            tensors.append((name, t))
+            if t.dtype != torch.int32 or tuple(t.shape) != (N,):
+                raise ValueError(f"{name} must be int32 [N]")
+    for name, t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if xq.dtype != torch.bfloat16 or xk.dtype != torch.bfloat16 or xv.dtype != torch.bfloat16:
+        raise ValueError("decode_conv takes bfloat16 projections")
+    if conv_weight.dtype != torch.float32 or tuple(conv_weight.shape) != (3, H * d, 4):
+        raise ValueError("conv_weight must be float32 [3][H*d][4]")
+    if conv_pool.dtype != torch.bfloat16 or tuple(conv_pool.shape[1:]) != (3, 3, H * d):
+        raise ValueError("conv_pool must be bfloat16 [num_slots][3][3][H*d]")
+    if state_pool.dtype != torch.float32 or tuple(state_pool.shape[1:]) != (H, d, d):
+        raise ValueError("state_pool must be float32 [num_slots][H][dv][dk]")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    if out is None:
+        out = torch.empty((N, H, d), dtype=xq.dtype, device=xq.device)
+    s = stream if stream is not None else torch.cuda.current_stream(xq.device)
+    handle = int(s.cuda_stream) if hasattr(s, "cuda_stream") else int(s)
+    st = kda_decode_conv(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(conv_weight), _ptr(conv_slots), _ptr(conv_pool),
+                         int(conv_pool.shape[0]), _ptr(g), _ptr(beta), _ptr(state_slots), _ptr(state_pool),
+                         int(state_pool.shape[0]), _ptr(out), N, H, d, d, ACTIVATIONS[activation], float(eps),
+                         handle)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_conv")
+    return out

@@ -265,6 +265,53 @@ int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
     return kda::launch_kda_decode_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+int kda_decode_conv(const uint16_t *xq, const uint16_t *xk, const uint16_t *xv, const float *conv_weight,
+                    const int32_t *conv_slots, uint16_t *conv_pool, int conv_num_slots, const float *g,
+                    const float *beta, const int32_t *state_slots, float *state_pool, int num_slots, uint16_t *out,
+                    int N, int H, int dk, int dv, int activation, float eps, void *stream)
+{
+    if (!xq || !xk || !xv || !conv_weight || !conv_pool || !g || !beta || !state_pool || !out) return KDA_ERR_NULL;
+    if (N < 1 || H < 1 || dk < 1 || dv < 1 || num_slots < 1 || conv_num_slots < 1) return KDA_ERR_SHAPE;
+    if ((!state_slots && num_slots < N) || (!conv_slots && conv_num_slots < N)) return KDA_ERR_SHAPE;
+    if (activation != 0 && activation != 1) return KDA_ERR_SHAPE;
+    if (!(eps >= 0.f && eps <= 3.0e38f)) return KDA_ERR_SHAPE;   // also rejects NaN
+    if ((size_t)N * (size_t)H > 0x1fffffffu || (size_t)num_slots * (size_t)H > 0x7fffffffu ||
+        (size_t)conv_num_slots * (size_t)H * 128 * 9 * 2 >= ((size_t)1 << 40))
+        return KDA_ERR_SHAPE;
+    if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+    const void *aligned_ptrs[] = {xq, xk, xv, conv_weight, conv_pool, g, out, state_pool};
+    for (const void *p : aligned_ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGN;
+    if (((uintptr_t)beta & 3u) || ((uintptr_t)state_slots & 3u) || ((uintptr_t)conv_slots & 3u))
+        return KDA_ERR_ALIGN;
+    const size_t rows = (size_t)N * H;
+    const Range in[] = {range_of(xq, rows * 256), range_of(xk, rows * 256), range_of(xv, rows * 256),
+                        range_of(conv_weight, (size_t)3 * H * 128 * 4 * sizeof(float)),
+                        range_of(conv_slots, (size_t)N * sizeof(int32_t)),
+                        range_of(g, rows * 128 * sizeof(float)), range_of(beta, rows * sizeof(float)),
+                        range_of(state_slots, (size_t)N * sizeof(int32_t))};
+    const Range rw[] = {range_of(conv_pool, (size_t)conv_num_slots * 9 * H * 128 * 2),
+                        range_of(state_pool, (size_t)num_slots * H * 128 * 128 * sizeof(float)),
+                        range_of(out, rows * 256)};
+    for (int i = 0; i < 3; i++) {
+        for (const Range &r : in)
+            if (overlap(rw[i], r)) return KDA_ERR_ALIAS;
+        for (int j = i + 1; j < 3; j++)
+            if (overlap(rw[i], rw[j])) return KDA_ERR_ALIAS;
+    }
+    DevInfo *d = nullptr;
+    int st;
+    if ((st = device_info(&d)) != KDA_OK) return st;
+    kda::DecodeConvArgs a;
+    a.xq = xq; a.xk = xk; a.xv = xv; a.conv_weight = conv_weight;
+    a.conv_slots = conv_slots; a.conv_pool = conv_pool; a.conv_num_slots = conv_num_slots;
+    a.g = g; a.beta = beta; a.state_slots = state_slots; a.state_pool = state_pool; a.num_slots = num_slots;
+    a.out = out; a.N = N; a.H = H; a.activation = activation; a.eps = eps;
+    a.stream = (cudaStream_t)stream;
+    a.err_word = d->err;
+    return kda::launch_kda_decode_conv_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 int kda_fold_commit(const uint16_t *k, const uint16_t *v, const float *g, const float *beta, const int32_t *accepted,
                     const int32_t *state_slots, float *state_pool, int num_slots, int N, int W, int H, int dk, int dv,
                     void *stream)

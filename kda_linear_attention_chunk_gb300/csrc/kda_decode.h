@@ -21,6 +21,24 @@ struct DecodeArgs {
 
 cudaError_t launch_kda_decode_bf16_d128(const DecodeArgs &a);
 
+// the decode step with the short conv fused in front of it, bf16, d = 128
+struct DecodeConvArgs {
+    const void *xq, *xk, *xv;       // [N][H][128] bf16 projections
+    const float *conv_weight;       // [3][H*128][4]
+    const int32_t *conv_slots;      // [N] or nullptr (entry n)
+    void *conv_pool;                // [conv_num_slots][3][3][H*128] bf16
+    const float *g, *beta;          // [N][H][128], [N][H]
+    const int32_t *state_slots;     // [N] or nullptr (entry n)
+    float *state_pool;              // [num_slots][H][128][128]
+    void *out;                      // [N][H][128] bf16
+    int N, H, num_slots, conv_num_slots, activation;
+    float eps;
+    cudaStream_t stream;
+    int *err_word;
+};
+
+cudaError_t launch_kda_decode_conv_bf16_d128(const DecodeConvArgs &a);
+
 // device error word bit of the fold (bits 1-8 are listed in kda_common.cuh):
 // an accepted count outside [0, window] (clamped)
 enum : int { kErrBadAccepted = 16 };

@@ -212,3 +212,40 @@ def test_conv_empty_rows_allow_null_tensors(kda_lib):
 def test_conv_valid_call_passes_validation(kda_lib):
     assert call_conv() == kda.KDA_ERR_DEVICE
     assert call_conv(slots=0, num_slots=3, act=0, eps=0.0) == kda.KDA_ERR_DEVICE
+
+
+def call_decode_conv(**over):
+    N, H = 3, 2
+    xb = N * H * 128 * 2
+    args = dict(xq=A, xk=A + xb, xv=A + 2 * xb, w=A + 3 * xb, cslots=A + 3 * xb + 16384, cpool=A + (8 << 20),
+                cnum=5, g=A + (1 << 20), beta=A + (1 << 20) + 8192, slots=A + (1 << 20) + 12288,
+                pool=A + (16 << 20), num_slots=4, out=A + (2 << 20), N=N, H=H, dk=128, dv=128, act=1, eps=1e-6,
+                stream=0)
+    args.update(over)
+    order = ["xq", "xk", "xv", "w", "cslots", "cpool", "cnum", "g", "beta", "slots", "pool", "num_slots", "out",
+             "N", "H", "dk", "dv", "act", "eps", "stream"]
+    return kda.kda_decode_conv(*[args[n] for n in order])
+
+
+def test_decode_conv_validation_statuses(kda_lib):
+    assert call_decode_conv(xq=0) == kda.KDA_ERR_NULL
+    assert call_decode_conv(cpool=0) == kda.KDA_ERR_NULL
+    assert call_decode_conv(pool=0) == kda.KDA_ERR_NULL
+    assert call_decode_conv(N=0) == kda.KDA_ERR_SHAPE
+    assert call_decode_conv(cnum=0) == kda.KDA_ERR_SHAPE
+    assert call_decode_conv(cslots=0, cnum=2) == kda.KDA_ERR_SHAPE          # entry n needs conv_num_slots >= N
+    assert call_decode_conv(slots=0, num_slots=2) == kda.KDA_ERR_SHAPE      # and num_slots >= N
+    assert call_decode_conv(act=2) == kda.KDA_ERR_SHAPE
+    assert call_decode_conv(eps=float("nan")) == kda.KDA_ERR_SHAPE
+    assert call_decode_conv(dk=64, dv=64) == kda.KDA_ERR_UNSUPPORTED
+    assert call_decode_conv(xk=A + 3 * 2 * 128 * 2 + 8) == kda.KDA_ERR_ALIGN
+    assert call_decode_conv(cslots=A + 3 * 3 * 2 * 128 * 2 + 16386) == kda.KDA_ERR_ALIGN
+    assert call_decode_conv(cpool=A) == kda.KDA_ERR_ALIAS                   # window pool over xq
+    assert call_decode_conv(out=A + (1 << 20)) == kda.KDA_ERR_ALIAS         # out over g
+    assert call_decode_conv(pool=A + (8 << 20)) == kda.KDA_ERR_ALIAS        # state pool over the window pool
+
+
+@pytest.mark.skipif(_has_gpu(), reason="on a GPU box a valid call would launch on these fake addresses")
+def test_decode_conv_valid_call_passes_validation(kda_lib):
+    assert call_decode_conv() == kda.KDA_ERR_DEVICE
+    assert call_decode_conv(slots=0, cslots=0, num_slots=3, cnum=3) == kda.KDA_ERR_DEVICE
