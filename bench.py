@@ -206,6 +206,79 @@ def measure_decode(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
                          "traffic": recorded_traffic("decode64_h32", DECODE_SOURCES)}}
 
 
+def decode_conv_bytes(n: int, h: int) -> int:
+    """Algorithmic bytes of one fused conv + decode step: the decode step's
+    (the projections in place of q, k, v), plus per sequence its window entry
+    read and written (3 taps x 3 streams x H x 128 bf16 each way), the filters
+    (3 x H x 128 x 4 fp32) and the window slot table."""
+    return decode_bytes(n, n, h) + n * 2 * 9 * h * 128 * 2 + 3 * h * 128 * 4 * 4 + 4 * n
+
+
+def measure_decode_conv(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
+    """kda_decode_conv (SiLU) on the decode step's shape: state and window pools
+    of 2 x DECODE_N entries, the steps alternating between two pairs of slot
+    tables over disjoint halves of them (134 MB of states each, above L2)."""
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+    n, h = DECODE_N, DECODE_H
+    w = syn.Workload("decode_conv64_h32", [1] * n, H=h, dk=128, dv=128, seed=78)
+    x = syn.draw(w)
+    d = {k: (torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16
+             else torch.from_numpy(v)).cuda() for k, v in x.items()}
+    rng = np.random.default_rng(78)
+    pool = torch.from_numpy((0.02 * rng.standard_normal((2 * n, h, 128, 128))).astype(np.float32)).cuda()
+    cpool = torch.from_numpy(rng.standard_normal((2 * n, 3, 3, h * 128)).astype(np.float32)).to(torch.bfloat16).cuda()
+    cw = torch.from_numpy((0.5 * rng.standard_normal((3, h * 128, 4))).astype(np.float32)).cuda()
+    perm = rng.permutation(2 * n).astype(np.int32)
+    tables = [torch.from_numpy(np.sort(perm[:n])).cuda(), torch.from_numpy(np.sort(perm[n:])).cuda()]
+    ctables = [tables[1].flip(0).contiguous(), tables[0].flip(0).contiguous()]
+    out = torch.empty((n, h, 128), dtype=torch.bfloat16, device="cuda")
+
+    def step(i):
+        kda.decode_conv(d["q"], d["k"], d["v"], cw, cpool, d["g"], d["beta"], pool, conv_slots=ctables[i % 2],
+                        state_slots=tables[i % 2], activation="silu", out=out, stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    # the same step as two calls: the short conv on the N one-row sequences, then
+    # the decode step on its bf16 q, k, v
+    cu1 = torch.arange(n + 1, dtype=torch.int32, device="cuda")
+    qkv = tuple(torch.empty_like(d["q"]) for _ in range(3))
+
+    def two_calls(i):
+        kda.short_conv(d["q"], d["k"], d["v"], cw, cu1, cpool, conv_slots=ctables[i % 2], activation="silu",
+                       out=qkv, stream=stream)
+        kda.decode(qkv[0], qkv[1], qkv[2], d["g"], d["beta"], pool, state_slots=tables[i % 2], out=out,
+                   stream=stream)
+
+    for i in range(warmup):
+        two_calls(i)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(steps):
+        two_calls(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms2 = ev0.elapsed_time(ev1) / steps
+    alg = decode_conv_bytes(n, h)
+    peak, peak_kind = peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    return {"workload": "decode_conv64_h32", "kernel": "kda_decode_conv_kernel", "N": n, "H": h, "steps": steps,
+            "activation": "silu", "us_per_step": ms * 1e3, "tokens_per_s": n / (ms / 1e3),
+            "two_calls_us_per_step": ms2 * 1e3,
+            "l2": "2 pairs of slot tables over disjoint halves of 2 x 64-entry state and window pools",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": alg,
+                         "traffic": recorded_traffic("decode_conv64_h32", DECODE_SOURCES)}}
+
+
 def conv_bytes(lengths, h: int) -> int:
     """Algorithmic bytes of one short-conv prologue call: per row-head the q, k,
     v projections in and q, k, v out (256 B each); the filters (3 x H x 128 x 4
@@ -492,6 +565,7 @@ def run_gpu_arm(args):
     decode = measure_decode(torch, np, kda, stream) if not args.no_decode else None
     fold = measure_fold(torch, np, kda, stream) if not args.no_decode else None
     conv = measure_conv(torch, np, kda, stream) if not args.no_decode else None
+    decode_conv = measure_decode_conv(torch, np, kda, stream) if not args.no_decode else None
     configs = measure_configs(torch, np, kda, stream) if not args.no_configs else None
     assert kda.device_error() == 0, "device error word set during the bench"
 
@@ -531,6 +605,8 @@ def run_gpu_arm(args):
         line["fold"] = fold
     if conv is not None:
         line["conv"] = conv
+    if decode_conv is not None:
+        line["decode_conv"] = decode_conv
     if configs is not None:
         line["configs"] = configs
     if not args.no_cpu_baseline:

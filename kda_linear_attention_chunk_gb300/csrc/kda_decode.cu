@@ -168,7 +168,7 @@ __device__ __forceinline__ float conv4(float4 w, uint16_t t0, uint16_t t1, uint1
     return act ? y / (1.f + dec_ex2(-y * kDecLog2e)) : y;
 }
 
-__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kDecThreads, 4) kda_decode_conv_kernel(DecodeConvParams p)
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kDecThreads, 5) kda_decode_conv_kernel(DecodeConvParams p)
 {
     __shared__ float4 sa[32], sk[32], sq[32];   // exp(g), k, q of this (sequence, head), 128 each
     __shared__ float sv[kDecRows];              // v of this quarter's value rows
@@ -183,6 +183,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kDecThreads, 4) kda_
     const size_t row = (size_t)n * p.H + h;
     const size_t C = (size_t)p.H * 128;
     const int tid = threadIdx.x, st_ = tid >> 7, c = tid & 127;   // stream (0 q, 1 k) and channel
+    // the state rows go out first: they do not depend on the conv
+    const int vr = kDecRows * vq + (tid >> 3), qe = tid & 7;
+    float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
+    float4 s[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) s[j] = st[8 * j + qe];
+    const float beta = p.beta[row];
     uint16_t *win = p.conv_pool + (size_t)cslot * 9 * C;       // [tap][stream][H*128]
     const size_t ch = (size_t)h * 128 + c;
     // q or k of channel c; the taps this thread carries into the new window
@@ -208,12 +215,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kDecThreads, 4) kda_
     for (int o = 16; o > 0; o >>= 1) y2 += __shfl_xor_sync(0xffffffffu, y2, o);
     if ((tid & 31) == 0) red[tid >> 5] = y2;
     if (tid < 128) reinterpret_cast<float *>(sa)[tid] = dec_ex2(p.g[row * 128 + tid] * kDecLog2e);
-    const int vr = kDecRows * vq + (tid >> 3), qe = tid & 7;
-    const float beta = p.beta[row];
-    float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
-    float4 s[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) s[j] = st[8 * j + qe];
     __syncthreads();
     {
         const float *r4 = red + 4 * st_;
