@@ -35,7 +35,7 @@
 namespace kda {
 namespace {
 
-constexpr int kConvRows = 64;    // rows per warp
+constexpr int kConvRows = 64;    // rows per warp when the sequences are long (see conv_rows)
 constexpr int kConvWarps = 4;    // warps per CTA
 
 struct ConvParams {
@@ -45,9 +45,20 @@ struct ConvParams {
     const int32_t *cu, *slots;
     uint16_t *pool;
     int N, T, H, num_slots, act;
+    int rows;                    // rows per warp
     float eps;
     int *err;
 };
+
+// Rows per warp: a warp walks its rows in order and pays two dependent loads
+// (slot id, window) at each sequence start, so short sequences get short
+// blocks (measured: 64 one-row sequences at H = 32 took 115 us in 64-row
+// blocks); long ones keep 64-row blocks.  Any size >= 4 keeps at most one
+// block edge among a sequence's first three rows.
+inline int conv_rows(long long T, int N)
+{
+    return T >= 48LL * N ? kConvRows : T >= 12LL * N ? 16 : 4;
+}
 
 // stream s of a 3-array kept in the kernel parameters (a runtime index would
 // copy the parameter block to local memory)
@@ -116,9 +127,9 @@ __global__ void __launch_bounds__(kConvWarps * 32, 6) kda_conv_kernel(ConvParams
             }
         }
     }
-    const int h = item % p.H, s = (item / p.H) % 3, b32 = (item / p.H / 3) * kConvRows;
+    const int h = item % p.H, s = (item / p.H) % 3, b32 = (item / p.H / 3) * p.rows;
     if (b32 >= p.T) return;
-    const int t0 = block_edge(p, b32, lane), t1 = block_edge(p, b32 + kConvRows, lane);
+    const int t0 = block_edge(p, b32, lane), t1 = block_edge(p, b32 + p.rows, lane);
     const size_t HC = (size_t)p.H * 128;         // elements per row of a stream
     const int gc = h * 128 + 4 * lane;            // this lane's first channel
     float wt[4][4];                               // [channel][tap]
@@ -257,7 +268,8 @@ cudaError_t launch_kda_conv_bf16_d128(const ConvArgs &a)
     p.act = a.activation;
     p.eps = a.eps;
     p.err = a.err_word;
-    const long long items = (long long)((a.T + kConvRows - 1) / kConvRows) * 3 * a.H;
+    p.rows = conv_rows(a.T, a.N);
+    const long long items = (long long)((a.T + p.rows - 1) / p.rows) * 3 * a.H;
     const long long blocks = items > 0 ? (items + kConvWarps - 1) / kConvWarps : 1;   // block 0 checks the ids
     kda_conv_kernel<<<(unsigned)blocks, kConvWarps * 32, 0, a.stream>>>(p);
     return cudaGetLastError();

@@ -189,3 +189,24 @@ def test_conv_then_prefill_matches_the_oracle_chain():
     o_ref, f_ref = oracle.run(qb, kb, vb, g, beta, cu, initial_state=s0)
     assert rel_l2(out.float().cpu().numpy(), o_ref) <= OUT_TOL
     assert rel_l2(fin.cpu().numpy(), f_ref) <= STATE_TOL
+
+
+@pytest.mark.parametrize("pattern", ["one_row", "about_20_rows"])
+def test_conv_short_blocks_for_short_sequences(pattern):
+    """Short mean lengths run in short row blocks (4 rows per warp for one-row
+    sequences, 16 for about 20): parity, padding and windows as for long ones."""
+    rng = np.random.default_rng(20 if pattern == "one_row" else 21)
+    lens = [1] * 64 if pattern == "one_row" else [int(x) for x in rng.integers(1, 40, 50)]
+    H = 4
+    num_slots = len(lens) + 3
+    xs, w, pool, cu = draw(lens, H, num_slots, seed=22)
+    slots = rng.permutation(num_slots)[:len(lens)].astype(np.int32)
+    slots[5] = -1
+    pool_t = dev_bf16(pool)
+    got = gpu_conv(xs, w, pool_t, cu, slots)
+    ref, new_pool, _ = oracle.short_conv(*xs, w, cu, pool, slots)
+    live = ~np.isnan(ref[0][:, 0, 0])
+    for g, r in zip(got, ref):
+        assert np.isnan(g[~live]).all()
+        assert rel_l2(g[live], r[live]) <= CONV_TOL
+    np.testing.assert_array_equal(host_bits(pool_t), new_pool)
