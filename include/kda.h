@@ -214,8 +214,8 @@ int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
  *     q, k, v and g, beta, writing out[n][h];
  *     the window becomes [taps 1, 2 ; x_n].
  *
- * One kernel: the four CTAs that share a (sequence, head) form a cluster and
- * rewrite the window only after all four have read it.  Results differ from
+ * One kernel: one CTA per (sequence, head) computes that head's conv once,
+ * steps all its value rows and rewrites its channels of the window.  Results differ from
  * kda_short_conv followed by kda_decode only in that q, k and v are not
  * rounded to bf16 between the two.
  *

@@ -135,15 +135,16 @@ __global__ void __launch_bounds__(kDecThreads, 5) kda_decode_kernel(DecodeParams
 }
 
 // ---------------------------------------------------------------------------
-// The decode step with the short conv fused in front of it.  The four CTAs of
-// one (sequence, head) -- one per quarter of the value rows -- form a cluster.
-// Each computes the token's q and k over all 128 channels (the 4-tap conv over
-// the window's three rows and the new projection row, optional SiLU, unit L2
-// norm per head) and v over its own 32 channels, then runs token_step exactly
-// as kda_decode_kernel does.  The window is shared by the four: each CTA
-// arrives on the cluster barrier once it has read the window, and only after
-// the barrier completes rewrites its own quarter of the channels (taps 1 and 2
-// move down, the projection row becomes tap 2).
+// The decode step with the short conv fused in front of it.  One CTA of 1024
+// threads per (sequence, head) owns all 128 value rows (eight threads a row,
+// as in kda_decode_kernel, so token_step runs unchanged) and so alone reads
+// and rewrites the head's channels of the sequence's window.  Threads 0-255
+// compute q and k over the 128 channels (the 4-tap conv over the window's
+// three rows and the new projection row, optional SiLU, unit L2 norm per
+// head), threads 256-383 v, threads 384-511 exp(g); every thread then steps
+// its value row.  After the block's first barrier every read of the window is
+// done, and the new window (taps 1 and 2 move down, the projection row
+// becomes tap 2) is written.
 // ---------------------------------------------------------------------------
 struct DecodeConvParams {
     const uint16_t *xq, *xk, *xv;  // [N][H][128] bf16: this step's projections
@@ -168,78 +169,68 @@ __device__ __forceinline__ float conv4(float4 w, uint16_t t0, uint16_t t1, uint1
     return act ? y / (1.f + dec_ex2(-y * kDecLog2e)) : y;
 }
 
-__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kDecThreads, 5) kda_decode_conv_kernel(DecodeConvParams p)
+constexpr int kDcThreads = 1024;   // 128 value rows x 8 threads
+
+__global__ void __launch_bounds__(kDcThreads, 1) kda_decode_conv_kernel(DecodeConvParams p)
 {
     __shared__ float4 sa[32], sk[32], sq[32];   // exp(g), k, q of this (sequence, head), 128 each
-    __shared__ float sv[kDecRows];              // v of this quarter's value rows
+    __shared__ float sv[128];                   // v
     __shared__ float red[8];                    // per-warp sums of y^2 (warps 0-3: q, 4-7: k)
-    const int rh = blockIdx.x >> 2, vq = blockIdx.x & 3;   // (sequence, head), quarter of the value rows
+    const int rh = blockIdx.x;                  // (sequence, head)
     const int n = rh / p.H, h = rh % p.H;
-    // the same decision in all four CTAs of the cluster (they read the same ids),
-    // so either all of them reach the cluster barrier or none does
     const int slot = decode_slot(p.slots, n, p.num_slots, p.err);
     const int cslot = decode_slot(p.conv_slots, n, p.conv_num_slots, p.err);
     if (slot < 0 || cslot < 0) return;   // padded row: nothing is computed or written
     const size_t row = (size_t)n * p.H + h;
     const size_t C = (size_t)p.H * 128;
-    const int tid = threadIdx.x, st_ = tid >> 7, c = tid & 127;   // stream (0 q, 1 k) and channel
-    // the state rows go out first: they do not depend on the conv
-    const int vr = kDecRows * vq + (tid >> 3), qe = tid & 7;
+    const int tid = threadIdx.x;
+    // this thread's state row goes out first: it does not depend on the conv
+    const int vr = tid >> 3, qe = tid & 7;
     float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
     float4 s[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) s[j] = st[8 * j + qe];
     const float beta = p.beta[row];
     uint16_t *win = p.conv_pool + (size_t)cslot * 9 * C;       // [tap][stream][H*128]
+    const int part = tid >> 7, c = tid & 127;                  // 0 q, 1 k, 2 v, 3 g; channel
     const size_t ch = (size_t)h * 128 + c;
-    // q or k of channel c; the taps this thread carries into the new window
-    const uint16_t t1 = win[(3 + st_) * C + ch], t2 = win[(6 + st_) * C + ch];
-    const uint16_t xn = (st_ ? p.xk : p.xq)[row * 128 + c];
-    const float y = conv4(*reinterpret_cast<const float4 *>(p.w + ((size_t)st_ * C + ch) * 4),
-                          win[st_ * C + ch], t1, t2, xn, p.act);
-    // v of this quarter's channel 32 vq + tid (warp 0)
-    const size_t chv = (size_t)h * 128 + kDecRows * vq + (tid & 31);
-    uint16_t v1 = 0, v2 = 0, vn = 0;
-    if (tid < kDecRows) {
-        v1 = win[5 * C + chv];
-        v2 = win[8 * C + chv];
-        vn = p.xv[row * 128 + kDecRows * vq + tid];
-        sv[tid] = conv4(*reinterpret_cast<const float4 *>(p.w + (2 * C + chv) * 4), win[2 * C + chv], v1, v2, vn,
-                        p.act);
+    float y = 0.f;
+    uint16_t t1 = 0, t2 = 0, xn = 0;    // the taps this thread carries into the new window
+    if (part < 3) {
+        t1 = win[(3 + part) * C + ch];
+        t2 = win[(6 + part) * C + ch];
+        xn = (part == 0 ? p.xq : part == 1 ? p.xk : p.xv)[row * 128 + c];
+        y = conv4(*reinterpret_cast<const float4 *>(p.w + ((size_t)part * C + ch) * 4), win[part * C + ch], t1, t2,
+                  xn, p.act);
+        if (part == 2) sv[c] = y;
+    } else if (part == 3) {
+        reinterpret_cast<float *>(sa)[c] = dec_ex2(p.g[row * 128 + c] * kDecLog2e);
     }
-    // every read of the window is done: the other CTAs may rewrite their quarters
-    // once all four have arrived
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    float y2 = y * y;
+    if (part < 2) {
+        float y2 = y * y;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) y2 += __shfl_xor_sync(0xffffffffu, y2, o);
-    if ((tid & 31) == 0) red[tid >> 5] = y2;
-    if (tid < 128) reinterpret_cast<float *>(sa)[tid] = dec_ex2(p.g[row * 128 + tid] * kDecLog2e);
-    __syncthreads();
-    {
-        const float *r4 = red + 4 * st_;
-        const float n2 = (r4[0] + r4[1]) + (r4[2] + r4[3]);
-        reinterpret_cast<float *>(st_ ? sk : sq)[c] = y / sqrtf(n2 + p.eps);
+        for (int o = 16; o > 0; o >>= 1) y2 += __shfl_xor_sync(0xffffffffu, y2, o);
+        if ((tid & 31) == 0) red[tid >> 5] = y2;
     }
     __syncthreads();
-    const float o = token_step(s, sa, sk, sq, qe, sv[tid >> 3], beta);
+    // every read of the window is done: the new one, this head's channels
+    if (part < 3) {
+        win[part * C + ch] = t1;
+        win[(3 + part) * C + ch] = t2;
+        win[(6 + part) * C + ch] = xn;
+    }
+    if (part < 2) {
+        const float *r4 = red + 4 * part;
+        const float n2 = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+        reinterpret_cast<float *>(part ? sk : sq)[c] = y / sqrtf(n2 + p.eps);
+    }
+    __syncthreads();
+    const float o = token_step(s, sa, sk, sq, qe, sv[vr], beta);
 #pragma unroll
     for (int j = 0; j < 4; j++) st[8 * j + qe] = s[j];
     if (qe == 0) {
         const __nv_bfloat16 ob = __float2bfloat16_rn(o);
         p.out[row * 128 + vr] = *reinterpret_cast<const uint16_t *>(&ob);
-    }
-    // the new window, this CTA's quarter of the channels: taps 1, 2 and the row
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if ((c >> 5) == vq) {
-        win[st_ * C + ch] = t1;
-        win[(3 + st_) * C + ch] = t2;
-        win[(6 + st_) * C + ch] = xn;
-    }
-    if (tid < kDecRows) {
-        win[2 * C + chv] = v1;
-        win[5 * C + chv] = v2;
-        win[8 * C + chv] = vn;
     }
 }
 
@@ -423,7 +414,7 @@ cudaError_t launch_kda_decode_conv_bf16_d128(const DecodeConvArgs &a)
     p.N = a.N; p.H = a.H; p.num_slots = a.num_slots; p.conv_num_slots = a.conv_num_slots;
     p.act = a.activation; p.eps = a.eps;
     p.err = a.err_word;
-    kda_decode_conv_kernel<<<(128 / kDecRows) * a.N * a.H, kDecThreads, 0, a.stream>>>(p);
+    kda_decode_conv_kernel<<<a.N * a.H, kDcThreads, 0, a.stream>>>(p);
     return cudaGetLastError();
 }
 
