@@ -40,12 +40,21 @@
  *  cu_seqlens contract: cu[0] = 0, nondecreasing, cu[N] = T.  It is not read
  *             on the host; the kernels clamp every row index into [0, T], so
  *             a bad table never makes them access memory out of bounds.
- *  Inputs     q and k are expected L2-normalised per head by the caller.  The
- *             tensor-core path rounds its MMA operands to fp16 (fp32
- *             accumulation).  Values must therefore stay in fp16 range:
- *             |v| and |S| below about 6.5e4, and the cumulative log-decay over
- *             half a chunk (32 rows) above about -11 per channel (with
- *             g ~ U[-0.2, 0] it is at least -6.4).
+ *  Inputs     q and k are expected L2-normalised per head by the caller.
+ *  Kernels    bf16 with dk = dv = 128 runs on the tensor-core kernel; every
+ *             other head size, every fp32 call and kda_chunk_prefill_fullrange
+ *             run on the CUDA-core kernel (fp32 arithmetic throughout).
+ *  Range      the tensor-core kernel rounds its MMA operands to fp16 (fp32
+ *             accumulation) and splits each in-chunk decay exp(G_i - G_j)
+ *             into exp(G_i - G_m) exp(G_m - G_j) around the chunk's middle
+ *             row m.  It therefore needs, per key channel and 64-row chunk,
+ *             |G_r - G_m| <= 15 ln 2 (about 10.4) for every row r -- with
+ *             g ~ U[-0.2, 0] the largest is about 4, with g ~ U[-0.5, 0]
+ *             about 10 -- and |v|, |S| below about 6.5e4.  A chunk whose decay
+ *             is outside that range sets bit 32 of the device error word
+ *             (kda_device_error); the results of that call are then not to be
+ *             used: run it again through kda_chunk_prefill_fullrange, which
+ *             forms every decay factor directly and has no such limit.
  *  Aliasing   final_state == initial_state (the same pointer) is allowed and
  *             updates the states in place; any other overlap between an output
  *             and any other argument returns KDA_ERR_ALIAS.
@@ -86,8 +95,12 @@ typedef enum {
  *   initial_state  fp32 [N][H][dv][dk], or NULL for a zero start.
  *   out            bf16 [T][H][dv]; every row in [0, T) is written.
  *   final_state    fp32 [N][H][dv][dk], or NULL (not written).
- *   N, T, H        sequences (1 <= N <= 1024), rows (T >= 0), heads (H >= 1).
- *   dk, dv         key and value head dims; supported: dk = dv = 128.
+ *   N, T, H        sequences (N >= 1), rows (T >= 0), heads (H >= 1);
+ *                  N * H must fit in 31 bits.
+ *   dk, dv         key and value head dims, each 64 or 128 (else
+ *                  KDA_ERR_UNSUPPORTED).  dk = dv = 128 runs on the
+ *                  tensor-core kernel (decay range: see "Range" above), the
+ *                  other sizes on the CUDA-core kernel.
  *   stream         cudaStream_t to launch on.
  * Returns a kda_status.
  */
@@ -97,13 +110,28 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       int N, int T, int H, int dk, int dv, void *stream);
 
 /*
- * kda_chunk_prefill_f32 -- the same operation with fp32 q/k/v and fp32 out.
- * Supported: dk = dv = 64.  All other conventions as kda_chunk_prefill.
+ * kda_chunk_prefill_f32 -- the same operation with fp32 q/k/v and fp32 out,
+ * on the CUDA-core kernel (fp32 arithmetic, no limit on the decay).  dk and
+ * dv each 64 or 128.  All other conventions as kda_chunk_prefill.
  */
 int kda_chunk_prefill_f32(const float *q, const float *k, const float *v,
                           const float *g, const float *beta, const int32_t *cu_seqlens,
                           const float *initial_state, float *out, float *final_state,
                           int N, int T, int H, int dk, int dv, void *stream);
+
+/*
+ * kda_chunk_prefill_fullrange -- kda_chunk_prefill (bf16 q/k/v/out, same
+ * arguments, layouts, sizes and errors) always on the CUDA-core kernel.  It
+ * computes every in-chunk decay factor exp(G_i - G_j) directly in fp32, so it
+ * holds for any finite decay the recurrence itself keeps finite: strong gates
+ * (alpha near 0, g of -20 and below), mixed signs and mild growth (g > 0).  It
+ * never sets bit 32.  One CTA per (sequence, head), fp32 on CUDA cores: slower
+ * than the tensor-core kernel, meant for inputs outside that kernel's range.
+ */
+int kda_chunk_prefill_fullrange(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                const float *g, const float *beta, const int32_t *cu_seqlens,
+                                const float *initial_state, uint16_t *out, float *final_state,
+                                int N, int T, int H, int dk, int dv, void *stream);
 
 /*
  * kda_chunk_prefill_noalloc -- kda_chunk_prefill for packed batches of up to
@@ -120,10 +148,11 @@ int kda_chunk_prefill_f32(const float *q, const float *k, const float *v,
  * nothing -- no cudaMalloc, cudaFree or library allocator.
  *
  * Arguments, layouts, results and errors are those of kda_chunk_prefill,
- * except 1 <= N <= KDA_NOALLOC_MAX_SEQS; a larger N returns
- * KDA_ERR_NOALLOC_LIMIT and launches nothing.  Results are the same as
- * kda_chunk_prefill's (the per-sequence arithmetic does not depend on the
- * schedule).
+ * except 1 <= N <= KDA_NOALLOC_MAX_SEQS: the arguments are checked as there
+ * first, and then a larger N returns KDA_ERR_NOALLOC_LIMIT; a failed check
+ * launches nothing.  Results equal kda_chunk_prefill's bit for bit (the
+ * per-sequence arithmetic does not depend on the schedule).  Head sizes other
+ * than dk = dv = 128 run on the CUDA-core kernel, which needs no table.
  *
  * The first call on a device looks up the array's device address (and checks
  * the device) with that device current; make that first call before any
@@ -330,8 +359,10 @@ const char *kda_status_string(int status);
  * undefined).  Bit 2: a cu_seqlens entry broke its contract (indices were
  * clamped).  Bit 8: a state slot id was outside [-1, num_slots) (that
  * sequence was skipped).  Bit 16: an accepted count of kda_fold_commit was
- * outside [0, W] (clamped).  0 means no kernel of this library has reported an
- * error.
+ * outside [0, W] (clamped).  Bit 32: the tensor-core prefill met a chunk whose
+ * decay is outside its fp16 operand range (see "Range" above; use
+ * kda_chunk_prefill_fullrange for such inputs).  0 means no kernel of this
+ * library has reported an error.
  * Synchronises the current device.  If `reset` is nonzero the word is
  * cleared after reading.  Returns KDA_OK or KDA_ERR_CUDA.
  */

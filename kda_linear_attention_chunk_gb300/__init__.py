@@ -19,11 +19,15 @@ KDA_ERR_ALIGN, KDA_ERR_ALIAS, KDA_ERR_CUDA, KDA_ERR_DEVICE = 4, 5, 6, 7
 KDA_ERR_NOALLOC_LIMIT = 8
 KDA_NOALLOC_MAX_SEQS = 16384
 
-EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_status_string", "kda_device_error",
-            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode", "kda_fold_commit",
-            "kda_short_conv", "kda_decode_conv")
-ERR_BAD_SLOT = 8   # device error word bit: a state slot id outside [-1, num_slots)
-ERR_BAD_ACCEPTED = 16   # device error word bit: an accepted count outside [0, window]
+EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_chunk_prefill_fullrange", "kda_status_string",
+            "kda_device_error", "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode",
+            "kda_fold_commit", "kda_short_conv", "kda_decode_conv")
+# device error word bits (kda_device_error)
+ERR_WAIT_TIMEOUT = 1    # a bounded wait ran out; the kernel wound down early
+ERR_BAD_SEQLENS = 2     # a cu_seqlens entry broke its contract (clamped)
+ERR_BAD_SLOT = 8        # a state slot id outside [-1, num_slots)
+ERR_BAD_ACCEPTED = 16   # an accepted count outside [0, window]
+ERR_DECAY_RANGE = 32    # the tensor-core prefill met a decay beyond its fp16 operand range
 
 _lib = None
 
@@ -44,7 +48,8 @@ def load(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     P, I = ctypes.c_void_p, ctypes.c_int
     sig = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P]
-    for name in ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_chunk_prefill_noalloc"):
+    for name in ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_chunk_prefill_fullrange",
+                 "kda_chunk_prefill_noalloc"):
         fn = getattr(lib, name)
         fn.argtypes = sig
         fn.restype = I
@@ -86,6 +91,14 @@ def kda_chunk_prefill_f32(q, k, v, g, beta, cu_seqlens, initial_state, out, fina
     """Raw C-ABI call for fp32 q/k/v/out."""
     return load().kda_chunk_prefill_f32(q, k, v, g, beta, cu_seqlens, initial_state, out,
                                         final_state, N, T, H, dk, dv, stream)
+
+
+def kda_chunk_prefill_fullrange(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
+                                N: int, T: int, H: int, dk: int, dv: int, stream) -> int:
+    """Raw C-ABI call of the bf16 prefill on the CUDA-core kernel, which takes
+    any decay (no fp16 operand range)."""
+    return load().kda_chunk_prefill_fullrange(q, k, v, g, beta, cu_seqlens, initial_state, out,
+                                              final_state, N, T, H, dk, dv, stream)
 
 
 def kda_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state,
@@ -145,14 +158,17 @@ def _ptr(t) -> int:
 
 
 def chunk_prefill(q, k, v, g, beta, cu_seqlens, initial_state=None, out=None, final_state=None,
-                  output_final_state: bool = True, stream=None) -> Tuple[object, Optional[object]]:
+                  output_final_state: bool = True, stream=None,
+                  full_range: bool = False) -> Tuple[object, Optional[object]]:
     """KDA chunked packed-varlen prefill on torch CUDA tensors.
 
-    q, k: [T][H][dk], v: [T][H][dv] (bfloat16, or float32 with dk = dv = 64);
+    q, k: [T][H][dk], v: [T][H][dv] (bfloat16 or float32; dk, dv in {64, 128});
     g: [T][H][dk] float32; beta: [T][H] float32; cu_seqlens: [N+1] int32 on
     the device; initial_state: [N][H][dv][dk] float32 or None.  Returns
     (out [T][H][dv] in q's dtype, final_state [N][H][dv][dk] float32 or None).
     Runs asynchronously on ``stream`` (default: torch's current stream).
+    ``full_range`` (bfloat16 only) selects kda_chunk_prefill_fullrange, for
+    decays beyond the tensor-core kernel's range (ERR_DECAY_RANGE).
     """
     import torch
 
@@ -171,7 +187,7 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens, initial_state=None, out=None, fi
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), _ptr(initial_state),
             _ptr(out), _ptr(final_state), N, T, H, dk, dv, handle)
     if q.dtype == torch.bfloat16:
-        st = kda_chunk_prefill(*args)
+        st = kda_chunk_prefill_fullrange(*args) if full_range else kda_chunk_prefill(*args)
     elif q.dtype == torch.float32:
         st = kda_chunk_prefill_f32(*args)
     else:

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "kda.h"
 #include "kda_conv.h"
@@ -24,16 +25,20 @@ constexpr int kSchedSlots = 256;
 static __device__ __align__(256) unsigned int g_kda_sched[kSchedSlots][2];
 std::atomic<unsigned> g_sched_next{0};
 
-constexpr int kMaxSeqs = 1024;
 constexpr int kMaxDevices = 64;
 
+// Per-device facts looked up on the first call with that device current.  The
+// fields are written under g_dev_mutex and published by the release store of
+// `checked`; a caller that sees `checked` != 0 through an acquire load also
+// sees the fields (host threads may race on a device's first call).
 struct DevInfo {
-    int checked = 0;   // 0 unknown, 1 ok, -1 unsupported
+    std::atomic<int> checked{0};   // 0 unknown, 1 ok, -1 unsupported
     int num_sms = 0;
     int *err = nullptr;
     unsigned int *sched = nullptr;
 };
 DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
 
 struct Range {
     uintptr_t lo, hi;  // [lo, hi)
@@ -49,6 +54,30 @@ Range range_of(const void *p, size_t bytes)
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Fills in d for device dev (called once, under g_dev_mutex).  A failed
+// query leaves d unknown, so that a later call asks again.
+int init_device(DevInfo &d, int dev)
+{
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_DEVICE;
+    }
+    void *err = nullptr, *sched = nullptr;
+    if (cudaGetSymbolAddress(&err, g_kda_error_word) != cudaSuccess ||
+        cudaGetSymbolAddress(&sched, g_kda_sched) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    d.num_sms = sms;
+    d.err = (int *)err;
+    d.sched = (unsigned int *)sched;
+    d.checked.store((major == 10 && minor == 3) ? 1 : -1, std::memory_order_release);
+    return KDA_OK;
+}
+
 int device_info(DevInfo **out)
 {
     int dev = -1;
@@ -57,26 +86,14 @@ int device_info(DevInfo **out)
         return KDA_ERR_DEVICE;
     }
     DevInfo &d = g_dev[dev];
-    if (d.checked == 0) {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return KDA_ERR_DEVICE;
+    if (d.checked.load(std::memory_order_acquire) == 0) {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        if (d.checked.load(std::memory_order_relaxed) == 0) {
+            const int st = init_device(d, dev);
+            if (st != KDA_OK) return st;
         }
-        void *err = nullptr, *sched = nullptr;
-        if (cudaGetSymbolAddress(&err, g_kda_error_word) != cudaSuccess ||
-            cudaGetSymbolAddress(&sched, g_kda_sched) != cudaSuccess) {
-            cudaGetLastError();
-            return KDA_ERR_CUDA;
-        }
-        d.num_sms = sms;
-        d.err = (int *)err;
-        d.sched = (unsigned int *)sched;
-        d.checked = (major == 10 && minor == 3) ? 1 : -1;
     }
-    if (d.checked != 1) return KDA_ERR_DEVICE;
+    if (d.checked.load(std::memory_order_acquire) != 1) return KDA_ERR_DEVICE;
     *out = &d;
     return KDA_OK;
 }
@@ -86,7 +103,7 @@ int device_info(DevInfo **out)
 // are addressed through the slot table `slots`, an [N] int32 input).
 int validate(const void *q, const void *k, const void *v, const float *g, const float *beta,
              const int32_t *cu, const float *s0, const void *out, const float *s1,
-             int N, int T, int H, int dk, int dv, size_t elem, bool bf16, int max_seqs = kMaxSeqs,
+             int N, int T, int H, int dk, int dv, size_t elem,
              const int32_t *slots = nullptr, int state_n = -1)
 {
     if (state_n < 0) state_n = N;
@@ -97,12 +114,7 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
     if ((size_t)N * (size_t)H > 0x7fffffffu || rows * (size_t)(dk > dv ? dk : dv) * 4 >= ((size_t)1 << 40) ||
         (size_t)state_n * (size_t)H > 0x7fffffffu)
         return KDA_ERR_SHAPE;
-    if (bf16) {
-        if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
-    } else {
-        if (dk != 64 || dv != 64) return KDA_ERR_UNSUPPORTED;
-    }
-    if (N > max_seqs) return KDA_ERR_UNSUPPORTED;
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return KDA_ERR_UNSUPPORTED;
     const void *aligned_ptrs[] = {q, k, v, g, out, s0, s1};
     for (const void *p : aligned_ptrs)
         if (p && !aligned16(p)) return KDA_ERR_ALIGN;
@@ -148,9 +160,9 @@ namespace kda {
 
 int validate_bf16_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
                        const int32_t *cu, const float *s0, const void *out, const float *s1, int N, int T, int H,
-                       int dk, int dv, int max_seqs)
+                       int dk, int dv)
 {
-    return validate(q, k, v, g, beta, cu, s0, out, s1, N, T, H, dk, dv, sizeof(uint16_t), true, max_seqs);
+    return validate(q, k, v, g, beta, cu, s0, out, s1, N, T, H, dk, dv, sizeof(uint16_t));
 }
 
 int error_word_address(int **out)
@@ -188,13 +200,29 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
                       void *stream)
 {
     int st = validate(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H, dk, dv,
-                      sizeof(uint16_t), true);
+                      sizeof(uint16_t));
     if (st != KDA_OK) return st;
     DevInfo *d = nullptr;
     if ((st = device_info(&d)) != KDA_OK) return st;
     kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H,
                                dk, dv, stream, d);
-    return kda::launch_kda_tc_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    const cudaError_t e = (dk == 128 && dv == 128) ? kda::launch_kda_tc_bf16_d128(a) : kda::launch_kda_simt(a, false);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_chunk_prefill_fullrange(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                                const float *beta, const int32_t *cu_seqlens, const float *initial_state,
+                                uint16_t *out, float *final_state, int N, int T, int H, int dk, int dv,
+                                void *stream)
+{
+    int st = validate(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H, dk, dv,
+                      sizeof(uint16_t));
+    if (st != KDA_OK) return st;
+    DevInfo *d = nullptr;
+    if ((st = device_info(&d)) != KDA_OK) return st;
+    kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H,
+                               dk, dv, stream, d);
+    return kda::launch_kda_simt(a, false) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_chunk_prefill_f32(const float *q, const float *k, const float *v, const float *g,
@@ -203,13 +231,13 @@ int kda_chunk_prefill_f32(const float *q, const float *k, const float *v, const 
                           void *stream)
 {
     int st = validate(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H, dk, dv,
-                      sizeof(float), false);
+                      sizeof(float));
     if (st != KDA_OK) return st;
     DevInfo *d = nullptr;
     if ((st = device_info(&d)) != KDA_OK) return st;
     kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H,
                                dk, dv, stream, d);
-    return kda::launch_kda_simt_f32_d64(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda::launch_kda_simt(a, true) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
@@ -220,7 +248,7 @@ int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t
     if (!state_slots || !state_pool) return KDA_ERR_NULL;
     if (num_slots < 1) return KDA_ERR_SHAPE;
     int st = validate(q, k, v, g, beta, cu_seqlens, state_pool, out, state_pool, N, T, H, dk, dv,
-                      sizeof(uint16_t), true, kMaxSeqs, state_slots, num_slots);
+                      sizeof(uint16_t), state_slots, num_slots);
     if (st != KDA_OK) return st;
     DevInfo *d = nullptr;
     if ((st = device_info(&d)) != KDA_OK) return st;
@@ -228,7 +256,8 @@ int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t
                                dk, dv, stream, d);
     a.state_slots = state_slots;
     a.num_slots = num_slots;
-    return kda::launch_kda_tc_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    const cudaError_t e = (dk == 128 && dv == 128) ? kda::launch_kda_tc_bf16_d128(a) : kda::launch_kda_simt(a, false);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g, const float *beta,

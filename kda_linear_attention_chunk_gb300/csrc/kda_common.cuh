@@ -15,6 +15,8 @@ enum : int {
     kErrBadSeqlens = 2,    // cu_seqlens violated its contract (indices clamped)
     kErrLayout = 4,        // shared-memory carve-up did not fit (never expected)
     kErrBadSlot = 8,       // a state slot id outside [-1, num_slots) (that sequence skipped)
+    kErrBadAccepted = 16,  // an accepted count of the fold outside [0, W] (clamped)
+    kErrDecayRange = 32,   // a chunk's decay factors left the fp16 operand range (tensor-core kernel)
 };
 
 __device__ __forceinline__ float load_in(const float *p) { return __ldg(p); }

@@ -39,10 +39,6 @@ struct DecodeConvArgs {
 
 cudaError_t launch_kda_decode_conv_bf16_d128(const DecodeConvArgs &a);
 
-// device error word bit of the fold (bits 1-8 are listed in kda_common.cuh):
-// an accepted count outside [0, window] (clamped)
-enum : int { kErrBadAccepted = 16 };
-
 // commit of a speculative round: the first accepted[n] tokens of each window
 struct FoldArgs {
     const void *k, *v;              // [N][W][H][128] bf16

@@ -30,15 +30,18 @@ struct KdaArgs {
     int num_slots = 0;
 };
 
-cudaError_t launch_kda_simt_f32_d64(const KdaArgs &a);
+// CUDA-core kernel, any dk, dv in {64, 128}, bf16 (f32 = false) or fp32
+// q/k/v/out, no limit on the decay range (kda_simt.cu)
+cudaError_t launch_kda_simt(const KdaArgs &a, bool f32);
+// tensor-core kernel, bf16, dk = dv = 128 (kda_tc.cu)
 cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a);
 int tc_max_sorted_seqs();   // largest N the tensor-core kernel sorts by itself
 
-// kda_api.cu: the checks of kda_chunk_prefill with another limit on N, and the
-// current device's error-word address (also checks the device)
+// kda_api.cu: the checks of kda_chunk_prefill, and the current device's
+// error-word address and SM count (also checks the device)
 int validate_bf16_args(const void *q, const void *k, const void *v, const float *g, const float *beta,
                        const int32_t *cu, const float *s0, const void *out, const float *s1, int N, int T, int H,
-                       int dk, int dv, int max_seqs);
+                       int dk, int dv);
 int error_word_address(int **out);
 
 }  // namespace kda

@@ -18,6 +18,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "kda.h"
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -35,13 +38,16 @@ constexpr int kWordsHead = 4;
 constexpr int kWords = kWordsHead + 2 * kMaxSeqs + kMaxSeqs;
 static __device__ __align__(256) int g_kda_noalloc_scratch[kWords];
 
+// Written under g_na_mutex and published by the release store of `ready`, so
+// that host threads racing on a device's first call see complete fields.
 struct NoAllocDev {
-    int ready = 0;          // 1 once the scratch address, SM count and error word are known
+    std::atomic<int> ready{0};   // 1 once the scratch address, SM count and error word are known
     int num_sms = 0;
-    int *scratch = nullptr; // device address of g_kda_noalloc_scratch
-    int *err = nullptr;     // device address of the library's error word
+    int *scratch = nullptr;      // device address of g_kda_noalloc_scratch
+    int *err = nullptr;          // device address of the library's error word
 };
 NoAllocDev g_na[kMaxDevices];
+std::mutex g_na_mutex;
 
 // rows and lengths: one thread per sequence
 __global__ void noalloc_rows(const int32_t *cu, int N, int T, int H, int *err, int *scratch)
@@ -89,7 +95,12 @@ int noalloc_setup(NoAllocDev **out)
         return KDA_ERR_DEVICE;
     }
     NoAllocDev &d = g_na[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_na_mutex);
+        if (d.ready.load(std::memory_order_relaxed)) {
+            *out = &d;
+            return KDA_OK;
+        }
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -109,7 +120,7 @@ int noalloc_setup(NoAllocDev **out)
         d.scratch = static_cast<int *>(ptr);
         d.err = err;
         d.num_sms = sms;
-        d.ready = 1;
+        d.ready.store(1, std::memory_order_release);
     }
     *out = &d;
     return KDA_OK;
@@ -122,27 +133,32 @@ extern "C" int kda_chunk_prefill_noalloc(const uint16_t *q, const uint16_t *k, c
                                          uint16_t *out, float *final_state, int N, int T, int H, int dk, int dv,
                                          void *stream)
 {
-    if (N > kMaxSeqs) return KDA_ERR_NOALLOC_LIMIT;
+    // the checks of kda_chunk_prefill first, so that a bad pointer or size gets
+    // the same status as there; then the size of the library-held table
     int st = kda::validate_bf16_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H, dk,
-                                     dv, kMaxSeqs);
+                                     dv);
     if (st != KDA_OK) return st;
+    if (N > kMaxSeqs) return KDA_ERR_NOALLOC_LIMIT;
     NoAllocDev *d = nullptr;
     if ((st = noalloc_setup(&d)) != KDA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the deal counters and the nonempty count must start at zero on every call
-    if (cudaMemsetAsync(d->scratch, 0, kWordsHead * sizeof(int), s) != cudaSuccess) return KDA_ERR_CUDA;
-    const int blocks = (N + kThreads - 1) / kThreads;
-    noalloc_rows<<<blocks, kThreads, 0, s>>>(cu_seqlens, N, T, H, d->err, d->scratch);
-    noalloc_order<<<blocks, kThreads, 0, s>>>(N, d->scratch);
-    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     kda::KdaArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu_seqlens = cu_seqlens;
     a.initial_state = initial_state; a.out = out; a.final_state = final_state;
     a.N = N; a.T = T; a.H = H; a.dk = dk; a.dv = dv;
     a.stream = s;
     a.err_word = d->err;
-    a.sched = reinterpret_cast<unsigned int *>(d->scratch);
     a.num_sms = d->num_sms;
+    // other head sizes run on the CUDA-core kernel, one CTA per (sequence,
+    // head): it needs no table
+    if (dk != 128 || dv != 128) return kda::launch_kda_simt(a, false) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    // the deal counters and the nonempty count must start at zero on every call
+    if (cudaMemsetAsync(d->scratch, 0, kWordsHead * sizeof(int), s) != cudaSuccess) return KDA_ERR_CUDA;
+    const int blocks = (N + kThreads - 1) / kThreads;
+    noalloc_rows<<<blocks, kThreads, 0, s>>>(cu_seqlens, N, T, H, d->err, d->scratch);
+    noalloc_order<<<blocks, kThreads, 0, s>>>(N, d->scratch);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    a.sched = reinterpret_cast<unsigned int *>(d->scratch);
     a.g_order = d->scratch + kWordsHead + 2 * kMaxSeqs;
     a.g_rows = reinterpret_cast<const int2 *>(d->scratch + kWordsHead);
     a.g_units_nonempty = d->scratch + 2;

@@ -1,220 +1,340 @@
-// kda_simt.cu -- fp32 CUDA-core KDA chunked prefill.
+// kda_simt.cu -- the full-range KDA chunked prefill on CUDA cores (fp32).
 //
-// The plain SIMT form of the chunked method: one CTA per (sequence, head),
-// fp32 throughout, no tensor cores.  It serves the fp32-input entry point
-// (kda_chunk_prefill_f32, dk = dv = 64) and computes the same per-chunk steps,
-// in the same order, as the tensor-core kernel.
+// One CTA of 512 threads per (sequence, head), fp32 throughout, no tensor
+// cores.  It serves every (dk, dv) in {64, 128} x {64, 128} with bf16 or fp32
+// q/k/v, and has no limit on the decay: every decay factor inside a chunk is
+// formed directly from a difference of cumulative log-decays, never split
+// into a product of a large and a small factor, so strong gates (alpha near
+// 0) and mild growth (g > 0) are computed as the recurrence defines them.
 //
-// Per 64-row chunk of one (sequence, head), rows r < L valid (L <= 64):
-//   G_r   = sum_{u<=r} g_u                                 (per channel)
-//   m     = (L-1)/2, a_r = exp(G_r - G_m), b_r = exp(G_m - G_r)  (midpoint reference)
-//   Kp = K*a, Km = K*b, Qp = Q*a                            (rows >= L are zero)
-//   A_ij  = beta_i Kp_i . Km_j  (j < i)   == beta_i sum_c k_ic k_jc exp(G_ic - G_jc)
-//   B_ri  = Qp_r . Km_i          (i <= r)  == sum_c q_rc k_ic exp(G_rc - G_ic)
-//   M     = (I + A)^-1 diag(beta)
-//   S'    = Diag(exp(G_m)) S0                               (state seen from row m)
-//   Delta = M (V - Kp S')        == U - W S0 with U = M V, W = M (K*exp(G))
-//   O     = Qp S' + B Delta      == (Q*exp(G)) S0 + B Delta
-//   S1    = Diag(exp(G_{L-1} - G_m)) (S' + Km^T Delta)
-//          == Diag(exp(G_{L-1})) S0 + sum_i (k_i*exp(G_{L-1}-G_i)) Delta_i^T
+// Per 64-row chunk of one (sequence, head), rows r < L valid (L <= 64), with
+// G_r = sum_{u<=r} g_u (per key channel) and S0 the state at the chunk start
+// (the chunked WY form of S_t = (I - b k k^T) Diag(exp(g_t)) S_{t-1} + b k v^T,
+// o_t = S_t^T q_t):
+//
+//   A_ij  = beta_i sum_c k_ic k_jc exp(G_ic - G_jc)      j < i   (strictly lower)
+//   B_ri  =        sum_c q_rc k_ic exp(G_rc - G_ic)      i <= r  (lower, diagonal included)
+//   T     = (I + A)^-1                                  (forward substitution)
+//   R     = diag(beta) (V - (K * exp(G)) S0)
+//   Delta = T R                                         (== U - W S0)
+//   O     = (Q * exp(G)) S0 + B Delta
+//   S1    = Diag(exp(G_{L-1})) S0 + (K * exp(G_{L-1} - G))^T Delta
+//
+// Every exponent above is <= 0 when g <= 0.  The state is complete at each
+// chunk end, so a sequence split into calls at a multiple of 64 rows gives the
+// same bits as one call.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
 namespace kda {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kAStride = kChunk + 1;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kAS = kChunk + 1;   // row stride of the 64 x 64 matrices
 
-template <int D>
-struct SimtSmem {
-    float S[D * D];                 // S'[c][v]
-    float Kp[kChunk * D];           // [r][c]; later Delta[r][v]
-    float Km[kChunk * D];           // [r][c]
-    float Qp[kChunk * D];           // [r][c]
-    float V[kChunk * D];            // [r][v]; later R = V - Kp S'
-    float A[kChunk * kAStride];     // L -> T -> M, in place
-    float B[kChunk * kAStride];
-    float G[kChunk * D];            // [r][c]: g of the chunk, then its cumulative sum G
-    float Kin[kChunk * D];          // [r][c]: k and q of the chunk as loaded
-    float Qin[kChunk * D];
-    float gm[D], gl[D], pend[D];
-    float beta[kChunk];
+struct SimtParams {
+    const void *q, *k, *v;
+    const float *g, *beta;
+    const int32_t *cu;
+    const float *s0;
+    void *out;
+    float *s1;
+    int N, T, H;
+    int *err;
+    const int32_t *slots;   // [N] state entries (-1 padding), or nullptr (entry n)
+    int num_slots;
 };
 
-template <typename Tin, typename Tout, int D>
-__global__ void __launch_bounds__(kThreads, 1)
-kda_simt_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
-                const float *__restrict__ g, const float *__restrict__ beta,
-                const int32_t *__restrict__ cu, const float *initial_state,
-                Tout *__restrict__ out, float *final_state, int N, int T, int H, int *err)
+// Shared memory, in floats.  S is the state S[c][v] (key channel major); K, Q
+// and G hold the chunk's k, q and cumulative log-decay and are later turned,
+// element by element, into K*exp(G_{L-1}-G), Q*exp(G) and beta*K*exp(G); V
+// holds beta*V and then R; Delta reuses G's slot once R is formed.
+template <int DK, int DV>
+struct SimtLayout {
+    static constexpr int S = 0;
+    static constexpr int K = S + DK * DV;
+    static constexpr int Q = K + kChunk * DK;
+    static constexpr int G = Q + kChunk * DK;
+    static constexpr int V = G + kChunk * (DK > DV ? DK : DV);
+    static constexpr int A = V + kChunk * DV;
+    static constexpr int B = A + kChunk * kAS;
+    static constexpr int Beta = B + kChunk * kAS;
+    static constexpr int GL = Beta + kChunk;     // G of the last valid row
+    static constexpr int EL = GL + DK;           // exp(G of the last valid row)
+    static constexpr int Floats = EL + DK;
+    static constexpr int Bytes = Floats * 4;
+};
+
+template <int W>
+__device__ __forceinline__ void load_vec(const float *p, float (&x)[W])
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SimtSmem<D> &sm = *reinterpret_cast<SimtSmem<D> *>(smem_raw);
-    const int tid = threadIdx.x;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
-    int bos = clamp_row(cu[n], T, err);
-    int eos = clamp_row(cu[n + 1], T, err);
-    if (eos < bos) eos = bos;
-    const size_t state_off = ((size_t)n * H + h) * D * D;
-
-    for (int idx = tid; idx < D * D; idx += kThreads) {
-        int c = idx / D, vv = idx % D;
-        sm.S[idx] = initial_state ? initial_state[state_off + (size_t)vv * D + c] : 0.f;
+    if constexpr (W == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(p);
+        x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2 *>(p);
+        x[0] = t.x; x[1] = t.y;
     }
-    for (int c = tid; c < D; c += kThreads) sm.pend[c] = 1.f;
-    __syncthreads();
+}
 
-    for (int c0 = bos; c0 < eos; c0 += kChunk) {
-        const int L = min(kChunk, eos - c0);
-        const int m = (L - 1) / 2;
-        // The chunk's g, k, q and v tiles into shared memory, all threads, one row
-        // of D channels per warp pass (rows past the chunk zero).
-        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
-            const int r = idx / D, c = idx % D;
-            const size_t off = ((size_t)(c0 + r) * H + h) * D + c;
+template <typename Tin, typename Tout, int DK, int DV, bool kSlots>
+__global__ void __launch_bounds__(kThreads, 1) kda_simt_kernel(SimtParams p)
+{
+    using Lay = SimtLayout<DK, DV>;
+    constexpr int VW = DV / 32;   // value columns per lane
+    constexpr int CW = DK / kWarps;   // key channels per warp in the state update
+    extern __shared__ __align__(16) float sm[];
+    float *S = sm + Lay::S, *Ks = sm + Lay::K, *Qs = sm + Lay::Q, *Gs = sm + Lay::G, *Vs = sm + Lay::V;
+    float *As = sm + Lay::A, *Bs = sm + Lay::B, *bs = sm + Lay::Beta, *gl = sm + Lay::GL, *el = sm + Lay::EL;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const Tin *q = static_cast<const Tin *>(p.q), *k = static_cast<const Tin *>(p.k), *v = static_cast<const Tin *>(p.v);
+    Tout *out = static_cast<Tout *>(p.out);
+
+    int st = n;
+    if constexpr (kSlots) {
+        st = p.slots[n];
+        if (st < -1 || st >= p.num_slots) {
+            if (tid == 0) atomicOr(p.err, kErrBadSlot);
+            return;
+        }
+        if (st < 0) return;   // padding: nothing computed or written
+    }
+    const int bos = clamp_row(p.cu[n], p.T, p.err);
+    int eos = clamp_row(p.cu[n + 1], p.T, p.err);
+    if (eos < bos) eos = bos;
+    const size_t soff = ((size_t)st * p.H + h) * DK * DV;   // [dv][dk] entry of this (sequence, head)
+
+    for (int i = tid; i < DK * DV; i += kThreads) {          // i = v * DK + c (coalesced global reads)
+        const int vv = i / DK, c = i % DK;
+        S[c * DV + vv] = p.s0 ? p.s0[soff + i] : 0.f;
+    }
+
+    const size_t rs = (size_t)p.H;   // row stride in heads
+    for (int row0 = bos; row0 < eos; row0 += kChunk) {
+        const int L = min(kChunk, eos - row0);
+        // ---- the chunk's tiles (rows past L zero) ----
+        for (int i = tid; i < kChunk * DK; i += kThreads) {
+            const int r = i / DK, c = i % DK;
+            const size_t off = ((size_t)(row0 + r) * rs + h) * DK + c;
             const bool in = r < L;
-            sm.G[idx] = in ? g[off] : 0.f;
-            sm.Kin[idx] = in ? load_in(k + off) : 0.f;
-            sm.Qin[idx] = in ? load_in(q + off) : 0.f;
-            sm.V[idx] = in ? load_in(v + off) : 0.f;
+            Ks[i] = in ? load_in(k + off) : 0.f;
+            Qs[i] = in ? load_in(q + off) : 0.f;
+            Gs[i] = in ? __ldg(p.g + off) : 0.f;
         }
-        if (tid < kChunk) sm.beta[tid] = tid < L ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        for (int i = tid; i < kChunk * DV; i += kThreads) {
+            const int r = i / DV, c = i % DV;
+            Vs[i] = r < L ? load_in(v + ((size_t)(row0 + r) * rs + h) * DV + c) : 0.f;
+        }
+        if (tid < kChunk) bs[tid] = tid < L ? __ldg(p.beta + (size_t)(row0 + tid) * rs + h) : 0.f;
         __syncthreads();
-        // G = running sum of g over the rows, per channel; G_m and G_{L-1}.
-        if (tid < D) {
+        // ---- G = running sum of g over the rows, per key channel ----
+        if (tid < DK) {
             float acc = 0.f;
-            for (int r = 0; r < L; r++) {
-                acc += sm.G[r * D + tid];
-                sm.G[r * D + tid] = acc;
+            for (int r = 0; r < kChunk; r++) {   // rows past L add zero
+                acc += Gs[r * DK + tid];
+                Gs[r * DK + tid] = acc;
             }
-            sm.gm[tid] = sm.G[m * D + tid];
-            sm.gl[tid] = acc;
+            gl[tid] = acc;
+            el[tid] = expf(acc);
         }
         __syncthreads();
-        // S <- Diag(exp(G_m)) Diag(pend) S: first the previous chunk's pending
-        // decay to its last row, then the view from row m.  Two separate
-        // roundings, so a context split into calls (state stored after the
-        // first multiply) reproduces the single-call bits.
-        for (int idx = tid; idx < D * D; idx += kThreads) {
-            int c = idx / D;
-            sm.S[idx] = (sm.S[idx] * sm.pend[c]) * expf(sm.gm[c]);
-        }
-        // Decay-scaled operands, all threads over the tile.
-        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
-            const int r = idx / D, c = idx % D;
-            float kp = 0.f, km = 0.f, qp = 0.f;
-            if (r < L) {
-                const float G = sm.G[idx];
-                const float a = expf(G - sm.gm[c]);
-                const float b = expf(sm.gm[c] - G);
-                const float kv = sm.Kin[idx], qv = sm.Qin[idx];
-                kp = kv * a;
-                km = kv * b;
-                qp = qv * a;
-            }
-            sm.Kp[idx] = kp;
-            sm.Km[idx] = km;
-            sm.Qp[idx] = qp;
-        }
-        __syncthreads();
-        // A (strictly lower, beta-scaled) and B (lower incl. diagonal).  The
-        // channel loop starts at a per-row offset so that a warp's reads of
-        // different rows fall in different banks.
-        for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-            const int i = idx / kChunk, j = idx % kChunk;
-            float sa = 0.f, sb = 0.f;
-            if (j <= i) {
-                for (int cc = 0; cc < D; cc++) {
-                    const int c = (cc + j) & (D - 1);
-                    const float kmj = sm.Km[j * D + c];
-                    sa += sm.Kp[i * D + c] * kmj;
-                    sb += sm.Qp[i * D + c] * kmj;
+        // ---- A (beta-scaled, strictly lower) and B (lower with diagonal) ----
+        // Warp w takes rows i = w, w+16, w+32, w+48; lane l the columns j = l and
+        // l + 32 (j <= i).  The channel loop is skewed by the lane, so that the
+        // lanes of a warp read 32 different banks.
+        for (int i = warp; i < kChunk; i += kWarps) {
+            const float *ki = Ks + i * DK, *qi = Qs + i * DK, *gi = Gs + i * DK;
+            for (int j = lane; j <= i; j += 32) {
+                const float *kj = Ks + j * DK, *gj = Gs + j * DK;
+                float sa = 0.f, sb = 0.f;
+#pragma unroll 4
+                for (int cc = 0; cc < DK; cc++) {
+                    const int c = (cc + lane) & (DK - 1);
+                    const float w = expf(gi[c] - gj[c]) * kj[c];
+                    sa = fmaf(ki[c], w, sa);
+                    sb = fmaf(qi[c], w, sb);
                 }
+                As[i * kAS + j] = j < i ? bs[i] * sa : 0.f;
+                Bs[i * kAS + j] = sb;
             }
-            sm.A[i * kAStride + j] = (j < i) ? sm.beta[i] * sa : 0.f;
-            sm.B[i * kAStride + j] = sb;
+            for (int j = i + 1 + lane; j < kChunk; j += 32) {
+                As[i * kAS + j] = 0.f;
+                Bs[i * kAS + j] = 0.f;
+            }
         }
-        // (I + A)^-1 by right-looking forward substitution, in place: at step j
-        // row j is final; rows i > j take -A_ij T_j.  Slot j of row i holds
-        // A_ij until step j reads it, then T_ij.
+        __syncthreads();
+        // ---- element-wise: K -> K*exp(G_L - G), Q -> Q*exp(G), G -> beta*K*exp(G);
+        //      V -> beta*V ----
+        for (int i = tid; i < kChunk * DK; i += kThreads) {
+            const int r = i / DK, c = i % DK;
+            const float x = Gs[i], kv = Ks[i];
+            const float e = expf(x);
+            Ks[i] = kv * expf(gl[c] - x);
+            Qs[i] = Qs[i] * e;
+            Gs[i] = bs[r] * (kv * e);
+        }
+        for (int i = tid; i < kChunk * DV; i += kThreads) Vs[i] *= bs[i / DV];
+        // ---- T = (I + A)^-1, in place (right-looking: at step j row j is final,
+        //      rows below take -A_ij T_j); T's unit diagonal stays implicit ----
         for (int j = 0; j < kChunk - 1; j++) {
             __syncthreads();
             const int i = tid;
             if (i > j && i < kChunk) {
-                float a = sm.A[i * kAStride + j];
-                sm.A[i * kAStride + j] = -a;
-                for (int l = 0; l < j; l++) sm.A[i * kAStride + l] -= a * sm.A[j * kAStride + l];
+                const float a = As[i * kAS + j];
+                As[i * kAS + j] = -a;
+                for (int l = 0; l < j; l++) As[i * kAS + l] = fmaf(-a, As[j * kAS + l], As[i * kAS + l]);
             }
         }
         __syncthreads();
-        // M = T diag(beta), T unit lower triangular.
-        for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-            const int i = idx / kChunk, j = idx % kChunk;
-            float t = (j < i) ? sm.A[i * kAStride + j] : (j == i ? 1.f : 0.f);
-            sm.A[i * kAStride + j] = t * sm.beta[j];
+        const int r0 = 4 * warp, v0 = VW * lane;   // this thread's 4 rows x VW value columns
+        // ---- R = beta*V - (beta*K*exp(G)) S0, in place over V ----
+        {
+            float acc[4][VW] = {};
+            for (int c = 0; c < DK; c++) {
+                float s[VW];
+                load_vec<VW>(S + c * DV + v0, s);
+#pragma unroll
+                for (int a = 0; a < 4; a++) {
+                    const float kg = Gs[(r0 + a) * DK + c];
+#pragma unroll
+                    for (int b = 0; b < VW; b++) acc[a][b] = fmaf(kg, s[b], acc[a][b]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 4; a++)   // this thread's own elements of V
+#pragma unroll
+                for (int b = 0; b < VW; b++) Vs[(r0 + a) * DV + v0 + b] -= acc[a][b];
+        }
+        __syncthreads();   // R complete, and every read of the KG slot done
+        // ---- Delta = T R into G's slot ----
+        float *D = Gs;
+        {
+            float acc[4][VW];
+#pragma unroll
+            for (int a = 0; a < 4; a++) load_vec<VW>(Vs + (r0 + a) * DV + v0, acc[a]);   // unit diagonal
+            for (int j = 0; j < r0 + 3; j++) {
+                float x[VW];
+                load_vec<VW>(Vs + j * DV + v0, x);
+#pragma unroll
+                for (int a = 0; a < 4; a++) {
+                    const float t = As[(r0 + a) * kAS + j];   // zero for j >= r0 + a
+#pragma unroll
+                    for (int b = 0; b < VW; b++) acc[a][b] = fmaf(t, x[b], acc[a][b]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 4; a++)
+#pragma unroll
+                for (int b = 0; b < VW; b++) D[(r0 + a) * DV + v0 + b] = acc[a][b];
         }
         __syncthreads();
-        // R = V - Kp S'
-        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
-            const int r = idx / D, vv = idx % D;
-            float s = 0.f;
-            for (int c = 0; c < D; c++) s += sm.Kp[r * D + c] * sm.S[c * D + vv];
-            sm.V[idx] -= s;
-        }
-        __syncthreads();
-        // Delta = M R  (into the Kp buffer)
-        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
-            const int r = idx / D, vv = idx % D;
-            float s = 0.f;
-            for (int j = 0; j <= r; j++) s += sm.A[r * kAStride + j] * sm.V[j * D + vv];
-            sm.Kp[idx] = s;
-        }
-        __syncthreads();
-        // O = Qp S' + B Delta
-        for (int idx = tid; idx < kChunk * D; idx += kThreads) {
-            const int r = idx / D, vv = idx % D;
-            if (r < L) {
-                float s = 0.f;
-                for (int c = 0; c < D; c++) s += sm.Qp[r * D + c] * sm.S[c * D + vv];
-                for (int i = 0; i <= r; i++) s += sm.B[r * kAStride + i] * sm.Kp[i * D + vv];
-                store_out(out + ((size_t)(c0 + r) * H + h) * D + vv, s);
+        // ---- O = (Q*exp(G)) S0 + B Delta -> out (rows < L) ----
+        {
+            float acc[4][VW] = {};
+            for (int c = 0; c < DK; c++) {
+                float s[VW];
+                load_vec<VW>(S + c * DV + v0, s);
+#pragma unroll
+                for (int a = 0; a < 4; a++) {
+                    const float qg = Qs[(r0 + a) * DK + c];
+#pragma unroll
+                    for (int b = 0; b < VW; b++) acc[a][b] = fmaf(qg, s[b], acc[a][b]);
+                }
+            }
+            for (int j = 0; j <= r0 + 3; j++) {
+                float x[VW];
+                load_vec<VW>(D + j * DV + v0, x);
+#pragma unroll
+                for (int a = 0; a < 4; a++) {
+                    const float bb = Bs[(r0 + a) * kAS + j];   // zero for j > r0 + a
+#pragma unroll
+                    for (int b = 0; b < VW; b++) acc[a][b] = fmaf(bb, x[b], acc[a][b]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 4; a++) {
+                if (r0 + a < L) {
+                    Tout *o = out + ((size_t)(row0 + r0 + a) * rs + h) * DV + v0;
+#pragma unroll
+                    for (int b = 0; b < VW; b++) store_out(o + b, acc[a][b]);
+                }
             }
         }
         __syncthreads();
-        // S <- S' + Km^T Delta; the decay to row L-1 is applied lazily.
-        for (int idx = tid; idx < D * D; idx += kThreads) {
-            const int c = idx / D, vv = idx % D;
-            float s = sm.S[idx];
-            for (int j = 0; j < L; j++) s += sm.Km[j * D + c] * sm.Kp[j * D + vv];
-            sm.S[idx] = s;
+        // ---- S <- Diag(exp(G_L)) S + (K*exp(G_L - G))^T Delta ----
+        {
+            const int c0 = CW * warp;
+            float acc[CW][VW];
+#pragma unroll
+            for (int a = 0; a < CW; a++) {
+                float s[VW];
+                load_vec<VW>(S + (c0 + a) * DV + v0, s);
+#pragma unroll
+                for (int b = 0; b < VW; b++) acc[a][b] = el[c0 + a] * s[b];
+            }
+            for (int r = 0; r < L; r++) {
+                float x[VW];
+                load_vec<VW>(D + r * DV + v0, x);
+#pragma unroll
+                for (int a = 0; a < CW; a++) {
+                    const float ke = Ks[r * DK + c0 + a];
+#pragma unroll
+                    for (int b = 0; b < VW; b++) acc[a][b] = fmaf(ke, x[b], acc[a][b]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < CW; a++)
+#pragma unroll
+                for (int b = 0; b < VW; b++) S[(c0 + a) * DV + v0 + b] = acc[a][b];
         }
-        for (int c = tid; c < D; c += kThreads) sm.pend[c] = expf(sm.gl[c] - sm.gm[c]);
         __syncthreads();
     }
-    if (final_state) {
-        for (int idx = tid; idx < D * D; idx += kThreads) {
-            const int vv = idx / D, c = idx % D;
-            final_state[state_off + idx] = sm.S[c * D + vv] * sm.pend[c];
+    if (p.s1) {
+        __syncthreads();
+        for (int i = tid; i < DK * DV; i += kThreads) {
+            const int vv = i / DK, c = i % DK;
+            p.s1[soff + i] = S[c * DV + vv];
         }
     }
+}
+
+template <typename Tin, typename Tout, int DK, int DV, bool kSlots>
+cudaError_t launch_one(const KdaArgs &a)
+{
+    auto kern = kda_simt_kernel<Tin, Tout, DK, DV, kSlots>;
+    constexpr int smem = SimtLayout<DK, DV>::Bytes;
+    static_assert(smem <= 232448, "shared memory of the CUDA-core kernel");
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    SimtParams p;
+    p.q = a.q; p.k = a.k; p.v = a.v; p.g = a.g; p.beta = a.beta; p.cu = a.cu_seqlens;
+    p.s0 = a.initial_state; p.out = a.out; p.s1 = a.final_state;
+    p.N = a.N; p.T = a.T; p.H = a.H; p.err = a.err_word;
+    p.slots = a.state_slots; p.num_slots = a.num_slots;
+    kern<<<(unsigned)((size_t)a.N * a.H), kThreads, smem, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout, bool kSlots>
+cudaError_t launch_dims(const KdaArgs &a)
+{
+    if (a.dk == 128 && a.dv == 128) return launch_one<Tin, Tout, 128, 128, kSlots>(a);
+    if (a.dk == 128 && a.dv == 64) return launch_one<Tin, Tout, 128, 64, kSlots>(a);
+    if (a.dk == 64 && a.dv == 128) return launch_one<Tin, Tout, 64, 128, kSlots>(a);
+    if (a.dk == 64 && a.dv == 64) return launch_one<Tin, Tout, 64, 64, kSlots>(a);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-template <typename Tin, typename Tout, int D>
-static cudaError_t launch_simt(const KdaArgs &a)
+cudaError_t launch_kda_simt(const KdaArgs &a, bool f32)
 {
-    auto kern = kda_simt_kernel<Tin, Tout, D>;
-    const int smem = (int)sizeof(SimtSmem<D>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    kern<<<a.N * a.H, kThreads, smem, a.stream>>>(
-        (const Tin *)a.q, (const Tin *)a.k, (const Tin *)a.v, a.g, a.beta, a.cu_seqlens,
-        a.initial_state, (Tout *)a.out, a.final_state, a.N, a.T, a.H, a.err_word);
-    return cudaGetLastError();
+    const bool slots = a.state_slots != nullptr;
+    if (f32) return slots ? launch_dims<float, float, true>(a) : launch_dims<float, float, false>(a);
+    return slots ? launch_dims<__nv_bfloat16, __nv_bfloat16, true>(a)
+                 : launch_dims<__nv_bfloat16, __nv_bfloat16, false>(a);
 }
-
-cudaError_t launch_kda_simt_f32_d64(const KdaArgs &a) { return launch_simt<float, float, 64>(a); }
 
 }  // namespace kda

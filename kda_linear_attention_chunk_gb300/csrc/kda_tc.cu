@@ -42,6 +42,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
@@ -72,6 +74,14 @@ __device__ __forceinline__ unsigned long long kda_gtimer()
 #define KDA_PHASE(role, item, point) \
     do {                             \
     } while (0)
+#endif
+
+// Poll limit of the chain's wait for MMA1.  A test build of the library sets
+// it to 0, so that the wait gives up at once although its MMA does complete:
+// that drives the kernel through its timeout path (error bit, wind-down,
+// TMEM freed after every MMA and copy in flight has landed) on the GPU.
+#ifndef KDA_WAIT_LIMIT_MMA1
+#define KDA_WAIT_LIMIT_MMA1 (1u << 18)
 #endif
 
 constexpr int kD = 128;
@@ -302,6 +312,12 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 constexpr float kLog2e = 1.4426950408889634f;   // 1 / ln 2
+// Largest |G_r - G_m| (base 2) of a chunk's operand factors.  At 2^15 an
+// operand beta*k*a stays below fp16's largest value 65504 for |beta k| <= 1,
+// and a factor of 2^-15 keeps a typical |k| ~ 2^-3.5 at 2^-18.5, whose fp16
+// subnormal still carries ~6 significant bits in the few products that pair
+// it with a factor of 2^15.
+constexpr float kMaxFactorLog2 = 15.f;
 
 __device__ __forceinline__ void record_error(const TcParams &p, const Smem &sm, int code)
 {
@@ -422,7 +438,7 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 }
 
 // =============================================================================
-// prep, group E (warps 4-7): cumulative log-decay, the decay-scaled operands,
+// prep, group E (warps 4-11): cumulative log-decay, the decay-scaled operands,
 // MMA-a and beta*V.  Loops are kept rolled: each warp runs its loop bodies
 // once per chunk next to two other roles, so compact code matters more than
 // unrolling.
@@ -439,7 +455,8 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // over the bf16 tiles (rows past the chunk zero).  Returns false if a wait ran
 // out.
 template <class F, class V>
-__device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r, F &&released, V &&before_kq)
+__device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r, int *err, F &&released,
+                       V &&before_kq)
 {
     const int lane = et & 31;
     const uint32_t st = s * kStageBytes;
@@ -497,6 +514,7 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
     }
     if (et == 0) KDA_PHASE(0, item, 10);
     const float2 gm = *reinterpret_cast<const float2 *>(gmx + c0);
+    float worst = 0.f;   // largest |G_r - G_m| of this thread's rows r < L
     uint8_t *kt = sm.base + st + kOffKQ + chh * 16384 + off_k(s);   // this channel half's 64-channel block
     uint8_t *qt = sm.base + st + kOffKQ + chh * 16384 + off_q(s);
     uint8_t *kmt = sm.base + st + off_km(s) + chh * 8192;
@@ -513,10 +531,12 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
             const float br = cst[256 + r];               // zero past the chunk
             float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
             if (r < L) {
-                a0 = ex2(x[t].x - gm.x);
-                a1 = ex2(x[t].y - gm.y);
-                b0 = ex2(gm.x - x[t].x);
-                b1 = ex2(gm.y - x[t].y);
+                const float d0 = x[t].x - gm.x, d1 = x[t].y - gm.y;
+                a0 = ex2(d0);
+                a1 = ex2(d1);
+                b0 = ex2(-d0);
+                b1 = ex2(-d1);
+                worst = fmaxf(worst, fmaxf(fabsf(d0), fabsf(d1)));
             }
             const float k0 = bf16lo(kw), k1 = bf16hi(kw);
             const float q0 = bf16lo(qw), q1 = bf16hi(qw);
@@ -527,6 +547,10 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
 #pragma unroll
         for (int t = 0; t < 8; t++) x[t] = x[t + 8];
     }
+    // every factor 2^(G_r - G_m) must lie in [2^-kMaxFactorLog2, 2^kMaxFactorLog2]:
+    // beyond it the fp16 operands overflow or lose their precision, and the
+    // chunk is reported (its results are not to be used)
+    if (worst > kMaxFactorLog2) atomicOr(err, kErrDecayRange);
     if (et == 0) KDA_PHASE(0, item, 11);
     return true;
 }
@@ -617,6 +641,11 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
         beta_next = load_beta(p, ahead, et);
     }
     int item = 0;
+    // after a wait ran out: the g load in flight (chunk ahead.item - 1, one past
+    // the last chunk whose g was waited for) lands before the role returns
+    auto drain_g = [&]() {
+        if (et == 0 && ahead.item > item) mbar_wait_drain(sm.bar(kBarGFull), (ahead.item - 1) & 1);
+    };
     for (int k = 0;; k++) {
         const int u = cta_unit<kSort>(sm, k, U);
         if (u < 0) break;
@@ -628,7 +657,11 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             const float beta_r = beta_next;
             if (et == 0) publish();
             bool ok = mbar_wait(sm.bar(kBarGFull), item & 1, sm.abort_flag());
-            if (role_any(!ok, kBarE, kEThreads)) { if (et == 0) record_error(p, sm, kErrWaitTimeout); return; }
+            if (role_any(!ok, kBarE, kEThreads)) {
+                if (et == 0) record_error(p, sm, kErrWaitTimeout);
+                drain_g();
+                return;
+            }
             if (et == 0) KDA_PHASE(0, item, 0);
             // the next chunk's g is requested as soon as this chunk's g is read
             auto next_g = [&]() {
@@ -651,8 +684,11 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                 mbar_arrive(sm.bar(kBarEDone + s));
                 return true;
             };
-            if (!e_pass(sm, s, item, L, et, beta_r, next_g, convert_v)) {
+            if (!e_pass(sm, s, item, L, et, beta_r, p.err, next_g, convert_v)) {
                 if (et == 0) record_error(p, sm, kErrWaitTimeout);
+                // this chunk's g was waited for (item + 1 of them); the next one may be in flight
+                item++;
+                drain_g();
                 return;
             }
             fence_proxy_async_smem();
@@ -675,7 +711,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
 }
 
 // =============================================================================
-// prep, group I (warps 8-11): the A readout, the inverse T = (I + A_kk)^-1,
+// prep, group I (warps 12-15): the A readout, the inverse T = (I + A_kk)^-1,
 // MMA-b and the -W' conversion
 // =============================================================================
 // fp32 blocks of the inverse in the shared kOffTmp region (float offsets):
@@ -1070,6 +1106,76 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, const Maps &m
     if (v == 0) KDA_PHASE(1, item, 9);
 }
 
+// ---- states between global memory and TMEM -------------------------------------
+// A state row (value channel v: 128 key channels, 512 contiguous bytes) lives
+// in TMEM lane v, so a thread that moved its own row would make every warp
+// instruction touch 32 rows.  Instead each warp moves 16 key channels of its
+// 32 rows at a time through its 2 KB slice of the output tile buffer: global
+// memory is read and written 8 rows x 64 bytes per instruction, shared memory
+// row by row.  Piece p (16 bytes) of staged row r sits in slot p ^ ((r/2) & 3),
+// which keeps both access patterns at the minimum of four shared-memory
+// wavefronts per warp instruction.
+__device__ __forceinline__ uint32_t stg_off(int r, int piece) { return r * 64 + ((piece ^ ((r >> 1) & 3)) << 4); }
+
+// this warp's 32 state rows (src: row 0 of them, or null for zeros) -> TMEM
+// columns tm .. tm+127 of its lanes; the global loads of the next round are
+// in flight while a round goes from the slice to TMEM
+__device__ void chain_load_state(const float *src, uint8_t *stg, uint32_t tm, int lane)
+{
+    const int rq = lane >> 2, pq = lane & 3;       // coalesced pattern: row 8i + rq, piece pq
+    float4 b[4];
+    auto fetch = [&](int r) {
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            b[i] = src ? *reinterpret_cast<const float4 *>(src + (8 * i + rq) * kD + 16 * r + 4 * pq)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    fetch(0);
+#pragma unroll 1
+    for (int r = 0; r < 8; r++) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) *reinterpret_cast<float4 *>(stg + stg_off(8 * i + rq, pq)) = b[i];
+        if (r < 7) fetch(r + 1);
+        __syncwarp();
+        uint32_t x[16];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float4 f = *reinterpret_cast<const float4 *>(stg + stg_off(lane, q));
+            x[4 * q] = __float_as_uint(f.x); x[4 * q + 1] = __float_as_uint(f.y);
+            x[4 * q + 2] = __float_as_uint(f.z); x[4 * q + 3] = __float_as_uint(f.w);
+        }
+        tmem_st16(tm + 16 * r, x);
+        __syncwarp();   // the slice is read before the next round overwrites it
+    }
+    tmem_wait_st();
+}
+
+// TMEM columns tm .. tm+127 of this warp's lanes, times pend per key channel ->
+// its 32 state rows at dst
+__device__ void chain_store_state(float *dst, const float *pend, uint8_t *stg, uint32_t tm, int lane)
+{
+    const int rq = lane >> 2, pq = lane & 3;
+#pragma unroll 1
+    for (int r = 0; r < 8; r++) {
+        uint32_t x[16];
+        tmem_ld16(tm + 16 * r, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float4 pe = *reinterpret_cast<const float4 *>(pend + 16 * r + 4 * q);
+            *reinterpret_cast<float4 *>(stg + stg_off(lane, q)) =
+                make_float4(__fmul_rn(__uint_as_float(x[4 * q]), pe.x), __fmul_rn(__uint_as_float(x[4 * q + 1]), pe.y),
+                            __fmul_rn(__uint_as_float(x[4 * q + 2]), pe.z), __fmul_rn(__uint_as_float(x[4 * q + 3]), pe.w));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            *reinterpret_cast<float4 *>(dst + (8 * i + rq) * kD + 16 * r + 4 * pq) =
+                *reinterpret_cast<const float4 *>(stg + stg_off(8 * i + rq, pq));
+        __syncwarp();
+    }
+}
+
 // S <- (S * pend) * fm column by column (pend may be null), written back, and
 // its fp16 copy S'h (two per 32-bit column) for the chain MMAs.
 __device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float *fm, const float *pend, int item)
@@ -1106,13 +1212,16 @@ __device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float 
     tmem_wait_st();
 }
 
+// kq_pending (thread 0): chunk cur.item-1's v is requested, its k and q not yet
 template <bool kSlots, int kSort>
 __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps,
-                            LoadCursor &cur, uint32_t tmem, uint32_t lane_off, int v)
+                            LoadCursor &cur, bool &kq_pending, uint32_t tmem, uint32_t lane_off, int v)
 {
     int item = 0;
-    bool kq_pending = false;  // thread 0: chunk cur.item-1's v is requested, its k and q not yet
     int o_pending = -1;       // thread 0: stage whose output copies may still read their tiles
+    // this warp's 2 KB staging slice for states, and its first state row of a unit
+    auto stg = [&]() { return sm.base + kOffOT + 2048 * (v >> 5); };
+    auto warp_rows = [&](const Unit &x) { return (((size_t)x.st * p.H + x.h) * kD + (v & ~31)) * kD; };
     for (int k = 0;; k++) {
         const int u = cta_unit<kSort>(sm, k, U);
         if (u < 0) break;
@@ -1127,20 +1236,9 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             }
             continue;
         }
-        // initial state -> S (TMEM, lane v, columns = key channels), 64 columns a round
-#pragma unroll 1
-        for (int hb = 0; hb < 2; hb++) {
-            uint32_t x[64];
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-                float4 f = p.s0 ? *reinterpret_cast<const float4 *>(p.s0 + soff + 64 * hb + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                x[j] = __float_as_uint(f.x); x[j + 1] = __float_as_uint(f.y);
-                x[j + 2] = __float_as_uint(f.z); x[j + 3] = __float_as_uint(f.w);
-            }
-            tmem_st32(tmem + kTmS + lane_off + 64 * hb, *reinterpret_cast<uint32_t(*)[32]>(x));
-            tmem_st32(tmem + kTmS + lane_off + 64 * hb + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
-        }
-        tmem_wait_st();
+        // initial state -> S (TMEM, lane v, columns = key channels), staged through
+        // the output tile buffer (free: no output copy is in flight here)
+        chain_load_state(p.s0 ? p.s0 + warp_rows(un) : nullptr, stg(), tmem + kTmS + lane_off, v & 31);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const uint32_t ph = (item >> 1) & 1;
@@ -1200,7 +1298,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
                 mma_commit(sm.bar(kBarMma1));
                 KDA_PHASE(1, item, 1);
             }
-            ok = mbar_wait(sm.bar(kBarMma1), item & 1, sm.abort_flag());
+            ok = mbar_wait(sm.bar(kBarMma1), item & 1, sm.abort_flag(), KDA_WAIT_LIMIT_MMA1);
             if (role_any(!ok, kBarChain, kChainThreads)) { if (v == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (v == 0) {
                 KDA_PHASE(1, item, 2);
@@ -1260,24 +1358,18 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
 #ifdef KDA_TRACE
         if (v == 0 && blockIdx.x < 1024) { g_kda_cta[blockIdx.x][2] = item; g_kda_cta[blockIdx.x][3] = k + 1; }
 #endif
-        // unit end: final state = S * pend of the unit's last chunk
-        if (p.s1) {
-            const float *pend = sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; cb++) {
-                uint32_t x[32];
-                tmem_ld32(tmem + kTmS + lane_off + 32 * cb, x);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float4 f = make_float4(__fmul_rn(__uint_as_float(x[j]), pend[32 * cb + j]),
-                                           __fmul_rn(__uint_as_float(x[j + 1]), pend[32 * cb + j + 1]),
-                                           __fmul_rn(__uint_as_float(x[j + 2]), pend[32 * cb + j + 2]),
-                                           __fmul_rn(__uint_as_float(x[j + 3]), pend[32 * cb + j + 3]));
-                    *reinterpret_cast<float4 *>(p.s1 + soff + 32 * cb + j) = f;
-                }
-            }
+        // unit end: the last chunk's output copies have read the tile buffers
+        // (then TMEM P_s and the buffers go back to the prep at once), and the
+        // final state = S * pend of the unit's last chunk leaves through them
+        if (v == 0 && o_pending >= 0) {
+            bulk_wait_read0();
+            mbar_arrive(sm.bar(kBarODone + o_pending));
+            o_pending = -1;
         }
+        named_bar(kBarChain, kChainThreads);
+        if (p.s1)
+            chain_store_state(p.s1 + warp_rows(un), sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128, stg(),
+                              tmem + kTmS + lane_off, v & 31);
     }
 }
 
@@ -1289,21 +1381,23 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
     const uint32_t tmem = *sm.tmem_base();
     const uint32_t lane_off = (uint32_t)(32 * w) << 16;
     LoadCursor cur;
+    bool kq_pending = false;
     if (v == 0) {
         for (int i = 0; i < 2 && cursor_next<kSlots, kSort>(cur, p, sm, order, U); i++) {
             issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
             issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
         }
     }
-    chain_units<kSlots, kSort>(p, sm, order, U, maps, cur, tmem, lane_off, v);
+    chain_units<kSlots, kSort>(p, sm, order, U, maps, cur, kq_pending, tmem, lane_off, v);
     if (v == 0) {
         bulk_wait0();   // the output copies are complete
-        // copies still in flight land before the CTA exits (normally none: every
-        // requested chunk has been consumed)
+        // copies still in flight land before the CTA exits: normally none (every
+        // requested chunk has been consumed); after a wait ran out, up to the
+        // last two requested chunks (the k and q of the last one only if issued)
         for (int back = 1; back <= 2 && cur.item - back >= 0; back++) {
             const int it = cur.item - back;
-            mbar_wait(sm.bar(kBarKQFull + (it & 1)), (it >> 1) & 1, sm.abort_flag(), 1u << 14);
-            mbar_wait(sm.bar(kBarVFull + (it & 1)), (it >> 1) & 1, sm.abort_flag(), 1u << 14);
+            if (!(back == 1 && kq_pending)) mbar_wait_drain(sm.bar(kBarKQFull + (it & 1)), (it >> 1) & 1);
+            mbar_wait_drain(sm.bar(kBarVFull + (it & 1)), (it >> 1) & 1);
         }
     }
 }
@@ -1412,7 +1506,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     // every MMA this CTA issued has completed before TMEM is released
     if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads) {
         mma_commit(sm.bar(kBarDrain));
-        mbar_wait(sm.bar(kBarDrain), 0, sm.abort_flag(), 1u << 14);
+        mbar_wait_drain(sm.bar(kBarDrain), 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -1434,16 +1528,18 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 }
 
 // ---- host side ------------------------------------------------------------------
+// The driver's tensor-map encoder, looked up once (a function-local static is
+// initialised exactly once even when host threads race on the first call).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -1509,13 +1605,15 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     static const Kernel kernels[6] = {kda_tc_kernel<false, 0>, kda_tc_kernel<false, 1>, kda_tc_kernel<false, 2>,
                                       kda_tc_kernel<true, 0>,  kda_tc_kernel<true, 1>,  kda_tc_kernel<true, 2>};
     const Kernel kernel = kernels[variant];
-    static int attr_set[6][64] = {{0}};
+    // the shared-memory opt-in, once per (kernel, device); setting it twice
+    // (two host threads racing on a first call) is harmless
+    static std::atomic<int> attr_set[6][64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[variant][dev]) {
+    if (dev < 0 || dev >= 64 || !attr_set[variant][dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set[variant][dev] = 1;
+        if (dev >= 0 && dev < 64) attr_set[variant][dev].store(1, std::memory_order_release);
     }
     TcParams p;
     p.cu = a.cu_seqlens;

@@ -40,6 +40,7 @@ _LIB = os.path.join(_HERE, "_build", "libsynth.so")
 
 KIND_Q, KIND_K, KIND_V, KIND_G, KIND_BETA, KIND_STATE = range(6)
 STREAM_LENS = 7
+STREAM_PROFILE = 11   # uniforms that pick the entries a decay profile changes
 _gen = None
 
 
@@ -192,12 +193,47 @@ def draw(w: Workload, row_lo: int = 0, row_hi: Optional[int] = None,
 
 
 def draw_initial_state(w: Workload, heads: Optional[Sequence[int]] = None) -> Optional[np.ndarray]:
-    """[N][nh][dv][dk] float32 initial states, or None for a zero start."""
+    """[N][nh][dv][dk] float32 initial states, or None for a zero start.  With
+    dk != dv the state is the [dv][dk] corner of the d x d draw, d = max."""
     if not w.init_state:
         return None
-    assert w.dk == w.dv
     hs = _heads(w, heads)
-    return _fill(KIND_STATE, w, 0, w.N, hs, w.dk, (w.N, len(hs), w.dv, w.dk), np.float32, 1)
+    d = max(w.dk, w.dv)
+    s = _fill(KIND_STATE, w, 0, w.N, hs, d, (w.N, len(hs), d, d), np.float32, 1)
+    return np.ascontiguousarray(s[:, :, :w.dv, :w.dk])
+
+
+DECAY_PROFILES = ("u02", "u05", "u1", "u3", "alpha0", "mixed")
+
+
+def decay_profile(g: np.ndarray, profile: str, seed: int = 0) -> np.ndarray:
+    """Another gate distribution from g as drawn (U[-0.2, 0], [T][H][dk]), for
+    tests of the decay range; a copy, float32:
+
+    * u02: unchanged;  u05, u1, u3: U[-a, 0] for a = 0.5, 1, 3 (g scaled);
+    * alpha0: about 3% of the (head, channel) pairs held at g = -20 on every
+      row (alpha = e^-20, a channel that forgets at once), the rest unchanged;
+    * mixed: about 5% of the entries replaced by U[0, 0.5] (a growing gate),
+      the rest unchanged.
+
+    The entries are picked by seeded uniforms over the whole tensor."""
+    g = np.array(g, dtype=np.float32)
+    T, H, dk = g.shape
+    if profile == "u02":
+        return g
+    if profile in ("u05", "u1", "u3"):
+        a = {"u05": 0.5, "u1": 1.0, "u3": 3.0}[profile]
+        return (g * np.float32(a / 0.2)).astype(np.float32)
+    if profile == "alpha0":
+        pick = uniform(seed, STREAM_PROFILE, H * dk).reshape(H, dk) < 0.03
+        g[:, pick] = -20.0
+        return g
+    if profile == "mixed":
+        u = uniform(seed, STREAM_PROFILE + 1, T * H * dk).reshape(T, H, dk)
+        pos = u < 0.05
+        g[pos] = (u[pos] * (0.5 / 0.05)).astype(np.float32)
+        return g
+    raise ValueError(f"unknown decay profile {profile!r}")
 
 
 def random_lengths(total: int, parts: int, seed: int, allow_empty: bool = False) -> List[int]:

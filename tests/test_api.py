@@ -51,7 +51,11 @@ def call(fn="kda_chunk_prefill", **over):
     return getattr(kda, fn)(*[args[n] for n in order])
 
 
-@pytest.mark.parametrize("fn", ["kda_chunk_prefill", "kda_chunk_prefill_f32"])
+PREFILL_ENTRIES = ["kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_chunk_prefill_fullrange",
+                   "kda_chunk_prefill_noalloc"]
+
+
+@pytest.mark.parametrize("fn", PREFILL_ENTRIES)
 def test_validation_statuses(kda_lib, fn):
     assert call(fn, q=0) == kda.KDA_ERR_NULL
     assert call(fn, cu=0) == kda.KDA_ERR_NULL
@@ -59,7 +63,8 @@ def test_validation_statuses(kda_lib, fn):
     assert call(fn, T=-1) == kda.KDA_ERR_SHAPE
     assert call(fn, H=0) == kda.KDA_ERR_SHAPE
     assert call(fn, dk=96, dv=96) == kda.KDA_ERR_UNSUPPORTED
-    assert call(fn, N=2000) == kda.KDA_ERR_UNSUPPORTED
+    assert call(fn, dk=128, dv=32) == kda.KDA_ERR_UNSUPPORTED
+    assert call(fn, dk=256, dv=128) == kda.KDA_ERR_UNSUPPORTED
     assert call(fn, q=A + 8) == kda.KDA_ERR_ALIGN
     assert call(fn, beta=A + 2) == kda.KDA_ERR_ALIGN
     assert call(fn, out=A + 16) == kda.KDA_ERR_ALIAS                                  # out overlaps q
@@ -77,6 +82,30 @@ def _has_gpu():
 @pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
 def test_exact_state_alias_passes_validation(kda_lib):
     assert call(s0=A + (40 << 20), s1=A + (40 << 20)) == kda.KDA_ERR_DEVICE
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+@pytest.mark.parametrize("fn", PREFILL_ENTRIES)
+def test_every_head_size_and_many_sequences_pass_validation(kda_lib, fn):
+    """dk, dv in {64, 128} in every combination, for both dtypes, and more
+    than 1024 sequences: all pass the checks (and reach the device check)."""
+    for dk in (64, 128):
+        for dv in (64, 128):
+            assert call(fn, dk=dk, dv=dv) == kda.KDA_ERR_DEVICE, (dk, dv)
+    assert call(fn, N=2000) == kda.KDA_ERR_DEVICE
+
+
+@pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
+def test_noalloc_checks_arguments_before_its_limit(kda_lib):
+    """The no-allocation entry checks its arguments as kda_chunk_prefill does,
+    then its own limit on N."""
+    n = kda.KDA_NOALLOC_MAX_SEQS + 1
+    cu = A + (80 << 20)                   # room for N + 1 entries
+    assert call("kda_chunk_prefill_noalloc", N=n, cu=cu, q=0) == kda.KDA_ERR_NULL
+    assert call("kda_chunk_prefill_noalloc", N=n, cu=cu, q=A + 8) == kda.KDA_ERR_ALIGN
+    assert call("kda_chunk_prefill_noalloc", N=n, cu=cu, out=A + 16) == kda.KDA_ERR_ALIAS
+    assert call("kda_chunk_prefill_noalloc", N=n, cu=cu) == kda.KDA_ERR_NOALLOC_LIMIT
+    assert call("kda_chunk_prefill_noalloc", N=n - 1, cu=cu) == kda.KDA_ERR_DEVICE
 
 
 @pytest.mark.skipif(_has_gpu(), reason="valid call with fake addresses: CPU-only check")
@@ -102,8 +131,7 @@ def test_slots_validation_statuses(kda_lib):
     assert call_slots(pool=0) == kda.KDA_ERR_NULL
     assert call_slots(num_slots=0) == kda.KDA_ERR_SHAPE
     assert call_slots(N=0) == kda.KDA_ERR_SHAPE
-    assert call_slots(dk=64, dv=64) == kda.KDA_ERR_UNSUPPORTED
-    assert call_slots(N=2000) == kda.KDA_ERR_UNSUPPORTED
+    assert call_slots(dk=96, dv=64) == kda.KDA_ERR_UNSUPPORTED
     assert call_slots(slots=A + (1 << 19) + 2) == kda.KDA_ERR_ALIGN
     assert call_slots(pool=A + (40 << 20) + 8) == kda.KDA_ERR_ALIGN
     assert call_slots(pool=A) == kda.KDA_ERR_ALIAS                                     # pool over q
@@ -115,6 +143,9 @@ def test_slots_validation_statuses(kda_lib):
 def test_slots_valid_call_passes_validation(kda_lib):
     assert call_slots() == kda.KDA_ERR_DEVICE
     assert call_slots(pool=A + (40 << 20) + 5 * 2 * 128 * 128 * 4) == kda.KDA_ERR_DEVICE   # pool just past
+    assert call_slots(dk=64, dv=64) == kda.KDA_ERR_DEVICE
+    assert call_slots(dk=64, dv=128) == kda.KDA_ERR_DEVICE
+    assert call_slots(N=2000) == kda.KDA_ERR_DEVICE
 
 
 def call_decode(**over):

@@ -114,12 +114,43 @@ def test_p1_full_width_chunk64():
     assert rel_l2(s, s_ref) <= 1e-12
 
 
+def strong_gates(g, kind, rng):
+    """Gate regimes beyond U[-0.2, 0]: U[-3, 0]; a few channels at -20 on
+    every row (alpha ~ 2e-9); 5% of the entries positive, U[0, 0.5]."""
+    g = np.array(g)
+    if kind == "u3":
+        return g * 15.0
+    if kind == "alpha0":
+        g[:, :, rng.choice(g.shape[2], 3, replace=False)] = -20.0
+        return g
+    pos = rng.uniform(size=g.shape) < 0.05
+    g[pos] = rng.uniform(0.0, 0.5, size=int(pos.sum()))
+    return g
+
+
+@pytest.mark.parametrize("kind", ["u3", "alpha0", "mixed"])
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_p1_chunked_matches_recurrence_for_strong_and_mixed_gates(kind, chunk):
+    """P1 again where the per-pair decays exp(G_i - G_j) span hundreds of
+    e-folds (or grow): the chunked route forms each one directly."""
+    case = random_case([37, 130, 64, 95], H=2, dk=32, dv=24, seed=20 + chunk)
+    case["g"] = strong_gates(case["g"], kind, np.random.default_rng(chunk))
+    o_ref, s_ref = run(case)
+    o, s = run(case, chunk=chunk)
+    assert np.isfinite(o).all() and np.isfinite(s).all()
+    assert rel_l2(o, o_ref) <= 1e-12
+    assert rel_l2(s, s_ref) <= 1e-12
+
+
 # --------------------------------------------------------------------------
 # P3 / P4: beta = 0 leaves the state only decayed; alpha = 1 too: nothing moves
 # --------------------------------------------------------------------------
+@pytest.mark.parametrize("gates", ["u02", "u3", "alpha0", "mixed"])
 @pytest.mark.parametrize("chunk", [0, 64])
-def test_p3_beta_zero_only_decays(chunk):
+def test_p3_beta_zero_only_decays(chunk, gates):
     case = random_case([90, 41], H=2, dk=16, dv=8, seed=5)
+    if gates != "u02":
+        case["g"] = strong_gates(case["g"], gates, np.random.default_rng(5))
     case["beta"][:] = 0.0
     o, s = run(case, chunk=chunk)
     cu, g, q, s0 = case["cu_seqlens"], case["g"], case["q"], case["initial_state"]

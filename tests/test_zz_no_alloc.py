@@ -5,9 +5,12 @@ Some callers cannot allocate device memory per call: a serving runtime that
 lays out all of its device memory when a model is loaded, or a layer library
 that is handed only its tensors.  For them the scheduling table that a large
 packed batch needs lives in a static array inside the library, shared by
-every call.  The GPU test therefore makes two calls in a row, on different
-batches, and checks each against the regular entry point within the parity
-tolerances of the other GPU tests.  This file is collected last.
+every call.  The GPU test therefore makes calls in a row, on different
+batches -- up to KDA_NOALLOC_MAX_SEQS sequences, the size of that array --
+and checks each against the regular entry point bit for bit: the per-sequence
+arithmetic does not depend on which SM runs a sequence or when, so the two
+entry points must give the same bytes.  The largest batch is also checked
+against the fp64 oracle on sampled sequences.  This file is collected last.
 """
 import ctypes
 
@@ -23,9 +26,14 @@ def _workloads():
     many = [int(x) for x in rng.integers(0, 96, size=600)]      # 600 short sequences, some empty
     many[17] = 0
     many[300] = 200
+    edge = [int(x) for x in rng.integers(0, 9, size=kda.KDA_NOALLOC_MAX_SEQS)]   # the limit itself
+    edge[0] = 0
+    edge[-1] = 0
+    edge[5000] = 130
     return [syn.Workload("many600", many, H=2, dk=128, dv=128, init_state=True, seed=21),
             syn.Workload("packed16", [90, 45, 1397, 48, 1088, 385, 352, 1002, 0, 209, 317, 563, 50, 154, 667, 491],
-                         H=4, dk=128, dv=128, init_state=True, seed=22)]
+                         H=4, dk=128, dv=128, init_state=True, seed=22),
+            syn.Workload("edge16384", edge, H=2, dk=128, dv=128, init_state=True, seed=23)]
 
 
 def _noalloc_call(t, d, cu, s0, w):
@@ -40,30 +48,48 @@ def _noalloc_call(t, d, cu, s0, w):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_regular_entry_on_two_calls_in_a_row():
-    from gpu_util import OUT_TOL, STATE_TOL, inputs_to_dev, out_to_f64, rel_l2, run_gpu, to_dev, torch
+def test_noalloc_matches_regular_entry_on_calls_in_a_row():
+    from gpu_util import OUT_TOL, STATE_TOL, inputs_to_dev, oracle_run, out_to_f64, rel_l2, run_gpu, to_dev, torch
     t = torch()
     results = []
     for w in _workloads():
-        d = inputs_to_dev(syn.draw(w))
+        x = syn.draw(w)
+        d = inputs_to_dev(x)
         s0 = to_dev(syn.draw_initial_state(w))
         cu = t.from_numpy(np.asarray(w.cu_seqlens(), dtype=np.int32)).cuda()
         o_na, f_na = _noalloc_call(t, d, cu, s0, w)
         o_ref, f_ref = run_gpu(d, cu, s0=s0)
-        results.append((w.name, o_na, f_na, o_ref, f_ref))
+        results.append((w, x, o_na, f_na, o_ref, f_ref))
     t.cuda.synchronize()
     assert kda.device_error(reset=True) == 0
-    for name, o_na, f_na, o_ref, f_ref in results:
-        assert rel_l2(out_to_f64(o_na), out_to_f64(o_ref)) <= OUT_TOL, name
-        assert rel_l2(f_na.cpu().numpy(), f_ref.cpu().numpy()) <= STATE_TOL, name
+    for w, x, o_na, f_na, o_ref, f_ref in results:
+        assert t.equal(o_na, o_ref), w.name
+        assert t.equal(f_na, f_ref), w.name
+    # the batch at the limit against the oracle, on sampled sequences
+    w, x, o_na, f_na, _, _ = results[-1]
+    cu = w.cu_seqlens()
+    s0 = syn.draw_initial_state(w)
+    picks = [5000] + [int(n) for n in np.random.default_rng(9).choice(w.N, size=24, replace=False)]
+    o = out_to_f64(o_na)
+    f = f_na.cpu().numpy().astype(np.float64)
+    for n in picks:
+        lo, hi = int(cu[n]), int(cu[n + 1])
+        xs = {k: v[lo:hi] for k, v in x.items()}
+        o_ref, f_ref = oracle_run(xs, np.array([0, hi - lo], dtype=np.int32), s0[n:n + 1])
+        if hi > lo:
+            assert rel_l2(o[lo:hi], o_ref) <= OUT_TOL, n
+        assert rel_l2(f[n:n + 1], f_ref) <= STATE_TOL, n
 
 
 def test_noalloc_rejects_too_many_sequences():
-    """N above the library-held table's size is refused before anything runs."""
+    """N above the library-held table's size is refused before anything runs
+    (the other checks, which come first, pass on these never-dereferenced
+    addresses)."""
     lib = kda.load()
-    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the size check comes first
     n = kda.KDA_NOALLOC_MAX_SEQS + 1
-    st = lib.kda_chunk_prefill_noalloc(fake, fake, fake, fake, fake, fake, None, fake, None,
-                                       n, 64, 2, 128, 128, None)
+    T, H, d = 64, 2, 128
+    base, step = 1 << 24, 1 << 22          # distinct, 16-byte aligned, far apart
+    q, k, v, g, beta, cu, out = (ctypes.c_void_p(base + i * step) for i in range(7))
+    st = lib.kda_chunk_prefill_noalloc(q, k, v, g, beta, cu, None, out, None, n, T, H, d, d, None)
     assert st == kda.KDA_ERR_NOALLOC_LIMIT
     assert "KDA_NOALLOC_MAX_SEQS" in kda.status_string(st)
