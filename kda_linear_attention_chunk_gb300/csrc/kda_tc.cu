@@ -1416,6 +1416,42 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     const int U = p.N * p.H;
     int *order = sm.ptr<int>(kOffOrder);
 
+    // Launched with programmatic stream serialisation, this CTA may start while
+    // the kernel before it on the stream is still running: the set-up below
+    // (barriers, TMEM, tensor maps) touches no global memory; griddepcontrol.wait
+    // then holds every thread until that kernel has completed and its writes
+    // are visible, before the first global access.  launch_dependents lets the
+    // next kernel's CTAs be placed as SMs free up.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid == 0) {
+        *sm.abort_flag() = 0;
+        for (int i = 0; i < 2; i++) {
+            mbar_init(sm.bar(kBarKQFull + i), 1);
+            mbar_init(sm.bar(kBarVFull + i), 1);
+            mbar_init(sm.bar(kBarPrepDone + i), 1);
+            mbar_init(sm.bar(kBarAFull + i), 1);
+            mbar_init(sm.bar(kBarEDone + i), kEThreads);
+            mbar_init(sm.bar(kBarODone + i), 1);
+            mbar_init(sm.bar(kBarFmReady + i), kGroupThreads);
+            mbar_init(sm.bar(kBarKmFree + i), 1);
+            mbar_init(sm.bar(kBarWReady + i), kGroupThreads);
+        }
+        mbar_init(sm.bar(kBarGFull), 1);
+        mbar_init(sm.bar(kBarMma1), 1);
+        mbar_init(sm.bar(kBarMma3), 1);
+        mbar_init(sm.bar(kBarDrain), 3);
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(sm.u32(kOffMisc), kTmCols);
+        tmem_relinquish();
+        if ((tid & 31) == 0) {
+            tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tg);
+            tma_prefetch_desc(&to);
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     // schedule: sequences sorted by length, longest first (ties: lower index), dealt
     // dynamically: CTA b starts with the b-th longest unit; the rest of the
     // nonempty units (longest first) go to whichever CTA claims them next, so
@@ -1459,33 +1495,6 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             sm.sched()[0] = first ? (int)blockIdx.x : -1;
             *sm.published() = first ? 1 : 0;
             *sm.claim_done() = first ? 0 : 1;
-        }
-    }
-    if (tid == 0) {
-        *sm.abort_flag() = 0;
-        for (int i = 0; i < 2; i++) {
-            mbar_init(sm.bar(kBarKQFull + i), 1);
-            mbar_init(sm.bar(kBarVFull + i), 1);
-            mbar_init(sm.bar(kBarPrepDone + i), 1);
-            mbar_init(sm.bar(kBarAFull + i), 1);
-            mbar_init(sm.bar(kBarEDone + i), kEThreads);
-            mbar_init(sm.bar(kBarODone + i), 1);
-            mbar_init(sm.bar(kBarFmReady + i), kGroupThreads);
-            mbar_init(sm.bar(kBarKmFree + i), 1);
-            mbar_init(sm.bar(kBarWReady + i), kGroupThreads);
-        }
-        mbar_init(sm.bar(kBarGFull), 1);
-        mbar_init(sm.bar(kBarMma1), 1);
-        mbar_init(sm.bar(kBarMma3), 1);
-        mbar_init(sm.bar(kBarDrain), 3);
-        mbar_fence_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(sm.u32(kOffMisc), kTmCols);
-        tmem_relinquish();
-        if ((tid & 31) == 0) {
-            tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tg);
-            tma_prefetch_desc(&to);
         }
     }
     tc_fence_before();
@@ -1633,8 +1642,19 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     p.num_slots = a.num_slots;
     const int units = a.N * a.H;
     const int grid = units < a.num_sms ? units : a.num_sms;
-    kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tg, to, p);
-    return cudaGetLastError();
+    // one CTA per SM (shared memory), so a CTA launched early waits for an SM
+    // that the previous kernel has left; its set-up overlaps that kernel's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tg, to, p);
 }
 
 }  // namespace kda
