@@ -337,6 +337,81 @@ def measure_conv(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
                          "traffic": recorded_traffic("conv_packed16_8192_h32", CONV_SOURCES)}}
 
 
+def conv_prefill_bytes(lengths, h: int) -> int:
+    """Algorithmic bytes of one fused layer call: per row-head the x_q, x_k, x_v
+    projections (256 B each), g (512 B), beta (4 B) and out (256 B); every
+    sequence's state entry read and written (64 KiB each way) and its window
+    entry read and written (9 x H x 128 bf16 each way); the filters."""
+    t = int(sum(lengths))
+    live = sum(1 for n in lengths if n > 0)
+    return (t * h * (3 * 256 + 512 + 4 + 256) + live * h * 2 * 128 * 128 * 4 + live * 2 * 9 * h * 128 * 2 +
+            3 * h * 128 * 4 * 4)
+
+
+def measure_conv_prefill(torch, np, kda, stream, steps: int = 100, warmup: int = 10):
+    """kda_chunk_prefill_conv (SiLU) on the packed 8192-row workload at H = 32,
+    against the same layer as two calls (kda_short_conv, then
+    kda_chunk_prefill_slots): two rotating input sets, state and window pools
+    of 2 x 16 entries with the calls alternating between their halves."""
+    from kda_linear_attention_chunk_gb300 import synthetic as syn
+    n_heads = 32
+    w_ = syn.workloads()[WORKLOAD]
+    lengths = list(w_.lengths)
+    rng = np.random.default_rng(83)
+    t_rows = int(sum(lengths))
+    n = len(lengths)
+    sets = []
+    for i in range(2):
+        xs = [torch.from_numpy(rng.standard_normal((t_rows, n_heads, 128)).astype(np.float32)).to(torch.bfloat16).cuda()
+              for _ in range(3)]
+        g = torch.from_numpy((-0.2 * rng.random((t_rows, n_heads, 128))).astype(np.float32)).cuda()
+        beta = torch.from_numpy(rng.random((t_rows, n_heads)).astype(np.float32)).cuda()
+        out = torch.empty((t_rows, n_heads, 128), dtype=torch.bfloat16, device="cuda")
+        qkv = tuple(torch.empty_like(xs[0]) for _ in range(3))
+        sets.append((xs, g, beta, out, qkv))
+    w = torch.from_numpy((0.5 * rng.standard_normal((3, n_heads * 128, 4))).astype(np.float32)).cuda()
+    pool = torch.zeros((2 * n, 3, 3, n_heads * 128), dtype=torch.bfloat16, device="cuda")
+    spool = torch.from_numpy((0.02 * rng.standard_normal((2 * n, n_heads, 128, 128))).astype(np.float32)).cuda()
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)).cuda()
+    tables = [torch.arange(0, n, dtype=torch.int32, device="cuda"), torch.arange(n, 2 * n, dtype=torch.int32, device="cuda")]
+
+    def fused(i):
+        xs, g, beta, out, _ = sets[i % 2]
+        kda.chunk_prefill_conv(xs[0], xs[1], xs[2], w, g, beta, cu, pool, spool, slots=tables[(i // 2) % 2],
+                               activation="silu", out=out, stream=stream)
+
+    def two_calls(i):
+        xs, g, beta, out, qkv = sets[i % 2]
+        sl = tables[(i // 2) % 2]
+        q, k, v = kda.short_conv(xs[0], xs[1], xs[2], w, cu, pool, conv_slots=sl, activation="silu", out=qkv,
+                                 stream=stream)
+        kda.chunk_prefill_slots(q, k, v, g, beta, cu, sl, spool, out=out, stream=stream)
+
+    def timed(fn):
+        for i in range(warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(steps):
+            fn(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / steps
+
+    ms = timed(fused)
+    ms2 = timed(two_calls)
+    alg = conv_prefill_bytes(lengths, n_heads)
+    peak, _ = peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    return {"workload": "conv_prefill_packed16_8192_h32", "kernel": "kda_tc_kernel (fused prologue)",
+            "T": t_rows, "N": n, "H": n_heads, "activation": "silu", "steps": steps, "us_per_call": ms * 1e3,
+            "tokens_per_s": t_rows / (ms / 1e3), "two_calls_us_per_step": ms2 * 1e3,
+            "l2": "2 rotating input sets of 470 MB each",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": alg, "traffic": None}}
+
+
 FOLD_W = 8   # speculative window: 8 draft tokens a sequence
 
 
@@ -565,6 +640,7 @@ def run_gpu_arm(args):
     decode = measure_decode(torch, np, kda, stream) if not args.no_decode else None
     fold = measure_fold(torch, np, kda, stream) if not args.no_decode else None
     conv = measure_conv(torch, np, kda, stream) if not args.no_decode else None
+    conv_prefill = measure_conv_prefill(torch, np, kda, stream) if not args.no_decode else None
     decode_conv = measure_decode_conv(torch, np, kda, stream) if not args.no_decode else None
     configs = measure_configs(torch, np, kda, stream) if not args.no_configs else None
     assert kda.device_error() == 0, "device error word set during the bench"
@@ -605,6 +681,7 @@ def run_gpu_arm(args):
         line["fold"] = fold
     if conv is not None:
         line["conv"] = conv
+        line["conv_prefill"] = conv_prefill
     if decode_conv is not None:
         line["decode_conv"] = decode_conv
     if configs is not None:

@@ -20,8 +20,11 @@
  * --------------------------------------
  *  Pointers   all tensor pointers are DEVICE pointers; every tensor is dense
  *             and row-major (innermost index last).  The caller owns every
- *             buffer.  The library allocates nothing per call, keeps no
- *             pointer after return, and is reentrant across streams.
+ *             buffer.  The library keeps no pointer after return and is
+ *             reentrant across streams.  It allocates nothing per call,
+ *             except in split mode (below), which takes a few MB of device
+ *             memory on the call's stream from a pool of the library's own
+ *             (kept for later calls) and returns them when the call ends.
  *  Async      calls are asynchronous on `stream` (a cudaStream_t; NULL = the
  *             legacy default stream).  The host never reads cu_seqlens and
  *             never synchronises.
@@ -44,6 +47,18 @@
  *  Kernels    bf16 with dk = dv = 128 runs on the tensor-core kernel; every
  *             other head size, every fp32 call and kda_chunk_prefill_fullrange
  *             run on the CUDA-core kernel (fp32 arithmetic throughout).
+ *  Split      the tensor-core kernel is one CTA per SM taking whole
+ *             (sequence, head) units, each unit's chunks one after another.
+ *             For calls with few units (N * H at most half the SMs, T >= 1024,
+ *             N <= 256) it runs in split mode instead: one SM per unit keeps
+ *             that unit's state chain, and every other SM prepares chunks of
+ *             any unit (the part of a chunk's work that does not depend on the
+ *             state), handing them over through a ring in device memory.  The
+ *             results are the same bytes.  The environment variable KDA_SPLIT,
+ *             read on every call, overrides the choice: "0" never splits, "1"
+ *             splits every call that allows it (T >= 1 in place of 1024).
+ *             A call that cannot get its ring or its cooperative launch runs
+ *             unsplit.
  *  Range      the tensor-core kernel rounds its MMA operands to fp16 (fp32
  *             accumulation) and splits each in-chunk decay exp(G_i - G_j)
  *             into exp(G_i - G_m) exp(G_m - G_j) around the chunk's middle
@@ -200,6 +215,58 @@ int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t
                             uint16_t *out, int N, int T, int H, int dk, int dv, void *stream);
 
 /*
+ * kda_chunk_prefill_conv -- the short-conv + L2-norm prologue of
+ * kda_short_conv fused into the tensor-core prefill, as a KDA layer runs it
+ * (kern-k3-pp-prefill README: section "P: the packed prefill" runs the KDA
+ * layers with per-sequence conv windows and states; section "D inside SGLang"
+ * keeps both in the engine's pools, indexed by the same slot ids).  For every
+ * sequence n, with e its pool entry (slots[n], or n when slots is NULL):
+ *
+ *     q, k, v = the conv of kda_short_conv over [window e ; the sequence's
+ *               rows of xq, xk, xv] (optional SiLU; q and k scaled to unit L2
+ *               norm per head with eps), rounded to bf16 as kda_short_conv's
+ *               outputs are;
+ *     then kda_chunk_prefill_slots on those q, k, v with the state pool entry e;
+ *     the window e becomes the last three rows of [old taps ; the rows].
+ *
+ * q, k and v are formed in shared memory inside the kernel and never written
+ * to global memory; the prologue's arithmetic is kda_short_conv's, in the same
+ * order, so results and windows equal kda_short_conv followed by
+ * kda_chunk_prefill_slots bit for bit.  Speed: the call saves the round trip
+ * of q, k and v through global memory (402 MB for 8192 rows at H = 32), but
+ * the prologue's arithmetic lengthens the prefill kernel's busiest role, and
+ * on a GB300 the two calls are faster (about 251 us against 293 us at that
+ * shape); use this call where memory traffic or capacity is the constraint.
+ *
+ *   xq, xk, xv   bf16 bits [T][H][128]: the layer's projections.
+ *   conv_weight  fp32 [3][H*128][4], as for kda_short_conv.
+ *   g, beta      fp32 [T][H][128], [T][H].
+ *   cu_seqlens   int32 [N+1], device memory.
+ *   slots        int32 [N], device memory, or NULL (entry n in both pools).
+ *                -1 marks a padded sequence: nothing of it is computed or
+ *                written (out rows, state, window).  An id that is not an
+ *                entry of both pools is treated like -1 and sets bit 8.
+ *   conv_pool    bf16 bits [conv_num_slots][3 taps][3 streams][H*128], the
+ *                windows, updated in place (the layout kda_short_conv uses).
+ *   state_pool   fp32 [num_slots][H][128][128], updated in place.
+ *   out          bf16 bits [T][H][128].
+ *   N, T, H      as for kda_chunk_prefill; with slots NULL, num_slots and
+ *                conv_num_slots must be at least N.
+ *   dk, dv       128 (else KDA_ERR_UNSUPPORTED).
+ *   activation   0 (none) or 1 (SiLU); eps >= 0, as for kda_short_conv.
+ * The decay range is that of the tensor-core kernel (bit 32, "Range" above).
+ * Tensor pointers must be 16-byte aligned (beta, cu_seqlens and slots
+ * 4-byte); out and the pools must not overlap an input or each other.
+ * Returns a kda_status.
+ */
+int kda_chunk_prefill_conv(const uint16_t *xq, const uint16_t *xk, const uint16_t *xv,
+                           const float *conv_weight, const float *g, const float *beta,
+                           const int32_t *cu_seqlens, const int32_t *slots, uint16_t *conv_pool,
+                           int conv_num_slots, float *state_pool, int num_slots, uint16_t *out,
+                           int N, int T, int H, int dk, int dv, int activation, float eps,
+                           void *stream);
+
+/*
  * kda_decode -- one step of the recurrence for each of N sequences (one new
  * token each), the decode that runs between prefills (kern-k3-pp-prefill
  * README: the KDA step over a rank's heads on the engine's state pool, padded
@@ -244,9 +311,10 @@ int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
  *     the window becomes [taps 1, 2 ; x_n].
  *
  * One kernel: one CTA per (sequence, head) computes that head's conv once,
- * steps all its value rows and rewrites its channels of the window.  Results differ from
- * kda_short_conv followed by kda_decode only in that q, k and v are not
- * rounded to bf16 between the two.
+ * steps all its value rows and rewrites its channels of the window; it is
+ * faster than kda_short_conv followed by kda_decode (on a GB300, 64 sequences
+ * x 32 heads: about 48 us against 58 us).  Results differ from those two
+ * calls only in that q, k and v are not rounded to bf16 between them.
  *
  *   xq, xk, xv   bf16 bits [N][H][dk|dv]: the step's projections.
  *   conv_weight  fp32 [3][H*128][4], as for kda_short_conv.

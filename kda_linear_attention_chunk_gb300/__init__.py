@@ -20,8 +20,8 @@ KDA_ERR_NOALLOC_LIMIT = 8
 KDA_NOALLOC_MAX_SEQS = 16384
 
 EXPORTED = ("kda_chunk_prefill", "kda_chunk_prefill_f32", "kda_chunk_prefill_fullrange", "kda_status_string",
-            "kda_device_error", "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_decode",
-            "kda_fold_commit", "kda_short_conv", "kda_decode_conv")
+            "kda_device_error", "kda_chunk_prefill_noalloc", "kda_chunk_prefill_slots", "kda_chunk_prefill_conv",
+            "kda_decode", "kda_fold_commit", "kda_short_conv", "kda_decode_conv")
 # device error word bits (kda_device_error)
 ERR_WAIT_TIMEOUT = 1    # a bounded wait ran out; the kernel wound down early
 ERR_BAD_SEQLENS = 2     # a cu_seqlens entry broke its contract (clamped)
@@ -55,6 +55,9 @@ def load(path: str = LIB_PATH):
         fn.restype = I
     lib.kda_chunk_prefill_slots.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, P]
     lib.kda_chunk_prefill_slots.restype = I
+    lib.kda_chunk_prefill_conv.argtypes = [P, P, P, P, P, P, P, P, P, I, P, I, P, I, I, I, I, I, I,
+                                           ctypes.c_float, P]
+    lib.kda_chunk_prefill_conv.restype = I
     lib.kda_decode.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, P]
     lib.kda_decode.restype = I
     lib.kda_fold_commit.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
@@ -115,6 +118,15 @@ def kda_chunk_prefill_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_poo
     """Raw C-ABI call with the states in a slot-addressed pool."""
     return load().kda_chunk_prefill_slots(q, k, v, g, beta, cu_seqlens, state_slots, state_pool,
                                           num_slots, out, N, T, H, dk, dv, stream)
+
+
+def kda_chunk_prefill_conv(xq, xk, xv, conv_weight, g, beta, cu_seqlens, slots, conv_pool, conv_num_slots: int,
+                           state_pool, num_slots: int, out, N: int, T: int, H: int, dk: int, dv: int,
+                           activation: int, eps: float, stream) -> int:
+    """Raw C-ABI call: the short-conv prologue fused into the prefill."""
+    return load().kda_chunk_prefill_conv(xq, xk, xv, conv_weight, g, beta, cu_seqlens, slots, conv_pool,
+                                         conv_num_slots, state_pool, num_slots, out, N, T, H, dk, dv, activation,
+                                         eps, stream)
 
 
 def kda_decode(q, k, v, g, beta, state_slots, state_pool, num_slots: int, out, N: int, H: int, dk: int, dv: int,
@@ -349,6 +361,54 @@ def short_conv(xq, xk, xv, conv_weight, cu_seqlens, conv_pool, conv_slots=None, 
     if st != KDA_OK:
         raise KdaError(st, "kda_short_conv")
     return q, k, v
+
+
+def chunk_prefill_conv(xq, xk, xv, conv_weight, g, beta, cu_seqlens, conv_pool, state_pool, slots=None,
+                       activation: str = "silu", eps: float = 1e-6, out=None, stream=None):
+    """A KDA layer's prefill with the short-conv + L2-norm prologue fused in,
+    on torch CUDA tensors.
+
+    xq, xk, xv: [T][H][128] bfloat16 projections; conv_weight: [3][H*128][4]
+    float32; g: [T][H][128] float32; beta: [T][H] float32; cu_seqlens: [N+1]
+    int32; conv_pool: [conv_num_slots][3][3][H*128] bfloat16 and state_pool:
+    [num_slots][H][128][128] float32, both updated in place; slots: [N] int32
+    (-1 = padded, skipped) or None for entry n of both pools.  Returns out
+    [T][H][128] bfloat16 (rows of padded sequences keep what ``out`` held).
+    """
+    import torch
+
+    T, H, d = xq.shape
+    N = int(cu_seqlens.shape[0]) - 1
+    tensors = [("xq", xq), ("xk", xk), ("xv", xv), ("conv_weight", conv_weight), ("g", g), ("beta", beta),
+               ("cu_seqlens", cu_seqlens), ("conv_pool", conv_pool), ("state_pool", state_pool)]
+    if slots is not None:
+        tensors.append(("slots", slots))
+        if slots.dtype != torch.int32 or tuple(slots.shape) != (N,):
+            raise ValueError("slots must be int32 [N]")
+    for name, t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if xq.dtype != torch.bfloat16 or xk.dtype != torch.bfloat16 or xv.dtype != torch.bfloat16:
+        raise ValueError("chunk_prefill_conv takes bfloat16 projections")
+    if conv_weight.dtype != torch.float32 or tuple(conv_weight.shape) != (3, H * d, 4):
+        raise ValueError("conv_weight must be float32 [3][H*d][4]")
+    if conv_pool.dtype != torch.bfloat16 or tuple(conv_pool.shape[1:]) != (3, 3, H * d):
+        raise ValueError("conv_pool must be bfloat16 [num_slots][3][3][H*d]")
+    if state_pool.dtype != torch.float32 or tuple(state_pool.shape[1:]) != (H, d, d):
+        raise ValueError("state_pool must be float32 [num_slots][H][d][d]")
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}")
+    if out is None:
+        out = torch.empty((T, H, d), dtype=xq.dtype, device=xq.device)
+    s = stream if stream is not None else torch.cuda.current_stream(xq.device)
+    handle = int(s.cuda_stream) if hasattr(s, "cuda_stream") else int(s)
+    st = kda_chunk_prefill_conv(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(conv_weight), _ptr(g), _ptr(beta),
+                                _ptr(cu_seqlens), _ptr(slots), _ptr(conv_pool), int(conv_pool.shape[0]),
+                                _ptr(state_pool), int(state_pool.shape[0]), _ptr(out), N, T, H, d, d,
+                                ACTIVATIONS[activation], float(eps), handle)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_prefill_conv")
+    return out
 
 
 def decode_conv(xq, xk, xv, conv_weight, conv_pool, g, beta, state_pool, conv_slots=None, state_slots=None,

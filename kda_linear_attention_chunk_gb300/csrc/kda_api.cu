@@ -3,6 +3,7 @@
 // before any CUDA call, so a rejected call touches no device state.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
@@ -36,6 +37,7 @@ struct DevInfo {
     int num_sms = 0;
     int *err = nullptr;
     unsigned int *sched = nullptr;
+    cudaMemPool_t pool = nullptr;  // the library's own stream-ordered pool (split mode's ring); null: none
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -74,6 +76,23 @@ int init_device(DevInfo &d, int dev)
     d.num_sms = sms;
     d.err = (int *)err;
     d.sched = (unsigned int *)sched;
+    // a pool of the library's own, which keeps what it has reserved (a few MB
+    // per call in split mode), so that calls after the first allocate nothing
+    // from the driver; without it split mode is off
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+        uint64_t keep = ~uint64_t(0);
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) == cudaSuccess) {
+            d.pool = pool;
+        } else {
+            cudaMemPoolDestroy(pool);
+        }
+    }
+    cudaGetLastError();
     d.checked.store((major == 10 && minor == 3) ? 1 : -1, std::memory_order_release);
     return KDA_OK;
 }
@@ -194,6 +213,46 @@ const char *kda_status_string(int status)
     }
 }
 
+// Split mode (kda.h, kda_chunk_prefill): on for calls of few units, unless
+// the environment variable KDA_SPLIT says otherwise ("0" never, "1" whenever
+// the call allows it).
+bool want_split(const kda::KdaArgs &a, const DevInfo *d)
+{
+    // (the producers pack a chunk index into 23 bits: far beyond any T that fits the device)
+    if (!d->pool || a.T == 0 || a.T >= (1 << 29) || !kda::tc_split_possible(a.N * a.H, a.N, d->num_sms))
+        return false;
+    const char *env = getenv("KDA_SPLIT");
+    if (env && env[0] == '0') return false;
+    if (env && env[0] == '1') return true;
+    return a.T >= 1024;
+}
+
+// the tensor-core kernel, split when that pays: the ring comes from the
+// library's pool on the call's stream and goes back to it after the launch
+cudaError_t launch_tc(kda::KdaArgs &a, const DevInfo *d)
+{
+    if (!want_split(a, d)) return kda::launch_kda_tc_bf16_d128(a);
+    const int units = a.N * a.H;
+    const size_t bytes = kda::tc_split_bytes(units), flag_bytes = kda::tc_split_flag_bytes(units);
+    void *ring = nullptr;
+    if (cudaMallocFromPoolAsync(&ring, bytes, d->pool, a.stream) != cudaSuccess) {
+        cudaGetLastError();
+        return kda::launch_kda_tc_bf16_d128(a);
+    }
+    cudaError_t e = cudaMemsetAsync((uint8_t *)ring + bytes - flag_bytes, 0, flag_bytes, a.stream);
+    if (e == cudaSuccess) {
+        a.split_ring = (uint8_t *)ring;
+        e = kda::launch_kda_tc_bf16_d128(a);
+        a.split_ring = nullptr;
+        if (e == cudaErrorCooperativeLaunchTooLarge) {   // the device cannot hold every CTA at once now
+            cudaGetLastError();
+            e = kda::launch_kda_tc_bf16_d128(a);
+        }
+    }
+    const cudaError_t ef = cudaFreeAsync(ring, a.stream);
+    return e != cudaSuccess ? e : ef;
+}
+
 int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
                       const float *beta, const int32_t *cu_seqlens, const float *initial_state,
                       uint16_t *out, float *final_state, int N, int T, int H, int dk, int dv,
@@ -206,7 +265,7 @@ int kda_chunk_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
     if ((st = device_info(&d)) != KDA_OK) return st;
     kda::KdaArgs a = make_args(q, k, v, g, beta, cu_seqlens, initial_state, out, final_state, N, T, H,
                                dk, dv, stream, d);
-    const cudaError_t e = (dk == 128 && dv == 128) ? kda::launch_kda_tc_bf16_d128(a) : kda::launch_kda_simt(a, false);
+    const cudaError_t e = (dk == 128 && dv == 128) ? launch_tc(a, d) : kda::launch_kda_simt(a, false);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -256,8 +315,51 @@ int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t
                                dk, dv, stream, d);
     a.state_slots = state_slots;
     a.num_slots = num_slots;
-    const cudaError_t e = (dk == 128 && dv == 128) ? kda::launch_kda_tc_bf16_d128(a) : kda::launch_kda_simt(a, false);
+    const cudaError_t e = (dk == 128 && dv == 128) ? launch_tc(a, d) : kda::launch_kda_simt(a, false);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_chunk_prefill_conv(const uint16_t *xq, const uint16_t *xk, const uint16_t *xv, const float *conv_weight,
+                           const float *g, const float *beta, const int32_t *cu_seqlens, const int32_t *slots,
+                           uint16_t *conv_pool, int conv_num_slots, float *state_pool, int num_slots, uint16_t *out,
+                           int N, int T, int H, int dk, int dv, int activation, float eps, void *stream)
+{
+    if (!cu_seqlens || !conv_weight || !conv_pool || !state_pool) return KDA_ERR_NULL;
+    if (N < 1 || T < 0 || H < 1 || num_slots < 1 || conv_num_slots < 1) return KDA_ERR_SHAPE;
+    if (!slots && (num_slots < N || conv_num_slots < N)) return KDA_ERR_SHAPE;
+    if (activation != 0 && activation != 1) return KDA_ERR_SHAPE;
+    if (!(eps >= 0.f && eps <= 3.0e38f)) return KDA_ERR_SHAPE;   // also rejects NaN
+    if ((size_t)conv_num_slots * (size_t)H * 128 * 9 * 2 >= ((size_t)1 << 40)) return KDA_ERR_SHAPE;
+    // the prefill's own checks, the state pool as both initial and final state
+    int st = validate(xq, xk, xv, g, beta, cu_seqlens, state_pool, out, state_pool, N, T, H, dk, dv,
+                      sizeof(uint16_t), slots, num_slots);
+    if (st != KDA_OK) return st;
+    if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+    if (!aligned16(conv_weight) || !aligned16(conv_pool)) return KDA_ERR_ALIGN;
+    const size_t rows = (size_t)T * H;
+    const Range rw = range_of(conv_weight, (size_t)3 * H * 128 * 4 * sizeof(float));
+    const Range rp = range_of(conv_pool, (size_t)conv_num_slots * 9 * H * 128 * 2);
+    const Range others[] = {range_of(xq, rows * 256), range_of(xk, rows * 256), range_of(xv, rows * 256),
+                            range_of(g, rows * 128 * sizeof(float)), range_of(beta, rows * sizeof(float)),
+                            range_of(cu_seqlens, (size_t)(N + 1) * sizeof(int32_t)),
+                            range_of(slots, (size_t)N * sizeof(int32_t)),
+                            range_of(state_pool, (size_t)num_slots * H * 128 * 128 * sizeof(float)),
+                            range_of(out, rows * 256)};
+    for (const Range &r : others)
+        if (overlap(rp, r) || overlap(rw, r)) return KDA_ERR_ALIAS;
+    if (overlap(rp, rw)) return KDA_ERR_ALIAS;
+    DevInfo *d = nullptr;
+    if ((st = device_info(&d)) != KDA_OK) return st;
+    kda::KdaArgs a = make_args(xq, xk, xv, g, beta, cu_seqlens, state_pool, out, state_pool, N, T, H, dk, dv,
+                               stream, d);
+    a.state_slots = slots;
+    // with a slot table an id must name an entry of both pools
+    a.num_slots = slots ? (num_slots < conv_num_slots ? num_slots : conv_num_slots) : num_slots;
+    a.conv_w = conv_weight;
+    a.conv_pool = conv_pool;
+    a.conv_act = activation;
+    a.conv_eps = eps;
+    return kda::launch_kda_tc_bf16_d128(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g, const float *beta,

@@ -21,8 +21,7 @@
 // the group and the group), with the next group's loads in flight; each row is
 // one 256-byte load and one 256-byte store per warp.  The L2 norms of a
 // group's four rows are one butterfly across the warp (ten shuffles).  The kernel is bound by instruction issue rather than by memory,
-// so the per-row code is kept short (no per-row register shifts; SiLU through
-// one tanh).  Only the warp that holds a sequence's first row reads the
+// so the per-row code is kept short (no per-row register shifts).  Only the warp that holds a sequence's first row reads the
 // sequence's window (for that row's three predecessors), so that warp also
 // writes the new window, right after reading the old one; the new taps are
 // input rows (or, for sequences shorter than three rows, old taps it holds).
@@ -74,13 +73,15 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&b);
 }
 
-// SiLU(a) = a * sigmoid(a) = (a/2) (1 + tanh(a/2)): one hardware tanh
+// SiLU(a) = a * sigmoid(a) = a / (1 + 2^(-a log2 e)).  ex2.approx and the
+// approximate division keep it to a few units of fp32 rounding (the form
+// (a/2)(1 + tanh(a/2)) through tanh.approx loses most of its digits for
+// negative a, where 1 + tanh cancels).
 __device__ __forceinline__ float silu(float a)
 {
-    const float h = 0.5f * a;
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
-    return fmaf(h, t, h);
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-a * 1.4426950408889634f));
+    return __fdividef(a, 1.f + e);
 }
 
 // cu_seqlens[i] clamped into [0, T]

@@ -135,16 +135,22 @@ __global__ void __launch_bounds__(kDecThreads, 5) kda_decode_kernel(DecodeParams
 }
 
 // ---------------------------------------------------------------------------
-// The decode step with the short conv fused in front of it.  One CTA of 1024
-// threads per (sequence, head) owns all 128 value rows (eight threads a row,
-// as in kda_decode_kernel, so token_step runs unchanged) and so alone reads
-// and rewrites the head's channels of the sequence's window.  Threads 0-255
-// compute q and k over the 128 channels (the 4-tap conv over the window's
-// three rows and the new projection row, optional SiLU, unit L2 norm per
-// head), threads 256-383 v, threads 384-511 exp(g); every thread then steps
-// its value row.  After the block's first barrier every read of the window is
-// done, and the new window (taps 1 and 2 move down, the projection row
-// becomes tap 2) is written.
+// The decode step with the short conv fused in front of it.  One CTA of 256
+// threads per (sequence, head) owns the whole head, so it alone reads and
+// rewrites the head's channels of the sequence's window, and no other CTA
+// waits on it.  Thread (part, c), part = tid / 128, convolves channel c of q
+// (part 0) or k (part 1) over the window's three rows and the new projection
+// row (optional SiLU), then channel c of v (part 0) or takes exp(g) of it
+// (part 1); the thread that read a channel's taps writes its new taps (taps 1
+// and 2 move down, the projection row becomes tap 2), since no other thread
+// touches that channel.  q and k are scaled to unit L2 norm per head after a
+// block reduction.  The 128 value rows are then stepped in four blocks of 32
+// (eight threads a row, as in kda_decode_kernel, so token_step runs unchanged).
+// All four blocks' state rows are requested before the conv and held in
+// registers (64 a thread, two CTAs per SM), so that the whole 64 KB state is
+// in flight while the slot ids, the window and the conv are dealt with
+// (measured per 64 x 32-head step: 47.9 us; two blocks in flight at three
+// CTAs per SM, 61.6 us; 512 threads a CTA, 52.0 us; 1024, 69 us).
 // ---------------------------------------------------------------------------
 struct DecodeConvParams {
     const uint16_t *xq, *xk, *xv;  // [N][H][128] bf16: this step's projections
@@ -169,69 +175,83 @@ __device__ __forceinline__ float conv4(float4 w, uint16_t t0, uint16_t t1, uint1
     return act ? y / (1.f + dec_ex2(-y * kDecLog2e)) : y;
 }
 
-constexpr int kDcThreads = 1024;   // 128 value rows x 8 threads
+constexpr int kDcThreads = 256;   // 32 value rows x 8 threads, four row blocks in turn
 
-__global__ void __launch_bounds__(kDcThreads, 1) kda_decode_conv_kernel(DecodeConvParams p)
+__global__ void __launch_bounds__(kDcThreads, 2) kda_decode_conv_kernel(DecodeConvParams p)
 {
     __shared__ float4 sa[32], sk[32], sq[32];   // exp(g), k, q of this (sequence, head), 128 each
     __shared__ float sv[128];                   // v
     __shared__ float red[8];                    // per-warp sums of y^2 (warps 0-3: q, 4-7: k)
     const int rh = blockIdx.x;                  // (sequence, head)
     const int n = rh / p.H, h = rh % p.H;
-    const int slot = decode_slot(p.slots, n, p.num_slots, p.err);
-    const int cslot = decode_slot(p.conv_slots, n, p.conv_num_slots, p.err);
-    if (slot < 0 || cslot < 0) return;   // padded row: nothing is computed or written
     const size_t row = (size_t)n * p.H + h;
     const size_t C = (size_t)p.H * 128;
     const int tid = threadIdx.x;
-    // this thread's state row goes out first: it does not depend on the conv
-    const int vr = tid >> 3, qe = tid & 7;
-    float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vr) * 128);
-    float4 s[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) s[j] = st[8 * j + qe];
-    const float beta = p.beta[row];
-    uint16_t *win = p.conv_pool + (size_t)cslot * 9 * C;       // [tap][stream][H*128]
-    const int part = tid >> 7, c = tid & 127;                  // 0 q, 1 k, 2 v, 3 g; channel
+    const int part = tid >> 7, c = tid & 127;                  // 0: q then v, 1: k then g; channel
     const size_t ch = (size_t)h * 128 + c;
-    float y = 0.f;
-    uint16_t t1 = 0, t2 = 0, xn = 0;    // the taps this thread carries into the new window
-    if (part < 3) {
-        t1 = win[(3 + part) * C + ch];
-        t2 = win[(6 + part) * C + ch];
-        xn = (part == 0 ? p.xq : part == 1 ? p.xk : p.xv)[row * 128 + c];
-        y = conv4(*reinterpret_cast<const float4 *>(p.w + ((size_t)part * C + ch) * 4), win[part * C + ch], t1, t2,
-                  xn, p.act);
-        if (part == 2) sv[c] = y;
-    } else if (part == 3) {
-        reinterpret_cast<float *>(sa)[c] = dec_ex2(p.g[row * 128 + c] * kDecLog2e);
-    }
-    if (part < 2) {
-        float y2 = y * y;
+    const int slot = decode_slot(p.slots, n, p.num_slots, p.err);
+    const int cslot = decode_slot(p.conv_slots, n, p.conv_num_slots, p.err);
+    if (slot < 0 || cslot < 0) return;   // padded row: nothing is computed or written
+    const int vl = tid >> 3, qe = tid & 7;      // value row vl of each block, its pieces 8j + qe
+    float4 *st = reinterpret_cast<float4 *>(p.pool + (((size_t)slot * p.H + h) * 128 + vl) * 128);
+    constexpr int kBlk = kDecRows * 128 / 4;    // float4 stride between row blocks
+    // every block's state rows go out first: they do not depend on the conv
+    float4 s0[4], s1[4], s2[4], s3[4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) y2 += __shfl_xor_sync(0xffffffffu, y2, o);
-        if ((tid & 31) == 0) red[tid >> 5] = y2;
+    for (int j = 0; j < 4; j++) s0[j] = st[8 * j + qe];
+#pragma unroll
+    for (int j = 0; j < 4; j++) s1[j] = st[kBlk + 8 * j + qe];
+#pragma unroll
+    for (int j = 0; j < 4; j++) s2[j] = st[2 * kBlk + 8 * j + qe];
+#pragma unroll
+    for (int j = 0; j < 4; j++) s3[j] = st[3 * kBlk + 8 * j + qe];
+    uint16_t *win = p.conv_pool + (size_t)cslot * 9 * C;       // [tap][stream][H*128]
+    const float4 wq4 = *reinterpret_cast<const float4 *>(p.w + ((size_t)part * C + ch) * 4);
+    float4 wv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint16_t ax = (part ? p.xk : p.xq)[row * 128 + c];
+    uint16_t bx = 0;
+    float gc = 0.f;
+    if (part == 0) {
+        wv4 = *reinterpret_cast<const float4 *>(p.w + ((size_t)2 * C + ch) * 4);
+        bx = p.xv[row * 128 + c];
+    } else {
+        gc = p.g[row * 128 + c];
     }
+    const float beta = p.beta[row];
+    const uint16_t a0 = win[part * C + ch], a1 = win[(3 + part) * C + ch], a2 = win[(6 + part) * C + ch];
+    uint16_t b0 = 0, b1 = 0, b2 = 0;
+    if (part == 0) { b0 = win[2 * C + ch]; b1 = win[5 * C + ch]; b2 = win[8 * C + ch]; }
+    // the taps this thread read are read by no other thread: the new window now
+    win[part * C + ch] = a1; win[(3 + part) * C + ch] = a2; win[(6 + part) * C + ch] = ax;
+    if (part == 0) { win[2 * C + ch] = b1; win[5 * C + ch] = b2; win[8 * C + ch] = bx; }
+    const float y = conv4(wq4, a0, a1, a2, ax, p.act);
+    if (part == 0) sv[c] = conv4(wv4, b0, b1, b2, bx, p.act);
+    else reinterpret_cast<float *>(sa)[c] = dec_ex2(gc * kDecLog2e);
+    float y2 = y * y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) y2 += __shfl_xor_sync(0xffffffffu, y2, o);
+    if ((tid & 31) == 0) red[tid >> 5] = y2;
     __syncthreads();
-    // every read of the window is done: the new one, this head's channels
-    if (part < 3) {
-        win[part * C + ch] = t1;
-        win[(3 + part) * C + ch] = t2;
-        win[(6 + part) * C + ch] = xn;
-    }
-    if (part < 2) {
+    {
         const float *r4 = red + 4 * part;
         const float n2 = (r4[0] + r4[1]) + (r4[2] + r4[3]);
         reinterpret_cast<float *>(part ? sk : sq)[c] = y / sqrtf(n2 + p.eps);
     }
     __syncthreads();
-    const float o = token_step(s, sa, sk, sq, qe, sv[vr], beta);
+    uint16_t *out = p.out + row * 128 + vl;
+    auto finish = [&](float4 (&s)[4], int b) {
+        const float o = token_step(s, sa, sk, sq, qe, sv[kDecRows * b + vl], beta);
 #pragma unroll
-    for (int j = 0; j < 4; j++) st[8 * j + qe] = s[j];
-    if (qe == 0) {
-        const __nv_bfloat16 ob = __float2bfloat16_rn(o);
-        p.out[row * 128 + vr] = *reinterpret_cast<const uint16_t *>(&ob);
-    }
+        for (int j = 0; j < 4; j++) st[kBlk * b + 8 * j + qe] = s[j];
+        if (qe == 0) {
+            const __nv_bfloat16 ob = __float2bfloat16_rn(o);
+            out[kDecRows * b] = *reinterpret_cast<const uint16_t *>(&ob);
+        }
+    };
+    finish(s0, 0);
+    finish(s1, 1);
+    finish(s2, 2);
+    finish(s3, 3);
 }
 
 struct FoldParams {

@@ -28,6 +28,16 @@ struct KdaArgs {
     // initial_state == final_state is then the pool [num_slots][H][dv][dk]
     const int32_t *state_slots = nullptr;    // [N], -1 = padded sequence
     int num_slots = 0;
+    // optional: the short-conv prologue fused into the tensor-core kernel; q, k,
+    // v above are then the raw projections x_q, x_k, x_v
+    const float *conv_w = nullptr;           // [3][H*128][4]
+    uint16_t *conv_pool = nullptr;           // [entries][3][3][H*128] bf16 windows, updated in place
+    int conv_act = 0;                        // 0 identity, 1 SiLU
+    float conv_eps = 0.f;
+    // optional: split mode (tensor-core kernel, no conv): the chunk ring and its
+    // flags, tc_split_bytes(N * H) bytes of device memory, the flags (the
+    // tail tc_split_flag_bytes(N * H) bytes) zeroed on the stream before the launch
+    uint8_t *split_ring = nullptr;
 };
 
 // CUDA-core kernel, any dk, dv in {64, 128}, bf16 (f32 = false) or fp32
@@ -36,6 +46,11 @@ cudaError_t launch_kda_simt(const KdaArgs &a, bool f32);
 // tensor-core kernel, bf16, dk = dv = 128 (kda_tc.cu)
 cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a);
 int tc_max_sorted_seqs();   // largest N the tensor-core kernel sorts by itself
+// split mode: whether a call of `units` (sequence, head) pairs and N sequences
+// can run split on a device of num_sms SMs, and the device memory it needs
+bool tc_split_possible(int units, int N, int num_sms);
+size_t tc_split_bytes(int units);
+size_t tc_split_flag_bytes(int units);
 
 // kda_api.cu: the checks of kda_chunk_prefill, and the current device's
 // error-word address and SM count (also checks the device)

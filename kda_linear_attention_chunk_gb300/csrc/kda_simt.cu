@@ -14,15 +14,15 @@
 //
 //   A_ij  = beta_i sum_c k_ic k_jc exp(G_ic - G_jc)      j < i   (strictly lower)
 //   B_ri  =        sum_c q_rc k_ic exp(G_rc - G_ic)      i <= r  (lower, diagonal included)
-//   T     = (I + A)^-1                                  (forward substitution)
+//   T     = (I + A)^-1                                  (blocked forward substitution)
 //   R     = diag(beta) (V - (K * exp(G)) S0)
 //   Delta = T R                                         (== U - W S0)
 //   O     = (Q * exp(G)) S0 + B Delta
 //   S1    = Diag(exp(G_{L-1})) S0 + (K * exp(G_{L-1} - G))^T Delta
 //
-// Every exponent above is <= 0 when g <= 0.  The state is complete at each
-// chunk end, so a sequence split into calls at a multiple of 64 rows gives the
-// same bits as one call.
+// Every exponent above is <= 0 when g <= 0; G is kept in base 2 (exp(x) =
+// 2^(x log2 e)).  The state is complete at each chunk end, so a sequence split
+// into calls at a multiple of 64 rows gives the same bits as one call.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -32,6 +32,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kAS = kChunk + 1;   // row stride of the 64 x 64 matrices
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct SimtParams {
     const void *q, *k, *v;
@@ -78,6 +79,115 @@ __device__ __forceinline__ void load_vec(const float *p, float (&x)[W])
     }
 }
 
+// 16 bytes of a row as fp32: 8 bf16 or 4 floats
+template <typename T> struct Piece;
+template <> struct Piece<float> {
+    static constexpr int n = 4;
+    static __device__ __forceinline__ void get(const float *src, float *dst)
+    {
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(src));
+        dst[0] = x.x; dst[1] = x.y; dst[2] = x.z; dst[3] = x.w;
+    }
+};
+template <> struct Piece<__nv_bfloat16> {
+    static constexpr int n = 8;
+    static __device__ __forceinline__ void get(const __nv_bfloat16 *src, float *dst)
+    {
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src));
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            dst[2 * e] = __uint_as_float(w[e] << 16);
+            dst[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+    }
+};
+
+// rows row0 .. row0+63 of one head of a [T][H][D] tensor -> [64][D] fp32 in
+// shared memory (rows at and past L zero); each thread's pieces are all
+// requested before the first is stored
+template <typename T, int D>
+__device__ __forceinline__ void load_tile(const T *src, float *dst, int row0, int L, size_t rs, int h, int tid)
+{
+    constexpr int P = Piece<T>::n, PR = D / P, N = (kChunk * PR + kThreads - 1) / kThreads;
+    float x[N][P];
+#pragma unroll
+    for (int k = 0; k < N; k++) {
+        const int i = tid + k * kThreads, r = i / PR, c = (i % PR) * P;
+        if (i < kChunk * PR && r < L) {
+            Piece<T>::get(src + ((size_t)(row0 + r) * rs + h) * D + c, x[k]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < P; e++) x[k][e] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < N; k++) {
+        const int i = tid + k * kThreads;
+        if (i < kChunk * PR) {
+            float *d = dst + (i / PR) * D + (i % PR) * P;
+#pragma unroll
+            for (int e = 0; e < P; e += 4) *reinterpret_cast<float4 *>(d + e) = make_float4(x[k][e], x[k][e + 1], x[k][e + 2], x[k][e + 3]);
+        }
+    }
+}
+
+// T = (I + A)^-1 for the strictly lower A in As ([64][kAS]; its upper half
+// zero).  T is unit lower triangular; T[i][j] (i > j) is written to As[j][i],
+// the upper half, so that A stays readable throughout.  In 16 x 16 blocks: the
+// diagonal blocks by forward substitution (two warps, a lane per column), then
+// T_IJ = -T_II sum_{K=J..I-1} A_IK T_KJ for I - J = 1, 2, 3 (block row I of
+// (I + A) T = I).  Callers synchronise before and after.
+__device__ void invert_unit_lower(float *As, int tid)
+{
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < 2) {
+        const int o = 16 * (2 * warp + (lane >> 4)), c = lane & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            float s = r == c ? 1.f : 0.f;
+#pragma unroll
+            for (int l = 0; l < r; l++) s = fmaf(-As[(o + r) * kAS + o + l], x[l], s);
+            x[r] = s;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; r++)
+            if (r > c) As[(o + c) * kAS + o + r] = x[r];
+    }
+    // T[16K + m][16J + c] for K >= J (transposed storage, unit diagonal implicit)
+    auto tval = [&](int K, int J, int m, int c) -> float {
+        if (K > J || m > c) return As[(16 * J + c) * kAS + 16 * K + m];
+        return m == c ? 1.f : 0.f;
+    };
+    for (int d = 1; d < 4; d++) {
+        __syncthreads();
+        const int nb = 4 - d;                                // blocks (J + d, J), J < nb
+        for (int e = tid; e < nb * 256; e += kThreads) {     // P_IJ[l][c] into T_IJ's place
+            const int J = e >> 8, I = J + d, l = (e >> 4) & 15, c = e & 15;
+            float s = 0.f;
+            for (int K = J; K < I; K++)
+#pragma unroll
+                for (int m = 0; m < 16; m++) s = fmaf(As[(16 * I + l) * kAS + 16 * K + m], tval(K, J, m, c), s);
+            As[(16 * J + c) * kAS + 16 * I + l] = s;
+        }
+        __syncthreads();
+        if (tid < nb * 16) {                                 // T_IJ[:, c] = -T_II P_IJ[:, c]
+            const int J = tid >> 4, I = J + d, c = tid & 15;
+            float pcol[16];
+#pragma unroll
+            for (int l = 0; l < 16; l++) pcol[l] = As[(16 * J + c) * kAS + 16 * I + l];
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+                float s = pcol[r];
+#pragma unroll
+                for (int l = 0; l < r; l++) s = fmaf(As[(16 * I + l) * kAS + 16 * I + r], pcol[l], s);
+                As[(16 * J + c) * kAS + 16 * I + r] = -s;
+            }
+        }
+    }
+}
+
 template <typename Tin, typename Tout, int DK, int DV, bool kSlots>
 __global__ void __launch_bounds__(kThreads, 1) kda_simt_kernel(SimtParams p)
 {
@@ -114,55 +224,55 @@ __global__ void __launch_bounds__(kThreads, 1) kda_simt_kernel(SimtParams p)
     const size_t rs = (size_t)p.H;   // row stride in heads
     for (int row0 = bos; row0 < eos; row0 += kChunk) {
         const int L = min(kChunk, eos - row0);
-        // ---- the chunk's tiles (rows past L zero) ----
-        for (int i = tid; i < kChunk * DK; i += kThreads) {
-            const int r = i / DK, c = i % DK;
-            const size_t off = ((size_t)(row0 + r) * rs + h) * DK + c;
-            const bool in = r < L;
-            Ks[i] = in ? load_in(k + off) : 0.f;
-            Qs[i] = in ? load_in(q + off) : 0.f;
-            Gs[i] = in ? __ldg(p.g + off) : 0.f;
-        }
-        for (int i = tid; i < kChunk * DV; i += kThreads) {
-            const int r = i / DV, c = i % DV;
-            Vs[i] = r < L ? load_in(v + ((size_t)(row0 + r) * rs + h) * DV + c) : 0.f;
-        }
+        // ---- the chunk's tiles (rows past L zero): 16-byte pieces, every load of a
+        //      tile issued before any is used ----
+        load_tile<Tin, DK>(k, Ks, row0, L, rs, h, tid);
+        load_tile<Tin, DK>(q, Qs, row0, L, rs, h, tid);
+        load_tile<float, DK>(p.g, Gs, row0, L, rs, h, tid);
+        load_tile<Tin, DV>(v, Vs, row0, L, rs, h, tid);
         if (tid < kChunk) bs[tid] = tid < L ? __ldg(p.beta + (size_t)(row0 + tid) * rs + h) : 0.f;
         __syncthreads();
-        // ---- G = running sum of g over the rows, per key channel ----
+        // ---- G = running sum of g over the rows, per key channel, kept in base 2
+        //      (exp(x) = 2^(x log2 e)) ----
         if (tid < DK) {
             float acc = 0.f;
             for (int r = 0; r < kChunk; r++) {   // rows past L add zero
                 acc += Gs[r * DK + tid];
-                Gs[r * DK + tid] = acc;
+                Gs[r * DK + tid] = acc * kLog2e;
             }
-            gl[tid] = acc;
-            el[tid] = expf(acc);
+            gl[tid] = acc * kLog2e;
+            el[tid] = exp2f(acc * kLog2e);
         }
         __syncthreads();
         // ---- A (beta-scaled, strictly lower) and B (lower with diagonal) ----
-        // Warp w takes rows i = w, w+16, w+32, w+48; lane l the columns j = l and
-        // l + 32 (j <= i).  The channel loop is skewed by the lane, so that the
-        // lanes of a warp read 32 different banks.
-        for (int i = warp; i < kChunk; i += kWarps) {
+        // The 2080 pairs j <= i are dealt over all threads in order (thread tid
+        // takes pairs tid, tid + 512, ...); the channel loop is skewed by the
+        // lane, so that the lanes of a warp read 32 different banks.
+        for (int pr = tid; pr < kChunk * (kChunk + 1) / 2; pr += kThreads) {
+            int i = (int)((sqrtf(8.f * pr + 1.f) - 1.f) * 0.5f);
+            if ((i + 1) * (i + 2) / 2 <= pr) i++;          // float rounding of the root
+            if (i * (i + 1) / 2 > pr) i--;
+            const int j = pr - i * (i + 1) / 2;
             const float *ki = Ks + i * DK, *qi = Qs + i * DK, *gi = Gs + i * DK;
-            for (int j = lane; j <= i; j += 32) {
-                const float *kj = Ks + j * DK, *gj = Gs + j * DK;
-                float sa = 0.f, sb = 0.f;
+            const float *kj = Ks + j * DK, *gj = Gs + j * DK;
+            float sa = 0.f, sb = 0.f;
 #pragma unroll 4
-                for (int cc = 0; cc < DK; cc++) {
-                    const int c = (cc + lane) & (DK - 1);
-                    const float w = expf(gi[c] - gj[c]) * kj[c];
-                    sa = fmaf(ki[c], w, sa);
-                    sb = fmaf(qi[c], w, sb);
-                }
-                As[i * kAS + j] = j < i ? bs[i] * sa : 0.f;
-                Bs[i * kAS + j] = sb;
+            for (int cc = 0; cc < DK; cc++) {
+                const int c = (cc + lane) & (DK - 1);
+                const float w = exp2f(gi[c] - gj[c]) * kj[c];
+                sa = fmaf(ki[c], w, sa);
+                sb = fmaf(qi[c], w, sb);
             }
-            for (int j = i + 1 + lane; j < kChunk; j += 32) {
-                As[i * kAS + j] = 0.f;
-                Bs[i * kAS + j] = 0.f;
-            }
+            As[i * kAS + j] = j < i ? bs[i] * sa : 0.f;
+            Bs[i * kAS + j] = sb;
+        }
+        for (int pr = tid; pr < kChunk * (kChunk - 1) / 2; pr += kThreads) {   // the upper triangles: zero
+            int j = (int)((sqrtf(8.f * pr + 1.f) - 1.f) * 0.5f);
+            if ((j + 1) * (j + 2) / 2 <= pr) j++;
+            if (j * (j + 1) / 2 > pr) j--;
+            const int i = pr - j * (j + 1) / 2;            // i < j + 1
+            As[i * kAS + j + 1] = 0.f;
+            Bs[i * kAS + j + 1] = 0.f;
         }
         __syncthreads();
         // ---- element-wise: K -> K*exp(G_L - G), Q -> Q*exp(G), G -> beta*K*exp(G);
@@ -170,23 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_simt_kernel(SimtParams p)
         for (int i = tid; i < kChunk * DK; i += kThreads) {
             const int r = i / DK, c = i % DK;
             const float x = Gs[i], kv = Ks[i];
-            const float e = expf(x);
-            Ks[i] = kv * expf(gl[c] - x);
+            const float e = exp2f(x);
+            Ks[i] = kv * exp2f(gl[c] - x);
             Qs[i] = Qs[i] * e;
             Gs[i] = bs[r] * (kv * e);
         }
         for (int i = tid; i < kChunk * DV; i += kThreads) Vs[i] *= bs[i / DV];
-        // ---- T = (I + A)^-1, in place (right-looking: at step j row j is final,
-        //      rows below take -A_ij T_j); T's unit diagonal stays implicit ----
-        for (int j = 0; j < kChunk - 1; j++) {
-            __syncthreads();
-            const int i = tid;
-            if (i > j && i < kChunk) {
-                const float a = As[i * kAS + j];
-                As[i * kAS + j] = -a;
-                for (int l = 0; l < j; l++) As[i * kAS + l] = fmaf(-a, As[j * kAS + l], As[i * kAS + l]);
-            }
-        }
+        __syncthreads();
+        invert_unit_lower(As, tid);
         __syncthreads();
         const int r0 = 4 * warp, v0 = VW * lane;   // this thread's 4 rows x VW value columns
         // ---- R = beta*V - (beta*K*exp(G)) S0, in place over V ----
@@ -219,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_simt_kernel(SimtParams p)
                 load_vec<VW>(Vs + j * DV + v0, x);
 #pragma unroll
                 for (int a = 0; a < 4; a++) {
-                    const float t = As[(r0 + a) * kAS + j];   // zero for j >= r0 + a
+                    const float t = j < r0 + a ? As[j * kAS + r0 + a] : 0.f;   // T[r0+a][j], kept transposed
 #pragma unroll
                     for (int b = 0; b < VW; b++) acc[a][b] = fmaf(t, x[b], acc[a][b]);
                 }

@@ -111,6 +111,10 @@ __device__ __forceinline__ uint32_t off_k(int s) { return s ? 8192u : 0u; }     
 __device__ __forceinline__ uint32_t off_q(int s) { return s ? 0u : 8192u; }        // Q rows in a kb block
 __device__ __forceinline__ uint32_t off_km(int s) { return s ? 49152u : 57344u; }   // Km
 __device__ __forceinline__ uint32_t off_bq(int s) { return s ? 65536u : 49152u; }   // tril(A_qk)^T
+// (the functions above take a layout bit lb: the stage index s in the fused
+// kernel, whose chain merges its MMAs across the two layouts; in split mode
+// the parity of the chunk's index in its sequence, so that a chain CTA sees
+// the layouts alternate -- see layout_bit)
 constexpr uint32_t kOffG = 2 * kStageBytes;     // g slot ([64][128] fp32, unswizzled), read once by the decay scan
 constexpr uint32_t kOffT16 = kOffG + 32768;     // T = (I + A_kk)^-1 [r][j] fp16, 8 KB (MMA-b operand)
 constexpr uint32_t kOffTmp = kOffT16 + 8192;    // group I fp32 blocks of the inverse, 16 KB
@@ -130,6 +134,29 @@ constexpr uint32_t kOffPend = kOffMisc + 128;
 // (rows 0-31 go to the stage's tril(A_qk) buffer, free once MMA3 is done)
 constexpr uint32_t kOffOT = (kOffPend + 3 * 512 + 1023) & ~1023u;
 constexpr uint32_t kSmemBytes = kOffOT + 8192 + 1024;   // + alignment slack
+
+// ---- split mode: chunk preparation and the state chain on separate SMs ----
+// For calls with few (sequence, head) units -- one long sequence, say -- one
+// unit per SM leaves most SMs idle and each unit's chunks run one after
+// another at the pace of a whole prep pipeline.  Only the state chain (the
+// rescale, MMA1, Delta, MMA3, outputs) depends on the previous chunk; the
+// decay scan, the operands, A, the inverse, W' and beta*V do not.  In split
+// mode CTA b < chains runs the chain of unit b alone, with all 16 warps, and
+// every other CTA prepares chunks -- any unit's, in the order (chunk index,
+// unit) -- with the prep roles unchanged and ships each finished stage through
+// a ring in global memory (kRingSlots slots per unit, in L2 in practice):
+// producer and chain hand over through flags with release/acquire ordering.
+constexpr int kSortChunks = 3;                          // the producers' deal: one chunk per claim
+constexpr int kRingSlots = 4;
+constexpr uint32_t kSlotT16 = kStageBytes;              // slot: the stage | T16 | fm, pend
+constexpr uint32_t kSlotHdr = kStageBytes + 8192;
+constexpr uint32_t kSlotBytes = kSlotHdr + 1024;
+// the chain CTA's shared memory: two slot buffers, then two output staging
+// buffers (16 KB each; also the state staging at unit start and end), then the
+// pend of the last two chunks; barriers and misc at the usual offsets
+constexpr uint32_t kCOut = 2 * kSlotBytes;
+constexpr uint32_t kCPend = kCOut + 2 * 16384;
+static_assert(kCPend + 1024 <= kOffOrder, "chain layout overlaps the unit table");
 
 // mbarrier slots ([2] = one per stage)
 constexpr int kBarKQFull = 0;      // [2]: k, q tiles landed
@@ -172,6 +199,27 @@ struct TcParams {
     int num_slots;         // entries in the state pool when slots is set
 };
 
+// The fused short-conv prologue's arguments (read by kConv builds only; a
+// separate kernel argument, so that the other builds' parameters and code
+// stay as they are).  The tensor maps then read the raw projections.
+struct ConvParams {
+    const uint16_t *x[3];  // x_q, x_k, x_v [T][H][128] bf16, for the rows before a chunk
+    const float *w;        // [3][H*128][4] fp32 (stream, channel, tap)
+    uint16_t *pool;        // [entries][3 taps][3 streams][H*128] bf16, the windows, updated in place
+    int H;
+    int act;               // 0 identity, 1 SiLU
+    float eps;
+};
+
+// Split mode's hand-over (zeroed by the host before each launch).
+struct SplitParams {
+    uint8_t *ring;         // [units][kRingSlots][kSlotBytes]
+    int *ready;            // [units][kRingSlots]: 2 (j + 1) + stage parity once chunk j is in the slot
+    int *freed;            // [units][kRingSlots]: j + 1 once the chain is done with chunk j
+    int *abort;            // set by a CTA whose wait on another CTA ran out
+    int chains;            // CTAs 0 .. chains-1 run the chains, one unit each (units in sorted order)
+};
+
 struct Smem {
     uint8_t *base;
     __device__ uint32_t u32(uint32_t off) const { return smem_u32(base + off); }
@@ -184,6 +232,8 @@ struct Smem {
     __device__ volatile int *claim_done() const { return ptr<volatile int>(kOffMisc + 16); }  // dynamic: no more claims
     __device__ int *units_nonempty() const { return ptr<int>(kOffMisc + 20); }
     __device__ int *sched() const { return ptr<int>(kOffMisc + 24); }      // ring [8] of claimed units
+    __device__ int *split_parity() const { return ptr<int>(kOffMisc + 56); }   // split chain: [2] per buffer
+    __device__ int *producers() const { return ptr<int>(kOffMisc + 64); }      // split: producer CTAs
 };
 
 __device__ __forceinline__ bool role_any(bool pred, int id, int n)
@@ -227,7 +277,18 @@ __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, in
     const int su = u / p.H;
     x.h = u % p.H;
     int b, e;
-    if constexpr (kSort == 1) {
+    if constexpr (kSort == kSortChunks) {
+        // a producer's claim: chunk j of unit uu (sorted order), packed (j << 8) | uu
+        const int j = u >> 8, uu = u & 255;
+        x.n = order[uu / p.H];
+        x.h = uu % p.H;
+        const int2 be = reinterpret_cast<const int2 *>(order + kMaxSortedSeqs)[x.n];
+        x.bos = be.x + kChunk * j;
+        x.eos = min(x.bos + kChunk, be.y);
+        x.nchunks = 1;
+        x.st = -1;   // producers touch no state
+        return x;
+    } else if constexpr (kSort == 1) {
         // order[] is followed in shared memory by the clamped {bos, eos} rows
         x.n = order[su];
         const int2 be = reinterpret_cast<const int2 *>(order + kMaxSortedSeqs)[x.n];
@@ -249,6 +310,19 @@ __device__ __forceinline__ Unit get_unit(const TcParams &p, const int *order, in
     x.eos = e;
     x.nchunks = (e - b + kChunk - 1) / kChunk;
     return x;
+}
+
+// Layout bit of a stage (off_k etc.): the stage index s, or for a split-mode
+// producer the parity of the chunk's index in its sequence
+template <int kSort>
+__device__ __forceinline__ int layout_bit(const int *order, const Unit &un, int s)
+{
+    if constexpr (kSort == kSortChunks) {
+        const int2 be = reinterpret_cast<const int2 *>(order + kMaxSortedSeqs)[un.n];
+        return ((un.bos - be.x) / kChunk) & 1;
+    } else {
+        return s;
+    }
 }
 
 // Dynamic deal: unit k of this CTA once group E's first thread has published
@@ -277,7 +351,7 @@ template <int kSort>
 __device__ __forceinline__ int cta_unit(const Smem &sm, int k, int U)
 {
     if constexpr (kSort != 0) {
-        return dyn_unit(sm, k, U);
+        return dyn_unit(sm, k, kSort == kSortChunks ? 0 : U);   // producers get no empty units
     } else {
         const int G = gridDim.x, b = blockIdx.x;
         const int u = k * G + ((k & 1) ? (G - 1 - b) : b);
@@ -286,7 +360,31 @@ __device__ __forceinline__ int cta_unit(const Smem &sm, int k, int U)
 }
 
 
-// byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
+// The producers' claims, in order: claim i is chunk j of unit u, where the
+// chunks are counted by index j first and then by unit (sorted order, so the
+// units that still have a chunk j are the first cnt(j) = H * (sequences with
+// more than j chunks)).  A producer's claims only grow, so a cursor over j
+// decodes them.
+struct ChunkDeal {
+    int j = 0, base = 0;   // chunks of index < j
+    int m = -1;            // sequences (sorted) with more than j chunks
+    __device__ int decode(const int *order, int N, int H, int i)
+    {
+        const int2 *rows = reinterpret_cast<const int2 *>(order + kMaxSortedSeqs);
+        auto nch = [&](int su) { const int2 be = rows[order[su]]; return (be.y - be.x + kChunk - 1) / kChunk; };
+        if (m < 0) {
+            m = N;
+            while (m > 0 && nch(m - 1) <= 0) m--;
+        }
+        while (i >= base + H * m) {
+            base += H * m;
+            j++;
+            while (m > 0 && nch(m - 1) <= j) m--;
+        }
+        return (j << 8) | (i - base);
+    }
+};
+
 // k-th unit of this CTA if it is already known (-1: exhausted, -2: not yet
 // claimed); never waits.
 template <int kSort>
@@ -301,6 +399,7 @@ __device__ __forceinline__ int cta_unit_peek(const Smem &sm, int k, int U)
     return u < U ? u : -1;
 }
 
+// byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
 
 // 2^x on the special-function unit (approximate, subnormal results flushed to
@@ -407,15 +506,15 @@ __device__ bool cursor_next(LoadCursor &L, const TcParams &p, const Smem &sm, co
 
 // k and q of chunk `item`: one 3-D box per 64-channel half (the halves of k and
 // q interleave in shared memory)
-__device__ void issue_kq(const Smem &sm, const Maps &m, int item, int row0, int h)
+__device__ void issue_kq(const Smem &sm, const Maps &m, int item, int row0, int h, int lb)
 {
     const uint32_t st = sm.u32((item & 1) * kStageBytes);
     const uint32_t bar = sm.bar(kBarKQFull + (item & 1));
     KDA_PHASE(2, item, 0);
     mbar_arrive_expect_tx(bar, kKQBytes);
     for (int kb = 0; kb < 2; kb++) {
-        tma_load_3d(st + kOffKQ + kb * 16384 + off_k(item & 1), m.k, 64 * kb, h, row0, bar);
-        tma_load_3d(st + kOffKQ + kb * 16384 + off_q(item & 1), m.q, 64 * kb, h, row0, bar);
+        tma_load_3d(st + kOffKQ + kb * 16384 + off_k(lb), m.k, 64 * kb, h, row0, bar);
+        tma_load_3d(st + kOffKQ + kb * 16384 + off_q(lb), m.q, 64 * kb, h, row0, bar);
     }
 }
 
@@ -444,6 +543,151 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // unrolling.
 // =============================================================================
 
+// -----------------------------------------------------------------------------
+// The fused short-conv prologue (kConv builds).  Group E turns a stage's raw
+// projection tiles into q, k and v in place before its own passes (v before
+// the beta*V conversion, q and k before the operand pass); q, k and v never
+// reach global memory.  Per row t of a sequence and channel c, with
+// x_{-3..-1} the window's taps: y_t = sum_j w_j x_{t-3+j}, SiLU if asked, and
+// q, k scaled to unit L2 norm over the head's 128 channels, y / sqrt(|y|^2 + eps).
+// -----------------------------------------------------------------------------
+// SiLU(a) = a sigmoid(a) = a / (1 + 2^(-a log2 e)); ex2.approx and the
+// approximate division keep it to a few units of fp32 rounding
+__device__ __forceinline__ float conv_silu(float a) { return __fdividef(a, 1.f + ex2(-a * kLog2e)); }
+
+// One stream over rows 8w .. 8w+7 of the chunk (w: the group E warp) and this
+// lane's channels 4l .. 4l+3 of the head, in place in the stage tile whose two
+// 64-channel blocks are `blk` apart from `tile` (bf16 in and out; rows at and
+// past L become zero); with kNorm each row is scaled to unit L2 norm over the
+// head's 128 channels -- the 32 lanes of the warp hold all of them, so the sum
+// needs no other warp.  halo[j]: row -3 + j of the chunk for warp 0 (the
+// sequence's previous rows, or its window's taps on its first chunk).  win
+// (only on a sequence's last chunk): tap 0 of the stream's window at this
+// lane's channels, taps tap_stride apart; it receives the last three raw rows
+// of [old taps ; the sequence's rows].
+template <bool kNorm>
+__device__ void e_conv_stream(uint8_t *tile, uint32_t blk, const uint2 (&halo)[3], const float (&w)[4][4], int L,
+                              int et, int act, float eps, uint16_t *win, size_t tap_stride)
+{
+    const int lane = et & 31, w8 = et >> 5;
+    uint8_t *base = tile + (lane >> 4) * blk + 8 * (lane & 1);
+    const int ch = (lane & 15) >> 1;                   // 16-byte chunk of channel 4l in its block row
+    uint2 raw[11];                                     // rows 8w - 3 .. 8w + 7
+#pragma unroll
+    for (int j = 0; j < 3; j++)
+        raw[j] = w8 == 0 ? halo[j] : *reinterpret_cast<const uint2 *>(base + sw128_chunk(8 * w8 - 3 + j, ch));
+#pragma unroll
+    for (int t = 0; t < 8; t++) raw[3 + t] = *reinterpret_cast<const uint2 *>(base + sw128_chunk(8 * w8 + t, ch));
+    named_bar(kBarE, kEThreads);   // every raw row is read before any row is rewritten
+    if (win) {
+#pragma unroll 1
+        for (int j = 0; j < 3; j++) {
+            const int r = L - 3 + j;                     // chunk row of new tap j (< 0: in the halo)
+            if ((r >= 0 ? (r >> 3) : 0) == w8) {
+                const int idx = 3 + r - 8 * w8;
+                uint2 val = make_uint2(0u, 0u);
+#pragma unroll
+                for (int i = 0; i < 11; i++) val = i == idx ? raw[i] : val;
+                *reinterpret_cast<uint2 *>(win + j * tap_stride) = val;
+            }
+        }
+    }
+    float y[8][4];
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const float x[4][4] = {{bf16lo(raw[t].x), bf16hi(raw[t].x), bf16lo(raw[t].y), bf16hi(raw[t].y)},
+                               {bf16lo(raw[t + 1].x), bf16hi(raw[t + 1].x), bf16lo(raw[t + 1].y), bf16hi(raw[t + 1].y)},
+                               {bf16lo(raw[t + 2].x), bf16hi(raw[t + 2].x), bf16lo(raw[t + 2].y), bf16hi(raw[t + 2].y)},
+                               {bf16lo(raw[t + 3].x), bf16hi(raw[t + 3].x), bf16lo(raw[t + 3].y), bf16hi(raw[t + 3].y)}};
+#pragma unroll
+        for (int c = 0; c < 4; c++) {                 // tap j weighs row t - 3 + j; the order of the sum is the prologue's
+            float a = w[c][0] * x[0][c];
+            a = fmaf(w[c][1], x[1][c], a);
+            a = fmaf(w[c][2], x[2][c], a);
+            a = fmaf(w[c][3], x[3][c], a);
+            y[t][c] = act ? conv_silu(a) : a;
+        }
+    }
+    if constexpr (kNorm) {
+        // the 8 rows' squared norms: a reduce-scatter over the warp leaves lane l
+        // with row l/4 (9 shuffles), then each row's total comes back by shuffle
+        float v[8];
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            v[t] = y[t][0] * y[t][0];
+            v[t] = fmaf(y[t][1], y[t][1], v[t]);
+            v[t] = fmaf(y[t][2], y[t][2], v[t]);
+            v[t] = fmaf(y[t][3], y[t][3], v[t]);
+        }
+        float a4[4], a2[2];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const bool up = lane & 16;
+            a4[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, up ? v[i] : v[i + 4], 16);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const bool up = lane & 8;
+            a2[i] = (up ? a4[i + 2] : a4[i]) + __shfl_xor_sync(0xffffffffu, up ? a4[i] : a4[i + 2], 8);
+        }
+        const bool up = lane & 4;
+        float tot = (up ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, up ? a2[0] : a2[1], 4);
+        tot += __shfl_xor_sync(0xffffffffu, tot, 2);
+        tot += __shfl_xor_sync(0xffffffffu, tot, 1);       // lane l: row l/4, all 128 channels
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            const float sc = rsqrtf(__shfl_sync(0xffffffffu, tot, 4 * t) + eps);
+#pragma unroll
+            for (int c = 0; c < 4; c++) y[t][c] *= sc;
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const bool in = 8 * w8 + t < L;
+        const uint2 out = in ? make_uint2(pack_bf16x2(y[t][0], y[t][1]), pack_bf16x2(y[t][2], y[t][3]))
+                             : make_uint2(0u, 0u);
+        *reinterpret_cast<uint2 *>(base + sw128_chunk(8 * w8 + t, ch)) = out;
+    }
+}
+
+// the three rows before a chunk, per stream (q, k, v), at a lane's four
+// channels, held by group E's first warp; nothing in builds without the prologue
+template <bool kConv> struct ConvHalo {
+    uint2 r[3][3] = {};
+};
+template <> struct ConvHalo<false> {};
+
+// where a group E lane's four channels (4l .. 4l+3 of the head) of a unit's
+// window live: tap = the distance between taps, and the window of stream s on
+// the unit's last chunk (null on the others)
+struct ConvAt {
+    uint16_t *base;   // tap 0, stream 0 at this lane's channels, or null
+    size_t tap, stream;
+    int c0;
+    __device__ uint16_t *window(int s) const { return base ? base + s * stream : nullptr; }
+};
+__device__ __forceinline__ ConvAt conv_at(const ConvParams &cp, const Unit &un, int c, int et)
+{
+    ConvAt a;
+    const size_t HC = (size_t)cp.H * kD;
+    a.c0 = 4 * (et & 31);
+    a.tap = 3 * HC;
+    a.stream = HC;
+    a.base = c == un.nchunks - 1 ? cp.pool + (size_t)un.st * 9 * HC + (size_t)un.h * kD + a.c0 : nullptr;
+    return a;
+}
+
+// conv weights of stream s at channels h*128 + c0 .. + 3
+__device__ __forceinline__ void conv_weights(const ConvParams &cp, int s, int h, int c0, float (&w)[4][4])
+{
+    const float4 *src = reinterpret_cast<const float4 *>(cp.w + ((size_t)s * cp.H * kD + (size_t)h * kD + c0) * 4);
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        const float4 a = __ldg(src + c);
+        w[c][0] = a.x; w[c][1] = a.y; w[c][2] = a.z; w[c][3] = a.w;
+    }
+}
+
 // Group E's decay pass over one chunk (256 threads); `beta_r` is the beta of
 // row et (zero past the chunk), loaded a chunk ahead.  Thread = (row group
 // ew: rows 16*ew .. +15) x (channel half chh) x (key channels c0 = 64*chh +
@@ -454,9 +698,9 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // 2^(G - G_m), Qp = Q*2^(G - G_m) and Km = K*2^(G_m - G) become fp16 in place
 // over the bf16 tiles (rows past the chunk zero).  Returns false if a wait ran
 // out.
-template <class F, class V>
-__device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float beta_r, int *err, F &&released,
-                       V &&before_kq)
+template <class F, class V, class C>
+__device__ bool e_pass(const Smem &sm, int s, int lb, int item, int L, int et, float beta_r, int *err, F &&released,
+                       V &&before_kq, C &&conv_qk)
 {
     const int lane = et & 31;
     const uint32_t st = s * kStageBytes;
@@ -507,6 +751,7 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
     if (ok && item >= 2) ok = mbar_wait(sm.bar(kBarKmFree + s), ((item >> 1) - 1) & 1, sm.abort_flag());
     if (role_any(!ok, kBarE, kEThreads)) return false;
     if (et == 0) KDA_PHASE(0, item, 14);
+    conv_qk();        // the fused prologue's q and k (nothing in other builds)
     if (et < 128) {   // chain constants, one thread per key channel
         cst[et] = ex2(gmx[et]);                                                  // view from row m
         sm.ptr<float>(kOffPend)[(item % 3) * 128 + et] = ex2(glx[et] - gmx[et]);  // row m -> last row
@@ -515,9 +760,9 @@ __device__ bool e_pass(const Smem &sm, int s, int item, int L, int et, float bet
     if (et == 0) KDA_PHASE(0, item, 10);
     const float2 gm = *reinterpret_cast<const float2 *>(gmx + c0);
     float worst = 0.f;   // largest |G_r - G_m| of this thread's rows r < L
-    uint8_t *kt = sm.base + st + kOffKQ + chh * 16384 + off_k(s);   // this channel half's 64-channel block
-    uint8_t *qt = sm.base + st + kOffKQ + chh * 16384 + off_q(s);
-    uint8_t *kmt = sm.base + st + off_km(s) + chh * 8192;
+    uint8_t *kt = sm.base + st + kOffKQ + chh * 16384 + off_k(lb);   // this channel half's 64-channel block
+    uint8_t *qt = sm.base + st + kOffKQ + chh * 16384 + off_q(lb);
+    uint8_t *kmt = sm.base + st + off_km(lb) + chh * 8192;
     const int jk = lane >> 2;                            // 16-byte chunk of channel c0 in the row
     const uint32_t cb = 4 * (lane & 3);                  // byte of channel c0 in that chunk
 #pragma unroll 1
@@ -577,7 +822,7 @@ __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
 
 // (unrolled, unlike the other issue loops: group E, which issues it, sets the
 // cadence, and the unrolled issue is faster; measured)
-__device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
+__device__ void issue_mma_a(const Smem &sm, int s, int lb, uint32_t tmem)
 {
     const uint32_t st = sm.u32(s * kStageBytes);
     const uint32_t id = idesc_f16(128, 64, 0, 0);
@@ -585,7 +830,7 @@ __device__ void issue_mma_a(const Smem &sm, int s, uint32_t tmem)
     for (int ks = 0; ks < 8; ks++) {
         const int kb = ks >> 2, kin = ks & 3;
         const uint64_t ad = smem_desc_sw128(st + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(st + off_km(s) + kb * 8192 + kin * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(st + off_km(lb) + kb * 8192 + kin * 32, 16, 1024);
         mma_ss(tmem + tm_o(s), ad, bd, id, ks > 0);
     }
 }
@@ -596,8 +841,9 @@ __device__ __forceinline__ float load_beta(const TcParams &p, const LoadCursor &
     return et < L ? __ldg(p.beta + (size_t)(c.row0 + et) * p.H + c.un.h) : 0.f;
 }
 
-template <bool kSlots, int kSort>
-__device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int U, const Maps &maps)
+template <bool kSlots, int kSort, bool kConv>
+__device__ void e_role(const TcParams &p, const ConvParams &cp, const Smem &sm, const int *order, int U,
+                       const Maps &maps)
 {
     const int et = threadIdx.x - kChainThreads;
     const uint32_t tmem = *sm.tmem_base();
@@ -612,10 +858,17 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
     constexpr bool dyn = kSort != 0;
     unsigned claim = 0;
     int claim_slot = -1;
+    ChunkDeal deal;   // split mode's producers: claims -> chunks
     auto publish = [&]() {
         if (claim_slot >= 0) {
-            const int u = (int)gridDim.x + (int)claim;
-            if (u < *sm.units_nonempty()) {
+            int u = (int)gridDim.x + (int)claim;
+            bool more = u < *sm.units_nonempty();
+            if constexpr (kSort == kSortChunks) {
+                const int i = *sm.producers() + (int)claim;
+                more = i < *sm.units_nonempty();
+                if (more) u = deal.decode(order, p.N, p.H, i);
+            }
+            if (more) {
                 reinterpret_cast<volatile int *>(sm.sched())[claim_slot & 7] = u;
                 __threadfence_block();
                 *sm.published() = claim_slot + 1;
@@ -656,6 +909,25 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             const int L = min(kChunk, un.eos - (un.bos + c * kChunk));
             const float beta_r = beta_next;
             if (et == 0) publish();
+            // fused prologue: the three rows before the chunk (ew == 0 threads), in
+            // flight during the decay scan -- the sequence's previous rows, or its
+            // window's taps on its first chunk
+            ConvHalo<kConv> halo;
+            if constexpr (kConv) {
+                if ((et >> 5) == 0) {
+                    const size_t HC = (size_t)p.H * kD;
+                    const int cc0 = 4 * (et & 31);                    // this lane's first channel
+                    const int row0 = un.bos + c * kChunk;
+#pragma unroll
+                    for (int sx = 0; sx < 3; sx++)
+#pragma unroll
+                        for (int j = 0; j < 3; j++)
+                            halo.r[sx][j] = c == 0
+                                ? *reinterpret_cast<const uint2 *>(cp.pool + ((size_t)un.st * 9 + 3 * j + sx) * HC +
+                                                                   (size_t)un.h * kD + cc0)
+                                : __ldg(reinterpret_cast<const uint2 *>(cp.x[sx] + ((size_t)(row0 - 3 + j) * p.H + un.h) * kD + cc0));
+                }
+            }
             bool ok = mbar_wait(sm.bar(kBarGFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarE, kEThreads)) {
                 if (et == 0) record_error(p, sm, kErrWaitTimeout);
@@ -679,12 +951,35 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
             auto convert_v = [&]() -> bool {
                 const bool okv = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
                 if (role_any(!okv, kBarE, kEThreads)) return false;
+                if constexpr (kConv) {
+                    const ConvAt at = conv_at(cp, un, c, et);
+                    float w[4][4];
+                    conv_weights(cp, 2, un.h, at.c0, w);
+                    e_conv_stream<false>(sm.base + s * kStageBytes + kOffV, 8192, halo.r[2], w, L, et, cp.act, cp.eps,
+                                         at.window(2), at.tap);
+                    named_bar(kBarE, kEThreads);   // v in place before the beta*V mapping reads it
+                }
                 e_convert_v(sm, s, L, et);
                 fence_proxy_async_smem();
                 mbar_arrive(sm.bar(kBarEDone + s));
                 return true;
             };
-            if (!e_pass(sm, s, item, L, et, beta_r, p.err, next_g, convert_v)) {
+            auto conv_qk = [&]() {
+                if constexpr (kConv) {
+                    const ConvAt at = conv_at(cp, un, c, et);
+                    uint8_t *kq = sm.base + s * kStageBytes + kOffKQ;
+                    float w[4][4];
+                    conv_weights(cp, 1, un.h, at.c0, w);
+                    e_conv_stream<true>(kq + off_k(s), 16384, halo.r[1], w, L, et, cp.act, cp.eps, at.window(1),
+                                        at.tap);
+                    conv_weights(cp, 0, un.h, at.c0, w);
+                    e_conv_stream<true>(kq + off_q(s), 16384, halo.r[0], w, L, et, cp.act, cp.eps, at.window(0),
+                                        at.tap);
+                    named_bar(kBarE, kEThreads);   // q and k in place before the operand pass reads them
+                }
+            };
+            const int lb = layout_bit<kSort>(order, un, s);
+            if (!e_pass(sm, s, lb, item, L, et, beta_r, p.err, next_g, convert_v, conv_qk)) {
                 if (et == 0) record_error(p, sm, kErrWaitTimeout);
                 // this chunk's g was waited for (item + 1 of them); the next one may be in flight
                 item++;
@@ -700,7 +995,7 @@ __device__ void e_role(const TcParams &p, const Smem &sm, const int *order, int 
                     record_error(p, sm, kErrWaitTimeout);
                 KDA_PHASE(0, item, 2);
                 tc_fence_after();
-                issue_mma_a(sm, s, tmem);
+                issue_mma_a(sm, s, lb, tmem);
                 mma_commit(sm.bar(kBarAFull + s));
                 KDA_PHASE(2, item, 2);
             }
@@ -751,13 +1046,19 @@ __device__ __forceinline__ void solve_column16(const float *Lb, int c, float (&x
 // beta-scaled A_kk): the strictly lower part goes to the L blocks; the 16x16
 // diagonal blocks are inverted column by column into D0/D1 and, as fp16, into
 // T16.
-__device__ void i_read_a(const Smem &sm, int s, uint32_t tmem, int it, int item)
+// T = (I + A_kk)^-1 as the fp16 MMA-b operand: one buffer, or in split mode
+// one per stage (the producer's shipper copies it out with the stage)
+template <bool kSplit>
+__device__ __forceinline__ uint32_t t16_off(int s) { return (kSplit && s) ? kOffOT : kOffT16; }
+
+template <bool kSplit>
+__device__ void i_read_a(const Smem &sm, int s, int lb, uint32_t tmem, int it, int item)
 {
     const int ew = it >> 5, lane = it & 31;
     const int hw = ew & 1;                        // which 32 rows of A_kk or A_qk
     const uint32_t src = tmem + tm_o(s) + ((uint32_t)(32 * ew) << 16);
-    if ((ew >= 2) != (s == 1)) {                  // A_qk: lanes 64-127 in stage 0, 0-63 in stage 1
-        const uint32_t bt = sm.u32(s * kStageBytes + off_bq(s));
+    if ((ew >= 2) != (lb == 1)) {                 // A_qk: lanes 64-127 in layout 0, 0-63 in layout 1
+        const uint32_t bt = sm.u32(s * kStageBytes + off_bq(lb));
         const int mi = lane >> 3, k8 = lane & 7;  // this thread's stored matrix and row
 #pragma unroll 1
         for (int hl = 0; hl < 2; hl++) {
@@ -841,7 +1142,7 @@ __device__ void i_read_a(const Smem &sm, int s, uint32_t tmem, int it, int item)
             h[2 * q] = pack_f16x2(v4.x, v4.y);
             h[2 * q + 1] = pack_f16x2(v4.z, v4.w);
         }
-        uint8_t *T16 = sm.base + kOffT16;
+        uint8_t *T16 = sm.base + t16_off<kSplit>(s);
         *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, 2 * blk)) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4 *>(T16 + sw128_chunk(i, 2 * blk + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
     }
@@ -853,11 +1154,12 @@ __device__ void i_read_a(const Smem &sm, int s, uint32_t tmem, int it, int item)
 // diagonal inverses are exact to fp32).
 //   level 1: T10 = -X1 (L10 X0),  T32 = -X3 (L32 X2)       (into D0 / D1)
 //   level 2: T[32:64, 0:32] = -D1 (L[32:64, 0:32] D0)
-__device__ void i_merge(const Smem &sm, int it)
+template <bool kSplit>
+__device__ void i_merge(const Smem &sm, int s, int it)
 {
     const int iw = it >> 5, lane = it & 31, g = lane >> 2, t = lane & 3;
     float *W = sm.ptr<float>(kOffTmp);
-    uint8_t *T16 = sm.base + kOffT16;
+    uint8_t *T16 = sm.base + t16_off<kSplit>(s);
     float *P1 = sm.ptr<float>(kOffP);            // [2][16][24]
     float *P2 = P1;                              // [32][40] once P1 is dead
     auto put16 = [&](int r, int c, float v0, float v1) {   // c even
@@ -926,14 +1228,15 @@ __device__ void i_merge(const Smem &sm, int it)
     }
 }
 
-__device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
+template <bool kSplit>
+__device__ void issue_mma_b(const Smem &sm, int s, int lb, uint32_t tmem)
 {
     const uint32_t st = sm.u32(s * kStageBytes);
     const uint32_t id = idesc_f16(128, 64, 1, 0);
 #pragma unroll 1
     for (int ks = 0; ks < 4; ks++) {
-        const uint64_t bd = smem_desc_sw128(sm.u32(kOffT16) + ks * 32, 16, 1024);
-        const uint64_t aw = smem_desc_sw128(st + kOffKQ + off_k(s) + ks * 2048, 16384, 1024);   // Kp^T, MN-major
+        const uint64_t bd = smem_desc_sw128(sm.u32(t16_off<kSplit>(s)) + ks * 32, 16, 1024);
+        const uint64_t aw = smem_desc_sw128(st + kOffKQ + off_k(lb) + ks * 2048, 16384, 1024);  // Kp^T, MN-major
         const uint64_t au = smem_desc_sw128(st + kOffV + ks * 2048, 8192, 1024);                // V^T, MN-major
         mma_ss(tmem + tm_o(s), aw, bd, id, ks > 0);
         mma_ss(tmem + tm_d(s), au, bd, id, ks > 0);
@@ -945,12 +1248,12 @@ __device__ void issue_mma_b(const Smem &sm, int s, uint32_t tmem)
 // [-W' ; Qp] is one 128-row operand for MMA1.  TMEM is read in the warp-MMA
 // fragment layout and each 8 x 8 block is stored transposed (stmatrix.trans).
 // Then the TMEM columns MMA1 accumulates the output into are zeroed.
-__device__ void i_read_w(const Smem &sm, int s, uint32_t tmem, int it)
+__device__ void i_read_w(const Smem &sm, int s, int lb, uint32_t tmem, int it)
 {
     const int iw = it >> 5, lane = it & 31;
     const int mi = lane >> 3, k8 = lane & 7;              // this thread's stored matrix and row
     const uint32_t src = tmem + tm_o(s) + ((uint32_t)(32 * iw) << 16);
-    const uint32_t kq = sm.u32(s * kStageBytes + kOffKQ + off_k(s));
+    const uint32_t kq = sm.u32(s * kStageBytes + kOffKQ + off_k(lb));
 #pragma unroll 1
     for (int hl = 0; hl < 2; hl++) {
         uint32_t f[4][8];                                 // [16-column block][fragment]
@@ -982,12 +1285,16 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
 {
     const int it = threadIdx.x - kChainThreads - kEThreads;
     const uint32_t tmem = *sm.tmem_base();
+    constexpr bool kSplit = kSort == kSortChunks;
     {   // zeros that stay for the whole kernel: T16's 16-byte chunks right of each
         // row's diagonal block, and the upper-right 16x16 blocks of D0 and D1
-        uint8_t *T16 = sm.base + kOffT16;
-        for (int idx = it; idx < 64 * 8; idx += kGroupThreads) {
-            const int r = idx >> 3, q = idx & 7;
-            if (q > 2 * (r >> 4) + 1) *reinterpret_cast<uint4 *>(T16 + sw128_chunk(r, q)) = make_uint4(0u, 0u, 0u, 0u);
+        for (int b = 0; b < (kSplit ? 2 : 1); b++) {
+            uint8_t *T16 = sm.base + t16_off<kSplit>(b);
+            for (int idx = it; idx < 64 * 8; idx += kGroupThreads) {
+                const int r = idx >> 3, q = idx & 7;
+                if (q > 2 * (r >> 4) + 1)
+                    *reinterpret_cast<uint4 *>(T16 + sw128_chunk(r, q)) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         float *W = sm.ptr<float>(kOffTmp);
         for (int idx = it; idx < 2 * 16 * 16; idx += kGroupThreads) {
@@ -1003,6 +1310,7 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
         const Unit un = get_unit<kSlots, kSort>(p, order, u);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
+            const int lb = layout_bit<kSort>(order, un, s);
             const uint32_t ph = (item >> 1) & 1;
             // MMA-a done implies group E's operand pass is over (MMA-b of the previous
             // chunk, the last reader of T16, was waited for below)
@@ -1010,12 +1318,12 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
             if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
             if (it == 0) KDA_PHASE(0, item, 5);
             tc_fence_after();
-            i_read_a(sm, s, tmem, it, item);
+            i_read_a<kSplit>(sm, s, lb, tmem, it, item);
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar(kBarI, kGroupThreads);
             if (it == 0) KDA_PHASE(0, item, 3);
-            i_merge(sm, it);
+            i_merge<kSplit>(sm, s, it);
             if (it == 0) KDA_PHASE(0, item, 6);
             fence_proxy_async_smem();
             named_bar(kBarI, kGroupThreads);
@@ -1025,7 +1333,7 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
                 } else {
                     KDA_PHASE(0, item, 7);
                     tc_fence_after();
-                    issue_mma_b(sm, s, tmem);
+                    issue_mma_b<kSplit>(sm, s, lb, tmem);
                     mma_commit(sm.bar(kBarPrepDone + s));
                     KDA_PHASE(0, item, 8);
                 }
@@ -1035,7 +1343,7 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
             ok = mbar_wait(sm.bar(kBarPrepDone + s), ph, sm.abort_flag());
             if (role_any(!ok, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
             tc_fence_after();
-            i_read_w(sm, s, tmem, it);
+            i_read_w(sm, s, lb, tmem, it);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(sm.bar(kBarWReady + s));
@@ -1303,7 +1611,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             if (v == 0) {
                 KDA_PHASE(1, item, 2);
                 if (kq_pending) {                             // -W' and Qp have been read
-                    issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+                    issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h, (cur.item - 1) & 1);
                     kq_pending = false;
                 }
             }
@@ -1384,7 +1692,7 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
     bool kq_pending = false;
     if (v == 0) {
         for (int i = 0; i < 2 && cursor_next<kSlots, kSort>(cur, p, sm, order, U); i++) {
-            issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+            issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h, (cur.item - 1) & 1);
             issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
         }
     }
@@ -1403,11 +1711,551 @@ __device__ void chain_role(const TcParams &p, const Smem &sm, const int *order, 
 }
 
 // =============================================================================
-template <bool kSlots, int kSort>
+// split mode
+// =============================================================================
+// Bounded wait, by one thread, until another CTA's flag reaches `target`
+// (acquire).  Gives up after about a second, or at once when this CTA or the
+// launch is winding down; false then.
+__device__ bool flag_wait(const int *flag, int target, const SplitParams &sp, volatile int *abort, int *seen = nullptr)
+{
+    for (uint32_t it = 0; it < (1u << 22); it++) {
+        const int x = ld_acquire_gpu(flag);
+        if (x >= target) {
+            if (seen) *seen = x;
+            return true;
+        }
+        if ((it & 15) == 15 && (*abort || *reinterpret_cast<volatile int *>(sp.abort))) return false;
+        __nanosleep(it < 64 ? 32 : 256);
+    }
+    return false;
+}
+
+// a wait on another CTA ran out, or this CTA is winding down: every CTA of the
+// launch stops waiting for the others
+__device__ __forceinline__ void split_abort(const TcParams &p, const SplitParams &sp, const Smem &sm)
+{
+    record_error(p, sm, kErrWaitTimeout);
+    atomicExch(sp.abort, 1);
+}
+
+// A producer's warps 0-3 (the chain's place in the fused kernel): once a stage
+// is finished -- -W' and Qp in its k/q rows, beta*V, Km and tril(A_qk)^T, T in
+// its T16 buffer, the decay constants written -- and the ring slot of its
+// chunk is free, copy it there, hand the stage back to the prep roles, request
+// the k, q and v of the chunk two ahead, and publish the slot.
+template <bool kSlots>
+__device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &sm, const int *order,
+                          const Maps &maps)
+{
+    const int v = threadIdx.x;
+    LoadCursor cur;
+    if (v == 0) {
+        for (int i = 0; i < 2 && cursor_next<kSlots, kSortChunks>(cur, p, sm, order, 0); i++) {
+            issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h, layout_bit<kSortChunks>(order, cur.un, 0));
+            issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+        }
+    }
+    bool failed = false;
+    for (int item = 0;; item++) {
+        const int u = cta_unit<kSortChunks>(sm, item, 0);
+        if (u < 0) break;
+        const int s = item & 1;
+        const uint32_t ph = (item >> 1) & 1;
+        const int j = u >> 8, uu = u & 255;
+        const int slot = uu * kRingSlots + j % kRingSlots;
+        if (v == 0) KDA_PHASE(1, item, 0);
+#ifdef KDA_TRACE
+        if (v == 0 && blockIdx.x == KDA_TRACE_CTA && item < 128) g_kda_trace[1][item][15] = (unsigned long long)u;
+#endif
+        bool ok = mbar_wait(sm.bar(kBarFmReady + s), ph, sm.abort_flag()) &&
+                  mbar_wait(sm.bar(kBarWReady + s), ph, sm.abort_flag());
+        if (v == 0) KDA_PHASE(1, item, 1);
+        // the chain has read the chunk kRingSlots back from this slot
+        if (ok && v == 0 && j >= kRingSlots) ok = flag_wait(sp.freed + slot, j - kRingSlots + 1, sp, sm.abort_flag());
+        if (role_any(!ok, kBarChain, kChainThreads)) {
+            failed = true;
+            break;
+        }
+        if (v == 0) KDA_PHASE(1, item, 2);
+        uint8_t *dst = sp.ring + (size_t)slot * kSlotBytes;
+        float *hdr = reinterpret_cast<float *>(dst + kSlotHdr);
+        hdr[v] = sm.ptr<float>(kOffConst + s * kConstBytes)[v];          // fm: view from the middle row
+        hdr[128 + v] = sm.ptr<float>(kOffPend)[(item % 3) * 128 + v];    // pend: middle row -> last row
+        if (v == 0) {
+            const uint32_t st = sm.u32(s * kStageBytes);
+            for (uint32_t off = 0; off < kStageBytes; off += 16384)
+                bulk_store(dst + off, st + off, kStageBytes - off < 16384u ? kStageBytes - off : 16384u);
+            bulk_store(dst + kSlotT16, sm.u32(t16_off<true>(s)), 8192);
+            bulk_commit();
+            bulk_wait_read0();
+            KDA_PHASE(1, item, 3);
+            // the stage is the prep's again: Km and tril(A_qk)^T, TMEM P_s, and the
+            // k/q and v tiles of the chunk two ahead
+            mbar_arrive(sm.bar(kBarKmFree + s));
+            mbar_arrive(sm.bar(kBarODone + s));
+            if (cursor_next<kSlots, kSortChunks>(cur, p, sm, order, 0)) {
+                issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h, layout_bit<kSortChunks>(order, cur.un, 0));
+                issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+            }
+            bulk_wait0();
+            KDA_PHASE(1, item, 4);
+        }
+        __threadfence();
+        named_bar(kBarChain, kChainThreads);
+        if (v == 0) {
+            fence_proxy_async_global();
+            st_release_gpu(sp.ready + slot, 2 * (j + 1) + (j & 1));   // + the stage's layout bit
+            KDA_PHASE(1, item, 5);
+        }
+    }
+    if (v == 0) {
+        if (failed) split_abort(p, sp, sm);
+        bulk_wait0();
+        // loads still in flight land before the CTA exits (normally none: every
+        // requested chunk was consumed)
+        for (int back = 1; back <= 2 && cur.item - back >= 0; back++) {
+            const int it = cur.item - back;
+            mbar_wait_drain(sm.bar(kBarKQFull + (it & 1)), (it >> 1) & 1);
+            mbar_wait_drain(sm.bar(kBarVFull + (it & 1)), (it >> 1) & 1);
+        }
+    }
+}
+
+// ---- the split chain: one unit, all 16 warps -----------------------------------
+// Warp w owns TMEM lanes 32 (w % 4) .. +31 (value channels) and the quarter
+// w / 4 of each lane's columns.  States move through the warp's 2 KB slice of
+// the output staging buffers, as in chain_load_state / chain_store_state.
+__device__ void split_load_state(const float *src, uint8_t *stg, uint32_t tm, int lane, int cg)
+{
+    const int rq = lane >> 2, pq = lane & 3;
+#pragma unroll 1
+    for (int r = 2 * cg; r < 2 * cg + 2; r++) {
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            *reinterpret_cast<float4 *>(stg + stg_off(8 * i + rq, pq)) =
+                src ? *reinterpret_cast<const float4 *>(src + (8 * i + rq) * kD + 16 * r + 4 * pq)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+        uint32_t x[16];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float4 f = *reinterpret_cast<const float4 *>(stg + stg_off(lane, q));
+            x[4 * q] = __float_as_uint(f.x); x[4 * q + 1] = __float_as_uint(f.y);
+            x[4 * q + 2] = __float_as_uint(f.z); x[4 * q + 3] = __float_as_uint(f.w);
+        }
+        tmem_st16(tm + 16 * r, x);
+        __syncwarp();
+    }
+    tmem_wait_st();
+}
+
+__device__ void split_store_state(float *dst, const float *pend, uint8_t *stg, uint32_t tm, int lane, int cg)
+{
+    const int rq = lane >> 2, pq = lane & 3;
+#pragma unroll 1
+    for (int r = 2 * cg; r < 2 * cg + 2; r++) {
+        uint32_t x[16];
+        tmem_ld16(tm + 16 * r, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float4 pe = *reinterpret_cast<const float4 *>(pend + 16 * r + 4 * q);
+            *reinterpret_cast<float4 *>(stg + stg_off(lane, q)) =
+                make_float4(__fmul_rn(__uint_as_float(x[4 * q]), pe.x), __fmul_rn(__uint_as_float(x[4 * q + 1]), pe.y),
+                            __fmul_rn(__uint_as_float(x[4 * q + 2]), pe.z), __fmul_rn(__uint_as_float(x[4 * q + 3]), pe.w));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            *reinterpret_cast<float4 *>(dst + (8 * i + rq) * kD + 16 * r + 4 * pq) =
+                *reinterpret_cast<const float4 *>(stg + stg_off(8 * i + rq, pq));
+        __syncwarp();
+    }
+}
+
+// S <- (S * pend) * fm on this warp's 32 columns, and their fp16 copy S'h (the
+// arithmetic of chain_scale_state)
+__device__ __forceinline__ void split_scale_state(uint32_t tmem, uint32_t lane_off, int cg, const float *fm,
+                                                  const float *pend)
+{
+    uint32_t x[32];
+    tmem_ld32(tmem + kTmS + lane_off + 32 * cg, x);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        const float4 f4 = *reinterpret_cast<const float4 *>(fm + 32 * cg + j);
+        const float4 p4 = pend ? *reinterpret_cast<const float4 *>(pend + 32 * cg + j) : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float fv[4] = {f4.x, f4.y, f4.z, f4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            float f = __uint_as_float(x[j + e]);
+            if (pend) f = __fmul_rn(f, pv[e]);
+            x[j + e] = __float_as_uint(__fmul_rn(f, fv[e]));
+        }
+    }
+    uint32_t h[16];
+#pragma unroll
+    for (int j = 0; j < 16; j++) h[j] = pack_f16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+    tmem_st32(tmem + kTmS + lane_off + 32 * cg, x);
+    tmem_st16(tmem + kTmS0h + lane_off + 16 * cg, h);
+}
+
+// Chain CTA of unit uu, warp 16 (its first lane): the slot copies.  Chunk j
+// goes into buffer j & 1 once the producers have published it and the chain's
+// MMA3 of chunk j - 2 is done with the buffer; once chunk j has landed, its
+// ring slot goes back to the producers.  (Done by the chain's own first
+// thread, the flag round trips cost about 3.7k cycles a chunk on its path.)
+template <bool kSlots>
+__device__ void split_loader(const TcParams &p, const SplitParams &sp, const Smem &sm, const int *order, int uu)
+{
+    const Unit un = get_unit<kSlots, 1>(p, order, uu);
+    const int nch = un.nchunks;
+    auto slot_of = [&](int j) { return uu * kRingSlots + j % kRingSlots; };
+    int issued = 0, landed = 0;
+    auto issue = [&](int j) -> bool {
+        const int *rf = sp.ready + slot_of(j);
+        int val = 0;
+        if (!flag_wait(rf, 2 * (j + 1), sp, sm.abort_flag(), &val)) return false;
+        fence_proxy_async_global();
+        const int b = j & 1;
+        sm.split_parity()[b] = val & 1;
+        const uint32_t dst = sm.u32(b * kSlotBytes), bar = sm.bar(kBarKQFull + b);
+        const uint8_t *src = sp.ring + (size_t)slot_of(j) * kSlotBytes;
+        mbar_arrive_expect_tx(bar, kSlotBytes);
+        for (uint32_t off = 0; off < kSlotBytes; off += 16384)
+            bulk_load(dst + off, src + off, kSlotBytes - off < 16384u ? kSlotBytes - off : 16384u, bar);
+        issued = j + 1;
+        return true;
+    };
+    bool ok = nch == 0 || (issue(0) && (nch < 2 || issue(1)));
+    for (int j = 0; ok && j < nch; j++) {
+        const int b = j & 1;
+        ok = mbar_wait(sm.bar(kBarKQFull + b), (j >> 1) & 1, sm.abort_flag());
+        if (!ok) break;
+        landed = j + 1;
+        st_release_gpu(sp.freed + slot_of(j), j + 1);   // the slot may take chunk j + kRingSlots
+        if (j + 2 < nch) ok = mbar_wait(sm.bar(kBarKmFree + b), (j >> 1) & 1, sm.abort_flag()) && issue(j + 2);
+    }
+    if (!ok) split_abort(p, sp, sm);
+    // copies still in flight land before the CTA exits
+    for (int j = landed; j < issued; j++) mbar_wait_drain(sm.bar(kBarKQFull + (j & 1)), (j >> 1) & 1);
+}
+
+// Chain CTA of unit uu (sorted order).  Per chunk j (slot buffer b = j & 1,
+// the producer's stage parity `par` fixing where K and Q rows, Km and
+// tril(A_qk)^T sit and so which TMEM columns take Delta and O):
+//   MMA-b's U half: U^T = (beta V)^T T^T into the Delta columns;
+//   S rescaled, O columns zeroed; MMA1 [U^T - S'^T W'^T | S'^T Qp^T];
+//   Delta^T -> fp16; MMA3 [O^T | S^T] += Delta^T [tril(A_qk)^T | Km];
+//   the slot goes back to the producers; O^T -> bf16 -> out.
+// The arithmetic, operand for operand, is the fused kernel's.
+template <bool kSlots>
+__device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem &sm, const int *order,
+                            const Maps &maps, int uu)
+{
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int q = w & 3, cg = w >> 2;
+    const uint32_t tmem = *sm.tmem_base();
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const Unit un = get_unit<kSlots, 1>(p, order, uu);
+    const size_t ubase = ((size_t)un.st * p.H + un.h) * kD * kD;   // used only when st >= 0
+    if (un.nchunks == 0) {   // empty (or padded) sequence: its state passes through
+        if (p.s1 && (!kSlots || un.st >= 0))
+            for (int i = tid; i < kD * kD / 4; i += kThreads)
+                reinterpret_cast<float4 *>(p.s1 + ubase)[i] =
+                    p.s0 ? reinterpret_cast<const float4 *>(p.s0 + ubase)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const int nch = un.nchunks;
+    float *pendr = sm.ptr<float>(kCPend);                 // [2][128]: pend of the last two chunks
+    uint8_t *stg = sm.base + kCOut + 2048 * w;            // this warp's state staging slice
+    const size_t wrows = ubase + (size_t)(32 * q) * kD;   // this warp's first state row
+    bool ok = true;
+    split_load_state(p.s0 ? p.s0 + wrows : nullptr, stg, tmem + kTmS + lane_off, lane, cg);
+    tc_fence_before();
+    // thread 0: U^T = (beta V)^T T^T of chunk jb into its Delta columns (MMA-b's
+    // second half), issued as soon as the chunk has landed and MMA3 of the
+    // chunk before has been issued (its Delta columns are free then)
+    int mmab_done = 0;   // chunks whose MMA-b is issued
+    auto issue_mmab = [&](int jb) {
+        const int bb = jb & 1, pb = sm.split_parity()[bb];
+        const uint32_t bufb = sm.u32(bb * kSlotBytes);
+        tc_fence_after();
+        const uint32_t id = idesc_f16(128, 64, 1, 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ks++) {
+            const uint64_t bd = smem_desc_sw128(bufb + kSlotT16 + ks * 32, 16, 1024);
+            const uint64_t au = smem_desc_sw128(bufb + kOffV + ks * 2048, 8192, 1024);
+            mma_ss(tmem + tm_d(pb), au, bd, id, ks > 0);
+        }
+        mmab_done = jb + 1;
+    };
+    int consumed = 0;
+    // O^T of chunk jo (layout paro) -> bf16 tiles of 32 rows in staging buffer
+    // jo & 1 (this warp: rows 16 cg .. +15, its 32 value channels), stored by
+    // bulk tensor copies; partial tiles row by row.  Thread 0 has made sure
+    // before (bulk_wait_read1 ahead of a block barrier) that the copies of
+    // chunk jo - 2 have read the buffer.  false: a thread's wait ran out.
+    auto outputs = [&](int jo, int paro) -> bool {
+        const int row0 = un.bos + jo * kChunk, L = min(kChunk, un.eos - row0);
+        const uint32_t ost = sm.u32(kCOut + (jo & 1) * 16384);
+        uint32_t o[2][8];
+        const uint32_t src = tmem + tm_o(paro) + lane_off;
+#pragma unroll
+        for (int hl = 0; hl < 2; hl++) tmem_ld16x256_x2(src + ((uint32_t)(16 * hl) << 16) + 16 * cg, o[hl]);
+        tmem_wait_ld();
+        tc_fence_before();
+        const int mi = lane >> 3, k8 = lane & 7;
+        const int rl = 16 * (cg & 1) + ((mi & 2) ? 8 : 0) + k8;
+#pragma unroll
+        for (int hl = 0; hl < 2; hl++) {
+            const uint32_t *f = o[hl];
+            const int vc = 32 * q + 16 * hl + ((mi & 1) ? 8 : 0);
+            stmatrix_x4_trans(ost + (cg >> 1) * 8192 + (vc >> 6) * 4096 + sw128_chunk(rl, (vc & 63) >> 3),
+                              pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1])),
+                              pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3])),
+                              pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5])),
+                              pack_bf16x2(__uint_as_float(f[6]), __uint_as_float(f[7])));
+        }
+        fence_proxy_async_smem();
+        if (role_any(!ok, kBarChain, kThreads)) return false;
+        if (tid == 0) {
+            if (L >= 32) tma_store_4d(maps.o, 0, row0, 0, un.h, ost);
+            if (L == kChunk) tma_store_4d(maps.o, 0, row0 + 32, 0, un.h, ost + 8192);
+            bulk_commit();
+            KDA_PHASE(1, jo, 10);
+        }
+        if (L < kChunk) {
+            const int half = L < 32 ? 0 : 1, nr = L - 32 * half;
+            const uint8_t *tb = sm.base + kCOut + (jo & 1) * 16384 + half * 8192;
+            const size_t row_stride = (size_t)p.H * kD;
+            __nv_bfloat16 *dst = p.out + ((size_t)(row0 + 32 * half) * p.H + un.h) * kD;
+            for (int idx = tid; idx < nr * 16; idx += kThreads) {
+                const int r = idx >> 4, pc = idx & 15;
+                *reinterpret_cast<uint4 *>(dst + (size_t)r * row_stride + 8 * pc) =
+                    *reinterpret_cast<const uint4 *>(tb + (pc >> 3) * 4096 + sw128_chunk(r, pc & 7));
+            }
+        }
+        return true;
+    };
+    bool out_failed = false;
+    // Failures are gathered at the block barriers of a chunk (role_any): a
+    // thread whose wait ran out goes on with harmless work up to the next one.
+    for (int j = 0; j < nch; j++) {
+        const int b = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (tid == 0) KDA_PHASE(1, j, 0);
+        ok = ok && mbar_wait(sm.bar(kBarKQFull + b), ph, sm.abort_flag());
+        tc_fence_after();
+        if (tid == 0) KDA_PHASE(1, j, 1);
+        const int par = sm.split_parity()[b];
+        const uint32_t buf = sm.u32(b * kSlotBytes);
+        const float *hdr = sm.ptr<float>(b * kSlotBytes + kSlotHdr);
+        if (tid == 0 && ok && mmab_done == j) issue_mmab(j);
+        if (tid == 0) KDA_PHASE(1, j, 2);
+        {
+            uint32_t z[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) z[i] = 0u;
+            tmem_st16(tmem + tm_o(par) + lane_off + 16 * cg, z);   // MMA1 accumulates the output here
+        }
+        split_scale_state(tmem, lane_off, cg, hdr, j > 0 ? pendr + ((j - 1) & 1) * 128 : nullptr);
+        if (tid < 128) pendr[(j & 1) * 128 + tid] = hdr[128 + tid];
+        tmem_wait_st();
+        tc_fence_before();
+        if (role_any(!ok, kBarChain, kThreads)) break;
+        consumed = j + 1;
+        if (tid == 0) {
+            KDA_PHASE(1, j, 3);
+            tc_fence_after();
+            const uint32_t id1 = idesc_f16(128, 128, 0, 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ks++) {
+                const int kb = ks >> 2, kin = ks & 3;
+                const uint64_t bwq = smem_desc_sw128(buf + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
+                mma_ts(tmem + (par ? tm_o(1) : tm_d(0)), tmem + kTmS0h + 8 * ks, bwq, id1, 1);
+            }
+            mma_commit(sm.bar(kBarMma1));
+            KDA_PHASE(1, j, 4);
+        }
+        ok = mbar_wait(sm.bar(kBarMma1), j & 1, sm.abort_flag(), KDA_WAIT_LIMIT_MMA1);
+        if (tid == 0) KDA_PHASE(1, j, 5);
+        tc_fence_after();
+        {   // Delta^T (fp32) -> fp16 A operand, this warp's 16 columns
+            uint32_t x[16], h[8];
+            tmem_ld16(tmem + tm_d(par) + lane_off + 16 * cg, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; i++) h[i] = pack_f16x2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+            tmem_st8(tmem + kTmDh + lane_off + 8 * cg, h);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        if (tid == 0) bulk_wait_read1();   // chunk j-2's output copies have read staging buffer j & 1
+        if (role_any(!ok, kBarChain, kThreads)) break;
+        if (tid == 0) {
+            KDA_PHASE(1, j, 6);
+            tc_fence_after();
+            const uint32_t id3 = idesc_f16(128, 192, 0, 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ks++) {
+                const uint64_t b3 = smem_desc_sw128(buf + kOffMma3 + ks * 2048, 8192, 1024);
+                mma_ts(tmem + (par ? kTmS : tm_o(0)), tmem + kTmDh + 8 * ks, b3, id3, 1);
+            }
+            mma_commit(sm.bar(kBarMma3));
+            // the next chunk's MMA-b, if it has landed: it runs after MMA3 (its
+            // Delta columns are this chunk's layout's other ones)
+            if (j + 1 < nch && mbar_try_wait(sm.bar(kBarKQFull + (b ^ 1)), ((j + 1) >> 1) & 1)) issue_mmab(j + 1);
+            KDA_PHASE(1, j, 7);
+        }
+        ok = mbar_wait(sm.bar(kBarMma3), j & 1, sm.abort_flag());
+        tc_fence_after();
+        if (tid == 0) {
+            KDA_PHASE(1, j, 8);
+            if (ok) mbar_arrive(sm.bar(kBarKmFree + b));   // the buffer may take chunk j + 2
+            KDA_PHASE(1, j, 9);
+        }
+        if (!outputs(j, par)) { out_failed = true; break; }
+    }
+    const bool any_failed = role_any(!ok || out_failed, kBarChain, kThreads);
+    const bool done = consumed == nch && !any_failed;
+    if (tid == 0) {
+        if (!done) split_abort(p, sp, sm);
+        bulk_wait_read0();
+    }
+    named_bar(kBarChain, kThreads);
+    // the final state = S * pend of the last chunk, through the staging slices
+    if (done && p.s1)
+        split_store_state(p.s1 + wrows, pendr + ((nch - 1) & 1) * 128, stg, tmem + kTmS + lane_off, lane, cg);
+    if (tid == 0) bulk_wait0();
+}
+
+// =============================================================================
+// The split-mode kernel: a cooperative launch of one CTA per SM (every CTA
+// resident at once, so that the chains and the producers can wait on one
+// another); CTA b < sp.chains runs the chain of unit b (sorted order), the
+// others prepare chunks.
+constexpr int kSplitThreads = kThreads + 32;   // + the chain CTAs' loader warp
+
+template <bool kSlots>
+__global__ void __launch_bounds__(kSplitThreads, 1)
+kda_tc_split_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
+                    const __grid_constant__ CUtensorMap to, TcParams p, const __grid_constant__ SplitParams sp)
+{
+    extern __shared__ uint8_t smem_raw[];
+    Smem sm;
+    sm.base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const bool chain = (int)blockIdx.x < sp.chains;
+    int *order = sm.ptr<int>(kOffOrder);
+    if (tid == 0) {
+        *sm.abort_flag() = 0;
+        for (int i = 0; i < 2; i++) {
+            mbar_init(sm.bar(kBarKQFull + i), 1);
+            mbar_init(sm.bar(kBarVFull + i), 1);
+            mbar_init(sm.bar(kBarPrepDone + i), 1);
+            mbar_init(sm.bar(kBarAFull + i), 1);
+            mbar_init(sm.bar(kBarEDone + i), kEThreads);
+            mbar_init(sm.bar(kBarODone + i), 1);
+            mbar_init(sm.bar(kBarFmReady + i), kGroupThreads);
+            mbar_init(sm.bar(kBarKmFree + i), 1);
+            mbar_init(sm.bar(kBarWReady + i), kGroupThreads);
+        }
+        mbar_init(sm.bar(kBarGFull), 1);
+        mbar_init(sm.bar(kBarMma1), 1);
+        mbar_init(sm.bar(kBarMma3), 1);
+        mbar_init(sm.bar(kBarDrain), 3);
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(sm.u32(kOffMisc), kTmCols);
+        tmem_relinquish();
+        if ((tid & 31) == 0) {
+            tma_prefetch_desc(&tq); tma_prefetch_desc(&tk); tma_prefetch_desc(&tv); tma_prefetch_desc(&tg);
+            tma_prefetch_desc(&to);
+        }
+    }
+    {   // sequences sorted by length, longest first (ties: lower index), as in the fused kernel
+        int *lens = sm.ptr<int>(kOffP);
+        int2 *rows = reinterpret_cast<int2 *>(order + kMaxSortedSeqs);
+        for (int n = tid; n < p.N; n += kSplitThreads) {
+            const int cb = p.cu[n], ce = p.cu[n + 1];
+            int b = min(max(cb, 0), p.T), e = min(max(ce, 0), p.T);
+            if (cb < 0 || cb > p.T || ce < 0 || ce > p.T) atomicOr(p.err, kErrBadSeqlens);
+            if (e < b || (kSlots && state_index<kSlots>(p, n) < 0)) e = b;
+            rows[n] = make_int2(b, e);
+            lens[n] = e - b;
+        }
+        __syncthreads();
+        for (int n = tid; n < p.N; n += kSplitThreads) {
+            int rank = 0;
+            const int ln = lens[n];
+            for (int m2 = 0; m2 < p.N; m2++) {
+                const int lm = lens[m2];
+                rank += (lm > ln) || (lm == ln && m2 < n);
+            }
+            order[rank] = n;
+        }
+        __syncthreads();
+        if (tid == 0 && !chain) {
+            // the producers' deal: claim i = chunk j of unit u, chunk index first;
+            // CTA b starts with claim b - chains, the rest come from the counter
+            int total = 0;
+            for (int n = 0; n < p.N; n++) total += (lens[n] + kChunk - 1) / kChunk;
+            total *= p.H;
+            const int i0 = (int)blockIdx.x - sp.chains;
+            *sm.units_nonempty() = total;
+            *sm.producers() = (int)gridDim.x - sp.chains;
+            ChunkDeal deal;
+            const bool first = i0 < total;
+            sm.sched()[0] = first ? deal.decode(order, p.N, p.H, i0) : -1;
+            *sm.published() = first ? 1 : 0;
+            *sm.claim_done() = first ? 0 : 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const Maps maps = {&tq, &tk, &tv, &tg, &to};
+    if (warp == 16) {
+        if (chain && tid == kThreads) split_loader<kSlots>(p, sp, sm, order, (int)blockIdx.x);
+    } else if (chain) {
+        split_chain<kSlots>(p, sp, sm, order, maps, (int)blockIdx.x);
+    } else if (warp < 4) {
+        ship_role<kSlots>(p, sp, sm, order, maps);
+    } else if (warp < 12) {
+        const ConvParams no_conv = {};
+        e_role<kSlots, kSortChunks, false>(p, no_conv, sm, order, 0, maps);
+    } else {
+        i_role<kSlots, kSortChunks>(p, sm, order, 0);
+    }
+    // every MMA this CTA issued has completed before TMEM is released
+    if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads) {
+        mma_commit(sm.bar(kBarDrain));
+        mbar_wait_drain(sm.bar(kBarDrain), 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(*sm.tmem_base(), kTmCols);
+    // the last CTA to finish returns the deal's scratch slot to zero
+    if (tid == 0 && p.sched) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
+        }
+    }
+}
+
+// =============================================================================
+template <bool kSlots, int kSort, bool kConv>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
-              const __grid_constant__ CUtensorMap to, TcParams p)
+              const __grid_constant__ CUtensorMap to, TcParams p, const __grid_constant__ ConvParams cp)
 {
     extern __shared__ uint8_t smem_raw[];
     Smem sm;
@@ -1508,7 +2356,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     if (warp < 4) {
         chain_role<kSlots, kSort>(p, sm, order, U, maps);
     } else if (warp < 12) {
-        e_role<kSlots, kSort>(p, sm, order, U, maps);
+        e_role<kSlots, kSort, kConv>(p, cp, sm, order, U, maps);
     } else {
         i_role<kSlots, kSort>(p, sm, order, U);
     }
@@ -1590,6 +2438,69 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem
 
 int tc_max_sorted_seqs() { return kMaxSortedSeqs; }
 
+// one chain CTA per unit, at least as many producer CTAs; units fit the
+// producers' packed claims (8 bits) and the sequences the sorted table
+bool tc_split_possible(int units, int N, int num_sms)
+{
+    return units >= 1 && 2 * units <= num_sms && units <= 255 && N <= kMaxSortedSeqs;
+}
+size_t tc_split_flag_bytes(int units) { return ((size_t)(2 * units * kRingSlots + 1) * sizeof(int) + 255) & ~size_t(255); }
+size_t tc_split_bytes(int units) { return (size_t)units * kRingSlots * kSlotBytes + tc_split_flag_bytes(units); }
+
+cudaError_t launch_kda_tc_split(const KdaArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                                const CUtensorMap &tv, const CUtensorMap &tg, const CUtensorMap &to)
+{
+    using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                            const CUtensorMap, TcParams, const SplitParams);
+    static const Kernel kernels[2] = {kda_tc_split_kernel<false>, kda_tc_split_kernel<true>};
+    const int variant = a.state_slots != nullptr;
+    const Kernel kernel = kernels[variant];
+    static std::atomic<int> attr_set[2][64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[variant][dev].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[variant][dev].store(1, std::memory_order_release);
+    }
+    const int units = a.N * a.H;
+    TcParams p;
+    p.cu = a.cu_seqlens;
+    p.beta = a.beta;
+    p.s0 = a.initial_state;
+    p.out = (__nv_bfloat16 *)a.out;
+    p.s1 = a.final_state;
+    p.N = a.N;
+    p.T = a.T;
+    p.H = a.H;
+    p.g_order = nullptr;
+    p.g_rows = nullptr;
+    p.g_une = nullptr;
+    p.err = a.err_word;
+    p.sched = a.sched;
+    p.slots = a.state_slots;
+    p.num_slots = a.num_slots;
+    SplitParams sp;
+    sp.ring = a.split_ring;
+    int *flags = reinterpret_cast<int *>(a.split_ring + (size_t)units * kRingSlots * kSlotBytes);
+    sp.ready = flags;
+    sp.freed = flags + units * kRingSlots;
+    sp.abort = flags + 2 * units * kRingSlots;
+    sp.chains = units;
+    // every CTA resident at once (one per SM): chains and producers wait on one another
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.num_sms);
+    cfg.blockDim = dim3(kSplitThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tg, to, p, sp);
+}
+
 cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
 {
     CUtensorMap tq, tk, tv, tg, to;
@@ -1603,20 +2514,30 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
             !make_map4(&to, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64, 32))
             return cudaErrorInvalidValue;
     }
+    if (a.split_ring) {
+        if (a.conv_w || a.g_order || !a.sched || a.T == 0 || !tc_split_possible(a.N * a.H, a.N, a.num_sms))
+            return cudaErrorInvalidValue;
+        return launch_kda_tc_split(a, tq, tk, tv, tg, to);
+    }
     // one kernel per (slot table, sort mode): 1 sorted here (N <= kMaxSortedSeqs),
     // 2 sorted order given in g_order/g_rows, 0 unsorted; modes 1 and 2 deal
     // dynamically and need the deal's scratch words
     const int sort = a.g_order ? 2 : (a.N <= kMaxSortedSeqs ? 1 : 0);
     if (sort != 0 && !a.sched) return cudaErrorInvalidValue;
-    const int variant = 3 * (a.state_slots != nullptr) + sort;
+    const bool conv = a.conv_w != nullptr;
+    if (conv && sort == 2) return cudaErrorInvalidValue;   // no conv build with a prepared order
+    const int variant = 6 * conv + 3 * (a.state_slots != nullptr) + sort;
     using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                            const CUtensorMap, TcParams);
-    static const Kernel kernels[6] = {kda_tc_kernel<false, 0>, kda_tc_kernel<false, 1>, kda_tc_kernel<false, 2>,
-                                      kda_tc_kernel<true, 0>,  kda_tc_kernel<true, 1>,  kda_tc_kernel<true, 2>};
+                            const CUtensorMap, TcParams, const ConvParams);
+    static const Kernel kernels[12] = {
+        kda_tc_kernel<false, 0, false>, kda_tc_kernel<false, 1, false>, kda_tc_kernel<false, 2, false>,
+        kda_tc_kernel<true, 0, false>,  kda_tc_kernel<true, 1, false>,  kda_tc_kernel<true, 2, false>,
+        kda_tc_kernel<false, 0, true>,  kda_tc_kernel<false, 1, true>,  nullptr,
+        kda_tc_kernel<true, 0, true>,   kda_tc_kernel<true, 1, true>,   nullptr};
     const Kernel kernel = kernels[variant];
     // the shared-memory opt-in, once per (kernel, device); setting it twice
     // (two host threads racing on a first call) is harmless
-    static std::atomic<int> attr_set[6][64];
+    static std::atomic<int> attr_set[12][64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[variant][dev].load(std::memory_order_acquire)) {
@@ -1640,6 +2561,15 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     p.sched = a.sched;
     p.slots = a.state_slots;
     p.num_slots = a.num_slots;
+    ConvParams cp;
+    cp.x[0] = (const uint16_t *)a.q;
+    cp.x[1] = (const uint16_t *)a.k;
+    cp.x[2] = (const uint16_t *)a.v;
+    cp.w = a.conv_w;
+    cp.pool = a.conv_pool;
+    cp.H = a.H;
+    cp.act = a.conv_act;
+    cp.eps = a.conv_eps;
     const int units = a.N * a.H;
     const int grid = units < a.num_sms ? units : a.num_sms;
     // one CTA per SM (shared memory), so a CTA launched early waits for an SM
@@ -1654,7 +2584,7 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tg, to, p);
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tg, to, p, cp);
 }
 
 }  // namespace kda

@@ -189,6 +189,9 @@ def test_conv_then_prefill_matches_the_oracle_chain():
     o_ref, f_ref = oracle.run(qb, kb, vb, g, beta, cu, initial_state=s0)
     assert rel_l2(out.float().cpu().numpy(), o_ref) <= OUT_TOL
     assert rel_l2(fin.cpu().numpy(), f_ref) <= STATE_TOL
+    from gpu_util import check_elementwise
+    check_elementwise(out.float().cpu().numpy(), o_ref, "tc_out")
+    check_elementwise(fin.cpu().numpy(), f_ref, "tc_state_prologue")
 
 
 @pytest.mark.parametrize("pattern", ["one_row", "about_20_rows"])

@@ -6,7 +6,8 @@ and winds down: every MMA and TMA copy already in flight lands before TMEM is
 freed and the CTA exits, so the GPU stays usable.  This test builds a copy of
 the library in which the chain's wait for MMA1 has a limit of zero polls: the
 wait gives up at once although its MMA does complete, which drives every CTA
-through that path.  The call must return, the copy's error word must hold
+through that path -- in split mode the chain CTAs, whose abort then stops
+the producer CTAs waiting on them.  The call must return, the copy's error word must hold
 bit 1, and a normal call afterwards (the regular library, same process and
 context) must still meet the parity bounds.
 """
@@ -22,9 +23,11 @@ from kda_linear_attention_chunk_gb300 import synthetic as syn
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_timeout_sets_bit_and_leaves_the_gpu_usable():
+@pytest.mark.parametrize("split", ["0", "1"])
+def test_wait_timeout_sets_bit_and_leaves_the_gpu_usable(split, monkeypatch):
     from gpu_util import (OUT_TOL, STATE_TOL, check_elementwise, inputs_to_dev, oracle_run, out_to_f64, rel_l2,
                           run_gpu, to_dev, torch)
+    monkeypatch.setenv("KDA_SPLIT", split)   # the fused kernel, or split mode (its chain's MMA1 wait)
     t = torch()
     lib = kda.load(kbuild.build_variant("wait0", ["KDA_WAIT_LIMIT_MMA1=0"]))
     w = syn.Workload("timeout", [300, 64, 1, 129], H=4, dk=128, dv=128, init_state=True, seed=41)
