@@ -493,18 +493,38 @@ def config_bytes(w, rows: int, with_initial: bool) -> int:
     return rows * w.H * per_row_head + n * w.H * w.dk * w.dv * 4 * (int(with_initial) + 1)
 
 
-def measure_configs(torch, np, kda, stream, reps: int = 3):
+def tc_mode(w, rows: int, num_sms: int) -> str:
+    """Which form of the tensor-core prefill a call of this workload runs
+    (kda.h, "Split"): split for few units (N * H at most half the SMs) and
+    T >= 1024 rows, unless KDA_SPLIT says otherwise; else the fused kernel."""
+    if w.qkv_dtype != "bf16" or w.dk != 128 or w.dv != 128:
+        return "cuda-core"
+    n = 1 if w.calls > 1 else w.N
+    env = os.environ.get("KDA_SPLIT", "")
+    ok = 2 * n * w.H <= num_sms and n <= 256 and rows >= 1
+    if env.startswith("0") or not ok:
+        return "fused"
+    return "split" if env.startswith("1") or rows >= 1024 else "fused"
+
+
+def measure_configs(torch, np, kda, stream, reps: int = 3, only=None, rows_override: int = 0):
     """The other four workloads, one line each: time per call (CUDA events, after
     one warm-up), tokens/s and the fraction of the HBM roofline.  The context of
     262,144 rows runs as its 32 chained calls of 8192 rows with the state carried;
     for timing, every call reads the same 8192-row input set (each call's inputs
-    exceed L2, so nothing is served from a previous call)."""
+    exceed L2, so nothing is served from a previous call).  `only` times one
+    workload alone (profiler captures); rows_override then shortens a
+    single-sequence workload to that many rows."""
     from kda_linear_attention_chunk_gb300 import synthetic as syn
     peak, _ = peaks()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     res = {}
     for name, w in syn.workloads().items():
-        if name == WORKLOAD:
+        if name == WORKLOAD or (only is not None and name != only):
             continue
+        if rows_override and w.N == 1 and w.calls == 1:
+            w = syn.Workload(f"{name[:name.rfind('_')]}_{rows_override}", [rows_override], H=w.H, dk=w.dk,
+                             dv=w.dv, qkv_dtype=w.qkv_dtype, init_state=w.init_state, seed=w.seed)
         rows = w.T // w.calls
         x = syn.draw(w, 0, rows)
         dt = torch.bfloat16 if w.qkv_dtype == "bf16" else torch.float32
@@ -534,10 +554,10 @@ def measure_configs(torch, np, kda, stream, reps: int = 3):
         torch.cuda.synchronize()
         ms_call = e0.elapsed_time(e1) / (reps * w.calls)
         alg = sum(config_bytes(w, rows, with_initial=(s0 is not None) or c > 0) for c in range(w.calls)) / w.calls
-        res[name] = {"calls": w.calls, "rows_per_call": rows, "us_per_call": ms_call * 1e3,
-                     "tokens_per_s": rows / (ms_call / 1e3),
-                     "roofline_frac": alg / (ms_call / 1e3) / 1e9 / peak,
-                     "units": n * w.H}
+        res[w.name] = {"calls": w.calls, "rows_per_call": rows, "us_per_call": ms_call * 1e3,
+                       "tokens_per_s": rows / (ms_call / 1e3),
+                       "roofline_frac": alg / (ms_call / 1e3) / 1e9 / peak,
+                       "units": n * w.H, "kernel": tc_mode(w, rows, sms)}
         del d, out, fin, s0
         torch.cuda.empty_cache()
     return res
@@ -766,9 +786,22 @@ def main():
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the decode-step, fold and short-conv measurements")
     ap.add_argument("--no-configs", action="store_true", help="skip the other four workloads")
+    ap.add_argument("--profile-config", default=None,
+                    help="time only this one of the other workloads (for profiler captures), nothing else")
+    ap.add_argument("--profile-rows", type=int, default=0,
+                    help="with --profile-config: a single-sequence workload shortened to this many rows")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile_config:
+        import numpy as np
+        import torch
+        import kda_linear_attention_chunk_gb300 as kda
+        res = measure_configs(torch, np, kda, torch.cuda.current_stream(), reps=args.steps, only=args.profile_config,
+                              rows_override=args.profile_rows)
+        assert kda.device_error() == 0, "device error word set"
+        print(json.dumps({"profile_config": res}), flush=True)
+        return
     line = run_reference_arm(args) if args.impl == "reference" else run_gpu_arm(args)
     if line is not None:
         print(json.dumps(line), flush=True)
