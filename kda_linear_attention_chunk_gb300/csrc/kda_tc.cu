@@ -1901,9 +1901,10 @@ __device__ __forceinline__ void split_scale_state(uint32_t tmem, uint32_t lane_o
 }
 
 // Chain CTA of unit uu, warp 16 (its first lane): the slot copies.  Chunk j
-// goes into buffer j & 1 once the producers have published it and the chain's
-// MMA3 of chunk j - 2 is done with the buffer; once chunk j has landed, its
-// ring slot goes back to the producers.  (Done by the chain's own first
+// goes into buffer j & 1 once the producers have published it (the flag is
+// awaited ahead of time) and the chain's MMAs of chunk j - 2 are done with the
+// buffer -- the part MMA1 reads as soon as MMA1 is done, the rest after MMA3;
+// once chunk j has landed, its ring slot goes back to the producers.  (Done by the chain's own first
 // thread, the flag round trips cost about 3.7k cycles a chunk on its path.)
 template <bool kSlots>
 __device__ void split_loader(const TcParams &p, const SplitParams &sp, const Smem &sm, const int *order, int uu)
@@ -1911,43 +1912,178 @@ __device__ void split_loader(const TcParams &p, const SplitParams &sp, const Sme
     const Unit un = get_unit<kSlots, 1>(p, order, uu);
     const int nch = un.nchunks;
     auto slot_of = [&](int j) { return uu * kRingSlots + j % kRingSlots; };
-    int issued = 0, landed = 0;
-    auto issue = [&](int j) -> bool {
-        const int *rf = sp.ready + slot_of(j);
-        int val = 0;
-        if (!flag_wait(rf, 2 * (j + 1), sp, sm.abort_flag(), &val)) return false;
-        fence_proxy_async_global();
-        const int b = j & 1;
-        sm.split_parity()[b] = val & 1;
-        const uint32_t dst = sm.u32(b * kSlotBytes), bar = sm.bar(kBarKQFull + b);
+    int issued_a = 0, issued_b = 0, landed = 0;
+    // part A of chunk j (k/q rows, beta*V, T16, the decay constants): what MMA-b,
+    // the rescale and MMA1 read; part B (Km, tril(A_qk)^T): what MMA3 reads
+    auto copy = [&](int j, uint32_t off, uint32_t bytes, uint32_t bar) {
+        const uint32_t dst = sm.u32((j & 1) * kSlotBytes);
         const uint8_t *src = sp.ring + (size_t)slot_of(j) * kSlotBytes;
-        mbar_arrive_expect_tx(bar, kSlotBytes);
-        for (uint32_t off = 0; off < kSlotBytes; off += 16384)
-            bulk_load(dst + off, src + off, kSlotBytes - off < 16384u ? kSlotBytes - off : 16384u, bar);
-        issued = j + 1;
+        for (uint32_t o = off; o < off + bytes; o += 16384)
+            bulk_load(dst + o, src + o, off + bytes - o < 16384u ? off + bytes - o : 16384u, bar);
+    };
+    int par_next = 0;   // layout bit of the chunk whose ready flag was seen last
+    auto await_ready = [&](int j) -> bool {
+        int val = 0;
+        KDA_PHASE(2, j, 0);
+        if (!flag_wait(sp.ready + slot_of(j), 2 * (j + 1), sp, sm.abort_flag(), &val)) return false;
+        KDA_PHASE(2, j, 1);
+        fence_proxy_async_global();
+        par_next = val & 1;
         return true;
     };
-    bool ok = nch == 0 || (issue(0) && (nch < 2 || issue(1)));
+    auto issue_a = [&](int j) {   // (buffer j & 1 is free: its layout bit may change now)
+        sm.split_parity()[j & 1] = par_next;   // read by the chain after the part A barrier
+        const uint32_t bar = sm.bar(kBarKQFull + (j & 1));
+        mbar_arrive_expect_tx(bar, kOffMma3 + (kSlotBytes - kSlotT16));
+        copy(j, 0, kOffMma3, bar);
+        copy(j, kSlotT16, kSlotBytes - kSlotT16, bar);
+        issued_a = j + 1;
+    };
+    auto issue_b = [&](int j) {
+        const uint32_t bar = sm.bar(kBarVFull + (j & 1));
+        mbar_arrive_expect_tx(bar, kSlotT16 - kOffMma3);
+        copy(j, kOffMma3, kSlotT16 - kOffMma3, bar);
+        issued_b = j + 1;
+    };
+    bool ok = true;
+    for (int j = 0; ok && j < 2 && j < nch; j++) {
+        ok = await_ready(j);
+        if (ok) { issue_a(j); issue_b(j); }
+    }
     for (int j = 0; ok && j < nch; j++) {
         const int b = j & 1;
-        ok = mbar_wait(sm.bar(kBarKQFull + b), (j >> 1) & 1, sm.abort_flag());
+        const uint32_t ph = (j >> 1) & 1;
+        ok = mbar_wait(sm.bar(kBarKQFull + b), ph, sm.abort_flag()) && mbar_wait(sm.bar(kBarVFull + b), ph, sm.abort_flag());
         if (!ok) break;
+        KDA_PHASE(2, j, 2);
         landed = j + 1;
         st_release_gpu(sp.freed + slot_of(j), j + 1);   // the slot may take chunk j + kRingSlots
-        if (j + 2 < nch) ok = mbar_wait(sm.bar(kBarKmFree + b), (j >> 1) & 1, sm.abort_flag()) && issue(j + 2);
+        if (j + 2 < nch) {
+            // chunk j + 2 into buffer b: part A once MMA1 of chunk j is done with it,
+            // part B once MMA3 is
+            ok = await_ready(j + 2) && mbar_wait(sm.bar(kBarAFull + b), ph, sm.abort_flag());
+            if (!ok) break;
+            issue_a(j + 2);
+            ok = mbar_wait(sm.bar(kBarKmFree + b), ph, sm.abort_flag());
+            if (!ok) break;
+            issue_b(j + 2);
+        }
     }
     if (!ok) split_abort(p, sp, sm);
     // copies still in flight land before the CTA exits
-    for (int j = landed; j < issued; j++) mbar_wait_drain(sm.bar(kBarKQFull + (j & 1)), (j >> 1) & 1);
+    for (int j = landed; j < issued_a; j++) mbar_wait_drain(sm.bar(kBarKQFull + (j & 1)), (j >> 1) & 1);
+    for (int j = landed; j < issued_b; j++) mbar_wait_drain(sm.bar(kBarVFull + (j & 1)), (j >> 1) & 1);
 }
 
-// Chain CTA of unit uu (sorted order).  Per chunk j (slot buffer b = j & 1,
-// the producer's stage parity `par` fixing where K and Q rows, Km and
-// tril(A_qk)^T sit and so which TMEM columns take Delta and O):
-//   MMA-b's U half: U^T = (beta V)^T T^T into the Delta columns;
-//   S rescaled, O columns zeroed; MMA1 [U^T - S'^T W'^T | S'^T Qp^T];
-//   Delta^T -> fp16; MMA3 [O^T | S^T] += Delta^T [tril(A_qk)^T | Km];
-//   the slot goes back to the producers; O^T -> bf16 -> out.
+// The split chain's two block barriers per chunk (compute warps and the MMA
+// issuer warp) and the mbarriers the issuer commits to (named barrier ids and
+// mbarrier slots of the chain CTA; kBarKmFree[b] marks buffer b free).
+constexpr int kBarSplitSync = 4;                       // named barrier: 16 compute warps + the issuer
+constexpr int kSplitSyncThreads = kThreads + 32;
+constexpr int kBarM1D = kBarMma1;                      // MMA1's Delta half done (and every MMA before it)
+constexpr int kBarM3S = kBarMma3;                      // MMA3's state half done
+constexpr int kBarM3O = kBarPrepDone;                  // MMA3's output half done
+
+// Chain CTA of unit uu, warp 17: the MMA issuer (its first lane issues, the
+// whole warp joins the block barriers).  Per chunk j, in this order on the
+// tensor pipe: MMA-b's U half of chunk j (once the chunk has landed), then --
+// after the compute warps' rescale -- MMA1's Delta half and its output half,
+// then -- after their Delta conversion -- MMA3's state half and its output
+// half.  The halves are the fused kernel's N = 128 MMA1 and N = 192 MMA3
+// split by their B rows (K rows / Q rows; Km / tril(A_qk)^T), so that the
+// compute warps can go on as soon as the half they need is done.
+template <bool kSlots>
+__device__ void split_issuer(const TcParams &p, const Smem &sm, const int *order, int uu)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t tmem = *sm.tmem_base();
+    const Unit un = get_unit<kSlots, 1>(p, order, uu);
+    const int nch = un.nchunks;
+    if (nch == 0) return;
+    bool ok = true;
+    auto mma_b = [&](int j) {   // U^T = (beta V)^T T^T into chunk j's Delta columns
+        const int b = j & 1, par = sm.split_parity()[b];
+        const uint32_t buf = sm.u32(b * kSlotBytes);
+        const uint32_t id = idesc_f16(128, 64, 1, 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ks++) {
+            const uint64_t bd = smem_desc_sw128(buf + kSlotT16 + ks * 32, 16, 1024);
+            const uint64_t au = smem_desc_sw128(buf + kOffV + ks * 2048, 8192, 1024);
+            mma_ss(tmem + tm_d(par), au, bd, id, ks > 0);
+        }
+    };
+    if (lane == 0) {
+        ok = mbar_wait(sm.bar(kBarKQFull), 0, sm.abort_flag());
+        tc_fence_after();
+        if (ok) mma_b(0);
+    }
+    for (int j = 0; j < nch; j++) {
+        const int b = j & 1;
+        if (role_any(!ok, kBarSplitSync, kSplitSyncThreads)) break;   // the rescale is done
+        if (lane == 0) KDA_PHASE(0, j, 0);
+        if (lane == 0) {
+            const int par = sm.split_parity()[b];
+            const uint32_t buf = sm.u32(b * kSlotBytes);
+            tc_fence_after();
+            const uint32_t id = idesc_f16(128, 64, 0, 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ks++) {   // U^T - S'^T W'^T: the K rows hold -W'
+                const int kb = ks >> 2, kin = ks & 3;
+                mma_ts(tmem + tm_d(par), tmem + kTmS0h + 8 * ks,
+                       smem_desc_sw128(buf + kOffKQ + kb * 16384 + off_k(par) + kin * 32, 16, 1024), id, 1);
+            }
+            mma_commit(sm.bar(kBarM1D));
+#pragma unroll
+            for (int ks = 0; ks < 8; ks++) {   // S'^T Qp^T: the Q rows
+                const int kb = ks >> 2, kin = ks & 3;
+                mma_ts(tmem + tm_o(par), tmem + kTmS0h + 8 * ks,
+                       smem_desc_sw128(buf + kOffKQ + kb * 16384 + off_q(par) + kin * 32, 16, 1024), id, ks > 0);
+            }
+            mma_commit(sm.bar(kBarAFull + b));   // MMA-b and MMA1 are done with part A of buffer b
+        }
+        if (role_any(!ok, kBarSplitSync, kSplitSyncThreads)) break;   // Delta is in fp16
+        if (lane == 0) KDA_PHASE(0, j, 1);
+        if (lane == 0) {
+            const int par = sm.split_parity()[b];
+            const uint32_t buf = sm.u32(b * kSlotBytes);
+            ok = mbar_wait(sm.bar(kBarVFull + b), (j >> 1) & 1, sm.abort_flag());   // part B (Km, tril(A_qk)^T)
+            tc_fence_after();
+            if (ok) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ks++)     // S^T += Delta^T Km
+                mma_ts(tmem + kTmS, tmem + kTmDh + 8 * ks,
+                       smem_desc_sw128(buf + off_km(par) + ks * 2048, 8192, 1024), idesc_f16(128, 128, 0, 1), 1);
+            }
+            mma_commit(sm.bar(kBarM3S));   // (also when nothing was issued: the compute warps' wait ends)
+            if (ok) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ks++)     // O^T += Delta^T tril(A_qk)^T
+                mma_ts(tmem + tm_o(par), tmem + kTmDh + 8 * ks,
+                       smem_desc_sw128(buf + off_bq(par) + ks * 2048, 8192, 1024), idesc_f16(128, 64, 0, 1), 1);
+            }
+            mma_commit(sm.bar(kBarM3O));
+            mma_commit(sm.bar(kBarKmFree + b));   // every MMA reading buffer b is done: it may take chunk j + 2
+            KDA_PHASE(0, j, 2);
+            if (ok && j + 1 < nch) {
+                ok = mbar_wait(sm.bar(kBarKQFull + (b ^ 1)), ((j + 1) >> 1) & 1, sm.abort_flag());
+                tc_fence_after();
+                if (ok) mma_b(j + 1);
+                KDA_PHASE(0, j, 3);
+            }
+        }
+    }
+}
+
+// Chain CTA of unit uu (sorted order), the 16 compute warps.  Per chunk j
+// (slot buffer b = j & 1; the layout bit `par` of the chunk, alternating
+// from chunk to chunk, fixes where K and Q rows, Km and tril(A_qk)^T sit and
+// so which TMEM columns take Delta and O):
+//   the state is rescaled (S' = S pend fm, and its fp16 copy);
+//   [block barrier: the issuer starts MMA1, Delta half first]
+//   chunk j-1's outputs leave (O^T -> bf16 -> out), while MMA1 runs;
+//   Delta^T -> fp16 once MMA1's Delta half is done;
+//   [block barrier: the issuer starts MMA3, state half first]
+//   the next chunk starts once MMA3's state half is done.
 // The arithmetic, operand for operand, is the fused kernel's.
 template <bool kSlots>
 __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem &sm, const int *order,
@@ -1972,31 +2108,14 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
     const size_t wrows = ubase + (size_t)(32 * q) * kD;   // this warp's first state row
     bool ok = true;
     split_load_state(p.s0 ? p.s0 + wrows : nullptr, stg, tmem + kTmS + lane_off, lane, cg);
-    tc_fence_before();
-    // thread 0: U^T = (beta V)^T T^T of chunk jb into its Delta columns (MMA-b's
-    // second half), issued as soon as the chunk has landed and MMA3 of the
-    // chunk before has been issued (its Delta columns are free then)
-    int mmab_done = 0;   // chunks whose MMA-b is issued
-    auto issue_mmab = [&](int jb) {
-        const int bb = jb & 1, pb = sm.split_parity()[bb];
-        const uint32_t bufb = sm.u32(bb * kSlotBytes);
-        tc_fence_after();
-        const uint32_t id = idesc_f16(128, 64, 1, 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ks++) {
-            const uint64_t bd = smem_desc_sw128(bufb + kSlotT16 + ks * 32, 16, 1024);
-            const uint64_t au = smem_desc_sw128(bufb + kOffV + ks * 2048, 8192, 1024);
-            mma_ss(tmem + tm_d(pb), au, bd, id, ks > 0);
-        }
-        mmab_done = jb + 1;
-    };
-    int consumed = 0;
     // O^T of chunk jo (layout paro) -> bf16 tiles of 32 rows in staging buffer
     // jo & 1 (this warp: rows 16 cg .. +15, its 32 value channels), stored by
     // bulk tensor copies; partial tiles row by row.  Thread 0 has made sure
     // before (bulk_wait_read1 ahead of a block barrier) that the copies of
     // chunk jo - 2 have read the buffer.  false: a thread's wait ran out.
     auto outputs = [&](int jo, int paro) -> bool {
+        ok = mbar_wait(sm.bar(kBarM3O), jo & 1, sm.abort_flag()) && ok;   // MMA3's output half of chunk jo
+        tc_fence_after();
         const int row0 = un.bos + jo * kChunk, L = min(kChunk, un.eos - row0);
         const uint32_t ost = sm.u32(kCOut + (jo & 1) * 16384);
         uint32_t o[2][8];
@@ -2038,49 +2157,35 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
         }
         return true;
     };
-    bool out_failed = false;
-    // Failures are gathered at the block barriers of a chunk (role_any): a
-    // thread whose wait ran out goes on with harmless work up to the next one.
+    int consumed = 0, prev_par = 0;
+    bool failed = false;
     for (int j = 0; j < nch; j++) {
         const int b = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
         if (tid == 0) KDA_PHASE(1, j, 0);
-        ok = ok && mbar_wait(sm.bar(kBarKQFull + b), ph, sm.abort_flag());
+        ok = ok && mbar_wait(sm.bar(kBarKQFull + b), (j >> 1) & 1, sm.abort_flag());
         tc_fence_after();
         if (tid == 0) KDA_PHASE(1, j, 1);
         const int par = sm.split_parity()[b];
-        const uint32_t buf = sm.u32(b * kSlotBytes);
         const float *hdr = sm.ptr<float>(b * kSlotBytes + kSlotHdr);
-        if (tid == 0 && ok && mmab_done == j) issue_mmab(j);
-        if (tid == 0) KDA_PHASE(1, j, 2);
-        {
-            uint32_t z[16];
-#pragma unroll
-            for (int i = 0; i < 16; i++) z[i] = 0u;
-            tmem_st16(tmem + tm_o(par) + lane_off + 16 * cg, z);   // MMA1 accumulates the output here
-        }
         split_scale_state(tmem, lane_off, cg, hdr, j > 0 ? pendr + ((j - 1) & 1) * 128 : nullptr);
+        if (tid == 0) KDA_PHASE(1, j, 11);
         if (tid < 128) pendr[(j & 1) * 128 + tid] = hdr[128 + tid];
         tmem_wait_st();
         tc_fence_before();
-        if (role_any(!ok, kBarChain, kThreads)) break;
+        if (tid == 0) KDA_PHASE(1, j, 12);
+        if (tid == 0) bulk_wait_read1();   // chunk j-3's output copies have read staging buffer (j-1) & 1
+        if (tid == 0) KDA_PHASE(1, j, 2);
+        if (role_any(!ok, kBarSplitSync, kSplitSyncThreads)) { failed = true; break; }
         consumed = j + 1;
-        if (tid == 0) {
-            KDA_PHASE(1, j, 3);
-            tc_fence_after();
-            const uint32_t id1 = idesc_f16(128, 128, 0, 0);
-#pragma unroll
-            for (int ks = 0; ks < 8; ks++) {
-                const int kb = ks >> 2, kin = ks & 3;
-                const uint64_t bwq = smem_desc_sw128(buf + kOffKQ + kb * 16384 + kin * 32, 16, 1024);
-                mma_ts(tmem + (par ? tm_o(1) : tm_d(0)), tmem + kTmS0h + 8 * ks, bwq, id1, 1);
-            }
-            mma_commit(sm.bar(kBarMma1));
-            KDA_PHASE(1, j, 4);
-        }
-        ok = mbar_wait(sm.bar(kBarMma1), j & 1, sm.abort_flag(), KDA_WAIT_LIMIT_MMA1);
-        if (tid == 0) KDA_PHASE(1, j, 5);
+        if (tid == 0) KDA_PHASE(1, j, 3);
+        // chunk j-1's outputs, while MMA1 of chunk j runs (it writes the other
+        // layout's columns); a failure there is gathered at the next barrier
+        // that the issuer also joins
+        if (j > 0 && !outputs(j - 1, prev_par)) ok = false;
+        if (tid == 0) KDA_PHASE(1, j, 4);
+        ok = mbar_wait(sm.bar(kBarM1D), j & 1, sm.abort_flag(), KDA_WAIT_LIMIT_MMA1) && ok;
         tc_fence_after();
+        if (tid == 0) KDA_PHASE(1, j, 5);
         {   // Delta^T (fp32) -> fp16 A operand, this warp's 16 columns
             uint32_t x[16], h[8];
             tmem_ld16(tmem + tm_d(par) + lane_off + 16 * cg, x);
@@ -2091,33 +2196,20 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
         }
         tmem_wait_st();
         tc_fence_before();
-        if (tid == 0) bulk_wait_read1();   // chunk j-2's output copies have read staging buffer j & 1
-        if (role_any(!ok, kBarChain, kThreads)) break;
-        if (tid == 0) {
-            KDA_PHASE(1, j, 6);
-            tc_fence_after();
-            const uint32_t id3 = idesc_f16(128, 192, 0, 1);
-#pragma unroll
-            for (int ks = 0; ks < 4; ks++) {
-                const uint64_t b3 = smem_desc_sw128(buf + kOffMma3 + ks * 2048, 8192, 1024);
-                mma_ts(tmem + (par ? kTmS : tm_o(0)), tmem + kTmDh + 8 * ks, b3, id3, 1);
-            }
-            mma_commit(sm.bar(kBarMma3));
-            // the next chunk's MMA-b, if it has landed: it runs after MMA3 (its
-            // Delta columns are this chunk's layout's other ones)
-            if (j + 1 < nch && mbar_try_wait(sm.bar(kBarKQFull + (b ^ 1)), ((j + 1) >> 1) & 1)) issue_mmab(j + 1);
-            KDA_PHASE(1, j, 7);
-        }
-        ok = mbar_wait(sm.bar(kBarMma3), j & 1, sm.abort_flag());
+        if (role_any(!ok, kBarSplitSync, kSplitSyncThreads)) { failed = true; break; }
+        if (tid == 0) KDA_PHASE(1, j, 6);
+        ok = mbar_wait(sm.bar(kBarM3S), j & 1, sm.abort_flag());
         tc_fence_after();
-        if (tid == 0) {
-            KDA_PHASE(1, j, 8);
-            if (ok) mbar_arrive(sm.bar(kBarKmFree + b));   // the buffer may take chunk j + 2
-            KDA_PHASE(1, j, 9);
-        }
-        if (!outputs(j, par)) { out_failed = true; break; }
+        if (tid == 0) KDA_PHASE(1, j, 7);
+        prev_par = par;
     }
-    const bool any_failed = role_any(!ok || out_failed, kBarChain, kThreads);
+    // the last chunk's outputs
+    if (!failed) {
+        if (tid == 0) bulk_wait_read1();
+        named_bar(kBarChain, kThreads);
+        if (!outputs(nch - 1, prev_par)) failed = true;
+    }
+    const bool any_failed = role_any(!ok || failed, kBarChain, kThreads);
     const bool done = consumed == nch && !any_failed;
     if (tid == 0) {
         if (!done) split_abort(p, sp, sm);
@@ -2135,7 +2227,7 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
 // resident at once, so that the chains and the producers can wait on one
 // another); CTA b < sp.chains runs the chain of unit b (sorted order), the
 // others prepare chunks.
-constexpr int kSplitThreads = kThreads + 32;   // + the chain CTAs' loader warp
+constexpr int kSplitThreads = kThreads + 64;   // + the chain CTAs' loader warp and MMA issuer warp
 
 template <bool kSlots>
 __global__ void __launch_bounds__(kSplitThreads, 1)
@@ -2165,7 +2257,7 @@ kda_tc_split_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         mbar_init(sm.bar(kBarGFull), 1);
         mbar_init(sm.bar(kBarMma1), 1);
         mbar_init(sm.bar(kBarMma3), 1);
-        mbar_init(sm.bar(kBarDrain), 3);
+        mbar_init(sm.bar(kBarDrain), 4);   // + the chain CTAs' MMA issuer (warp 17)
         mbar_fence_init();
     }
     if (warp == 0) {
@@ -2221,6 +2313,8 @@ kda_tc_split_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     const Maps maps = {&tq, &tk, &tv, &tg, &to};
     if (warp == 16) {
         if (chain && tid == kThreads) split_loader<kSlots>(p, sp, sm, order, (int)blockIdx.x);
+    } else if (warp == 17) {
+        if (chain) split_issuer<kSlots>(p, sm, order, (int)blockIdx.x);
     } else if (chain) {
         split_chain<kSlots>(p, sp, sm, order, maps, (int)blockIdx.x);
     } else if (warp < 4) {
@@ -2232,7 +2326,7 @@ kda_tc_split_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         i_role<kSlots, kSortChunks>(p, sm, order, 0);
     }
     // every MMA this CTA issued has completed before TMEM is released
-    if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads) {
+    if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads || tid == kThreads + 32) {
         mma_commit(sm.bar(kBarDrain));
         mbar_wait_drain(sm.bar(kBarDrain), 0);
     }
