@@ -544,20 +544,35 @@ def measure_configs(torch, np, kda, stream, reps: int = 3, only=None, rows_overr
                                   final_state=fin[c % 2], stream=stream)
                 state = fin[c % 2]
 
-        run()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
+        def timed() -> float:
             run()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms_call = e0.elapsed_time(e1) / (reps * w.calls)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / (reps * w.calls)
+
+        ms_call = timed()
         alg = sum(config_bytes(w, rows, with_initial=(s0 is not None) or c > 0) for c in range(w.calls)) / w.calls
+        mode = tc_mode(w, rows, sms)
         res[w.name] = {"calls": w.calls, "rows_per_call": rows, "us_per_call": ms_call * 1e3,
                        "tokens_per_s": rows / (ms_call / 1e3),
                        "roofline_frac": alg / (ms_call / 1e3) / 1e9 / peak,
-                       "units": n * w.H, "kernel": tc_mode(w, rows, sms)}
+                       "units": n * w.H, "kernel": mode}
+        if mode == "split" and only is None:
+            # the same calls on the fused kernel, for comparison (KDA_SPLIT is read on every call)
+            old = os.environ.get("KDA_SPLIT")
+            os.environ["KDA_SPLIT"] = "0"
+            try:
+                res[w.name]["fused_us_per_call"] = timed() * 1e3
+            finally:
+                if old is None:
+                    del os.environ["KDA_SPLIT"]
+                else:
+                    os.environ["KDA_SPLIT"] = old
         del d, out, fin, s0
         torch.cuda.empty_cache()
     return res

@@ -6,7 +6,8 @@ in which that holds (|G_r - G_m| <= 15 ln 2 per chunk and key channel) and
 that a chunk outside it sets bit 32 of the device error word.  These tests
 draw gates of several strengths (synthetic.decay_profile: U[-a, 0] for
 a = 0.2, 0.5, 1, 3; channels held at g = -20; 5% of the entries positive)
-and check on the same inputs that
+and check on the same inputs -- with the tensor-core kernel fused and in
+split mode (environment variable KDA_SPLIT) -- that
 
 * the bit is set when the inputs leave the range and clear when they stay
   inside it (the extent is computed here in fp64 from g; calls within 1% of
@@ -41,8 +42,11 @@ def gpu_call(x, cu, s0, full_range):
     return out_to_f64(out), fin.cpu().numpy().astype(np.float64), kda.device_error(reset=True)
 
 
+@pytest.mark.parametrize("split", ["0", "1"])
 @pytest.mark.parametrize("profile", syn.DECAY_PROFILES)
-def test_tensor_core_range_bit_and_parity(profile):
+def test_tensor_core_range_bit_and_parity(profile, split, monkeypatch):
+    # the fused kernel, and split mode (whose producers run the same decay scan)
+    monkeypatch.setenv("KDA_SPLIT", split)
     x, cu, s0 = draw(profile)
     extent = tc_decay_extent(x["g"], cu)
     o, f, word = gpu_call(x, cu, s0, full_range=False)
