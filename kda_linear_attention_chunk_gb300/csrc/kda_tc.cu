@@ -141,13 +141,18 @@ constexpr uint32_t kSmemBytes = kOffOT + 8192 + 1024;   // + alignment slack
 // another at the pace of a whole prep pipeline.  Only the state chain (the
 // rescale, MMA1, Delta, MMA3, outputs) depends on the previous chunk; the
 // decay scan, the operands, A, the inverse, W' and beta*V do not.  In split
-// mode CTA b < chains runs the chain of unit b alone, with all 16 warps, and
+// mode CTA b < chains runs the chain of unit b alone -- 16 compute warps, a
+// loader warp and an MMA-issuer warp (576 threads for every CTA) -- and
 // every other CTA prepares chunks -- any unit's, in the order (chunk index,
 // unit) -- with the prep roles unchanged and ships each finished stage through
 // a ring in global memory (kRingSlots slots per unit, in L2 in practice):
 // producer and chain hand over through flags with release/acquire ordering.
 constexpr int kSortChunks = 3;                          // the producers' deal: one chunk per claim
 constexpr int kRingSlots = 4;
+// each ring slot's two flags in cache lines of their own (128 B apart, the
+// next slot 256 B on), so that the polling spreads over L2 (measured: with
+// the flags packed together, long_65536 took 18 % longer in some runs)
+constexpr int kFlagSlotStride = 64;                     // ints per ring slot: ready at +0, freed at +32
 constexpr uint32_t kSlotT16 = kStageBytes;              // slot: the stage | T16 | fm, pend
 constexpr uint32_t kSlotHdr = kStageBytes + 8192;
 constexpr uint32_t kSlotBytes = kSlotHdr + 1024;
@@ -214,8 +219,8 @@ struct ConvParams {
 // Split mode's hand-over (zeroed by the host before each launch).
 struct SplitParams {
     uint8_t *ring;         // [units][kRingSlots][kSlotBytes]
-    int *ready;            // [units][kRingSlots]: 2 (j + 1) + stage parity once chunk j is in the slot
-    int *freed;            // [units][kRingSlots]: j + 1 once the chain is done with chunk j
+    int *ready;            // per slot (stride kFlagSlotStride): 2 (j + 1) + layout bit once chunk j is in the slot
+    int *freed;            // per slot (stride kFlagSlotStride): j + 1 once the chain is done with chunk j
     int *abort;            // set by a CTA whose wait on another CTA ran out
     int chains;            // CTAs 0 .. chains-1 run the chains, one unit each (units in sorted order)
 };
@@ -1771,7 +1776,8 @@ __device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &
                   mbar_wait(sm.bar(kBarWReady + s), ph, sm.abort_flag());
         if (v == 0) KDA_PHASE(1, item, 1);
         // the chain has read the chunk kRingSlots back from this slot
-        if (ok && v == 0 && j >= kRingSlots) ok = flag_wait(sp.freed + slot, j - kRingSlots + 1, sp, sm.abort_flag());
+        if (ok && v == 0 && j >= kRingSlots)
+            ok = flag_wait(sp.freed + slot * kFlagSlotStride, j - kRingSlots + 1, sp, sm.abort_flag());
         if (role_any(!ok, kBarChain, kChainThreads)) {
             failed = true;
             break;
@@ -1804,7 +1810,7 @@ __device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &
         named_bar(kBarChain, kChainThreads);
         if (v == 0) {
             fence_proxy_async_global();
-            st_release_gpu(sp.ready + slot, 2 * (j + 1) + (j & 1));   // + the stage's layout bit
+            st_release_gpu(sp.ready + slot * kFlagSlotStride, 2 * (j + 1) + (j & 1));   // + the stage's layout bit
             KDA_PHASE(1, item, 5);
         }
     }
@@ -1821,7 +1827,7 @@ __device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &
     }
 }
 
-// ---- the split chain: one unit, all 16 warps -----------------------------------
+// ---- the split chain: one unit, 16 compute warps -------------------------------
 // Warp w owns TMEM lanes 32 (w % 4) .. +31 (value channels) and the quarter
 // w / 4 of each lane's columns.  States move through the warp's 2 KB slice of
 // the output staging buffers, as in chain_load_state / chain_store_state.
@@ -1925,7 +1931,7 @@ __device__ void split_loader(const TcParams &p, const SplitParams &sp, const Sme
     auto await_ready = [&](int j) -> bool {
         int val = 0;
         KDA_PHASE(2, j, 0);
-        if (!flag_wait(sp.ready + slot_of(j), 2 * (j + 1), sp, sm.abort_flag(), &val)) return false;
+        if (!flag_wait(sp.ready + slot_of(j) * kFlagSlotStride, 2 * (j + 1), sp, sm.abort_flag(), &val)) return false;
         KDA_PHASE(2, j, 1);
         fence_proxy_async_global();
         par_next = val & 1;
@@ -1957,7 +1963,7 @@ __device__ void split_loader(const TcParams &p, const SplitParams &sp, const Sme
         if (!ok) break;
         KDA_PHASE(2, j, 2);
         landed = j + 1;
-        st_release_gpu(sp.freed + slot_of(j), j + 1);   // the slot may take chunk j + kRingSlots
+        st_release_gpu(sp.freed + slot_of(j) * kFlagSlotStride, j + 1);   // the slot may take chunk j + kRingSlots
         if (j + 2 < nch) {
             // chunk j + 2 into buffer b: part A once MMA1 of chunk j is done with it,
             // part B once MMA3 is
@@ -2538,7 +2544,7 @@ bool tc_split_possible(int units, int N, int num_sms)
 {
     return units >= 1 && 2 * units <= num_sms && units <= 255 && N <= kMaxSortedSeqs;
 }
-size_t tc_split_flag_bytes(int units) { return ((size_t)(2 * units * kRingSlots + 1) * sizeof(int) + 255) & ~size_t(255); }
+size_t tc_split_flag_bytes(int units) { return ((size_t)units * kRingSlots * kFlagSlotStride + 32) * sizeof(int); }
 size_t tc_split_bytes(int units) { return (size_t)units * kRingSlots * kSlotBytes + tc_split_flag_bytes(units); }
 
 cudaError_t launch_kda_tc_split(const KdaArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
@@ -2578,8 +2584,8 @@ cudaError_t launch_kda_tc_split(const KdaArgs &a, const CUtensorMap &tq, const C
     sp.ring = a.split_ring;
     int *flags = reinterpret_cast<int *>(a.split_ring + (size_t)units * kRingSlots * kSlotBytes);
     sp.ready = flags;
-    sp.freed = flags + units * kRingSlots;
-    sp.abort = flags + 2 * units * kRingSlots;
+    sp.freed = flags + kFlagSlotStride / 2;
+    sp.abort = flags + (size_t)units * kRingSlots * kFlagSlotStride;
     sp.chains = units;
     // every CTA resident at once (one per SM): chains and producers wait on one another
     cudaLaunchConfig_t cfg = {};

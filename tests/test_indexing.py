@@ -26,7 +26,9 @@ def packed_run(w, x, s0):
     return out, fin
 
 
-def test_each_sequence_alone_equals_packed_bitwise():
+@pytest.mark.parametrize("split", ["0", "1"])
+def test_each_sequence_alone_equals_packed_bitwise(split, monkeypatch):
+    monkeypatch.setenv("KDA_SPLIT", split)   # the fused kernel, or split mode wherever a call allows it
     w, x, s0 = case()
     out, fin = packed_run(w, x, s0)
     cu = w.cu_seqlens()
@@ -39,7 +41,9 @@ def test_each_sequence_alone_equals_packed_bitwise():
         assert torch().equal(f1[0], fin[n]), f"state {n}"
 
 
-def test_sequence_order_permutation_bitwise():
+@pytest.mark.parametrize("split", ["0", "1"])
+def test_sequence_order_permutation_bitwise(split, monkeypatch):
+    monkeypatch.setenv("KDA_SPLIT", split)
     w, x, s0 = case()
     out, fin = packed_run(w, x, s0)
     cu = w.cu_seqlens()
@@ -129,14 +133,21 @@ def test_side_stream():
     assert t.equal(o1, o2) and t.equal(f1, f2)
 
 
-def test_chained_calls_equal_single_call_bitwise():
+@pytest.mark.parametrize("one_mode,chain_mode", [("", ""), ("1", "0"), ("0", "1")])
+def test_chained_calls_equal_single_call_bitwise(one_mode, chain_mode, monkeypatch):
     """A context split into calls of 8192 rows (a multiple of the 64-row chunk)
-    with the fp32 state carried gives the same bits as one call."""
+    with the fp32 state carried gives the same bits as one call -- also with the
+    one call in split mode and the chained calls on the fused kernel, and the
+    other way round."""
     t = torch()
     w = syn.Workload("chain", [4 * 8192], H=4, dk=128, dv=128, seed=11)
     x = syn.draw(w)
     d = inputs_to_dev(x)
+    if one_mode:
+        monkeypatch.setenv("KDA_SPLIT", one_mode)
     o_one, f_one = run_gpu(d, w.cu_seqlens())
+    if chain_mode:
+        monkeypatch.setenv("KDA_SPLIT", chain_mode)
     cu = t.tensor([0, 8192], dtype=t.int32, device="cuda")
     state = None
     for c in range(4):
