@@ -496,7 +496,9 @@ def config_bytes(w, rows: int, with_initial: bool) -> int:
 def tc_mode(w, rows: int, num_sms: int) -> str:
     """Which form of the tensor-core prefill a call of this workload runs
     (kda.h, "Split"): split for few units (N * H at most half the SMs) and
-    T >= 1024 rows, unless KDA_SPLIT says otherwise; else the fused kernel."""
+    T >= 1024 rows, with two chain CTAs a unit ("split-half") where N * H is
+    at most a fifth of the SMs, or a quarter with sequences of at most 16384
+    rows on average, unless KDA_SPLIT says otherwise; else the fused kernel."""
     if w.qkv_dtype != "bf16" or w.dk != 128 or w.dv != 128:
         return "cuda-core"
     n = 1 if w.calls > 1 else w.N
@@ -504,7 +506,15 @@ def tc_mode(w, rows: int, num_sms: int) -> str:
     ok = 2 * n * w.H <= num_sms and n <= 256 and rows >= 1
     if env.startswith("0") or not ok:
         return "fused"
-    return "split" if env.startswith("1") or rows >= 1024 else "fused"
+    if not (env.startswith("1") or env in ("full", "half") or rows >= 1024):
+        return "fused"
+    u = n * w.H
+    half_ok = 4 * u <= num_sms
+    if env == "full" or not half_ok:
+        return "split"
+    if env == "half" or 5 * u <= num_sms or rows <= 16384 * n:
+        return "split-half"
+    return "split"
 
 
 def measure_configs(torch, np, kda, stream, reps: int = 3, only=None, rows_override: int = 0):
@@ -562,15 +572,20 @@ def measure_configs(torch, np, kda, stream, reps: int = 3, only=None, rows_overr
                        "tokens_per_s": rows / (ms_call / 1e3),
                        "roofline_frac": alg / (ms_call / 1e3) / 1e9 / peak,
                        "units": n * w.H, "kernel": mode}
-        if mode == "split" and only is None:
-            # the same calls on the fused kernel, for comparison (KDA_SPLIT is read on every call)
+        if mode.startswith("split") and only is None:
+            # the same calls on the fused kernel and in the other split form
+            # where the SMs allow both, for comparison (KDA_SPLIT is read on
+            # every call)
             old = os.environ.get("KDA_SPLIT")
-            os.environ["KDA_SPLIT"] = "0"
+            other = [("full_chain_us_per_call", "full")] if mode == "split-half" else (
+                [("half_chain_us_per_call", "half")] if 4 * n * w.H <= sms else [])
             try:
-                res[w.name]["fused_us_per_call"] = timed() * 1e3
+                for key, env in [("fused_us_per_call", "0")] + other:
+                    os.environ["KDA_SPLIT"] = env
+                    res[w.name][key] = timed() * 1e3
             finally:
                 if old is None:
-                    del os.environ["KDA_SPLIT"]
+                    os.environ.pop("KDA_SPLIT", None)
                 else:
                     os.environ["KDA_SPLIT"] = old
         del d, out, fin, s0

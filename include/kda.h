@@ -53,10 +53,15 @@
  *             N <= 256) it runs in split mode instead: one SM per unit keeps
  *             that unit's state chain, and every other SM prepares chunks of
  *             any unit (the part of a chunk's work that does not depend on the
- *             state), handing them over through a ring in device memory.  The
- *             results are the same bytes.  The environment variable KDA_SPLIT,
- *             read on every call, overrides the choice: "0" never splits, "1"
- *             splits every call that allows it (T >= 1 in place of 1024).
+ *             state), handing them over through a ring in device memory.
+ *             Where N * H is at most a quarter of the SMs, two SMs keep each
+ *             unit's chain, 64 of the 128 value channels each (the value
+ *             channels of the state evolve independently).  The results are
+ *             the same bytes in every form.  The environment variable
+ *             KDA_SPLIT, read on every call, overrides the choice: "0" never
+ *             splits, "1" splits every call that allows it (T >= 1 in place
+ *             of 1024), "full" and "half" do so in that form ("half" falls
+ *             back to one chain SM a unit where the SMs do not allow two).
  *             A call that cannot get its ring or its cooperative launch runs
  *             unsplit.
  *  Range      the tensor-core kernel rounds its MMA operands to fp16 (fp32

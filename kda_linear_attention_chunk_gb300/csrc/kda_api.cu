@@ -213,25 +213,36 @@ const char *kda_status_string(int status)
     }
 }
 
-// Split mode (kda.h, kda_chunk_prefill): on for calls of few units, unless
-// the environment variable KDA_SPLIT says otherwise ("0" never, "1" whenever
-// the call allows it).
-bool want_split(const kda::KdaArgs &a, const DevInfo *d)
+// Split mode (kda.h, kda_chunk_prefill): 0 off, 1 one chain CTA per unit,
+// 2 two (half chains).  On for calls of few units and T >= 1024, unless the
+// environment variable KDA_SPLIT says otherwise: "0" never, "1" whenever the
+// call allows it, "full" / "half" whenever it allows it and in that form
+// (half only where possible).  Half chains by default where the producers
+// keep up with them: units at most a fifth of the SMs (measured 18-21 %
+// faster at 8-24 units), or at most a quarter with sequences of 16384 rows or
+// fewer on average (8192 rows at 32 units: 5 % faster; 65536 rows at 32
+// units, where 88 producers set the pace in steady state: 1-5 % slower).
+int want_split(const kda::KdaArgs &a, const DevInfo *d)
 {
     // (the producers pack a chunk index into 23 bits: far beyond any T that fits the device)
-    if (!d->pool || a.T == 0 || a.T >= (1 << 29) || !kda::tc_split_possible(a.N * a.H, a.N, d->num_sms))
-        return false;
+    const int units = a.N * a.H;
+    if (!d->pool || a.T == 0 || a.T >= (1 << 29) || !kda::tc_split_possible(units, a.N, d->num_sms)) return 0;
+    const bool half_ok = kda::tc_split_half_possible(units, a.N, d->num_sms);
     const char *env = getenv("KDA_SPLIT");
-    if (env && env[0] == '0') return false;
-    if (env && env[0] == '1') return true;
-    return a.T >= 1024;
+    if (env && env[0] == '0') return 0;
+    if (env && strcmp(env, "full") == 0) return 1;
+    if (env && strcmp(env, "half") == 0) return half_ok ? 2 : 1;
+    const bool half = half_ok && (5 * units <= d->num_sms || (long long)a.T <= 16384LL * a.N);
+    if (env && env[0] == '1') return half ? 2 : 1;
+    return a.T >= 1024 ? (half ? 2 : 1) : 0;
 }
 
 // the tensor-core kernel, split when that pays: the ring comes from the
 // library's pool on the call's stream and goes back to it after the launch
 cudaError_t launch_tc(kda::KdaArgs &a, const DevInfo *d)
 {
-    if (!want_split(a, d)) return kda::launch_kda_tc_bf16_d128(a);
+    const int mode = want_split(a, d);
+    if (!mode) return kda::launch_kda_tc_bf16_d128(a);
     const int units = a.N * a.H;
     const size_t bytes = kda::tc_split_bytes(units), flag_bytes = kda::tc_split_flag_bytes(units);
     void *ring = nullptr;
@@ -242,8 +253,10 @@ cudaError_t launch_tc(kda::KdaArgs &a, const DevInfo *d)
     cudaError_t e = cudaMemsetAsync((uint8_t *)ring + bytes - flag_bytes, 0, flag_bytes, a.stream);
     if (e == cudaSuccess) {
         a.split_ring = (uint8_t *)ring;
+        a.split_half = mode == 2;
         e = kda::launch_kda_tc_bf16_d128(a);
         a.split_ring = nullptr;
+        a.split_half = false;
         if (e == cudaErrorCooperativeLaunchTooLarge) {   // the device cannot hold every CTA at once now
             cudaGetLastError();
             e = kda::launch_kda_tc_bf16_d128(a);

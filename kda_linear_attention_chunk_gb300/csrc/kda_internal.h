@@ -38,6 +38,7 @@ struct KdaArgs {
     // flags, tc_split_bytes(N * H) bytes of device memory, the flags (the
     // tail tc_split_flag_bytes(N * H) bytes) zeroed on the stream before the launch
     uint8_t *split_ring = nullptr;
+    bool split_half = false;   // split mode with two chain CTAs per unit (tc_split_half_possible)
 };
 
 // CUDA-core kernel, any dk, dv in {64, 128}, bf16 (f32 = false) or fp32
@@ -49,6 +50,7 @@ int tc_max_sorted_seqs();   // largest N the tensor-core kernel sorts by itself
 // split mode: whether a call of `units` (sequence, head) pairs and N sequences
 // can run split on a device of num_sms SMs, and the device memory it needs
 bool tc_split_possible(int units, int N, int num_sms);
+bool tc_split_half_possible(int units, int N, int num_sms);
 size_t tc_split_bytes(int units);
 size_t tc_split_flag_bytes(int units);
 

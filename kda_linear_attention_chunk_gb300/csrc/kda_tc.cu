@@ -142,7 +142,8 @@ constexpr uint32_t kSmemBytes = kOffOT + 8192 + 1024;   // + alignment slack
 // rescale, MMA1, Delta, MMA3, outputs) depends on the previous chunk; the
 // decay scan, the operands, A, the inverse, W' and beta*V do not.  In split
 // mode CTA b < chains runs the chain of unit b alone -- 16 compute warps, a
-// loader warp and an MMA-issuer warp (576 threads for every CTA) -- and
+// loader warp and an MMA-issuer warp (576 threads for every CTA); with half
+// chains, CTAs 2u and 2u + 1 each keep 64 of unit u's value channels -- and
 // every other CTA prepares chunks -- any unit's, in the order (chunk index,
 // unit) -- with the prep roles unchanged and ships each finished stage through
 // a ring in global memory (kRingSlots slots per unit, in L2 in practice):
@@ -221,8 +222,9 @@ struct SplitParams {
     uint8_t *ring;         // [units][kRingSlots][kSlotBytes]
     int *ready;            // per slot (stride kFlagSlotStride): 2 (j + 1) + layout bit once chunk j is in the slot
     int *freed;            // per slot (stride kFlagSlotStride): j + 1 once the chain is done with chunk j
+                           // (half chains: +1 from each of the two for every chunk of the slot)
     int *abort;            // set by a CTA whose wait on another CTA ran out
-    int chains;            // CTAs 0 .. chains-1 run the chains, one unit each (units in sorted order)
+    int chains;            // CTAs 0 .. chains-1 run the chains, one unit (or half unit) each, in sorted order
 };
 
 struct Smem {
@@ -1746,9 +1748,11 @@ __device__ __forceinline__ void split_abort(const TcParams &p, const SplitParams
 // A producer's warps 0-3 (the chain's place in the fused kernel): once a stage
 // is finished -- -W' and Qp in its k/q rows, beta*V, Km and tril(A_qk)^T, T in
 // its T16 buffer, the decay constants written -- and the ring slot of its
-// chunk is free, copy it there, hand the stage back to the prep roles, request
-// the k, q and v of the chunk two ahead, and publish the slot.
-template <bool kSlots>
+// chunk is free, copy it there in three groups, in the order the chunk two
+// ahead needs the regions back (v, which group E reads first; k and q; the
+// rest), request that chunk's v and its k and q as soon as their regions have
+// been read, hand the stage back to the prep roles, and publish the slot.
+template <bool kSlots, bool kHalf>
 __device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &sm, const int *order,
                           const Maps &maps)
 {
@@ -1775,9 +1779,11 @@ __device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &
         bool ok = mbar_wait(sm.bar(kBarFmReady + s), ph, sm.abort_flag()) &&
                   mbar_wait(sm.bar(kBarWReady + s), ph, sm.abort_flag());
         if (v == 0) KDA_PHASE(1, item, 1);
-        // the chain has read the chunk kRingSlots back from this slot
+        // the chain has read the chunk kRingSlots back from this slot (half
+        // chains: both have counted every chunk of the slot up to that one)
         if (ok && v == 0 && j >= kRingSlots)
-            ok = flag_wait(sp.freed + slot * kFlagSlotStride, j - kRingSlots + 1, sp, sm.abort_flag());
+            ok = flag_wait(sp.freed + slot * kFlagSlotStride, kHalf ? 2 * (j / kRingSlots) : j - kRingSlots + 1, sp,
+                           sm.abort_flag());
         if (role_any(!ok, kBarChain, kChainThreads)) {
             failed = true;
             break;
@@ -1789,26 +1795,34 @@ __device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &
         hdr[128 + v] = sm.ptr<float>(kOffPend)[(item % 3) * 128 + v];    // pend: middle row -> last row
         if (v == 0) {
             const uint32_t st = sm.u32(s * kStageBytes);
-            for (uint32_t off = 0; off < kStageBytes; off += 16384)
-                bulk_store(dst + off, st + off, kStageBytes - off < 16384u ? kStageBytes - off : 16384u);
+            bulk_store(dst + kOffV, st + kOffV, kVBytes);                    // group 1: beta*V
+            bulk_commit();
+            bulk_store(dst + kOffKQ, st + kOffKQ, 16384);                    // group 2: -W' and Qp
+            bulk_store(dst + kOffKQ + 16384, st + kOffKQ + 16384, 16384);
+            bulk_commit();
+            bulk_store(dst + kOffMma3, st + kOffMma3, 16384);                // group 3: Km, tril(A_qk)^T, T16
+            bulk_store(dst + kOffMma3 + 16384, st + kOffMma3 + 16384, kStageBytes - kOffMma3 - 16384);
             bulk_store(dst + kSlotT16, sm.u32(t16_off<true>(s)), 8192);
             bulk_commit();
+            const bool more = cursor_next<kSlots, kSortChunks>(cur, p, sm, order, 0);
+            bulk_wait_read2();
+            if (more) issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
+            bulk_wait_read1();
+            if (more)
+                issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h, layout_bit<kSortChunks>(order, cur.un, 0));
             bulk_wait_read0();
             KDA_PHASE(1, item, 3);
-            // the stage is the prep's again: Km and tril(A_qk)^T, TMEM P_s, and the
-            // k/q and v tiles of the chunk two ahead
+            // the stage is the prep's again: Km and tril(A_qk)^T, TMEM P_s
             mbar_arrive(sm.bar(kBarKmFree + s));
             mbar_arrive(sm.bar(kBarODone + s));
-            if (cursor_next<kSlots, kSortChunks>(cur, p, sm, order, 0)) {
-                issue_kq(sm, maps, cur.item - 1, cur.row0, cur.un.h, layout_bit<kSortChunks>(order, cur.un, 0));
-                issue_v(sm, maps, cur.item - 1, cur.row0, cur.un.h);
-            }
             bulk_wait0();
             KDA_PHASE(1, item, 4);
         }
-        __threadfence();
+        // every thread's header stores and thread 0's copies are done; one
+        // release after the block barrier publishes them all
         named_bar(kBarChain, kChainThreads);
         if (v == 0) {
+            __threadfence();
             fence_proxy_async_global();
             st_release_gpu(sp.ready + slot * kFlagSlotStride, 2 * (j + 1) + (j & 1));   // + the stage's layout bit
             KDA_PHASE(1, item, 5);
@@ -1831,13 +1845,17 @@ __device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &
 // Warp w owns TMEM lanes 32 (w % 4) .. +31 (value channels) and the quarter
 // w / 4 of each lane's columns.  States move through the warp's 2 KB slice of
 // the output staging buffers, as in chain_load_state / chain_store_state.
+// kRows: the warp's state rows, 32, or 16 in a half chain (its rows sit in
+// lanes 0-15 of the warp's 32; lanes 16-31 take whatever the staging slice
+// holds there, and nothing reads them).
+template <int kRows>
 __device__ void split_load_state(const float *src, uint8_t *stg, uint32_t tm, int lane, int cg)
 {
     const int rq = lane >> 2, pq = lane & 3;
 #pragma unroll 1
     for (int r = 2 * cg; r < 2 * cg + 2; r++) {
 #pragma unroll
-        for (int i = 0; i < 4; i++)
+        for (int i = 0; i < kRows / 8; i++)
             *reinterpret_cast<float4 *>(stg + stg_off(8 * i + rq, pq)) =
                 src ? *reinterpret_cast<const float4 *>(src + (8 * i + rq) * kD + 16 * r + 4 * pq)
                     : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1855,6 +1873,7 @@ __device__ void split_load_state(const float *src, uint8_t *stg, uint32_t tm, in
     tmem_wait_st();
 }
 
+template <int kRows>
 __device__ void split_store_state(float *dst, const float *pend, uint8_t *stg, uint32_t tm, int lane, int cg)
 {
     const int rq = lane >> 2, pq = lane & 3;
@@ -1872,7 +1891,7 @@ __device__ void split_store_state(float *dst, const float *pend, uint8_t *stg, u
         }
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 4; i++)
+        for (int i = 0; i < kRows / 8; i++)
             *reinterpret_cast<float4 *>(dst + (8 * i + rq) * kD + 16 * r + 4 * pq) =
                 *reinterpret_cast<const float4 *>(stg + stg_off(8 * i + rq, pq));
         __syncwarp();
@@ -1906,13 +1925,50 @@ __device__ __forceinline__ void split_scale_state(uint32_t tmem, uint32_t lane_o
     tmem_st16(tmem + kTmS0h + lane_off + 16 * cg, h);
 }
 
+// The same for a half chain (M = 64: value row i in TMEM lane
+// (i % 16) + 32 (i / 16), so the 16 rows of sub-partition q sit in its lanes
+// 0-15): this warp's 16 rows x 32 columns in the 16x256b fragment layout
+// (thread t: rows t/4 and 8 + t/4, columns 8b + 2 (t%4), +1), and the fp16
+// copy in the 16x128b layout, where thread t writes exactly the packed columns
+// 4b + t%4 of those two rows -- the pairs it holds.
+__device__ __forceinline__ void split_scale_state_half(uint32_t tmem, uint32_t lane_off, int cg, const float *fm,
+                                                       const float *pend, int lane)
+{
+    uint32_t x[16];
+    tmem_ld16x256_x4(tmem + kTmS + lane_off + 32 * cg, x);
+    tmem_wait_ld();
+    const int c0 = 32 * cg + 2 * (lane & 3);
+#pragma unroll
+    for (int b = 0; b < 4; b++) {
+        const float2 f2 = *reinterpret_cast<const float2 *>(fm + c0 + 8 * b);
+        const float2 p2 = pend ? *reinterpret_cast<const float2 *>(pend + c0 + 8 * b) : make_float2(1.f, 1.f);
+        const float fv[2] = {f2.x, f2.y}, pv[2] = {p2.x, p2.y};
+#pragma unroll
+        for (int hr = 0; hr < 2; hr++)
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+                float f = __uint_as_float(x[4 * b + 2 * hr + e]);
+                if (pend) f = __fmul_rn(f, pv[e]);
+                x[4 * b + 2 * hr + e] = __float_as_uint(__fmul_rn(f, fv[e]));
+            }
+    }
+    uint32_t h[8];
+#pragma unroll
+    for (int b = 0; b < 4; b++) {
+        h[2 * b] = pack_f16x2(__uint_as_float(x[4 * b]), __uint_as_float(x[4 * b + 1]));
+        h[2 * b + 1] = pack_f16x2(__uint_as_float(x[4 * b + 2]), __uint_as_float(x[4 * b + 3]));
+    }
+    tmem_st16x256_x4(tmem + kTmS + lane_off + 32 * cg, x);
+    tmem_st16x128_x4(tmem + kTmS0h + lane_off + 16 * cg, h);
+}
+
 // Chain CTA of unit uu, warp 16 (its first lane): the slot copies.  Chunk j
 // goes into buffer j & 1 once the producers have published it (the flag is
 // awaited ahead of time) and the chain's MMAs of chunk j - 2 are done with the
 // buffer -- the part MMA1 reads as soon as MMA1 is done, the rest after MMA3;
 // once chunk j has landed, its ring slot goes back to the producers.  (Done by the chain's own first
 // thread, the flag round trips cost about 3.7k cycles a chunk on its path.)
-template <bool kSlots>
+template <bool kSlots, bool kHalf>
 __device__ void split_loader(const TcParams &p, const SplitParams &sp, const Smem &sm, const int *order, int uu)
 {
     const Unit un = get_unit<kSlots, 1>(p, order, uu);
@@ -1963,7 +2019,10 @@ __device__ void split_loader(const TcParams &p, const SplitParams &sp, const Sme
         if (!ok) break;
         KDA_PHASE(2, j, 2);
         landed = j + 1;
-        st_release_gpu(sp.freed + slot_of(j) * kFlagSlotStride, j + 1);   // the slot may take chunk j + kRingSlots
+        // the slot may take chunk j + kRingSlots (a unit of half chains: once both
+        // have counted it)
+        if constexpr (kHalf) red_release_add_gpu(sp.freed + slot_of(j) * kFlagSlotStride, 1);
+        else st_release_gpu(sp.freed + slot_of(j) * kFlagSlotStride, j + 1);
         if (j + 2 < nch) {
             // chunk j + 2 into buffer b: part A once MMA1 of chunk j is done with it,
             // part B once MMA3 is
@@ -1998,9 +2057,10 @@ constexpr int kBarM3O = kBarPrepDone;                  // MMA3's output half don
 // half.  The halves are the fused kernel's N = 128 MMA1 and N = 192 MMA3
 // split by their B rows (K rows / Q rows; Km / tril(A_qk)^T), so that the
 // compute warps can go on as soon as the half they need is done.
-template <bool kSlots>
-__device__ void split_issuer(const TcParams &p, const Smem &sm, const int *order, int uu)
+template <bool kSlots, bool kHalf>
+__device__ void split_issuer(const TcParams &p, const Smem &sm, const int *order, int uu, int half)
 {
+    constexpr int M = kHalf ? 64 : 128;   // a half chain: value channels 64 half .. +63
     const int lane = threadIdx.x & 31;
     const uint32_t tmem = *sm.tmem_base();
     const Unit un = get_unit<kSlots, 1>(p, order, uu);
@@ -2010,11 +2070,11 @@ __device__ void split_issuer(const TcParams &p, const Smem &sm, const int *order
     auto mma_b = [&](int j) {   // U^T = (beta V)^T T^T into chunk j's Delta columns
         const int b = j & 1, par = sm.split_parity()[b];
         const uint32_t buf = sm.u32(b * kSlotBytes);
-        const uint32_t id = idesc_f16(128, 64, 1, 0);
+        const uint32_t id = idesc_f16(M, 64, 1, 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ks++) {
             const uint64_t bd = smem_desc_sw128(buf + kSlotT16 + ks * 32, 16, 1024);
-            const uint64_t au = smem_desc_sw128(buf + kOffV + ks * 2048, 8192, 1024);
+            const uint64_t au = smem_desc_sw128(buf + kOffV + 8192 * half + ks * 2048, 8192, 1024);
             mma_ss(tmem + tm_d(par), au, bd, id, ks > 0);
         }
     };
@@ -2031,7 +2091,7 @@ __device__ void split_issuer(const TcParams &p, const Smem &sm, const int *order
             const int par = sm.split_parity()[b];
             const uint32_t buf = sm.u32(b * kSlotBytes);
             tc_fence_after();
-            const uint32_t id = idesc_f16(128, 64, 0, 0);
+            const uint32_t id = idesc_f16(M, 64, 0, 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ks++) {   // U^T - S'^T W'^T: the K rows hold -W'
                 const int kb = ks >> 2, kin = ks & 3;
@@ -2058,14 +2118,14 @@ __device__ void split_issuer(const TcParams &p, const Smem &sm, const int *order
 #pragma unroll
             for (int ks = 0; ks < 4; ks++)     // S^T += Delta^T Km
                 mma_ts(tmem + kTmS, tmem + kTmDh + 8 * ks,
-                       smem_desc_sw128(buf + off_km(par) + ks * 2048, 8192, 1024), idesc_f16(128, 128, 0, 1), 1);
+                       smem_desc_sw128(buf + off_km(par) + ks * 2048, 8192, 1024), idesc_f16(M, 128, 0, 1), 1);
             }
             mma_commit(sm.bar(kBarM3S));   // (also when nothing was issued: the compute warps' wait ends)
             if (ok) {
 #pragma unroll
             for (int ks = 0; ks < 4; ks++)     // O^T += Delta^T tril(A_qk)^T
                 mma_ts(tmem + tm_o(par), tmem + kTmDh + 8 * ks,
-                       smem_desc_sw128(buf + off_bq(par) + ks * 2048, 8192, 1024), idesc_f16(128, 64, 0, 1), 1);
+                       smem_desc_sw128(buf + off_bq(par) + ks * 2048, 8192, 1024), idesc_f16(M, 64, 0, 1), 1);
             }
             mma_commit(sm.bar(kBarM3O));
             mma_commit(sm.bar(kBarKmFree + b));   // every MMA reading buffer b is done: it may take chunk j + 2
@@ -2090,53 +2150,62 @@ __device__ void split_issuer(const TcParams &p, const Smem &sm, const int *order
 //   Delta^T -> fp16 once MMA1's Delta half is done;
 //   [block barrier: the issuer starts MMA3, state half first]
 //   the next chunk starts once MMA3's state half is done.
-// The arithmetic, operand for operand, is the fused kernel's.
-template <bool kSlots>
+// The arithmetic, operand for operand, is the fused kernel's.  A half chain
+// (kHalf) keeps value channels 64 half .. +63 of the unit, with M = 64 MMAs:
+// row i of its accumulators in TMEM lane (i % 16) + 32 (i / 16), so warp w
+// holds rows 16 (w % 4) .. +15 in lanes 0-15 of its sub-partition, and moves
+// half the TMEM bytes a chunk of a whole chain.
+template <bool kSlots, bool kHalf>
 __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem &sm, const int *order,
-                            const Maps &maps, int uu)
+                            const Maps &maps, int uu, int half)
 {
+    constexpr int kRows = kHalf ? 16 : 32;                // state rows of a warp
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int q = w & 3, cg = w >> 2;
     const uint32_t tmem = *sm.tmem_base();
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const Unit un = get_unit<kSlots, 1>(p, order, uu);
     const size_t ubase = ((size_t)un.st * p.H + un.h) * kD * kD;   // used only when st >= 0
-    if (un.nchunks == 0) {   // empty (or padded) sequence: its state passes through
+    const size_t hbase = ubase + (size_t)(kHalf ? 64 * half : 0) * kD;   // this chain's first state row
+    if (un.nchunks == 0) {   // empty (or padded) sequence: its state (rows) pass through
         if (p.s1 && (!kSlots || un.st >= 0))
-            for (int i = tid; i < kD * kD / 4; i += kThreads)
-                reinterpret_cast<float4 *>(p.s1 + ubase)[i] =
-                    p.s0 ? reinterpret_cast<const float4 *>(p.s0 + ubase)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = tid; i < 4 * kRows * kD / 4; i += kThreads)
+                reinterpret_cast<float4 *>(p.s1 + hbase)[i] =
+                    p.s0 ? reinterpret_cast<const float4 *>(p.s0 + hbase)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
     const int nch = un.nchunks;
-    float *pendr = sm.ptr<float>(kCPend);                 // [2][128]: pend of the last two chunks
-    uint8_t *stg = sm.base + kCOut + 2048 * w;            // this warp's state staging slice
-    const size_t wrows = ubase + (size_t)(32 * q) * kD;   // this warp's first state row
+    float *pendr = sm.ptr<float>(kCPend);                     // [2][128]: pend of the last two chunks
+    uint8_t *stg = sm.base + kCOut + 2048 * w;                // this warp's state staging slice
+    const size_t wrows = hbase + (size_t)(kRows * q) * kD;   // this warp's first state row
     bool ok = true;
-    split_load_state(p.s0 ? p.s0 + wrows : nullptr, stg, tmem + kTmS + lane_off, lane, cg);
+    split_load_state<kRows>(p.s0 ? p.s0 + wrows : nullptr, stg, tmem + kTmS + lane_off, lane, cg);
     // O^T of chunk jo (layout paro) -> bf16 tiles of 32 rows in staging buffer
-    // jo & 1 (this warp: rows 16 cg .. +15, its 32 value channels), stored by
-    // bulk tensor copies; partial tiles row by row.  Thread 0 has made sure
-    // before (bulk_wait_read1 ahead of a block barrier) that the copies of
-    // chunk jo - 2 have read the buffer.  false: a thread's wait ran out.
+    // jo & 1 (this warp: rows 16 cg .. +15, its 32 value channels; 16 in a
+    // half chain, whose tiles hold its 64 channels only), stored by bulk
+    // tensor copies; partial tiles row by row.  Thread 0 has made sure before
+    // (bulk_wait_read1 ahead of a block barrier) that the copies of chunk
+    // jo - 2 have read the buffer.  false: a thread's wait ran out.
+    constexpr int kTileBytes = kHalf ? 4096 : 8192;   // one tile: 32 rows x the chain's channels
     auto outputs = [&](int jo, int paro) -> bool {
         ok = mbar_wait(sm.bar(kBarM3O), jo & 1, sm.abort_flag()) && ok;   // MMA3's output half of chunk jo
         tc_fence_after();
         const int row0 = un.bos + jo * kChunk, L = min(kChunk, un.eos - row0);
         const uint32_t ost = sm.u32(kCOut + (jo & 1) * 16384);
-        uint32_t o[2][8];
+        constexpr int kHl = kHalf ? 1 : 2;   // 16-lane halves of the warp's lanes that hold rows
+        uint32_t o[kHl][8];
         const uint32_t src = tmem + tm_o(paro) + lane_off;
 #pragma unroll
-        for (int hl = 0; hl < 2; hl++) tmem_ld16x256_x2(src + ((uint32_t)(16 * hl) << 16) + 16 * cg, o[hl]);
+        for (int hl = 0; hl < kHl; hl++) tmem_ld16x256_x2(src + ((uint32_t)(16 * hl) << 16) + 16 * cg, o[hl]);
         tmem_wait_ld();
         tc_fence_before();
         const int mi = lane >> 3, k8 = lane & 7;
         const int rl = 16 * (cg & 1) + ((mi & 2) ? 8 : 0) + k8;
 #pragma unroll
-        for (int hl = 0; hl < 2; hl++) {
+        for (int hl = 0; hl < kHl; hl++) {
             const uint32_t *f = o[hl];
-            const int vc = 32 * q + 16 * hl + ((mi & 1) ? 8 : 0);
-            stmatrix_x4_trans(ost + (cg >> 1) * 8192 + (vc >> 6) * 4096 + sw128_chunk(rl, (vc & 63) >> 3),
+            const int vc = kRows * q + 16 * hl + ((mi & 1) ? 8 : 0);   // the chain's channel
+            stmatrix_x4_trans(ost + (cg >> 1) * kTileBytes + (vc >> 6) * 4096 + sw128_chunk(rl, (vc & 63) >> 3),
                               pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1])),
                               pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3])),
                               pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5])),
@@ -2144,19 +2213,21 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
         }
         fence_proxy_async_smem();
         if (role_any(!ok, kBarChain, kThreads)) return false;
+        const int blk = kHalf ? half : 0;   // the chain's first 64-channel block
         if (tid == 0) {
-            if (L >= 32) tma_store_4d(maps.o, 0, row0, 0, un.h, ost);
-            if (L == kChunk) tma_store_4d(maps.o, 0, row0 + 32, 0, un.h, ost + 8192);
+            if (L >= 32) tma_store_4d(maps.o, 0, row0, blk, un.h, ost);
+            if (L == kChunk) tma_store_4d(maps.o, 0, row0 + 32, blk, un.h, ost + kTileBytes);
             bulk_commit();
             KDA_PHASE(1, jo, 10);
         }
         if (L < kChunk) {
-            const int half = L < 32 ? 0 : 1, nr = L - 32 * half;
-            const uint8_t *tb = sm.base + kCOut + (jo & 1) * 16384 + half * 8192;
+            constexpr int kPieces = kTileBytes / 512;   // 16-byte pieces of a row
+            const int tile = L < 32 ? 0 : 1, nr = L - 32 * tile;
+            const uint8_t *tb = sm.base + kCOut + (jo & 1) * 16384 + tile * kTileBytes;
             const size_t row_stride = (size_t)p.H * kD;
-            __nv_bfloat16 *dst = p.out + ((size_t)(row0 + 32 * half) * p.H + un.h) * kD;
-            for (int idx = tid; idx < nr * 16; idx += kThreads) {
-                const int r = idx >> 4, pc = idx & 15;
+            __nv_bfloat16 *dst = p.out + ((size_t)(row0 + 32 * tile) * p.H + un.h) * kD + 64 * blk;
+            for (int idx = tid; idx < nr * kPieces; idx += kThreads) {
+                const int r = idx / kPieces, pc = idx % kPieces;
                 *reinterpret_cast<uint4 *>(dst + (size_t)r * row_stride + 8 * pc) =
                     *reinterpret_cast<const uint4 *>(tb + (pc >> 3) * 4096 + sw128_chunk(r, pc & 7));
             }
@@ -2173,7 +2244,10 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
         if (tid == 0) KDA_PHASE(1, j, 1);
         const int par = sm.split_parity()[b];
         const float *hdr = sm.ptr<float>(b * kSlotBytes + kSlotHdr);
-        split_scale_state(tmem, lane_off, cg, hdr, j > 0 ? pendr + ((j - 1) & 1) * 128 : nullptr);
+        if constexpr (kHalf)
+            split_scale_state_half(tmem, lane_off, cg, hdr, j > 0 ? pendr + ((j - 1) & 1) * 128 : nullptr, lane);
+        else
+            split_scale_state(tmem, lane_off, cg, hdr, j > 0 ? pendr + ((j - 1) & 1) * 128 : nullptr);
         if (tid == 0) KDA_PHASE(1, j, 11);
         if (tid < 128) pendr[(j & 1) * 128 + tid] = hdr[128 + tid];
         tmem_wait_st();
@@ -2192,7 +2266,17 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
         ok = mbar_wait(sm.bar(kBarM1D), j & 1, sm.abort_flag(), KDA_WAIT_LIMIT_MMA1) && ok;
         tc_fence_after();
         if (tid == 0) KDA_PHASE(1, j, 5);
-        {   // Delta^T (fp32) -> fp16 A operand, this warp's 16 columns
+        if constexpr (kHalf) {   // the same on the warp's 16 lanes (layouts as in the rescale)
+            uint32_t x[8], h[4];
+            tmem_ld16x256_x2(tmem + tm_d(par) + lane_off + 16 * cg, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int b = 0; b < 2; b++) {
+                h[2 * b] = pack_f16x2(__uint_as_float(x[4 * b]), __uint_as_float(x[4 * b + 1]));
+                h[2 * b + 1] = pack_f16x2(__uint_as_float(x[4 * b + 2]), __uint_as_float(x[4 * b + 3]));
+            }
+            tmem_st16x128_x2(tmem + kTmDh + lane_off + 8 * cg, h);
+        } else {   // Delta^T (fp32) -> fp16 A operand, this warp's 16 columns
             uint32_t x[16], h[8];
             tmem_ld16(tmem + tm_d(par) + lane_off + 16 * cg, x);
             tmem_wait_ld();
@@ -2224,18 +2308,18 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
     named_bar(kBarChain, kThreads);
     // the final state = S * pend of the last chunk, through the staging slices
     if (done && p.s1)
-        split_store_state(p.s1 + wrows, pendr + ((nch - 1) & 1) * 128, stg, tmem + kTmS + lane_off, lane, cg);
+        split_store_state<kRows>(p.s1 + wrows, pendr + ((nch - 1) & 1) * 128, stg, tmem + kTmS + lane_off, lane, cg);
     if (tid == 0) bulk_wait0();
 }
 
 // =============================================================================
 // The split-mode kernel: a cooperative launch of one CTA per SM (every CTA
 // resident at once, so that the chains and the producers can wait on one
-// another); CTA b < sp.chains runs the chain of unit b (sorted order), the
-// others prepare chunks.
+// another); CTA b < sp.chains runs the chain of unit b (sorted order) -- with
+// half chains, half b & 1 of unit b / 2 -- and the others prepare chunks.
 constexpr int kSplitThreads = kThreads + 64;   // + the chain CTAs' loader warp and MMA issuer warp
 
-template <bool kSlots>
+template <bool kSlots, bool kHalf>
 __global__ void __launch_bounds__(kSplitThreads, 1)
 kda_tc_split_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -2317,14 +2401,15 @@ kda_tc_split_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     tc_fence_after();
 
     const Maps maps = {&tq, &tk, &tv, &tg, &to};
+    const int cu_ = kHalf ? (int)blockIdx.x >> 1 : (int)blockIdx.x, half = kHalf ? (int)blockIdx.x & 1 : 0;
     if (warp == 16) {
-        if (chain && tid == kThreads) split_loader<kSlots>(p, sp, sm, order, (int)blockIdx.x);
+        if (chain && tid == kThreads) split_loader<kSlots, kHalf>(p, sp, sm, order, cu_);
     } else if (warp == 17) {
-        if (chain) split_issuer<kSlots>(p, sm, order, (int)blockIdx.x);
+        if (chain) split_issuer<kSlots, kHalf>(p, sm, order, cu_, half);
     } else if (chain) {
-        split_chain<kSlots>(p, sp, sm, order, maps, (int)blockIdx.x);
+        split_chain<kSlots, kHalf>(p, sp, sm, order, maps, cu_, half);
     } else if (warp < 4) {
-        ship_role<kSlots>(p, sp, sm, order, maps);
+        ship_role<kSlots, kHalf>(p, sp, sm, order, maps);
     } else if (warp < 12) {
         const ConvParams no_conv = {};
         e_role<kSlots, kSortChunks, false>(p, no_conv, sm, order, 0, maps);
@@ -2501,17 +2586,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // [T][H][128] viewed as 4-D {c (box_inner wide), row, channel block, head}:
-// one box {box_inner, box_rows, 128/box_inner blocks, 1} is [block][row][c] in
-// shared memory -- the 128B-swizzled tiles, blocks apart.
+// one box {box_inner, box_rows, box_blocks (default all 128/box_inner), 1} is
+// [block][row][c] in shared memory -- the 128B-swizzled tiles, blocks apart.
 bool make_map4(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem, int T, int H, int box_inner,
-               int box_rows = kChunk)
+               int box_rows = kChunk, int box_blocks = 0)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     const int nblk = kD / box_inner;
     cuuint64_t dims[4] = {(cuuint64_t)box_inner, (cuuint64_t)T, (cuuint64_t)nblk, (cuuint64_t)H};
     cuuint64_t strides[3] = {(cuuint64_t)H * kD * elem, (cuuint64_t)box_inner * elem, (cuuint64_t)kD * elem};
-    cuuint32_t box[4] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, (cuuint32_t)nblk, 1};
+    cuuint32_t box[4] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, (cuuint32_t)(box_blocks ? box_blocks : nblk), 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -2544,6 +2629,11 @@ bool tc_split_possible(int units, int N, int num_sms)
 {
     return units >= 1 && 2 * units <= num_sms && units <= 255 && N <= kMaxSortedSeqs;
 }
+// half chains: two chain CTAs per unit, at least as many producers again
+bool tc_split_half_possible(int units, int N, int num_sms)
+{
+    return tc_split_possible(units, N, num_sms) && 4 * units <= num_sms;
+}
 size_t tc_split_flag_bytes(int units) { return ((size_t)units * kRingSlots * kFlagSlotStride + 32) * sizeof(int); }
 size_t tc_split_bytes(int units) { return (size_t)units * kRingSlots * kSlotBytes + tc_split_flag_bytes(units); }
 
@@ -2552,10 +2642,11 @@ cudaError_t launch_kda_tc_split(const KdaArgs &a, const CUtensorMap &tq, const C
 {
     using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                             const CUtensorMap, TcParams, const SplitParams);
-    static const Kernel kernels[2] = {kda_tc_split_kernel<false>, kda_tc_split_kernel<true>};
-    const int variant = a.state_slots != nullptr;
+    static const Kernel kernels[4] = {kda_tc_split_kernel<false, false>, kda_tc_split_kernel<true, false>,
+                                      kda_tc_split_kernel<false, true>, kda_tc_split_kernel<true, true>};
+    const int variant = (a.state_slots != nullptr) + 2 * a.split_half;
     const Kernel kernel = kernels[variant];
-    static std::atomic<int> attr_set[2][64];
+    static std::atomic<int> attr_set[4][64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[variant][dev].load(std::memory_order_acquire)) {
@@ -2586,7 +2677,7 @@ cudaError_t launch_kda_tc_split(const KdaArgs &a, const CUtensorMap &tq, const C
     sp.ready = flags;
     sp.freed = flags + kFlagSlotStride / 2;
     sp.abort = flags + (size_t)units * kRingSlots * kFlagSlotStride;
-    sp.chains = units;
+    sp.chains = a.split_half ? 2 * units : units;
     // every CTA resident at once (one per SM): chains and producers wait on one another
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.num_sms);
@@ -2615,7 +2706,11 @@ cudaError_t launch_kda_tc_bf16_d128(const KdaArgs &a)
             return cudaErrorInvalidValue;
     }
     if (a.split_ring) {
-        if (a.conv_w || a.g_order || !a.sched || a.T == 0 || !tc_split_possible(a.N * a.H, a.N, a.num_sms))
+        if (a.conv_w || a.g_order || !a.sched || a.T == 0 || !tc_split_possible(a.N * a.H, a.N, a.num_sms) ||
+            (a.split_half && !tc_split_half_possible(a.N * a.H, a.N, a.num_sms)))
+            return cudaErrorInvalidValue;
+        // a half chain stores the 32-row output tiles of its 64 channels
+        if (a.split_half && !make_map4(&to, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.T, a.H, 64, 32, 1))
             return cudaErrorInvalidValue;
         return launch_kda_tc_split(a, tq, tk, tv, tg, to);
     }

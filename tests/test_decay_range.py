@@ -42,7 +42,7 @@ def gpu_call(x, cu, s0, full_range):
     return out_to_f64(out), fin.cpu().numpy().astype(np.float64), kda.device_error(reset=True)
 
 
-@pytest.mark.parametrize("split", ["0", "1"])
+@pytest.mark.parametrize("split", ["0", "full", "half"])
 @pytest.mark.parametrize("profile", syn.DECAY_PROFILES)
 def test_tensor_core_range_bit_and_parity(profile, split, monkeypatch):
     # the fused kernel, and split mode (whose producers run the same decay scan)

@@ -26,9 +26,10 @@ def packed_run(w, x, s0):
     return out, fin
 
 
-@pytest.mark.parametrize("split", ["0", "1"])
+@pytest.mark.parametrize("split", ["0", "full", "half"])
 def test_each_sequence_alone_equals_packed_bitwise(split, monkeypatch):
-    monkeypatch.setenv("KDA_SPLIT", split)   # the fused kernel, or split mode wherever a call allows it
+    # the fused kernel, or split mode (one or two chain CTAs a unit) wherever a call allows it
+    monkeypatch.setenv("KDA_SPLIT", split)
     w, x, s0 = case()
     out, fin = packed_run(w, x, s0)
     cu = w.cu_seqlens()
@@ -41,7 +42,7 @@ def test_each_sequence_alone_equals_packed_bitwise(split, monkeypatch):
         assert torch().equal(f1[0], fin[n]), f"state {n}"
 
 
-@pytest.mark.parametrize("split", ["0", "1"])
+@pytest.mark.parametrize("split", ["0", "full", "half"])
 def test_sequence_order_permutation_bitwise(split, monkeypatch):
     monkeypatch.setenv("KDA_SPLIT", split)
     w, x, s0 = case()
@@ -133,12 +134,12 @@ def test_side_stream():
     assert t.equal(o1, o2) and t.equal(f1, f2)
 
 
-@pytest.mark.parametrize("one_mode,chain_mode", [("", ""), ("1", "0"), ("0", "1")])
+@pytest.mark.parametrize("one_mode,chain_mode", [("", ""), ("full", "0"), ("0", "half"), ("half", "full")])
 def test_chained_calls_equal_single_call_bitwise(one_mode, chain_mode, monkeypatch):
     """A context split into calls of 8192 rows (a multiple of the 64-row chunk)
     with the fp32 state carried gives the same bits as one call -- also with the
-    one call in split mode and the chained calls on the fused kernel, and the
-    other way round."""
+    one call in split mode and the chained calls on the fused kernel, the other
+    way round, and with half chains against whole ones."""
     t = torch()
     w = syn.Workload("chain", [4 * 8192], H=4, dk=128, dv=128, seed=11)
     x = syn.draw(w)

@@ -4,8 +4,10 @@ an SM of its own, the two handing chunks over through a ring in device memory.
 
 The chain computes exactly the fused kernel's operations on exactly its
 operands (the producers run the fused kernel's prep code), so the split and
-the fused kernel must give the same bytes.  KDA_SPLIT=0 / 1 (read on every
-call) forces either mode.  Parity against the oracle is covered here on a
+the fused kernel must give the same bytes -- with one chain CTA a unit, or
+two that keep half of the value channels each.  KDA_SPLIT=0 / full / half
+(read on every call) forces a mode; half falls back to full where the SMs do
+not allow two chains a unit.  Parity against the oracle is covered here on a
 ragged batch with a long sequence, and by test_parity's varlen4_4096,
 long_65536 and context_262144 workloads (64 and 32 units: split by default).
 """
@@ -50,15 +52,16 @@ def dense_call(w, x, s0):
 
 
 @pytest.mark.parametrize("lens,H", [([700], 2), ([300, 1, 0, 64, 65, 129, 5], 3), ([64 * 20 + 3, 17], 8),
-                                    ([2519, 1000, 513, 64], 16)])
+                                    ([2519, 1000, 513, 64], 16), ([64 * 40 + 31, 0, 1], 12)])
 def test_split_equals_fused_bit_for_bit(lens, H):
     w = syn.Workload("split", lens, H=H, dk=128, dv=128, init_state=True, seed=51)
     x = syn.draw(w)
     go = dense_call(w, x, syn.draw_initial_state(w))
     o_f, s_f = run_mode("0", go)
-    o_s, s_s = run_mode("1", go)
-    np.testing.assert_array_equal(o_s, o_f)
-    np.testing.assert_array_equal(s_s, s_f)
+    for mode in ("full", "half"):
+        o_s, s_s = run_mode(mode, go)
+        np.testing.assert_array_equal(o_s, o_f, err_msg=mode)
+        np.testing.assert_array_equal(s_s, s_f, err_msg=mode)
 
 
 def test_split_slots_equals_fused_bit_for_bit():
@@ -82,14 +85,16 @@ def test_split_slots_equals_fused_bit_for_bit():
         assert kda.device_error(reset=True) == 0
         return out.view(t.int16).cpu().numpy(), pool.cpu().numpy()
     o_f, p_f = run_mode("0", go)
-    o_s, p_s = run_mode("1", go)
-    np.testing.assert_array_equal(o_s, o_f)
-    np.testing.assert_array_equal(p_s, p_f)
-    untouched = [0, 1, 3, 4, 6, 8]
-    np.testing.assert_array_equal(p_s[untouched], pool0[untouched])
+    for mode in ("full", "half"):
+        o_s, p_s = run_mode(mode, go)
+        np.testing.assert_array_equal(o_s, o_f, err_msg=mode)
+        np.testing.assert_array_equal(p_s, p_f, err_msg=mode)
+        untouched = [0, 1, 3, 4, 6, 8]
+        np.testing.assert_array_equal(p_s[untouched], pool0[untouched])
 
 
-def test_split_parity_ragged_long():
+@pytest.mark.parametrize("mode", ["full", "half"])
+def test_split_parity_ragged_long(mode):
     """Against the oracle, element by element: a long sequence with short ones."""
     w = syn.Workload("split_parity", [64 * 24 + 37, 5, 130, 64], H=4, dk=128, dv=128, init_state=True, seed=53)
     x = syn.draw(w)
@@ -100,21 +105,22 @@ def test_split_parity_ragged_long():
         o, f = run_gpu(d, w.cu_seqlens(), s0=to_dev(s0))
         torch().cuda.synchronize()
         return out_to_f64(o), f.cpu().numpy().astype(np.float64)
-    o, f = run_mode("1", go)
+    o, f = run_mode(mode, go)
     o_ref, f_ref = oracle_run(x, w.cu_seqlens(), s0)
     assert rel_l2(o, o_ref) <= OUT_TOL and rel_l2(f, f_ref) <= STATE_TOL
     check_elementwise(o, o_ref, "tc_out")
     check_elementwise(f, f_ref, "tc_state")
 
 
-def test_split_repeated_calls_identical():
+@pytest.mark.parametrize("mode", ["full", "half"])
+def test_split_repeated_calls_identical(mode):
     """The ring and its flags are fresh each call: back-to-back calls on one
     stream give the same bytes."""
     w = syn.Workload("split_repeat", [2000, 300], H=6, dk=128, dv=128, init_state=True, seed=54)
     x = syn.draw(w)
     go = dense_call(w, x, syn.draw_initial_state(w))
-    first = run_mode("1", go)
+    first = run_mode(mode, go)
     for _ in range(3):
-        again = run_mode("1", go)
+        again = run_mode(mode, go)
         np.testing.assert_array_equal(again[0], first[0])
         np.testing.assert_array_equal(again[1], first[1])

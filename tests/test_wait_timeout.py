@@ -23,11 +23,12 @@ from kda_linear_attention_chunk_gb300 import synthetic as syn
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("split", ["0", "1"])
+@pytest.mark.parametrize("split", ["0", "full", "half"])
 def test_wait_timeout_sets_bit_and_leaves_the_gpu_usable(split, monkeypatch):
     from gpu_util import (OUT_TOL, STATE_TOL, check_elementwise, inputs_to_dev, oracle_run, out_to_f64, rel_l2,
                           run_gpu, to_dev, torch)
-    monkeypatch.setenv("KDA_SPLIT", split)   # the fused kernel, or split mode (its chain's MMA1 wait)
+    # the fused kernel, or split mode with one or two chain CTAs a unit (their MMA1 wait)
+    monkeypatch.setenv("KDA_SPLIT", split)
     t = torch()
     lib = kda.load(kbuild.build_variant("wait0", ["KDA_WAIT_LIMIT_MMA1=0"]))
     w = syn.Workload("timeout", [300, 64, 1, 129], H=4, dk=128, dv=128, init_state=True, seed=41)
