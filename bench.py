@@ -497,8 +497,8 @@ def tc_mode(w, rows: int, num_sms: int) -> str:
     """Which form of the tensor-core prefill a call of this workload runs
     (kda.h, "Split"): split for few units (N * H at most half the SMs) and
     T >= 1024 rows, with two chain CTAs a unit ("split-half") where N * H is
-    at most a fifth of the SMs, or a quarter with sequences of at most 16384
-    rows on average, unless KDA_SPLIT says otherwise; else the fused kernel."""
+    at most a fifth of the SMs, unless KDA_SPLIT says otherwise; else the
+    fused kernel."""
     if w.qkv_dtype != "bf16" or w.dk != 128 or w.dv != 128:
         return "cuda-core"
     n = 1 if w.calls > 1 else w.N
@@ -512,7 +512,7 @@ def tc_mode(w, rows: int, num_sms: int) -> str:
     half_ok = 4 * u <= num_sms
     if env == "full" or not half_ok:
         return "split"
-    if env == "half" or 5 * u <= num_sms or rows <= 16384 * n:
+    if env == "half" or 5 * u <= num_sms:
         return "split-half"
     return "split"
 

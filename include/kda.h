@@ -54,7 +54,7 @@
  *             that unit's state chain, and every other SM prepares chunks of
  *             any unit (the part of a chunk's work that does not depend on the
  *             state), handing them over through a ring in device memory.
- *             Where N * H is at most a quarter of the SMs, two SMs keep each
+ *             Where N * H is at most a fifth of the SMs, two SMs keep each
  *             unit's chain, 64 of the 128 value channels each (the value
  *             channels of the state evolve independently).  The results are
  *             the same bytes in every form.  The environment variable

@@ -219,9 +219,9 @@ const char *kda_status_string(int status)
 // call allows it, "full" / "half" whenever it allows it and in that form
 // (half only where possible).  Half chains by default where the producers
 // keep up with them: units at most a fifth of the SMs (measured 18-21 %
-// faster at 8-24 units), or at most a quarter with sequences of 16384 rows or
-// fewer on average (8192 rows at 32 units: 5 % faster; 65536 rows at 32
-// units, where 88 producers set the pace in steady state: 1-5 % slower).
+// faster at 8-24 units on 152 SMs; at 32 units the 88 producers set the pace
+// and the two forms come within a few per cent of each other, either way
+// from run to run).
 int want_split(const kda::KdaArgs &a, const DevInfo *d)
 {
     // (the producers pack a chunk index into 23 bits: far beyond any T that fits the device)
@@ -232,7 +232,7 @@ int want_split(const kda::KdaArgs &a, const DevInfo *d)
     if (env && env[0] == '0') return 0;
     if (env && strcmp(env, "full") == 0) return 1;
     if (env && strcmp(env, "half") == 0) return half_ok ? 2 : 1;
-    const bool half = half_ok && (5 * units <= d->num_sms || (long long)a.T <= 16384LL * a.N);
+    const bool half = half_ok && 5 * units <= d->num_sms;
     if (env && env[0] == '1') return half ? 2 : 1;
     return a.T >= 1024 ? (half ? 2 : 1) : 0;
 }

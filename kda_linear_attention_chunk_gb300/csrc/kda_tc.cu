@@ -409,6 +409,32 @@ __device__ __forceinline__ int cta_unit_peek(const Smem &sm, int k, int U)
 // byte offset of 16-byte chunk `ch` of row `r` in a 128B-swizzled tile
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
 
+// Two fp32 operations in one instruction on a register pair (mul / sub / add
+// .rn.f32x2, sm_100 and later): each half is the IEEE single-precision
+// operation rounded to nearest even, so the results are the scalar ones, for
+// half the instructions on the issue slots the roles of a CTA share.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n .reg .b64 x, y;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n mul.rn.f32x2 x, x, y;\n mov.b64 {%0, %1}, x;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n .reg .b64 x, y;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n sub.rn.f32x2 x, x, y;\n mov.b64 {%0, %1}, x;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n .reg .b64 x, y;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n add.rn.f32x2 x, x, y;\n mov.b64 {%0, %1}, x;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // 2^x on the special-function unit (approximate, subnormal results flushed to
 // zero).  The decay pass keeps its log-decays in base 2: exp(G) = 2^(G log2 e).
 __device__ __forceinline__ float ex2(float x)
@@ -724,13 +750,11 @@ __device__ bool e_pass(const Smem &sm, int s, int lb, int item, int L, int et, f
         for (int t = 0; t < 16; t++) {
             const int r = 16 * ew + t;
             const float2 g2 = r < L ? *reinterpret_cast<const float2 *>(gb + 512 * r) : make_float2(0.f, 0.f);
-            x[t] = make_float2(g2.x * kLog2e, g2.y * kLog2e);   // base-2 log-decay
+            x[t] = fmul2(g2, make_float2(kLog2e, kLog2e));   // base-2 log-decay
         }
     }
 #pragma unroll
-    for (int t = 1; t < 16; t++) {
-        x[t].x += x[t - 1].x; x[t].y += x[t - 1].y;
-    }
+    for (int t = 1; t < 16; t++) x[t] = fadd2(x[t], x[t - 1]);
     *reinterpret_cast<float2 *>(xchg + ew * 128 + c0) = x[15];
     fence_proxy_async_smem();   // the reads of the g slot come before a load that overwrites it
     named_bar(kBarE, kEThreads);
@@ -742,7 +766,7 @@ __device__ bool e_pass(const Smem &sm, int s, int lb, int item, int L, int et, f
     }
 #pragma unroll
     for (int t = 0; t < 16; t++) {
-        x[t].x += pre.x; x[t].y += pre.y;
+        x[t] = fadd2(x[t], pre);
         const int r = 16 * ew + t;
         if (r == m) *reinterpret_cast<float2 *>(gmx + c0) = x[t];
         if (r == L - 1) *reinterpret_cast<float2 *>(glx + c0) = x[t];
@@ -781,20 +805,22 @@ __device__ bool e_pass(const Smem &sm, int s, int lb, int item, int L, int et, f
             const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
             const uint32_t qw = *reinterpret_cast<const uint32_t *>(qt + off);
             const float br = cst[256 + r];               // zero past the chunk
-            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+            float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
             if (r < L) {
-                const float d0 = x[t].x - gm.x, d1 = x[t].y - gm.y;
-                a0 = ex2(d0);
-                a1 = ex2(d1);
-                b0 = ex2(-d0);
-                b1 = ex2(-d1);
-                worst = fmaxf(worst, fmaxf(fabsf(d0), fabsf(d1)));
+                const float2 d = fsub2(x[t], gm);
+                a.x = ex2(d.x);
+                a.y = ex2(d.y);
+                b.x = ex2(-d.x);
+                b.y = ex2(-d.y);
+                worst = fmaxf(worst, fmaxf(fabsf(d.x), fabsf(d.y)));
             }
-            const float k0 = bf16lo(kw), k1 = bf16hi(kw);
-            const float q0 = bf16lo(qw), q1 = bf16hi(qw);
-            *reinterpret_cast<uint32_t *>(kt + off) = pack_f16x2(k0 * (a0 * br), k1 * (a1 * br));
-            *reinterpret_cast<uint32_t *>(qt + off) = pack_f16x2(q0 * a0, q1 * a1);
-            *reinterpret_cast<uint32_t *>(kmt + off) = pack_f16x2(k0 * b0, k1 * b1);
+            const float2 kk = make_float2(bf16lo(kw), bf16hi(kw));
+            const float2 qq = make_float2(bf16lo(qw), bf16hi(qw));
+            const float2 kp = fmul2(kk, fmul2(a, make_float2(br, br)));
+            const float2 qp = fmul2(qq, a), km = fmul2(kk, b);
+            *reinterpret_cast<uint32_t *>(kt + off) = pack_f16x2(kp.x, kp.y);
+            *reinterpret_cast<uint32_t *>(qt + off) = pack_f16x2(qp.x, qp.y);
+            *reinterpret_cast<uint32_t *>(kmt + off) = pack_f16x2(km.x, km.y);
         }
 #pragma unroll
         for (int t = 0; t < 8; t++) x[t] = x[t + 8];
@@ -822,7 +848,10 @@ __device__ void e_convert_v(const Smem &sm, int s, int L, int et)
         uint32_t o[4];
         const float br = bt[r];
 #pragma unroll
-        for (int e = 0; e < 4; e++) o[e] = r < L ? pack_f16x2(bf16lo(in[e]) * br, bf16hi(in[e]) * br) : 0u;
+        for (int e = 0; e < 4; e++) {
+            const float2 y = fmul2(make_float2(bf16lo(in[e]), bf16hi(in[e])), make_float2(br, br));
+            o[e] = r < L ? pack_f16x2(y.x, y.y) : 0u;
+        }
         *ptr = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
@@ -1509,13 +1538,16 @@ __device__ void chain_scale_state(uint32_t tmem, uint32_t lane_off, const float 
             const float4 f4 = *reinterpret_cast<const float4 *>(fm + 32 * q + j);
             const float4 p4 = pend ? *reinterpret_cast<const float4 *>(pend + 32 * q + j)
                                    : make_float4(1.f, 1.f, 1.f, 1.f);
-            const float fv[4] = {f4.x, f4.y, f4.z, f4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                float f = __uint_as_float(x[j + e]);
-                if (pend) f = __fmul_rn(f, pv[e]);
-                x[j + e] = __float_as_uint(__fmul_rn(f, fv[e]));
+            float2 lo = make_float2(__uint_as_float(x[j]), __uint_as_float(x[j + 1]));
+            float2 hi = make_float2(__uint_as_float(x[j + 2]), __uint_as_float(x[j + 3]));
+            if (pend) {
+                lo = fmul2(lo, make_float2(p4.x, p4.y));
+                hi = fmul2(hi, make_float2(p4.z, p4.w));
             }
+            lo = fmul2(lo, make_float2(f4.x, f4.y));
+            hi = fmul2(hi, make_float2(f4.z, f4.w));
+            x[j] = __float_as_uint(lo.x); x[j + 1] = __float_as_uint(lo.y);
+            x[j + 2] = __float_as_uint(hi.x); x[j + 3] = __float_as_uint(hi.y);
         }
         uint32_t h[16];
 #pragma unroll
@@ -1910,13 +1942,16 @@ __device__ __forceinline__ void split_scale_state(uint32_t tmem, uint32_t lane_o
     for (int j = 0; j < 32; j += 4) {
         const float4 f4 = *reinterpret_cast<const float4 *>(fm + 32 * cg + j);
         const float4 p4 = pend ? *reinterpret_cast<const float4 *>(pend + 32 * cg + j) : make_float4(1.f, 1.f, 1.f, 1.f);
-        const float fv[4] = {f4.x, f4.y, f4.z, f4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            float f = __uint_as_float(x[j + e]);
-            if (pend) f = __fmul_rn(f, pv[e]);
-            x[j + e] = __float_as_uint(__fmul_rn(f, fv[e]));
+        float2 lo = make_float2(__uint_as_float(x[j]), __uint_as_float(x[j + 1]));
+        float2 hi = make_float2(__uint_as_float(x[j + 2]), __uint_as_float(x[j + 3]));
+        if (pend) {
+            lo = fmul2(lo, make_float2(p4.x, p4.y));
+            hi = fmul2(hi, make_float2(p4.z, p4.w));
         }
+        lo = fmul2(lo, make_float2(f4.x, f4.y));
+        hi = fmul2(hi, make_float2(f4.z, f4.w));
+        x[j] = __float_as_uint(lo.x); x[j + 1] = __float_as_uint(lo.y);
+        x[j + 2] = __float_as_uint(hi.x); x[j + 3] = __float_as_uint(hi.y);
     }
     uint32_t h[16];
 #pragma unroll
