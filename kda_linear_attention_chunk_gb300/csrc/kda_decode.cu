@@ -46,43 +46,74 @@ struct DecodeParams {
     int *err;
 };
 
+// Two fp32 operations in one instruction on a register pair (mul / fma
+// .rn.f32x2, sm_100 and later): each half is the IEEE single-precision
+// operation rounded to nearest even.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n .reg .b64 x, y;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n mul.rn.f32x2 x, x, y;\n mov.b64 {%0, %1}, x;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n mov.b64 z, {%6, %7};\n"
+        " fma.rn.f32x2 x, x, y, z;\n mov.b64 {%0, %1}, x;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 lo2(const float4 &v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(const float4 &v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float4 cat2(float2 lo, float2 hi) { return make_float4(lo.x, lo.y, hi.x, hi.y); }
+
+// dot of this thread's 16 entries with the staged vector x: two pair
+// accumulators (pieces j = 0, 1 and j = 2, 3), each a chain of four fused
+// pair operations, then their four lanes summed
+__device__ __forceinline__ float dot16(const float4 (&s)[4], const float4 *x, int qe)
+{
+    float2 acc[2];
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        const float4 x0 = x[8 * (2 * h) + qe], x1 = x[8 * (2 * h + 1) + qe];
+        acc[h] = fmul2(lo2(s[2 * h]), lo2(x0));
+        acc[h] = ffma2(hi2(s[2 * h]), hi2(x0), acc[h]);
+        acc[h] = ffma2(lo2(s[2 * h + 1]), lo2(x1), acc[h]);
+        acc[h] = ffma2(hi2(s[2 * h + 1]), hi2(x1), acc[h]);
+    }
+    return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+}
+
 // One token's update of this thread's 16 state entries (row vr, pieces 8j + e),
 // with exp(g), k and q of the token staged in shared memory:
 //   S' = S exp(g),  e = S' . k (over the row's eight threads),
 //   S = S' + k beta (v - e),  returns S . q (over the row's eight threads).
 // The decode step and the fold both run exactly this sequence of operations,
-// so folding a tokens equals a decode steps bit for bit.
+// so folding a tokens equals a decode steps bit for bit.  The entries go
+// through the fp32 pipes two at a time (pairs of a float4).
 __device__ __forceinline__ float token_step(float4 (&s)[4], const float4 *sa, const float4 *sk, const float4 *sq,
                                             int qe, float vv, float beta)
 {
-    float ep[4];                      // four partial sums: short dependent chains
 #pragma unroll
     for (int j = 0; j < 4; j++) {
-        const float4 a = sa[8 * j + qe], kk = sk[8 * j + qe];
-        s[j].x *= a.x; s[j].y *= a.y; s[j].z *= a.z; s[j].w *= a.w;
-        ep[j] = s[j].x * kk.x; ep[j] = fmaf(s[j].y, kk.y, ep[j]);
-        ep[j] = fmaf(s[j].z, kk.z, ep[j]); ep[j] = fmaf(s[j].w, kk.w, ep[j]);
+        const float4 a = sa[8 * j + qe];
+        s[j] = cat2(fmul2(lo2(s[j]), lo2(a)), fmul2(hi2(s[j]), hi2(a)));
     }
-    float e = (ep[0] + ep[1]) + (ep[2] + ep[3]);
+    float e = dot16(s, sk, qe);
     e += __shfl_xor_sync(0xffffffffu, e, 1);
     e += __shfl_xor_sync(0xffffffffu, e, 2);
     e += __shfl_xor_sync(0xffffffffu, e, 4);
     const float u = beta * (vv - e);
-    float op[4];
+    const float2 u2 = make_float2(u, u);
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         const float4 kk = sk[8 * j + qe];
-        s[j].x = fmaf(kk.x, u, s[j].x); s[j].y = fmaf(kk.y, u, s[j].y);
-        s[j].z = fmaf(kk.z, u, s[j].z); s[j].w = fmaf(kk.w, u, s[j].w);
-        if (sq) {
-            const float4 qq = sq[8 * j + qe];
-            op[j] = s[j].x * qq.x; op[j] = fmaf(s[j].y, qq.y, op[j]);
-            op[j] = fmaf(s[j].z, qq.z, op[j]); op[j] = fmaf(s[j].w, qq.w, op[j]);
-        }
+        s[j] = cat2(ffma2(lo2(kk), u2, lo2(s[j])), ffma2(hi2(kk), u2, hi2(s[j])));
     }
     float o = 0.f;
     if (sq) {
-        o = (op[0] + op[1]) + (op[2] + op[3]);
+        o = dot16(s, sq, qe);
         o += __shfl_xor_sync(0xffffffffu, o, 1);
         o += __shfl_xor_sync(0xffffffffu, o, 2);
         o += __shfl_xor_sync(0xffffffffu, o, 4);
