@@ -1452,71 +1452,74 @@ __device__ void chain_store_out(const TcParams &p, const Smem &sm, const Maps &m
 
 // ---- states between global memory and TMEM -------------------------------------
 // A state row (value channel v: 128 key channels, 512 contiguous bytes) lives
-// in TMEM lane v, so a thread that moved its own row would make every warp
-// instruction touch 32 rows.  Instead each warp moves 16 key channels of its
-// 32 rows at a time through its 2 KB slice of the output tile buffer: global
-// memory is read and written 8 rows x 64 bytes per instruction, shared memory
-// row by row.  Piece p (16 bytes) of staged row r sits in slot p ^ ((r/2) & 3),
-// which keeps both access patterns at the minimum of four shared-memory
-// wavefronts per warp instruction.
-__device__ __forceinline__ uint32_t stg_off(int r, int piece) { return r * 64 + ((piece ^ ((r >> 1) & 3)) << 4); }
-
-// this warp's 32 state rows (src: row 0 of them, or null for zeros) -> TMEM
-// columns tm .. tm+127 of its lanes; the global loads of the next round are
-// in flight while a round goes from the slice to TMEM
-__device__ void chain_load_state(const float *src, uint8_t *stg, uint32_t tm, int lane)
+// in TMEM lane v.  This warp's 32 state rows <-> TMEM columns tm .. tm+127 of its lanes, in the
+// 16x256b fragment layout: thread t holds rows t/4 and 8 + t/4 of each 16-lane
+// half and, in each group of 32 columns, columns 8b + 2 (t%4), +1 -- so the
+// four threads of a row move 32 contiguous bytes, a whole sector, and no
+// staging is needed.  Groups go two at a time (one in flight while the other
+// is written).
+__device__ void chain_load_state(const float *src, uint32_t tm, int lane)
 {
-    const int rq = lane >> 2, pq = lane & 3;       // coalesced pattern: row 8i + rq, piece pq
-    float4 b[4];
-    auto fetch = [&](int r) {
+    if (!src) {   // zeros: straight into TMEM
+        uint32_t z[16];
 #pragma unroll
-        for (int i = 0; i < 4; i++)
-            b[i] = src ? *reinterpret_cast<const float4 *>(src + (8 * i + rq) * kD + 16 * r + 4 * pq)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 16; j++) z[j] = 0u;
+#pragma unroll
+        for (int r = 0; r < 8; r++) tmem_st16(tm + 16 * r, z);
+        tmem_wait_st();
+        return;
+    }
+    const int rr = lane >> 2, cc = 2 * (lane & 3);
+    float2 v[2][8];
+    auto fetch = [&](int gi, float2 (&d)[8]) {   // group gi: half gi >> 2, columns 32 (gi & 3) ..
+        const float *base = src + (16 * (gi >> 2) + rr) * kD + 32 * (gi & 3) + cc;
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            d[2 * b] = *reinterpret_cast<const float2 *>(base + 8 * b);
+            d[2 * b + 1] = *reinterpret_cast<const float2 *>(base + 8 * kD + 8 * b);
+        }
     };
-    fetch(0);
-#pragma unroll 1
-    for (int r = 0; r < 8; r++) {
+    fetch(0, v[0]);
 #pragma unroll
-        for (int i = 0; i < 4; i++) *reinterpret_cast<float4 *>(stg + stg_off(8 * i + rq, pq)) = b[i];
-        if (r < 7) fetch(r + 1);
-        __syncwarp();
+    for (int gi = 0; gi < 8; gi++) {
+        if (gi + 1 < 8) fetch(gi + 1, v[(gi + 1) & 1]);
+        const float2 *d = v[gi & 1];
         uint32_t x[16];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const float4 f = *reinterpret_cast<const float4 *>(stg + stg_off(lane, q));
-            x[4 * q] = __float_as_uint(f.x); x[4 * q + 1] = __float_as_uint(f.y);
-            x[4 * q + 2] = __float_as_uint(f.z); x[4 * q + 3] = __float_as_uint(f.w);
+        for (int b = 0; b < 4; b++) {
+            x[4 * b] = __float_as_uint(d[2 * b].x); x[4 * b + 1] = __float_as_uint(d[2 * b].y);
+            x[4 * b + 2] = __float_as_uint(d[2 * b + 1].x); x[4 * b + 3] = __float_as_uint(d[2 * b + 1].y);
         }
-        tmem_st16(tm + 16 * r, x);
-        __syncwarp();   // the slice is read before the next round overwrites it
+        tmem_st16x256_x4(tm + ((uint32_t)(16 * (gi >> 2)) << 16) + 32 * (gi & 3), x);
     }
     tmem_wait_st();
 }
 
 // TMEM columns tm .. tm+127 of this warp's lanes, times pend per key channel ->
-// its 32 state rows at dst
-__device__ void chain_store_state(float *dst, const float *pend, uint8_t *stg, uint32_t tm, int lane)
+// its 32 state rows at dst (the same fragment layout)
+__device__ void chain_store_state(float *dst, const float *pend, uint32_t tm, int lane)
 {
-    const int rq = lane >> 2, pq = lane & 3;
-#pragma unroll 1
-    for (int r = 0; r < 8; r++) {
-        uint32_t x[16];
-        tmem_ld16(tm + 16 * r, x);
-        tmem_wait_ld();
+    const int rr = lane >> 2, cc = 2 * (lane & 3);
+    uint32_t x[2][16];
+    auto ld = [&](int gi, uint32_t (&d)[16]) {
+        tmem_ld16x256_x4(tm + ((uint32_t)(16 * (gi >> 2)) << 16) + 32 * (gi & 3), d);
+    };
+    ld(0, x[0]);
+    tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const float4 pe = *reinterpret_cast<const float4 *>(pend + 16 * r + 4 * q);
-            *reinterpret_cast<float4 *>(stg + stg_off(lane, q)) =
-                make_float4(__fmul_rn(__uint_as_float(x[4 * q]), pe.x), __fmul_rn(__uint_as_float(x[4 * q + 1]), pe.y),
-                            __fmul_rn(__uint_as_float(x[4 * q + 2]), pe.z), __fmul_rn(__uint_as_float(x[4 * q + 3]), pe.w));
+    for (int gi = 0; gi < 8; gi++) {
+        if (gi + 1 < 8) ld(gi + 1, x[(gi + 1) & 1]);
+        const uint32_t *y = x[gi & 1];
+        float *base = dst + (16 * (gi >> 2) + rr) * kD + 32 * (gi & 3) + cc;
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            const float2 pe = *reinterpret_cast<const float2 *>(pend + 32 * (gi & 3) + 8 * b + cc);
+            *reinterpret_cast<float2 *>(base + 8 * b) =
+                make_float2(__fmul_rn(__uint_as_float(y[4 * b]), pe.x), __fmul_rn(__uint_as_float(y[4 * b + 1]), pe.y));
+            *reinterpret_cast<float2 *>(base + 8 * kD + 8 * b) =
+                make_float2(__fmul_rn(__uint_as_float(y[4 * b + 2]), pe.x), __fmul_rn(__uint_as_float(y[4 * b + 3]), pe.y));
         }
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; i++)
-            *reinterpret_cast<float4 *>(dst + (8 * i + rq) * kD + 16 * r + 4 * pq) =
-                *reinterpret_cast<const float4 *>(stg + stg_off(8 * i + rq, pq));
-        __syncwarp();
+        if (gi + 1 < 8) tmem_wait_ld();
     }
 }
 
@@ -1566,8 +1569,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
 {
     int item = 0;
     int o_pending = -1;       // thread 0: stage whose output copies may still read their tiles
-    // this warp's 2 KB staging slice for states, and its first state row of a unit
-    auto stg = [&]() { return sm.base + kOffOT + 2048 * (v >> 5); };
+    // this warp's first state row of a unit
     auto warp_rows = [&](const Unit &x) { return (((size_t)x.st * p.H + x.h) * kD + (v & ~31)) * kD; };
     for (int k = 0;; k++) {
         const int u = cta_unit<kSort>(sm, k, U);
@@ -1583,9 +1585,8 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
             }
             continue;
         }
-        // initial state -> S (TMEM, lane v, columns = key channels), staged through
-        // the output tile buffer (free: no output copy is in flight here)
-        chain_load_state(p.s0 ? p.s0 + warp_rows(un) : nullptr, stg(), tmem + kTmS + lane_off, v & 31);
+        // initial state -> S (TMEM, lane v, columns = key channels)
+        chain_load_state(p.s0 ? p.s0 + warp_rows(un) : nullptr, tmem + kTmS + lane_off, v & 31);
         for (int c = 0; c < un.nchunks; c++, item++) {
             const int s = item & 1;
             const uint32_t ph = (item >> 1) & 1;
@@ -1707,7 +1708,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
 #endif
         // unit end: the last chunk's output copies have read the tile buffers
         // (then TMEM P_s and the buffers go back to the prep at once), and the
-        // final state = S * pend of the unit's last chunk leaves through them
+        // final state = S * pend of the unit's last chunk leaves from TMEM
         if (v == 0 && o_pending >= 0) {
             bulk_wait_read0();
             mbar_arrive(sm.bar(kBarODone + o_pending));
@@ -1715,7 +1716,7 @@ __device__ void chain_units(const TcParams &p, const Smem &sm, const int *order,
         }
         named_bar(kBarChain, kChainThreads);
         if (p.s1)
-            chain_store_state(p.s1 + warp_rows(un), sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128, stg(),
+            chain_store_state(p.s1 + warp_rows(un), sm.ptr<float>(kOffPend) + ((item - 1) % 3) * 128,
                               tmem + kTmS + lane_off, v & 31);
     }
 }
@@ -1875,58 +1876,48 @@ __device__ void ship_role(const TcParams &p, const SplitParams &sp, const Smem &
 
 // ---- the split chain: one unit, 16 compute warps -------------------------------
 // Warp w owns TMEM lanes 32 (w % 4) .. +31 (value channels) and the quarter
-// w / 4 of each lane's columns.  States move through the warp's 2 KB slice of
-// the output staging buffers, as in chain_load_state / chain_store_state.
-// kRows: the warp's state rows, 32, or 16 in a half chain (its rows sit in
-// lanes 0-15 of the warp's 32; lanes 16-31 take whatever the staging slice
-// holds there, and nothing reads them).
+// cg = w / 4 of each lane's columns.  States move as in chain_load_state /
+// chain_store_state, in the 16x256b fragment layout, here over the warp's 32
+// columns and its kRows rows: 32, or 16 in a half chain (its rows sit in lanes
+// 0-15 of the warp's 32).
 template <int kRows>
-__device__ void split_load_state(const float *src, uint8_t *stg, uint32_t tm, int lane, int cg)
+__device__ void split_load_state(const float *src, uint32_t tm, int lane, int cg)
 {
-    const int rq = lane >> 2, pq = lane & 3;
-#pragma unroll 1
-    for (int r = 2 * cg; r < 2 * cg + 2; r++) {
+    const int rr = lane >> 2, cc = 2 * (lane & 3);
 #pragma unroll
-        for (int i = 0; i < kRows / 8; i++)
-            *reinterpret_cast<float4 *>(stg + stg_off(8 * i + rq, pq)) =
-                src ? *reinterpret_cast<const float4 *>(src + (8 * i + rq) * kD + 16 * r + 4 * pq)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-        __syncwarp();
+    for (int gi = 0; gi < kRows / 16; gi++) {
         uint32_t x[16];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const float4 f = *reinterpret_cast<const float4 *>(stg + stg_off(lane, q));
-            x[4 * q] = __float_as_uint(f.x); x[4 * q + 1] = __float_as_uint(f.y);
-            x[4 * q + 2] = __float_as_uint(f.z); x[4 * q + 3] = __float_as_uint(f.w);
+        for (int b = 0; b < 4; b++) {
+            const float *r0 = src ? src + (16 * gi + rr) * kD + 32 * cg + 8 * b + cc : nullptr;
+            const float2 lo = r0 ? *reinterpret_cast<const float2 *>(r0) : make_float2(0.f, 0.f);
+            const float2 hi = r0 ? *reinterpret_cast<const float2 *>(r0 + 8 * kD) : make_float2(0.f, 0.f);
+            x[4 * b] = __float_as_uint(lo.x); x[4 * b + 1] = __float_as_uint(lo.y);
+            x[4 * b + 2] = __float_as_uint(hi.x); x[4 * b + 3] = __float_as_uint(hi.y);
         }
-        tmem_st16(tm + 16 * r, x);
-        __syncwarp();
+        tmem_st16x256_x4(tm + ((uint32_t)(16 * gi) << 16) + 32 * cg, x);
     }
     tmem_wait_st();
 }
 
 template <int kRows>
-__device__ void split_store_state(float *dst, const float *pend, uint8_t *stg, uint32_t tm, int lane, int cg)
+__device__ void split_store_state(float *dst, const float *pend, uint32_t tm, int lane, int cg)
 {
-    const int rq = lane >> 2, pq = lane & 3;
-#pragma unroll 1
-    for (int r = 2 * cg; r < 2 * cg + 2; r++) {
+    const int rr = lane >> 2, cc = 2 * (lane & 3);
+#pragma unroll
+    for (int gi = 0; gi < kRows / 16; gi++) {
         uint32_t x[16];
-        tmem_ld16(tm + 16 * r, x);
+        tmem_ld16x256_x4(tm + ((uint32_t)(16 * gi) << 16) + 32 * cg, x);
         tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const float4 pe = *reinterpret_cast<const float4 *>(pend + 16 * r + 4 * q);
-            *reinterpret_cast<float4 *>(stg + stg_off(lane, q)) =
-                make_float4(__fmul_rn(__uint_as_float(x[4 * q]), pe.x), __fmul_rn(__uint_as_float(x[4 * q + 1]), pe.y),
-                            __fmul_rn(__uint_as_float(x[4 * q + 2]), pe.z), __fmul_rn(__uint_as_float(x[4 * q + 3]), pe.w));
+        for (int b = 0; b < 4; b++) {
+            const float2 pe = *reinterpret_cast<const float2 *>(pend + 32 * cg + 8 * b + cc);
+            float *r0 = dst + (16 * gi + rr) * kD + 32 * cg + 8 * b + cc;
+            *reinterpret_cast<float2 *>(r0) =
+                make_float2(__fmul_rn(__uint_as_float(x[4 * b]), pe.x), __fmul_rn(__uint_as_float(x[4 * b + 1]), pe.y));
+            *reinterpret_cast<float2 *>(r0 + 8 * kD) =
+                make_float2(__fmul_rn(__uint_as_float(x[4 * b + 2]), pe.x), __fmul_rn(__uint_as_float(x[4 * b + 3]), pe.y));
         }
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < kRows / 8; i++)
-            *reinterpret_cast<float4 *>(dst + (8 * i + rq) * kD + 16 * r + 4 * pq) =
-                *reinterpret_cast<const float4 *>(stg + stg_off(8 * i + rq, pq));
-        __syncwarp();
     }
 }
 
@@ -2211,10 +2202,9 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
     }
     const int nch = un.nchunks;
     float *pendr = sm.ptr<float>(kCPend);                     // [2][128]: pend of the last two chunks
-    uint8_t *stg = sm.base + kCOut + 2048 * w;                // this warp's state staging slice
     const size_t wrows = hbase + (size_t)(kRows * q) * kD;   // this warp's first state row
     bool ok = true;
-    split_load_state<kRows>(p.s0 ? p.s0 + wrows : nullptr, stg, tmem + kTmS + lane_off, lane, cg);
+    split_load_state<kRows>(p.s0 ? p.s0 + wrows : nullptr, tmem + kTmS + lane_off, lane, cg);
     // O^T of chunk jo (layout paro) -> bf16 tiles of 32 rows in staging buffer
     // jo & 1 (this warp: rows 16 cg .. +15, its 32 value channels; 16 in a
     // half chain, whose tiles hold its 64 channels only), stored by bulk
@@ -2343,7 +2333,7 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
     named_bar(kBarChain, kThreads);
     // the final state = S * pend of the last chunk, through the staging slices
     if (done && p.s1)
-        split_store_state<kRows>(p.s1 + wrows, pendr + ((nch - 1) & 1) * 128, stg, tmem + kTmS + lane_off, lane, cg);
+        split_store_state<kRows>(p.s1 + wrows, pendr + ((nch - 1) & 1) * 128, tmem + kTmS + lane_off, lane, cg);
     if (tid == 0) bulk_wait0();
 }
 
