@@ -2331,7 +2331,7 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
         bulk_wait_read0();
     }
     named_bar(kBarChain, kThreads);
-    // the final state = S * pend of the last chunk, through the staging slices
+    // the final state = S * pend of the last chunk, straight from TMEM
     if (done && p.s1)
         split_store_state<kRows>(p.s1 + wrows, pendr + ((nch - 1) & 1) * 128, tmem + kTmS + lane_off, lane, cg);
     if (tid == 0) bulk_wait0();
