@@ -158,7 +158,7 @@ constexpr uint32_t kSlotT16 = kStageBytes;              // slot: the stage | T16
 constexpr uint32_t kSlotHdr = kStageBytes + 8192;
 constexpr uint32_t kSlotBytes = kSlotHdr + 1024;
 // the chain CTA's shared memory: two slot buffers, then two output staging
-// buffers (16 KB each; also the state staging at unit start and end), then the
+// buffers (16 KB each), then the
 // pend of the last two chunks; barriers and misc at the usual offsets
 constexpr uint32_t kCOut = 2 * kSlotBytes;
 constexpr uint32_t kCPend = kCOut + 2 * 16384;
