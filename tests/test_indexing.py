@@ -170,3 +170,27 @@ def test_bad_cu_seqlens_stay_in_bounds():
     t.cuda.synchronize()
     assert t.isnan(big[w.T:].float()).all()
     assert kda.device_error(reset=True) & 2
+
+
+def test_many_units_per_cta_equal_each_sequence_alone_bitwise():
+    """More (sequence, head) units than CTAs, so every CTA changes units
+    several times -- the finished unit's state leaves TMEM and the next one's
+    initial state comes in -- with initial states and ragged lengths: every
+    sampled sequence must come out exactly as in a call of its own (one unit a
+    CTA, no change)."""
+    t = torch()
+    rng = np.random.default_rng(61)
+    lens = [int(x) for x in rng.integers(1, 300, size=120)]
+    lens[7] = 0
+    lens[50] = 64
+    w, x, s0 = case(lens=lens, H=4, seed=61)   # 480 units on at most 152 CTAs
+    out, fin = packed_run(w, x, s0)
+    cu = w.cu_seqlens()
+    for n in [0, 1, 7, 13, 50, 64, 99, 119]:
+        L = w.lengths[n]
+        xn = {k: v[cu[n]:cu[n + 1]] for k, v in x.items()}
+        wn = syn.Workload("one", [L], H=w.H, dk=128, dv=128)
+        o1, f1 = packed_run(wn, xn, s0[n:n + 1])
+        if L:
+            assert t.equal(o1, out[cu[n]:cu[n + 1]]), f"sequence {n}"
+        assert t.equal(f1[0], fin[n]), f"state {n}"
