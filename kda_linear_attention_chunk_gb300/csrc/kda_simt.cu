@@ -245,26 +245,47 @@ __global__ void __launch_bounds__(kThreads, 1) kda_simt_kernel(SimtParams p)
         }
         __syncthreads();
         // ---- A (beta-scaled, strictly lower) and B (lower with diagonal) ----
-        // The 2080 pairs j <= i are dealt over all threads in order (thread tid
-        // takes pairs tid, tid + 512, ...); the channel loop is skewed by the
-        // lane, so that the lanes of a warp read 32 different banks.
-        for (int pr = tid; pr < kChunk * (kChunk + 1) / 2; pr += kThreads) {
-            int i = (int)((sqrtf(8.f * pr + 1.f) - 1.f) * 0.5f);
-            if ((i + 1) * (i + 2) / 2 <= pr) i++;          // float rounding of the root
-            if (i * (i + 1) / 2 > pr) i--;
-            const int j = pr - i * (i + 1) / 2;
-            const float *ki = Ks + i * DK, *qi = Qs + i * DK, *gi = Gs + i * DK;
-            const float *kj = Ks + j * DK, *gj = Gs + j * DK;
-            float sa = 0.f, sb = 0.f;
-#pragma unroll 4
+        // In 2 x 2 tiles of pairs: rows 2I, 2I+1 against rows 2J, 2J+1 (J <= I;
+        // 528 tiles, thread tid takes tiles tid, tid + 512), so that each channel
+        // step reads ten values for four pairs.  The channel loop is skewed by
+        // the lane, so that the lanes of a warp read 32 different banks.
+        for (int tl = tid; tl < (kChunk / 2) * (kChunk / 2 + 1) / 2; tl += kThreads) {
+            int I = (int)((sqrtf(8.f * tl + 1.f) - 1.f) * 0.5f);
+            if ((I + 1) * (I + 2) / 2 <= tl) I++;          // float rounding of the root
+            if (I * (I + 1) / 2 > tl) I--;
+            const int J = tl - I * (I + 1) / 2;
+            const int i0 = 2 * I, j0 = 2 * J;
+            float sa[2][2] = {}, sb[2][2] = {};
+#pragma unroll 2
             for (int cc = 0; cc < DK; cc++) {
                 const int c = (cc + lane) & (DK - 1);
-                const float w = exp2f(gi[c] - gj[c]) * kj[c];
-                sa = fmaf(ki[c], w, sa);
-                sb = fmaf(qi[c], w, sb);
+                float ki[2], qi[2], gi[2], kj[2], gj[2];
+#pragma unroll
+                for (int a = 0; a < 2; a++) {
+                    ki[a] = Ks[(i0 + a) * DK + c];
+                    qi[a] = Qs[(i0 + a) * DK + c];
+                    gi[a] = Gs[(i0 + a) * DK + c];
+                    kj[a] = Ks[(j0 + a) * DK + c];
+                    gj[a] = Gs[(j0 + a) * DK + c];
+                }
+#pragma unroll
+                for (int a = 0; a < 2; a++)
+#pragma unroll
+                    for (int b2 = 0; b2 < 2; b2++) {
+                        const float w = exp2f(gi[a] - gj[b2]) * kj[b2];
+                        sa[a][b2] = fmaf(ki[a], w, sa[a][b2]);
+                        sb[a][b2] = fmaf(qi[a], w, sb[a][b2]);
+                    }
             }
-            As[i * kAS + j] = j < i ? bs[i] * sa : 0.f;
-            Bs[i * kAS + j] = sb;
+#pragma unroll
+            for (int a = 0; a < 2; a++)
+#pragma unroll
+                for (int b2 = 0; b2 < 2; b2++) {
+                    const int i = i0 + a, j = j0 + b2;
+                    if (j > i) continue;                   // (the diagonal tile's upper corner)
+                    As[i * kAS + j] = j < i ? bs[i] * sa[a][b2] : 0.f;
+                    Bs[i * kAS + j] = sb[a][b2];
+                }
         }
         for (int pr = tid; pr < kChunk * (kChunk - 1) / 2; pr += kThreads) {   // the upper triangles: zero
             int j = (int)((sqrtf(8.f * pr + 1.f) - 1.f) * 0.5f);
