@@ -2193,7 +2193,7 @@ __device__ void split_chain(const TcParams &p, const SplitParams &sp, const Smem
     const Unit un = get_unit<kSlots, 1>(p, order, uu);
     const size_t ubase = ((size_t)un.st * p.H + un.h) * kD * kD;   // used only when st >= 0
     const size_t hbase = ubase + (size_t)(kHalf ? 64 * half : 0) * kD;   // this chain's first state row
-    if (un.nchunks == 0) {   // empty (or padded) sequence: its state (rows) pass through
+    if (un.nchunks == 0) {   // empty (or padded) sequence: its state rows pass through
         if (p.s1 && (!kSlots || un.st >= 0))
             for (int i = tid; i < 4 * kRows * kD / 4; i += kThreads)
                 reinterpret_cast<float4 *>(p.s1 + hbase)[i] =
