@@ -409,7 +409,8 @@ def measure_conv_prefill(torch, np, kda, stream, steps: int = 100, warmup: int =
             "tokens_per_s": t_rows / (ms / 1e3), "two_calls_us_per_step": ms2 * 1e3,
             "l2": "2 rotating input sets of 470 MB each",
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "algorithmic_bytes_per_launch": alg, "traffic": None}}
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": alg,
+                         "traffic": recorded_traffic("conv_prefill_packed16_8192_h32", KERNEL_SOURCES)}}
 
 
 FOLD_W = 8   # speculative window: 8 draft tokens a sequence

@@ -577,10 +577,10 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // =============================================================================
 
 // -----------------------------------------------------------------------------
-// The fused short-conv prologue (kConv builds).  Group E turns a stage's raw
-// projection tiles into q, k and v in place before its own passes (v before
-// the beta*V conversion, q and k before the operand pass); q, k and v never
-// reach global memory.  Per row t of a sequence and channel c, with
+// The fused short-conv prologue (kConv builds).  The stage's raw projection
+// tiles become q, k and v in place: group E converts q and k before its
+// operand pass, group I the value rows (straight to beta*V, i_conv_v) before
+// it takes the chunk; q, k and v never reach global memory.  Per row t of a sequence and channel c, with
 // x_{-3..-1} the window's taps: y_t = sum_j w_j x_{t-3+j}, SiLU if asked, and
 // q, k scaled to unit L2 norm over the head's 128 channels, y / sqrt(|y|^2 + eps).
 // -----------------------------------------------------------------------------
@@ -593,11 +593,13 @@ __device__ __forceinline__ float conv_silu(float a) { return __fdividef(a, 1.f +
 // 64-channel blocks are `blk` apart from `tile` (bf16 in and out; rows at and
 // past L become zero); with kNorm each row is scaled to unit L2 norm over the
 // head's 128 channels -- the 32 lanes of the warp hold all of them, so the sum
-// needs no other warp.  halo[j]: row -3 + j of the chunk for warp 0 (the
-// sequence's previous rows, or its window's taps on its first chunk).  win
-// (only on a sequence's last chunk): tap 0 of the stream's window at this
-// lane's channels, taps tap_stride apart; it receives the last three raw rows
-// of [old taps ; the sequence's rows].
+// needs no other warp.  halo[j]: row 8w - 3 + j of the chunk (for warp 0 the
+// sequence's previous rows, or its window's taps on its first chunk); a warp
+// reads from the tile only the rows it rewrites, so the warps need no barrier
+// here.  win (only on a sequence's last chunk): tap 0 of the stream's window
+// at this lane's channels, taps tap_stride apart; it receives the last three
+// raw rows of [old taps ; the sequence's rows] (warp 0 read the old taps into
+// its halo before the decay pass's barriers).
 template <bool kNorm>
 __device__ void e_conv_stream(uint8_t *tile, uint32_t blk, const uint2 (&halo)[3], const float (&w)[4][4], int L,
                               int et, int act, float eps, uint16_t *win, size_t tap_stride)
@@ -607,11 +609,9 @@ __device__ void e_conv_stream(uint8_t *tile, uint32_t blk, const uint2 (&halo)[3
     const int ch = (lane & 15) >> 1;                   // 16-byte chunk of channel 4l in its block row
     uint2 raw[11];                                     // rows 8w - 3 .. 8w + 7
 #pragma unroll
-    for (int j = 0; j < 3; j++)
-        raw[j] = w8 == 0 ? halo[j] : *reinterpret_cast<const uint2 *>(base + sw128_chunk(8 * w8 - 3 + j, ch));
+    for (int j = 0; j < 3; j++) raw[j] = halo[j];
 #pragma unroll
     for (int t = 0; t < 8; t++) raw[3 + t] = *reinterpret_cast<const uint2 *>(base + sw128_chunk(8 * w8 + t, ch));
-    named_bar(kBarE, kEThreads);   // every raw row is read before any row is rewritten
     if (win) {
 #pragma unroll 1
         for (int j = 0; j < 3; j++) {
@@ -683,10 +683,10 @@ __device__ void e_conv_stream(uint8_t *tile, uint32_t blk, const uint2 (&halo)[3
     }
 }
 
-// the three rows before a chunk, per stream (q, k, v), at a lane's four
+// the three rows before a chunk, per stream (q, k), at a lane's four
 // channels, held by group E's first warp; nothing in builds without the prologue
 template <bool kConv> struct ConvHalo {
-    uint2 r[3][3] = {};
+    uint2 r[2][3] = {};
 };
 template <> struct ConvHalo<false> {};
 
@@ -945,24 +945,30 @@ __device__ void e_role(const TcParams &p, const ConvParams &cp, const Smem &sm, 
             const int L = min(kChunk, un.eos - (un.bos + c * kChunk));
             const float beta_r = beta_next;
             if (et == 0) publish();
-            // fused prologue: the three rows before the chunk (ew == 0 threads), in
-            // flight during the decay scan -- the sequence's previous rows, or its
-            // window's taps on its first chunk
+            // fused prologue: the three rows before each warp's first row, in flight
+            // during the decay scan -- for warp 0 the sequence's previous rows, or
+            // its window's taps on its first chunk; for the others rows of the chunk
+            // (zero past its end), read from global memory so that no warp reads
+            // rows another rewrites
             ConvHalo<kConv> halo;
             if constexpr (kConv) {
-                if ((et >> 5) == 0) {
-                    const size_t HC = (size_t)p.H * kD;
-                    const int cc0 = 4 * (et & 31);                    // this lane's first channel
-                    const int row0 = un.bos + c * kChunk;
+                const size_t HC = (size_t)p.H * kD;
+                const int cc0 = 4 * (et & 31);                        // this lane's first channel
+                const int row0 = un.bos + c * kChunk;
+                const int rh = 8 * (et >> 5) - 3;                     // chunk row of halo row 0
 #pragma unroll
-                    for (int sx = 0; sx < 3; sx++)
+                for (int sx = 0; sx < 2; sx++)
 #pragma unroll
-                        for (int j = 0; j < 3; j++)
+                    for (int j = 0; j < 3; j++) {
+                        const uint2 *src = reinterpret_cast<const uint2 *>(cp.x[sx] + (size_t)(row0 + rh + j) * HC + (size_t)un.h * kD + cc0);
+                        if (rh < 0)
                             halo.r[sx][j] = c == 0
                                 ? *reinterpret_cast<const uint2 *>(cp.pool + ((size_t)un.st * 9 + 3 * j + sx) * HC +
                                                                    (size_t)un.h * kD + cc0)
-                                : __ldg(reinterpret_cast<const uint2 *>(cp.x[sx] + ((size_t)(row0 - 3 + j) * p.H + un.h) * kD + cc0));
-                }
+                                : __ldg(src);
+                        else
+                            halo.r[sx][j] = rh + j < L ? __ldg(src) : make_uint2(0u, 0u);
+                    }
             }
             bool ok = mbar_wait(sm.bar(kBarGFull), item & 1, sm.abort_flag());
             if (role_any(!ok, kBarE, kEThreads)) {
@@ -985,20 +991,16 @@ __device__ void e_role(const TcParams &p, const ConvParams &cp, const Smem &sm, 
             // beta*V as soon as v has landed (the betas are in place after the scan):
             // before the wait for k and q, so that MMA-b never waits for it
             auto convert_v = [&]() -> bool {
-                const bool okv = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
-                if (role_any(!okv, kBarE, kEThreads)) return false;
                 if constexpr (kConv) {
-                    const ConvAt at = conv_at(cp, un, c, et);
-                    float w[4][4];
-                    conv_weights(cp, 2, un.h, at.c0, w);
-                    e_conv_stream<false>(sm.base + s * kStageBytes + kOffV, 8192, halo.r[2], w, L, et, cp.act, cp.eps,
-                                         at.window(2), at.tap);
-                    named_bar(kBarE, kEThreads);   // v in place before the beta*V mapping reads it
+                    return true;   // group I maps the raw value rows (i_conv_v)
+                } else {
+                    const bool okv = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
+                    if (role_any(!okv, kBarE, kEThreads)) return false;
+                    e_convert_v(sm, s, L, et);
+                    fence_proxy_async_smem();
+                    mbar_arrive(sm.bar(kBarEDone + s));
+                    return true;
                 }
-                e_convert_v(sm, s, L, et);
-                fence_proxy_async_smem();
-                mbar_arrive(sm.bar(kBarEDone + s));
-                return true;
             };
             auto conv_qk = [&]() {
                 if constexpr (kConv) {
@@ -1043,7 +1045,7 @@ __device__ void e_role(const TcParams &p, const ConvParams &cp, const Smem &sm, 
 
 // =============================================================================
 // prep, group I (warps 12-15): the A readout, the inverse T = (I + A_kk)^-1,
-// MMA-b and the -W' conversion
+// MMA-b and the -W' conversion (and, with the fused prologue, the value rows)
 // =============================================================================
 // fp32 blocks of the inverse in the shared kOffTmp region (float offsets):
 //   D0 = T[0:32, 0:32], D1 = T[32:64, 32:64]  dense [32][36] (upper-right 16x16 zero)
@@ -1316,8 +1318,95 @@ __device__ void i_read_w(const Smem &sm, int s, int lb, uint32_t tmem, int it)
     tmem_wait_st();
 }
 
-template <bool kSlots, int kSort>
-__device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int U)
+// The fused prologue's value stream (kConv builds), done by group I on the
+// chunk it is about to take, before it waits for that chunk's MMA-a (group E
+// has the q and k streams and the decay pass): the conv (and SiLU) of the raw
+// v rows, rounded to bf16 as the prologue's own outputs are, then beta_r * v
+// as fp16 in place -- the bytes of e_conv_stream followed by e_convert_v.
+// Warp w takes rows 16w .. 16w+15 in two passes of 8 rows, lane l channels
+// 4l .. 4l+3 of the head.  A warp reads from shared memory only the rows it
+// rewrites itself, and the three rows before its first row from global memory
+// (warp 0 on a sequence's first chunk: the window's taps), so the warps never
+// wait for one another; warp 0 also rewrites the window, after it has read
+// the old taps.
+__device__ void i_conv_v(const TcParams &p, const ConvParams &cp, const Smem &sm, int s, const Unit &un, int c, int L,
+                         int it)
+{
+    const int lane = it & 31, iw = it >> 5;
+    const size_t HC = (size_t)p.H * kD;
+    const int c0 = 4 * lane;
+    const int row0 = un.bos + c * kChunk;
+    uint8_t *base = sm.base + s * kStageBytes + kOffV + (lane >> 4) * 8192 + 8 * (lane & 1);
+    const int ch = (lane & 15) >> 1;                              // 16-byte chunk of channel c0 in its block row
+    const uint16_t *xv = cp.x[2] + (size_t)un.h * kD + c0;        // row r of the projection at xv + r * HC
+    uint2 raw[11];                                                // rows r0 - 3 .. r0 + 7 of a pass
+    {
+        uint16_t *win = cp.pool + ((size_t)un.st * 9 + 2) * HC + (size_t)un.h * kD + c0;   // tap j at win + 3 j HC
+#pragma unroll
+        for (int j = 0; j < 3; j++) {
+            const int r = 16 * iw - 3 + j;
+            const uint2 *src = reinterpret_cast<const uint2 *>(xv + (size_t)(row0 + r) * HC);
+            if (r < 0)
+                raw[j] = c == 0 ? *reinterpret_cast<const uint2 *>(win + 3 * j * HC) : __ldg(src);
+            else
+                raw[j] = r < L ? __ldg(src) : make_uint2(0u, 0u);
+        }
+        if (iw == 0 && c == un.nchunks - 1) {
+            // the new window: the last three raw rows of [old taps ; the sequence's
+            // rows], all read before the first is written
+            uint2 nt[3];
+#pragma unroll
+            for (int j = 0; j < 3; j++) {
+                const int r = L - 3 + j;                          // < 0 on a first chunk: old tap j + L
+                nt[j] = r >= 0 || c > 0 ? __ldg(reinterpret_cast<const uint2 *>(xv + (size_t)(row0 + r) * HC))
+                                        : *reinterpret_cast<const uint2 *>(win + 3 * (j + L) * HC);
+            }
+#pragma unroll
+            for (int j = 0; j < 3; j++) *reinterpret_cast<uint2 *>(win + 3 * j * HC) = nt[j];
+        }
+    }
+    // beta of row 16w + l at lane l < 16 (zero past the chunk), shuffled out per row
+    const int rb = 16 * iw + (lane & 15);
+    const float bl = rb < L ? __ldg(p.beta + (size_t)(row0 + rb) * p.H + un.h) : 0.f;
+    float w[4][4];
+    conv_weights(cp, 2, un.h, c0, w);
+#pragma unroll
+    for (int hp = 0; hp < 2; hp++) {
+        const int r0 = 16 * iw + 8 * hp;
+        if (hp) {
+#pragma unroll
+            for (int j = 0; j < 3; j++) raw[j] = raw[8 + j];
+        }
+#pragma unroll
+        for (int t = 0; t < 8; t++) raw[3 + t] = *reinterpret_cast<const uint2 *>(base + sw128_chunk(r0 + t, ch));
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            const float x[4][4] = {{bf16lo(raw[t].x), bf16hi(raw[t].x), bf16lo(raw[t].y), bf16hi(raw[t].y)},
+                                   {bf16lo(raw[t + 1].x), bf16hi(raw[t + 1].x), bf16lo(raw[t + 1].y), bf16hi(raw[t + 1].y)},
+                                   {bf16lo(raw[t + 2].x), bf16hi(raw[t + 2].x), bf16lo(raw[t + 2].y), bf16hi(raw[t + 2].y)},
+                                   {bf16lo(raw[t + 3].x), bf16hi(raw[t + 3].x), bf16lo(raw[t + 3].y), bf16hi(raw[t + 3].y)}};
+            float y[4];
+#pragma unroll
+            for (int cc = 0; cc < 4; cc++) {                      // the same order of the sum as e_conv_stream
+                float a = w[cc][0] * x[0][cc];
+                a = fmaf(w[cc][1], x[1][cc], a);
+                a = fmaf(w[cc][2], x[2][cc], a);
+                a = fmaf(w[cc][3], x[3][cc], a);
+                y[cc] = cp.act ? conv_silu(a) : a;
+            }
+            const uint32_t b0 = pack_bf16x2(y[0], y[1]), b1 = pack_bf16x2(y[2], y[3]);
+            const float b = __shfl_sync(0xffffffffu, bl, 8 * hp + t);
+            const float2 v0 = fmul2(make_float2(bf16lo(b0), bf16hi(b0)), make_float2(b, b));
+            const float2 v1 = fmul2(make_float2(bf16lo(b1), bf16hi(b1)), make_float2(b, b));
+            const uint2 out = r0 + t < L ? make_uint2(pack_f16x2(v0.x, v0.y), pack_f16x2(v1.x, v1.y))
+                                         : make_uint2(0u, 0u);
+            *reinterpret_cast<uint2 *>(base + sw128_chunk(r0 + t, ch)) = out;
+        }
+    }
+}
+
+template <bool kSlots, int kSort, bool kConv>
+__device__ void i_role(const TcParams &p, const ConvParams *cp, const Smem &sm, const int *order, int U)
 {
     const int it = threadIdx.x - kChainThreads - kEThreads;
     const uint32_t tmem = *sm.tmem_base();
@@ -1348,6 +1437,11 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
             const int s = item & 1;
             const int lb = layout_bit<kSort>(order, un, s);
             const uint32_t ph = (item >> 1) & 1;
+            if constexpr (kConv) {   // the value rows, once landed: beta*V for MMA-b
+                const bool okv = mbar_wait(sm.bar(kBarVFull + s), ph, sm.abort_flag());
+                if (role_any(!okv, kBarI, kGroupThreads)) { if (it == 0) record_error(p, sm, kErrWaitTimeout); return; }
+                i_conv_v(p, *cp, sm, s, un, c, min(kChunk, un.eos - (un.bos + c * kChunk)), it);
+            }
             // MMA-a done implies group E's operand pass is over (MMA-b of the previous
             // chunk, the last reader of T16, was waited for below)
             bool ok = mbar_wait(sm.bar(kBarAFull + s), ph, sm.abort_flag());
@@ -1364,7 +1458,7 @@ __device__ void i_role(const TcParams &p, const Smem &sm, const int *order, int 
             fence_proxy_async_smem();
             named_bar(kBarI, kGroupThreads);
             if (it == 0) {
-                if (!mbar_wait(sm.bar(kBarEDone + s), ph, sm.abort_flag())) {
+                if (!kConv && !mbar_wait(sm.bar(kBarEDone + s), ph, sm.abort_flag())) {   // group E's beta*V
                     record_error(p, sm, kErrWaitTimeout);
                 } else {
                     KDA_PHASE(0, item, 7);
@@ -2439,7 +2533,7 @@ kda_tc_split_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         const ConvParams no_conv = {};
         e_role<kSlots, kSortChunks, false>(p, no_conv, sm, order, 0, maps);
     } else {
-        i_role<kSlots, kSortChunks>(p, sm, order, 0);
+        i_role<kSlots, kSortChunks, false>(p, nullptr, sm, order, 0);
     }
     // every MMA this CTA issued has completed before TMEM is released
     if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads || tid == kThreads + 32) {
@@ -2568,7 +2662,7 @@ kda_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     } else if (warp < 12) {
         e_role<kSlots, kSort, kConv>(p, cp, sm, order, U, maps);
     } else {
-        i_role<kSlots, kSort>(p, sm, order, U);
+        i_role<kSlots, kSort, kConv>(p, &cp, sm, order, U);
     }
     // every MMA this CTA issued has completed before TMEM is released
     if (tid == 0 || tid == kChainThreads || tid == kChainThreads + kEThreads) {
