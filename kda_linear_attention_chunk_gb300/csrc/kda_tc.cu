@@ -169,7 +169,7 @@ constexpr int kBarKQFull = 0;      // [2]: k, q tiles landed
 constexpr int kBarVFull = 2;       // [2]: v tile landed
 constexpr int kBarPrepDone = 4;    // [2]: MMA-b of a chunk is done (W'^T and U^T in TMEM)
 constexpr int kBarAFull = 6;       // [2]: MMA-a done
-constexpr int kBarEDone = 8;       // [2]: group E has written a chunk's beta*V (256 arrivals)
+constexpr int kBarEDone = 8;       // [2]: group E has written a chunk's beta*V (256 arrivals; not with the fused prologue)
 constexpr int kBarODone = 10;      // [2]: the chain has read a chunk's outputs (TMEM P_s free)
 constexpr int kBarFmReady = 12;    // [2]: the chunk's decay constants are written (128 arrivals)
 constexpr int kBarKmFree = 14;     // [2]: the chain's MMAs on the stage are done (Km, B free)
@@ -580,9 +580,10 @@ __device__ void issue_g(const Smem &sm, const Maps &m, int row0, int h)
 // The fused short-conv prologue (kConv builds).  The stage's raw projection
 // tiles become q, k and v in place: group E converts q and k before its
 // operand pass, group I the value rows (straight to beta*V, i_conv_v) before
-// it takes the chunk; q, k and v never reach global memory.  Per row t of a sequence and channel c, with
-// x_{-3..-1} the window's taps: y_t = sum_j w_j x_{t-3+j}, SiLU if asked, and
-// q, k scaled to unit L2 norm over the head's 128 channels, y / sqrt(|y|^2 + eps).
+// it takes the chunk; q, k and v never reach global memory.  Per row t of a
+// sequence and channel c, with x_{-3..-1} the window's taps:
+// y_t = sum_j w_j x_{t-3+j}, SiLU if asked, and q, k scaled to unit L2 norm
+// over the head's 128 channels, y / sqrt(|y|^2 + eps).
 // -----------------------------------------------------------------------------
 // SiLU(a) = a sigmoid(a) = a / (1 + 2^(-a log2 e)); ex2.approx and the
 // approximate division keep it to a few units of fp32 rounding
@@ -683,8 +684,8 @@ __device__ void e_conv_stream(uint8_t *tile, uint32_t blk, const uint2 (&halo)[3
     }
 }
 
-// the three rows before a chunk, per stream (q, k), at a lane's four
-// channels, held by group E's first warp; nothing in builds without the prologue
+// the three rows before a group E warp's first row, per stream (q, k), at a
+// lane's four channels; nothing in builds without the prologue
 template <bool kConv> struct ConvHalo {
     uint2 r[2][3] = {};
 };
@@ -989,7 +990,8 @@ __device__ void e_role(const TcParams &p, const ConvParams &cp, const Smem &sm, 
                 }
             };
             // beta*V as soon as v has landed (the betas are in place after the scan):
-            // before the wait for k and q, so that MMA-b never waits for it
+            // before the wait for k and q, so that MMA-b never waits for it (builds
+            // with the fused prologue: group I does it, i_conv_v)
             auto convert_v = [&]() -> bool {
                 if constexpr (kConv) {
                     return true;   // group I maps the raw value rows (i_conv_v)
