@@ -240,7 +240,7 @@ int kda_chunk_prefill_slots(const uint16_t *q, const uint16_t *k, const uint16_t
  * kda_chunk_prefill_slots bit for bit.  Speed: the call saves the round trip
  * of q, k and v through global memory (402 MB for 8192 rows at H = 32), but
  * the prologue's arithmetic lengthens the prefill kernel's busiest role, and
- * on a GB300 the two calls are faster (about 239 us against 273 us at that
+ * on a GB300 the two calls are faster (about 239 us against 256 us at that
  * shape); use this call where memory traffic or capacity is the constraint.
  *
  *   xq, xk, xv   bf16 bits [T][H][128]: the layer's projections.

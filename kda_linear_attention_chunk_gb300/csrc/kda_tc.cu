@@ -1372,8 +1372,8 @@ __device__ void i_conv_v(const TcParams &p, const ConvParams &cp, const Smem &sm
     const float bl = rb < L ? __ldg(p.beta + (size_t)(row0 + rb) * p.H + un.h) : 0.f;
     float w[4][4];
     conv_weights(cp, 2, un.h, c0, w);
-#pragma unroll
-    for (int hp = 0; hp < 2; hp++) {
+#pragma unroll 1
+    for (int hp = 0; hp < 2; hp++) {   // rolled: one copy of the code (it runs once a chunk)
         const int r0 = 16 * iw + 8 * hp;
         if (hp) {
 #pragma unroll
