@@ -52,3 +52,40 @@ def test_bench_workloads(name, monkeypatch):
     expect = {"long_65536": "split", "context_262144": "split", "varlen4_4096": "split",
               "packed16_8192": "fused"}[name]
     assert bench.tc_mode(w, rows, SMS) == expect
+
+
+def test_traffic_records_follow_the_kernel_sources(tmp_path, monkeypatch):
+    """A committed ncu traffic figure is reported only while the kernel sources
+    it was captured on are the current ones (comments aside), and only for its
+    own workload; every committed record parses."""
+    for name in sorted(os.listdir(os.path.join(bench.ROOT, "profiles"))):
+        if name.startswith("traffic") and name.endswith(".txt"):
+            keys = {}
+            for line in open(os.path.join(bench.ROOT, "profiles", name)):
+                if ":" in line and not line.lstrip().startswith("#"):
+                    k, v = line.split(":", 1)
+                    keys[k.strip()] = v.strip()
+            assert {"kernel", "workload", "kernel_source_sha", "dram_bytes_per_launch"} <= set(keys), name
+            assert int(keys["dram_bytes_per_launch"]) > 0 and len(keys["kernel_source_sha"]) == 16, name
+
+    src = "int f(int x) {  // twice\n    return 2 * x;\n}\n"
+    edited = "/* doubles */\nint f(int x) {\n\n    return 2 * x;   \n}\n"
+    assert bench.code_only(src) == bench.code_only(edited)            # comments and blanks do not count
+    assert bench.code_only(src) != bench.code_only(src.replace("2 *", "3 *"))
+
+    csrc = tmp_path / "kda_linear_attention_chunk_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text(src)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.kernel_source_sha(("k.cu",))
+    record = f"# a capture\nkernel: k\nworkload: w1\nkernel_source_sha: {sha}\ndram_bytes_per_launch: 1234\n"
+    (tmp_path / "profiles" / "traffic_w1.txt").write_text(record)
+    assert bench.recorded_traffic("w1", ("k.cu",)) == 1234
+    assert bench.recorded_traffic("w2", ("k.cu",)) is None                 # no record for that workload
+    (tmp_path / "profiles" / "traffic_w2.txt").write_text(record)           # a record naming another workload
+    assert bench.recorded_traffic("w2", ("k.cu",)) is None
+    (csrc / "k.cu").write_text(edited)
+    assert bench.recorded_traffic("w1", ("k.cu",)) == 1234                  # a comment edit keeps it
+    (csrc / "k.cu").write_text(src.replace("2 *", "3 *"))
+    assert bench.recorded_traffic("w1", ("k.cu",)) is None                  # a code change drops it
